@@ -1,0 +1,234 @@
+/*
+ * Titans neural long-term memory, forward pass: the plain fp64 CPU oracle.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only tests/, __graft_entry__.smoke() and the
+ * cpu_baseline / reference legs of bench.py may load this library.  The
+ * product path (libnm.so and its Python binding) never calls it and shares no
+ * code, header, table or helper with it.
+ *
+ * Sources (page title, then section):
+ *   [IT] "Titans: Imparare a Memorizzare al Tempo di Test" (lowest.today):
+ *        "Meccanismo di Aggiornamento della Memoria"  - gradient step and the
+ *            momentum ("surprise") recursion, gradient taken at the previous
+ *            weights;
+ *        "Meccanismo di Dimenticanza"                 - the (1 - alpha_t) decay;
+ *        "Funzione Obiettivo"                         - loss ||M(k) - v||^2;
+ *        "Addestramento Parallelizzato"               - chunks of size b,
+ *            mini-batch gradient descent inside a chunk.
+ *   [JA] "論文解説: Titans — 推論時ニューラルメモリ更新による200万トークン超の長期記憶"
+ *        (0h-n0.github.io):
+ *        "メモリ読み出し"     - retrieval y_t = M_t(q_t);
+ *        "モメンタム機構"     - s_t = beta s_{t-1} + (1 - beta) grad;
+ *        "適応的重み減衰"     - theta <- (1 - alpha_t) theta - eta_t s_t;
+ *        "ニューラル長期メモリモジュール" - the memory is an MLP whose weights
+ *            are the storage.
+ *
+ * What is computed, per (batch, head), in the pages' order and notation:
+ *
+ *   for every chunk of b consecutive tokens (the grid restarts at t = 0 of
+ *   each call; the last chunk may be shorter):
+ *       W0 <- M                         (weights at chunk start; [IT] parallel
+ *                                        training: every token of a chunk takes
+ *                                        its gradient at these weights)
+ *       for every token t of the chunk, in order:
+ *           g_t = grad_W ||M_W0(k_t) - v_t||^2      (explicit forward+backward)
+ *           S   = beta_t S + c_t g_t                 (momentum over surprise)
+ *           M   = (1 - alpha_t) M - eta_t S          (forgetting + step)
+ *           y_t = M(q_t)                             (retrieval after the update)
+ *   M_T = M, S_T = S.
+ *
+ * The momentum coefficient c_t is ONE (c_t = 1), ONE_MINUS_BETA (c_t = 1 -
+ * beta_t, the form of [JA] "モメンタム機構") or PER_TOKEN (c_t read from an
+ * array; with eta = 1 and the sign of S flipped this is the form of [IT]).
+ *
+ * Memories:
+ *   LINEAR: M(x) = M x, M in R^{d x d}, row-major [out][in].
+ *   MLP2  : M(x) = W2 silu(W1 x), W1 in R^{h x d}, W2 in R^{d x h}, no bias;
+ *           parameters packed as W1 (row-major h x d) followed by W2
+ *           (row-major d x h).
+ *
+ * Readings where the pages are silent or disagree:
+ *   - the squared norm has no 1/2, so grad = 2 (M(k) - v) ... (kept);
+ *   - retrieval uses the weights after token t's update (inclusive);
+ *   - gates are one scalar per token per head, shared by every parameter.
+ *
+ * No blocking, no fusion, no reordering: a reader can check each loop against
+ * the equations above.  Everything is double precision.
+ */
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define OR_LINEAR 0
+#define OR_MLP2 1
+
+#define OR_C_ONE 0
+#define OR_C_ONE_MINUS_BETA 1
+#define OR_C_PER_TOKEN 2
+
+static double or_sigmoid(double z) { return 1.0 / (1.0 + exp(-z)); }
+static double or_silu(double z) { return z * or_sigmoid(z); }
+/* d/dz [z * sigmoid(z)] = sigmoid(z) + z sigmoid(z) (1 - sigmoid(z)) */
+static double or_dsilu(double z) {
+    double s = or_sigmoid(z);
+    return s * (1.0 + z * (1.0 - s));
+}
+
+/* Number of parameters of one memory. */
+long oracle_param_count(int kind, int d, int h) {
+    if (kind == OR_LINEAR) return (long)d * d;
+    if (kind == OR_MLP2) return 2L * h * d;
+    return -1;
+}
+
+/* y = M_W(x).  work must hold h doubles for MLP2. */
+void oracle_memory_apply(int kind, int d, int h, const double* W,
+                         const double* x, double* y, double* work) {
+    if (kind == OR_LINEAR) {
+        for (int o = 0; o < d; ++o) {
+            double acc = 0.0;
+            for (int i = 0; i < d; ++i) acc += W[(long)o * d + i] * x[i];
+            y[o] = acc;
+        }
+        return;
+    }
+    const double* W1 = W;                 /* h x d */
+    const double* W2 = W + (long)h * d;   /* d x h */
+    for (int j = 0; j < h; ++j) {
+        double z = 0.0;
+        for (int i = 0; i < d; ++i) z += W1[(long)j * d + i] * x[i];
+        work[j] = or_silu(z);
+    }
+    for (int o = 0; o < d; ++o) {
+        double acc = 0.0;
+        for (int j = 0; j < h; ++j) acc += W2[(long)o * h + j] * work[j];
+        y[o] = acc;
+    }
+}
+
+/* The associative loss l(W; k, v) = ||M_W(k) - v||_2^2 ([IT] "Funzione
+ * Obiettivo").  work: d + h doubles. */
+double oracle_loss(int kind, int d, int h, const double* W, const double* k,
+                   const double* v, double* work) {
+    double* yhat = work;
+    oracle_memory_apply(kind, d, h, W, k, yhat, work + d);
+    double acc = 0.0;
+    for (int o = 0; o < d; ++o) {
+        double r = yhat[o] - v[o];
+        acc += r * r;
+    }
+    return acc;
+}
+
+/* g = grad_W l(W; k, v), by an explicit forward and backward pass.
+ * work: 3h + 2d doubles. */
+void oracle_grad(int kind, int d, int h, const double* W, const double* k,
+                 const double* v, double* g, double* work) {
+    if (kind == OR_LINEAR) {
+        /* l = sum_o (sum_i M[o][i] k[i] - v[o])^2
+         * dl/dM[o][i] = 2 (M k - v)[o] k[i]                                  */
+        double* e = work;
+        for (int o = 0; o < d; ++o) {
+            double acc = 0.0;
+            for (int i = 0; i < d; ++i) acc += W[(long)o * d + i] * k[i];
+            e[o] = 2.0 * (acc - v[o]);
+        }
+        for (int o = 0; o < d; ++o)
+            for (int i = 0; i < d; ++i) g[(long)o * d + i] = e[o] * k[i];
+        return;
+    }
+    const double* W1 = W;
+    const double* W2 = W + (long)h * d;
+    double* gW1 = g;
+    double* gW2 = g + (long)h * d;
+    double* z = work;          /* h */
+    double* a = work + h;      /* h */
+    double* da = work + 2 * h; /* h */
+    double* e = work + 3 * h;  /* d */
+    /* forward: z = W1 k, a = silu(z), yhat = W2 a */
+    for (int j = 0; j < h; ++j) {
+        double acc = 0.0;
+        for (int i = 0; i < d; ++i) acc += W1[(long)j * d + i] * k[i];
+        z[j] = acc;
+        a[j] = or_silu(acc);
+    }
+    /* dl/dyhat = 2 (yhat - v) */
+    for (int o = 0; o < d; ++o) {
+        double acc = 0.0;
+        for (int j = 0; j < h; ++j) acc += W2[(long)o * h + j] * a[j];
+        e[o] = 2.0 * (acc - v[o]);
+    }
+    /* dl/dW2[o][j] = e[o] a[j] */
+    for (int o = 0; o < d; ++o)
+        for (int j = 0; j < h; ++j) gW2[(long)o * h + j] = e[o] * a[j];
+    /* dl/da[j] = sum_o W2[o][j] e[o];  dl/dz[j] = dl/da[j] silu'(z[j]) */
+    for (int j = 0; j < h; ++j) {
+        double acc = 0.0;
+        for (int o = 0; o < d; ++o) acc += W2[(long)o * h + j] * e[o];
+        da[j] = acc * or_dsilu(z[j]);
+    }
+    /* dl/dW1[j][i] = dl/dz[j] k[i] */
+    for (int j = 0; j < h; ++j)
+        for (int i = 0; i < d; ++i) gW1[(long)j * d + i] = da[j] * k[i];
+}
+
+/* One (batch, head) unit.  Pointers are already offset to the unit. */
+static void oracle_unit(int kind, int d, int h, int chunk, int c_mode, int T,
+                        const double* q, const double* k, const double* v,
+                        const double* alpha, const double* eta,
+                        const double* beta, const double* c, const double* M0,
+                        const double* S0, double* y, double* MT, double* ST) {
+    long P = oracle_param_count(kind, d, h);
+    double* M = (double*)malloc(sizeof(double) * P);
+    double* S = (double*)malloc(sizeof(double) * P);
+    double* W0 = (double*)malloc(sizeof(double) * P);
+    double* g = (double*)malloc(sizeof(double) * P);
+    double* work = (double*)malloc(sizeof(double) * (3 * (long)h + 2 * (long)d + 8));
+    memcpy(M, M0, sizeof(double) * P);
+    memcpy(S, S0, sizeof(double) * P);
+    for (int t0 = 0; t0 < T; t0 += chunk) {
+        int t1 = t0 + chunk < T ? t0 + chunk : T;
+        memcpy(W0, M, sizeof(double) * P); /* chunk-start weights */
+        for (int t = t0; t < t1; ++t) {
+            oracle_grad(kind, d, h, W0, k + (long)t * d, v + (long)t * d, g, work);
+            double ct = 1.0;
+            if (c_mode == OR_C_ONE_MINUS_BETA) ct = 1.0 - beta[t];
+            else if (c_mode == OR_C_PER_TOKEN) ct = c[t];
+            for (long p = 0; p < P; ++p) S[p] = beta[t] * S[p] + ct * g[p];
+            for (long p = 0; p < P; ++p) M[p] = (1.0 - alpha[t]) * M[p] - eta[t] * S[p];
+            oracle_memory_apply(kind, d, h, M, q + (long)t * d, y + (long)t * d, work);
+        }
+    }
+    memcpy(MT, M, sizeof(double) * P);
+    memcpy(ST, S, sizeof(double) * P);
+    free(M); free(S); free(W0); free(g); free(work);
+}
+
+/*
+ * Full forward over B x H independent (batch, head) units.
+ *   q, k, v, y : [B, H, T, d]      alpha, eta, beta, c : [B, H, T]
+ *   M0, S0, MT, ST : [B, H, P]     (c may be NULL unless c_mode == PER_TOKEN)
+ * Returns 0, or -1 on a bad argument.  Units run in parallel with OpenMP;
+ * each unit's arithmetic is sequential and identical to a one-thread run.
+ */
+int oracle_forward(int kind, int d, int h, int chunk, int c_mode, int B, int H,
+                   int T, const double* q, const double* k, const double* v,
+                   const double* alpha, const double* eta, const double* beta,
+                   const double* c, const double* M0, const double* S0,
+                   double* y, double* MT, double* ST) {
+    if ((kind != OR_LINEAR && kind != OR_MLP2) || d <= 0 || chunk <= 0 ||
+        B < 0 || H < 0 || T < 0)
+        return -1;
+    if (kind == OR_MLP2 && h <= 0) return -1;
+    if (c_mode == OR_C_PER_TOKEN && c == NULL) return -1;
+    long P = oracle_param_count(kind, d, h);
+    long units = (long)B * H;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (long u = 0; u < units; ++u) {
+        oracle_unit(kind, d, h, chunk, c_mode, T, q + u * T * d, k + u * T * d,
+                    v + u * T * d, alpha + u * T, eta + u * T, beta + u * T,
+                    c ? c + u * T : NULL, M0 + u * P, S0 + u * P, y + u * T * d,
+                    MT + u * P, ST + u * P);
+    }
+    return 0;
+}
