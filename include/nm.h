@@ -1,0 +1,167 @@
+/*
+ * nm.h - C ABI of the Titans neural long-term memory forward pass (B300, sm_103a).
+ *
+ * The operation ("Titans: Imparare a Memorizzare al Tempo di Test",
+ * lowest.today; sections "Meccanismo di Aggiornamento della Memoria",
+ * "Meccanismo di Dimenticanza", "Funzione Obiettivo", "Addestramento
+ * Parallelizzato"; and the 0h-n0.github.io Titans explainer, sections
+ * "メモリ読み出し", "モメンタム機構", "適応的重み減衰"):
+ *
+ *   per (batch b, head h), for every chunk of `chunk` consecutive tokens
+ *   (the chunk grid starts at token 0 of each call; the last chunk may be
+ *   shorter), with W0 the memory at chunk start:
+ *       g_t = grad_W || M_W0(k_t) - v_t ||^2          (no 1/2: factor 2 kept)
+ *       S   = beta_t S + c_t g_t                       (momentum over surprise)
+ *       M   = (1 - alpha_t) M - eta_t S                (forgetting + step)
+ *       y_t = M(q_t)                                   (retrieval after the update)
+ *
+ *   memory kinds:  NM_LINEAR  M(x) = M x,  M in R^{d x d}, row-major [out][in]
+ *                  NM_MLP2    M(x) = W2 silu(W1 x), W1 in R^{hidden x d},
+ *                             W2 in R^{d x hidden}, no bias; parameters packed
+ *                             as W1 (row-major) followed by W2 (row-major).
+ *   P (parameters per unit) = d*d (LINEAR) or 2*hidden*d (MLP2).
+ *
+ * The library computes this in the chunked-parallel form (matrix products
+ * plus a decay / momentum scan inside each chunk), with every unit's state
+ * kept on chip by one persistent kernel over the sequence.
+ *
+ * Threading: a handle may be used from one host thread at a time.
+ * All device entry points are asynchronous on the caller's stream.
+ */
+#ifndef NM_H
+#define NM_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes (return values of every entry point) ------------------ */
+#define NM_OK                  0
+#define NM_ERR_ARG             1  /* null pointer, bad size, bad enum          */
+#define NM_ERR_ALIGN           2  /* a pointer is not 16-byte aligned          */
+#define NM_ERR_UNSUPPORTED     3  /* (kind, d, hidden, chunk, dtype) not built */
+#define NM_ERR_ALIAS           4  /* buffers overlap other than M_T==M0, S_T==S0 */
+#define NM_ERR_CUDA            5  /* a CUDA runtime call failed                */
+#define NM_ERR_NOMEM           6  /* host or device allocation failed          */
+#define NM_ERR_DEVICE_TIMEOUT  7  /* a bounded on-device wait gave up          */
+#define NM_ERR_DEVICE_CHECK    8  /* an on-device consistency check failed     */
+
+/* ---- configuration enums ------------------------------------------------ */
+#define NM_LINEAR 0
+#define NM_MLP2   1
+
+#define NM_F32  0
+#define NM_BF16 1
+
+/* momentum coefficient c_t in S = beta_t S + c_t g_t */
+#define NM_C_ONE            0  /* c_t = 1                                   */
+#define NM_C_ONE_MINUS_BETA 1  /* c_t = 1 - beta_t (explainer, "モメンタム機構") */
+#define NM_C_PER_TOKEN      2  /* c_t read from the `c` array (with eta = 1 and
+                                  S negated this is the form of "Meccanismo di
+                                  Aggiornamento della Memoria")             */
+
+/* kernel family; AUTO picks the tensor-core path for bf16 inputs when one is
+ * built for the shape, else the fp32 FFMA path */
+#define NM_PATH_AUTO 0
+#define NM_PATH_SIMT 1  /* fp32 FFMA kernels: any supported shape, fp32 or bf16 in */
+#define NM_PATH_TC   2  /* tcgen05 tensor-core kernels: bf16 in, fp32 state      */
+
+typedef struct nm_config {
+    int kind;       /* NM_LINEAR | NM_MLP2                                    */
+    int d;          /* key / value / query width: 16, 32, 64 or 128          */
+    int hidden;     /* MLP2 hidden width (multiple of 32, <= 1024); ignored for LINEAR */
+    int chunk;      /* chunk size b, 1..256                                   */
+    int in_dtype;   /* dtype of q, k, v: NM_F32 | NM_BF16                    */
+    int out_dtype;  /* dtype of y: NM_F32 | NM_BF16                          */
+    int c_mode;     /* NM_C_ONE | NM_C_ONE_MINUS_BETA | NM_C_PER_TOKEN       */
+    int path;       /* NM_PATH_AUTO | NM_PATH_SIMT | NM_PATH_TC              */
+} nm_config;
+
+typedef struct nm_handle* nm_handle_t;
+
+/*
+ * nm_create - validate `cfg` and bind a handle to CUDA device `device`.
+ *   The handle owns: a device status word (bounded waits and on-device checks
+ *   report into it), and a device workspace that grows on demand in
+ *   nm_forward (so the first call at a larger B*H allocates).
+ *   Returns NM_ERR_ARG for null pointers or bad enums, NM_ERR_UNSUPPORTED when
+ *   no kernel is built for the shape, NM_ERR_CUDA / NM_ERR_NOMEM on failures.
+ *   *out is set only on NM_OK.
+ */
+int nm_create(const nm_config* cfg, int device, nm_handle_t* out);
+
+/*
+ * nm_forward - one forward call over B x H independent units of T tokens.
+ *   All pointers are DEVICE pointers on the handle's device, owned by the
+ *   caller, contiguous, 16-byte aligned:
+ *     q, k, v   [B, H, T, d]  in_dtype
+ *     alpha, eta, beta [B, H, T] fp32   (alpha in [0, 1] forgets, eta is the
+ *                                        step, beta the momentum decay)
+ *     c         [B, H, T] fp32, used only when c_mode == NM_C_PER_TOKEN
+ *                                       (must be NULL otherwise)
+ *     M0, S0    [B, H, P] fp32  memory and momentum at token 0
+ *     y         [B, H, T, d]  out_dtype   (written)
+ *     M_T, S_T  [B, H, P] fp32  memory and momentum after token T-1 (written)
+ *   M_T == M0 and / or S_T == S0 (exact aliasing) is allowed, for streaming
+ *   one long sequence through successive calls; any other overlap between an
+ *   output and any buffer returns NM_ERR_ALIAS.
+ *   `stream` is a cudaStream_t (NULL = the legacy default stream).
+ *   B*H == 0 is a no-op; T == 0 copies M0, S0 into M_T, S_T.
+ *   Host-side failures return an error with nothing launched.  Device-side
+ *   failures (bounded waits, on-device checks) are recorded in the handle's
+ *   status word and returned by nm_synchronize.
+ */
+int nm_forward(nm_handle_t h, int B, int H, int T,
+               const void* q, const void* k, const void* v,
+               const float* alpha, const float* eta, const float* beta,
+               const float* c, const float* M0, const float* S0,
+               void* y, float* M_T, float* S_T, void* stream);
+
+/*
+ * nm_forward_host - the same operation on HOST buffers (same layouts).
+ *   Copies the inputs to the handle's device (into handle-owned buffers that
+ *   grow on demand), runs nm_forward on `stream`, copies y, M_T, S_T back and
+ *   synchronises the stream before returning.  Pinned host memory gives
+ *   asynchronous copies; pageable memory works but is slower.
+ *   Returns the first host-side error, or the device status word as
+ *   nm_synchronize would.
+ */
+int nm_forward_host(nm_handle_t h, int B, int H, int T,
+                    const void* q, const void* k, const void* v,
+                    const float* alpha, const float* eta, const float* beta,
+                    const float* c, const float* M0, const float* S0,
+                    void* y, float* M_T, float* S_T, void* stream);
+
+/*
+ * nm_synchronize - wait for all work on the device, then return and clear
+ *   the handle's device status word (NM_OK, NM_ERR_DEVICE_TIMEOUT,
+ *   NM_ERR_DEVICE_CHECK) or NM_ERR_CUDA if the device reported an error.
+ */
+int nm_synchronize(nm_handle_t h);
+
+/*
+ * nm_destroy - free everything the handle owns (after synchronising its
+ *   device).  NULL is accepted and ignored.
+ */
+int nm_destroy(nm_handle_t h);
+
+/* nm_status_string - static, never-NULL description of a status code. */
+const char* nm_status_string(int status);
+
+/*
+ * nm_selected_path - the kernel family nm_forward will use for this handle
+ *   (NM_PATH_SIMT or NM_PATH_TC), or a negative status for a bad handle.
+ */
+int nm_selected_path(nm_handle_t h);
+
+/*
+ * nm_launch_count - number of kernels this handle has launched so far
+ *   (monotonic; used to count launches inside a timed region).
+ */
+long long nm_launch_count(nm_handle_t h);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NM_H */

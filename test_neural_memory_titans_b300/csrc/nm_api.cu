@@ -1,0 +1,319 @@
+// Host side of the C ABI declared in include/nm.h: argument validation,
+// aliasing rules, handle-owned device memory, dispatch to the kernel files.
+// No arithmetic of the method happens here.
+#include <stdlib.h>
+#include <string.h>
+
+#include "nm_internal.h"
+
+namespace {
+
+// Makes `dev` current for the scope and restores the caller's device after.
+struct DeviceGuard {
+    int prev = -1;
+    bool ok = false;
+    explicit DeviceGuard(int dev) {
+        if (cudaGetDevice(&prev) != cudaSuccess) prev = -1;
+        ok = cudaSetDevice(dev) == cudaSuccess;
+    }
+    ~DeviceGuard() {
+        if (prev >= 0) cudaSetDevice(prev);
+    }
+};
+
+bool valid_dtype(int t) { return t == NM_F32 || t == NM_BF16; }
+size_t dtype_bytes(int t) { return t == NM_BF16 ? 2 : 4; }
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+struct Range {
+    const char* p;
+    size_t n;
+};
+
+bool overlaps(Range a, Range b) {
+    if (a.n == 0 || b.n == 0 || a.p == nullptr || b.p == nullptr) return false;
+    return a.p < b.p + b.n && b.p < a.p + a.n;
+}
+
+int check_config(const nm_config* c) {
+    if (!c) return NM_ERR_ARG;
+    if (c->kind != NM_LINEAR && c->kind != NM_MLP2) return NM_ERR_ARG;
+    if (!valid_dtype(c->in_dtype) || !valid_dtype(c->out_dtype)) return NM_ERR_ARG;
+    if (c->c_mode < NM_C_ONE || c->c_mode > NM_C_PER_TOKEN) return NM_ERR_ARG;
+    if (c->path < NM_PATH_AUTO || c->path > NM_PATH_TC) return NM_ERR_ARG;
+    if (c->d <= 0 || c->chunk <= 0) return NM_ERR_ARG;
+    if (c->kind == NM_MLP2 && c->hidden <= 0) return NM_ERR_ARG;
+    return NM_OK;
+}
+
+int select_path(const nm_config& c) {
+    bool tc = nm_tc_supports(c);
+    bool simt = nm_simt_supports(c);
+    if (c.path == NM_PATH_TC) return tc ? NM_PATH_TC : -1;
+    if (c.path == NM_PATH_SIMT) return simt ? NM_PATH_SIMT : -1;
+    if (tc) return NM_PATH_TC;
+    if (simt) return NM_PATH_SIMT;
+    return -1;
+}
+
+int ensure_workspace(nm_handle* h, size_t bytes) {
+    if (bytes <= h->workspace_bytes) return NM_OK;
+    if (h->workspace) {
+        if (cudaFree(h->workspace) != cudaSuccess) return NM_ERR_CUDA;
+        h->workspace = nullptr;
+        h->workspace_bytes = 0;
+    }
+    if (cudaMalloc(&h->workspace, bytes) != cudaSuccess) {
+        cudaGetLastError();
+        h->workspace = nullptr;
+        return NM_ERR_NOMEM;
+    }
+    h->workspace_bytes = bytes;
+    return NM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* nm_status_string(int s) {
+    switch (s) {
+        case NM_OK: return "ok";
+        case NM_ERR_ARG: return "invalid argument (null pointer, bad size or bad enum)";
+        case NM_ERR_ALIGN: return "pointer not 16-byte aligned";
+        case NM_ERR_UNSUPPORTED: return "no kernel built for this (kind, d, hidden, chunk, dtype, path)";
+        case NM_ERR_ALIAS: return "output buffer overlaps another buffer (only M_T==M0 and S_T==S0 may alias)";
+        case NM_ERR_CUDA: return "CUDA runtime error";
+        case NM_ERR_NOMEM: return "allocation failed";
+        case NM_ERR_DEVICE_TIMEOUT: return "a bounded on-device wait gave up";
+        case NM_ERR_DEVICE_CHECK: return "an on-device consistency check failed";
+        default: return "unknown status";
+    }
+}
+
+int nm_create(const nm_config* cfg, int device, nm_handle_t* out) {
+    if (!out) return NM_ERR_ARG;
+    int rc = check_config(cfg);
+    if (rc != NM_OK) return rc;
+    int path = select_path(*cfg);
+    if (path < 0) return NM_ERR_UNSUPPORTED;
+    int ndev = 0;
+    if (cudaGetDeviceCount(&ndev) != cudaSuccess) {
+        cudaGetLastError();
+        return NM_ERR_CUDA;
+    }
+    if (device < 0 || device >= ndev) return NM_ERR_ARG;
+    DeviceGuard g(device);
+    if (!g.ok) return NM_ERR_CUDA;
+    nm_handle* h = (nm_handle*)calloc(1, sizeof(nm_handle));
+    if (!h) return NM_ERR_NOMEM;
+    h->cfg = *cfg;
+    h->device = device;
+    h->path = path;
+    if (cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) {
+        free(h);
+        return NM_ERR_CUDA;
+    }
+    if (cudaMalloc(&h->d_status, sizeof(int)) != cudaSuccess) {
+        cudaGetLastError();
+        free(h);
+        return NM_ERR_NOMEM;
+    }
+    if (cudaMemset(h->d_status, 0, sizeof(int)) != cudaSuccess) {
+        cudaFree(h->d_status);
+        free(h);
+        return NM_ERR_CUDA;
+    }
+    *out = h;
+    return NM_OK;
+}
+
+int nm_selected_path(nm_handle_t h) { return h ? h->path : -NM_ERR_ARG; }
+
+long long nm_launch_count(nm_handle_t h) { return h ? h->launches : -1; }
+
+int nm_forward(nm_handle_t h, int B, int H, int T, const void* q, const void* k, const void* v,
+               const float* alpha, const float* eta, const float* beta, const float* c,
+               const float* M0, const float* S0, void* y, float* M_T, float* S_T, void* stream) {
+    if (!h) return NM_ERR_ARG;
+    const nm_config& cfg = h->cfg;
+    if (B < 0 || H < 0 || T < 0) return NM_ERR_ARG;
+    const long long units = (long long)B * H;
+    if (units == 0) return NM_OK;
+    if (units > (1LL << 31) - 1 || (long long)T * cfg.d > (1LL << 40)) return NM_ERR_ARG;
+    const bool need_c = cfg.c_mode == NM_C_PER_TOKEN;
+    if (!M0 || !S0 || !M_T || !S_T) return NM_ERR_ARG;
+    if (T > 0 && (!q || !k || !v || !alpha || !eta || !beta || !y)) return NM_ERR_ARG;
+    if (T > 0 && need_c && !c) return NM_ERR_ARG;
+    if (!need_c && c) return NM_ERR_ARG;
+    const void* ptrs[] = {q, k, v, alpha, eta, beta, c, M0, S0, y, M_T, S_T};
+    for (const void* p : ptrs)
+        if (p && !aligned16(p)) return NM_ERR_ALIGN;
+
+    const size_t tok = (size_t)units * (size_t)T;
+    const size_t P = (size_t)nm_param_count(cfg);
+    const size_t in_b = tok * cfg.d * dtype_bytes(cfg.in_dtype);
+    const size_t out_b = tok * cfg.d * dtype_bytes(cfg.out_dtype);
+    const size_t gate_b = tok * sizeof(float);
+    const size_t st_b = (size_t)units * P * sizeof(float);
+    Range in_r[] = {{(const char*)q, T ? in_b : 0},       {(const char*)k, T ? in_b : 0},
+                    {(const char*)v, T ? in_b : 0},       {(const char*)alpha, gate_b},
+                    {(const char*)eta, gate_b},           {(const char*)beta, gate_b},
+                    {(const char*)c, need_c ? gate_b : 0}, {(const char*)M0, st_b},
+                    {(const char*)S0, st_b}};
+    Range out_r[] = {{(const char*)y, T ? out_b : 0}, {(const char*)M_T, st_b}, {(const char*)S_T, st_b}};
+    for (int o = 0; o < 3; ++o) {
+        for (int i = 0; i < 9; ++i) {
+            bool exact_ok = (o == 1 && i == 7) || (o == 2 && i == 8);
+            if (exact_ok && out_r[o].p == in_r[i].p) continue;
+            if (overlaps(out_r[o], in_r[i])) return NM_ERR_ALIAS;
+        }
+        for (int o2 = o + 1; o2 < 3; ++o2)
+            if (overlaps(out_r[o], out_r[o2])) return NM_ERR_ALIAS;
+    }
+
+    DeviceGuard g(h->device);
+    if (!g.ok) return NM_ERR_CUDA;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (T == 0) {
+        if (M_T != M0 && cudaMemcpyAsync(M_T, M0, st_b, cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+            return NM_ERR_CUDA;
+        if (S_T != S0 && cudaMemcpyAsync(S_T, S0, st_b, cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+            return NM_ERR_CUDA;
+        return NM_OK;
+    }
+    size_t ws = h->path == NM_PATH_TC ? nm_tc_scratch_bytes(cfg, B, H) : nm_simt_scratch_bytes(cfg, B, H);
+    int rc = ensure_workspace(h, ws);
+    if (rc != NM_OK) return rc;
+
+    nm_args a;
+    a.B = B; a.H = H; a.T = T;
+    a.q = q; a.k = k; a.v = v;
+    a.alpha = alpha; a.eta = eta; a.beta = beta; a.c = c;
+    a.M0 = M0; a.S0 = S0; a.y = y; a.M_T = M_T; a.S_T = S_T;
+    a.status = h->d_status;
+    a.scratch = h->workspace;
+    a.scratch_bytes = h->workspace_bytes;
+    cudaError_t e = h->path == NM_PATH_TC ? nm_tc_launch(cfg, a, s, h->num_sms, &h->launches)
+                                          : nm_simt_launch(cfg, a, s, &h->launches);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return NM_ERR_CUDA;
+    }
+    return NM_OK;
+}
+
+int nm_synchronize(nm_handle_t h) {
+    if (!h) return NM_ERR_ARG;
+    DeviceGuard g(h->device);
+    if (!g.ok) return NM_ERR_CUDA;
+    if (cudaDeviceSynchronize() != cudaSuccess) {
+        cudaGetLastError();
+        return NM_ERR_CUDA;
+    }
+    int st = 0;
+    if (cudaMemcpy(&st, h->d_status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return NM_ERR_CUDA;
+    if (st != 0 && cudaMemset(h->d_status, 0, sizeof(int)) != cudaSuccess) return NM_ERR_CUDA;
+    return st;
+}
+
+int nm_forward_host(nm_handle_t h, int B, int H, int T, const void* q, const void* k, const void* v,
+                    const float* alpha, const float* eta, const float* beta, const float* c,
+                    const float* M0, const float* S0, void* y, float* M_T, float* S_T, void* stream) {
+    if (!h) return NM_ERR_ARG;
+    const nm_config& cfg = h->cfg;
+    if (B < 0 || H < 0 || T < 0) return NM_ERR_ARG;
+    const size_t units = (size_t)B * H;
+    if (units == 0) return NM_OK;
+    const bool need_c = cfg.c_mode == NM_C_PER_TOKEN;
+    if (!M0 || !S0 || !M_T || !S_T) return NM_ERR_ARG;
+    if (T > 0 && (!q || !k || !v || !alpha || !eta || !beta || !y)) return NM_ERR_ARG;
+    if (T > 0 && need_c && !c) return NM_ERR_ARG;
+    if (!need_c && c) return NM_ERR_ARG;
+    const size_t tok = units * (size_t)T;
+    const size_t P = (size_t)nm_param_count(cfg);
+    auto up = [](size_t n) { return (n + 255) & ~(size_t)255; };
+    const size_t in_b = tok * cfg.d * dtype_bytes(cfg.in_dtype);
+    const size_t out_b = tok * cfg.d * dtype_bytes(cfg.out_dtype);
+    const size_t gate_b = tok * sizeof(float);
+    const size_t st_b = units * P * sizeof(float);
+    const size_t total = 3 * up(in_b) + 4 * up(gate_b) + 4 * up(st_b) + up(out_b);
+
+    DeviceGuard g(h->device);
+    if (!g.ok) return NM_ERR_CUDA;
+    if (total > h->stage_bytes) {
+        if (h->stage) cudaFree(h->stage);
+        h->stage = nullptr;
+        h->stage_bytes = 0;
+        if (cudaMalloc(&h->stage, total) != cudaSuccess) {
+            cudaGetLastError();
+            return NM_ERR_NOMEM;
+        }
+        h->stage_bytes = total;
+    }
+    char* base = (char*)h->stage;
+    size_t off = 0;
+    auto carve = [&](size_t n) {
+        char* p = base + off;
+        off += up(n);
+        return (void*)p;
+    };
+    void* dq = carve(in_b);
+    void* dk = carve(in_b);
+    void* dv = carve(in_b);
+    float* da = (float*)carve(gate_b);
+    float* de = (float*)carve(gate_b);
+    float* db = (float*)carve(gate_b);
+    float* dc = (float*)carve(gate_b);
+    float* dM0 = (float*)carve(st_b);
+    float* dS0 = (float*)carve(st_b);
+    float* dMT = (float*)carve(st_b);
+    float* dST = (float*)carve(st_b);
+    void* dy = carve(out_b);
+    cudaStream_t s = (cudaStream_t)stream;
+    struct Cp { void* dst; const void* src; size_t n; } ins[] = {
+        {dq, q, T ? in_b : 0}, {dk, k, T ? in_b : 0}, {dv, v, T ? in_b : 0},
+        {da, alpha, T ? gate_b : 0}, {de, eta, T ? gate_b : 0}, {db, beta, T ? gate_b : 0},
+        {dc, c, (T && need_c) ? gate_b : 0}, {dM0, M0, st_b}, {dS0, S0, st_b}};
+    for (auto& cp : ins)
+        if (cp.n && cudaMemcpyAsync(cp.dst, cp.src, cp.n, cudaMemcpyHostToDevice, s) != cudaSuccess)
+            return NM_ERR_CUDA;
+    int rc = nm_forward(h, B, H, T, T ? dq : nullptr, T ? dk : nullptr, T ? dv : nullptr,
+                        T ? da : nullptr, T ? de : nullptr, T ? db : nullptr,
+                        (T && need_c) ? dc : nullptr, dM0, dS0, T ? dy : nullptr, dMT, dST, stream);
+    if (rc != NM_OK) return rc;
+    if (T && cudaMemcpyAsync(y, dy, out_b, cudaMemcpyDeviceToHost, s) != cudaSuccess) return NM_ERR_CUDA;
+    if (cudaMemcpyAsync(M_T, dMT, st_b, cudaMemcpyDeviceToHost, s) != cudaSuccess) return NM_ERR_CUDA;
+    if (cudaMemcpyAsync(S_T, dST, st_b, cudaMemcpyDeviceToHost, s) != cudaSuccess) return NM_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) {
+        cudaGetLastError();
+        return NM_ERR_CUDA;
+    }
+    int st = 0;
+    if (cudaMemcpy(&st, h->d_status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return NM_ERR_CUDA;
+    if (st != 0) cudaMemset(h->d_status, 0, sizeof(int));
+    return st;
+}
+
+int nm_destroy(nm_handle_t h) {
+    if (!h) return NM_OK;
+    int rc = NM_OK;
+    {
+        DeviceGuard g(h->device);
+        if (g.ok) {
+            if (cudaDeviceSynchronize() != cudaSuccess) {
+                cudaGetLastError();
+                rc = NM_ERR_CUDA;
+            }
+            if (h->workspace) cudaFree(h->workspace);
+            if (h->stage) cudaFree(h->stage);
+            if (h->d_status) cudaFree(h->d_status);
+        } else {
+            rc = NM_ERR_CUDA;
+        }
+    }
+    free(h);
+    return rc;
+}
+
+}  // extern "C"

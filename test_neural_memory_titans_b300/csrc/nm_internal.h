@@ -1,0 +1,57 @@
+// Internal declarations shared by the host API (nm_api.cu) and the kernel
+// files.  Not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "nm.h"
+
+// One forward call's arguments, already validated on the host.
+struct nm_args {
+    int B, H, T;
+    const void* q;
+    const void* k;
+    const void* v;
+    const float* alpha;
+    const float* eta;
+    const float* beta;
+    const float* c;
+    const float* M0;
+    const float* S0;
+    void* y;
+    float* M_T;
+    float* S_T;
+    int* status;      // device status word owned by the handle
+    void* scratch;    // device workspace owned by the handle (may be NULL)
+    size_t scratch_bytes;
+};
+
+struct nm_handle {
+    nm_config cfg;
+    int device;
+    int path;          // NM_PATH_SIMT or NM_PATH_TC
+    int num_sms;
+    int* d_status;
+    void* workspace;
+    size_t workspace_bytes;
+    void* stage;       // device staging for nm_forward_host
+    size_t stage_bytes;
+    long long launches;
+};
+
+// Parameters per unit.
+static inline long long nm_param_count(const nm_config& c) {
+    return c.kind == NM_LINEAR ? (long long)c.d * c.d : 2LL * c.hidden * c.d;
+}
+
+// ---- fp32 FFMA kernels (nm_simt.cu) ----------------------------------------
+bool nm_simt_supports(const nm_config& c);
+size_t nm_simt_scratch_bytes(const nm_config& c, int B, int H);
+cudaError_t nm_simt_launch(const nm_config& c, const nm_args& a, cudaStream_t s, long long* launches);
+
+// ---- tcgen05 tensor-core kernels (nm_tc_*.cu) -----------------------------
+bool nm_tc_supports(const nm_config& c);
+size_t nm_tc_scratch_bytes(const nm_config& c, int B, int H);
+cudaError_t nm_tc_launch(const nm_config& c, const nm_args& a, cudaStream_t s, int num_sms, long long* launches);

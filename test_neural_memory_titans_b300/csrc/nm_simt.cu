@@ -1,0 +1,404 @@
+// fp32 FFMA kernels for the neural-memory forward pass.
+//
+// These are the precision path (fp32 inputs at 1e-4 parity) and the
+// any-shape path.  Both keep one (batch, head) unit per CTA for the whole
+// sequence and take every gradient of a chunk at the chunk-start weights
+// ("Titans: Imparare a Memorizzare al Tempo di Test", section "Addestramento
+// Parallelizzato"); the update and retrieval rules are those of sections
+// "Meccanismo di Aggiornamento della Memoria" / "Meccanismo di Dimenticanza"
+// and of the 0h-n0.github.io explainer, "メモリ読み出し".
+//
+//  * Linear memory: the CTA holds M, S and the chunk-start copy W0 in
+//    registers, one row per group of R threads.  Each chunk first forms the
+//    errors e_t = 2 (W0 k_t - v_t) for all its tokens (they only need W0),
+//    then advances S and M token by token with rank-1 updates and reads
+//    y_t = M_t q_t.  Exact fp32 recurrence, no b x b matrices.
+//
+//  * 2-layer MLP memory: the chunked-parallel form.  With a_t = 1 - alpha_t
+//    and, inside a chunk, A_t = prod_{j<=t} a_j, B_t = prod_{j<=t} beta_j,
+//    sigma_t = a_t sigma_{t-1} + eta_t B_t,
+//    u_{t,i} = c_i prod_{j=i+1..t} beta_j,
+//    Gamma_{t,i} = a_t Gamma_{t-1,i} + eta_t u_{t,i}  (Gamma_{i-1,i} = 0),
+//    the weights after token t are
+//        W_t = A_t W0 - sigma_t S0 - sum_{i<=t} Gamma_{t,i} g_i,
+//        S_t = B_t S0 + sum_{i<=t} u_{t,i} g_i,
+//    so retrieval and the chunk-end state are matrix products of the chunk's
+//    keys, queries, errors and backpropagated errors.  Gamma is built by the
+//    recursion above (never by dividing cumulative products), so beta = 0 and
+//    alpha = 1 are safe.  Intermediates live in a per-unit global workspace.
+#include <cuda_bf16.h>
+
+#include "nm_internal.h"
+
+namespace {
+
+template <typename T>
+__device__ __forceinline__ float ld_in(const T* p);
+template <>
+__device__ __forceinline__ float ld_in<float>(const float* p) { return *p; }
+template <>
+__device__ __forceinline__ float ld_in<__nv_bfloat16>(const __nv_bfloat16* p) { return __bfloat162float(*p); }
+
+template <typename T>
+__device__ __forceinline__ void st_out(T* p, float x);
+template <>
+__device__ __forceinline__ void st_out<float>(float* p, float x) { *p = x; }
+template <>
+__device__ __forceinline__ void st_out<__nv_bfloat16>(__nv_bfloat16* p, float x) { *p = __float2bfloat16_rn(x); }
+
+__device__ __forceinline__ float momentum_coef(int mode, float beta, const float* c, long long i) {
+    if (mode == NM_C_ONE_MINUS_BETA) return 1.0f - beta;
+    if (mode == NM_C_PER_TOKEN) return c[i];
+    return 1.0f;
+}
+
+__device__ __forceinline__ float silu_f(float z) { return z / (1.0f + expf(-z)); }
+__device__ __forceinline__ float dsilu_f(float z) {
+    float s = 1.0f / (1.0f + expf(-z));
+    return s * (1.0f + z * (1.0f - s));
+}
+
+// ----------------------------------------------------------------- linear
+
+constexpr int LIN_SB = 64;  // tokens staged in shared memory at a time
+constexpr int LIN_R = 4;    // threads per memory row
+
+template <int D>
+constexpr size_t lin_smem_bytes() {
+    return sizeof(float) * (3 * LIN_SB * D + 4 * LIN_SB);
+}
+
+template <int D, typename Tin, typename Tout>
+__global__ void __launch_bounds__(D * LIN_R) simt_linear_kernel(nm_args a, int chunk, int c_mode) {
+    constexpr int R = LIN_R;
+    constexpr int NT = D * R;
+    constexpr int J = D / R;
+    extern __shared__ float smem[];
+    float* Ks = smem;               // [LIN_SB][D]
+    float* Qs = Ks + LIN_SB * D;    // [LIN_SB][D]
+    float* Es = Qs + LIN_SB * D;    // [LIN_SB][D] errors at W0
+    float* ga = Es + LIN_SB * D;    // 1 - alpha
+    float* ge = ga + LIN_SB;        // eta
+    float* gb = ge + LIN_SB;        // beta
+    float* gc = gb + LIN_SB;        // c
+
+    const long long unit = blockIdx.x;
+    const int tid = threadIdx.x;
+    const int r = tid / R;
+    const int s = tid % R;
+    const long long T = a.T;
+    const long long P = (long long)D * D;
+    const Tin* q = (const Tin*)a.q + unit * T * D;
+    const Tin* k = (const Tin*)a.k + unit * T * D;
+    const Tin* v = (const Tin*)a.v + unit * T * D;
+    const float* al = a.alpha + unit * T;
+    const float* et = a.eta + unit * T;
+    const float* be = a.beta + unit * T;
+    const float* cc = a.c ? a.c + unit * T : nullptr;
+    Tout* y = (Tout*)a.y + unit * T * D;
+
+    float M[J], S[J], W0[J];
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+        M[j] = a.M0[unit * P + (long long)r * D + j * R + s];
+        S[j] = a.S0[unit * P + (long long)r * D + j * R + s];
+    }
+    for (long long t0 = 0; t0 < T; t0 += chunk) {
+        const long long t1 = min(t0 + (long long)chunk, T);
+#pragma unroll
+        for (int j = 0; j < J; ++j) W0[j] = M[j];
+        for (long long sb = t0; sb < t1; sb += LIN_SB) {
+            const int n = (int)min((long long)LIN_SB, t1 - sb);
+            __syncthreads();
+            for (int i = tid; i < n * D; i += NT) {
+                Ks[i] = ld_in(k + sb * D + i);
+                Qs[i] = ld_in(q + sb * D + i);
+            }
+            for (int i = tid; i < n; i += NT) {
+                ga[i] = 1.0f - al[sb + i];
+                ge[i] = et[sb + i];
+                gb[i] = be[sb + i];
+                gc[i] = momentum_coef(c_mode, be[sb + i], cc, sb + i);
+            }
+            __syncthreads();
+            // e_t = 2 (W0 k_t - v_t): gradient of ||W0 k - v||^2 is e k^T
+            for (int t = 0; t < n; ++t) {
+                float acc = 0.f;
+#pragma unroll
+                for (int j = 0; j < J; ++j) acc = fmaf(W0[j], Ks[t * D + j * R + s], acc);
+#pragma unroll
+                for (int o = R / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+                if (s == 0) Es[t * D + r] = 2.0f * (acc - ld_in(v + (sb + t) * D + r));
+            }
+            __syncthreads();
+            for (int t = 0; t < n; ++t) {
+                const float ce = gc[t] * Es[t * D + r];
+                const float at = ga[t], eh = ge[t], bt = gb[t];
+                float acc = 0.f;
+#pragma unroll
+                for (int j = 0; j < J; ++j) {
+                    const float kv = Ks[t * D + j * R + s];
+                    S[j] = fmaf(bt, S[j], ce * kv);          // S = beta S + c e k^T
+                    M[j] = fmaf(at, M[j], -eh * S[j]);       // M = (1-alpha) M - eta S
+                    acc = fmaf(M[j], Qs[t * D + j * R + s], acc);
+                }
+#pragma unroll
+                for (int o = R / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+                if (s == 0) st_out(y + (sb + t) * D + r, acc);
+            }
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+        a.M_T[unit * P + (long long)r * D + j * R + s] = M[j];
+        a.S_T[unit * P + (long long)r * D + j * R + s] = S[j];
+    }
+}
+
+template <int D, typename Tin, typename Tout>
+cudaError_t launch_linear(const nm_config& c, const nm_args& a, cudaStream_t s) {
+    constexpr size_t smem = lin_smem_bytes<D>();
+    auto kern = simt_linear_kernel<D, Tin, Tout>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    kern<<<(unsigned)(a.B * a.H), D * LIN_R, smem, s>>>(a, c.chunk, c.c_mode);
+    return cudaGetLastError();
+}
+
+template <typename Tin, typename Tout>
+cudaError_t launch_linear_d(const nm_config& c, const nm_args& a, cudaStream_t s) {
+    switch (c.d) {
+        case 16: return launch_linear<16, Tin, Tout>(c, a, s);
+        case 32: return launch_linear<32, Tin, Tout>(c, a, s);
+        case 64: return launch_linear<64, Tin, Tout>(c, a, s);
+        case 128: return launch_linear<128, Tin, Tout>(c, a, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+// ----------------------------------------------------------------- MLP2
+
+constexpr int MLP_THREADS = 512;
+constexpr int MLP_MAX_CHUNK = 256;
+
+__host__ __device__ inline size_t mlp_unit_floats(int d, int h, int b) {
+    return 2 * (size_t)b * b + 2 * (size_t)b + 4 * (size_t)b * d + 4 * (size_t)b * h;
+}
+
+template <typename Tin, typename Tout>
+__global__ void __launch_bounds__(MLP_THREADS) simt_mlp_kernel(nm_args a, int d, int hd, int chunk, int c_mode) {
+    __shared__ float sA[MLP_MAX_CHUNK], sB[MLP_MAX_CHUNK], sSg[MLP_MAX_CHUNK];
+    __shared__ float sa[MLP_MAX_CHUNK], se[MLP_MAX_CHUNK], sbt[MLP_MAX_CHUNK], sc[MLP_MAX_CHUNK];
+    const long long unit = blockIdx.x;
+    const int tid = threadIdx.x;
+    const int NT = blockDim.x;
+    const long long T = a.T;
+    const long long P = 2LL * hd * d;
+    const int b = chunk;
+
+    float* ws = (float*)a.scratch + unit * mlp_unit_floats(d, hd, b);
+    float* Gam = ws;                   // [b][b]   Gamma_{t,i}
+    float* ub = Gam + (size_t)b * b;   // [b]      u_{n-1,i}
+    float* gl = ub + b;                // [b]      Gamma_{n-1,i}
+    float* Kf = gl + b;                // [b][d]
+    float* Qf = Kf + (size_t)b * d;    // [b][d]
+    float* Vf = Qf + (size_t)b * d;    // [b][d]
+    float* E = Vf + (size_t)b * d;     // [b][d]   e_t = 2 (yhat_t - v_t)
+    float* Z = E + (size_t)b * d;      // [b][h]   W1 k_t
+    float* Ak = Z + (size_t)b * hd;    // [b][h]   silu(W1 k_t)
+    float* Dl = Ak + (size_t)b * hd;   // [b][h]   delta_t = (W2^T e_t) * silu'(z_t)
+    float* Aq = Dl + (size_t)b * hd;   // [b][h]   silu(W1_t q_t)
+    float* Pm = Aq + (size_t)b * hd;   // [b][b]   Gamma (.) (inner products)
+
+    const Tin* q = (const Tin*)a.q + unit * T * d;
+    const Tin* k = (const Tin*)a.k + unit * T * d;
+    const Tin* v = (const Tin*)a.v + unit * T * d;
+    const float* al = a.alpha + unit * T;
+    const float* et = a.eta + unit * T;
+    const float* be = a.beta + unit * T;
+    const float* cc = a.c ? a.c + unit * T : nullptr;
+    Tout* y = (Tout*)a.y + unit * T * d;
+    float* W1 = a.M_T + unit * P;        // [h][d]
+    float* W2 = W1 + (long long)hd * d;  // [d][h]
+    float* S1 = a.S_T + unit * P;
+    float* S2 = S1 + (long long)hd * d;
+    if (a.M_T != a.M0)
+        for (long long i = tid; i < P; i += NT) W1[i] = a.M0[unit * P + i];
+    if (a.S_T != a.S0)
+        for (long long i = tid; i < P; i += NT) S1[i] = a.S0[unit * P + i];
+    __syncthreads();
+
+    for (long long t0 = 0; t0 < T; t0 += b) {
+        const int n = (int)min((long long)b, T - t0);
+        for (int i = tid; i < n * d; i += NT) {
+            Kf[i] = ld_in(k + t0 * d + i);
+            Qf[i] = ld_in(q + t0 * d + i);
+            Vf[i] = ld_in(v + t0 * d + i);
+        }
+        for (int i = tid; i < n; i += NT) {
+            sa[i] = 1.0f - al[t0 + i];
+            se[i] = et[t0 + i];
+            sbt[i] = be[t0 + i];
+            sc[i] = momentum_coef(c_mode, be[t0 + i], cc, t0 + i);
+        }
+        __syncthreads();
+        // decay / momentum scan, one column i of Gamma per thread
+        for (int i = tid; i < n; i += NT) {
+            float u = sc[i];
+            float G = se[i] * u;
+            Gam[(size_t)i * b + i] = G;
+            for (int t = i + 1; t < n; ++t) {
+                u *= sbt[t];
+                G = fmaf(sa[t], G, se[t] * u);
+                Gam[(size_t)t * b + i] = G;
+            }
+            ub[i] = u;
+            gl[i] = G;
+        }
+        if (tid == 0) {
+            float A = 1.f, Bc = 1.f, sg = 0.f;
+            for (int t = 0; t < n; ++t) {
+                A *= sa[t];
+                Bc *= sbt[t];
+                sg = fmaf(sa[t], sg, se[t] * Bc);
+                sA[t] = A;
+                sB[t] = Bc;
+                sSg[t] = sg;
+            }
+        }
+        __syncthreads();
+        // key forward at W0: z = W1 k, a = silu(z)
+        for (int idx = tid; idx < n * hd; idx += NT) {
+            const int t = idx / hd, j = idx % hd;
+            float acc = 0.f;
+            for (int x = 0; x < d; ++x) acc = fmaf(Kf[t * d + x], W1[(long long)j * d + x], acc);
+            Z[idx] = acc;
+            Ak[idx] = silu_f(acc);
+        }
+        __syncthreads();
+        // e = 2 (W2 a - v)
+        for (int idx = tid; idx < n * d; idx += NT) {
+            const int t = idx / d, o = idx % d;
+            float acc = 0.f;
+            for (int j = 0; j < hd; ++j) acc = fmaf(Ak[t * hd + j], W2[(long long)o * hd + j], acc);
+            E[idx] = 2.0f * (acc - Vf[idx]);
+        }
+        __syncthreads();
+        // delta = (W2^T e) * silu'(z);  Pm = Gamma (.) (Q K^T), lower triangle
+        for (int idx = tid; idx < n * hd; idx += NT) {
+            const int t = idx / hd, j = idx % hd;
+            float acc = 0.f;
+            for (int o = 0; o < d; ++o) acc = fmaf(E[t * d + o], W2[(long long)o * hd + j], acc);
+            Dl[idx] = acc * dsilu_f(Z[idx]);
+        }
+        for (int idx = tid; idx < n * n; idx += NT) {
+            const int t = idx / n, i = idx % n;
+            float acc = 0.f;
+            if (i <= t) {
+                for (int x = 0; x < d; ++x) acc = fmaf(Qf[t * d + x], Kf[i * d + x], acc);
+                acc *= Gam[(size_t)t * b + i];
+            }
+            Pm[(size_t)t * b + i] = acc;
+        }
+        __syncthreads();
+        // layer 1 at token t: A_t W1 q - sigma_t S1 q - sum_i Gamma_{t,i} (k_i.q) delta_i
+        for (int idx = tid; idx < n * hd; idx += NT) {
+            const int t = idx / hd, j = idx % hd;
+            float m1 = 0.f, s1 = 0.f, g = 0.f;
+            for (int x = 0; x < d; ++x) {
+                const float qx = Qf[t * d + x];
+                m1 = fmaf(qx, W1[(long long)j * d + x], m1);
+                s1 = fmaf(qx, S1[(long long)j * d + x], s1);
+            }
+            for (int i = 0; i <= t; ++i) g = fmaf(Pm[(size_t)t * b + i], Dl[i * hd + j], g);
+            Aq[idx] = silu_f(sA[t] * m1 - sSg[t] * s1 - g);
+        }
+        __syncthreads();
+        // Pm = Gamma (.) (Aq Ak^T)
+        for (int idx = tid; idx < n * n; idx += NT) {
+            const int t = idx / n, i = idx % n;
+            float acc = 0.f;
+            if (i <= t) {
+                for (int j = 0; j < hd; ++j) acc = fmaf(Aq[t * hd + j], Ak[i * hd + j], acc);
+                acc *= Gam[(size_t)t * b + i];
+            }
+            Pm[(size_t)t * b + i] = acc;
+        }
+        __syncthreads();
+        // layer 2 at token t: A_t W2 a - sigma_t S2 a - sum_i Gamma_{t,i} (a(k_i).a) e_i
+        for (int idx = tid; idx < n * d; idx += NT) {
+            const int t = idx / d, o = idx % d;
+            float m2 = 0.f, s2 = 0.f, g = 0.f;
+            for (int j = 0; j < hd; ++j) {
+                const float aj = Aq[t * hd + j];
+                m2 = fmaf(aj, W2[(long long)o * hd + j], m2);
+                s2 = fmaf(aj, S2[(long long)o * hd + j], s2);
+            }
+            for (int i = 0; i <= t; ++i) g = fmaf(Pm[(size_t)t * b + i], E[i * d + o], g);
+            st_out(y + (t0 + t) * d + o, sA[t] * m2 - sSg[t] * s2 - g);
+        }
+        __syncthreads();
+        // chunk-end state: W = A W0 - sigma S0 - sum_i Gamma_{n-1,i} g_i, S = B S0 + sum_i u_{n-1,i} g_i
+        const float An = sA[n - 1], Bn = sB[n - 1], sn = sSg[n - 1];
+        for (int idx = tid; idx < hd * d; idx += NT) {
+            const int j = idx / d, x = idx % d;
+            float gw = 0.f, gs = 0.f;
+            for (int i = 0; i < n; ++i) {
+                const float dk = Dl[i * hd + j] * Kf[i * d + x];
+                gw = fmaf(gl[i], dk, gw);
+                gs = fmaf(ub[i], dk, gs);
+            }
+            const float w = W1[idx], s1 = S1[idx];
+            W1[idx] = An * w - sn * s1 - gw;
+            S1[idx] = Bn * s1 + gs;
+        }
+        for (int idx = tid; idx < d * hd; idx += NT) {
+            const int o = idx / hd, j = idx % hd;
+            float gw = 0.f, gs = 0.f;
+            for (int i = 0; i < n; ++i) {
+                const float ea = E[i * d + o] * Ak[i * hd + j];
+                gw = fmaf(gl[i], ea, gw);
+                gs = fmaf(ub[i], ea, gs);
+            }
+            const float w = W2[idx], s2 = S2[idx];
+            W2[idx] = An * w - sn * s2 - gw;
+            S2[idx] = Bn * s2 + gs;
+        }
+        __syncthreads();
+    }
+}
+
+template <typename Tin, typename Tout>
+cudaError_t launch_mlp(const nm_config& c, const nm_args& a, cudaStream_t s) {
+    simt_mlp_kernel<Tin, Tout><<<(unsigned)(a.B * a.H), MLP_THREADS, 0, s>>>(a, c.d, c.hidden, c.chunk, c.c_mode);
+    return cudaGetLastError();
+}
+
+template <typename Tin>
+cudaError_t dispatch_out(const nm_config& c, const nm_args& a, cudaStream_t s) {
+    if (c.kind == NM_LINEAR)
+        return c.out_dtype == NM_BF16 ? launch_linear_d<Tin, __nv_bfloat16>(c, a, s)
+                                      : launch_linear_d<Tin, float>(c, a, s);
+    return c.out_dtype == NM_BF16 ? launch_mlp<Tin, __nv_bfloat16>(c, a, s) : launch_mlp<Tin, float>(c, a, s);
+}
+
+}  // namespace
+
+bool nm_simt_supports(const nm_config& c) {
+    if (c.chunk < 1 || c.chunk > 256) return false;
+    const bool d_ok = c.d == 16 || c.d == 32 || c.d == 64 || c.d == 128;
+    if (!d_ok) return false;
+    if (c.kind == NM_LINEAR) return true;
+    return c.hidden > 0 && c.hidden <= 1024 && c.hidden % 32 == 0;
+}
+
+size_t nm_simt_scratch_bytes(const nm_config& c, int B, int H) {
+    if (c.kind == NM_LINEAR) return 0;
+    return sizeof(float) * mlp_unit_floats(c.d, c.hidden, c.chunk) * (size_t)B * (size_t)H;
+}
+
+cudaError_t nm_simt_launch(const nm_config& c, const nm_args& a, cudaStream_t s, long long* launches) {
+    cudaError_t e = c.in_dtype == NM_BF16 ? dispatch_out<__nv_bfloat16>(c, a, s) : dispatch_out<float>(c, a, s);
+    if (e == cudaSuccess) *launches += 1;
+    return e;
+}

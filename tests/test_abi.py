@@ -1,0 +1,149 @@
+"""The C-ABI boundary: the library loads without a GPU, exports every entry
+point include/nm.h declares, and (on a GPU) rejects bad arguments on the host
+with the documented status and nothing launched."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+import torch
+
+import test_neural_memory_titans_b300 as nm
+from test_neural_memory_titans_b300 import workloads as W
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADERS = [os.path.join(ROOT, "include", f) for f in sorted(os.listdir(os.path.join(ROOT, "include")))
+           if f.endswith(".h")]
+
+
+def _declared():
+    names = set()
+    for h in HEADERS:
+        src = open(h).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        for m in re.finditer(r"^\s*(?:const\s+)?[\w\s\*]+?\b(nm_\w+)\s*\(", src, flags=re.M):
+            names.add(m.group(1))
+    return names
+
+
+def test_library_loads_and_exports_header_symbols():
+    lib = nm.load_library()
+    declared = _declared()
+    assert {"nm_create", "nm_forward", "nm_destroy", "nm_synchronize", "nm_status_string"} <= declared
+    for name in declared:
+        assert hasattr(lib, name), name
+    out = subprocess.run(["nm", "-D", "--defined-only", nm.LIB_PATH], capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\bT (nm_\w+)", out))
+    assert declared <= exported, declared - exported
+    assert set(nm.EXPORTED) <= exported
+
+
+def test_status_strings_without_gpu():
+    for code in range(0, 9):
+        s = nm.status_string(code)
+        assert isinstance(s, str) and s
+    assert nm.status_string(12345) == "unknown status"
+
+
+def test_status_codes_match_header():
+    src = open(os.path.join(ROOT, "include", "nm.h")).read()
+    defs = dict((k, int(v)) for k, v in re.findall(r"#define\s+(NM_\w+)\s+(-?\d+)", src))
+    for name in ("NM_OK", "NM_ERR_ARG", "NM_ERR_ALIGN", "NM_ERR_UNSUPPORTED", "NM_ERR_ALIAS", "NM_ERR_CUDA",
+                 "NM_ERR_NOMEM", "NM_ERR_DEVICE_TIMEOUT", "NM_ERR_DEVICE_CHECK"):
+        assert getattr(nm, name) == defs[name]
+    for name, py in (("NM_LINEAR", "LINEAR"), ("NM_MLP2", "MLP2"), ("NM_F32", "F32"), ("NM_BF16", "BF16"),
+                     ("NM_C_ONE", "C_ONE"), ("NM_C_ONE_MINUS_BETA", "C_ONE_MINUS_BETA"),
+                     ("NM_C_PER_TOKEN", "C_PER_TOKEN"), ("NM_PATH_AUTO", "PATH_AUTO"),
+                     ("NM_PATH_SIMT", "PATH_SIMT"), ("NM_PATH_TC", "PATH_TC")):
+        assert getattr(nm, py) == defs[name]
+
+
+def test_null_handle_and_bad_config_without_gpu():
+    lib = nm.load_library()
+    assert lib.nm_forward(None, 1, 1, 1, *([None] * 12), None) == nm.NM_ERR_ARG
+    assert lib.nm_synchronize(None) == nm.NM_ERR_ARG
+    assert lib.nm_destroy(None) == nm.NM_OK
+    h = ctypes.c_void_p()
+    bad = nm._Config(7, 64, 0, 64, nm.BF16, nm.BF16, nm.C_ONE, nm.PATH_AUTO)
+    assert lib.nm_create(ctypes.byref(bad), 0, ctypes.byref(h)) == nm.NM_ERR_ARG
+    unsupported = nm._Config(nm.LINEAR, 48, 0, 64, nm.BF16, nm.BF16, nm.C_ONE, nm.PATH_SIMT)
+    assert lib.nm_create(ctypes.byref(unsupported), 0, ctypes.byref(h)) == nm.NM_ERR_UNSUPPORTED
+    big_chunk = nm._Config(nm.LINEAR, 64, 0, 1024, nm.BF16, nm.BF16, nm.C_ONE, nm.PATH_AUTO)
+    assert lib.nm_create(ctypes.byref(big_chunk), 0, ctypes.byref(h)) == nm.NM_ERR_UNSUPPORTED
+    assert lib.nm_create(None, 0, ctypes.byref(h)) == nm.NM_ERR_ARG
+
+
+# ------------------------------------------------------------------ on a GPU
+
+def _args(wl, dev="cuda"):
+    x = W.make_inputs(wl, dev)
+    y = torch.empty(x["q"].shape, dtype=wl.dtype, device=dev)
+    MT = torch.empty_like(x["M0"])
+    ST = torch.empty_like(x["S0"])
+    return x, y, MT, ST
+
+
+def _call(mem, B, H, T, x, y, MT, ST, **over):
+    p = dict(q=x["q"], k=x["k"], v=x["v"], alpha=x["alpha"], eta=x["eta"], beta=x["beta"], c=None,
+             M0=x["M0"], S0=x["S0"], y=y, M_T=MT, S_T=ST)
+    p.update(over)
+
+    def ptr(t):
+        if t is None:
+            return None
+        if isinstance(t, int):
+            return ctypes.c_void_p(t)
+        return ctypes.c_void_p(t.data_ptr())
+    return nm.load_library().nm_forward(mem._h, B, H, T, *(ptr(p[k]) for k in
+                                        ("q", "k", "v", "alpha", "eta", "beta", "c", "M0", "S0", "y", "M_T",
+                                         "S_T")), None)
+
+
+@pytest.mark.gpu
+def test_host_validation_launches_nothing():
+    wl = W.WORKLOADS[2].with_sizes(B=2, H=2, T=128)
+    x, y, MT, ST = _args(wl)
+    mem = nm.NeuralMemory(wl.kind, wl.d, 0, wl.chunk, in_dtype=wl.dtype)
+    n0 = mem.launches
+    B, H, T = wl.B, wl.H, wl.T
+    assert _call(mem, B, H, T, x, y, MT, ST, q=None) == nm.NM_ERR_ARG
+    assert _call(mem, -1, H, T, x, y, MT, ST) == nm.NM_ERR_ARG
+    assert _call(mem, B, H, T, x, y, MT, ST, c=x["alpha"]) == nm.NM_ERR_ARG  # c given but c_mode is ONE
+    assert _call(mem, B, H, T, x, y, MT, ST, k=x["k"].data_ptr() + 2) == nm.NM_ERR_ALIGN
+    assert _call(mem, B, H, T, x, y, MT, ST, M_T=x["S0"]) == nm.NM_ERR_ALIAS          # M_T on S0
+    assert _call(mem, B, H, T, x, y, MT, ST, y=x["q"]) == nm.NM_ERR_ALIAS             # y on an input
+    assert _call(mem, B, H, T, x, y, MT, ST, S_T=MT) == nm.NM_ERR_ALIAS               # outputs overlap
+    part = x["M0"].data_ptr() + 16 * 4
+    assert _call(mem, B, H, T, x, y, MT, ST, M_T=part) == nm.NM_ERR_ALIAS             # partial overlap
+    assert mem.launches == n0
+    assert _call(mem, 0, H, T, x, y, MT, ST) == nm.NM_OK and mem.launches == n0     # empty batch
+    # exact aliasing of the state is allowed
+    M = x["M0"].clone()
+    S = x["S0"].clone()
+    assert _call(mem, B, H, T, x, y, M, S, M0=M, S0=S) == nm.NM_OK
+    assert mem.synchronize() == nm.NM_OK
+    assert mem.launches == n0 + 1
+
+
+@pytest.mark.gpu
+def test_per_token_c_required():
+    wl = W.WORKLOADS[2].with_sizes(B=1, H=1, T=64)
+    x, y, MT, ST = _args(wl)
+    mem = nm.NeuralMemory(wl.kind, wl.d, 0, wl.chunk, in_dtype=wl.dtype, c_mode=nm.C_PER_TOKEN)
+    assert _call(mem, 1, 1, 64, x, y, MT, ST) == nm.NM_ERR_ARG
+    assert _call(mem, 1, 1, 64, x, y, MT, ST, c=x["beta"]) == nm.NM_OK
+    assert mem.synchronize() == nm.NM_OK
+
+
+@pytest.mark.gpu
+def test_binding_rejects_wrong_tensors():
+    wl = W.WORKLOADS[2].with_sizes(B=1, H=1, T=64)
+    x = W.make_inputs(wl, "cuda")
+    mem = nm.NeuralMemory(wl.kind, wl.d, 0, wl.chunk, in_dtype=wl.dtype)
+    with pytest.raises(TypeError):
+        mem.forward(x["q"].float(), x["k"], x["v"], x["alpha"], x["eta"], x["beta"], x["M0"], x["S0"])
+    with pytest.raises(ValueError):
+        mem.forward(x["q"].cpu(), x["k"], x["v"], x["alpha"], x["eta"], x["beta"], x["M0"], x["S0"])
+    with pytest.raises(ValueError):
+        mem.forward(x["q"], x["k"], x["v"], x["alpha"], x["eta"], x["beta"], x["M0"][..., :-1], x["S0"])

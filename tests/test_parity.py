@@ -1,0 +1,245 @@
+"""Parity of the CUDA path with the fp64 oracle, element by element on the
+same seeded inputs (relative L2; tolerances in tests/_helpers.py).
+
+Linear-memory workloads are stable and use plain full-length parity.  The
+2-layer MLP workloads diverge to inf under the literal reading within a few
+chunks (in the oracle as well), so they use: prefix parity over the chunks
+before the divergence, teacher-forced parity on every (sampled) chunk started
+from random nondegenerate states, and agreement on the chunk where the
+literal run blows up.
+"""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import test_neural_memory_titans_b300 as nm
+from test_neural_memory_titans_b300 import workloads as W
+
+from _helpers import TOL, chunks_as_units, compare, f64, gpu_forward, oracle_forward, pick, rel_l2
+
+pytestmark = pytest.mark.gpu
+
+PATHS = [nm.PATH_SIMT, nm.PATH_TC]
+
+
+def _skip_unsupported(wl, path, chunk=None):
+    try:
+        m = nm.NeuralMemory(wl.kind, wl.d, wl.hidden, wl.chunk if chunk is None else chunk, in_dtype=wl.dtype,
+                            path=path)
+        m.close()
+    except nm.NMError as e:
+        if e.status == nm.NM_ERR_UNSUPPORTED:
+            pytest.skip("path %d not built for this shape" % path)
+        raise
+
+
+# ------------------------------------------------------------ workload 0 (fp32)
+
+@pytest.mark.parametrize("path", [nm.PATH_AUTO, nm.PATH_SIMT])
+def test_workload0_full(path):
+    wl = W.WORKLOADS[0]
+    x = W.make_inputs(wl, "cuda")
+    gpu = gpu_forward(wl, x, path)
+    ref = oracle_forward(wl, x)
+    compare(wl, gpu, ref)
+
+
+# ------------------------------------------------------------ linear, small shapes
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("wid,T,chunk", [(2, 1000, 64), (2, 130, 64), (4, 1100, 256), (4, 300, 64),
+                                         (0, 333, 16), (2, 64, 64), (4, 17, 256)])
+def test_linear_small_ragged(path, wid, T, chunk):
+    wl = W.WORKLOADS[wid].with_sizes(B=2, H=3, T=T, segment=0)
+    wl = dataclasses.replace(wl, chunk=chunk)
+    _skip_unsupported(wl, path)
+    x = W.make_inputs(wl, "cuda", seed=5 + T)
+    M0, S0 = W.random_state(wl, "cuda", seed=T, scale=0.5)
+    gpu = gpu_forward(wl, x, path, M0=M0, S0=S0)
+    ref = oracle_forward(wl, x, M0=M0, S0=S0)
+    compare(wl, gpu, ref)
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("c_mode", [nm.C_ONE_MINUS_BETA, nm.C_PER_TOKEN])
+def test_momentum_forms(path, c_mode):
+    wl = W.WORKLOADS[2].with_sizes(B=1, H=2, T=200)
+    _skip_unsupported(wl, path)
+    x = W.make_inputs(wl, "cuda", seed=31)
+    if c_mode == nm.C_PER_TOKEN:
+        x["c"] = torch.rand(x["alpha"].shape, device="cuda", generator=torch.Generator("cuda").manual_seed(3))
+    gpu = gpu_forward(wl, x, path, c_mode=c_mode)
+    ref = oracle_forward(wl, x, c_mode=c_mode)
+    compare(wl, gpu, ref)
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_workload2_full_sampled_units(path):
+    """Full size B=8, H=16, T=16384 in the benchmarked launch; the oracle
+    checks three units (first, a middle one, last)."""
+    wl = W.WORKLOADS[2]
+    _skip_unsupported(wl, path)
+    x = W.make_inputs(wl, "cuda")
+    gpu = gpu_forward(wl, x, path)
+    units = [0, 77, wl.B * wl.H - 1]
+    ref = oracle_forward(wl, x, units=units)
+    compare(wl, gpu, ref, units=units)
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_workload4_streaming(path):
+    """Segments of the streamed workload carry (M, S) in place (M_T == M0);
+    two segments of 4096 tokens checked against one oracle run over 8192."""
+    wl = W.WORKLOADS[4].with_sizes(T=8192, segment=4096)
+    _skip_unsupported(wl, path)
+    x = W.make_inputs(wl, "cuda", seed=44)
+    mem = nm.NeuralMemory(wl.kind, wl.d, 0, wl.chunk, in_dtype=wl.dtype, path=path)
+    M = x["M0"].clone()
+    S = x["S0"].clone()
+    ys = []
+    for s0 in range(0, wl.T, wl.segment):
+        sl = lambda t: t[:, :, s0:s0 + wl.segment].contiguous()
+        y, _, _ = mem.forward(sl(x["q"]), sl(x["k"]), sl(x["v"]), sl(x["alpha"]), sl(x["eta"]), sl(x["beta"]),
+                              M, S, M_T=M, S_T=S)
+        ys.append(y)
+    assert mem.synchronize() == nm.NM_OK
+    y = torch.cat(ys, dim=2)
+    ref = oracle_forward(wl, x)
+    compare(wl, (y, M, S), ref)
+
+
+# ------------------------------------------------------------ MLP memories
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("wid", [1, 3])
+def test_mlp_prefix_parity_full_heads(path, wid):
+    """Every unit of the workload over the first 3 chunks (before the
+    literal run diverges)."""
+    wl = W.WORKLOADS[wid]
+    wl = wl.with_sizes(T=3 * wl.chunk)
+    _skip_unsupported(wl, path)
+    x = W.make_inputs(wl, "cuda")
+    gpu = gpu_forward(wl, x, path)
+    ref = oracle_forward(wl, x)
+    compare(wl, gpu, ref)
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("wid,n_units", [(1, 192), (3, 48)])
+def test_mlp_teacher_forced_chunks(path, wid, n_units):
+    """Chunks of the full-size workload, each pair of consecutive chunks
+    started from a random nondegenerate state (W ~ N(0, 1/fan_in))."""
+    wl = W.WORKLOADS[wid]
+    _skip_unsupported(wl, path)
+    x = W.make_inputs(wl, "cuda")
+    nchunks = wl.T // wl.chunk
+    rng = np.random.default_rng(wid)
+    ids = [(int(rng.integers(wl.B * wl.H)), int(rng.integers(nchunks - 1))) for _ in range(n_units)]
+    wl2, x2 = chunks_as_units(wl, x, ids, span=2 * wl.chunk)
+    gpu = gpu_forward(wl2, x2, path)
+    ref = oracle_forward(wl2, x2)
+    compare(wl2, gpu, ref)
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("wid", [1])
+def test_mlp_literal_run_diverges_at_same_chunk(path, wid):
+    """The literal full-length run: the first chunk whose |y| exceeds 1e6
+    agrees with the oracle's within one chunk, on sampled units."""
+    wl = W.WORKLOADS[wid]
+    _skip_unsupported(wl, path)
+    x = W.make_inputs(wl, "cuda")
+    gpu = gpu_forward(wl, x, path)
+    T = 12 * wl.chunk
+    units = [0, wl.B * wl.H - 1]
+    ref = oracle_forward(wl, x, units=units, T=T)
+    yg = pick(gpu[0], wl, units, T)[0]
+    yr = ref[0][0]
+    for i in range(len(units)):
+        def first_big(y):
+            for c in range(T // wl.chunk):
+                blk = y[i, c * wl.chunk:(c + 1) * wl.chunk]
+                if not np.all(np.isfinite(blk)) or np.abs(blk).max() > 1e6:
+                    return c
+            return T // wl.chunk
+        cg, cr = first_big(yg), first_big(yr)
+        assert cr < T // wl.chunk, "oracle did not diverge in the window"
+        assert abs(cg - cr) <= 1, (cg, cr)
+
+
+# ------------------------------------------------------------ edge cases
+
+@pytest.mark.parametrize("path", PATHS)
+def test_zero_tokens_copies_state(path):
+    wl = W.WORKLOADS[2].with_sizes(B=1, H=2, T=0)
+    _skip_unsupported(wl, path)
+    x = W.make_inputs(wl.with_sizes(T=1), "cuda")
+    for key in ("q", "k", "v", "alpha", "eta", "beta"):
+        x[key] = x[key][:, :, :0].contiguous()
+    M0, S0 = W.random_state(wl, "cuda")
+    y, MT, ST, _ = gpu_forward(wl, x, path, M0=M0, S0=S0)
+    assert y.numel() == 0 and torch.equal(MT, M0) and torch.equal(ST, S0)
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("T,chunk", [(1, 64), (5, 1), (63, 64), (65, 64)])
+def test_tiny_and_chunk_edges(path, T, chunk):
+    wl = W.WORKLOADS[2].with_sizes(B=1, H=2, T=T)
+    wl = dataclasses.replace(wl, chunk=chunk)
+    _skip_unsupported(wl, path)
+    x = W.make_inputs(wl, "cuda", seed=9)
+    M0, S0 = W.random_state(wl, "cuda", seed=2, scale=0.5)
+    gpu = gpu_forward(wl, x, path, M0=M0, S0=S0)
+    compare(wl, gpu, oracle_forward(wl, x, M0=M0, S0=S0))
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_degenerate_gates(path):
+    """alpha = 1 (full wipe), beta = 0 (no momentum) and eta = 0 (pure decay)
+    inside one call."""
+    wl = W.WORKLOADS[2].with_sizes(B=1, H=2, T=256)
+    _skip_unsupported(wl, path)
+    x = W.make_inputs(wl, "cuda", seed=12)
+    x["alpha"][:, :, 40] = 1.0
+    x["beta"][:, :, 100:140] = 0.0
+    x["eta"][:, :, 180:200] = 0.0
+    M0, S0 = W.random_state(wl, "cuda", seed=3)
+    gpu = gpu_forward(wl, x, path, M0=M0, S0=S0)
+    compare(wl, gpu, oracle_forward(wl, x, M0=M0, S0=S0))
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_mlp_small_ragged_and_forms(path):
+    wl = W.WORKLOADS[1].with_sizes(B=1, H=3, T=100)
+    _skip_unsupported(wl, path)
+    x = W.make_inputs(wl, "cuda", seed=21)
+    M0, S0 = W.random_state(wl, "cuda", seed=4)
+    for c_mode in (nm.C_ONE, nm.C_ONE_MINUS_BETA):
+        gpu = gpu_forward(wl, x, path, M0=M0, S0=S0, c_mode=c_mode)
+        compare(wl, gpu, oracle_forward(wl, x, M0=M0, S0=S0, c_mode=c_mode))
+
+
+def test_simt_path_fp32_mlp_tight():
+    """The FFMA path on fp32 inputs meets the fp32 tolerance for an MLP memory."""
+    wl = W.WORKLOADS[1].with_sizes(B=1, H=2, T=150)
+    wl = dataclasses.replace(wl, dtype=torch.float32)
+    x = W.make_inputs(wl, "cuda", seed=8)
+    M0, S0 = W.random_state(wl, "cuda", seed=5)
+    gpu = gpu_forward(wl, x, nm.PATH_SIMT, M0=M0, S0=S0)
+    compare(wl, gpu, oracle_forward(wl, x, M0=M0, S0=S0))
+
+
+def test_forward_host_matches_device():
+    wl = W.WORKLOADS[2].with_sizes(B=2, H=2, T=300)
+    x = W.make_inputs(wl, "cpu", seed=13)
+    mem = nm.NeuralMemory(wl.kind, wl.d, 0, wl.chunk, in_dtype=wl.dtype)
+    pin = {k: (v.pin_memory() if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
+    yh, Mh, Sh = mem.forward_host(pin["q"], pin["k"], pin["v"], pin["alpha"], pin["eta"], pin["beta"],
+                                  pin["M0"], pin["S0"])
+    g = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
+    yd, Md, Sd = mem.forward(g["q"], g["k"], g["v"], g["alpha"], g["eta"], g["beta"], g["M0"], g["S0"])
+    assert mem.synchronize() == nm.NM_OK
+    assert torch.equal(yh, yd.cpu()) and torch.equal(Mh, Md.cpu()) and torch.equal(Sh, Sd.cpu())
