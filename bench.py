@@ -81,26 +81,23 @@ class ClockSampler:
         self.reasons = set()
         self.max_mhz = None
         self.period = period_s
+        self.err = None
         self._stop = threading.Event()
         self._t = None
+        self.nv = None
+        props = torch.cuda.get_device_properties(device_index)
+        self.pci = "%08x:%02x:%02x.0" % (props.pci_domain_id, props.pci_bus_id, props.pci_device_id)
         try:
             import pynvml
             pynvml.nvmlInit()
-            self.nv = pynvml
-            uuid = torch.cuda.get_device_properties(device_index).uuid
-            self.h = None
-            for i in range(pynvml.nvmlDeviceGetCount()):
-                hh = pynvml.nvmlDeviceGetHandleByIndex(i)
-                u = pynvml.nvmlDeviceGetUUID(hh)
-                u = u.decode() if isinstance(u, bytes) else u
-                if str(uuid) in u:
-                    self.h = hh
-            if self.h is None:
+            try:
+                self.h = pynvml.nvmlDeviceGetHandleByPciBusId(self.pci.encode())
+            except Exception:
                 self.h = pynvml.nvmlDeviceGetHandleByIndex(device_index)
             self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
-        except Exception as e:  # NVML missing: report no clocks rather than guess
-            self.nv = None
-            self.err = str(e)
+            self.nv = pynvml
+        except Exception as e:  # NVML missing: fall back to nvidia-smi
+            self.err = "%s: %s" % (type(e).__name__, e)
 
     def _run(self):
         while not self._stop.is_set():
@@ -127,7 +124,7 @@ class ClockSampler:
 
     def summary(self):
         if self.nv is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "note": "NVML unavailable"}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "note": "NVML unavailable: %s" % self.err}
         return {"sm_mhz": statistics.median(self.samples) if self.samples else None,
                 "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons - {"gpu_idle"}),
                 "samples": len(self.samples)}

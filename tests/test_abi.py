@@ -84,9 +84,9 @@ def _args(wl, dev="cuda"):
     return x, y, MT, ST
 
 
-def _call(mem, B, H, T, x, y, MT, ST, **over):
+def _call(mem, B, H, T, x, yo, MTo, STo, **over):
     p = dict(q=x["q"], k=x["k"], v=x["v"], alpha=x["alpha"], eta=x["eta"], beta=x["beta"], c=None,
-             M0=x["M0"], S0=x["S0"], y=y, M_T=MT, S_T=ST)
+             M0=x["M0"], S0=x["S0"], y=yo, M_T=MTo, S_T=STo)
     p.update(over)
 
     def ptr(t):
