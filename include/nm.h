@@ -45,6 +45,7 @@ extern "C" {
 #define NM_ERR_NOMEM           6  /* host or device allocation failed          */
 #define NM_ERR_DEVICE_TIMEOUT  7  /* a bounded on-device wait gave up          */
 #define NM_ERR_DEVICE_CHECK    8  /* an on-device consistency check failed     */
+#define NM_ERR_TOO_LARGE       9  /* call needs more than the fixed no-alloc workspace */
 
 /* ---- configuration enums ------------------------------------------------ */
 #define NM_LINEAR 0
@@ -159,6 +160,38 @@ int nm_selected_path(nm_handle_t h);
  *   (monotonic; used to count launches inside a timed region).
  */
 long long nm_launch_count(nm_handle_t h);
+
+/*
+ * nm_forward_mlp2_noalloc - the MLP2 forward without any allocation.
+ *   The paper has no counterpart to this entry point; it exists for callers
+ *   that cannot call cudaMalloc when they run the layer: a host that has
+ *   reserved the whole device for its own memory pool (a side allocation
+ *   would fail or fragment it), or a latency-critical loop that cannot
+ *   afford cudaMalloc's implicit device-wide synchronisation.  It needs no
+ *   handle (nm_create allocates) and calls no cudaMalloc, cudaFree or
+ *   allocating library routine.
+ *   Arguments, layouts, aliasing rules and host-side errors are those of
+ *   nm_forward, with the configuration passed directly; cfg->kind must be
+ *   NM_MLP2 and cfg->path NM_PATH_AUTO or NM_PATH_SIMT (the fp32 FFMA
+ *   kernel runs).  The work runs on the CURRENT device, on `stream`.
+ *   Workspace: one file-scope device array of NM_NOALLOC_SCRATCH_BYTES,
+ *   present on every GPU that loads this library until the process exits.
+ *   A call needing more than that (B*H units of
+ *   4*(2b^2 + 2b + 4bd + 4bh) bytes each) returns NM_ERR_TOO_LARGE with
+ *   nothing launched.  The first call on a device looks up the array's device
+ *   address (cudaGetSymbolAddress, with that device current); make that first
+ *   call before any stream capture.  Every call shares the array, which keeps
+ *   the previous call's contents (the kernel writes each workspace element
+ *   before reading it, so nothing needs clearing); calls whose kernels overlap
+ *   on the GPU race on it, so the caller must order them.  Bounded-wait
+ *   status is not reported (this kernel has no waits).
+ */
+#define NM_NOALLOC_SCRATCH_BYTES (16u << 20)
+int nm_forward_mlp2_noalloc(const nm_config* cfg, int B, int H, int T,
+                            const void* q, const void* k, const void* v,
+                            const float* alpha, const float* eta, const float* beta,
+                            const float* c, const float* M0, const float* S0,
+                            void* y, float* M_T, float* S_T, void* stream);
 
 #ifdef __cplusplus
 }

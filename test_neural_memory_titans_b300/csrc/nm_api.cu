@@ -87,6 +87,7 @@ const char* nm_status_string(int s) {
         case NM_ERR_NOMEM: return "allocation failed";
         case NM_ERR_DEVICE_TIMEOUT: return "a bounded on-device wait gave up";
         case NM_ERR_DEVICE_CHECK: return "an on-device consistency check failed";
+        case NM_ERR_TOO_LARGE: return "call needs more workspace than the fixed no-alloc array holds";
         default: return "unknown status";
     }
 }
