@@ -1,9 +1,11 @@
-// tcgen05 tensor-core kernels: dispatch.  (Kernels land in later files.)
+// Dispatch to the tcgen05 tensor-core kernels.
 #include "nm_internal.h"
 
+bool nm_tc_linear_supports(const nm_config& c);
+cudaError_t nm_tc_linear_launch(const nm_config& c, const nm_args& a, cudaStream_t s);
+
 bool nm_tc_supports(const nm_config& c) {
-    (void)c;
-    return false;
+    return nm_tc_linear_supports(c);
 }
 
 size_t nm_tc_scratch_bytes(const nm_config& c, int B, int H) {
@@ -12,6 +14,9 @@ size_t nm_tc_scratch_bytes(const nm_config& c, int B, int H) {
 }
 
 cudaError_t nm_tc_launch(const nm_config& c, const nm_args& a, cudaStream_t s, int num_sms, long long* launches) {
-    (void)c; (void)a; (void)s; (void)num_sms; (void)launches;
-    return cudaErrorNotSupported;
+    (void)num_sms;
+    cudaError_t e = cudaErrorNotSupported;
+    if (nm_tc_linear_supports(c)) e = nm_tc_linear_launch(c, a, s);
+    if (e == cudaSuccess) *launches += 1;
+    return e;
 }
