@@ -70,11 +70,16 @@ def load_peaks():
 # --------------------------------------------------------------------- clocks
 
 class ClockSampler:
-    """Samples SM clock and throttle reasons through NVML while running."""
+    """Samples the SM clock and the clock-event (throttle) reasons while the
+    timed region runs: through NVML when pynvml imports, else by running
+    ``nvidia-smi --query-gpu=... -lms 100`` for the device in a subprocess."""
 
     REASONS = {0x8: "hw_slowdown", 0x40: "hw_thermal_slowdown", 0x20: "sw_thermal_slowdown",
                0x4: "sw_power_cap", 0x80: "hw_power_brake_slowdown", 0x1: "gpu_idle",
                0x2: "applications_clocks_setting", 0x100: "sync_boost", 0x10: "display_clock_setting"}
+    SMI_FIELDS = ("clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.hw_slowdown",
+                  "clocks_event_reasons.hw_thermal_slowdown", "clocks_event_reasons.sw_thermal_slowdown",
+                  "clocks_event_reasons.sw_power_cap")
 
     def __init__(self, device_index: int, period_s: float = 0.01):
         self.samples = []
@@ -82,8 +87,10 @@ class ClockSampler:
         self.max_mhz = None
         self.period = period_s
         self.err = None
+        self.source = None
         self._stop = threading.Event()
         self._t = None
+        self._proc = None
         self.nv = None
         props = torch.cuda.get_device_properties(device_index)
         self.pci = "%08x:%02x:%02x.0" % (props.pci_domain_id, props.pci_bus_id, props.pci_device_id)
@@ -96,7 +103,8 @@ class ClockSampler:
                 self.h = pynvml.nvmlDeviceGetHandleByIndex(device_index)
             self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
             self.nv = pynvml
-        except Exception as e:  # NVML missing: fall back to nvidia-smi
+            self.source = "nvml"
+        except Exception as e:
             self.err = "%s: %s" % (type(e).__name__, e)
 
     def _run(self):
@@ -115,19 +123,48 @@ class ClockSampler:
         if self.nv is not None:
             self._t = threading.Thread(target=self._run, daemon=True)
             self._t.start()
+        else:
+            import shutil
+            import subprocess
+            smi = shutil.which("nvidia-smi")
+            if smi:
+                self._proc = subprocess.Popen(
+                    [smi, "-i", self.pci, "--query-gpu=" + ",".join(self.SMI_FIELDS), "--format=csv,noheader,nounits",
+                     "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                self.source = "nvidia-smi"
+                time.sleep(0.3)  # let the first sample land before the timed work starts
+            else:
+                self.err = (self.err or "") + "; nvidia-smi not found"
         return self
 
     def __exit__(self, *exc):
         self._stop.set()
         if self._t is not None:
             self._t.join()
+        if self._proc is not None:
+            self._proc.terminate()
+            out, _ = self._proc.communicate(timeout=10)
+            names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+            for line in out.splitlines():
+                f = [s.strip() for s in line.split(",")]
+                if len(f) != len(self.SMI_FIELDS):
+                    continue
+                try:
+                    self.samples.append(float(f[0]))
+                    self.max_mhz = float(f[1])
+                except ValueError:
+                    continue
+                for name, val in zip(names, f[3:]):
+                    if val.lower() == "active":
+                        self.reasons.add(name)
 
     def summary(self):
-        if self.nv is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "note": "NVML unavailable: %s" % self.err}
-        return {"sm_mhz": statistics.median(self.samples) if self.samples else None,
-                "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons - {"gpu_idle"}),
-                "samples": len(self.samples)}
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons),
+                    "note": "no clock samples (%s)" % (self.err or self.source)}
+        return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(self.reasons - {"gpu_idle"}), "samples": len(self.samples),
+                "source": self.source}
 
 
 # --------------------------------------------------------------------- oracle timing
@@ -170,13 +207,28 @@ def time_oracle(wl, x, budget_s: float = 12.0):
 
 # --------------------------------------------------------------------- our arm
 
+def workload(args):
+    """The selected workload, with --B / --H / --T overrides applied (a
+    streamed workload overridden to T below one segment runs as one call)."""
+    from test_neural_memory_titans_b300 import workloads as W
+
+    wl = W.WORKLOADS[args.workload]
+    if args.B is None and args.H is None and args.T is None:
+        return wl
+    wl = wl.with_sizes(B=args.B, H=args.H, T=args.T)
+    if wl.segment and (wl.T % wl.segment or wl.T < wl.segment):
+        wl = wl.with_sizes(segment=0)
+    import dataclasses
+    return dataclasses.replace(wl, name="%s@B%dH%dT%d" % (wl.name, wl.B, wl.H, wl.T))
+
+
 def run_ours(args, rank, world, local_rank):
     import test_neural_memory_titans_b300 as nm
     from test_neural_memory_titans_b300 import workloads as W
 
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
-    wl = W.WORKLOADS[args.workload]
+    wl = workload(args)
     x = W.make_inputs(wl, dev, seed=1000 + args.workload + 100 * rank)
     mem = nm.NeuralMemory(wl.kind, wl.d, wl.hidden, wl.chunk, in_dtype=wl.dtype, path=args.path, device=local_rank)
     stream = torch.cuda.current_stream(dev)
@@ -306,7 +358,7 @@ def run_reference(args, rank, world):
         return None
     from test_neural_memory_titans_b300 import workloads as W
 
-    wl = W.WORKLOADS[args.workload]
+    wl = workload(args)
     x = W.make_inputs(wl, "cpu", seed=1000 + args.workload)
     budget = max(1.0, 150.0 / max(1, args.steps + args.warmup))
     for _ in range(args.warmup):
@@ -338,6 +390,9 @@ def main():
                     help="DRAM bytes per launch of the dominant kernel from an ncu capture")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--B", type=int, default=None, help="override the workload's batch (small profiling cases)")
+    ap.add_argument("--H", type=int, default=None, help="override the workload's heads")
+    ap.add_argument("--T", type=int, default=None, help="override the workload's tokens per unit")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3

@@ -73,18 +73,6 @@ __device__ __forceinline__ void store_y<__nv_bfloat16>(__nv_bfloat16* p, float x
 template <>
 __device__ __forceinline__ void store_y<float>(float* p, float x) { *p = x; }
 
-// Writes 32 fp32 values (columns c0..c0+31 of row r) as bf16 into a
-// 128-byte-swizzled tile with `rows` rows.
-__device__ __forceinline__ void put_row32(unsigned char* tile, uint32_t rows, uint32_t r, uint32_t c0, const float* v) {
-    const uint32_t base = smem_u32(tile);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        const uint32_t off = sw128_offset(r, c0 + 8 * q, rows);
-        st_shared_v4(base + off, pack_bf16(v[8 * q], v[8 * q + 1]), pack_bf16(v[8 * q + 2], v[8 * q + 3]),
-                     pack_bf16(v[8 * q + 4], v[8 * q + 5]), pack_bf16(v[8 * q + 6], v[8 * q + 7]));
-    }
-}
-
 __device__ __forceinline__ float momentum_c(int mode, float beta, const float* c, long long i) {
     if (mode == NM_C_ONE_MINUS_BETA) return 1.0f - beta;
     if (mode == NM_C_PER_TOKEN) return c[i];
@@ -410,37 +398,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (warp == 0) tmem_dealloc(tm, 512);
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 get_encoder() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (!fn) {
-        cudaDriverEntryPointQueryResult q;
-        void* p = nullptr;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    }
-    return fn;
-}
-
-// [units][T][d] bf16 viewed as a 3-D tensor; 64 x 64 boxes, 128-byte swizzle.
-// Tokens past T read as zero.
-bool make_map(CUtensorMap* m, const void* base, int d, long long T, long long units) {
-    auto enc = get_encoder();
-    if (!enc) return false;
-    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)T, (cuuint64_t)units};
-    cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)T * d * 2};
-    cuuint32_t box[3] = {64, 64, 1};
-    cuuint32_t es[3] = {1, 1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <typename Tout>
 cudaError_t launch(const nm_config& c, const nm_args& a, cudaStream_t s) {
     CUtensorMap tq, tk, tv;
     const long long units = (long long)a.B * a.H;
-    if (!make_map(&tq, a.q, D, a.T, units) || !make_map(&tk, a.k, D, a.T, units) || !make_map(&tv, a.v, D, a.T, units))
+    if (!make_token_map(&tq, a.q, D, a.T, units) || !make_token_map(&tk, a.k, D, a.T, units) ||
+        !make_token_map(&tv, a.v, D, a.T, units))
         return cudaErrorInvalidValue;
     auto kern = tc_linear_kernel<Tout>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
