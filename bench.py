@@ -130,7 +130,7 @@ class ClockSampler:
             if smi:
                 self._proc = subprocess.Popen(
                     [smi, "-i", self.pci, "--query-gpu=" + ",".join(self.SMI_FIELDS), "--format=csv,noheader,nounits",
-                     "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                     "-lms", "20"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
                 self.source = "nvidia-smi"
                 time.sleep(0.3)  # let the first sample land before the timed work starts
             else:
@@ -381,7 +381,7 @@ def run_reference(args, rank, world):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--workload", type=int, default=DEFAULT_WORKLOAD, choices=[0, 1, 2, 3, 4])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])

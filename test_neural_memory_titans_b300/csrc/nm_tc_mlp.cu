@@ -1,0 +1,655 @@
+// tcgen05 tensor-core kernel for the 2-layer SiLU MLP memory
+// M(x) = W2 silu(W1 x), d = 64, hidden h = 128 * NC, chunk b = 64.
+//
+// Method ("Titans: Imparare a Memorizzare al Tempo di Test", sections
+// "Meccanismo di Aggiornamento della Memoria", "Meccanismo di Dimenticanza",
+// "Funzione Obiettivo", "Addestramento Parallelizzato"; the 0h-n0.github.io
+// explainer, "ニューラル長期メモリモジュール" and "メモリ読み出し"): inside a chunk
+// every token takes its gradient at the chunk-start weights W0, and with
+// a_t = 1 - alpha_t,
+//   A_t = prod_{j<=t} a_j,  B_t = prod_{j<=t} beta_j,
+//   sigma_t = a_t sigma_{t-1} + eta_t B_t,
+//   Gamma_{t,i} = a_t Gamma_{t-1,i} + eta_t u_{t,i},  u_{t,i} = c_i prod_{l=i+1..t} beta_l,
+// the weights after token t are W_t = A_t W0 - sigma_t S0 - sum_{i<=t} Gamma_{t,i} g_i
+// and the momentum S_t = B_t S0 + sum_{i<=t} u_{t,i} g_i.  For this memory
+//   z_i = W1 k_i, a(k_i) = silu(z_i), e_i = 2 (W2 a(k_i) - v_i),
+//   delta_i = (W2^T e_i) (.) silu'(z_i),  g_i = (delta_i k_i^T, e_i a(k_i)^T),
+// so retrieval after token t is
+//   h_t = A_t W1 q_t - sigma_t S1 q_t - sum_i Gamma_{t,i} (k_i . q_t) delta_i,
+//   y_t = A_t W2 a_t - sigma_t S2 a_t - sum_i Gamma_{t,i} (a(k_i) . a_t) e_i,  a_t = silu(h_t),
+// and the chunk-end state is W_end = A_n W0 - sigma_n S0 - sum_i gamma_i g_i,
+// S_end = B_n S0 + sum_i u_i g_i with gamma_i = Gamma_{n-1,i}, u_i = u_{n-1,i}.
+//
+// Work split: a cluster of NC CTAs per (batch, head) unit, CTA r owning the
+// hidden units j in [128 r, 128 r + 128): its rows of W1 and S1 and its
+// columns of W2 and S2 (kept transposed, [j][o]).  Everything indexed by j is
+// local; the two sums over j are exchanged through distributed shared memory:
+//   * the key forward W2 a(k_i): each CTA adds its slice's partial sum to the
+//     peer's (all-reduce), then both form e_i;
+//   * the retrieval y_t: each CTA's partial (its slice of W2 a_t, S2 a_t and
+//     of (a(k_i) . a_t)) is reduced onto the CTA that owns those output
+//     columns, which writes y.
+//
+// Per CTA (256 threads; thread 0 issues TMA and MMA):
+//   TMEM, 128 lanes x 512 fp32 columns; lane = j for M=128 products, row t at
+//   lane (t % 16) + 32 (t / 16) for M=64 products:
+//     0..63 W1 [j][x], 64..127 S1 [j][x], 128..191 W2^T [j][o], 192..255 S2^T
+//     (the fp32 state, resident for the whole sequence), 256..511 per-chunk
+//     accumulators reused phase by phase (see COL_* below).
+//   SMEM: the chunk's Q|K tile and V tile (TMA, 128-byte swizzle), bf16
+//     copies of the state as tensor-core operands, the chunk's intermediates
+//     as bf16 operand tiles, Gamma in fp32, exchange buffers for the peer.
+// Per chunk: G1 W1 [q|k], S1 q, Q K^T -> Z, a(k), P1 = Gamma (.) QK^T ->
+// G2 partial yhat -> exchange -> E -> G3 W2^T e -> delta -> G4 state update
+// and sum_i P1 delta_i -> h, a_t -> G5 W2 a_t | S2 a_t, a_t . a(k_i) -> P2 ->
+// G6 P2 E -> y partials -> exchange -> y.  Then the new state becomes the
+// next chunk's bf16 operands.
+#include <cuda_bf16.h>
+
+#include "nm_internal.h"
+#include "tc_common.cuh"
+
+namespace {
+
+using namespace tc;
+
+constexpr int D = 64;         // key / value width
+constexpr int HS = 128;       // hidden units per CTA
+constexpr int BC = 64;        // chunk size
+constexpr int NTHREADS = 256;
+constexpr uint32_t T64 = 64 * 128;    // [64 rows][64 bf16] swizzled tile
+constexpr uint32_t T128 = 128 * 128;  // [128 rows][64 bf16]
+
+constexpr uint32_t OFF_QK = 0;                // [128][64]: q rows 0..63, k rows 64..127 (TMA)
+constexpr uint32_t OFF_V = OFF_QK + T128;     // [64 t][64 o] (TMA)
+constexpr uint32_t OFF_W1 = OFF_V + T64;      // [128 j][64 x]  bf16 copy of W1 (this CTA's rows)
+constexpr uint32_t OFF_S1 = OFF_W1 + T128;    // [128 j][64 x]
+constexpr uint32_t OFF_W2 = OFF_S1 + T128;    // [128 j][64 o]  W2 transposed
+constexpr uint32_t OFF_S2 = OFF_W2 + T128;    // [128 j][64 o]  (follows W2: one N=128 operand)
+constexpr uint32_t OFF_AK = OFF_S2 + T128;    // [128 j][64 t]  a(k_t)
+constexpr uint32_t OFF_DT = OFF_AK + T128;    // [128 j][64 t]  delta_t, later a_t (retrieval)
+constexpr uint32_t OFF_KG = OFF_DT + T128;    // [64 t][64 x]   -gamma_t k_t
+constexpr uint32_t OFF_KU = OFF_KG + T64;     // [64 t][64 x]   u_t k_t
+constexpr uint32_t OFF_E = OFF_KU + T64;      // [64 t][64 o]   e_t
+constexpr uint32_t OFF_EG = OFF_E + T64;      // -gamma_t e_t
+constexpr uint32_t OFF_EU = OFF_EG + T64;     // u_t e_t
+constexpr uint32_t OFF_P = OFF_EU + T64;      // [64 t][64 i]   Gamma (.) inner products
+constexpr int GS = 68;                        // padded fp32 row stride (conflict-free row reads)
+constexpr int RS = 36;
+constexpr uint32_t OFF_GM = OFF_P + T64;                // fp32 Gamma [64][GS]
+constexpr uint32_t OFF_YX = OFF_GM + 64 * GS * 4;       // fp32 [64][GS] the peer's partial key forward
+constexpr uint32_t OFF_YR = OFF_YX + 64 * GS * 4;       // fp32 [64][RS] the peer's partial y (own columns)
+constexpr uint32_t OFF_F = OFF_YR + 64 * RS * 4;        // gates [2][4][64], A, B, sigma, gamma, u
+constexpr uint32_t N_F = 2 * 4 * BC + 5 * BC;
+constexpr uint32_t OFF_BAR = OFF_F + 4 * N_F;
+constexpr uint32_t SMEM_USED = OFF_BAR + 64;
+constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;  // slack for the 1024-byte alignment
+static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+static_assert(OFF_S2 == OFF_W2 + T128, "W2 and S2 copies form one N=128 operand");
+
+// TMEM columns
+constexpr uint32_t COL_W1 = 0, COL_S1 = 64, COL_W2 = 128, COL_S2 = 192;
+constexpr uint32_t COL_XA = 256;  // G1: [j][t] W1 q_t (256..319), W1 k_t = z_t (320..383)
+constexpr uint32_t COL_Z = 320;
+constexpr uint32_t COL_XB = 384;  // G1: [j][t] S1 q_t
+constexpr uint32_t COL_QK = 448;  // G1: lanes 0..63 [t][i] q_t . k_i
+constexpr uint32_t COL_YH = 320;  // G2: M=64 [t][o] partial W2 a(k_t)
+constexpr uint32_t COL_XD = 320;  // G3: [j][t] W2^T e_t
+constexpr uint32_t COL_R1 = 320;  // G4: [j][t] sum_i P1[t][i] delta_i
+constexpr uint32_t COL_YW = 256;  // G5: M=64 [t][o] W2 a_t (256..319), S2 a_t (320..383)
+constexpr uint32_t COL_AA = 384;  // G5: M=64 [t][i] a_t . a(k_i)
+constexpr uint32_t COL_PE = 448;  // G6: M=64 [t][o] sum_i P2[t][i] e_i
+
+constexpr uint32_t ID_XA = idesc_bf16_f32(128, 128, false, false);
+constexpr uint32_t ID_M128N64 = idesc_bf16_f32(128, 64, false, false);
+constexpr uint32_t ID_UPD = idesc_bf16_f32(128, 64, false, true);
+constexpr uint32_t ID_M64N64_TT = idesc_bf16_f32(64, 64, true, true);
+constexpr uint32_t ID_M64N128_TT = idesc_bf16_f32(64, 128, true, true);
+constexpr uint32_t ID_M64N64_BT = idesc_bf16_f32(64, 64, false, true);
+constexpr uint64_t WAIT_NS = 2000000000ull;  // 2 s
+
+__device__ __forceinline__ uint64_t kdesc(uint32_t a) { return sw128_desc(a, 16, 1024); }
+__device__ __forceinline__ uint64_t mdesc(uint32_t a, uint32_t lbo) { return sw128_desc(a, lbo, 1024); }
+
+// sigmoid with the fast exponential and reciprocal; z is clamped below at
+// -80 so that 1 + e^{-z} stays finite (silu and its derivative are 0 to
+// within fp32 there)
+__device__ __forceinline__ float sigmoid_f(float z) { return __fdividef(1.0f, 1.0f + __expf(-fmaxf(z, -80.0f))); }
+__device__ __forceinline__ float silu_f(float z) { return z * sigmoid_f(z); }
+
+__device__ __forceinline__ float momentum_c(int mode, float beta, const float* c, long long i) {
+    if (mode == NM_C_ONE_MINUS_BETA) return 1.0f - beta;
+    if (mode == NM_C_PER_TOKEN) return c[i];
+    return 1.0f;
+}
+
+// 32 bf16 of row r, columns c0..c0+31, of a swizzled tile, as floats.
+__device__ __forceinline__ void get_row32(const unsigned char* tile, uint32_t rows, uint32_t r, uint32_t c0, float* v) {
+    const uint32_t base = smem_u32(tile);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const uint4 w = ld_shared_v4(base + sw128_offset(r, c0 + 8 * q, rows));
+        v[8 * q + 0] = bf16_lo(w.x); v[8 * q + 1] = bf16_hi(w.x);
+        v[8 * q + 2] = bf16_lo(w.y); v[8 * q + 3] = bf16_hi(w.y);
+        v[8 * q + 4] = bf16_lo(w.z); v[8 * q + 5] = bf16_hi(w.z);
+        v[8 * q + 6] = bf16_lo(w.w); v[8 * q + 7] = bf16_hi(w.w);
+    }
+}
+
+template <typename Tout>
+__device__ __forceinline__ void store_y32(Tout* p, const float* v);
+template <>
+__device__ __forceinline__ void store_y32<__nv_bfloat16>(__nv_bfloat16* p, const float* v) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+        reinterpret_cast<uint4*>(p)[q] = make_uint4(pack_bf16(v[8 * q], v[8 * q + 1]), pack_bf16(v[8 * q + 2], v[8 * q + 3]),
+                                                    pack_bf16(v[8 * q + 4], v[8 * q + 5]), pack_bf16(v[8 * q + 6], v[8 * q + 7]));
+}
+template <>
+__device__ __forceinline__ void store_y32<float>(float* p, const float* v) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+        reinterpret_cast<float4*>(p)[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+}
+
+template <int NC, typename Tout>
+__global__ void __launch_bounds__(NTHREADS, 1)
+    tc_mlp_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                  const __grid_constant__ CUtensorMap tv, nm_args a, int c_mode) {
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    float* gates = reinterpret_cast<float*>(sm + OFF_F);  // [2 stages][a, eta, beta, c][64]
+    float* sA = gates + 2 * 4 * BC;
+    float* sBc = sA + BC;
+    float* sSg = sBc + BC;
+    float* sGl = sSg + BC;
+    float* sU = sGl + BC;
+    float* Gm = reinterpret_cast<float*>(sm + OFF_GM);
+    float* Yx = reinterpret_cast<float*>(sm + OFF_YX);
+    float* Yr = reinterpret_cast<float*>(sm + OFF_YR);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + OFF_BAR);  // 0: tiles, 1: mma
+    __shared__ uint32_t s_tmem;
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    const int qd = warp & 3;   // TMEM lane quadrant of this warp
+    const int hf = warp >> 2;  // which 32 of a 64-column accumulator this thread reads
+    const int rank = NC > 1 ? (int)cluster_ctarank() : 0;
+    const long long unit = blockIdx.x / NC;
+    const long long T = a.T;
+    const int hid = HS * NC;
+    const long long P = 2LL * hid * D;
+    const int nchunks = (int)((T + BC - 1) / BC);
+    const float* alpha = a.alpha + unit * T;
+    const float* eta = a.eta + unit * T;
+    const float* beta = a.beta + unit * T;
+    const float* cc = a.c ? a.c + unit * T : nullptr;
+    Tout* y = reinterpret_cast<Tout*>(a.y) + unit * T * D;
+    const int jr = 32 * qd + lane;           // row of an M=128 accumulator
+    const int tr = 16 * qd + lane;           // row of an M=64 accumulator (valid for lane < 16)
+    const bool r64 = lane < 16;
+    const int j_glob = HS * rank + jr;       // hidden unit of row jr
+
+    if (tid == 0) {
+        mbar_init(&bars[0], 1);
+        mbar_init(&bars[1], 1);
+        fence_mbar_init();
+        prefetch_tmap(&tq);
+        prefetch_tmap(&tk);
+        prefetch_tmap(&tv);
+    }
+    if (warp == 0) {
+        tmem_alloc(&s_tmem, 512);
+        tmem_relinquish();
+    }
+    auto load_gates = [&](int chunk, int stage) {
+        if (tid < BC) {
+            const long long t = (long long)chunk * BC + tid;
+            float* g = gates + stage * 4 * BC;
+            if (t < T) {
+                const float b = beta[t];
+                g[tid] = 1.0f - alpha[t];
+                g[BC + tid] = eta[t];
+                g[2 * BC + tid] = b;
+                g[3 * BC + tid] = momentum_c(c_mode, b, cc, t);
+            } else {  // tokens past T change nothing: a = 1, eta = 0, beta = 1, c = 0
+                g[tid] = 1.0f;
+                g[BC + tid] = 0.0f;
+                g[2 * BC + tid] = 1.0f;
+                g[3 * BC + tid] = 0.0f;
+            }
+        }
+    };
+    auto issue_tiles = [&](int chunk) {
+        mbar_arrive_expect_tx(&bars[0], 3 * T64);
+        const int t0 = chunk * BC;
+        tma_load_3d(sm + OFF_QK, &tq, &bars[0], 0, t0, (int)unit);
+        tma_load_3d(sm + OFF_QK + T64, &tk, &bars[0], 0, t0, (int)unit);
+        tma_load_3d(sm + OFF_V, &tv, &bars[0], 0, t0, (int)unit);
+    };
+
+    load_gates(0, 0);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tm = s_tmem;
+    const uint32_t tl = tm + ((uint32_t)(32 * qd) << 16);  // this warp's lane quadrant
+    if (tid == 0 && nchunks > 0) issue_tiles(0);
+
+    // initial state: fp32 into TMEM, bf16 operand copies into shared memory
+    {
+        const float* m0 = a.M0 + unit * P;
+        const float* s0 = a.S0 + unit * P;
+        float r[32];
+#pragma unroll
+        for (int which = 0; which < 2; ++which) {
+            const float* src = which ? s0 : m0;
+            // W1 (or S1) row j_glob, columns 32 hf .. 32 hf + 31
+            const float* w1 = src + (long long)j_glob * D + 32 * hf;
+#pragma unroll
+            for (int q = 0; q < 32; q += 4) {
+                const float4 w = *reinterpret_cast<const float4*>(w1 + q);
+                r[q] = w.x; r[q + 1] = w.y; r[q + 2] = w.z; r[q + 3] = w.w;
+            }
+            tmem_st32(tl + (which ? COL_S1 : COL_W1) + 32 * hf, r);
+            put_row32(sm + (which ? OFF_S1 : OFF_W1), 128, jr, 32 * hf, r);
+            // W2 (or S2) transposed: [j][o] = W2[o][j_glob], o = 32 hf + q
+            const float* w2 = src + (long long)hid * D + j_glob;
+#pragma unroll
+            for (int q = 0; q < 32; ++q) r[q] = w2[(long long)(32 * hf + q) * hid];
+            tmem_st32(tl + (which ? COL_S2 : COL_W2) + 32 * hf, r);
+            put_row32(sm + (which ? OFF_S2 : OFF_W2), 128, jr, 32 * hf, r);
+        }
+    }
+    fence_proxy_async();
+    tc_fence_before();
+    if (NC > 1) cluster_sync(); else __syncthreads();
+    tc_fence_after();
+
+    const uint32_t aQK = smem_u32(sm + OFF_QK), aW1 = smem_u32(sm + OFF_W1), aS1 = smem_u32(sm + OFF_S1);
+    const uint32_t aW2 = smem_u32(sm + OFF_W2), aAK = smem_u32(sm + OFF_AK), aDT = smem_u32(sm + OFF_DT);
+    const uint32_t aKG = smem_u32(sm + OFF_KG), aKU = smem_u32(sm + OFF_KU), aE = smem_u32(sm + OFF_E);
+    const uint32_t aEG = smem_u32(sm + OFF_EG), aEU = smem_u32(sm + OFF_EU), aP = smem_u32(sm + OFF_P);
+    const int peer = rank ^ 1;
+
+    bool failed = false;
+    uint32_t mma_phase = 0;
+    // Waits (bounded) for the MMAs committed by thread 0; uniform over the CTA.
+    auto mma_wait = [&](bool committed) {
+        bool ok = true;
+        if (committed) {
+            ok = mbar_wait(&bars[1], mma_phase, WAIT_NS);
+            mma_phase ^= 1u;
+        }
+        failed = __syncthreads_or(!ok) || failed;
+        tc_fence_after();
+    };
+    auto handoff = [&]() {  // epilogue smem / TMEM writes -> tensor-core reads
+        fence_proxy_async();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+    };
+
+    float ds[32];  // silu'(z) for this thread's row and columns, kept from E1 to E3
+    for (int c = 0; c < nchunks; ++c) {
+        const int stage = c & 1;
+        const long long t0 = (long long)c * BC;
+        const int n = (int)min((long long)BC, T - t0);
+        const float* g = gates + stage * 4 * BC;
+
+        // ---- G1 (thread 0, as soon as the tiles land): W1 [q|k], S1 q, Q K^T;
+        //      meanwhile the scan of the chunk's gates: Gamma (by columns), gamma, u; A, B, sigma
+        bool tiles_ok = true;
+        if (tid == 0 && !failed) {
+            tiles_ok = mbar_wait(&bars[0], (uint32_t)(c & 1), WAIT_NS);
+            if (tiles_ok) {
+                tc_fence_after();
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks) {
+                    const uint32_t acc = ks ? 1u : 0u;
+                    mma_bf16(tm + COL_XA, kdesc(aW1 + 32 * ks), kdesc(aQK + 32 * ks), ID_XA, acc);
+                    mma_bf16(tm + COL_XB, kdesc(aS1 + 32 * ks), kdesc(aQK + 32 * ks), ID_M128N64, acc);
+                    mma_bf16(tm + COL_QK, kdesc(aQK + 32 * ks), kdesc(aQK + T64 + 32 * ks), ID_M128N64, acc);
+                }
+                mma_commit(&bars[1]);
+            }
+        }
+        if (tid >= 128 && tid < 128 + BC) {
+            const int i = tid - 128;
+            float u = g[3 * BC + i];
+            float G = g[BC + i] * u;
+            for (int t = 0; t < i; ++t) Gm[t * GS + i] = 0.0f;
+            Gm[i * GS + i] = G;
+            for (int t = i + 1; t < BC; ++t) {
+                u *= g[2 * BC + t];
+                G = fmaf(g[t], G, g[BC + t] * u);
+                Gm[t * GS + i] = G;
+            }
+            sGl[i] = G;
+            sU[i] = u;
+        } else if (tid == 224) {
+            float A = 1.f, Bc = 1.f, sg = 0.f;
+            for (int t = 0; t < BC; ++t) {
+                A *= g[t];
+                Bc *= g[2 * BC + t];
+                sg = fmaf(g[t], sg, g[BC + t] * Bc);
+                sA[t] = A;
+                sBc[t] = Bc;
+                sSg[t] = sg;
+            }
+        }
+        // the tiles (waited for by thread 0) and the scan are visible to all after this
+        const bool go1 = !failed && !__syncthreads_or(!tiles_ok);
+        if (!go1 && !failed) failed = true;
+        // -gamma_t k_t and u_t k_t as bf16 operand rows (while G1 runs)
+        if (tid < BC) {
+            float kv[32], o1[32], o2[32];
+            const float gm = -sGl[tid], uu = sU[tid];
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+                get_row32(sm + OFF_QK, 128, 64 + tid, 32 * h2, kv);
+#pragma unroll
+                for (int q = 0; q < 32; ++q) {
+                    o1[q] = gm * kv[q];
+                    o2[q] = uu * kv[q];
+                }
+                put_row32(sm + OFF_KG, 64, tid, 32 * h2, o1);
+                put_row32(sm + OFF_KU, 64, tid, 32 * h2, o2);
+            }
+        }
+        // rescale the fp32 state for this chunk: W <- A_n W - sigma_n S, S <- B_n S
+        {
+            const float An = sA[BC - 1], Bn = sBc[BC - 1], sn = sSg[BC - 1];
+            float w[32], s[32];
+#pragma unroll
+            for (int pr = 0; pr < 2; ++pr) {
+                const uint32_t cw = (pr ? COL_W2 : COL_W1) + 32 * hf, cs = (pr ? COL_S2 : COL_S1) + 32 * hf;
+                tmem_ld32_async(tl + cw, w);
+                tmem_ld32_async(tl + cs, s);
+                tmem_wait_ld();
+#pragma unroll
+                for (int q = 0; q < 32; ++q) {
+                    w[q] = fmaf(An, w[q], -sn * s[q]);
+                    s[q] = Bn * s[q];
+                }
+                tmem_st32(tl + cw, w);
+                tmem_st32(tl + cs, s);
+            }
+        }
+        mma_wait(go1);
+        // ---- E1: a(k) and silu'(z) from z = W1 k; P1 = Gamma (.) Q K^T
+        {
+            float z[32], p[32];
+            tmem_ld32_async(tl + COL_Z + 32 * hf, z);
+            if (qd < 2) tmem_ld32_async(tl + COL_QK + 32 * hf, p);
+            tmem_wait_ld();
+#pragma unroll
+            for (int q = 0; q < 32; ++q) {
+                const float sg = sigmoid_f(z[q]);
+                ds[q] = fmaf(z[q] * sg, 1.0f - sg, sg);  // silu'(z) = s + z s (1 - s)
+                z[q] *= sg;
+            }
+            put_row32(sm + OFF_AK, 128, jr, 32 * hf, z);
+            if (qd < 2) {
+                const float* gr = Gm + jr * GS + 32 * hf;
+#pragma unroll
+                for (int q = 0; q < 32; q += 4) {
+                    const float4 gg = *reinterpret_cast<const float4*>(gr + q);
+                    p[q] *= gg.x; p[q + 1] *= gg.y; p[q + 2] *= gg.z; p[q + 3] *= gg.w;
+                }
+                put_row32(sm + OFF_P, 64, jr, 32 * hf, p);
+            }
+        }
+        handoff();
+        // ---- G2: partial key forward yhat[t][o] = sum_{j in slice} a(k_t)_j W2[o][j]
+        const bool go2 = !failed;
+        if (go2 && tid == 0) {
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks)
+                mma_bf16(tm + COL_YH, mdesc(aAK + 2048 * ks, T128), mdesc(aW2 + 2048 * ks, T128), ID_M64N64_TT,
+                         ks ? 1u : 0u);
+            mma_commit(&bars[1]);
+        }
+        mma_wait(go2);
+        // ---- E2: all-reduce of the key forward over the cluster, e = 2 (yhat - v)
+        float ev[32];
+        {
+            tmem_ld32(tl + COL_YH + 32 * hf, ev);
+            if (r64) {
+                if (NC > 1) {
+                    const uint32_t dst = map_to_rank(smem_u32(Yx + tr * GS + 32 * hf), (uint32_t)peer);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        st_cluster_v4(dst + 16 * q, ev[4 * q], ev[4 * q + 1], ev[4 * q + 2], ev[4 * q + 3]);
+                }
+                float vv[32];
+                get_row32(sm + OFF_V, 64, tr, 32 * hf, vv);
+#pragma unroll
+                for (int q = 0; q < 32; ++q) ev[q] = 2.0f * (ev[q] - vv[q]);
+            }
+        }
+        if (NC > 1) cluster_sync();
+        if (r64) {
+            if (NC > 1) {
+                const float* yx = Yx + tr * GS + 32 * hf;
+#pragma unroll
+                for (int q = 0; q < 32; q += 4) {
+                    const float4 w = *reinterpret_cast<const float4*>(yx + q);
+                    ev[q] = fmaf(2.0f, w.x, ev[q]);
+                    ev[q + 1] = fmaf(2.0f, w.y, ev[q + 1]);
+                    ev[q + 2] = fmaf(2.0f, w.z, ev[q + 2]);
+                    ev[q + 3] = fmaf(2.0f, w.w, ev[q + 3]);
+                }
+            }
+            put_row32(sm + OFF_E, 64, tr, 32 * hf, ev);
+            float o1[32];
+            const float gm = -sGl[tr], uu = sU[tr];
+#pragma unroll
+            for (int q = 0; q < 32; ++q) o1[q] = gm * ev[q];
+            put_row32(sm + OFF_EG, 64, tr, 32 * hf, o1);
+#pragma unroll
+            for (int q = 0; q < 32; ++q) o1[q] = uu * ev[q];
+            put_row32(sm + OFF_EU, 64, tr, 32 * hf, o1);
+        }
+        if (c + 1 < nchunks) load_gates(c + 1, stage ^ 1);
+        handoff();
+        // ---- G3: W2^T e (the next chunk's tiles start loading: Q|K and V are free)
+        const bool go3 = !failed;
+        if (go3 && tid == 0) {
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+                mma_bf16(tm + COL_XD, kdesc(aW2 + 32 * ks), kdesc(aE + 32 * ks), ID_M128N64, ks ? 1u : 0u);
+            mma_commit(&bars[1]);
+            if (c + 1 < nchunks) issue_tiles(c + 1);
+        }
+        mma_wait(go3);
+        // ---- E3: delta = (W2^T e) (.) silu'(z)
+        {
+            float xd[32];
+            tmem_ld32(tl + COL_XD + 32 * hf, xd);
+#pragma unroll
+            for (int q = 0; q < 32; ++q) xd[q] *= ds[q];
+            put_row32(sm + OFF_DT, 128, jr, 32 * hf, xd);
+        }
+        handoff();
+        // ---- G4: state update and sum_i P1[t][i] delta_i
+        const bool go4 = !failed;
+        if (go4 && tid == 0) {
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
+                mma_bf16(tm + COL_W1, kdesc(aDT + 32 * ks), mdesc(aKG + 2048 * ks, T64), ID_UPD, 1u);
+                mma_bf16(tm + COL_S1, kdesc(aDT + 32 * ks), mdesc(aKU + 2048 * ks, T64), ID_UPD, 1u);
+                mma_bf16(tm + COL_W2, kdesc(aAK + 32 * ks), mdesc(aEG + 2048 * ks, T64), ID_UPD, 1u);
+                mma_bf16(tm + COL_S2, kdesc(aAK + 32 * ks), mdesc(aEU + 2048 * ks, T64), ID_UPD, 1u);
+                mma_bf16(tm + COL_R1, kdesc(aDT + 32 * ks), kdesc(aP + 32 * ks), ID_M128N64, ks ? 1u : 0u);
+            }
+            mma_commit(&bars[1]);
+        }
+        mma_wait(go4);
+        // ---- E4: h_t = A_t W1 q_t - sigma_t S1 q_t - sum_i P1[t][i] delta_i, a_t = silu(h_t)
+        {
+            float xa[32], xb[32], r1[32];
+            tmem_ld32_async(tl + COL_XA + 32 * hf, xa);
+            tmem_ld32_async(tl + COL_XB + 32 * hf, xb);
+            tmem_ld32_async(tl + COL_R1 + 32 * hf, r1);
+            tmem_wait_ld();
+#pragma unroll
+            for (int q = 0; q < 32; ++q) {
+                const int t = 32 * hf + q;
+                xa[q] = silu_f(fmaf(sA[t], xa[q], -fmaf(sSg[t], xb[q], r1[q])));
+            }
+            put_row32(sm + OFF_DT, 128, jr, 32 * hf, xa);
+        }
+        handoff();
+        // ---- G5: [W2 a_t | S2 a_t] and a_t . a(k_i), partial over this CTA's slice
+        const bool go5 = !failed;
+        if (go5 && tid == 0) {
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                const uint32_t acc = ks ? 1u : 0u;
+                mma_bf16(tm + COL_YW, mdesc(aDT + 2048 * ks, T128), mdesc(aW2 + 2048 * ks, T128), ID_M64N128_TT, acc);
+                mma_bf16(tm + COL_AA, mdesc(aDT + 2048 * ks, T128), mdesc(aAK + 2048 * ks, T128), ID_M64N64_TT, acc);
+            }
+            mma_commit(&bars[1]);
+        }
+        mma_wait(go5);
+        // ---- E5: P2 = Gamma (.) (a_t . a(k_i))
+        {
+            float p[32];
+            tmem_ld32(tl + COL_AA + 32 * hf, p);
+            if (r64) {
+                const float* gr = Gm + tr * GS + 32 * hf;
+#pragma unroll
+                for (int q = 0; q < 32; q += 4) {
+                    const float4 gg = *reinterpret_cast<const float4*>(gr + q);
+                    p[q] *= gg.x; p[q + 1] *= gg.y; p[q + 2] *= gg.z; p[q + 3] *= gg.w;
+                }
+                put_row32(sm + OFF_P, 64, tr, 32 * hf, p);
+            }
+        }
+        handoff();
+        // ---- G6: sum_i P2[t][i] e_i
+        const bool go6 = !failed;
+        if (go6 && tid == 0) {
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+                mma_bf16(tm + COL_PE, kdesc(aP + 32 * ks), mdesc(aE + 2048 * ks, T64), ID_M64N64_BT, ks ? 1u : 0u);
+            mma_commit(&bars[1]);
+        }
+        mma_wait(go6);
+        // ---- E6: partial y, reduced onto the CTA that owns the columns
+        {
+            float yw[32], ys[32], pe[32];
+            tmem_ld32_async(tl + COL_YW + 32 * hf, yw);
+            tmem_ld32_async(tl + COL_YW + 64 + 32 * hf, ys);
+            tmem_ld32_async(tl + COL_PE + 32 * hf, pe);
+            tmem_wait_ld();
+            const bool own = NC == 1 || hf == rank;
+            if (r64) {
+                const float At = sA[tr], st = sSg[tr];
+#pragma unroll
+                for (int q = 0; q < 32; ++q) yw[q] = fmaf(At, yw[q], -fmaf(st, ys[q], pe[q]));
+                if (!own) {
+                    const uint32_t dst = map_to_rank(smem_u32(Yr + tr * RS), (uint32_t)peer);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        st_cluster_v4(dst + 16 * q, yw[4 * q], yw[4 * q + 1], yw[4 * q + 2], yw[4 * q + 3]);
+                }
+            }
+            if (NC > 1) cluster_sync();
+            if (r64 && own && tr < n) {
+                if (NC > 1) {
+                    const float* yr = Yr + tr * RS;
+#pragma unroll
+                    for (int q = 0; q < 32; q += 4) {
+                        const float4 w = *reinterpret_cast<const float4*>(yr + q);
+                        yw[q] += w.x; yw[q + 1] += w.y; yw[q + 2] += w.z; yw[q + 3] += w.w;
+                    }
+                }
+                store_y32<Tout>(y + (t0 + tr) * D + 32 * hf, yw);
+            }
+        }
+        // ---- the new state: bf16 operand copies for the next chunk, or the result
+        {
+            const bool last = c + 1 == nchunks;
+            float w[32];
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                const uint32_t col = (m == 0 ? COL_W1 : m == 1 ? COL_S1 : m == 2 ? COL_W2 : COL_S2) + 32 * hf;
+                tmem_ld32(tl + col, w);
+                if (!last) {
+                    const uint32_t off = m == 0 ? OFF_W1 : m == 1 ? OFF_S1 : m == 2 ? OFF_W2 : OFF_S2;
+                    put_row32(sm + off, 128, jr, 32 * hf, w);
+                } else {
+                    float* dst = (m & 1) ? a.S_T + unit * P : a.M_T + unit * P;
+                    if (m < 2) {
+                        float* r = dst + (long long)j_glob * D + 32 * hf;
+#pragma unroll
+                        for (int q = 0; q < 32; q += 4)
+                            *reinterpret_cast<float4*>(r + q) = make_float4(w[q], w[q + 1], w[q + 2], w[q + 3]);
+                    } else {
+                        float* r = dst + (long long)hid * D + j_glob;
+#pragma unroll
+                        for (int q = 0; q < 32; ++q) r[(long long)(32 * hf + q) * hid] = w[q];
+                    }
+                }
+            }
+        }
+        handoff();
+    }
+    if (failed) {
+        if (tid == 0 && a.status) atomicExch(a.status, NM_ERR_DEVICE_TIMEOUT);
+        // let copies and products still in flight land before the CTA leaves
+        mbar_wait(&bars[0], (uint32_t)(nchunks & 1), WAIT_NS);
+        mbar_wait(&bars[1], mma_phase, WAIT_NS);
+    }
+    tc_fence_before();
+    if (NC > 1) cluster_sync(); else __syncthreads();
+    if (warp == 0) tmem_dealloc(tm, 512);
+}
+
+template <int NC, typename Tout>
+cudaError_t launch(const nm_config& c, const nm_args& a, cudaStream_t s) {
+    CUtensorMap tq, tk, tv;
+    const long long units = (long long)a.B * a.H;
+    if (!make_token_map(&tq, a.q, D, a.T, units) || !make_token_map(&tk, a.k, D, a.T, units) ||
+        !make_token_map(&tv, a.v, D, a.T, units))
+        return cudaErrorInvalidValue;
+    auto kern = tc_mlp_kernel<NC, Tout>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(units * NC), 1, 1);
+    cfg.blockDim = dim3(NTHREADS, 1, 1);
+    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = NC;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, tq, tk, tv, a, c.c_mode);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+template <int NC>
+cudaError_t launch_nc(const nm_config& c, const nm_args& a, cudaStream_t s) {
+    return c.out_dtype == NM_BF16 ? launch<NC, __nv_bfloat16>(c, a, s) : launch<NC, float>(c, a, s);
+}
+
+}  // namespace
+
+bool nm_tc_mlp_supports(const nm_config& c) {
+    return c.kind == NM_MLP2 && c.d == D && (c.hidden == HS || c.hidden == 2 * HS) && c.chunk == BC &&
+           c.in_dtype == NM_BF16;
+}
+
+cudaError_t nm_tc_mlp_launch(const nm_config& c, const nm_args& a, cudaStream_t s) {
+    if (c.hidden == HS) return launch_nc<1>(c, a, s);
+    return launch_nc<2>(c, a, s);
+}

@@ -243,3 +243,36 @@ def test_forward_host_matches_device():
     yd, Md, Sd = mem.forward(g["q"], g["k"], g["v"], g["alpha"], g["eta"], g["beta"], g["M0"], g["S0"])
     assert mem.synchronize() == nm.NM_OK
     assert torch.equal(yh, yd.cpu()) and torch.equal(Mh, Md.cpu()) and torch.equal(Sh, Sd.cpu())
+
+
+@pytest.mark.parametrize("hidden", [128, 256])
+@pytest.mark.parametrize("T,eta_scale,state_scale", [(64, 1.0, 1.0), (100, 1.0, 1.0), (257, 0.5, 0.5),
+                                                     (385, 0.5, 0.5)])
+def test_mlp_tc_hidden_slices(hidden, T, eta_scale, state_scale):
+    """The tensor-core MLP kernel with one CTA (hidden 128) and a two-CTA
+    cluster (hidden 256) per unit, on ragged lengths from random states.
+    Runs longer than two chunks halve the step eta: with the workload's
+    steps the fp64 oracle's own weights pass 1e6 within four chunks from
+    these states, and the comparison would measure that divergence rather
+    than the kernel.  At half the step the weights stay of order 0.1-1
+    over 1000 tokens."""
+    wl = dataclasses.replace(W.WORKLOADS[1], hidden=hidden).with_sizes(B=2, H=2, T=T)
+    _skip_unsupported(wl, nm.PATH_TC)
+    x = W.make_inputs(wl, "cuda", seed=60 + T)
+    x["eta"] *= eta_scale
+    M0, S0 = W.random_state(wl, "cuda", seed=hidden + T, scale=state_scale)
+    gpu = gpu_forward(wl, x, nm.PATH_TC, M0=M0, S0=S0)
+    assert gpu[3] == nm.PATH_TC
+    compare(wl, gpu, oracle_forward(wl, x, M0=M0, S0=S0))
+
+
+@pytest.mark.parametrize("c_mode", [nm.C_ONE_MINUS_BETA, nm.C_PER_TOKEN])
+def test_mlp_tc_momentum_forms(c_mode):
+    wl = W.WORKLOADS[1].with_sizes(B=1, H=3, T=192)
+    _skip_unsupported(wl, nm.PATH_TC)
+    x = W.make_inputs(wl, "cuda", seed=71)
+    if c_mode == nm.C_PER_TOKEN:
+        x["c"] = torch.rand(x["alpha"].shape, device="cuda", generator=torch.Generator("cuda").manual_seed(5))
+    M0, S0 = W.random_state(wl, "cuda", seed=72)
+    gpu = gpu_forward(wl, x, nm.PATH_TC, M0=M0, S0=S0, c_mode=c_mode)
+    compare(wl, gpu, oracle_forward(wl, x, M0=M0, S0=S0, c_mode=c_mode))
