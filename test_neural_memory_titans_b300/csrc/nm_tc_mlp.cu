@@ -108,8 +108,21 @@ constexpr uint32_t ID_M64N128_TT = idesc_bf16_f32(64, 128, true, true);
 constexpr uint32_t ID_M64N64_BT = idesc_bf16_f32(64, 64, false, true);
 constexpr uint64_t WAIT_NS = 2000000000ull;  // 2 s
 
-__device__ __forceinline__ uint64_t kdesc(uint32_t a) { return sw128_desc(a, 16, 1024); }
-__device__ __forceinline__ uint64_t mdesc(uint32_t a, uint32_t lbo) { return sw128_desc(a, lbo, 1024); }
+// Shared-memory descriptors (the sw128_desc fields) for K-major operands and
+// for MN-major operands whose 64-element blocks along M/N are `lbo` bytes
+// apart.  The start-address field holds bits 4..17 of the shared address; the
+// mask matters: in a cluster launch the shared::cta addresses of this CTA
+// carry bits above bit 17, which would otherwise spill into the
+// leading-byte-offset field.  Tiles lie below 228 KB of the window, so a
+// k-step adds to the descriptor directly without carrying out of the field:
+// +2 for 32 bytes (K-major), +128 for 2048 bytes (16 rows, MN-major).
+constexpr uint64_t desc_hi(uint32_t lbo) {
+    return (static_cast<uint64_t>(lbo >> 4) << 16) | (static_cast<uint64_t>(1024 >> 4) << 32) | (1ull << 46) |
+           (2ull << 61);
+}
+__device__ __forceinline__ uint64_t kdesc(uint32_t a) { return desc_hi(16) | ((a >> 4) & 0x3FFFu); }
+__device__ __forceinline__ uint64_t mdesc(uint32_t a, uint32_t lbo) { return desc_hi(lbo) | ((a >> 4) & 0x3FFFu); }
+constexpr uint64_t KS_K = 2, KS_M = 128;
 
 // sigmoid with the fast exponential and reciprocal; z is clamped below at
 // -80 so that 1 + e^{-z} stays finite (silu and its derivative are 0 to
@@ -298,6 +311,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const long long t0 = (long long)c * BC;
         const int n = (int)min((long long)BC, T - t0);
         const float* g = gates + stage * 4 * BC;
+        // the next chunk's gates, loaded now and stored to shared memory after E2
+        float nxt_a = 1.0f, nxt_e = 0.0f, nxt_b = 1.0f, nxt_c = 0.0f;
+        if (tid < BC && c + 1 < nchunks) {
+            const long long t = t0 + BC + tid;
+            if (t < T) {
+                nxt_b = beta[t];
+                nxt_a = 1.0f - alpha[t];
+                nxt_e = eta[t];
+                nxt_c = momentum_c(c_mode, nxt_b, cc, t);
+            }
+        }
 
         // ---- G1 (thread 0, as soon as the tiles land): W1 [q|k], S1 q, Q K^T;
         //      meanwhile the scan of the chunk's gates: Gamma (by columns), gamma, u; A, B, sigma
@@ -306,38 +330,61 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             tiles_ok = mbar_wait(&bars[0], (uint32_t)(c & 1), WAIT_NS);
             if (tiles_ok) {
                 tc_fence_after();
+                const uint64_t dW1 = kdesc(aW1), dS1 = kdesc(aS1), dQK = kdesc(aQK), dK = kdesc(aQK + T64);
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks) {
                     const uint32_t acc = ks ? 1u : 0u;
-                    mma_bf16(tm + COL_XA, kdesc(aW1 + 32 * ks), kdesc(aQK + 32 * ks), ID_XA, acc);
-                    mma_bf16(tm + COL_XB, kdesc(aS1 + 32 * ks), kdesc(aQK + 32 * ks), ID_M128N64, acc);
-                    mma_bf16(tm + COL_QK, kdesc(aQK + 32 * ks), kdesc(aQK + T64 + 32 * ks), ID_M128N64, acc);
+                    mma_bf16(tm + COL_XA, dW1 + KS_K * ks, dQK + KS_K * ks, ID_XA, acc);
+                    mma_bf16(tm + COL_XB, dS1 + KS_K * ks, dQK + KS_K * ks, ID_M128N64, acc);
+                    mma_bf16(tm + COL_QK, dQK + KS_K * ks, dK + KS_K * ks, ID_M128N64, acc);
                 }
                 mma_commit(&bars[1]);
             }
         }
         if (tid >= 128 && tid < 128 + BC) {
+            // column i of Gamma: Gamma_{t,i} = a_t Gamma_{t-1,i} + eta_t u_{t,i}, zero above the diagonal
             const int i = tid - 128;
             float u = g[3 * BC + i];
             float G = g[BC + i] * u;
-            for (int t = 0; t < i; ++t) Gm[t * GS + i] = 0.0f;
-            Gm[i * GS + i] = G;
-            for (int t = i + 1; t < BC; ++t) {
-                u *= g[2 * BC + t];
-                G = fmaf(g[t], G, g[BC + t] * u);
-                Gm[t * GS + i] = G;
+            const float4* g4 = reinterpret_cast<const float4*>(g);
+#pragma unroll
+            for (int t4 = 0; t4 < BC / 4; ++t4) {
+                const float4 va = g4[t4], ve = g4[BC / 4 + t4], vb = g4[BC / 2 + t4];
+                const float ga[4] = {va.x, va.y, va.z, va.w}, ge[4] = {ve.x, ve.y, ve.z, ve.w},
+                            gb[4] = {vb.x, vb.y, vb.z, vb.w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int t = 4 * t4 + k;
+                    if (t > i) {
+                        u *= gb[k];
+                        G = fmaf(ga[k], G, ge[k] * u);
+                    }
+                    Gm[t * GS + i] = t >= i ? G : 0.0f;
+                }
             }
             sGl[i] = G;
             sU[i] = u;
         } else if (tid == 224) {
             float A = 1.f, Bc = 1.f, sg = 0.f;
-            for (int t = 0; t < BC; ++t) {
-                A *= g[t];
-                Bc *= g[2 * BC + t];
-                sg = fmaf(g[t], sg, g[BC + t] * Bc);
-                sA[t] = A;
-                sBc[t] = Bc;
-                sSg[t] = sg;
+            const float4* g4 = reinterpret_cast<const float4*>(g);
+#pragma unroll
+            for (int t4 = 0; t4 < BC / 4; ++t4) {
+                const float4 va = g4[t4], ve = g4[BC / 4 + t4], vb = g4[BC / 2 + t4];
+                const float ga[4] = {va.x, va.y, va.z, va.w}, ge[4] = {ve.x, ve.y, ve.z, ve.w},
+                            gb[4] = {vb.x, vb.y, vb.z, vb.w};
+                float oa[4], ob[4], os[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    A *= ga[k];
+                    Bc *= gb[k];
+                    sg = fmaf(ga[k], sg, ge[k] * Bc);
+                    oa[k] = A;
+                    ob[k] = Bc;
+                    os[k] = sg;
+                }
+                reinterpret_cast<float4*>(sA)[t4] = make_float4(oa[0], oa[1], oa[2], oa[3]);
+                reinterpret_cast<float4*>(sBc)[t4] = make_float4(ob[0], ob[1], ob[2], ob[3]);
+                reinterpret_cast<float4*>(sSg)[t4] = make_float4(os[0], os[1], os[2], os[3]);
             }
         }
         // the tiles (waited for by thread 0) and the scan are visible to all after this
@@ -366,9 +413,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
             for (int pr = 0; pr < 2; ++pr) {
                 const uint32_t cw = (pr ? COL_W2 : COL_W1) + 32 * hf, cs = (pr ? COL_S2 : COL_S1) + 32 * hf;
-                tmem_ld32_async(tl + cw, w);
-                tmem_ld32_async(tl + cs, s);
-                tmem_wait_ld();
+                tmem_ld32x2(tl + cw, tl + cs, w, s);
 #pragma unroll
                 for (int q = 0; q < 32; ++q) {
                     w[q] = fmaf(An, w[q], -sn * s[q]);
@@ -382,9 +427,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         // ---- E1: a(k) and silu'(z) from z = W1 k; P1 = Gamma (.) Q K^T
         {
             float z[32], p[32];
-            tmem_ld32_async(tl + COL_Z + 32 * hf, z);
-            if (qd < 2) tmem_ld32_async(tl + COL_QK + 32 * hf, p);
-            tmem_wait_ld();
+            if (qd < 2) tmem_ld32x2(tl + COL_Z + 32 * hf, tl + COL_QK + 32 * hf, z, p);
+            else tmem_ld32(tl + COL_Z + 32 * hf, z);
 #pragma unroll
             for (int q = 0; q < 32; ++q) {
                 const float sg = sigmoid_f(z[q]);
@@ -406,10 +450,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         // ---- G2: partial key forward yhat[t][o] = sum_{j in slice} a(k_t)_j W2[o][j]
         const bool go2 = !failed;
         if (go2 && tid == 0) {
+            const uint64_t dAK = mdesc(aAK, T128), dW2 = mdesc(aW2, T128);
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks)
-                mma_bf16(tm + COL_YH, mdesc(aAK + 2048 * ks, T128), mdesc(aW2 + 2048 * ks, T128), ID_M64N64_TT,
-                         ks ? 1u : 0u);
+                mma_bf16(tm + COL_YH, dAK + KS_M * ks, dW2 + KS_M * ks, ID_M64N64_TT, ks ? 1u : 0u);
             mma_commit(&bars[1]);
         }
         mma_wait(go2);
@@ -453,14 +497,21 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             for (int q = 0; q < 32; ++q) o1[q] = uu * ev[q];
             put_row32(sm + OFF_EU, 64, tr, 32 * hf, o1);
         }
-        if (c + 1 < nchunks) load_gates(c + 1, stage ^ 1);
+        if (tid < BC && c + 1 < nchunks) {
+            float* gn = gates + (stage ^ 1) * 4 * BC;
+            gn[tid] = nxt_a;
+            gn[BC + tid] = nxt_e;
+            gn[2 * BC + tid] = nxt_b;
+            gn[3 * BC + tid] = nxt_c;
+        }
         handoff();
         // ---- G3: W2^T e (the next chunk's tiles start loading: Q|K and V are free)
         const bool go3 = !failed;
         if (go3 && tid == 0) {
+            const uint64_t dW2 = kdesc(aW2), dE = kdesc(aE);
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks)
-                mma_bf16(tm + COL_XD, kdesc(aW2 + 32 * ks), kdesc(aE + 32 * ks), ID_M128N64, ks ? 1u : 0u);
+                mma_bf16(tm + COL_XD, dW2 + KS_K * ks, dE + KS_K * ks, ID_M128N64, ks ? 1u : 0u);
             mma_commit(&bars[1]);
             if (c + 1 < nchunks) issue_tiles(c + 1);
         }
@@ -477,13 +528,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         // ---- G4: state update and sum_i P1[t][i] delta_i
         const bool go4 = !failed;
         if (go4 && tid == 0) {
+            const uint64_t dDT = kdesc(aDT), dAK = kdesc(aAK), dP = kdesc(aP);
+            const uint64_t dKG = mdesc(aKG, T64), dKU = mdesc(aKU, T64), dEG = mdesc(aEG, T64), dEU = mdesc(aEU, T64);
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) {
-                mma_bf16(tm + COL_W1, kdesc(aDT + 32 * ks), mdesc(aKG + 2048 * ks, T64), ID_UPD, 1u);
-                mma_bf16(tm + COL_S1, kdesc(aDT + 32 * ks), mdesc(aKU + 2048 * ks, T64), ID_UPD, 1u);
-                mma_bf16(tm + COL_W2, kdesc(aAK + 32 * ks), mdesc(aEG + 2048 * ks, T64), ID_UPD, 1u);
-                mma_bf16(tm + COL_S2, kdesc(aAK + 32 * ks), mdesc(aEU + 2048 * ks, T64), ID_UPD, 1u);
-                mma_bf16(tm + COL_R1, kdesc(aDT + 32 * ks), kdesc(aP + 32 * ks), ID_M128N64, ks ? 1u : 0u);
+                mma_bf16(tm + COL_W1, dDT + KS_K * ks, dKG + KS_M * ks, ID_UPD, 1u);
+                mma_bf16(tm + COL_S1, dDT + KS_K * ks, dKU + KS_M * ks, ID_UPD, 1u);
+                mma_bf16(tm + COL_W2, dAK + KS_K * ks, dEG + KS_M * ks, ID_UPD, 1u);
+                mma_bf16(tm + COL_S2, dAK + KS_K * ks, dEU + KS_M * ks, ID_UPD, 1u);
+                mma_bf16(tm + COL_R1, dDT + KS_K * ks, dP + KS_K * ks, ID_M128N64, ks ? 1u : 0u);
             }
             mma_commit(&bars[1]);
         }
@@ -491,10 +544,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         // ---- E4: h_t = A_t W1 q_t - sigma_t S1 q_t - sum_i P1[t][i] delta_i, a_t = silu(h_t)
         {
             float xa[32], xb[32], r1[32];
-            tmem_ld32_async(tl + COL_XA + 32 * hf, xa);
-            tmem_ld32_async(tl + COL_XB + 32 * hf, xb);
-            tmem_ld32_async(tl + COL_R1 + 32 * hf, r1);
-            tmem_wait_ld();
+            tmem_ld32x3(tl + COL_XA + 32 * hf, tl + COL_XB + 32 * hf, tl + COL_R1 + 32 * hf, xa, xb, r1);
 #pragma unroll
             for (int q = 0; q < 32; ++q) {
                 const int t = 32 * hf + q;
@@ -506,11 +556,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         // ---- G5: [W2 a_t | S2 a_t] and a_t . a(k_i), partial over this CTA's slice
         const bool go5 = !failed;
         if (go5 && tid == 0) {
+            const uint64_t dAQ = mdesc(aDT, T128), dW2 = mdesc(aW2, T128), dAK = mdesc(aAK, T128);
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
                 const uint32_t acc = ks ? 1u : 0u;
-                mma_bf16(tm + COL_YW, mdesc(aDT + 2048 * ks, T128), mdesc(aW2 + 2048 * ks, T128), ID_M64N128_TT, acc);
-                mma_bf16(tm + COL_AA, mdesc(aDT + 2048 * ks, T128), mdesc(aAK + 2048 * ks, T128), ID_M64N64_TT, acc);
+                mma_bf16(tm + COL_YW, dAQ + KS_M * ks, dW2 + KS_M * ks, ID_M64N128_TT, acc);
+                mma_bf16(tm + COL_AA, dAQ + KS_M * ks, dAK + KS_M * ks, ID_M64N64_TT, acc);
             }
             mma_commit(&bars[1]);
         }
@@ -533,19 +584,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         // ---- G6: sum_i P2[t][i] e_i
         const bool go6 = !failed;
         if (go6 && tid == 0) {
+            const uint64_t dP = kdesc(aP), dE = mdesc(aE, T64);
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks)
-                mma_bf16(tm + COL_PE, kdesc(aP + 32 * ks), mdesc(aE + 2048 * ks, T64), ID_M64N64_BT, ks ? 1u : 0u);
+                mma_bf16(tm + COL_PE, dP + KS_K * ks, dE + KS_M * ks, ID_M64N64_BT, ks ? 1u : 0u);
             mma_commit(&bars[1]);
         }
         mma_wait(go6);
         // ---- E6: partial y, reduced onto the CTA that owns the columns
         {
             float yw[32], ys[32], pe[32];
-            tmem_ld32_async(tl + COL_YW + 32 * hf, yw);
-            tmem_ld32_async(tl + COL_YW + 64 + 32 * hf, ys);
-            tmem_ld32_async(tl + COL_PE + 32 * hf, pe);
-            tmem_wait_ld();
+            tmem_ld32x3(tl + COL_YW + 32 * hf, tl + COL_YW + 64 + 32 * hf, tl + COL_PE + 32 * hf, yw, ys, pe);
             const bool own = NC == 1 || hf == rank;
             if (r64) {
                 const float At = sA[tr], st = sSg[tr];
