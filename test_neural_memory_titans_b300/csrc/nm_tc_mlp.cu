@@ -30,7 +30,8 @@
 //     of (a(k_i) . a_t)) is reduced onto the CTA that owns those output
 //     columns, which writes y.
 //
-// Per CTA (256 threads; thread 0 issues TMA and MMA):
+// Per CTA (512 threads, each epilogue thread owning 16 columns of an
+// accumulator row; thread 0 issues TMA and MMA):
 //   TMEM, 128 lanes x 512 fp32 columns; lane = j for M=128 products, row t at
 //   lane (t % 16) + 32 (t / 16) for M=64 products:
 //     0..63 W1 [j][x], 64..127 S1 [j][x], 128..191 W2^T [j][o], 192..255 S2^T
@@ -56,7 +57,7 @@ using namespace tc;
 constexpr int D = 64;         // key / value width
 constexpr int HS = 128;       // hidden units per CTA
 constexpr int BC = 64;        // chunk size
-constexpr int NTHREADS = 256;
+constexpr int CW_DEFAULT = 16;  // columns per thread in the epilogues (512 threads)
 constexpr uint32_t T64 = 64 * 128;    // [64 rows][64 bf16] swizzled tile
 constexpr uint32_t T128 = 128 * 128;  // [128 rows][64 bf16]
 
@@ -136,11 +137,12 @@ __device__ __forceinline__ float momentum_c(int mode, float beta, const float* c
     return 1.0f;
 }
 
-// 32 bf16 of row r, columns c0..c0+31, of a swizzled tile, as floats.
-__device__ __forceinline__ void get_row32(const unsigned char* tile, uint32_t rows, uint32_t r, uint32_t c0, float* v) {
+// W (16 or 32) bf16 of row r, columns c0..c0+W-1, of a swizzled tile, as floats.
+template <int W>
+__device__ __forceinline__ void get_row(const unsigned char* tile, uint32_t rows, uint32_t r, uint32_t c0, float* v) {
     const uint32_t base = smem_u32(tile);
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
+    for (int q = 0; q < W / 8; ++q) {
         const uint4 w = ld_shared_v4(base + sw128_offset(r, c0 + 8 * q, rows));
         v[8 * q + 0] = bf16_lo(w.x); v[8 * q + 1] = bf16_hi(w.x);
         v[8 * q + 2] = bf16_lo(w.y); v[8 * q + 3] = bf16_hi(w.y);
@@ -149,24 +151,23 @@ __device__ __forceinline__ void get_row32(const unsigned char* tile, uint32_t ro
     }
 }
 
-template <typename Tout>
-__device__ __forceinline__ void store_y32(Tout* p, const float* v);
-template <>
-__device__ __forceinline__ void store_y32<__nv_bfloat16>(__nv_bfloat16* p, const float* v) {
+// W consecutive outputs of one row of y.
+template <int W>
+__device__ __forceinline__ void store_y(__nv_bfloat16* p, const float* v) {
 #pragma unroll
-    for (int q = 0; q < 4; ++q)
+    for (int q = 0; q < W / 8; ++q)
         reinterpret_cast<uint4*>(p)[q] = make_uint4(pack_bf16(v[8 * q], v[8 * q + 1]), pack_bf16(v[8 * q + 2], v[8 * q + 3]),
                                                     pack_bf16(v[8 * q + 4], v[8 * q + 5]), pack_bf16(v[8 * q + 6], v[8 * q + 7]));
 }
-template <>
-__device__ __forceinline__ void store_y32<float>(float* p, const float* v) {
+template <int W>
+__device__ __forceinline__ void store_y(float* p, const float* v) {
 #pragma unroll
-    for (int q = 0; q < 8; ++q)
+    for (int q = 0; q < W / 4; ++q)
         reinterpret_cast<float4*>(p)[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
 }
 
-template <int NC, typename Tout>
-__global__ void __launch_bounds__(NTHREADS, 1)
+template <int NC, int CW, typename Tout>
+__global__ void __launch_bounds__(128 * (64 / CW), 1)
     tc_mlp_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, nm_args a, int c_mode) {
     extern __shared__ unsigned char smem_raw[];
@@ -187,7 +188,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int warp = tid >> 5;
     const int lane = tid & 31;
     const int qd = warp & 3;   // TMEM lane quadrant of this warp
-    const int hf = warp >> 2;  // which 32 of a 64-column accumulator this thread reads
+    constexpr int NQ = 64 / CW;  // column groups: threads = 128 * NQ
+    const int hq = warp >> 2;    // which CW columns of a 64-column accumulator this thread reads
     const int rank = NC > 1 ? (int)cluster_ctarank() : 0;
     const long long unit = blockIdx.x / NC;
     const long long T = a.T;
@@ -254,25 +256,25 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     {
         const float* m0 = a.M0 + unit * P;
         const float* s0 = a.S0 + unit * P;
-        float r[32];
+        float r[CW];
 #pragma unroll
         for (int which = 0; which < 2; ++which) {
             const float* src = which ? s0 : m0;
             // W1 (or S1) row j_glob, columns 32 hf .. 32 hf + 31
-            const float* w1 = src + (long long)j_glob * D + 32 * hf;
+            const float* w1 = src + (long long)j_glob * D + CW * hq;
 #pragma unroll
-            for (int q = 0; q < 32; q += 4) {
+            for (int q = 0; q < CW; q += 4) {
                 const float4 w = *reinterpret_cast<const float4*>(w1 + q);
                 r[q] = w.x; r[q + 1] = w.y; r[q + 2] = w.z; r[q + 3] = w.w;
             }
-            tmem_st32(tl + (which ? COL_S1 : COL_W1) + 32 * hf, r);
-            put_row32(sm + (which ? OFF_S1 : OFF_W1), 128, jr, 32 * hf, r);
+            tmem_st_n(tl + (which ? COL_S1 : COL_W1) + CW * hq, r);
+            put_row<CW>(sm + (which ? OFF_S1 : OFF_W1), 128, jr, CW * hq, r);
             // W2 (or S2) transposed: [j][o] = W2[o][j_glob], o = 32 hf + q
             const float* w2 = src + (long long)hid * D + j_glob;
 #pragma unroll
-            for (int q = 0; q < 32; ++q) r[q] = w2[(long long)(32 * hf + q) * hid];
-            tmem_st32(tl + (which ? COL_S2 : COL_W2) + 32 * hf, r);
-            put_row32(sm + (which ? OFF_S2 : OFF_W2), 128, jr, 32 * hf, r);
+            for (int q = 0; q < CW; ++q) r[q] = w2[(long long)(CW * hq + q) * hid];
+            tmem_st_n(tl + (which ? COL_S2 : COL_W2) + CW * hq, r);
+            put_row<CW>(sm + (which ? OFF_S2 : OFF_W2), 128, jr, CW * hq, r);
         }
     }
     fence_proxy_async();
@@ -305,22 +307,23 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tc_fence_after();
     };
 
-    float ds[32];  // silu'(z) for this thread's row and columns, kept from E1 to E3
+    float ds[CW];  // silu'(z) for this thread's row and columns, kept from E1 to E3
     for (int c = 0; c < nchunks; ++c) {
         const int stage = c & 1;
         const long long t0 = (long long)c * BC;
         const int n = (int)min((long long)BC, T - t0);
         const float* g = gates + stage * 4 * BC;
-        // the next chunk's gates, loaded now and stored to shared memory after E2
-        float nxt_a = 1.0f, nxt_e = 0.0f, nxt_b = 1.0f, nxt_c = 0.0f;
-        if (tid < BC && c + 1 < nchunks) {
-            const long long t = t0 + BC + tid;
-            if (t < T) {
-                nxt_b = beta[t];
-                nxt_a = 1.0f - alpha[t];
-                nxt_e = eta[t];
-                nxt_c = momentum_c(c_mode, nxt_b, cc, t);
-            }
+        // the next chunk's gates: warps 2-3 load them now (raw, so that nothing
+        // waits for the loads until they are stored to shared memory after E2)
+        const int gi = tid - 64;
+        const bool nxt_valid = gi >= 0 && gi < BC && c + 1 < nchunks && t0 + BC + gi < T;
+        float nxt_al = 0.0f, nxt_e = 0.0f, nxt_b = 1.0f, nxt_c = 0.0f;
+        if (nxt_valid) {
+            const long long t = t0 + BC + gi;
+            nxt_al = alpha[t];
+            nxt_e = eta[t];
+            nxt_b = beta[t];
+            if (c_mode == NM_C_PER_TOKEN) nxt_c = cc[t];
         }
 
         // ---- G1 (thread 0, as soon as the tiles land): W1 [q|k], S1 q, Q K^T;
@@ -391,59 +394,40 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const bool go1 = !failed && !__syncthreads_or(!tiles_ok);
         if (!go1 && !failed) failed = true;
         // -gamma_t k_t and u_t k_t as bf16 operand rows (while G1 runs)
-        if (tid < BC) {
-            float kv[32], o1[32], o2[32];
-            const float gm = -sGl[tid], uu = sU[tid];
+        if (tid < 64 * NQ) {  // row t = tid % 64, columns CW * (tid / 64) ..
+            const int t = tid & 63, c0 = CW * (tid >> 6);
+            float kv[CW], o1[CW], o2[CW];
+            const float gm = -sGl[t], uu = sU[t];
+            get_row<CW>(sm + OFF_QK, 128, 64 + t, c0, kv);
 #pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2) {
-                get_row32(sm + OFF_QK, 128, 64 + tid, 32 * h2, kv);
-#pragma unroll
-                for (int q = 0; q < 32; ++q) {
-                    o1[q] = gm * kv[q];
-                    o2[q] = uu * kv[q];
-                }
-                put_row32(sm + OFF_KG, 64, tid, 32 * h2, o1);
-                put_row32(sm + OFF_KU, 64, tid, 32 * h2, o2);
+            for (int q = 0; q < CW; ++q) {
+                o1[q] = gm * kv[q];
+                o2[q] = uu * kv[q];
             }
-        }
-        // rescale the fp32 state for this chunk: W <- A_n W - sigma_n S, S <- B_n S
-        {
-            const float An = sA[BC - 1], Bn = sBc[BC - 1], sn = sSg[BC - 1];
-            float w[32], s[32];
-#pragma unroll
-            for (int pr = 0; pr < 2; ++pr) {
-                const uint32_t cw = (pr ? COL_W2 : COL_W1) + 32 * hf, cs = (pr ? COL_S2 : COL_S1) + 32 * hf;
-                tmem_ld32x2(tl + cw, tl + cs, w, s);
-#pragma unroll
-                for (int q = 0; q < 32; ++q) {
-                    w[q] = fmaf(An, w[q], -sn * s[q]);
-                    s[q] = Bn * s[q];
-                }
-                tmem_st32(tl + cw, w);
-                tmem_st32(tl + cs, s);
-            }
+            put_row<CW>(sm + OFF_KG, 64, t, c0, o1);
+            put_row<CW>(sm + OFF_KU, 64, t, c0, o2);
         }
         mma_wait(go1);
         // ---- E1: a(k) and silu'(z) from z = W1 k; P1 = Gamma (.) Q K^T
         {
-            float z[32], p[32];
-            if (qd < 2) tmem_ld32x2(tl + COL_Z + 32 * hf, tl + COL_QK + 32 * hf, z, p);
-            else tmem_ld32(tl + COL_Z + 32 * hf, z);
+            float z[CW], p[CW];
+            if (qd < 2) tmem_ld_n(tl + COL_Z + CW * hq, tl + COL_QK + CW * hq, z, p);
+            else tmem_ld_n(tl + COL_Z + CW * hq, z);
 #pragma unroll
-            for (int q = 0; q < 32; ++q) {
+            for (int q = 0; q < CW; ++q) {
                 const float sg = sigmoid_f(z[q]);
                 ds[q] = fmaf(z[q] * sg, 1.0f - sg, sg);  // silu'(z) = s + z s (1 - s)
                 z[q] *= sg;
             }
-            put_row32(sm + OFF_AK, 128, jr, 32 * hf, z);
+            put_row<CW>(sm + OFF_AK, 128, jr, CW * hq, z);
             if (qd < 2) {
-                const float* gr = Gm + jr * GS + 32 * hf;
+                const float* gr = Gm + jr * GS + CW * hq;
 #pragma unroll
-                for (int q = 0; q < 32; q += 4) {
+                for (int q = 0; q < CW; q += 4) {
                     const float4 gg = *reinterpret_cast<const float4*>(gr + q);
                     p[q] *= gg.x; p[q + 1] *= gg.y; p[q + 2] *= gg.z; p[q + 3] *= gg.w;
                 }
-                put_row32(sm + OFF_P, 64, jr, 32 * hf, p);
+                put_row<CW>(sm + OFF_P, 64, jr, CW * hq, p);
             }
         }
         handoff();
@@ -458,28 +442,46 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         mma_wait(go2);
         // ---- E2: all-reduce of the key forward over the cluster, e = 2 (yhat - v)
-        float ev[32];
+        float ev[CW];
         {
-            tmem_ld32(tl + COL_YH + 32 * hf, ev);
+            tmem_ld_n(tl + COL_YH + CW * hq, ev);
             if (r64) {
                 if (NC > 1) {
-                    const uint32_t dst = map_to_rank(smem_u32(Yx + tr * GS + 32 * hf), (uint32_t)peer);
+                    const uint32_t dst = map_to_rank(smem_u32(Yx + tr * GS + CW * hq), (uint32_t)peer);
 #pragma unroll
-                    for (int q = 0; q < 8; ++q)
+                    for (int q = 0; q < CW / 4; ++q)
                         st_cluster_v4(dst + 16 * q, ev[4 * q], ev[4 * q + 1], ev[4 * q + 2], ev[4 * q + 3]);
                 }
-                float vv[32];
-                get_row32(sm + OFF_V, 64, tr, 32 * hf, vv);
+                float vv[CW];
+                get_row<CW>(sm + OFF_V, 64, tr, CW * hq, vv);
 #pragma unroll
-                for (int q = 0; q < 32; ++q) ev[q] = 2.0f * (ev[q] - vv[q]);
+                for (int q = 0; q < CW; ++q) ev[q] = 2.0f * (ev[q] - vv[q]);
+            }
+        }
+        // while the peer's partial sums arrive: rescale the fp32 state for this
+        // chunk, W <- A_n W - sigma_n S, S <- B_n S (before G4 accumulates into it)
+        {
+            const float An = sA[BC - 1], Bn = sBc[BC - 1], sn = sSg[BC - 1];
+            float w[CW], s[CW];
+#pragma unroll
+            for (int pr = 0; pr < 2; ++pr) {
+                const uint32_t cw = (pr ? COL_W2 : COL_W1) + CW * hq, cs = (pr ? COL_S2 : COL_S1) + CW * hq;
+                tmem_ld_n(tl + cw, tl + cs, w, s);
+#pragma unroll
+                for (int q = 0; q < CW; ++q) {
+                    w[q] = fmaf(An, w[q], -sn * s[q]);
+                    s[q] = Bn * s[q];
+                }
+                tmem_st_n(tl + cw, w);
+                tmem_st_n(tl + cs, s);
             }
         }
         if (NC > 1) cluster_sync();
         if (r64) {
             if (NC > 1) {
-                const float* yx = Yx + tr * GS + 32 * hf;
+                const float* yx = Yx + tr * GS + CW * hq;
 #pragma unroll
-                for (int q = 0; q < 32; q += 4) {
+                for (int q = 0; q < CW; q += 4) {
                     const float4 w = *reinterpret_cast<const float4*>(yx + q);
                     ev[q] = fmaf(2.0f, w.x, ev[q]);
                     ev[q + 1] = fmaf(2.0f, w.y, ev[q + 1]);
@@ -487,22 +489,25 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     ev[q + 3] = fmaf(2.0f, w.w, ev[q + 3]);
                 }
             }
-            put_row32(sm + OFF_E, 64, tr, 32 * hf, ev);
-            float o1[32];
+            put_row<CW>(sm + OFF_E, 64, tr, CW * hq, ev);
+            float o1[CW];
             const float gm = -sGl[tr], uu = sU[tr];
 #pragma unroll
-            for (int q = 0; q < 32; ++q) o1[q] = gm * ev[q];
-            put_row32(sm + OFF_EG, 64, tr, 32 * hf, o1);
+            for (int q = 0; q < CW; ++q) o1[q] = gm * ev[q];
+            put_row<CW>(sm + OFF_EG, 64, tr, CW * hq, o1);
 #pragma unroll
-            for (int q = 0; q < 32; ++q) o1[q] = uu * ev[q];
-            put_row32(sm + OFF_EU, 64, tr, 32 * hf, o1);
+            for (int q = 0; q < CW; ++q) o1[q] = uu * ev[q];
+            put_row<CW>(sm + OFF_EU, 64, tr, CW * hq, o1);
         }
-        if (tid < BC && c + 1 < nchunks) {
+        if (gi >= 0 && gi < BC && c + 1 < nchunks) {
+            // tokens past T change nothing: a = 1, eta = 0, beta = 1, c = 0
             float* gn = gates + (stage ^ 1) * 4 * BC;
-            gn[tid] = nxt_a;
-            gn[BC + tid] = nxt_e;
-            gn[2 * BC + tid] = nxt_b;
-            gn[3 * BC + tid] = nxt_c;
+            gn[gi] = nxt_valid ? 1.0f - nxt_al : 1.0f;
+            gn[BC + gi] = nxt_e;
+            gn[2 * BC + gi] = nxt_b;
+            gn[3 * BC + gi] = !nxt_valid ? 0.0f
+                              : c_mode == NM_C_ONE_MINUS_BETA ? 1.0f - nxt_b
+                              : c_mode == NM_C_PER_TOKEN ? nxt_c : 1.0f;
         }
         handoff();
         // ---- G3: W2^T e (the next chunk's tiles start loading: Q|K and V are free)
@@ -518,11 +523,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         mma_wait(go3);
         // ---- E3: delta = (W2^T e) (.) silu'(z)
         {
-            float xd[32];
-            tmem_ld32(tl + COL_XD + 32 * hf, xd);
+            float xd[CW];
+            tmem_ld_n(tl + COL_XD + CW * hq, xd);
 #pragma unroll
-            for (int q = 0; q < 32; ++q) xd[q] *= ds[q];
-            put_row32(sm + OFF_DT, 128, jr, 32 * hf, xd);
+            for (int q = 0; q < CW; ++q) xd[q] *= ds[q];
+            put_row<CW>(sm + OFF_DT, 128, jr, CW * hq, xd);
         }
         handoff();
         // ---- G4: state update and sum_i P1[t][i] delta_i
@@ -530,54 +535,62 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (go4 && tid == 0) {
             const uint64_t dDT = kdesc(aDT), dAK = kdesc(aAK), dP = kdesc(aP);
             const uint64_t dKG = mdesc(aKG, T64), dKU = mdesc(aKU, T64), dEG = mdesc(aEG, T64), dEU = mdesc(aEU, T64);
+            // R1 and the W1 / S1 updates first (E4 overwrites delta, which they
+            // read, with a_t); the W2 / S2 updates complete behind them (the next
+            // commit covers them)
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) {
+                mma_bf16(tm + COL_R1, dDT + KS_K * ks, dP + KS_K * ks, ID_M128N64, ks ? 1u : 0u);
                 mma_bf16(tm + COL_W1, dDT + KS_K * ks, dKG + KS_M * ks, ID_UPD, 1u);
                 mma_bf16(tm + COL_S1, dDT + KS_K * ks, dKU + KS_M * ks, ID_UPD, 1u);
-                mma_bf16(tm + COL_W2, dAK + KS_K * ks, dEG + KS_M * ks, ID_UPD, 1u);
-                mma_bf16(tm + COL_S2, dAK + KS_K * ks, dEU + KS_M * ks, ID_UPD, 1u);
-                mma_bf16(tm + COL_R1, dDT + KS_K * ks, dP + KS_K * ks, ID_M128N64, ks ? 1u : 0u);
             }
             mma_commit(&bars[1]);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
+                mma_bf16(tm + COL_W2, dAK + KS_K * ks, dEG + KS_M * ks, ID_UPD, 1u);
+                mma_bf16(tm + COL_S2, dAK + KS_K * ks, dEU + KS_M * ks, ID_UPD, 1u);
+            }
         }
         mma_wait(go4);
         // ---- E4: h_t = A_t W1 q_t - sigma_t S1 q_t - sum_i P1[t][i] delta_i, a_t = silu(h_t)
         {
-            float xa[32], xb[32], r1[32];
-            tmem_ld32x3(tl + COL_XA + 32 * hf, tl + COL_XB + 32 * hf, tl + COL_R1 + 32 * hf, xa, xb, r1);
+            float xa[CW], xb[CW], r1[CW];
+            tmem_ld_n(tl + COL_XA + CW * hq, tl + COL_XB + CW * hq, tl + COL_R1 + CW * hq, xa, xb, r1);
 #pragma unroll
-            for (int q = 0; q < 32; ++q) {
-                const int t = 32 * hf + q;
+            for (int q = 0; q < CW; ++q) {
+                const int t = CW * hq + q;
                 xa[q] = silu_f(fmaf(sA[t], xa[q], -fmaf(sSg[t], xb[q], r1[q])));
             }
-            put_row32(sm + OFF_DT, 128, jr, 32 * hf, xa);
+            put_row<CW>(sm + OFF_DT, 128, jr, CW * hq, xa);
         }
         handoff();
         // ---- G5: [W2 a_t | S2 a_t] and a_t . a(k_i), partial over this CTA's slice
         const bool go5 = !failed;
         if (go5 && tid == 0) {
             const uint64_t dAQ = mdesc(aDT, T128), dW2 = mdesc(aW2, T128), dAK = mdesc(aAK, T128);
+            // a_t . a(k_i) first: E5 waits only for it (and for the state
+            // updates issued before it); W2 a_t | S2 a_t completes behind it
 #pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-                const uint32_t acc = ks ? 1u : 0u;
-                mma_bf16(tm + COL_YW, dAQ + KS_M * ks, dW2 + KS_M * ks, ID_M64N128_TT, acc);
-                mma_bf16(tm + COL_AA, dAQ + KS_M * ks, dAK + KS_M * ks, ID_M64N64_TT, acc);
-            }
+            for (int ks = 0; ks < 8; ++ks)
+                mma_bf16(tm + COL_AA, dAQ + KS_M * ks, dAK + KS_M * ks, ID_M64N64_TT, ks ? 1u : 0u);
             mma_commit(&bars[1]);
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks)
+                mma_bf16(tm + COL_YW, dAQ + KS_M * ks, dW2 + KS_M * ks, ID_M64N128_TT, ks ? 1u : 0u);
         }
         mma_wait(go5);
         // ---- E5: P2 = Gamma (.) (a_t . a(k_i))
         {
-            float p[32];
-            tmem_ld32(tl + COL_AA + 32 * hf, p);
+            float p[CW];
+            tmem_ld_n(tl + COL_AA + CW * hq, p);
             if (r64) {
-                const float* gr = Gm + tr * GS + 32 * hf;
+                const float* gr = Gm + tr * GS + CW * hq;
 #pragma unroll
-                for (int q = 0; q < 32; q += 4) {
+                for (int q = 0; q < CW; q += 4) {
                     const float4 gg = *reinterpret_cast<const float4*>(gr + q);
                     p[q] *= gg.x; p[q + 1] *= gg.y; p[q + 2] *= gg.z; p[q + 3] *= gg.w;
                 }
-                put_row32(sm + OFF_P, 64, tr, 32 * hf, p);
+                put_row<CW>(sm + OFF_P, 64, tr, CW * hq, p);
             }
         }
         handoff();
@@ -593,57 +606,58 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         mma_wait(go6);
         // ---- E6: partial y, reduced onto the CTA that owns the columns
         {
-            float yw[32], ys[32], pe[32];
-            tmem_ld32x3(tl + COL_YW + 32 * hf, tl + COL_YW + 64 + 32 * hf, tl + COL_PE + 32 * hf, yw, ys, pe);
-            const bool own = NC == 1 || hf == rank;
+            float yw[CW], ys[CW], pe[CW];
+            tmem_ld_n(tl + COL_YW + CW * hq, tl + COL_YW + 64 + CW * hq, tl + COL_PE + CW * hq, yw, ys, pe);
+            const bool own = NC == 1 || (CW * hq) / 32 == rank;
             if (r64) {
                 const float At = sA[tr], st = sSg[tr];
 #pragma unroll
-                for (int q = 0; q < 32; ++q) yw[q] = fmaf(At, yw[q], -fmaf(st, ys[q], pe[q]));
+                for (int q = 0; q < CW; ++q) yw[q] = fmaf(At, yw[q], -fmaf(st, ys[q], pe[q]));
                 if (!own) {
-                    const uint32_t dst = map_to_rank(smem_u32(Yr + tr * RS), (uint32_t)peer);
+                    const uint32_t dst = map_to_rank(smem_u32(Yr + tr * RS + (CW * hq) % 32), (uint32_t)peer);
 #pragma unroll
-                    for (int q = 0; q < 8; ++q)
+                    for (int q = 0; q < CW / 4; ++q)
                         st_cluster_v4(dst + 16 * q, yw[4 * q], yw[4 * q + 1], yw[4 * q + 2], yw[4 * q + 3]);
+                }
+            }
+            // while the peer's partial y arrives: the new state becomes the next
+            // chunk's bf16 operands (or, after the last chunk, the result)
+            {
+                const bool last = c + 1 == nchunks;
+                float w[CW];
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    const uint32_t col = (m == 0 ? COL_W1 : m == 1 ? COL_S1 : m == 2 ? COL_W2 : COL_S2) + CW * hq;
+                    tmem_ld_n(tl + col, w);
+                    if (!last) {
+                        const uint32_t off = m == 0 ? OFF_W1 : m == 1 ? OFF_S1 : m == 2 ? OFF_W2 : OFF_S2;
+                        put_row<CW>(sm + off, 128, jr, CW * hq, w);
+                    } else {
+                        float* dst = (m & 1) ? a.S_T + unit * P : a.M_T + unit * P;
+                        if (m < 2) {
+                            float* r = dst + (long long)j_glob * D + CW * hq;
+#pragma unroll
+                            for (int q = 0; q < CW; q += 4)
+                                *reinterpret_cast<float4*>(r + q) = make_float4(w[q], w[q + 1], w[q + 2], w[q + 3]);
+                        } else {
+                            float* r = dst + (long long)hid * D + j_glob;
+#pragma unroll
+                            for (int q = 0; q < CW; ++q) r[(long long)(CW * hq + q) * hid] = w[q];
+                        }
+                    }
                 }
             }
             if (NC > 1) cluster_sync();
             if (r64 && own && tr < n) {
                 if (NC > 1) {
-                    const float* yr = Yr + tr * RS;
+                    const float* yr = Yr + tr * RS + (CW * hq) % 32;
 #pragma unroll
-                    for (int q = 0; q < 32; q += 4) {
+                    for (int q = 0; q < CW; q += 4) {
                         const float4 w = *reinterpret_cast<const float4*>(yr + q);
                         yw[q] += w.x; yw[q + 1] += w.y; yw[q + 2] += w.z; yw[q + 3] += w.w;
                     }
                 }
-                store_y32<Tout>(y + (t0 + tr) * D + 32 * hf, yw);
-            }
-        }
-        // ---- the new state: bf16 operand copies for the next chunk, or the result
-        {
-            const bool last = c + 1 == nchunks;
-            float w[32];
-#pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                const uint32_t col = (m == 0 ? COL_W1 : m == 1 ? COL_S1 : m == 2 ? COL_W2 : COL_S2) + 32 * hf;
-                tmem_ld32(tl + col, w);
-                if (!last) {
-                    const uint32_t off = m == 0 ? OFF_W1 : m == 1 ? OFF_S1 : m == 2 ? OFF_W2 : OFF_S2;
-                    put_row32(sm + off, 128, jr, 32 * hf, w);
-                } else {
-                    float* dst = (m & 1) ? a.S_T + unit * P : a.M_T + unit * P;
-                    if (m < 2) {
-                        float* r = dst + (long long)j_glob * D + 32 * hf;
-#pragma unroll
-                        for (int q = 0; q < 32; q += 4)
-                            *reinterpret_cast<float4*>(r + q) = make_float4(w[q], w[q + 1], w[q + 2], w[q + 3]);
-                    } else {
-                        float* r = dst + (long long)hid * D + j_glob;
-#pragma unroll
-                        for (int q = 0; q < 32; ++q) r[(long long)(32 * hf + q) * hid] = w[q];
-                    }
-                }
+                store_y<CW>(y + (t0 + tr) * D + CW * hq, yw);
             }
         }
         handoff();
@@ -659,19 +673,19 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (warp == 0) tmem_dealloc(tm, 512);
 }
 
-template <int NC, typename Tout>
+template <int NC, int CW, typename Tout>
 cudaError_t launch(const nm_config& c, const nm_args& a, cudaStream_t s) {
     CUtensorMap tq, tk, tv;
     const long long units = (long long)a.B * a.H;
     if (!make_token_map(&tq, a.q, D, a.T, units) || !make_token_map(&tk, a.k, D, a.T, units) ||
         !make_token_map(&tv, a.v, D, a.T, units))
         return cudaErrorInvalidValue;
-    auto kern = tc_mlp_kernel<NC, Tout>;
+    auto kern = tc_mlp_kernel<NC, CW, Tout>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(units * NC), 1, 1);
-    cfg.blockDim = dim3(NTHREADS, 1, 1);
+    cfg.blockDim = dim3(128 * (64 / CW), 1, 1);
     cfg.dynamicSmemBytes = SMEM_BYTES;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
@@ -688,7 +702,8 @@ cudaError_t launch(const nm_config& c, const nm_args& a, cudaStream_t s) {
 
 template <int NC>
 cudaError_t launch_nc(const nm_config& c, const nm_args& a, cudaStream_t s) {
-    return c.out_dtype == NM_BF16 ? launch<NC, __nv_bfloat16>(c, a, s) : launch<NC, float>(c, a, s);
+    return c.out_dtype == NM_BF16 ? launch<NC, CW_DEFAULT, __nv_bfloat16>(c, a, s)
+                                  : launch<NC, CW_DEFAULT, float>(c, a, s);
 }
 
 }  // namespace

@@ -73,6 +73,19 @@ __device__ __forceinline__ void put_row32(unsigned char* tile, uint32_t rows, ui
     }
 }
 
+// Writes W (16 or 32) fp32 values, columns c0..c0+W-1 of row r (c0 a
+// multiple of 8), as bf16 into a 128-byte-swizzled tile with `rows` rows.
+template <int W>
+__device__ __forceinline__ void put_row(unsigned char* tile, uint32_t rows, uint32_t r, uint32_t c0, const float* v) {
+    const uint32_t base = smem_u32(tile);
+#pragma unroll
+    for (int q = 0; q < W / 8; ++q) {
+        const uint32_t off = sw128_offset(r, c0 + 8 * q, rows);
+        st_shared_v4(base + off, pack_bf16(v[8 * q], v[8 * q + 1]), pack_bf16(v[8 * q + 2], v[8 * q + 3]),
+                     pack_bf16(v[8 * q + 4], v[8 * q + 5]), pack_bf16(v[8 * q + 6], v[8 * q + 7]));
+    }
+}
+
 // ------------------------------------------------------------------ mbarrier
 
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
@@ -235,6 +248,80 @@ __device__ __forceinline__ void tmem_ld32x3(uint32_t a0, uint32_t a1, uint32_t a
         "tcgen05.wait::ld.sync.aligned;\n"
         : "=f"(r0[0]), "=f"(r0[1]), "=f"(r0[2]), "=f"(r0[3]), "=f"(r0[4]), "=f"(r0[5]), "=f"(r0[6]), "=f"(r0[7]), "=f"(r0[8]), "=f"(r0[9]), "=f"(r0[10]), "=f"(r0[11]), "=f"(r0[12]), "=f"(r0[13]), "=f"(r0[14]), "=f"(r0[15]), "=f"(r0[16]), "=f"(r0[17]), "=f"(r0[18]), "=f"(r0[19]), "=f"(r0[20]), "=f"(r0[21]), "=f"(r0[22]), "=f"(r0[23]), "=f"(r0[24]), "=f"(r0[25]), "=f"(r0[26]), "=f"(r0[27]), "=f"(r0[28]), "=f"(r0[29]), "=f"(r0[30]), "=f"(r0[31]), "=f"(r1[0]), "=f"(r1[1]), "=f"(r1[2]), "=f"(r1[3]), "=f"(r1[4]), "=f"(r1[5]), "=f"(r1[6]), "=f"(r1[7]), "=f"(r1[8]), "=f"(r1[9]), "=f"(r1[10]), "=f"(r1[11]), "=f"(r1[12]), "=f"(r1[13]), "=f"(r1[14]), "=f"(r1[15]), "=f"(r1[16]), "=f"(r1[17]), "=f"(r1[18]), "=f"(r1[19]), "=f"(r1[20]), "=f"(r1[21]), "=f"(r1[22]), "=f"(r1[23]), "=f"(r1[24]), "=f"(r1[25]), "=f"(r1[26]), "=f"(r1[27]), "=f"(r1[28]), "=f"(r1[29]), "=f"(r1[30]), "=f"(r1[31]), "=f"(r2[0]), "=f"(r2[1]), "=f"(r2[2]), "=f"(r2[3]), "=f"(r2[4]), "=f"(r2[5]), "=f"(r2[6]), "=f"(r2[7]), "=f"(r2[8]), "=f"(r2[9]), "=f"(r2[10]), "=f"(r2[11]), "=f"(r2[12]), "=f"(r2[13]), "=f"(r2[14]), "=f"(r2[15]), "=f"(r2[16]), "=f"(r2[17]), "=f"(r2[18]), "=f"(r2[19]), "=f"(r2[20]), "=f"(r2[21]), "=f"(r2[22]), "=f"(r2[23]), "=f"(r2[24]), "=f"(r2[25]), "=f"(r2[26]), "=f"(r2[27]), "=f"(r2[28]), "=f"(r2[29]), "=f"(r2[30]), "=f"(r2[31])
         : "r"(a0), "r"(a1), "r"(a2)
+        : "memory");
+}
+
+
+// ---- width-generic TMEM access: 16 or 32 consecutive fp32 columns of this
+// warp's 32 lanes (one lane per thread).  tmem_ld_n with several addresses
+// issues all loads and waits once, in one asm statement, so that no register
+// is read before the wait.
+__device__ __forceinline__ void tmem_ld_n(uint32_t a0, float (&r0)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n\t"
+        "tcgen05.wait::ld.sync.aligned;\n"
+        : "=f"(r0[0]), "=f"(r0[1]), "=f"(r0[2]), "=f"(r0[3]), "=f"(r0[4]), "=f"(r0[5]), "=f"(r0[6]), "=f"(r0[7]), "=f"(r0[8]), "=f"(r0[9]), "=f"(r0[10]), "=f"(r0[11]), "=f"(r0[12]), "=f"(r0[13]), "=f"(r0[14]), "=f"(r0[15])
+        : "r"(a0)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_ld_n(uint32_t a0, uint32_t a1, float (&r0)[16], float (&r1)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%32];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%33];\n\t"
+        "tcgen05.wait::ld.sync.aligned;\n"
+        : "=f"(r0[0]), "=f"(r0[1]), "=f"(r0[2]), "=f"(r0[3]), "=f"(r0[4]), "=f"(r0[5]), "=f"(r0[6]), "=f"(r0[7]), "=f"(r0[8]), "=f"(r0[9]), "=f"(r0[10]), "=f"(r0[11]), "=f"(r0[12]), "=f"(r0[13]), "=f"(r0[14]), "=f"(r0[15]), "=f"(r1[0]), "=f"(r1[1]), "=f"(r1[2]), "=f"(r1[3]), "=f"(r1[4]), "=f"(r1[5]), "=f"(r1[6]), "=f"(r1[7]), "=f"(r1[8]), "=f"(r1[9]), "=f"(r1[10]), "=f"(r1[11]), "=f"(r1[12]), "=f"(r1[13]), "=f"(r1[14]), "=f"(r1[15])
+        : "r"(a0), "r"(a1)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_ld_n(uint32_t a0, uint32_t a1, uint32_t a2, float (&r0)[16], float (&r1)[16], float (&r2)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%48];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%49];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47}, [%50];\n\t"
+        "tcgen05.wait::ld.sync.aligned;\n"
+        : "=f"(r0[0]), "=f"(r0[1]), "=f"(r0[2]), "=f"(r0[3]), "=f"(r0[4]), "=f"(r0[5]), "=f"(r0[6]), "=f"(r0[7]), "=f"(r0[8]), "=f"(r0[9]), "=f"(r0[10]), "=f"(r0[11]), "=f"(r0[12]), "=f"(r0[13]), "=f"(r0[14]), "=f"(r0[15]), "=f"(r1[0]), "=f"(r1[1]), "=f"(r1[2]), "=f"(r1[3]), "=f"(r1[4]), "=f"(r1[5]), "=f"(r1[6]), "=f"(r1[7]), "=f"(r1[8]), "=f"(r1[9]), "=f"(r1[10]), "=f"(r1[11]), "=f"(r1[12]), "=f"(r1[13]), "=f"(r1[14]), "=f"(r1[15]), "=f"(r2[0]), "=f"(r2[1]), "=f"(r2[2]), "=f"(r2[3]), "=f"(r2[4]), "=f"(r2[5]), "=f"(r2[6]), "=f"(r2[7]), "=f"(r2[8]), "=f"(r2[9]), "=f"(r2[10]), "=f"(r2[11]), "=f"(r2[12]), "=f"(r2[13]), "=f"(r2[14]), "=f"(r2[15])
+        : "r"(a0), "r"(a1), "r"(a2)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_ld_n(uint32_t a0, float (&r0)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n\t"
+        "tcgen05.wait::ld.sync.aligned;\n"
+        : "=f"(r0[0]), "=f"(r0[1]), "=f"(r0[2]), "=f"(r0[3]), "=f"(r0[4]), "=f"(r0[5]), "=f"(r0[6]), "=f"(r0[7]), "=f"(r0[8]), "=f"(r0[9]), "=f"(r0[10]), "=f"(r0[11]), "=f"(r0[12]), "=f"(r0[13]), "=f"(r0[14]), "=f"(r0[15]), "=f"(r0[16]), "=f"(r0[17]), "=f"(r0[18]), "=f"(r0[19]), "=f"(r0[20]), "=f"(r0[21]), "=f"(r0[22]), "=f"(r0[23]), "=f"(r0[24]), "=f"(r0[25]), "=f"(r0[26]), "=f"(r0[27]), "=f"(r0[28]), "=f"(r0[29]), "=f"(r0[30]), "=f"(r0[31])
+        : "r"(a0)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_ld_n(uint32_t a0, uint32_t a1, float (&r0)[32], float (&r1)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%64];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%65];\n\t"
+        "tcgen05.wait::ld.sync.aligned;\n"
+        : "=f"(r0[0]), "=f"(r0[1]), "=f"(r0[2]), "=f"(r0[3]), "=f"(r0[4]), "=f"(r0[5]), "=f"(r0[6]), "=f"(r0[7]), "=f"(r0[8]), "=f"(r0[9]), "=f"(r0[10]), "=f"(r0[11]), "=f"(r0[12]), "=f"(r0[13]), "=f"(r0[14]), "=f"(r0[15]), "=f"(r0[16]), "=f"(r0[17]), "=f"(r0[18]), "=f"(r0[19]), "=f"(r0[20]), "=f"(r0[21]), "=f"(r0[22]), "=f"(r0[23]), "=f"(r0[24]), "=f"(r0[25]), "=f"(r0[26]), "=f"(r0[27]), "=f"(r0[28]), "=f"(r0[29]), "=f"(r0[30]), "=f"(r0[31]), "=f"(r1[0]), "=f"(r1[1]), "=f"(r1[2]), "=f"(r1[3]), "=f"(r1[4]), "=f"(r1[5]), "=f"(r1[6]), "=f"(r1[7]), "=f"(r1[8]), "=f"(r1[9]), "=f"(r1[10]), "=f"(r1[11]), "=f"(r1[12]), "=f"(r1[13]), "=f"(r1[14]), "=f"(r1[15]), "=f"(r1[16]), "=f"(r1[17]), "=f"(r1[18]), "=f"(r1[19]), "=f"(r1[20]), "=f"(r1[21]), "=f"(r1[22]), "=f"(r1[23]), "=f"(r1[24]), "=f"(r1[25]), "=f"(r1[26]), "=f"(r1[27]), "=f"(r1[28]), "=f"(r1[29]), "=f"(r1[30]), "=f"(r1[31])
+        : "r"(a0), "r"(a1)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_ld_n(uint32_t a0, uint32_t a1, uint32_t a2, float (&r0)[32], float (&r1)[32], float (&r2)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%96];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%97];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%64,%65,%66,%67,%68,%69,%70,%71,%72,%73,%74,%75,%76,%77,%78,%79,%80,%81,%82,%83,%84,%85,%86,%87,%88,%89,%90,%91,%92,%93,%94,%95}, [%98];\n\t"
+        "tcgen05.wait::ld.sync.aligned;\n"
+        : "=f"(r0[0]), "=f"(r0[1]), "=f"(r0[2]), "=f"(r0[3]), "=f"(r0[4]), "=f"(r0[5]), "=f"(r0[6]), "=f"(r0[7]), "=f"(r0[8]), "=f"(r0[9]), "=f"(r0[10]), "=f"(r0[11]), "=f"(r0[12]), "=f"(r0[13]), "=f"(r0[14]), "=f"(r0[15]), "=f"(r0[16]), "=f"(r0[17]), "=f"(r0[18]), "=f"(r0[19]), "=f"(r0[20]), "=f"(r0[21]), "=f"(r0[22]), "=f"(r0[23]), "=f"(r0[24]), "=f"(r0[25]), "=f"(r0[26]), "=f"(r0[27]), "=f"(r0[28]), "=f"(r0[29]), "=f"(r0[30]), "=f"(r0[31]), "=f"(r1[0]), "=f"(r1[1]), "=f"(r1[2]), "=f"(r1[3]), "=f"(r1[4]), "=f"(r1[5]), "=f"(r1[6]), "=f"(r1[7]), "=f"(r1[8]), "=f"(r1[9]), "=f"(r1[10]), "=f"(r1[11]), "=f"(r1[12]), "=f"(r1[13]), "=f"(r1[14]), "=f"(r1[15]), "=f"(r1[16]), "=f"(r1[17]), "=f"(r1[18]), "=f"(r1[19]), "=f"(r1[20]), "=f"(r1[21]), "=f"(r1[22]), "=f"(r1[23]), "=f"(r1[24]), "=f"(r1[25]), "=f"(r1[26]), "=f"(r1[27]), "=f"(r1[28]), "=f"(r1[29]), "=f"(r1[30]), "=f"(r1[31]), "=f"(r2[0]), "=f"(r2[1]), "=f"(r2[2]), "=f"(r2[3]), "=f"(r2[4]), "=f"(r2[5]), "=f"(r2[6]), "=f"(r2[7]), "=f"(r2[8]), "=f"(r2[9]), "=f"(r2[10]), "=f"(r2[11]), "=f"(r2[12]), "=f"(r2[13]), "=f"(r2[14]), "=f"(r2[15]), "=f"(r2[16]), "=f"(r2[17]), "=f"(r2[18]), "=f"(r2[19]), "=f"(r2[20]), "=f"(r2[21]), "=f"(r2[22]), "=f"(r2[23]), "=f"(r2[24]), "=f"(r2[25]), "=f"(r2[26]), "=f"(r2[27]), "=f"(r2[28]), "=f"(r2[29]), "=f"(r2[30]), "=f"(r2[31])
+        : "r"(a0), "r"(a1), "r"(a2)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_st_n(uint32_t taddr, const float (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};\n\t"
+        "tcgen05.wait::st.sync.aligned;\n" ::"r"(taddr),
+        "f"(r[0]), "f"(r[1]), "f"(r[2]), "f"(r[3]), "f"(r[4]), "f"(r[5]), "f"(r[6]), "f"(r[7]), "f"(r[8]), "f"(r[9]), "f"(r[10]), "f"(r[11]), "f"(r[12]), "f"(r[13]), "f"(r[14]), "f"(r[15])
+        : "memory");
+}
+__device__ __forceinline__ void tmem_st_n(uint32_t taddr, const float (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};\n\t"
+        "tcgen05.wait::st.sync.aligned;\n" ::"r"(taddr),
+        "f"(r[0]), "f"(r[1]), "f"(r[2]), "f"(r[3]), "f"(r[4]), "f"(r[5]), "f"(r[6]), "f"(r[7]), "f"(r[8]), "f"(r[9]), "f"(r[10]), "f"(r[11]), "f"(r[12]), "f"(r[13]), "f"(r[14]), "f"(r[15]), "f"(r[16]), "f"(r[17]), "f"(r[18]), "f"(r[19]), "f"(r[20]), "f"(r[21]), "f"(r[22]), "f"(r[23]), "f"(r[24]), "f"(r[25]), "f"(r[26]), "f"(r[27]), "f"(r[28]), "f"(r[29]), "f"(r[30]), "f"(r[31])
         : "memory");
 }
 
