@@ -169,11 +169,12 @@ class ClockSampler:
 
 # --------------------------------------------------------------------- oracle timing
 
-def time_oracle(wl, x, budget_s: float = 12.0):
-    """The fp64 oracle, as it stands, on a bounded sample of the workload:
-    whole units (all T tokens of a unit when it fits the budget, else the
-    first tokens of one unit per core).  Returns tokens/s, cores, sample."""
-    import numpy as np
+def time_oracle(wl, x, budget_s: float = 15.0):
+    """The fp64 oracle, as it stands, on a bounded sample of the workload
+    sized to about ``budget_s`` seconds: whole units (all T tokens when one
+    round of units fits the budget, else a prefix of T), as many units as
+    fit up to B*H, repeated while the budget allows.  Returns tokens/s (all
+    units and repeats over the summed wall time), cores and the sample."""
     import oracle
 
     cores = len(os.sched_getaffinity(0))
@@ -190,18 +191,25 @@ def time_oracle(wl, x, budget_s: float = 12.0):
         oracle.forward(wl.kind, wl.d, wl.hidden, wl.chunk, oracle.C_ONE, *args)
         return time.perf_counter() - t0
 
-    # calibrate on one chunk's worth of tokens per core
+    # calibrate on one round of units (one per core) over a few chunks
     units = min(BH, cores)
     Tc = min(wl.T, max(wl.chunk, 256))
-    dt = run(prep(units, Tc))
-    per_tok = dt / (units * Tc)  # wall seconds per token at this parallelism
-    T = wl.T if per_tok * units * wl.T <= budget_s else max(wl.chunk, int(budget_s / (per_tok * units)) // wl.chunk * wl.chunk)
-    T = min(T, wl.T)
+    per_tok = run(prep(units, Tc)) / (units * Tc)  # wall seconds per token at this parallelism
+    if per_tok * units * wl.T > budget_s:  # a prefix of T for one round of units
+        T = max(wl.chunk, int(budget_s / (per_tok * units)) // wl.chunk * wl.chunk)
+        T = min(T, wl.T)
+        reps = 1
+    else:  # whole units: more rounds of units, then repeats
+        T = wl.T
+        rounds = max(1, min(-(-BH // units), int(budget_s / (per_tok * units * T))))
+        units = min(BH, rounds * units)
+        reps = max(1, int(budget_s / (per_tok * units * T)))
     args = prep(units, T)
-    dt = run(args)
-    tokens = units * T
+    dt = sum(run(args) for _ in range(reps))
+    tokens = units * T * reps
     return {"value": tokens / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-            "sample": "%d units x %d tokens of the workload (fp64, OpenMP over units), %.1f s" % (units, T, dt),
+            "sample": "%d units x %d tokens of the workload, %d run(s) (fp64, OpenMP over units), %.1f s"
+                      % (units, T, reps, dt),
             "seconds": dt, "tokens": tokens}
 
 
