@@ -1,4 +1,5 @@
-// tcgen05 tensor-core kernel for the linear memory, d = 128, chunk b = 64.
+// tcgen05 tensor-core kernel for the linear memory M(x) = M x, d = 128,
+// chunk b = 64.
 //
 // One persistent CTA per (batch, head) unit walks the sequence chunk by
 // chunk ("Titans: Imparare a Memorizzare al Tempo di Test", section
@@ -10,27 +11,31 @@
 // With a_t = 1 - alpha_t and, inside a chunk of n tokens,
 //   A_t = prod_{j<=t} a_j,  B_t = prod_{j<=t} beta_j,
 //   sigma_t = a_t sigma_{t-1} + eta_t B_t,
-//   Gamma_{t,i} = c_i sum_{j=i..t} (prod_{l=j+1..t} a_l) eta_j (prod_{l=i+1..j} beta_l),
-//   gamma_i = Gamma_{n-1,i},  u_i = c_i prod_{l=i+1..n-1} beta_l,
-// and E = 2 (K W0^T - V) (one row per token), the chunk is
-//   Y^T   = M0 Q^T diag(A) - S0 Q^T diag(sigma) - E^T (Gamma (.) Q K^T)^T
-//   M_end = A_{n-1} M0 - sigma_{n-1} S0 - E^T diag(gamma) K
-//   S_end = B_{n-1} S0 + E^T diag(u) K.
-// Gamma is built per row by a division-free recursion over i = t, t-1, ..., 0:
-//   R <- eta_t;  R <- (prod a) eta_i + beta_{i+1} R;  Gamma_{t,i} = c_i R,
-// so beta = 0 and alpha = 1 are exact.
+//   Gamma_{t,i} = a_t Gamma_{t-1,i} + eta_t u_{t,i},  u_{t,i} = c_i prod_{l=i+1..t} beta_l,
+//   gamma_i = Gamma_{n-1,i},  u_i = u_{n-1,i},
+// and e_t = 2 (M0 k_t - v_t) (the gradient of ||M k_t - v_t||^2 at M0 is
+// e_t k_t^T), the chunk is
+//   y_t   = A_t M0 q_t - sigma_t S0 q_t - sum_{i<=t} Gamma_{t,i} (q_t . k_i) e_i
+//   M_end = A_{n-1} M0 - sigma_{n-1} S0 - sum_i gamma_i e_i k_i^T
+//   S_end = B_{n-1} S0 + sum_i u_i e_i k_i^T.
+// Gamma is built column by column with the division-free recursion, so
+// beta = 0 and alpha = 1 are exact.
 //
-// Data placement (one CTA, 4 warps; thread 0 issues TMA and MMA):
-//   TMEM (512 columns x 128 lanes, fp32): M [lane o][col i] 0..127,
-//     S 128..255, E^T accumulator 256..319, M0 Q^T 320..383, S0 Q^T 384..447,
-//     Q K^T (M=64 layout) then E^T P^T 448..511.
-//   SMEM: Q, K, V tiles (TMA, 128-byte swizzle, double-buffered), bf16
-//     copies of M and S (the state as a tensor-core operand), E^T, -E^T
-//     diag(gamma), E^T diag(u), P = Gamma (.) Q K^T, gates and scan values.
-// The state never leaves the chip between chunks; HBM traffic is the q, k,
-// v tiles in, y out, the gates, and the state once in and once out.
+// Per CTA (256 threads; thread 0 issues TMA and MMA):
+//   TMEM (128 lanes x 512 fp32 columns): M [o][i] in 0..127 and S in 128..255
+//     for the whole sequence; per chunk the key forward yhat [t][o] (M=64
+//     layout, 256..383), Q K^T [t][i] (M=64, 384..447), M0 q [o][t] (448..511),
+//     then S0 q [o][t] (256..319) and sum_i P[t][i] e_i [o][t] (320..383).
+//   SMEM: Q and K tiles double-buffered and V single-buffered (TMA, 128-byte
+//     swizzle), bf16 copies of M and S (the state as a tensor-core operand),
+//     E, -gamma E, u E as [t][o] tiles, P = Gamma (.) Q K^T, Gamma in fp32.
+// Per chunk two MMA batches: (1) yhat = K M0^T, Q K^T, M0 Q^T; then e, P and
+// the scaled e tiles; (2) S0 Q^T, E^T P^T and the two state updates; then y
+// and the next chunk's bf16 state.  The fp32 state is rescaled in TMEM
+// (M <- A_n M - sigma_n S, S <- B_n S) while batch (1) runs.  The state never
+// leaves the chip between chunks; HBM traffic is q, k, v in, y out, the gates,
+// and the state once in and once out.
 #include <cuda_bf16.h>
-#include <cudaTypedefs.h>
 
 #include "nm_internal.h"
 #include "tc_common.cuh"
@@ -41,30 +46,70 @@ using namespace tc;
 
 constexpr int D = 128;
 constexpr int BC = 64;
-constexpr int NTHREADS = 128;
-constexpr uint32_t HALF = BC * 128;       // one 64-column block of a 64-row tile
-constexpr uint32_t TILE = 2 * HALF;       // 64 tokens x 128 features, bf16
-constexpr uint32_t OFF_Q = 0;
-constexpr uint32_t OFF_K = OFF_Q + 2 * TILE;
+constexpr int NTHREADS = 256;
+constexpr uint32_t HALF = BC * 128;   // one 64-column block of a 64-row bf16 tile (8 KB)
+constexpr uint32_t TILE = 2 * HALF;   // 64 tokens x 128 features, bf16 (16 KB)
+constexpr uint32_t SBLK = 128 * 128;  // one 64-column block of a 128-row tile (16 KB)
+
+constexpr uint32_t OFF_Q = 0;                    // 2 stages
+constexpr uint32_t OFF_K = OFF_Q + 2 * TILE;     // 2 stages
 constexpr uint32_t OFF_V = OFF_K + 2 * TILE;
-constexpr uint32_t OFF_MH = OFF_V + 2 * TILE;  // [128][128] bf16: two 16 KB blocks
-constexpr uint32_t OFF_SH = OFF_MH + 32768;
-constexpr uint32_t OFF_ET = OFF_SH + 32768;    // [128][64] bf16
-constexpr uint32_t OFF_EG = OFF_ET + 16384;
-constexpr uint32_t OFF_EU = OFF_EG + 16384;
-constexpr uint32_t OFF_P = OFF_EU + 16384;     // [64][64] bf16
-constexpr uint32_t OFF_F = OFF_P + 8192;       // floats
-constexpr uint32_t N_FLOATS = 2 * 4 * BC + 5 * BC;
-constexpr uint32_t OFF_BAR = OFF_F + 4 * N_FLOATS;
+constexpr uint32_t OFF_MH = OFF_V + TILE;        // [128 o][128 i] bf16: two 16 KB column blocks
+constexpr uint32_t OFF_SH = OFF_MH + 2 * SBLK;
+constexpr uint32_t OFF_E = OFF_SH + 2 * SBLK;    // [64 t][128 o] bf16
+constexpr uint32_t OFF_EG = OFF_E + TILE;        // -gamma_t e_t
+constexpr uint32_t OFF_EU = OFF_EG + TILE;       // u_t e_t
+constexpr uint32_t OFF_P = OFF_EU + TILE;        // [64 t][64 i] bf16
+constexpr int GS = 68;                           // padded fp32 row stride of Gamma
+constexpr uint32_t OFF_GM = OFF_P + HALF;
+constexpr uint32_t OFF_F = OFF_GM + 64 * GS * 4; // gates [2][4][64], A, B, sigma, gamma, u
+constexpr uint32_t N_F = 2 * 4 * BC + 5 * BC;
+constexpr uint32_t OFF_BAR = OFF_F + 4 * N_F;
 constexpr uint32_t SMEM_USED = OFF_BAR + 64;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;  // slack for 1024-byte alignment
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
-constexpr uint32_t COL_M = 0, COL_S = 128, COL_E = 256, COL_Y1 = 320, COL_Y2 = 384, COL_QK = 448;
-constexpr uint32_t ID_128x64 = idesc_bf16_f32(128, 64, false, false);
-constexpr uint32_t ID_64x64 = idesc_bf16_f32(64, 64, false, false);
-constexpr uint32_t ID_128x128_BMN = idesc_bf16_f32(128, 128, false, true);
+constexpr uint32_t COL_M = 0, COL_S = 128;
+constexpr uint32_t COL_YH = 256, COL_QK = 384, COL_Y1 = 448;  // batch 1
+constexpr uint32_t COL_Y2 = 256, COL_PE = 320;                // batch 2
+constexpr uint32_t ID_YH = idesc_bf16_f32(64, 128, false, false);
+constexpr uint32_t ID_QK = idesc_bf16_f32(64, 64, false, false);
+constexpr uint32_t ID_Y = idesc_bf16_f32(128, 64, false, false);
+constexpr uint32_t ID_PE = idesc_bf16_f32(128, 64, true, false);
+constexpr uint32_t ID_UPD = idesc_bf16_f32(128, 128, true, true);
 constexpr uint64_t WAIT_NS = 2000000000ull;  // 2 s
+
+// Shared-memory descriptors (the sw128_desc fields), K-major and MN-major
+// with 64-element blocks `lbo` bytes apart.  The start-address field keeps
+// bits 4..17 of the address (shared::cta addresses may carry higher bits).
+// A k-step adds to the descriptor directly: +2 for 32 bytes (K-major), +128
+// for 2048 bytes (16 rows, MN-major).
+constexpr uint64_t desc_hi(uint32_t lbo) {
+    return (static_cast<uint64_t>(lbo >> 4) << 16) | (static_cast<uint64_t>(1024 >> 4) << 32) | (1ull << 46) |
+           (2ull << 61);
+}
+__device__ __forceinline__ uint64_t kdesc(uint32_t a) { return desc_hi(16) | ((a >> 4) & 0x3FFFu); }
+__device__ __forceinline__ uint64_t mdesc(uint32_t a, uint32_t lbo) { return desc_hi(lbo) | ((a >> 4) & 0x3FFFu); }
+constexpr uint64_t KS_K = 2, KS_M = 128;
+
+__device__ __forceinline__ float momentum_c(int mode, float beta, const float* c, long long i) {
+    if (mode == NM_C_ONE_MINUS_BETA) return 1.0f - beta;
+    if (mode == NM_C_PER_TOKEN) return c[i];
+    return 1.0f;
+}
+
+// 32 bf16 of row r, columns c0..c0+31, of a swizzled tile, as floats.
+__device__ __forceinline__ void get_row32(const unsigned char* tile, uint32_t rows, uint32_t r, uint32_t c0, float* v) {
+    const uint32_t base = smem_u32(tile);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const uint4 w = ld_shared_v4(base + sw128_offset(r, c0 + 8 * q, rows));
+        v[8 * q + 0] = bf16_lo(w.x); v[8 * q + 1] = bf16_hi(w.x);
+        v[8 * q + 2] = bf16_lo(w.y); v[8 * q + 3] = bf16_hi(w.y);
+        v[8 * q + 4] = bf16_lo(w.z); v[8 * q + 5] = bf16_hi(w.z);
+        v[8 * q + 6] = bf16_lo(w.w); v[8 * q + 7] = bf16_hi(w.w);
+    }
+}
 
 template <typename Tout>
 __device__ __forceinline__ void store_y(Tout* p, float x);
@@ -72,12 +117,6 @@ template <>
 __device__ __forceinline__ void store_y<__nv_bfloat16>(__nv_bfloat16* p, float x) { *p = __float2bfloat16_rn(x); }
 template <>
 __device__ __forceinline__ void store_y<float>(float* p, float x) { *p = x; }
-
-__device__ __forceinline__ float momentum_c(int mode, float beta, const float* c, long long i) {
-    if (mode == NM_C_ONE_MINUS_BETA) return 1.0f - beta;
-    if (mode == NM_C_PER_TOKEN) return c[i];
-    return 1.0f;
-}
 
 template <typename Tout>
 __global__ void __launch_bounds__(NTHREADS, 1)
@@ -91,12 +130,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     float* sSg = sBc + BC;
     float* sGl = sSg + BC;
     float* sU = sGl + BC;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + OFF_BAR);  // 0,1: tile stages; 2: mma
+    float* Gm = reinterpret_cast<float*>(sm + OFF_GM);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + OFF_BAR);  // 0,1: Q|K stages; 2: V; 3: mma
     __shared__ uint32_t s_tmem;
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
+    const int qd = warp & 3;   // TMEM lane quadrant
+    const int hf = warp >> 2;  // which half of the columns this thread handles
     const long long unit = blockIdx.x;
     const long long T = a.T;
     const long long P = (long long)D * D;
@@ -106,11 +148,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const float* beta = a.beta + unit * T;
     const float* cc = a.c ? a.c + unit * T : nullptr;
     Tout* y = reinterpret_cast<Tout*>(a.y) + unit * T * D;
+    const int orow = 32 * qd + lane;  // row of an M=128 accumulator: output feature o
+    const int tr = 16 * qd + lane;    // row of an M=64 accumulator: token (valid for lane < 16)
+    const bool r64 = lane < 16;
 
     if (tid == 0) {
-        mbar_init(&bars[0], 1);
-        mbar_init(&bars[1], 1);
-        mbar_init(&bars[2], 1);
+        for (int i = 0; i < 4; ++i) mbar_init(&bars[i], 1);
         fence_mbar_init();
         prefetch_tmap(&tq);
         prefetch_tmap(&tk);
@@ -120,64 +163,60 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tmem_alloc(&s_tmem, 512);
         tmem_relinquish();
     }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tm = s_tmem;
-    const uint32_t lb = (uint32_t)(warp * 32) << 16;  // this warp's TMEM lane quadrant
-
-    auto issue_tiles = [&](int chunk, int stage) {
-        mbar_arrive_expect_tx(&bars[stage], 3 * TILE);
+    auto issue_qk = [&](int chunk, int stage) {
+        mbar_arrive_expect_tx(&bars[stage], 2 * TILE);
         const int t0 = chunk * BC;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             tma_load_3d(sm + OFF_Q + stage * TILE + h * HALF, &tq, &bars[stage], h * 64, t0, (int)unit);
             tma_load_3d(sm + OFF_K + stage * TILE + h * HALF, &tk, &bars[stage], h * 64, t0, (int)unit);
-            tma_load_3d(sm + OFF_V + stage * TILE + h * HALF, &tv, &bars[stage], h * 64, t0, (int)unit);
         }
     };
-    auto load_gates = [&](int chunk, int stage) {
-        if (tid < BC) {
-            const long long t = (long long)chunk * BC + tid;
-            float* g = gates + stage * 4 * BC;
-            if (t < T) {
-                const float b = beta[t];
-                g[tid] = 1.0f - alpha[t];
-                g[BC + tid] = eta[t];
-                g[2 * BC + tid] = b;
-                g[3 * BC + tid] = momentum_c(c_mode, b, cc, t);
-            } else {
-                g[tid] = 1.0f;
-                g[BC + tid] = 0.0f;
-                g[2 * BC + tid] = 0.0f;
-                g[3 * BC + tid] = 0.0f;
-            }
-        }
+    auto issue_v = [&](int chunk) {
+        mbar_arrive_expect_tx(&bars[2], TILE);
+        const int t0 = chunk * BC;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) tma_load_3d(sm + OFF_V + h * HALF, &tv, &bars[2], h * 64, t0, (int)unit);
     };
+    if (tid < BC) {  // gates of chunk 0; tokens past T change nothing: a = 1, eta = 0, beta = 1, c = 0
+        const long long t = tid;
+        float* g = gates;
+        const bool ok = t < T;
+        const float b = ok ? beta[t] : 1.0f;
+        g[tid] = ok ? 1.0f - alpha[t] : 1.0f;
+        g[BC + tid] = ok ? eta[t] : 0.0f;
+        g[2 * BC + tid] = b;
+        g[3 * BC + tid] = ok ? momentum_c(c_mode, b, cc, t) : 0.0f;
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tm = s_tmem;
+    const uint32_t tl = tm + ((uint32_t)(32 * qd) << 16);  // this warp's lane quadrant
+    if (tid == 0 && nchunks > 0) {
+        issue_qk(0, 0);
+        issue_v(0);
+    }
 
-    if (tid == 0 && nchunks > 0) issue_tiles(0, 0);
-    load_gates(0, 0);
     // initial state: TMEM fp32 (lane o = row o of M, S) and bf16 operand copies
     {
         float r[32];
-        const float* m0 = a.M0 + unit * P + (long long)tid * D;
-        const float* s0 = a.S0 + unit * P + (long long)tid * D;
+        const float* m0 = a.M0 + unit * P + (long long)orow * D;
+        const float* s0 = a.S0 + unit * P + (long long)orow * D;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
+        for (int which = 0; which < 2; ++which) {
+            const float* src = which ? s0 : m0;
 #pragma unroll
-            for (int q = 0; q < 32; q += 4) {
-                float4 w = *reinterpret_cast<const float4*>(m0 + 32 * j + q);
-                r[q] = w.x; r[q + 1] = w.y; r[q + 2] = w.z; r[q + 3] = w.w;
+            for (int j = 0; j < 2; ++j) {
+                const int c0 = 64 * hf + 32 * j;
+#pragma unroll
+                for (int q = 0; q < 32; q += 4) {
+                    const float4 w = *reinterpret_cast<const float4*>(src + c0 + q);
+                    r[q] = w.x; r[q + 1] = w.y; r[q + 2] = w.z; r[q + 3] = w.w;
+                }
+                tmem_st32(tl + (which ? COL_S : COL_M) + c0, r);
+                put_row32(sm + (which ? OFF_SH : OFF_MH), 128, orow, c0, r);
             }
-            tmem_st32(tm + lb + COL_M + 32 * j, r);
-            put_row32(sm + OFF_MH, 128, tid, 32 * j, r);
-#pragma unroll
-            for (int q = 0; q < 32; q += 4) {
-                float4 w = *reinterpret_cast<const float4*>(s0 + 32 * j + q);
-                r[q] = w.x; r[q + 1] = w.y; r[q + 2] = w.z; r[q + 3] = w.w;
-            }
-            tmem_st32(tm + lb + COL_S + 32 * j, r);
-            put_row32(sm + OFF_SH, 128, tid, 32 * j, r);
         }
     }
     fence_proxy_async();
@@ -185,195 +224,225 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     __syncthreads();
     tc_fence_after();
 
-    uint32_t mma_phase = 0;
+    const uint32_t aMH = smem_u32(sm + OFF_MH), aSH = smem_u32(sm + OFF_SH), aE = smem_u32(sm + OFF_E);
+    const uint32_t aEG = smem_u32(sm + OFF_EG), aEU = smem_u32(sm + OFF_EU), aP = smem_u32(sm + OFF_P);
+
     bool failed = false;
-    int c = 0;
-    for (; c < nchunks; ++c) {
+    uint32_t mma_phase = 0;
+    auto mma_wait = [&](bool committed) {  // bounded; uniform over the CTA
+        bool ok = true;
+        if (committed) {
+            ok = mbar_wait(&bars[3], mma_phase, WAIT_NS);
+            mma_phase ^= 1u;
+        }
+        failed = __syncthreads_or(!ok) || failed;
+        tc_fence_after();
+    };
+    auto handoff = [&]() {  // epilogue smem / TMEM writes -> tensor-core reads
+        fence_proxy_async();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+    };
+
+    for (int c = 0; c < nchunks; ++c) {
         const int stage = c & 1;
         const long long t0 = (long long)c * BC;
         const int n = (int)min((long long)BC, T - t0);
         const float* g = gates + stage * 4 * BC;
-        if (c + 1 < nchunks) {
-            if (tid == 0) issue_tiles(c + 1, stage ^ 1);
-            load_gates(c + 1, stage ^ 1);
+        const uint32_t aQ = smem_u32(sm + OFF_Q + stage * TILE), aK = smem_u32(sm + OFF_K + stage * TILE);
+
+        // the next chunk's gates: warps 2-3 load them now, raw, and store them after batch 1
+        const int gi = tid - 64;
+        const bool nxt_valid = gi >= 0 && gi < BC && c + 1 < nchunks && t0 + BC + gi < T;
+        float nxt_al = 0.0f, nxt_e = 0.0f, nxt_b = 1.0f, nxt_c = 0.0f;
+        if (nxt_valid) {
+            const long long t = t0 + BC + gi;
+            nxt_al = alpha[t];
+            nxt_e = eta[t];
+            nxt_b = beta[t];
+            if (c_mode == NM_C_PER_TOKEN) nxt_c = cc[t];
         }
-        // chunk scan: A, B, sigma (thread 0); gamma, u by the row recursion (thread 32)
-        if (tid == 0) {
-            float A = 1.f, Bc = 1.f, sg = 0.f;
-            for (int t = 0; t < n; ++t) {
-                A *= g[t];
-                Bc *= g[2 * BC + t];
-                sg = fmaf(g[t], sg, g[BC + t] * Bc);
-                sA[t] = A;
-                sBc[t] = Bc;
-                sSg[t] = sg;
-            }
-        }
-        if (tid == 32) {
-            float Dp = 1.f, R = g[BC + n - 1], Bp = 1.f;
-            sGl[n - 1] = g[3 * BC + n - 1] * R;
-            sU[n - 1] = g[3 * BC + n - 1];
-            for (int i = n - 2; i >= 0; --i) {
-                Dp *= g[i + 1];
-                R = fmaf(Dp, g[BC + i], g[2 * BC + i + 1] * R);
-                Bp *= g[2 * BC + i + 1];
-                sGl[i] = g[3 * BC + i] * R;
-                sU[i] = g[3 * BC + i] * Bp;
-            }
-            for (int i = n; i < BC; ++i) {
-                sGl[i] = 0.f;
-                sU[i] = 0.f;
-            }
-        }
-        // wait for this chunk's tiles
-        bool ok = mbar_wait(&bars[stage], (uint32_t)((c >> 1) & 1), WAIT_NS);
-        if (__syncthreads_or(!ok)) {
-            failed = true;
-            break;
-        }
-        const uint32_t qa = smem_u32(sm + OFF_Q + stage * TILE);
-        const uint32_t ka = smem_u32(sm + OFF_K + stage * TILE);
-        if (tid == 0) {
-            tc_fence_after();
-            const uint32_t mh = smem_u32(sm + OFF_MH), sh = smem_u32(sm + OFF_SH);
+
+        // ---- batch 1 (thread 0, as soon as the tiles land): yhat = K M0^T, Q K^T, M0 Q^T;
+        //      then the next chunk's Q|K tiles; meanwhile the gate scan
+        bool tiles_ok = true;
+        if (tid == 0 && !failed) {
+            tiles_ok = mbar_wait(&bars[stage], (uint32_t)((c >> 1) & 1), WAIT_NS) &&
+                       mbar_wait(&bars[2], (uint32_t)(c & 1), WAIT_NS);
+            if (tiles_ok) {
+                tc_fence_after();
+                const uint64_t dQ = kdesc(aQ), dK = kdesc(aK), dM = kdesc(aMH);
 #pragma unroll
-            for (int kb = 0; kb < 2; ++kb)
-#pragma unroll
-                for (int ks = 0; ks < 4; ++ks) {
-                    const uint32_t acc = (kb | ks) ? 1u : 0u;
-                    const uint32_t ko = kb * HALF + ks * 32;      // 64-row tiles
-                    const uint32_t mo = kb * 16384 + ks * 32;     // 128-row tiles
-                    mma_bf16(tm + COL_E, sw128_desc(mh + mo, 16, 1024), sw128_desc(ka + ko, 16, 1024), ID_128x64, acc);
-                    mma_bf16(tm + COL_Y1, sw128_desc(mh + mo, 16, 1024), sw128_desc(qa + ko, 16, 1024), ID_128x64, acc);
-                    mma_bf16(tm + COL_Y2, sw128_desc(sh + mo, 16, 1024), sw128_desc(qa + ko, 16, 1024), ID_128x64, acc);
-                    mma_bf16(tm + COL_QK, sw128_desc(qa + ko, 16, 1024), sw128_desc(ka + ko, 16, 1024), ID_64x64, acc);
+                for (int ks = 0; ks < 8; ++ks) {
+                    const uint32_t acc = ks ? 1u : 0u;
+                    // k-step ks covers features 16 ks .. 16 ks + 15: column block ks / 4 of each tile
+                    const uint64_t kt = (ks >> 2) * (HALF >> 4) + KS_K * (ks & 3);
+                    const uint64_t km = (ks >> 2) * (SBLK >> 4) + KS_K * (ks & 3);
+                    mma_bf16(tm + COL_YH, dK + kt, dM + km, ID_YH, acc);
+                    mma_bf16(tm + COL_QK, dQ + kt, dK + kt, ID_QK, acc);
+                    mma_bf16(tm + COL_Y1, dM + km, dQ + kt, ID_Y, acc);
                 }
-            mma_commit(&bars[2]);
+                mma_commit(&bars[3]);
+                if (c + 1 < nchunks) issue_qk(c + 1, stage ^ 1);
+            }
         }
-        // rescale the fp32 state for this chunk: M <- A M - sigma S, S <- B S
+        if (tid >= 128 && tid < 128 + BC) {
+            // column i of Gamma: Gamma_{t,i} = a_t Gamma_{t-1,i} + eta_t u_{t,i}, zero above the diagonal
+            const int i = tid - 128;
+            float u = g[3 * BC + i];
+            float G = g[BC + i] * u;
+            const float4* g4 = reinterpret_cast<const float4*>(g);
+#pragma unroll
+            for (int t4 = 0; t4 < BC / 4; ++t4) {
+                const float4 va = g4[t4], ve = g4[BC / 4 + t4], vb = g4[BC / 2 + t4];
+                const float ga[4] = {va.x, va.y, va.z, va.w}, ge[4] = {ve.x, ve.y, ve.z, ve.w},
+                            gb[4] = {vb.x, vb.y, vb.z, vb.w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int t = 4 * t4 + k;
+                    if (t > i) {
+                        u *= gb[k];
+                        G = fmaf(ga[k], G, ge[k] * u);
+                    }
+                    Gm[t * GS + i] = t >= i ? G : 0.0f;
+                }
+            }
+            sGl[i] = G;
+            sU[i] = u;
+        } else if (tid == 224) {
+            float A = 1.f, Bc = 1.f, sg = 0.f;
+            const float4* g4 = reinterpret_cast<const float4*>(g);
+#pragma unroll
+            for (int t4 = 0; t4 < BC / 4; ++t4) {
+                const float4 va = g4[t4], ve = g4[BC / 4 + t4], vb = g4[BC / 2 + t4];
+                const float ga[4] = {va.x, va.y, va.z, va.w}, ge[4] = {ve.x, ve.y, ve.z, ve.w},
+                            gb[4] = {vb.x, vb.y, vb.z, vb.w};
+                float oa[4], ob[4], os[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    A *= ga[k];
+                    Bc *= gb[k];
+                    sg = fmaf(ga[k], sg, ge[k] * Bc);
+                    oa[k] = A;
+                    ob[k] = Bc;
+                    os[k] = sg;
+                }
+                reinterpret_cast<float4*>(sA)[t4] = make_float4(oa[0], oa[1], oa[2], oa[3]);
+                reinterpret_cast<float4*>(sBc)[t4] = make_float4(ob[0], ob[1], ob[2], ob[3]);
+                reinterpret_cast<float4*>(sSg)[t4] = make_float4(os[0], os[1], os[2], os[3]);
+            }
+        }
+        const bool go1 = !failed && !__syncthreads_or(!tiles_ok);
+        if (!go1 && !failed) failed = true;
+        // rescale the fp32 state for this chunk (batch 1 does not touch it):
+        // M <- A_n M - sigma_n S, S <- B_n S
         {
-            const float An = sA[n - 1], Bn = sBc[n - 1], sn = sSg[n - 1];
+            const float An = sA[BC - 1], Bn = sBc[BC - 1], sn = sSg[BC - 1];
             float m[32], s[32];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                tmem_ld32(tm + lb + COL_M + 32 * j, m);
-                tmem_ld32(tm + lb + COL_S + 32 * j, s);
+            for (int j = 0; j < 2; ++j) {
+                const uint32_t c0 = 64 * hf + 32 * j;
+                tmem_ld_n(tl + COL_M + c0, tl + COL_S + c0, m, s);
 #pragma unroll
                 for (int q = 0; q < 32; ++q) {
                     m[q] = fmaf(An, m[q], -sn * s[q]);
                     s[q] = Bn * s[q];
                 }
-                tmem_st32(tm + lb + COL_M + 32 * j, m);
-                tmem_st32(tm + lb + COL_S + 32 * j, s);
+                tmem_st_n(tl + COL_M + c0, m);
+                tmem_st_n(tl + COL_S + c0, s);
             }
         }
-        ok = mbar_wait(&bars[2], mma_phase, WAIT_NS);
-        mma_phase ^= 1u;
-        if (__syncthreads_or(!ok)) {
-            failed = true;
-            break;
-        }
-        tc_fence_after();
-        // errors e_t = 2 (W0 k_t - v_t): lane o holds E^T[o][t]
+        mma_wait(go1);
+        // ---- e_t = 2 (M0 k_t - v_t) and its gamma / u scaled copies (rows t,
+        //      columns 64 hf ..); P = Gamma (.) Q K^T (row t, columns 32 hf ..)
         {
-            const unsigned char* vt = sm + OFF_V + stage * TILE;
-            float acc[32], e[32], eg[32], eu[32];
+            float e0[32], e1[32], qk[32];
+            tmem_ld_n(tl + COL_YH + 64 * hf, tl + COL_YH + 64 * hf + 32, tl + COL_QK + 32 * hf, e0, e1, qk);
+            if (r64) {
+                const bool live = tr < n;
+                const float gm = -sGl[tr], uu = sU[tr];
+                float vv[32], o[32];
 #pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                tmem_ld32(tm + lb + COL_E + 32 * j, acc);
+                for (int j = 0; j < 2; ++j) {
+                    float* ev = j ? e1 : e0;
+                    const uint32_t c0 = 64 * hf + 32 * j;
+                    get_row32(sm + OFF_V, BC, tr, c0, vv);
 #pragma unroll
-                for (int q = 0; q < 32; ++q) {
-                    const int t = 32 * j + q;
-                    const float vv = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(vt + sw128_offset(t, tid, BC)));
-                    const float ev = t < n ? 2.0f * (acc[q] - vv) : 0.0f;
-                    e[q] = ev;
-                    eg[q] = -ev * sGl[t];
-                    eu[q] = ev * sU[t];
+                    for (int q = 0; q < 32; ++q) ev[q] = live ? 2.0f * (ev[q] - vv[q]) : 0.0f;
+                    put_row32(sm + OFF_E, BC, tr, c0, ev);
+#pragma unroll
+                    for (int q = 0; q < 32; ++q) o[q] = gm * ev[q];
+                    put_row32(sm + OFF_EG, BC, tr, c0, o);
+#pragma unroll
+                    for (int q = 0; q < 32; ++q) o[q] = uu * ev[q];
+                    put_row32(sm + OFF_EU, BC, tr, c0, o);
                 }
-                put_row32(sm + OFF_ET, 128, tid, 32 * j, e);
-                put_row32(sm + OFF_EG, 128, tid, 32 * j, eg);
-                put_row32(sm + OFF_EU, 128, tid, 32 * j, eu);
+                const float* gr = Gm + tr * GS + 32 * hf;
+#pragma unroll
+                for (int q = 0; q < 32; q += 4) {
+                    const float4 gg = *reinterpret_cast<const float4*>(gr + q);
+                    qk[q] *= gg.x; qk[q + 1] *= gg.y; qk[q + 2] *= gg.z; qk[q + 3] *= gg.w;
+                }
+                put_row32(sm + OFF_P, BC, tr, 32 * hf, qk);
             }
         }
-        // P = Gamma (.) Q K^T; the M=64 accumulator holds row r at lane (r % 16) + 32 (r / 16)
+        if (gi >= 0 && gi < BC && c + 1 < nchunks) {
+            float* gn = gates + (stage ^ 1) * 4 * BC;
+            gn[gi] = nxt_valid ? 1.0f - nxt_al : 1.0f;
+            gn[BC + gi] = nxt_e;
+            gn[2 * BC + gi] = nxt_b;
+            gn[3 * BC + gi] = !nxt_valid ? 0.0f
+                              : c_mode == NM_C_ONE_MINUS_BETA ? 1.0f - nxt_b
+                              : c_mode == NM_C_PER_TOKEN ? nxt_c : 1.0f;
+        }
+        handoff();
+        // ---- batch 2: S0 Q^T, E^T P^T, M += (-gamma E)^T K, S += (u E)^T K; the next V tile
+        const bool go2 = !failed;
+        if (go2 && tid == 0) {
+            const uint64_t dQ = kdesc(aQ), dS = kdesc(aSH), dP = kdesc(aP);
+            const uint64_t dE = mdesc(aE, HALF), dEG = mdesc(aEG, HALF), dEU = mdesc(aEU, HALF);
+            const uint64_t dKm = mdesc(aK, HALF);
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                const uint64_t kt = (ks >> 2) * (HALF >> 4) + KS_K * (ks & 3);
+                const uint64_t km = (ks >> 2) * (SBLK >> 4) + KS_K * (ks & 3);
+                mma_bf16(tm + COL_Y2, dS + km, dQ + kt, ID_Y, ks ? 1u : 0u);
+            }
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {  // contraction over 64 tokens: 16 rows per k-step
+                mma_bf16(tm + COL_PE, dE + KS_M * ks, dP + KS_K * ks, ID_PE, ks ? 1u : 0u);
+                mma_bf16(tm + COL_M, dEG + KS_M * ks, dKm + KS_M * ks, ID_UPD, 1u);
+                mma_bf16(tm + COL_S, dEU + KS_M * ks, dKm + KS_M * ks, ID_UPD, 1u);
+            }
+            mma_commit(&bars[3]);
+            if (c + 1 < nchunks) issue_v(c + 1);
+        }
+        mma_wait(go2);
+        // ---- y_t[o] = A_t (M0 q_t)[o] - sigma_t (S0 q_t)[o] - (E^T P^T)[o][t], tokens 32 hf ..
         {
-            float qk0[32], qk1[32];
-            tmem_ld32(tm + lb + COL_QK, qk0);
-            tmem_ld32(tm + lb + COL_QK + 32, qk1);
-            if (lane < 16) {
-                const int t = warp * 16 + lane;
-                float p[64];
-                float Dp = 1.f, R = 0.f;
+            float y1[32], y2[32], pe[32];
+            tmem_ld_n(tl + COL_Y1 + 32 * hf, tl + COL_Y2 + 32 * hf, tl + COL_PE + 32 * hf, y1, y2, pe);
 #pragma unroll
-                for (int i = BC - 1; i >= 0; --i) {
-                    if (i == t) {
-                        R = g[BC + t];
-                        Dp = 1.f;
-                    } else if (i < t) {
-                        Dp *= g[i + 1];
-                        R = fmaf(Dp, g[BC + i], g[2 * BC + i + 1] * R);
-                    }
-                    const float qkv = i < 32 ? qk0[i & 31] : qk1[i & 31];
-                    p[i] = (i <= t && t < n) ? g[3 * BC + i] * R * qkv : 0.0f;
-                }
-                put_row32(sm + OFF_P, BC, t, 0, p);
-                put_row32(sm + OFF_P, BC, t, 32, p + 32);
+            for (int q = 0; q < 32; ++q) {
+                const int t = 32 * hf + q;
+                if (t < n) store_y(y + (t0 + t) * D + orow, fmaf(sA[t], y1[q], -fmaf(sSg[t], y2[q], pe[q])));
             }
         }
-        fence_proxy_async();
-        tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
-        if (tid == 0) {
-            const uint32_t et = smem_u32(sm + OFF_ET), eg = smem_u32(sm + OFF_EG), eu = smem_u32(sm + OFF_EU);
-            const uint32_t pa = smem_u32(sm + OFF_P);
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks) {
-                const uint32_t acc = ks ? 1u : 0u;
-                mma_bf16(tm + COL_QK, sw128_desc(et + ks * 32, 16, 1024), sw128_desc(pa + ks * 32, 16, 1024), ID_128x64, acc);
-                mma_bf16(tm + COL_M, sw128_desc(eg + ks * 32, 16, 1024), sw128_desc(ka + ks * 2048, HALF, 1024),
-                         ID_128x128_BMN, 1u);
-                mma_bf16(tm + COL_S, sw128_desc(eu + ks * 32, 16, 1024), sw128_desc(ka + ks * 2048, HALF, 1024),
-                         ID_128x128_BMN, 1u);
-            }
-            mma_commit(&bars[2]);
-        }
-        ok = mbar_wait(&bars[2], mma_phase, WAIT_NS);
-        mma_phase ^= 1u;
-        if (__syncthreads_or(!ok)) {
-            failed = true;
-            break;
-        }
-        tc_fence_after();
-        // retrieval: y_t[o] = A_t (M0 q_t)[o] - sigma_t (S0 q_t)[o] - (E^T P^T)[o][t]
-        {
-            float y1[32], y2[32], y3[32];
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                tmem_ld32(tm + lb + COL_Y1 + 32 * j, y1);
-                tmem_ld32(tm + lb + COL_Y2 + 32 * j, y2);
-                tmem_ld32(tm + lb + COL_QK + 32 * j, y3);
-#pragma unroll
-                for (int q = 0; q < 32; ++q) {
-                    const int t = 32 * j + q;
-                    if (t < n) store_y(y + (t0 + t) * D + tid, fmaf(sA[t], y1[q], -fmaf(sSg[t], y2[q], y3[q])));
-                }
-            }
-        }
-        // state for the next chunk: bf16 operand copies (and the result after the last chunk)
+        // ---- the new state: bf16 operand copies for the next chunk, or the result
         {
             const bool last = c + 1 == nchunks;
             float m[32], s[32];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                tmem_ld32(tm + lb + COL_M + 32 * j, m);
-                tmem_ld32(tm + lb + COL_S + 32 * j, s);
+            for (int j = 0; j < 2; ++j) {
+                const uint32_t c0 = 64 * hf + 32 * j;
+                tmem_ld_n(tl + COL_M + c0, tl + COL_S + c0, m, s);
                 if (!last) {
-                    put_row32(sm + OFF_MH, 128, tid, 32 * j, m);
-                    put_row32(sm + OFF_SH, 128, tid, 32 * j, s);
+                    put_row32(sm + OFF_MH, 128, orow, c0, m);
+                    put_row32(sm + OFF_SH, 128, orow, c0, s);
                 } else {
-                    float* mt = a.M_T + unit * P + (long long)tid * D + 32 * j;
-                    float* st = a.S_T + unit * P + (long long)tid * D + 32 * j;
+                    float* mt = a.M_T + unit * P + (long long)orow * D + c0;
+                    float* st = a.S_T + unit * P + (long long)orow * D + c0;
 #pragma unroll
                     for (int q = 0; q < 32; q += 4) {
                         *reinterpret_cast<float4*>(mt + q) = make_float4(m[q], m[q + 1], m[q + 2], m[q + 3]);
@@ -382,16 +451,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 }
             }
         }
-        fence_proxy_async();
-        tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
+        handoff();
     }
     if (failed) {
         if (tid == 0 && a.status) atomicExch(a.status, NM_ERR_DEVICE_TIMEOUT);
         // let copies and products still in flight land before the CTA leaves
-        if (c + 1 < nchunks) mbar_wait(&bars[(c & 1) ^ 1], (uint32_t)(((c + 1) >> 1) & 1), WAIT_NS);
-        mbar_wait(&bars[2], mma_phase, WAIT_NS);
+        for (int i = 0; i < 3; ++i) mbar_wait(&bars[i], 0, WAIT_NS / 4);
+        mbar_wait(&bars[3], mma_phase, WAIT_NS);
     }
     tc_fence_before();
     __syncthreads();
