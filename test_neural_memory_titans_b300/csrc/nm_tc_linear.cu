@@ -31,7 +31,8 @@
 //     E, -gamma E, u E as [t][o] tiles, P = Gamma (.) Q K^T, Gamma in fp32.
 // Per chunk two MMA batches: (1) yhat = K M0^T, Q K^T, M0 Q^T; then e, P and
 // the scaled e tiles; (2) S0 Q^T, E^T P^T and the two state updates; then y
-// and the next chunk's bf16 state.  The fp32 state is rescaled in TMEM
+// (a [t][o] tile in shared memory, written out by one TMA store) and the next
+// chunk's bf16 state.  The fp32 state is rescaled in TMEM
 // (M <- A_n M - sigma_n S, S <- B_n S) while batch (1) runs.  The state never
 // leaves the chip between chunks; HBM traffic is q, k, v in, y out, the gates,
 // and the state once in and once out.
@@ -68,6 +69,7 @@ constexpr uint32_t OFF_BAR = OFF_F + 4 * N_F;
 constexpr uint32_t SMEM_USED = OFF_BAR + 64;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;  // slack for 1024-byte alignment
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+static_assert(OFF_EU == OFF_EG + TILE, "a fp32 y tile spans EG and EU");
 
 constexpr uint32_t COL_M = 0, COL_S = 128;
 constexpr uint32_t COL_YH = 256, COL_QK = 384, COL_Y1 = 448;  // batch 1
@@ -121,7 +123,8 @@ __device__ __forceinline__ void store_y<float>(float* p, float x) { *p = x; }
 template <typename Tout>
 __global__ void __launch_bounds__(NTHREADS, 1)
     tc_linear_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-                     const __grid_constant__ CUtensorMap tv, nm_args a, int c_mode) {
+                     const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap ty, nm_args a,
+                     int c_mode) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     float* gates = reinterpret_cast<float*>(sm + OFF_F);  // [2 stages][a, eta, beta, c][64]
@@ -147,10 +150,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const float* eta = a.eta + unit * T;
     const float* beta = a.beta + unit * T;
     const float* cc = a.c ? a.c + unit * T : nullptr;
-    Tout* y = reinterpret_cast<Tout*>(a.y) + unit * T * D;
     const int orow = 32 * qd + lane;  // row of an M=128 accumulator: output feature o
-    const int tr = 16 * qd + lane;    // row of an M=64 accumulator: token (valid for lane < 16)
-    const bool r64 = lane < 16;
 
     if (tid == 0) {
         for (int i = 0; i < 4; ++i) mbar_init(&bars[i], 1);
@@ -158,6 +158,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         prefetch_tmap(&tq);
         prefetch_tmap(&tk);
         prefetch_tmap(&tv);
+        prefetch_tmap(&ty);
     }
     if (warp == 0) {
         tmem_alloc(&s_tmem, 512);
@@ -286,6 +287,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 mma_commit(&bars[3]);
                 if (c + 1 < nchunks) issue_qk(c + 1, stage ^ 1);
             }
+            bulk_wait_read();  // the previous chunk's y tile (in EG / EU) has been read by its store
         }
         if (tid >= 128 && tid < 128 + BC) {
             // column i of Gamma: Gamma_{t,i} = a_t Gamma_{t-1,i} + eta_t u_{t,i}, zero above the diagonal
@@ -354,38 +356,48 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             }
         }
         mma_wait(go1);
-        // ---- e_t = 2 (M0 k_t - v_t) and its gamma / u scaled copies (rows t,
-        //      columns 64 hf ..); P = Gamma (.) Q K^T (row t, columns 32 hf ..)
+        // ---- e_t = 2 (M0 k_t - v_t) and its gamma / u scaled copies, and
+        //      P = Gamma (.) Q K^T.  The M=64 accumulators hold token t in lane
+        //      t % 16 of quadrant t / 16; lanes 16..31 take over half of each
+        //      row by shuffle: e columns 64 hf + 32 .. (lanes 0..15: 64 hf ..),
+        //      P columns 32 hf + 16 .. (lanes 0..15: 32 hf ..)
         {
             float e0[32], e1[32], qk[32];
             tmem_ld_n(tl + COL_YH + 64 * hf, tl + COL_YH + 64 * hf + 32, tl + COL_QK + 32 * hf, e0, e1, qk);
-            if (r64) {
-                const bool live = tr < n;
-                const float gm = -sGl[tr], uu = sU[tr];
-                float vv[32], o[32];
+            const bool upper = lane >= 16;
+            const int t = 16 * qd + (lane & 15);
 #pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    float* ev = j ? e1 : e0;
-                    const uint32_t c0 = 64 * hf + 32 * j;
-                    get_row32(sm + OFF_V, BC, tr, c0, vv);
-#pragma unroll
-                    for (int q = 0; q < 32; ++q) ev[q] = live ? 2.0f * (ev[q] - vv[q]) : 0.0f;
-                    put_row32(sm + OFF_E, BC, tr, c0, ev);
-#pragma unroll
-                    for (int q = 0; q < 32; ++q) o[q] = gm * ev[q];
-                    put_row32(sm + OFF_EG, BC, tr, c0, o);
-#pragma unroll
-                    for (int q = 0; q < 32; ++q) o[q] = uu * ev[q];
-                    put_row32(sm + OFF_EU, BC, tr, c0, o);
-                }
-                const float* gr = Gm + tr * GS + 32 * hf;
-#pragma unroll
-                for (int q = 0; q < 32; q += 4) {
-                    const float4 gg = *reinterpret_cast<const float4*>(gr + q);
-                    qk[q] *= gg.x; qk[q + 1] *= gg.y; qk[q + 2] *= gg.z; qk[q + 3] *= gg.w;
-                }
-                put_row32(sm + OFF_P, BC, tr, 32 * hf, qk);
+            for (int q = 0; q < 32; ++q) {
+                const float hi = __shfl_sync(0xffffffffu, e1[q], lane & 15);
+                e0[q] = upper ? hi : e0[q];
             }
+#pragma unroll
+            for (int q = 0; q < 16; ++q) {
+                const float hi = __shfl_sync(0xffffffffu, qk[16 + q], lane & 15);
+                qk[q] = upper ? hi : qk[q];
+            }
+            const bool live = t < n;
+            const float gm = -sGl[t], uu = sU[t];
+            const uint32_t c0 = 64 * hf + (upper ? 32 : 0);
+            float vv[32], o[32];
+            get_row32(sm + OFF_V, BC, t, c0, vv);
+#pragma unroll
+            for (int q = 0; q < 32; ++q) e0[q] = live ? 2.0f * (e0[q] - vv[q]) : 0.0f;
+            put_row32(sm + OFF_E, BC, t, c0, e0);
+#pragma unroll
+            for (int q = 0; q < 32; ++q) o[q] = gm * e0[q];
+            put_row32(sm + OFF_EG, BC, t, c0, o);
+#pragma unroll
+            for (int q = 0; q < 32; ++q) o[q] = uu * e0[q];
+            put_row32(sm + OFF_EU, BC, t, c0, o);
+            const uint32_t p0 = 32 * hf + (upper ? 16 : 0);
+            const float* gr = Gm + t * GS + p0;
+#pragma unroll
+            for (int q = 0; q < 16; q += 4) {
+                const float4 gg = *reinterpret_cast<const float4*>(gr + q);
+                qk[q] *= gg.x; qk[q + 1] *= gg.y; qk[q + 2] *= gg.z; qk[q + 3] *= gg.w;
+            }
+            put_row<16>(sm + OFF_P, BC, t, p0, qk);
         }
         if (gi >= 0 && gi < BC && c + 1 < nchunks) {
             float* gn = gates + (stage ^ 1) * 4 * BC;
@@ -419,14 +431,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             if (c + 1 < nchunks) issue_v(c + 1);
         }
         mma_wait(go2);
-        // ---- y_t[o] = A_t (M0 q_t)[o] - sigma_t (S0 q_t)[o] - (E^T P^T)[o][t], tokens 32 hf ..
+        // ---- y_t[o] = A_t (M0 q_t)[o] - sigma_t (S0 q_t)[o] - (E^T P^T)[o][t], tokens 32 hf ..,
+        //      into a row-major [64 t][128 o] tile in the EG / EU space (free after batch 2),
+        //      written to global memory by one TMA store (rows past T are not written)
         {
             float y1[32], y2[32], pe[32];
             tmem_ld_n(tl + COL_Y1 + 32 * hf, tl + COL_Y2 + 32 * hf, tl + COL_PE + 32 * hf, y1, y2, pe);
+            Tout* yt = reinterpret_cast<Tout*>(sm + OFF_EG);
 #pragma unroll
             for (int q = 0; q < 32; ++q) {
                 const int t = 32 * hf + q;
-                if (t < n) store_y(y + (t0 + t) * D + orow, fmaf(sA[t], y1[q], -fmaf(sSg[t], y2[q], pe[q])));
+                store_y(yt + t * D + orow, fmaf(sA[t], y1[q], -fmaf(sSg[t], y2[q], pe[q])));
             }
         }
         // ---- the new state: bf16 operand copies for the next chunk, or the result
@@ -452,7 +467,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             }
         }
         handoff();
+        if (tid == 0 && !failed) {
+            tma_store_3d(&ty, sm + OFF_EG, 0, (int)t0, (int)unit);
+            bulk_commit();
+        }
     }
+    if (tid == 0) bulk_wait_all();
     if (failed) {
         if (tid == 0 && a.status) atomicExch(a.status, NM_ERR_DEVICE_TIMEOUT);
         // let copies and products still in flight land before the CTA leaves
@@ -466,15 +486,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
 template <typename Tout>
 cudaError_t launch(const nm_config& c, const nm_args& a, cudaStream_t s) {
-    CUtensorMap tq, tk, tv;
+    CUtensorMap tq, tk, tv, ty;
     const long long units = (long long)a.B * a.H;
     if (!make_token_map(&tq, a.q, D, a.T, units) || !make_token_map(&tk, a.k, D, a.T, units) ||
-        !make_token_map(&tv, a.v, D, a.T, units))
+        !make_token_map(&tv, a.v, D, a.T, units) ||
+        !make_token_store_map(&ty, a.y, D, a.T, units, sizeof(Tout) == 2))
         return cudaErrorInvalidValue;
     auto kern = tc_linear_kernel<Tout>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    kern<<<(unsigned)units, NTHREADS, SMEM_BYTES, s>>>(tq, tk, tv, a, c.c_mode);
+    kern<<<(unsigned)units, NTHREADS, SMEM_BYTES, s>>>(tq, tk, tv, ty, a, c.c_mode);
     return cudaGetLastError();
 }
 
