@@ -198,14 +198,15 @@ def time_oracle(wl, x, budget_s: float = 15.0):
     if per_tok * units * wl.T > budget_s:  # a prefix of T for one round of units
         T = max(wl.chunk, int(budget_s / (per_tok * units)) // wl.chunk * wl.chunk)
         T = min(T, wl.T)
-        reps = 1
     else:  # whole units: more rounds of units, then repeats
         T = wl.T
         rounds = max(1, min(-(-BH // units), int(budget_s / (per_tok * units * T))))
         units = min(BH, rounds * units)
-        reps = max(1, int(budget_s / (per_tok * units * T)))
     args = prep(units, T)
-    dt = sum(run(args) for _ in range(reps))
+    dt, reps = 0.0, 0
+    while reps == 0 or dt < 0.8 * budget_s:  # the calibration overestimates; repeat to the budget
+        dt += run(args)
+        reps += 1
     tokens = units * T * reps
     return {"value": tokens / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
             "sample": "%d units x %d tokens of the workload, %d run(s) (fp64, OpenMP over units), %.1f s"
