@@ -369,7 +369,7 @@ def run_reference(args, rank, world):
 
     wl = workload(args)
     x = W.make_inputs(wl, "cpu", seed=1000 + args.workload)
-    budget = max(1.0, 150.0 / max(1, args.steps + args.warmup))
+    budget = args.cpu_budget if args.cpu_budget else max(1.0, 150.0 / max(1, args.steps + args.warmup))
     for _ in range(args.warmup):
         time_oracle(wl, x, budget_s=budget)
     runs = [time_oracle(wl, x, budget_s=budget) for _ in range(args.steps)]
@@ -399,6 +399,8 @@ def main():
                     help="DRAM bytes per launch of the dominant kernel from an ncu capture")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=None,
+                    help="seconds of oracle work per step of the reference arm (default: about 150 s in all)")
     ap.add_argument("--B", type=int, default=None, help="override the workload's batch (small profiling cases)")
     ap.add_argument("--H", type=int, default=None, help="override the workload's heads")
     ap.add_argument("--T", type=int, default=None, help="override the workload's tokens per unit")

@@ -162,6 +162,22 @@ int nm_selected_path(nm_handle_t h);
 long long nm_launch_count(nm_handle_t h);
 
 /*
+ * nm_inject_missing_load - test hook for the device-side failure detection.
+ *   Arms the handle so that its next nm_forward launches the tensor-core
+ *   kernel without loading the first chunk's tiles.  The kernel's bounded wait
+ *   for those tiles (2 s) then expires; the kernel records
+ *   NM_ERR_DEVICE_TIMEOUT in the handle's status word, skips the rest of its
+ *   tensor-core work and exits normally, leaving the CUDA context usable.  That
+ *   call's outputs are undefined; nm_synchronize returns the status.  The hook
+ *   is consumed by that one call.  Not part of the method (the pages have no
+ *   counterpart): it exists so that tests can check the timeout path without
+ *   faulting a GPU.
+ *   Returns NM_ERR_ARG for a NULL handle, NM_ERR_UNSUPPORTED when the handle
+ *   uses the fp32 FFMA kernels (they have no waits).
+ */
+int nm_inject_missing_load(nm_handle_t h);
+
+/*
  * nm_forward_mlp2_noalloc - the MLP2 forward without any allocation.
  *   The paper has no counterpart to this entry point; it exists for callers
  *   that cannot call cudaMalloc when they run the layer: a host that has

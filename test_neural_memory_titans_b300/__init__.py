@@ -47,7 +47,8 @@ NM_ERR_DEVICE_CHECK = 8
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libnm.so")
 EXPORTED = ("nm_create", "nm_forward", "nm_forward_host", "nm_synchronize", "nm_destroy",
-            "nm_status_string", "nm_selected_path", "nm_launch_count")
+            "nm_status_string", "nm_selected_path", "nm_launch_count", "nm_inject_missing_load",
+            "nm_forward_mlp2_noalloc")
 
 _DT = {torch.float32: F32, torch.bfloat16: BF16}
 _TORCH_DT = {F32: torch.float32, BF16: torch.bfloat16}
@@ -94,6 +95,8 @@ def load_library() -> ctypes.CDLL:
         lib.nm_selected_path.restype = i
         lib.nm_launch_count.argtypes = [vp]
         lib.nm_launch_count.restype = ctypes.c_longlong
+        lib.nm_inject_missing_load.argtypes = [vp]
+        lib.nm_inject_missing_load.restype = i
         _lib = lib
     return _lib
 
@@ -213,6 +216,12 @@ class NeuralMemory:
         if rc != NM_OK:
             raise NMError(rc, "nm_forward_host")
         return y, M_T, S_T
+
+    def inject_missing_load(self) -> int:
+        """Test hook: the next forward runs without its first tile loads, so
+        its bounded wait expires and nm_synchronize reports
+        NM_ERR_DEVICE_TIMEOUT (see nm_inject_missing_load in include/nm.h)."""
+        return int(load_library().nm_inject_missing_load(self._h))
 
     def synchronize(self) -> int:
         """Wait for the device; return (and clear) the device status word."""

@@ -131,6 +131,13 @@ int nm_create(const nm_config* cfg, int device, nm_handle_t* out) {
 
 int nm_selected_path(nm_handle_t h) { return h ? h->path : -NM_ERR_ARG; }
 
+int nm_inject_missing_load(nm_handle_t h) {
+    if (!h) return NM_ERR_ARG;
+    if (h->path != NM_PATH_TC) return NM_ERR_UNSUPPORTED;
+    h->inject_load_skip = 1;
+    return NM_OK;
+}
+
 long long nm_launch_count(nm_handle_t h) { return h ? h->launches : -1; }
 
 int nm_forward(nm_handle_t h, int B, int H, int T, const void* q, const void* k, const void* v,
@@ -195,6 +202,8 @@ int nm_forward(nm_handle_t h, int B, int H, int T, const void* q, const void* k,
     a.status = h->d_status;
     a.scratch = h->workspace;
     a.scratch_bytes = h->workspace_bytes;
+    a.skip_first_load = h->inject_load_skip;
+    h->inject_load_skip = 0;
     cudaError_t e = h->path == NM_PATH_TC ? nm_tc_launch(cfg, a, s, h->num_sms, &h->launches)
                                           : nm_simt_launch(cfg, a, s, &h->launches);
     if (e != cudaSuccess) {

@@ -26,6 +26,7 @@ struct nm_args {
     int* status;      // device status word owned by the handle
     void* scratch;    // device workspace owned by the handle (may be NULL)
     size_t scratch_bytes;
+    int skip_first_load;  // test hook: tensor-core kernels skip chunk 0's tile loads
 };
 
 struct nm_handle {
@@ -39,6 +40,7 @@ struct nm_handle {
     void* stage;       // device staging for nm_forward_host
     size_t stage_bytes;
     long long launches;
+    int inject_load_skip;  // armed by nm_inject_missing_load, consumed by the next nm_forward
 };
 
 // Parameters per unit.

@@ -131,6 +131,7 @@ extern "C" int nm_forward_mlp2_noalloc(const nm_config* cfg, int B, int H, int T
     a.status = nullptr;  // the FFMA kernels have no bounded waits to report
     a.scratch = scratch;
     a.scratch_bytes = NM_NOALLOC_SCRATCH_BYTES;
+    a.skip_first_load = 0;
     long long launched = 0;
     if (nm_simt_launch(run, a, s, &launched) != cudaSuccess) {
         cudaGetLastError();

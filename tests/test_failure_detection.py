@@ -1,0 +1,46 @@
+"""Device-side failure detection, tested without a GPU fault.
+
+Every wait of the tensor-core kernels (TMA tiles, tensor-core completion) is
+bounded (2 s).  The test hook nm_inject_missing_load makes the next launch
+skip its first tile loads, so that wait expires: the kernel must record
+NM_ERR_DEVICE_TIMEOUT in the handle's status word, skip the rest of its
+tensor-core work, exit normally, and leave the context usable, so that the
+next call on the same handle is correct again.
+"""
+import time
+
+import pytest
+import torch
+
+import test_neural_memory_titans_b300 as nm
+from test_neural_memory_titans_b300 import workloads as W
+
+from _helpers import compare, oracle_forward
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("wid", [2, 1], ids=["linear_d128", "mlp_64x256_cluster"])
+def test_missing_tile_load_times_out_and_the_handle_recovers(wid):
+    wl = W.WORKLOADS[wid].with_sizes(B=1, H=2, T=192)
+    x = W.make_inputs(wl, "cuda", seed=3)
+    M0, S0 = W.random_state(wl, "cuda", seed=4, scale=0.5)
+    mem = nm.NeuralMemory(wl.kind, wl.d, wl.hidden, wl.chunk, in_dtype=wl.dtype, path=nm.PATH_TC)
+    args = (x["q"], x["k"], x["v"], x["alpha"], x["eta"], x["beta"], M0, S0)
+    assert mem.inject_missing_load() == nm.NM_OK
+    t0 = time.time()
+    mem.forward(*args)
+    assert mem.synchronize() == nm.NM_ERR_DEVICE_TIMEOUT
+    assert time.time() - t0 < 60
+    # the status word was cleared by synchronize, and the same handle works again
+    y, MT, ST = mem.forward(*args)
+    assert mem.synchronize() == nm.NM_OK
+    compare(wl, (y, MT, ST), oracle_forward(wl, x, M0=M0, S0=S0))
+    mem.close()
+
+
+def test_injection_needs_the_tensor_core_path():
+    wl = W.WORKLOADS[0]
+    mem = nm.NeuralMemory(wl.kind, wl.d, 0, wl.chunk, in_dtype=torch.float32, path=nm.PATH_SIMT)
+    assert mem.inject_missing_load() == nm.NM_ERR_UNSUPPORTED
+    mem.close()

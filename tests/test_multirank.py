@@ -1,0 +1,32 @@
+"""The multi-rank launch of bench.py on CPU: two gloo ranks under
+torch.distributed.run (127.0.0.1).  The reference arm runs on rank 0 only and
+prints exactly one JSON line; the other rank exits 0 without work."""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def test_reference_arm_two_gloo_ranks():
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+           "--master-addr", "127.0.0.1", "--master-port", str(_free_port()), "bench.py",
+           "--impl", "reference", "--gpus", "2", "--steps", "2", "--warmup", "1", "--workload", "0",
+           "--cpu-budget", "0.2"]
+    env = dict(os.environ, OMP_NUM_THREADS="2")
+    r = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=300, env=env)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    out = json.loads(lines[0])
+    assert out["impl"] == "reference" and out["n_gpus"] == 2 and out["steps"] == 2
+    assert out["value"] > 0 and out["cpu_baseline"]["kind"] == "oracle"
+    assert out["e2e"]["h2d_bytes_per_step"] == 0
