@@ -1,0 +1,707 @@
+// tcgen05 tensor-core kernel for the 2-layer SiLU MLP memory
+// M(x) = W2 silu(W1 x) with d = 128, hidden h = 64 * NC (NC = 2, 4 or 8 CTAs
+// per unit, a thread-block cluster), chunk b = 64.
+//
+// The method is that of nm_tc_mlp.cu ("Titans: Imparare a Memorizzare al
+// Tempo di Test", sections "Meccanismo di Aggiornamento della Memoria",
+// "Meccanismo di Dimenticanza", "Funzione Obiettivo", "Addestramento
+// Parallelizzato"; the 0h-n0.github.io explainer, "ニューラル長期メモリモジュール"
+// and "メモリ読み出し"): per chunk, with A_t, B_t, sigma_t, Gamma, gamma, u from
+// the gate scan, z_i = W1 k_i, a(k_i) = silu(z_i), e_i = 2 (W2 a(k_i) - v_i),
+// delta_i = (W2^T e_i) (.) silu'(z_i),
+//   h_t = A_t W1 q_t - sigma_t S1 q_t - sum_i Gamma_{t,i} (k_i . q_t) delta_i,
+//   y_t = A_t W2 a_t - sigma_t S2 a_t - sum_i Gamma_{t,i} (a(k_i) . a_t) e_i,
+//   W_end = A_n W0 - sigma_n S0 - sum_i gamma_i g_i,  S_end = B_n S0 + sum_i u_i g_i,
+// with g_i = (delta_i k_i^T, e_i a(k_i)^T).
+//
+// With d = 128 the state of a unit is 1 MB of fp32; it stays on chip split
+// over NC CTAs, CTA r owning hidden units j in [64 r, 64 r + 64).  Each CTA
+// keeps its slice transposed in TMEM, one lane per input / output feature:
+// W1^T [x][j] (columns 0..63), S1^T (64..127), W2 [o][j] (128..191), S2
+// (192..255).  Products over the 64 tokens of a chunk whose natural M is 64
+// are stacked to M=128 (two 64-row operands one above the other; only the
+// wanted half of the result is read).  The sums over the hidden dimension go
+// through distributed shared memory:
+//   * the key forward W2 a(k_t): each CTA's partial [o][t] is reduce-scattered
+//     (CTA r owns output rows [128 r / NC, 128 (r + 1) / NC)); the owner forms
+//     e for its rows and all-gathers e^T as bf16 into every CTA;
+//   * the retrieval y: the partials [o][t] are reduce-scattered the same way
+//     and each owner writes its rows of y.
+// Four cluster barriers per chunk order the exchanges (one receive buffer
+// serves both reduce-scatters).
+#include <cuda_bf16.h>
+
+#include "nm_internal.h"
+#include "tc_common.cuh"
+
+namespace {
+
+using namespace tc;
+
+constexpr int D = 128;        // key / value width
+constexpr int HS = 64;        // hidden units per CTA
+constexpr int BC = 64;        // chunk size
+constexpr int NTHREADS = 256;
+constexpr uint32_t T64 = 64 * 128;    // [64 rows][64 bf16] swizzled tile (8 KB)
+constexpr uint32_t T128 = 128 * 128;  // [128 rows][64 bf16] (16 KB)
+constexpr int GST = 72;               // Gamma row stride (bf16 elements)
+constexpr int RXS = 68;               // exchange row stride (floats)
+
+template <int NC>
+struct Layout {
+    static constexpr int OR = D / NC;  // output rows owned by each CTA
+    static constexpr uint32_t KQ = 0;               // two column blocks of [128 rows][64]: k rows 0..63, q rows 64..127
+    static constexpr uint32_t W1 = KQ + 2 * T128;   // [128 x][64 j] bf16 copy of W1^T
+    static constexpr uint32_t S1 = W1 + T128;
+    static constexpr uint32_t W2 = S1 + T128;       // [128 o][64 j]
+    static constexpr uint32_t S2 = W2 + T128;
+    static constexpr uint32_t AK = S2 + T128;       // [64 t][64 j] a(k_t)
+    static constexpr uint32_t AQ = AK + T64;        // [64 t][64 j] a_t (follows AK: stacked operand)
+    static constexpr uint32_t AKG = AQ + T64;       // -gamma_t a(k_t)
+    static constexpr uint32_t AKU = AKG + T64;      // u_t a(k_t)
+    static constexpr uint32_t ET = AKU + T64;       // [128 o][64 t] e^T (all-gathered)
+    static constexpr uint32_t DT = ET + T128;       // [64 t][64 j] delta_t
+    static constexpr uint32_t DG = DT + T64;        // -gamma_t delta_t
+    static constexpr uint32_t DU = DG + T64;        // u_t delta_t
+    static constexpr uint32_t P = DU + T64;         // [64 t][64 i] Gamma (.) inner products (follows DU: stacked operand)
+    static constexpr uint32_t GM = P + T64;         // bf16 Gamma [64][GST]
+    static constexpr uint32_t V = GM + 64 * GST * 2;              // bf16 [64 t][OR] this CTA's columns of v
+    static constexpr uint32_t RX = V + 64 * OR * 2;               // fp32 [NC-1][OR][RXS] partials from the peers
+    static constexpr uint32_t F = RX + (NC - 1) * OR * RXS * 4;   // gates [4][64], A, B, sigma, gamma, u
+    static constexpr uint32_t BAR = F + 4 * (4 * BC + 5 * BC);
+    static constexpr uint32_t USED = BAR + 64;
+    static constexpr uint32_t BYTES = USED + 1024;  // slack for the 1024-byte alignment
+    static_assert(BYTES <= 232448, "shared memory budget");
+    static_assert(AQ == AK + T64 && P == DU + T64, "stacked operands");
+    static_assert(GM % 128 == 0 && V % 128 == 0 && RX % 16 == 0, "alignment");
+};
+
+// TMEM columns
+constexpr uint32_t COL_W1 = 0, COL_S1 = 64, COL_W2 = 128, COL_S2 = 192;
+constexpr uint32_t COL_XA = 256;   // G1: rows 0..63 z_t[j], rows 64..127 (W1 q_t)[j]
+constexpr uint32_t COL_XB = 320;   // G1: rows 64..127 (S1 q_t)[j]
+constexpr uint32_t COL_QK = 384;   // G1: rows 64..127 q_t . k_i
+constexpr uint32_t COL_YH = 448;   // G2: [o][t] partial W2 a(k_t)
+constexpr uint32_t COL_X = 448;    // G3: rows 0..63 (W2^T e_t)[j]
+constexpr uint32_t COL_R1 = 384;   // G4: rows 64..127 sum_i P1[t][i] delta_i[j]
+constexpr uint32_t COL_AA = 256;   // G5: rows 64..127 a_t . a(k_i)
+constexpr uint32_t COL_YW = 320;   // G5: [o][t] partial W2 a_t
+constexpr uint32_t COL_YS = 448;   // G5: [o][t] partial S2 a_t
+constexpr uint32_t COL_PE = 384;   // G6: [o][t] partial sum_i P2[t][i] e_i
+
+constexpr uint32_t ID_KB = idesc_bf16_f32(128, 64, false, true);  // A K-major, B MN-major
+constexpr uint32_t ID_KK = idesc_bf16_f32(128, 64, false, false);
+constexpr uint32_t ID_MB = idesc_bf16_f32(128, 64, true, true);   // A MN-major, B MN-major
+constexpr uint64_t WAIT_NS = 2000000000ull;  // 2 s
+
+// Shared-memory descriptors (sw128_desc fields): K-major, and MN-major with
+// 64-element blocks along M/N `lbo` bytes apart.  The start-address field
+// keeps bits 4..17 of the address (cluster shared::cta addresses carry higher
+// bits).  A k-step adds +2 (32 bytes, K-major) or +128 (16 rows, MN-major).
+constexpr uint64_t desc_hi(uint32_t lbo) {
+    return (static_cast<uint64_t>(lbo >> 4) << 16) | (static_cast<uint64_t>(1024 >> 4) << 32) | (1ull << 46) |
+           (2ull << 61);
+}
+__device__ __forceinline__ uint64_t kdesc(uint32_t a) { return desc_hi(16) | ((a >> 4) & 0x3FFFu); }
+__device__ __forceinline__ uint64_t mdesc(uint32_t a, uint32_t lbo) { return desc_hi(lbo) | ((a >> 4) & 0x3FFFu); }
+constexpr uint64_t KS_K = 2, KS_M = 128;
+
+__device__ __forceinline__ float sigmoid_f(float z) { return __fdividef(1.0f, 1.0f + __expf(-fmaxf(z, -80.0f))); }
+
+__device__ __forceinline__ float momentum_c(int mode, float beta, const float* c, long long i) {
+    if (mode == NM_C_ONE_MINUS_BETA) return 1.0f - beta;
+    if (mode == NM_C_PER_TOKEN) return c[i];
+    return 1.0f;
+}
+
+template <typename Tout>
+__device__ __forceinline__ void store_y1(Tout* p, float x);
+template <>
+__device__ __forceinline__ void store_y1<__nv_bfloat16>(__nv_bfloat16* p, float x) { *p = __float2bfloat16_rn(x); }
+template <>
+__device__ __forceinline__ void store_y1<float>(float* p, float x) { *p = x; }
+
+// 32 bf16 of a plain row-major bf16 row (16-byte aligned), as floats.
+__device__ __forceinline__ void get_plain32(uint32_t addr, float* v) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const uint4 w = ld_shared_v4(addr + 16 * q);
+        v[8 * q + 0] = bf16_lo(w.x); v[8 * q + 1] = bf16_hi(w.x);
+        v[8 * q + 2] = bf16_lo(w.y); v[8 * q + 3] = bf16_hi(w.y);
+        v[8 * q + 4] = bf16_lo(w.z); v[8 * q + 5] = bf16_hi(w.z);
+        v[8 * q + 6] = bf16_lo(w.w); v[8 * q + 7] = bf16_hi(w.w);
+    }
+}
+
+template <int NC, typename Tout>
+__global__ void __launch_bounds__(NTHREADS, 1)
+    tc_mlpw_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                   const __grid_constant__ CUtensorMap tv, nm_args a, int c_mode) {
+    using L = Layout<NC>;
+    constexpr int OR = L::OR;
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    float* gates = reinterpret_cast<float*>(sm + L::F);  // [a, eta, beta, c][64]
+    float* sA = gates + 4 * BC;
+    float* sBc = sA + BC;
+    float* sSg = sBc + BC;
+    float* sGl = sSg + BC;
+    float* sU = sGl + BC;
+    __nv_bfloat16* Gm = reinterpret_cast<__nv_bfloat16*>(sm + L::GM);
+    float* RX = reinterpret_cast<float*>(sm + L::RX);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::BAR);  // 0: q|k tiles, 1: mma, 2: v slice
+    __shared__ uint32_t s_tmem;
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    const int qd = warp & 3;   // TMEM lane quadrant
+    const int hf = warp >> 2;  // which 32 of a 64-column accumulator this thread reads
+    const int rank = (int)cluster_ctarank();
+    const long long unit = blockIdx.x / NC;
+    const long long T = a.T;
+    const int hid = HS * NC;
+    const long long P = 2LL * hid * D;
+    const int nchunks = (int)((T + BC - 1) / BC);
+    const float* alpha = a.alpha + unit * T;
+    const float* eta = a.eta + unit * T;
+    const float* beta = a.beta + unit * T;
+    const float* cc = a.c ? a.c + unit * T : nullptr;
+    Tout* y = reinterpret_cast<Tout*>(a.y) + unit * T * D;
+    const int lr = 32 * qd + lane;        // accumulator row (lane) of this thread
+    const int own_lo = OR * rank;         // this CTA's output rows [own_lo, own_lo + OR)
+    const bool owner = lr >= own_lo && lr < own_lo + OR;
+    const int jg0 = HS * rank;            // this CTA's first hidden unit
+
+    if (tid == 0) {
+        for (int i = 0; i < 3; ++i) mbar_init(&bars[i], 1);
+        fence_mbar_init();
+        prefetch_tmap(&tq);
+        prefetch_tmap(&tk);
+        prefetch_tmap(&tv);
+    }
+    if (warp == 0) {
+        tmem_alloc(&s_tmem, 512);
+        tmem_relinquish();
+    }
+    auto issue_kq = [&](int chunk) {
+        mbar_arrive_expect_tx(&bars[0], 4 * T64);
+        const int t0 = chunk * BC;
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+            tma_load_3d(sm + L::KQ + b * T128, &tk, &bars[0], 64 * b, t0, (int)unit);
+            tma_load_3d(sm + L::KQ + b * T128 + T64, &tq, &bars[0], 64 * b, t0, (int)unit);
+        }
+    };
+    auto issue_v = [&](int chunk) {
+        mbar_arrive_expect_tx(&bars[2], 64 * OR * 2);
+        tma_load_3d(sm + L::V, &tv, &bars[2], own_lo, chunk * BC, (int)unit);
+    };
+    auto load_gates = [&](int chunk) {
+        if (tid < BC) {  // tokens past T change nothing: a = 1, eta = 0, beta = 1, c = 0
+            const long long t = (long long)chunk * BC + tid;
+            const bool ok = t < T;
+            const float b = ok ? beta[t] : 1.0f;
+            gates[tid] = ok ? 1.0f - alpha[t] : 1.0f;
+            gates[BC + tid] = ok ? eta[t] : 0.0f;
+            gates[2 * BC + tid] = b;
+            gates[3 * BC + tid] = ok ? momentum_c(c_mode, b, cc, t) : 0.0f;
+        }
+    };
+
+    load_gates(0);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tm = s_tmem;
+    const uint32_t tl = tm + ((uint32_t)(32 * qd) << 16);
+    if (tid == 0 && nchunks > 0 && !a.skip_first_load) {  // (the test hook leaves chunk 0 unloaded)
+        issue_kq(0);
+        issue_v(0);
+    }
+
+    // initial state, transposed: lane x of W1^T holds W1[jg0 + j][x], lane o of W2 holds W2[o][jg0 + j]
+    {
+        float r[32];
+#pragma unroll
+        for (int which = 0; which < 2; ++which) {
+            const float* src = (which ? a.S0 : a.M0) + unit * P;
+            const float* w1 = src + (long long)(jg0 + 32 * hf) * D + lr;
+#pragma unroll
+            for (int q = 0; q < 32; ++q) r[q] = w1[(long long)q * D];
+            tmem_st32(tl + (which ? COL_S1 : COL_W1) + 32 * hf, r);
+            put_row32(sm + (which ? L::S1 : L::W1), 128, lr, 32 * hf, r);
+            const float* w2 = src + (long long)hid * D + (long long)lr * hid + jg0 + 32 * hf;
+#pragma unroll
+            for (int q = 0; q < 32; q += 4) {
+                const float4 w = *reinterpret_cast<const float4*>(w2 + q);
+                r[q] = w.x; r[q + 1] = w.y; r[q + 2] = w.z; r[q + 3] = w.w;
+            }
+            tmem_st32(tl + (which ? COL_S2 : COL_W2) + 32 * hf, r);
+            put_row32(sm + (which ? L::S2 : L::W2), 128, lr, 32 * hf, r);
+        }
+    }
+    fence_proxy_async();
+    tc_fence_before();
+    cluster_sync();
+    tc_fence_after();
+
+    const uint32_t aKQ = smem_u32(sm + L::KQ), aW1 = smem_u32(sm + L::W1), aS1 = smem_u32(sm + L::S1);
+    const uint32_t aW2 = smem_u32(sm + L::W2), aS2 = smem_u32(sm + L::S2), aAK = smem_u32(sm + L::AK);
+    const uint32_t aAQ = smem_u32(sm + L::AQ), aAKG = smem_u32(sm + L::AKG), aAKU = smem_u32(sm + L::AKU);
+    const uint32_t aET = smem_u32(sm + L::ET), aDT = smem_u32(sm + L::DT), aDG = smem_u32(sm + L::DG);
+    const uint32_t aDU = smem_u32(sm + L::DU), aP = smem_u32(sm + L::P);
+
+    bool failed = false;
+    uint32_t mma_phase = 0;
+    auto mma_wait = [&](bool committed) {  // bounded; uniform over the CTA
+        bool ok = true;
+        if (committed) {
+            ok = mbar_wait(&bars[1], mma_phase, WAIT_NS);
+            mma_phase ^= 1u;
+        }
+        failed = __syncthreads_or(!ok) || failed;
+        tc_fence_after();
+    };
+    auto handoff = [&]() {
+        fence_proxy_async();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+    };
+    // Sends this thread's 32 partial values of row lr (columns 32 hf ..) to the
+    // CTA owning the row (its exchange slot for this CTA), or keeps them.
+    auto scatter_row = [&](const float* v) {
+        const int q_own = lr / OR;
+        if (q_own != rank) {
+            const int slot = rank < q_own ? rank : rank - 1;
+            const uint32_t dst =
+                map_to_rank(smem_u32(RX + ((size_t)slot * OR + (lr - OR * q_own)) * RXS + 32 * hf), (uint32_t)q_own);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) st_cluster_v4(dst + 16 * q, v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+        }
+    };
+    // Adds the peers' partials of an owned row (after the barrier).
+    auto gather_row = [&](float* v) {
+#pragma unroll
+        for (int s = 0; s < NC - 1; ++s) {
+            const float* src = RX + ((size_t)s * OR + (lr - own_lo)) * RXS + 32 * hf;
+#pragma unroll
+            for (int q = 0; q < 32; q += 4) {
+                const float4 w = *reinterpret_cast<const float4*>(src + q);
+                v[q] += w.x; v[q + 1] += w.y; v[q + 2] += w.z; v[q + 3] += w.w;
+            }
+        }
+    };
+
+    float ds[32];  // silu'(z) of this thread's token row (rows 0..63), kept from E1 to E3
+    for (int c = 0; c < nchunks; ++c) {
+        const long long t0 = (long long)c * BC;
+        const int n = (int)min((long long)BC, T - t0);
+
+        // the next chunk's gates (warps 2-3), stored after this chunk's scan
+        const int gi = tid - 64;
+        const bool nxt_valid = gi >= 0 && gi < BC && c + 1 < nchunks && t0 + BC + gi < T;
+        float nxt_al = 0.0f, nxt_e = 0.0f, nxt_b = 1.0f, nxt_c = 0.0f;
+        if (nxt_valid) {
+            const long long t = t0 + BC + gi;
+            nxt_al = alpha[t];
+            nxt_e = eta[t];
+            nxt_b = beta[t];
+            if (c_mode == NM_C_PER_TOKEN) nxt_c = cc[t];
+        }
+
+        // ---- G1 (thread 0): [K;Q] W1^T, [K;Q] S1^T, [K;Q] K^T; meanwhile the gate scan
+        bool tiles_ok = true;
+        if (tid == 0 && !failed) {
+            tiles_ok = mbar_wait(&bars[0], (uint32_t)(c & 1), WAIT_NS);
+            if (tiles_ok) {
+                tc_fence_after();
+                const uint64_t dKQ = kdesc(aKQ), dW1 = mdesc(aW1, T128), dS1 = mdesc(aS1, T128);
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {  // 16 features per k-step
+                    const uint32_t acc = ks ? 1u : 0u;
+                    const uint64_t ka = (ks >> 2) * (T128 >> 4) + KS_K * (ks & 3);
+                    mma_bf16(tm + COL_XA, dKQ + ka, dW1 + KS_M * ks, ID_KB, acc);
+                    mma_bf16(tm + COL_XB, dKQ + ka, dS1 + KS_M * ks, ID_KB, acc);
+                    mma_bf16(tm + COL_QK, dKQ + ka, dKQ + ka, ID_KK, acc);
+                }
+                mma_commit(&bars[1]);
+            }
+        }
+        if (tid >= 128 && tid < 128 + BC) {
+            // column i of Gamma: Gamma_{t,i} = a_t Gamma_{t-1,i} + eta_t u_{t,i}, zero above the diagonal
+            const int i = tid - 128;
+            float u = gates[3 * BC + i];
+            float G = gates[BC + i] * u;
+            const float4* g4 = reinterpret_cast<const float4*>(gates);
+#pragma unroll
+            for (int t4 = 0; t4 < BC / 4; ++t4) {
+                const float4 va = g4[t4], ve = g4[BC / 4 + t4], vb = g4[BC / 2 + t4];
+                const float ga[4] = {va.x, va.y, va.z, va.w}, ge[4] = {ve.x, ve.y, ve.z, ve.w},
+                            gb[4] = {vb.x, vb.y, vb.z, vb.w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int t = 4 * t4 + k;
+                    if (t > i) {
+                        u *= gb[k];
+                        G = fmaf(ga[k], G, ge[k] * u);
+                    }
+                    Gm[t * GST + i] = __float2bfloat16_rn(t >= i ? G : 0.0f);
+                }
+            }
+            sGl[i] = G;
+            sU[i] = u;
+        } else if (tid == 224) {
+            float A = 1.f, Bc = 1.f, sg = 0.f;
+            const float4* g4 = reinterpret_cast<const float4*>(gates);
+#pragma unroll
+            for (int t4 = 0; t4 < BC / 4; ++t4) {
+                const float4 va = g4[t4], ve = g4[BC / 4 + t4], vb = g4[BC / 2 + t4];
+                const float ga[4] = {va.x, va.y, va.z, va.w}, ge[4] = {ve.x, ve.y, ve.z, ve.w},
+                            gb[4] = {vb.x, vb.y, vb.z, vb.w};
+                float oa[4], ob[4], os[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    A *= ga[k];
+                    Bc *= gb[k];
+                    sg = fmaf(ga[k], sg, ge[k] * Bc);
+                    oa[k] = A;
+                    ob[k] = Bc;
+                    os[k] = sg;
+                }
+                reinterpret_cast<float4*>(sA)[t4] = make_float4(oa[0], oa[1], oa[2], oa[3]);
+                reinterpret_cast<float4*>(sBc)[t4] = make_float4(ob[0], ob[1], ob[2], ob[3]);
+                reinterpret_cast<float4*>(sSg)[t4] = make_float4(os[0], os[1], os[2], os[3]);
+            }
+        }
+        const bool go1 = !failed && !__syncthreads_or(!tiles_ok);
+        if (!go1 && !failed) failed = true;
+        // rescale the fp32 state for this chunk: W <- A_n W - sigma_n S, S <- B_n S
+        {
+            const float An = sA[BC - 1], Bn = sBc[BC - 1], sn = sSg[BC - 1];
+            float w[32], s[32];
+#pragma unroll
+            for (int pr = 0; pr < 2; ++pr) {
+                const uint32_t cw = (pr ? COL_W2 : COL_W1) + 32 * hf, cs = (pr ? COL_S2 : COL_S1) + 32 * hf;
+                tmem_ld_n(tl + cw, tl + cs, w, s);
+#pragma unroll
+                for (int q = 0; q < 32; ++q) {
+                    w[q] = fmaf(An, w[q], -sn * s[q]);
+                    s[q] = Bn * s[q];
+                }
+                tmem_st_n(tl + cw, w);
+                tmem_st_n(tl + cs, s);
+            }
+        }
+        mma_wait(go1);
+        // ---- E1: rows 0..63: a(k) = silu(z), silu'(z), and the gamma / u scaled
+        //      a(k); rows 64..127: P1 = Gamma (.) Q K^T
+        {
+            float v[32];
+            if (qd < 2) {
+                tmem_ld32(tl + COL_XA + 32 * hf, v);
+                const int t = lr;
+                const float gm = -sGl[t], uu = sU[t];
+                float o1[32];
+#pragma unroll
+                for (int q = 0; q < 32; ++q) {
+                    const float sg = sigmoid_f(v[q]);
+                    ds[q] = fmaf(v[q] * sg, 1.0f - sg, sg);  // silu'(z) = s + z s (1 - s)
+                    v[q] *= sg;
+                }
+                put_row32(sm + L::AK, 64, t, 32 * hf, v);
+#pragma unroll
+                for (int q = 0; q < 32; ++q) o1[q] = gm * v[q];
+                put_row32(sm + L::AKG, 64, t, 32 * hf, o1);
+#pragma unroll
+                for (int q = 0; q < 32; ++q) o1[q] = uu * v[q];
+                put_row32(sm + L::AKU, 64, t, 32 * hf, o1);
+            } else {
+                tmem_ld32(tl + COL_QK + 32 * hf, v);
+                const int t = lr - 64;
+                float gr[32];
+                get_plain32(smem_u32(Gm + t * GST + 32 * hf), gr);
+#pragma unroll
+                for (int q = 0; q < 32; ++q) v[q] *= gr[q];
+                put_row32(sm + L::P, 64, t, 32 * hf, v);
+            }
+        }
+        handoff();
+        // ---- G2: partial key forward [o][t] = sum_{j in slice} W2[o][j] a(k_t)[j]
+        const bool go2 = !failed;
+        if (go2 && tid == 0) {
+            const uint64_t dW2 = kdesc(aW2), dAK = kdesc(aAK);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+                mma_bf16(tm + COL_YH, dW2 + KS_K * ks, dAK + KS_K * ks, ID_KK, ks ? 1u : 0u);
+            mma_commit(&bars[1]);
+        }
+        // the next chunk's gates (this chunk's are scanned)
+        if (gi >= 0 && gi < BC && c + 1 < nchunks) {
+            gates[gi] = nxt_valid ? 1.0f - nxt_al : 1.0f;
+            gates[BC + gi] = nxt_e;
+            gates[2 * BC + gi] = nxt_b;
+            gates[3 * BC + gi] = !nxt_valid ? 0.0f
+                                 : c_mode == NM_C_ONE_MINUS_BETA ? 1.0f - nxt_b
+                                 : c_mode == NM_C_PER_TOKEN ? nxt_c : 1.0f;
+        }
+        mma_wait(go2);
+        // ---- exchange 1: reduce-scatter of the key forward; the owners form
+        //      e = 2 (yhat - v) for their rows and all-gather e^T (bf16)
+        {
+            float v[32];
+            tmem_ld32(tl + COL_YH + 32 * hf, v);
+            scatter_row(v);
+            bool okv = true;  // the owners read this chunk's v slice
+            if (owner && !failed) okv = mbar_wait(&bars[2], (uint32_t)(c & 1), WAIT_NS);
+            failed = __syncthreads_or(!okv) || failed;
+            cluster_sync();  // barrier A
+            if (owner) {
+                gather_row(v);
+                const __nv_bfloat16* vs = reinterpret_cast<const __nv_bfloat16*>(sm + L::V);
+#pragma unroll
+                for (int q = 0; q < 32; ++q) {
+                    const int t = 32 * hf + q;
+                    v[q] = t < n ? 2.0f * (v[q] - __bfloat162float(vs[t * OR + (lr - own_lo)])) : 0.0f;
+                }
+                // e^T row lr into every CTA of the cluster (same swizzled place)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const uint32_t off = sw128_offset(lr, 32 * hf + 8 * q, 128);
+                    const uint32_t w0 = pack_bf16(v[8 * q], v[8 * q + 1]), w1 = pack_bf16(v[8 * q + 2], v[8 * q + 3]);
+                    const uint32_t w2 = pack_bf16(v[8 * q + 4], v[8 * q + 5]), w3 = pack_bf16(v[8 * q + 6], v[8 * q + 7]);
+#pragma unroll
+                    for (int p = 0; p < NC; ++p) {
+                        const uint32_t dst = map_to_rank(aET + off, (uint32_t)p);
+                        asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(w0), "r"(w1),
+                                     "r"(w2), "r"(w3)
+                                     : "memory");
+                    }
+                }
+            }
+            cluster_sync();  // barrier B: e^T complete everywhere
+        }
+        handoff();
+        // ---- G3: rows 0..63: (W2^T e_t)[j] (A = e as [t][o] via the e^T tile, MN-major;
+        //      the upper 64 rows of the stacked operand are not read); the next v slice
+        const bool go3 = !failed;
+        if (go3 && tid == 0) {
+            const uint64_t dE = mdesc(aET, T128), dW2 = mdesc(aW2, T128);
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks)  // 16 output features per k-step
+                mma_bf16(tm + COL_X, dE + KS_M * ks, dW2 + KS_M * ks, ID_MB, ks ? 1u : 0u);
+            mma_commit(&bars[1]);
+            if (c + 1 < nchunks) issue_v(c + 1);
+        }
+        mma_wait(go3);
+        // ---- E3: delta = (W2^T e) (.) silu'(z) and its gamma / u scaled copies (rows 0..63)
+        if (qd < 2) {
+            float x[32], o1[32];
+            tmem_ld32(tl + COL_X + 32 * hf, x);
+            const int t = lr;
+            const float gm = -sGl[t], uu = sU[t];
+#pragma unroll
+            for (int q = 0; q < 32; ++q) x[q] *= ds[q];
+            put_row32(sm + L::DT, 64, t, 32 * hf, x);
+#pragma unroll
+            for (int q = 0; q < 32; ++q) o1[q] = gm * x[q];
+            put_row32(sm + L::DG, 64, t, 32 * hf, o1);
+#pragma unroll
+            for (int q = 0; q < 32; ++q) o1[q] = uu * x[q];
+            put_row32(sm + L::DU, 64, t, 32 * hf, o1);
+        }
+        handoff();
+        // ---- G4: [DU; P1] delta -> rows 64..127 sum_i P1[t][i] delta_i; state updates
+        //      W1^T += K^T (-gamma delta), S1^T += K^T (u delta), W2 += E^T (-gamma a(k)), S2 += E^T (u a(k))
+        const bool go4 = !failed;
+        if (go4 && tid == 0) {
+            const uint64_t dDUP = kdesc(aDU), dDT = mdesc(aDT, T64);
+            const uint64_t dKt = mdesc(aKQ, T128), dDG = mdesc(aDG, T64), dDU = mdesc(aDU, T64);
+            const uint64_t dET = kdesc(aET), dAKG = mdesc(aAKG, T64), dAKU = mdesc(aAKU, T64);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {  // 16 tokens per k-step
+                mma_bf16(tm + COL_R1, dDUP + KS_K * ks, dDT + KS_M * ks, ID_KB, ks ? 1u : 0u);
+                mma_bf16(tm + COL_W1, dKt + KS_M * ks, dDG + KS_M * ks, ID_MB, 1u);
+                mma_bf16(tm + COL_S1, dKt + KS_M * ks, dDU + KS_M * ks, ID_MB, 1u);
+                mma_bf16(tm + COL_W2, dET + KS_K * ks, dAKG + KS_M * ks, ID_KB, 1u);
+                mma_bf16(tm + COL_S2, dET + KS_K * ks, dAKU + KS_M * ks, ID_KB, 1u);
+            }
+            mma_commit(&bars[1]);
+        }
+        mma_wait(go4);
+        // the next chunk's q|k tiles (K^T and Q have been read)
+        if (tid == 0 && !failed && c + 1 < nchunks) issue_kq(c + 1);
+        // ---- E4 (rows 64..127): h_t = A_t W1 q_t - sigma_t S1 q_t - R1, a_t = silu(h_t)
+        if (qd >= 2) {
+            float xa[32], xb[32], r1[32];
+            tmem_ld32x3(tl + COL_XA + 32 * hf, tl + COL_XB + 32 * hf, tl + COL_R1 + 32 * hf, xa, xb, r1);
+            const int t = lr - 64;
+            const float At = sA[t], st = sSg[t];
+#pragma unroll
+            for (int q = 0; q < 32; ++q) {
+                const float h = fmaf(At, xa[q], -fmaf(st, xb[q], r1[q]));
+                xa[q] = h * sigmoid_f(h);
+            }
+            put_row32(sm + L::AQ, 64, t, 32 * hf, xa);
+        }
+        handoff();
+        // ---- G5: [AK; AQ] AK^T -> rows 64..127 a_t . a(k_i); [o][t] partial W2 a_t and S2 a_t
+        const bool go5 = !failed;
+        if (go5 && tid == 0) {
+            const uint64_t dAK = kdesc(aAK), dAQ = kdesc(aAQ), dW2 = kdesc(aW2), dS2 = kdesc(aS2);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+                mma_bf16(tm + COL_AA, dAK + KS_K * ks, dAK + KS_K * ks, ID_KK, ks ? 1u : 0u);
+            mma_commit(&bars[1]);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
+                mma_bf16(tm + COL_YW, dW2 + KS_K * ks, dAQ + KS_K * ks, ID_KK, ks ? 1u : 0u);
+                mma_bf16(tm + COL_YS, dS2 + KS_K * ks, dAQ + KS_K * ks, ID_KK, ks ? 1u : 0u);
+            }
+        }
+        mma_wait(go5);
+        // ---- E5 (rows 64..127): P2 = Gamma (.) (a_t . a(k_i)), partial over this CTA's slice
+        if (qd >= 2) {
+            float v[32], gr[32];
+            tmem_ld32(tl + COL_AA + 32 * hf, v);
+            const int t = lr - 64;
+            get_plain32(smem_u32(Gm + t * GST + 32 * hf), gr);
+#pragma unroll
+            for (int q = 0; q < 32; ++q) v[q] *= gr[q];
+            put_row32(sm + L::P, 64, t, 32 * hf, v);
+        }
+        handoff();
+        // ---- G6: [o][t] partial sum_i P2[t][i] e_i
+        const bool go6 = !failed;
+        if (go6 && tid == 0) {
+            const uint64_t dET = kdesc(aET), dP = kdesc(aP);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) mma_bf16(tm + COL_PE, dET + KS_K * ks, dP + KS_K * ks, ID_KK, ks ? 1u : 0u);
+            mma_commit(&bars[1]);
+        }
+        mma_wait(go6);
+        // ---- exchange 2: partial y [o][t] reduce-scattered onto the owners, who write
+        //      their rows of y; meanwhile the new state becomes the next chunk's operands
+        {
+            float yw[32], ys[32], pe[32];
+            tmem_ld32x3(tl + COL_YW + 32 * hf, tl + COL_YS + 32 * hf, tl + COL_PE + 32 * hf, yw, ys, pe);
+#pragma unroll
+            for (int q = 0; q < 32; ++q) {
+                const int t = 32 * hf + q;
+                yw[q] = fmaf(sA[t], yw[q], -fmaf(sSg[t], ys[q], pe[q]));
+            }
+            scatter_row(yw);
+            {
+                const bool last = c + 1 == nchunks;
+                float w[32];
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    const uint32_t col = (m == 0 ? COL_W1 : m == 1 ? COL_S1 : m == 2 ? COL_W2 : COL_S2) + 32 * hf;
+                    tmem_ld32(tl + col, w);
+                    if (!last) {
+                        const uint32_t off = m == 0 ? L::W1 : m == 1 ? L::S1 : m == 2 ? L::W2 : L::S2;
+                        put_row32(sm + off, 128, lr, 32 * hf, w);
+                    } else {
+                        float* dst = ((m & 1) ? a.S_T : a.M_T) + unit * P;
+                        if (m < 2) {  // W1[jg0 + j][x] for x = lr
+                            float* r = dst + (long long)(jg0 + 32 * hf) * D + lr;
+#pragma unroll
+                            for (int q = 0; q < 32; ++q) r[(long long)q * D] = w[q];
+                        } else {      // W2[o][jg0 + j] for o = lr
+                            float* r = dst + (long long)hid * D + (long long)lr * hid + jg0 + 32 * hf;
+#pragma unroll
+                            for (int q = 0; q < 32; q += 4)
+                                *reinterpret_cast<float4*>(r + q) = make_float4(w[q], w[q + 1], w[q + 2], w[q + 3]);
+                        }
+                    }
+                }
+            }
+            cluster_sync();  // barrier C
+            if (owner) {
+                gather_row(yw);
+#pragma unroll
+                for (int q = 0; q < 32; ++q) {
+                    const int t = 32 * hf + q;
+                    if (t < n) store_y1(y + (t0 + t) * D + lr, yw[q]);
+                }
+            }
+        }
+        // barrier D: the exchange buffer has been read before any peer refills it
+        // for the next chunk; the bf16 state copies are visible to the tensor cores
+        fence_proxy_async();
+        tc_fence_before();
+        cluster_sync();
+        tc_fence_after();
+    }
+    if (failed) {
+        if (tid == 0 && a.status) atomicExch(a.status, NM_ERR_DEVICE_TIMEOUT);
+        // let copies and products still in flight land before the CTA leaves
+        mbar_wait(&bars[0], (uint32_t)(nchunks & 1), WAIT_NS / 4);
+        mbar_wait(&bars[2], (uint32_t)(nchunks & 1), WAIT_NS / 4);
+        mbar_wait(&bars[1], mma_phase, WAIT_NS);
+    }
+    tc_fence_before();
+    cluster_sync();
+    if (warp == 0) tmem_dealloc(tm, 512);
+}
+
+// A [units][T][d] bf16 array read in boxes of `cols` features x 64 tokens x 1
+// unit without swizzle (a plain row-major [64][cols] tile).
+bool make_plain_map(CUtensorMap* m, const void* base, int d, long long T, long long units, int cols) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)T, (cuuint64_t)units};
+    cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)T * d * 2};
+    cuuint32_t box[3] = {(cuuint32_t)cols, 64, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int NC, typename Tout>
+cudaError_t launch(const nm_config& c, const nm_args& a, cudaStream_t s) {
+    using L = Layout<NC>;
+    CUtensorMap tq, tk, tv;
+    const long long units = (long long)a.B * a.H;
+    if (!make_token_map(&tq, a.q, D, a.T, units) || !make_token_map(&tk, a.k, D, a.T, units) ||
+        !make_plain_map(&tv, a.v, D, a.T, units, L::OR))
+        return cudaErrorInvalidValue;
+    auto kern = tc_mlpw_kernel<NC, Tout>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::BYTES);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(units * NC), 1, 1);
+    cfg.blockDim = dim3(NTHREADS, 1, 1);
+    cfg.dynamicSmemBytes = L::BYTES;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = NC;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, tq, tk, tv, a, c.c_mode);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+template <int NC>
+cudaError_t launch_nc(const nm_config& c, const nm_args& a, cudaStream_t s) {
+    return c.out_dtype == NM_BF16 ? launch<NC, __nv_bfloat16>(c, a, s) : launch<NC, float>(c, a, s);
+}
+
+}  // namespace
+
+bool nm_tc_mlp_wide_supports(const nm_config& c) {
+    return c.kind == NM_MLP2 && c.d == D && (c.hidden == 2 * HS || c.hidden == 4 * HS || c.hidden == 8 * HS) &&
+           c.chunk == BC && c.in_dtype == NM_BF16;
+}
+
+cudaError_t nm_tc_mlp_wide_launch(const nm_config& c, const nm_args& a, cudaStream_t s) {
+    if (c.hidden == 2 * HS) return launch_nc<2>(c, a, s);
+    if (c.hidden == 4 * HS) return launch_nc<4>(c, a, s);
+    return launch_nc<8>(c, a, s);
+}

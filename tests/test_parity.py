@@ -276,3 +276,20 @@ def test_mlp_tc_momentum_forms(c_mode):
     M0, S0 = W.random_state(wl, "cuda", seed=72)
     gpu = gpu_forward(wl, x, nm.PATH_TC, M0=M0, S0=S0, c_mode=c_mode)
     compare(wl, gpu, oracle_forward(wl, x, M0=M0, S0=S0, c_mode=c_mode))
+
+
+@pytest.mark.parametrize("hidden", [128, 256, 512])
+@pytest.mark.parametrize("T,eta_scale", [(64, 1.0), (100, 1.0), (257, 0.5)])
+def test_mlp_tc_d128_clusters(hidden, T, eta_scale):
+    """The tensor-core MLP kernel for d = 128 with 2, 4 and 8 CTAs per unit
+    (64 hidden units each), on ragged lengths from random states; the run
+    over five chunks halves the step eta (the oracle's own weights grow
+    without bound under the workload's steps from these states)."""
+    wl = dataclasses.replace(W.WORKLOADS[3], hidden=hidden).with_sizes(B=1, H=2, T=T)
+    _skip_unsupported(wl, nm.PATH_TC)
+    x = W.make_inputs(wl, "cuda", seed=80 + T + hidden)
+    x["eta"] *= eta_scale
+    M0, S0 = W.random_state(wl, "cuda", seed=hidden + T, scale=0.5)
+    gpu = gpu_forward(wl, x, nm.PATH_TC, M0=M0, S0=S0)
+    assert gpu[3] == nm.PATH_TC
+    compare(wl, gpu, oracle_forward(wl, x, M0=M0, S0=S0))
