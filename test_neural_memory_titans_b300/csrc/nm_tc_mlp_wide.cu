@@ -23,6 +23,7 @@
 // wanted half of the result is read).  The sums over the hidden dimension go
 // through distributed shared memory:
 //   * the key forward W2 a(k_t): each CTA's partial [o][t] is reduce-scattered
+//     (the partials travel as bf16, the sum is taken in fp32)
 //     (CTA r owns output rows [128 r / NC, 128 (r + 1) / NC)); the owner forms
 //     e for its rows and all-gathers e^T as bf16 into every CTA;
 //   * the retrieval y: the partials [o][t] are reduce-scattered the same way
@@ -45,7 +46,8 @@ constexpr int NTHREADS = 256;
 constexpr uint32_t T64 = 64 * 128;    // [64 rows][64 bf16] swizzled tile (8 KB)
 constexpr uint32_t T128 = 128 * 128;  // [128 rows][64 bf16] (16 KB)
 constexpr int GST = 72;               // Gamma row stride (bf16 elements)
-constexpr int RXS = 68;               // exchange row stride (floats)
+constexpr int RXS = 68;               // row stride of the own partial (floats)
+constexpr int RBS = 72;               // row stride of the peers' partials (bf16 elements)
 
 template <int NC>
 struct Layout {
@@ -66,14 +68,17 @@ struct Layout {
     static constexpr uint32_t P = DU + T64;         // [64 t][64 i] Gamma (.) inner products (follows DU: stacked operand)
     static constexpr uint32_t GM = P + T64;         // bf16 Gamma [64][GST]
     static constexpr uint32_t V = GM + 64 * GST * 2;              // bf16 [64 t][OR] this CTA's columns of v
-    static constexpr uint32_t RX = V + 64 * OR * 2;               // fp32 [NC-1][OR][RXS] partials from the peers
-    static constexpr uint32_t F = RX + (NC - 1) * OR * RXS * 4;   // gates [4][64], A, B, sigma, gamma, u
+    static constexpr uint32_t RX = V + 64 * OR * 2;               // bf16 [NC-1][OR][RBS] partials from the peers
+    static constexpr uint32_t F = RX + (NC - 1) * OR * RBS * 2;   // gates [4][64], A, B, sigma, gamma, u
     static constexpr uint32_t BAR = F + 4 * (4 * BC + 5 * BC);
     static constexpr uint32_t USED = BAR + 64;
     static constexpr uint32_t BYTES = USED + 1024;  // slack for the 1024-byte alignment
     static_assert(BYTES <= 232448, "shared memory budget");
     static_assert(AQ == AK + T64 && P == DU + T64, "stacked operands");
-    static_assert(GM % 128 == 0 && V % 128 == 0 && RX % 16 == 0, "alignment");
+    static_assert(GM % 128 == 0 && V % 128 == 0 && RX % 16 == 0 && (RBS * 2) % 16 == 0, "alignment");
+    // the owner's own partial rows (fp32 [OR][RXS]) during an exchange live in
+    // the delta tiles, which are dead at both exchange points
+    static_assert(OR * RXS * 4 <= 3 * T64, "own partial fits the delta tiles");
 };
 
 // TMEM columns
@@ -148,7 +153,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     float* sGl = sSg + BC;
     float* sU = sGl + BC;
     __nv_bfloat16* Gm = reinterpret_cast<__nv_bfloat16*>(sm + L::GM);
-    float* RX = reinterpret_cast<float*>(sm + L::RX);
+    __nv_bfloat16* RX = reinterpret_cast<__nv_bfloat16*>(sm + L::RX);
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::BAR);  // 0: q|k tiles, 1: mma, 2: v slice
     __shared__ uint32_t s_tmem;
 
@@ -271,28 +276,38 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     };
     // Sends this thread's 32 partial values of row lr (columns 32 hf ..) to the
     // CTA owning the row (its exchange slot for this CTA), or keeps them.
+    float* OWN = reinterpret_cast<float*>(sm + L::DT);  // fp32 [OR][RXS] during an exchange
     auto scatter_row = [&](const float* v) {
         const int q_own = lr / OR;
-        if (q_own != rank) {
+        if (q_own == rank) {
+            float* dst = OWN + (size_t)(lr - own_lo) * RXS + 32 * hf;
+#pragma unroll
+            for (int q = 0; q < 32; q += 4) *reinterpret_cast<float4*>(dst + q) = make_float4(v[q], v[q + 1], v[q + 2], v[q + 3]);
+        } else {
+            // partial sums travel as bf16 (the sums themselves are taken in fp32)
             const int slot = rank < q_own ? rank : rank - 1;
             const uint32_t dst =
-                map_to_rank(smem_u32(RX + ((size_t)slot * OR + (lr - OR * q_own)) * RXS + 32 * hf), (uint32_t)q_own);
+                map_to_rank(smem_u32(RX + ((size_t)slot * OR + (lr - OR * q_own)) * RBS + 32 * hf), (uint32_t)q_own);
 #pragma unroll
-            for (int q = 0; q < 8; ++q) st_cluster_v4(dst + 16 * q, v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+            for (int q = 0; q < 4; ++q)
+                asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst + 16 * q),
+                             "r"(pack_bf16(v[8 * q], v[8 * q + 1])), "r"(pack_bf16(v[8 * q + 2], v[8 * q + 3])),
+                             "r"(pack_bf16(v[8 * q + 4], v[8 * q + 5])), "r"(pack_bf16(v[8 * q + 6], v[8 * q + 7]))
+                             : "memory");
         }
     };
-    // Adds the peers' partials of an owned row (after the barrier).
-    auto gather_row = [&](float* v) {
+    // After the barrier: the sum over the cluster of 4 consecutive columns
+    // (tokens 4 c4 .. 4 c4 + 3) of owned row `row` (own partial + the peers').
+    auto reduce4 = [&](int row, int c4) {
+        float4 acc = *reinterpret_cast<const float4*>(OWN + (size_t)row * RXS + 4 * c4);
 #pragma unroll
-        for (int s = 0; s < NC - 1; ++s) {
-            const float* src = RX + ((size_t)s * OR + (lr - own_lo)) * RXS + 32 * hf;
-#pragma unroll
-            for (int q = 0; q < 32; q += 4) {
-                const float4 w = *reinterpret_cast<const float4*>(src + q);
-                v[q] += w.x; v[q + 1] += w.y; v[q + 2] += w.z; v[q + 3] += w.w;
-            }
+        for (int sl = 0; sl < NC - 1; ++sl) {
+            const uint2 w = *reinterpret_cast<const uint2*>(RX + ((size_t)sl * OR + row) * RBS + 4 * c4);
+            acc.x += bf16_lo(w.x); acc.y += bf16_hi(w.x); acc.z += bf16_lo(w.y); acc.w += bf16_hi(w.y);
         }
+        return acc;
     };
+    constexpr int TASKS = OR * 16;  // owned rows x 16 groups of 4 tokens
 
     float ds[32];  // silu'(z) of this thread's token row (rows 0..63), kept from E1 to E3
     for (int c = 0; c < nchunks; ++c) {
@@ -457,26 +472,25 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             if (owner && !failed) okv = mbar_wait(&bars[2], (uint32_t)(c & 1), WAIT_NS);
             failed = __syncthreads_or(!okv) || failed;
             cluster_sync();  // barrier A
-            if (owner) {
-                gather_row(v);
+            // every thread: e = 2 (yhat - v) for 4 tokens of an owned row, all-gathered as bf16
+            {
                 const __nv_bfloat16* vs = reinterpret_cast<const __nv_bfloat16*>(sm + L::V);
+                for (int task = tid; task < TASKS; task += NTHREADS) {
+                    const int row = task >> 4, c4 = task & 15;
+                    const float4 sum = reduce4(row, c4);
+                    const float sv[4] = {sum.x, sum.y, sum.z, sum.w};
+                    float e[4];
 #pragma unroll
-                for (int q = 0; q < 32; ++q) {
-                    const int t = 32 * hf + q;
-                    v[q] = t < n ? 2.0f * (v[q] - __bfloat162float(vs[t * OR + (lr - own_lo)])) : 0.0f;
-                }
-                // e^T row lr into every CTA of the cluster (same swizzled place)
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const uint32_t off = sw128_offset(lr, 32 * hf + 8 * q, 128);
-                    const uint32_t w0 = pack_bf16(v[8 * q], v[8 * q + 1]), w1 = pack_bf16(v[8 * q + 2], v[8 * q + 3]);
-                    const uint32_t w2 = pack_bf16(v[8 * q + 4], v[8 * q + 5]), w3 = pack_bf16(v[8 * q + 6], v[8 * q + 7]);
+                    for (int k = 0; k < 4; ++k) {
+                        const int t = 4 * c4 + k;
+                        e[k] = t < n ? 2.0f * (sv[k] - __bfloat162float(vs[t * OR + row])) : 0.0f;
+                    }
+                    const uint32_t w0 = pack_bf16(e[0], e[1]), w1 = pack_bf16(e[2], e[3]);
+                    const uint32_t off = sw128_offset(own_lo + row, 4 * c4, 128);
 #pragma unroll
                     for (int p = 0; p < NC; ++p) {
                         const uint32_t dst = map_to_rank(aET + off, (uint32_t)p);
-                        asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(w0), "r"(w1),
-                                     "r"(w2), "r"(w3)
-                                     : "memory");
+                        asm volatile("st.shared::cluster.v2.b32 [%0], {%1, %2};" ::"r"(dst), "r"(w0), "r"(w1) : "memory");
                     }
                 }
             }
@@ -618,12 +632,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 }
             }
             cluster_sync();  // barrier C
-            if (owner) {
-                gather_row(yw);
+            // every thread: 4 tokens of an owned row of y
+            for (int task = tid; task < TASKS; task += NTHREADS) {
+                const int row = task >> 4, c4 = task & 15;
+                const float4 sum = reduce4(row, c4);
+                const float sv[4] = {sum.x, sum.y, sum.z, sum.w};
 #pragma unroll
-                for (int q = 0; q < 32; ++q) {
-                    const int t = 32 * hf + q;
-                    if (t < n) store_y1(y + (t0 + t) * D + lr, yw[q]);
+                for (int k = 0; k < 4; ++k) {
+                    const int t = 4 * c4 + k;
+                    if (t < n) store_y1(y + (t0 + t) * D + own_lo + row, sv[k]);
                 }
             }
         }
