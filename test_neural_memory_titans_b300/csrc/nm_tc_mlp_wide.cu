@@ -476,7 +476,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             {
                 const __nv_bfloat16* vs = reinterpret_cast<const __nv_bfloat16*>(sm + L::V);
                 for (int task = tid; task < TASKS; task += NTHREADS) {
-                    const int row = task >> 4, c4 = task & 15;
+                    const int row = task >> 4, c4 = task & 15;  // consecutive threads: one row's tokens
                     const float4 sum = reduce4(row, c4);
                     const float sv[4] = {sum.x, sum.y, sum.z, sum.w};
                     float e[4];
@@ -634,7 +634,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             cluster_sync();  // barrier C
             // every thread: 4 tokens of an owned row of y
             for (int task = tid; task < TASKS; task += NTHREADS) {
-                const int row = task >> 4, c4 = task & 15;
+                const int row = task % OR, c4 = task / OR;  // consecutive threads: consecutive rows
                 const float4 sum = reduce4(row, c4);
                 const float sv[4] = {sum.x, sum.y, sum.z, sum.w};
 #pragma unroll
