@@ -6,10 +6,13 @@ cudaError_t nm_tc_linear_launch(const nm_config& c, const nm_args& a, cudaStream
 bool nm_tc_mlp_supports(const nm_config& c);
 cudaError_t nm_tc_mlp_launch(const nm_config& c, const nm_args& a, cudaStream_t s);
 bool nm_tc_mlp_wide_supports(const nm_config& c);
+bool nm_tc_linear64_supports(const nm_config& c);
+cudaError_t nm_tc_linear64_launch(const nm_config& c, const nm_args& a, cudaStream_t s);
 cudaError_t nm_tc_mlp_wide_launch(const nm_config& c, const nm_args& a, cudaStream_t s);
 
 bool nm_tc_supports(const nm_config& c) {
-    return nm_tc_linear_supports(c) || nm_tc_mlp_supports(c) || nm_tc_mlp_wide_supports(c);
+    return nm_tc_linear_supports(c) || nm_tc_linear64_supports(c) || nm_tc_mlp_supports(c) ||
+           nm_tc_mlp_wide_supports(c);
 }
 
 size_t nm_tc_scratch_bytes(const nm_config& c, int B, int H) {
@@ -21,6 +24,7 @@ cudaError_t nm_tc_launch(const nm_config& c, const nm_args& a, cudaStream_t s, i
     (void)num_sms;
     cudaError_t e = cudaErrorNotSupported;
     if (nm_tc_linear_supports(c)) e = nm_tc_linear_launch(c, a, s);
+    else if (nm_tc_linear64_supports(c)) e = nm_tc_linear64_launch(c, a, s);
     else if (nm_tc_mlp_supports(c)) e = nm_tc_mlp_launch(c, a, s);
     else if (nm_tc_mlp_wide_supports(c)) e = nm_tc_mlp_wide_launch(c, a, s);
     if (e == cudaSuccess) *launches += 1;

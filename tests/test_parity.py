@@ -293,3 +293,35 @@ def test_mlp_tc_d128_clusters(hidden, T, eta_scale):
     gpu = gpu_forward(wl, x, nm.PATH_TC, M0=M0, S0=S0)
     assert gpu[3] == nm.PATH_TC
     compare(wl, gpu, oracle_forward(wl, x, M0=M0, S0=S0))
+
+
+@pytest.mark.parametrize("chunk", [64, 128, 256])
+@pytest.mark.parametrize("T", [1, 300, 700])
+def test_linear_d64_blocked_chunks(chunk, T):
+    """The d = 64 tensor-core kernel processes a chunk of 64, 128 or 256
+    tokens as 64-token blocks (earlier blocks through two d x d
+    accumulators); ragged lengths from random states, with degenerate gates
+    inside a chunk (alpha = 1, beta = 0 and eta = 0 stretches)."""
+    wl = dataclasses.replace(W.WORKLOADS[4], chunk=chunk).with_sizes(B=1, H=3, T=T, segment=0)
+    _skip_unsupported(wl, nm.PATH_TC)
+    x = W.make_inputs(wl, "cuda", seed=90 + T + chunk)
+    if T > 200:
+        x["alpha"][:, :, 150] = 1.0
+        x["beta"][:, :, 60:75] = 0.0
+        x["eta"][:, :, 100:110] = 0.0
+    M0, S0 = W.random_state(wl, "cuda", seed=T + chunk, scale=0.5)
+    gpu = gpu_forward(wl, x, nm.PATH_TC, M0=M0, S0=S0)
+    assert gpu[3] == nm.PATH_TC
+    compare(wl, gpu, oracle_forward(wl, x, M0=M0, S0=S0))
+
+
+@pytest.mark.parametrize("c_mode", [nm.C_ONE_MINUS_BETA, nm.C_PER_TOKEN])
+def test_linear_d64_momentum_forms(c_mode):
+    wl = W.WORKLOADS[4].with_sizes(B=1, H=2, T=600, segment=0)
+    _skip_unsupported(wl, nm.PATH_TC)
+    x = W.make_inputs(wl, "cuda", seed=95)
+    if c_mode == nm.C_PER_TOKEN:
+        x["c"] = torch.rand(x["alpha"].shape, device="cuda", generator=torch.Generator("cuda").manual_seed(6))
+    M0, S0 = W.random_state(wl, "cuda", seed=96, scale=0.5)
+    gpu = gpu_forward(wl, x, nm.PATH_TC, M0=M0, S0=S0, c_mode=c_mode)
+    compare(wl, gpu, oracle_forward(wl, x, M0=M0, S0=S0, c_mode=c_mode))
