@@ -76,11 +76,12 @@ constexpr uint32_t OFF_EG = OFF_E + T64;      // -gamma_t e_t
 constexpr uint32_t OFF_EU = OFF_EG + T64;     // u_t e_t
 constexpr uint32_t OFF_P = OFF_EU + T64;      // [64 t][64 i]   Gamma (.) inner products
 constexpr int GS = 68;                        // padded fp32 row stride (conflict-free row reads)
-constexpr int RS = 36;
 constexpr uint32_t OFF_GM = OFF_P + T64;                // fp32 Gamma [64][GS]
-constexpr uint32_t OFF_YX = OFF_GM + 64 * GS * 4;       // fp32 [64][GS] the peer's partial key forward
-constexpr uint32_t OFF_YR = OFF_YX + 64 * GS * 4;       // fp32 [64][RS] the peer's partial y (own columns)
-constexpr uint32_t OFF_F = OFF_YR + 64 * RS * 4;        // gates [2][4][64], A, B, sigma, gamma, u
+constexpr int XS = 72;                                  // bf16 row stride of the key-forward exchange
+constexpr int RB = 40;                                  // bf16 row stride of the y exchange
+constexpr uint32_t OFF_YX = OFF_GM + 64 * GS * 4;       // bf16 [64][XS] the peer's partial key forward
+constexpr uint32_t OFF_YR = OFF_YX + 64 * XS * 2;       // bf16 [64][RB] the peer's partial y (own columns)
+constexpr uint32_t OFF_F = OFF_YR + 64 * RB * 2;        // gates [2][4][64], A, B, sigma, gamma, u
 constexpr uint32_t N_F = 2 * 4 * BC + 5 * BC;
 constexpr uint32_t OFF_BAR = OFF_F + 4 * N_F;
 constexpr uint32_t SMEM_USED = OFF_BAR + 64;
@@ -166,6 +167,28 @@ __device__ __forceinline__ void store_y(float* p, const float* v) {
         reinterpret_cast<float4*>(p)[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
 }
 
+// W values as bf16 into a peer's shared memory (16-byte stores) / back to floats.
+template <int W>
+__device__ __forceinline__ void push_bf16(uint32_t dst, const float* v) {
+#pragma unroll
+    for (int q = 0; q < W / 8; ++q)
+        asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst + 16 * q),
+                     "r"(pack_bf16(v[8 * q], v[8 * q + 1])), "r"(pack_bf16(v[8 * q + 2], v[8 * q + 3])),
+                     "r"(pack_bf16(v[8 * q + 4], v[8 * q + 5])), "r"(pack_bf16(v[8 * q + 6], v[8 * q + 7]))
+                     : "memory");
+}
+template <int W>
+__device__ __forceinline__ void pull_bf16(uint32_t src, float* v) {
+#pragma unroll
+    for (int q = 0; q < W / 8; ++q) {
+        const uint4 w = ld_shared_v4(src + 16 * q);
+        v[8 * q + 0] = bf16_lo(w.x); v[8 * q + 1] = bf16_hi(w.x);
+        v[8 * q + 2] = bf16_lo(w.y); v[8 * q + 3] = bf16_hi(w.y);
+        v[8 * q + 4] = bf16_lo(w.z); v[8 * q + 5] = bf16_hi(w.z);
+        v[8 * q + 6] = bf16_lo(w.w); v[8 * q + 7] = bf16_hi(w.w);
+    }
+}
+
 template <int NC, int CW, typename Tout>
 __global__ void __launch_bounds__(128 * (64 / CW), 1)
     tc_mlp_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
@@ -179,8 +202,9 @@ __global__ void __launch_bounds__(128 * (64 / CW), 1)
     float* sGl = sSg + BC;
     float* sU = sGl + BC;
     float* Gm = reinterpret_cast<float*>(sm + OFF_GM);
-    float* Yx = reinterpret_cast<float*>(sm + OFF_YX);
-    float* Yr = reinterpret_cast<float*>(sm + OFF_YR);
+    // exchange buffers: the peer's partial sums as bf16 (summed here in fp32)
+    __nv_bfloat16* Yx = reinterpret_cast<__nv_bfloat16*>(sm + OFF_YX);  // [64][XS]
+    __nv_bfloat16* Yr = reinterpret_cast<__nv_bfloat16*>(sm + OFF_YR);  // [64][RB]
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + OFF_BAR);  // 0: tiles, 1: mma
     __shared__ uint32_t s_tmem;
 
@@ -447,10 +471,8 @@ __global__ void __launch_bounds__(128 * (64 / CW), 1)
             tmem_ld_n(tl + COL_YH + CW * hq, ev);
             if (r64) {
                 if (NC > 1) {
-                    const uint32_t dst = map_to_rank(smem_u32(Yx + tr * GS + CW * hq), (uint32_t)peer);
-#pragma unroll
-                    for (int q = 0; q < CW / 4; ++q)
-                        st_cluster_v4(dst + 16 * q, ev[4 * q], ev[4 * q + 1], ev[4 * q + 2], ev[4 * q + 3]);
+                    const uint32_t dst = map_to_rank(smem_u32(Yx + tr * XS + CW * hq), (uint32_t)peer);
+                    push_bf16<CW>(dst, ev);
                 }
                 float vv[CW];
                 get_row<CW>(sm + OFF_V, 64, tr, CW * hq, vv);
@@ -479,15 +501,10 @@ __global__ void __launch_bounds__(128 * (64 / CW), 1)
         if (NC > 1) cluster_sync();
         if (r64) {
             if (NC > 1) {
-                const float* yx = Yx + tr * GS + CW * hq;
+                float px[CW];
+                pull_bf16<CW>(smem_u32(Yx + tr * XS + CW * hq), px);
 #pragma unroll
-                for (int q = 0; q < CW; q += 4) {
-                    const float4 w = *reinterpret_cast<const float4*>(yx + q);
-                    ev[q] = fmaf(2.0f, w.x, ev[q]);
-                    ev[q + 1] = fmaf(2.0f, w.y, ev[q + 1]);
-                    ev[q + 2] = fmaf(2.0f, w.z, ev[q + 2]);
-                    ev[q + 3] = fmaf(2.0f, w.w, ev[q + 3]);
-                }
+                for (int q = 0; q < CW; ++q) ev[q] = fmaf(2.0f, px[q], ev[q]);
             }
             put_row<CW>(sm + OFF_E, 64, tr, CW * hq, ev);
             float o1[CW];
@@ -614,10 +631,8 @@ __global__ void __launch_bounds__(128 * (64 / CW), 1)
 #pragma unroll
                 for (int q = 0; q < CW; ++q) yw[q] = fmaf(At, yw[q], -fmaf(st, ys[q], pe[q]));
                 if (!own) {
-                    const uint32_t dst = map_to_rank(smem_u32(Yr + tr * RS + (CW * hq) % 32), (uint32_t)peer);
-#pragma unroll
-                    for (int q = 0; q < CW / 4; ++q)
-                        st_cluster_v4(dst + 16 * q, yw[4 * q], yw[4 * q + 1], yw[4 * q + 2], yw[4 * q + 3]);
+                    const uint32_t dst = map_to_rank(smem_u32(Yr + tr * RB + (CW * hq) % 32), (uint32_t)peer);
+                    push_bf16<CW>(dst, yw);
                 }
             }
             // while the peer's partial y arrives: the new state becomes the next
@@ -650,12 +665,10 @@ __global__ void __launch_bounds__(128 * (64 / CW), 1)
             if (NC > 1) cluster_sync();
             if (r64 && own && tr < n) {
                 if (NC > 1) {
-                    const float* yr = Yr + tr * RS + (CW * hq) % 32;
+                    float pr[CW];
+                    pull_bf16<CW>(smem_u32(Yr + tr * RB + (CW * hq) % 32), pr);
 #pragma unroll
-                    for (int q = 0; q < CW; q += 4) {
-                        const float4 w = *reinterpret_cast<const float4*>(yr + q);
-                        yw[q] += w.x; yw[q + 1] += w.y; yw[q + 2] += w.z; yw[q + 3] += w.w;
-                    }
+                    for (int q = 0; q < CW; ++q) yw[q] += pr[q];
                 }
                 store_y<CW>(y + (t0 + tr) * D + CW * hq, yw);
             }
