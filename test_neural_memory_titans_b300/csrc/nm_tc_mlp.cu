@@ -76,13 +76,13 @@ constexpr uint32_t OFF_EG = OFF_E + T64;      // -gamma_t e_t
 constexpr uint32_t OFF_EU = OFF_EG + T64;     // u_t e_t
 constexpr uint32_t OFF_P = OFF_EU + T64;      // [64 t][64 i]   Gamma (.) inner products
 constexpr int GS = 68;                        // padded fp32 row stride (conflict-free row reads)
-constexpr uint32_t OFF_GM = OFF_P + T64;                // fp32 Gamma [64][GS]
+constexpr uint32_t OFF_GM = OFF_P + T64;                // fp32 Gamma [2 stages][64][GS]
 constexpr int XS = 72;                                  // bf16 row stride of the key-forward exchange
 constexpr int RB = 40;                                  // bf16 row stride of the y exchange
-constexpr uint32_t OFF_YX = OFF_GM + 64 * GS * 4;       // bf16 [64][XS] the peer's partial key forward
+constexpr uint32_t OFF_YX = OFF_GM + 2 * 64 * GS * 4;   // bf16 [64][XS] the peer's partial key forward
 constexpr uint32_t OFF_YR = OFF_YX + 64 * XS * 2;       // bf16 [64][RB] the peer's partial y (own columns)
-constexpr uint32_t OFF_F = OFF_YR + 64 * RB * 2;        // gates [2][4][64], A, B, sigma, gamma, u
-constexpr uint32_t N_F = 2 * 4 * BC + 5 * BC;
+constexpr uint32_t OFF_F = OFF_YR + 64 * RB * 2;        // gates [2][4][64]; scan [2][A, B, sigma, gamma, u][64]
+constexpr uint32_t N_F = 2 * 4 * BC + 2 * 5 * BC;
 constexpr uint32_t OFF_BAR = OFF_F + 4 * N_F;
 constexpr uint32_t SMEM_USED = OFF_BAR + 64;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;  // slack for the 1024-byte alignment
@@ -126,10 +126,6 @@ __device__ __forceinline__ uint64_t kdesc(uint32_t a) { return desc_hi(16) | ((a
 __device__ __forceinline__ uint64_t mdesc(uint32_t a, uint32_t lbo) { return desc_hi(lbo) | ((a >> 4) & 0x3FFFu); }
 constexpr uint64_t KS_K = 2, KS_M = 128;
 
-// sigmoid with the fast exponential and reciprocal; z is clamped below at
-// -80 so that 1 + e^{-z} stays finite (silu and its derivative are 0 to
-// within fp32 there)
-__device__ __forceinline__ float sigmoid_f(float z) { return __fdividef(1.0f, 1.0f + __expf(-fmaxf(z, -80.0f))); }
 __device__ __forceinline__ float silu_f(float z) { return z * sigmoid_f(z); }
 
 __device__ __forceinline__ float momentum_c(int mode, float beta, const float* c, long long i) {
@@ -196,12 +192,8 @@ __global__ void __launch_bounds__(128 * (64 / CW), 1)
     extern __shared__ unsigned char smem_raw[];
     unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     float* gates = reinterpret_cast<float*>(sm + OFF_F);  // [2 stages][a, eta, beta, c][64]
-    float* sA = gates + 2 * 4 * BC;
-    float* sBc = sA + BC;
-    float* sSg = sBc + BC;
-    float* sGl = sSg + BC;
-    float* sU = sGl + BC;
-    float* Gm = reinterpret_cast<float*>(sm + OFF_GM);
+    float* scan_out = gates + 2 * 4 * BC;                 // [2 stages][A, B, sigma, gamma, u][64]
+    float* gamma_all = reinterpret_cast<float*>(sm + OFF_GM);  // [2 stages][64][GS]
     // exchange buffers: the peer's partial sums as bf16 (summed here in fp32)
     __nv_bfloat16* Yx = reinterpret_cast<__nv_bfloat16*>(sm + OFF_YX);  // [64][XS]
     __nv_bfloat16* Yr = reinterpret_cast<__nv_bfloat16*>(sm + OFF_YR);  // [64][RB]
@@ -268,12 +260,90 @@ __global__ void __launch_bounds__(128 * (64 / CW), 1)
         tma_load_3d(sm + OFF_V, &tv, &bars[0], 0, t0, (int)unit);
     };
 
+    // The scan of one chunk's gates (stage st), one chunk ahead of its use:
+    // Gamma column by column (threads 128..191, the division-free recursion
+    // Gamma_{t,i} = a_t Gamma_{t-1,i} + eta_t u_{t,i}, zero above the
+    // diagonal), gamma_i = Gamma_{n-1,i} and u_i = u_{n-1,i}; A, B, sigma by
+    // thread 224.
+    auto scan = [&](int st) {
+        const float* g = gates + st * 4 * BC;
+        float* so = scan_out + st * 5 * BC;
+        if (tid >= 128 && tid < 128 + BC) {
+            float* Gm = gamma_all + st * 64 * GS;
+            const int i = tid - 128;
+            float u = g[3 * BC + i];
+            float G = g[BC + i] * u;
+            const float4* g4 = reinterpret_cast<const float4*>(g);
+#pragma unroll
+            for (int t4 = 0; t4 < BC / 4; ++t4) {
+                const float4 va = g4[t4], ve = g4[BC / 4 + t4], vb = g4[BC / 2 + t4];
+                const float ga[4] = {va.x, va.y, va.z, va.w}, ge[4] = {ve.x, ve.y, ve.z, ve.w},
+                            gb[4] = {vb.x, vb.y, vb.z, vb.w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int t = 4 * t4 + k;
+                    if (t > i) {
+                        u *= gb[k];
+                        G = fmaf(ga[k], G, ge[k] * u);
+                    }
+                    Gm[t * GS + i] = t >= i ? G : 0.0f;
+                }
+            }
+            so[3 * BC + i] = G;
+            so[4 * BC + i] = u;
+        } else if (tid == 224) {
+            float A = 1.f, Bc = 1.f, sg = 0.f;
+            const float4* g4 = reinterpret_cast<const float4*>(g);
+#pragma unroll
+            for (int t4 = 0; t4 < BC / 4; ++t4) {
+                const float4 va = g4[t4], ve = g4[BC / 4 + t4], vb = g4[BC / 2 + t4];
+                const float ga[4] = {va.x, va.y, va.z, va.w}, ge[4] = {ve.x, ve.y, ve.z, ve.w},
+                            gb[4] = {vb.x, vb.y, vb.z, vb.w};
+                float oa[4], ob[4], os[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    A *= ga[k];
+                    Bc *= gb[k];
+                    sg = fmaf(ga[k], sg, ge[k] * Bc);
+                    oa[k] = A;
+                    ob[k] = Bc;
+                    os[k] = sg;
+                }
+                reinterpret_cast<float4*>(so)[t4] = make_float4(oa[0], oa[1], oa[2], oa[3]);
+                reinterpret_cast<float4*>(so + BC)[t4] = make_float4(ob[0], ob[1], ob[2], ob[3]);
+                reinterpret_cast<float4*>(so + 2 * BC)[t4] = make_float4(os[0], os[1], os[2], os[3]);
+            }
+        }
+    };
     load_gates(0, 0);
+    __syncthreads();
+    scan(0);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tm = s_tmem;
     const uint32_t tl = tm + ((uint32_t)(32 * qd) << 16);  // this warp's lane quadrant
+    // The fp32 state m (0..3: W1, S1, W2, S2) from TMEM into its bf16 operand
+    // copy in shared memory, or after the last chunk into M_T / S_T.
+    auto convert_state = [&](int m, bool last) {
+        float w[CW];
+        tmem_ld_n(tl + (m == 0 ? COL_W1 : m == 1 ? COL_S1 : m == 2 ? COL_W2 : COL_S2) + CW * hq, w);
+        if (!last) {
+            put_row<CW>(sm + (m == 0 ? OFF_W1 : m == 1 ? OFF_S1 : m == 2 ? OFF_W2 : OFF_S2), 128, jr, CW * hq, w);
+        } else {
+            float* dst = (m & 1) ? a.S_T + unit * P : a.M_T + unit * P;
+            if (m < 2) {
+                float* r = dst + (long long)j_glob * D + CW * hq;
+#pragma unroll
+                for (int q = 0; q < CW; q += 4)
+                    *reinterpret_cast<float4*>(r + q) = make_float4(w[q], w[q + 1], w[q + 2], w[q + 3]);
+            } else {
+                float* r = dst + (long long)hid * D + j_glob;
+#pragma unroll
+                for (int q = 0; q < CW; ++q) r[(long long)(CW * hq + q) * hid] = w[q];
+            }
+        }
+    };
     if (tid == 0 && nchunks > 0 && !a.skip_first_load) issue_tiles(0);  // (the test hook skips it)
 
     // initial state: fp32 into TMEM, bf16 operand copies into shared memory
@@ -336,7 +406,10 @@ __global__ void __launch_bounds__(128 * (64 / CW), 1)
         const int stage = c & 1;
         const long long t0 = (long long)c * BC;
         const int n = (int)min((long long)BC, T - t0);
-        const float* g = gates + stage * 4 * BC;
+        // this chunk's scan (computed during the previous chunk)
+        const float* so = scan_out + stage * 5 * BC;
+        const float *sA = so, *sBc = so + BC, *sSg = so + 2 * BC, *sGl = so + 3 * BC, *sU = so + 4 * BC;
+        const float* Gm = gamma_all + stage * 64 * GS;
         // the next chunk's gates: warps 2-3 load them now (raw, so that nothing
         // waits for the loads until they are stored to shared memory after E2)
         const int gi = tid - 64;
@@ -350,8 +423,7 @@ __global__ void __launch_bounds__(128 * (64 / CW), 1)
             if (c_mode == NM_C_PER_TOKEN) nxt_c = cc[t];
         }
 
-        // ---- G1 (thread 0, as soon as the tiles land): W1 [q|k], S1 q, Q K^T;
-        //      meanwhile the scan of the chunk's gates: Gamma (by columns), gamma, u; A, B, sigma
+        // ---- G1 (thread 0, as soon as the tiles land): W1 [q|k], S1 q, Q K^T
         bool tiles_ok = true;
         if (tid == 0 && !failed) {
             tiles_ok = mbar_wait(&bars[0], (uint32_t)(c & 1), WAIT_NS);
@@ -368,53 +440,7 @@ __global__ void __launch_bounds__(128 * (64 / CW), 1)
                 mma_commit(&bars[1]);
             }
         }
-        if (tid >= 128 && tid < 128 + BC) {
-            // column i of Gamma: Gamma_{t,i} = a_t Gamma_{t-1,i} + eta_t u_{t,i}, zero above the diagonal
-            const int i = tid - 128;
-            float u = g[3 * BC + i];
-            float G = g[BC + i] * u;
-            const float4* g4 = reinterpret_cast<const float4*>(g);
-#pragma unroll
-            for (int t4 = 0; t4 < BC / 4; ++t4) {
-                const float4 va = g4[t4], ve = g4[BC / 4 + t4], vb = g4[BC / 2 + t4];
-                const float ga[4] = {va.x, va.y, va.z, va.w}, ge[4] = {ve.x, ve.y, ve.z, ve.w},
-                            gb[4] = {vb.x, vb.y, vb.z, vb.w};
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const int t = 4 * t4 + k;
-                    if (t > i) {
-                        u *= gb[k];
-                        G = fmaf(ga[k], G, ge[k] * u);
-                    }
-                    Gm[t * GS + i] = t >= i ? G : 0.0f;
-                }
-            }
-            sGl[i] = G;
-            sU[i] = u;
-        } else if (tid == 224) {
-            float A = 1.f, Bc = 1.f, sg = 0.f;
-            const float4* g4 = reinterpret_cast<const float4*>(g);
-#pragma unroll
-            for (int t4 = 0; t4 < BC / 4; ++t4) {
-                const float4 va = g4[t4], ve = g4[BC / 4 + t4], vb = g4[BC / 2 + t4];
-                const float ga[4] = {va.x, va.y, va.z, va.w}, ge[4] = {ve.x, ve.y, ve.z, ve.w},
-                            gb[4] = {vb.x, vb.y, vb.z, vb.w};
-                float oa[4], ob[4], os[4];
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    A *= ga[k];
-                    Bc *= gb[k];
-                    sg = fmaf(ga[k], sg, ge[k] * Bc);
-                    oa[k] = A;
-                    ob[k] = Bc;
-                    os[k] = sg;
-                }
-                reinterpret_cast<float4*>(sA)[t4] = make_float4(oa[0], oa[1], oa[2], oa[3]);
-                reinterpret_cast<float4*>(sBc)[t4] = make_float4(ob[0], ob[1], ob[2], ob[3]);
-                reinterpret_cast<float4*>(sSg)[t4] = make_float4(os[0], os[1], os[2], os[3]);
-            }
-        }
-        // the tiles (waited for by thread 0) and the scan are visible to all after this
+        // the tiles (waited for by thread 0) are visible to all after this
         const bool go1 = !failed && !__syncthreads_or(!tiles_ok);
         if (!go1 && !failed) failed = true;
         // -gamma_t k_t and u_t k_t as bf16 operand rows (while G1 runs)
@@ -464,24 +490,8 @@ __global__ void __launch_bounds__(128 * (64 / CW), 1)
                 mma_bf16(tm + COL_YH, dAK + KS_M * ks, dW2 + KS_M * ks, ID_M64N64_TT, ks ? 1u : 0u);
             mma_commit(&bars[1]);
         }
-        mma_wait(go2);
-        // ---- E2: all-reduce of the key forward over the cluster, e = 2 (yhat - v)
-        float ev[CW];
-        {
-            tmem_ld_n(tl + COL_YH + CW * hq, ev);
-            if (r64) {
-                if (NC > 1) {
-                    const uint32_t dst = map_to_rank(smem_u32(Yx + tr * XS + CW * hq), (uint32_t)peer);
-                    push_bf16<CW>(dst, ev);
-                }
-                float vv[CW];
-                get_row<CW>(sm + OFF_V, 64, tr, CW * hq, vv);
-#pragma unroll
-                for (int q = 0; q < CW; ++q) ev[q] = 2.0f * (ev[q] - vv[q]);
-            }
-        }
-        // while the peer's partial sums arrive: rescale the fp32 state for this
-        // chunk, W <- A_n W - sigma_n S, S <- B_n S (before G4 accumulates into it)
+        // while G2 runs: rescale the fp32 state for this chunk,
+        // W <- A_n W - sigma_n S, S <- B_n S (before G4 accumulates into it)
         {
             const float An = sA[BC - 1], Bn = sBc[BC - 1], sn = sSg[BC - 1];
             float w[CW], s[CW];
@@ -496,6 +506,22 @@ __global__ void __launch_bounds__(128 * (64 / CW), 1)
                 }
                 tmem_st_n(tl + cw, w);
                 tmem_st_n(tl + cs, s);
+            }
+        }
+        mma_wait(go2);
+        // ---- E2: all-reduce of the key forward over the cluster, e = 2 (yhat - v)
+        float ev[CW];
+        {
+            tmem_ld_n(tl + COL_YH + CW * hq, ev);
+            if (r64) {
+                if (NC > 1) {
+                    const uint32_t dst = map_to_rank(smem_u32(Yx + tr * XS + CW * hq), (uint32_t)peer);
+                    push_bf16<CW>(dst, ev);
+                }
+                float vv[CW];
+                get_row<CW>(sm + OFF_V, 64, tr, CW * hq, vv);
+#pragma unroll
+                for (int q = 0; q < CW; ++q) ev[q] = 2.0f * (ev[q] - vv[q]);
             }
         }
         if (NC > 1) cluster_sync();
@@ -568,6 +594,8 @@ __global__ void __launch_bounds__(128 * (64 / CW), 1)
                 mma_bf16(tm + COL_S2, dAK + KS_K * ks, dEU + KS_M * ks, ID_UPD, 1u);
             }
         }
+        // while G4 runs: the next chunk's scan (its gates were stored in E2)
+        if (c + 1 < nchunks) scan(stage ^ 1);
         mma_wait(go4);
         // ---- E4: h_t = A_t W1 q_t - sigma_t S1 q_t - sum_i P1[t][i] delta_i, a_t = silu(h_t)
         {
@@ -595,6 +623,10 @@ __global__ void __launch_bounds__(128 * (64 / CW), 1)
             for (int ks = 0; ks < 8; ++ks)
                 mma_bf16(tm + COL_YW, dAQ + KS_M * ks, dW2 + KS_M * ks, ID_M64N128_TT, ks ? 1u : 0u);
         }
+        // while G5 runs: W1 and S1 (complete since G4) become the next chunk's
+        // bf16 operands, or after the last chunk the result
+        convert_state(0, c + 1 == nchunks);
+        convert_state(1, c + 1 == nchunks);
         mma_wait(go5);
         // ---- E5: P2 = Gamma (.) (a_t . a(k_i))
         {
@@ -635,33 +667,10 @@ __global__ void __launch_bounds__(128 * (64 / CW), 1)
                     push_bf16<CW>(dst, yw);
                 }
             }
-            // while the peer's partial y arrives: the new state becomes the next
-            // chunk's bf16 operands (or, after the last chunk, the result)
-            {
-                const bool last = c + 1 == nchunks;
-                float w[CW];
-#pragma unroll
-                for (int m = 0; m < 4; ++m) {
-                    const uint32_t col = (m == 0 ? COL_W1 : m == 1 ? COL_S1 : m == 2 ? COL_W2 : COL_S2) + CW * hq;
-                    tmem_ld_n(tl + col, w);
-                    if (!last) {
-                        const uint32_t off = m == 0 ? OFF_W1 : m == 1 ? OFF_S1 : m == 2 ? OFF_W2 : OFF_S2;
-                        put_row<CW>(sm + off, 128, jr, CW * hq, w);
-                    } else {
-                        float* dst = (m & 1) ? a.S_T + unit * P : a.M_T + unit * P;
-                        if (m < 2) {
-                            float* r = dst + (long long)j_glob * D + CW * hq;
-#pragma unroll
-                            for (int q = 0; q < CW; q += 4)
-                                *reinterpret_cast<float4*>(r + q) = make_float4(w[q], w[q + 1], w[q + 2], w[q + 3]);
-                        } else {
-                            float* r = dst + (long long)hid * D + j_glob;
-#pragma unroll
-                            for (int q = 0; q < CW; ++q) r[(long long)(CW * hq + q) * hid] = w[q];
-                        }
-                    }
-                }
-            }
+            // while the peer's partial y arrives: W2 and S2 (no longer read by
+            // G5) become the next chunk's bf16 operands, or the result
+            convert_state(2, c + 1 == nchunks);
+            convert_state(3, c + 1 == nchunks);
             if (NC > 1) cluster_sync();
             if (r64 && own && tr < n) {
                 if (NC > 1) {

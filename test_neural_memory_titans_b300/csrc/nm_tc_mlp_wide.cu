@@ -111,8 +111,6 @@ __device__ __forceinline__ uint64_t kdesc(uint32_t a) { return desc_hi(16) | ((a
 __device__ __forceinline__ uint64_t mdesc(uint32_t a, uint32_t lbo) { return desc_hi(lbo) | ((a >> 4) & 0x3FFFu); }
 constexpr uint64_t KS_K = 2, KS_M = 128;
 
-__device__ __forceinline__ float sigmoid_f(float z) { return __fdividef(1.0f, 1.0f + __expf(-fmaxf(z, -80.0f))); }
-
 __device__ __forceinline__ float momentum_c(int mode, float beta, const float* c, long long i) {
     if (mode == NM_C_ONE_MINUS_BETA) return 1.0f - beta;
     if (mode == NM_C_PER_TOKEN) return c[i];

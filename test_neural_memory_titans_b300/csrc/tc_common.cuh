@@ -126,6 +126,18 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64
     }
 }
 
+// sigmoid(z) = (1 + tanh(z / 2)) / 2 with the hardware tanh approximation
+// (relative error about 2^-11, below the bf16 rounding its results go
+// through): one special-function op per element instead of an exponential
+// and a reciprocal.  Epilogues that evaluate silu over a whole tile are
+// bound by the special-function issue rate.
+__device__ __forceinline__ float tanh_approx(float x) {
+    float r;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+__device__ __forceinline__ float sigmoid_f(float z) { return fmaf(0.5f, tanh_approx(0.5f * z), 0.5f); }
+
 // ------------------------------------------------------------------ TMA
 
 __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1, int c2) {
