@@ -107,6 +107,8 @@ constexpr uint32_t ID_M128N64 = idesc_bf16_f32(128, 64, false, false);
 constexpr uint32_t ID_UPD = idesc_bf16_f32(128, 64, false, true);
 constexpr uint32_t ID_M64N64_TT = idesc_bf16_f32(64, 64, true, true);
 constexpr uint32_t ID_M64N128_TT = idesc_bf16_f32(64, 128, true, true);
+constexpr uint32_t ID_M64N192_TT = idesc_bf16_f32(64, 192, true, true);
+static_assert(OFF_AK == OFF_S2 + T128 && COL_AA == COL_YW + 128, "N=192 operand and accumulator");
 constexpr uint32_t ID_M64N64_BT = idesc_bf16_f32(64, 64, false, true);
 constexpr uint64_t WAIT_NS = 2000000000ull;  // 2 s
 
@@ -261,32 +263,39 @@ __global__ void __launch_bounds__(128 * (64 / CW), 1)
     };
 
     // The scan of one chunk's gates (stage st), one chunk ahead of its use:
-    // Gamma column by column (threads 128..191, the division-free recursion
-    // Gamma_{t,i} = a_t Gamma_{t-1,i} + eta_t u_{t,i}, zero above the
-    // diagonal), gamma_i = Gamma_{n-1,i} and u_i = u_{n-1,i}; A, B, sigma by
-    // thread 224.
+    // Gamma column by column (threads 128..191), gamma_i = Gamma_{n-1,i} and
+    // u_i = u_{n-1,i}; A, B, sigma by thread 224.  Column i runs the
+    // division-free recursion from row 0 with u = Gamma = 0 and the start
+    // injected, u_t = beta_t u_{t-1} + [t = i] c_i, Gamma_{t,i} =
+    // a_t Gamma_{t-1,i} + eta_t u_t: rows above the diagonal come out exactly
+    // zero and no row takes a branch.  The gates of the next four tokens are
+    // loaded before a group's stores (shared loads stay behind earlier
+    // shared stores).
     auto scan = [&](int st) {
         const float* g = gates + st * 4 * BC;
         float* so = scan_out + st * 5 * BC;
         if (tid >= 128 && tid < 128 + BC) {
             float* Gm = gamma_all + st * 64 * GS;
             const int i = tid - 128;
-            float u = g[3 * BC + i];
-            float G = g[BC + i] * u;
+            const float ci = g[3 * BC + i];
+            float u = 0.0f, G = 0.0f;
             const float4* g4 = reinterpret_cast<const float4*>(g);
+            float4 va = g4[0], ve = g4[BC / 4], vb = g4[BC / 2];
 #pragma unroll
             for (int t4 = 0; t4 < BC / 4; ++t4) {
-                const float4 va = g4[t4], ve = g4[BC / 4 + t4], vb = g4[BC / 2 + t4];
                 const float ga[4] = {va.x, va.y, va.z, va.w}, ge[4] = {ve.x, ve.y, ve.z, ve.w},
                             gb[4] = {vb.x, vb.y, vb.z, vb.w};
+                if (t4 + 1 < BC / 4) {
+                    va = g4[t4 + 1];
+                    ve = g4[BC / 4 + t4 + 1];
+                    vb = g4[BC / 2 + t4 + 1];
+                }
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
                     const int t = 4 * t4 + k;
-                    if (t > i) {
-                        u *= gb[k];
-                        G = fmaf(ga[k], G, ge[k] * u);
-                    }
-                    Gm[t * GS + i] = t >= i ? G : 0.0f;
+                    u = fmaf(gb[k], u, t == i ? ci : 0.0f);
+                    G = fmaf(ga[k], G, ge[k] * u);
+                    Gm[t * GS + i] = G;
                 }
             }
             so[3 * BC + i] = G;
@@ -294,11 +303,16 @@ __global__ void __launch_bounds__(128 * (64 / CW), 1)
         } else if (tid == 224) {
             float A = 1.f, Bc = 1.f, sg = 0.f;
             const float4* g4 = reinterpret_cast<const float4*>(g);
+            float4 va = g4[0], ve = g4[BC / 4], vb = g4[BC / 2];
 #pragma unroll
             for (int t4 = 0; t4 < BC / 4; ++t4) {
-                const float4 va = g4[t4], ve = g4[BC / 4 + t4], vb = g4[BC / 2 + t4];
                 const float ga[4] = {va.x, va.y, va.z, va.w}, ge[4] = {ve.x, ve.y, ve.z, ve.w},
                             gb[4] = {vb.x, vb.y, vb.z, vb.w};
+                if (t4 + 1 < BC / 4) {
+                    va = g4[t4 + 1];
+                    ve = g4[BC / 4 + t4 + 1];
+                    vb = g4[BC / 2 + t4 + 1];
+                }
                 float oa[4], ob[4], os[4];
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
@@ -490,7 +504,23 @@ __global__ void __launch_bounds__(128 * (64 / CW), 1)
                 mma_bf16(tm + COL_YH, dAK + KS_M * ks, dW2 + KS_M * ks, ID_M64N64_TT, ks ? 1u : 0u);
             mma_commit(&bars[1]);
         }
-        // while G2 runs: rescale the fp32 state for this chunk,
+        mma_wait(go2);
+        // ---- E2: all-reduce of the key forward over the cluster, e = 2 (yhat - v)
+        float ev[CW];
+        {
+            tmem_ld_n(tl + COL_YH + CW * hq, ev);
+            if (r64) {
+                if (NC > 1) {
+                    const uint32_t dst = map_to_rank(smem_u32(Yx + tr * XS + CW * hq), (uint32_t)peer);
+                    push_bf16<CW>(dst, ev);
+                }
+                float vv[CW];
+                get_row<CW>(sm + OFF_V, 64, tr, CW * hq, vv);
+#pragma unroll
+                for (int q = 0; q < CW; ++q) ev[q] = 2.0f * (ev[q] - vv[q]);
+            }
+        }
+        // while the peer's partial sums arrive: rescale the fp32 state for this chunk,
         // W <- A_n W - sigma_n S, S <- B_n S (before G4 accumulates into it)
         {
             const float An = sA[BC - 1], Bn = sBc[BC - 1], sn = sSg[BC - 1];
@@ -506,22 +536,6 @@ __global__ void __launch_bounds__(128 * (64 / CW), 1)
                 }
                 tmem_st_n(tl + cw, w);
                 tmem_st_n(tl + cs, s);
-            }
-        }
-        mma_wait(go2);
-        // ---- E2: all-reduce of the key forward over the cluster, e = 2 (yhat - v)
-        float ev[CW];
-        {
-            tmem_ld_n(tl + COL_YH + CW * hq, ev);
-            if (r64) {
-                if (NC > 1) {
-                    const uint32_t dst = map_to_rank(smem_u32(Yx + tr * XS + CW * hq), (uint32_t)peer);
-                    push_bf16<CW>(dst, ev);
-                }
-                float vv[CW];
-                get_row<CW>(sm + OFF_V, 64, tr, CW * hq, vv);
-#pragma unroll
-                for (int q = 0; q < CW; ++q) ev[q] = 2.0f * (ev[q] - vv[q]);
             }
         }
         if (NC > 1) cluster_sync();
@@ -613,15 +627,11 @@ __global__ void __launch_bounds__(128 * (64 / CW), 1)
         const bool go5 = !failed;
         if (go5 && tid == 0) {
             const uint64_t dAQ = mdesc(aDT, T128), dW2 = mdesc(aW2, T128), dAK = mdesc(aAK, T128);
-            // a_t . a(k_i) first: E5 waits only for it (and for the state
-            // updates issued before it); W2 a_t | S2 a_t completes behind it
+            // [W2 a_t | S2 a_t | a_t . a(k_i)] in one N=192 product (W2, S2, a(k) copies are consecutive)
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks)
-                mma_bf16(tm + COL_AA, dAQ + KS_M * ks, dAK + KS_M * ks, ID_M64N64_TT, ks ? 1u : 0u);
+                mma_bf16(tm + COL_YW, dAQ + KS_M * ks, dW2 + KS_M * ks, ID_M64N192_TT, ks ? 1u : 0u);
             mma_commit(&bars[1]);
-#pragma unroll
-            for (int ks = 0; ks < 8; ++ks)
-                mma_bf16(tm + COL_YW, dAQ + KS_M * ks, dW2 + KS_M * ks, ID_M64N128_TT, ks ? 1u : 0u);
         }
         // while G5 runs: W1 and S1 (complete since G4) become the next chunk's
         // bf16 operands, or after the last chunk the result
