@@ -301,22 +301,28 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (tid >= 128 && tid < 128 + SB) {
             // column i of the block's Gamma (division-free recursion), gamma_i, u_i
             const int i = tid - 128;
-            float u = gt[3 * SB + i];
-            float G = gt[SB + i] * u;
+            // from row 0 with u = Gamma = 0 and the start injected,
+            // u_t = beta_t u_{t-1} + [t = i] c_i: zero above the diagonal, no branch per row;
+            // the next four gates are loaded before this group's stores
+            const float ci = gt[3 * SB + i];
+            float u = 0.0f, G = 0.0f;
             const float4* g4 = reinterpret_cast<const float4*>(gt);
+            float4 va = g4[0], ve = g4[SB / 4], vb = g4[SB / 2];
 #pragma unroll
             for (int t4 = 0; t4 < SB / 4; ++t4) {
-                const float4 va = g4[t4], ve = g4[SB / 4 + t4], vb = g4[SB / 2 + t4];
                 const float ga[4] = {va.x, va.y, va.z, va.w}, ge[4] = {ve.x, ve.y, ve.z, ve.w},
                             gb[4] = {vb.x, vb.y, vb.z, vb.w};
+                if (t4 + 1 < SB / 4) {
+                    va = g4[t4 + 1];
+                    ve = g4[SB / 4 + t4 + 1];
+                    vb = g4[SB / 2 + t4 + 1];
+                }
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
                     const int t = 4 * t4 + k;
-                    if (t > i) {
-                        u *= gb[k];
-                        G = fmaf(ga[k], G, ge[k] * u);
-                    }
-                    Gm[t * GS + i] = t >= i ? G : 0.0f;
+                    u = fmaf(gb[k], u, t == i ? ci : 0.0f);
+                    G = fmaf(ga[k], G, ge[k] * u);
+                    Gm[t * GS + i] = G;
                 }
             }
             sGl[i] = G;
