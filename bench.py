@@ -30,6 +30,29 @@ sys.path.insert(0, ROOT)
 import torch  # noqa: E402
 
 METRIC = "memory-layer fwd tokens/sec (B*H*T/s) and % of roofline (TC FLOPs vs HBM)"
+
+# DRAM bytes (read + write) per launch of the dominant kernel, from ncu captures summarised under
+# profiles/: workload -> (kernel sources, sha256 prefix of those sources when captured, bytes).
+# A capture describes the kernel it was taken on only: when the sources differ, traffic is null.
+NCU_TRAFFIC = {
+    "mlp_64x256_bf16_b4h8_t4096_c64": (("nm_tc_mlp.cu", "tc_common.cuh"), "028f9092d6e01339", 62.49e6),
+    "linear_d128_bf16_b8h16_t16384_c64": (("nm_tc_linear.cu", "tc_common.cuh"), "bd1e1accbb15e2c3", 2.121e9),
+}
+
+
+def ncu_traffic(workload_name: str):
+    """DRAM bytes per launch from the table above, or None if absent or stale."""
+    import hashlib
+    entry = NCU_TRAFFIC.get(workload_name)
+    if entry is None:
+        return None
+    files, digest, nbytes = entry
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(os.path.dirname(os.path.abspath(__file__)), "test_neural_memory_titans_b300", "csrc", f),
+                  "rb") as fh:
+            h.update(fh.read())
+    return nbytes if h.hexdigest()[:16] == digest else None
 DEFAULT_WORKLOAD = 1
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 
@@ -364,7 +387,10 @@ def run_ours(args, rank, world, local_rank):
         peak = float(peaks["hbm_gbs"])
         unit = "GB/s"
     roof = {"bound": "hbm" if alg["bound"] == "hbm" else "tensor", "achieved": achieved, "peak": peak, "unit": unit,
-            "frac": achieved / peak, "traffic": args.traffic, "peak_source": peak_src + " (burst)",
+            "frac": achieved / peak,
+            "traffic": args.traffic if args.traffic is not None else
+            (ncu_traffic(wl.name) if mem.path == nm.PATH_TC and (args.B, args.H, args.T) == (None, None, None) else None),
+            "peak_source": peak_src + " (burst)",
             "kernel": "nm_forward (%s path)" % ("tcgen05" if mem.path == nm.PATH_TC else "fp32 FFMA"),
             "per_launch_ms": per_launch_ms,
             "frac_tensor": alg["flops"] / (per_launch_ms * alg["calls"] * 1e-3) / (float(peaks["bf16_tflops"]) * 1e12),

@@ -30,6 +30,8 @@ MLP2 = 1
 C_ONE = 0
 C_ONE_MINUS_BETA = 1
 C_PER_TOKEN = 2
+LOSS_L2 = 0
+LOSS_HUBER = 1
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "nm_oracle.c")
@@ -54,11 +56,12 @@ def _load():
         lib = ctypes.CDLL(_LIB)
         dp = ctypes.POINTER(ctypes.c_double)
         i = ctypes.c_int
-        lib.oracle_forward.argtypes = [i, i, i, i, i, i, i, i] + [dp] * 12
+        dd = ctypes.c_double
+        lib.oracle_forward.argtypes = [i, i, i, i, i, i, dd, i, i, i] + [dp] * 13
         lib.oracle_forward.restype = i
-        lib.oracle_grad.argtypes = [i, i, i, dp, dp, dp, dp, dp]
+        lib.oracle_grad.argtypes = [i, i, i, i, dd, dp, dp, dp, dp, dp]
         lib.oracle_grad.restype = None
-        lib.oracle_loss.argtypes = [i, i, i, dp, dp, dp, dp]
+        lib.oracle_loss.argtypes = [i, i, i, i, dd, dp, dp, dp, dp]
         lib.oracle_loss.restype = ctypes.c_double
         lib.oracle_memory_apply.argtypes = [i, i, i, dp, dp, dp, dp]
         lib.oracle_memory_apply.restype = None
@@ -89,27 +92,32 @@ def memory_apply(kind: int, d: int, hidden: int, W, x) -> np.ndarray:
     return y
 
 
-def loss(kind: int, d: int, hidden: int, W, k, v) -> float:
-    """||M_W(k) - v||^2."""
+def loss(kind: int, d: int, hidden: int, W, k, v, loss_kind: int = LOSS_L2, huber_delta: float = np.inf) -> float:
+    """||M_W(k) - v||^2, or the element-wise Huber sum (rho(r) = r^2 inside delta,
+    2 delta |r| - delta^2 beyond)."""
     W, k, v = _f64(W), _f64(k), _f64(v)
     work = np.zeros(d + max(hidden, 1) + 8)
-    return float(_load().oracle_loss(kind, d, hidden, _ptr(W), _ptr(k), _ptr(v), _ptr(work)))
+    return float(_load().oracle_loss(kind, d, hidden, loss_kind, float(huber_delta), _ptr(W), _ptr(k), _ptr(v),
+                                     _ptr(work)))
 
 
-def grad(kind: int, d: int, hidden: int, W, k, v) -> np.ndarray:
-    """grad_W ||M_W(k) - v||^2 by explicit backprop."""
+def grad(kind: int, d: int, hidden: int, W, k, v, loss_kind: int = LOSS_L2, huber_delta: float = np.inf) -> np.ndarray:
+    """grad_W of the loss above by explicit backprop."""
     W, k, v = _f64(W), _f64(k), _f64(v)
     g = np.zeros(param_count(kind, d, hidden))
     work = np.zeros(3 * max(hidden, 1) + 2 * d + 8)
-    _load().oracle_grad(kind, d, hidden, _ptr(W), _ptr(k), _ptr(v), _ptr(g), _ptr(work))
+    _load().oracle_grad(kind, d, hidden, loss_kind, float(huber_delta), _ptr(W), _ptr(k), _ptr(v), _ptr(g),
+                        _ptr(work))
     return g
 
 
 def forward(kind: int, d: int, hidden: int, chunk: int, c_mode: int,
-            q, k, v, alpha, eta, beta, c, M0, S0):
+            q, k, v, alpha, eta, beta, c, M0, S0, loss_kind: int = LOSS_L2, huber_delta: float = np.inf,
+            surprise: bool = False):
     """The chunked forward on [B, H, T, d] inputs and [B, H, T] gates.
 
-    Returns (y [B,H,T,d], M_T [B,H,P], S_T [B,H,P]) as float64 arrays.
+    Returns (y [B,H,T,d], M_T [B,H,P], S_T [B,H,P]) as float64 arrays, and with
+    surprise=True also the per-token gradient norms [B,H,T].
     """
     q, k, v = _f64(q), _f64(k), _f64(v)
     B, H, T, dd = q.shape
@@ -129,9 +137,11 @@ def forward(kind: int, d: int, hidden: int, chunk: int, c_mode: int,
     y = np.zeros((B, H, T, d))
     MT = np.zeros((B, H, P))
     ST = np.zeros((B, H, P))
-    rc = _load().oracle_forward(kind, d, hidden, chunk, c_mode, B, H, T,
+    sp = np.zeros((B, H, T)) if surprise else None
+    rc = _load().oracle_forward(kind, d, hidden, chunk, c_mode, loss_kind, float(huber_delta), B, H, T,
                                 _ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(eta), _ptr(beta),
-                                cp, _ptr(M0), _ptr(S0), _ptr(y), _ptr(MT), _ptr(ST))
+                                cp, _ptr(M0), _ptr(S0), _ptr(y), _ptr(MT), _ptr(ST),
+                                _ptr(sp) if surprise else None)
     if rc != 0:
         raise ValueError("oracle_forward rejected its arguments")
-    return y, MT, ST
+    return (y, MT, ST, sp) if surprise else (y, MT, ST)

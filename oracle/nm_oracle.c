@@ -52,6 +52,19 @@
  *   - retrieval uses the weights after token t's update (inclusive);
  *   - gates are one scalar per token per head, shared by every parameter.
  *
+ * Two extensions, both optional:
+ *   - the Huber loss of the YAAD variant ([JA] "MIRASフレームワーク", "3つの変種";
+ *     es.news.hada.io, "Modelos basados en MIRAS"), which the pages name
+ *     without a formula or threshold.  Reading: element-wise on the residual
+ *     r = M(k) - v, with a caller-given threshold delta, scaled to agree with
+ *     ||r||^2 inside it:  rho(r) = r^2 for |r| <= delta, 2 delta |r| - delta^2
+ *     beyond, so d rho / d r = 2 clip(r, -delta, delta).  delta = +inf is the
+ *     squared loss exactly.
+ *   - the surprise of each token ([JA] "技術的詳細", "Surprise機構": the norm of the
+ *     loss gradient with respect to the memory's parameters), read as the
+ *     Frobenius norm over all parameters of g_t, the gradient the update uses
+ *     (at the chunk-start weights).
+ *
  * No blocking, no fusion, no reordering: a reader can check each loop against
  * the equations above.  Everything is double precision.
  */
@@ -65,6 +78,18 @@
 #define OR_C_ONE 0
 #define OR_C_ONE_MINUS_BETA 1
 #define OR_C_PER_TOKEN 2
+
+#define OR_LOSS_L2 0
+#define OR_LOSS_HUBER 1
+
+/* d rho / d r: 2 r (squared loss) or 2 clip(r, -delta, delta) (Huber). */
+static double or_dloss(int loss, double delta, double r) {
+    if (loss == OR_LOSS_HUBER) {
+        if (r > delta) return 2.0 * delta;
+        if (r < -delta) return -2.0 * delta;
+    }
+    return 2.0 * r;
+}
 
 static double or_sigmoid(double z) { return 1.0 / (1.0 + exp(-z)); }
 static double or_silu(double z) { return z * or_sigmoid(z); }
@@ -107,31 +132,35 @@ void oracle_memory_apply(int kind, int d, int h, const double* W,
 }
 
 /* The associative loss l(W; k, v) = ||M_W(k) - v||_2^2 ([IT] "Funzione
- * Obiettivo").  work: d + h doubles. */
-double oracle_loss(int kind, int d, int h, const double* W, const double* k,
-                   const double* v, double* work) {
+ * Obiettivo"), or with loss = OR_LOSS_HUBER the sum of rho(r_o) above.
+ * work: d + h doubles. */
+double oracle_loss(int kind, int d, int h, int loss, double delta, const double* W,
+                   const double* k, const double* v, double* work) {
     double* yhat = work;
     oracle_memory_apply(kind, d, h, W, k, yhat, work + d);
     double acc = 0.0;
     for (int o = 0; o < d; ++o) {
         double r = yhat[o] - v[o];
-        acc += r * r;
+        if (loss == OR_LOSS_HUBER && fabs(r) > delta)
+            acc += 2.0 * delta * fabs(r) - delta * delta;
+        else
+            acc += r * r;
     }
     return acc;
 }
 
 /* g = grad_W l(W; k, v), by an explicit forward and backward pass.
  * work: 3h + 2d doubles. */
-void oracle_grad(int kind, int d, int h, const double* W, const double* k,
-                 const double* v, double* g, double* work) {
+void oracle_grad(int kind, int d, int h, int loss, double delta, const double* W,
+                 const double* k, const double* v, double* g, double* work) {
     if (kind == OR_LINEAR) {
-        /* l = sum_o (sum_i M[o][i] k[i] - v[o])^2
-         * dl/dM[o][i] = 2 (M k - v)[o] k[i]                                  */
+        /* l = sum_o rho((M k - v)[o]),  rho(r) = r^2 for the squared loss
+         * dl/dM[o][i] = rho'((M k - v)[o]) k[i]                              */
         double* e = work;
         for (int o = 0; o < d; ++o) {
             double acc = 0.0;
             for (int i = 0; i < d; ++i) acc += W[(long)o * d + i] * k[i];
-            e[o] = 2.0 * (acc - v[o]);
+            e[o] = or_dloss(loss, delta, acc - v[o]);
         }
         for (int o = 0; o < d; ++o)
             for (int i = 0; i < d; ++i) g[(long)o * d + i] = e[o] * k[i];
@@ -152,11 +181,11 @@ void oracle_grad(int kind, int d, int h, const double* W, const double* k,
         z[j] = acc;
         a[j] = or_silu(acc);
     }
-    /* dl/dyhat = 2 (yhat - v) */
+    /* dl/dyhat = rho'(yhat - v): 2 (yhat - v) for the squared loss */
     for (int o = 0; o < d; ++o) {
         double acc = 0.0;
         for (int j = 0; j < h; ++j) acc += W2[(long)o * h + j] * a[j];
-        e[o] = 2.0 * (acc - v[o]);
+        e[o] = or_dloss(loss, delta, acc - v[o]);
     }
     /* dl/dW2[o][j] = e[o] a[j] */
     for (int o = 0; o < d; ++o)
@@ -173,11 +202,12 @@ void oracle_grad(int kind, int d, int h, const double* W, const double* k,
 }
 
 /* One (batch, head) unit.  Pointers are already offset to the unit. */
-static void oracle_unit(int kind, int d, int h, int chunk, int c_mode, int T,
-                        const double* q, const double* k, const double* v,
-                        const double* alpha, const double* eta,
+static void oracle_unit(int kind, int d, int h, int chunk, int c_mode, int loss,
+                        double delta, int T, const double* q, const double* k,
+                        const double* v, const double* alpha, const double* eta,
                         const double* beta, const double* c, const double* M0,
-                        const double* S0, double* y, double* MT, double* ST) {
+                        const double* S0, double* y, double* MT, double* ST,
+                        double* surprise) {
     long P = oracle_param_count(kind, d, h);
     double* M = (double*)malloc(sizeof(double) * P);
     double* S = (double*)malloc(sizeof(double) * P);
@@ -190,7 +220,12 @@ static void oracle_unit(int kind, int d, int h, int chunk, int c_mode, int T,
         int t1 = t0 + chunk < T ? t0 + chunk : T;
         memcpy(W0, M, sizeof(double) * P); /* chunk-start weights */
         for (int t = t0; t < t1; ++t) {
-            oracle_grad(kind, d, h, W0, k + (long)t * d, v + (long)t * d, g, work);
+            oracle_grad(kind, d, h, loss, delta, W0, k + (long)t * d, v + (long)t * d, g, work);
+            if (surprise) {
+                double n2 = 0.0;
+                for (long p = 0; p < P; ++p) n2 += g[p] * g[p];
+                surprise[t] = sqrt(n2);
+            }
             double ct = 1.0;
             if (c_mode == OR_C_ONE_MINUS_BETA) ct = 1.0 - beta[t];
             else if (c_mode == OR_C_PER_TOKEN) ct = c[t];
@@ -206,29 +241,34 @@ static void oracle_unit(int kind, int d, int h, int chunk, int c_mode, int T,
 
 /*
  * Full forward over B x H independent (batch, head) units.
- *   q, k, v, y : [B, H, T, d]      alpha, eta, beta, c : [B, H, T]
- *   M0, S0, MT, ST : [B, H, P]     (c may be NULL unless c_mode == PER_TOKEN)
+ *   q, k, v, y : [B, H, T, d]      alpha, eta, beta, c, surprise : [B, H, T]
+ *   M0, S0, MT, ST : [B, H, P]     (c may be NULL unless c_mode == PER_TOKEN;
+ *                                   surprise may be NULL)
+ *   loss: OR_LOSS_L2 or OR_LOSS_HUBER with threshold delta > 0.
  * Returns 0, or -1 on a bad argument.  Units run in parallel with OpenMP;
  * each unit's arithmetic is sequential and identical to a one-thread run.
  */
-int oracle_forward(int kind, int d, int h, int chunk, int c_mode, int B, int H,
-                   int T, const double* q, const double* k, const double* v,
-                   const double* alpha, const double* eta, const double* beta,
-                   const double* c, const double* M0, const double* S0,
-                   double* y, double* MT, double* ST) {
+int oracle_forward(int kind, int d, int h, int chunk, int c_mode, int loss,
+                   double delta, int B, int H, int T, const double* q,
+                   const double* k, const double* v, const double* alpha,
+                   const double* eta, const double* beta, const double* c,
+                   const double* M0, const double* S0, double* y, double* MT,
+                   double* ST, double* surprise) {
     if ((kind != OR_LINEAR && kind != OR_MLP2) || d <= 0 || chunk <= 0 ||
         B < 0 || H < 0 || T < 0)
         return -1;
+    if (loss != OR_LOSS_L2 && !(loss == OR_LOSS_HUBER && delta > 0.0)) return -1;
     if (kind == OR_MLP2 && h <= 0) return -1;
     if (c_mode == OR_C_PER_TOKEN && c == NULL) return -1;
     long P = oracle_param_count(kind, d, h);
     long units = (long)B * H;
 #pragma omp parallel for schedule(dynamic, 1)
     for (long u = 0; u < units; ++u) {
-        oracle_unit(kind, d, h, chunk, c_mode, T, q + u * T * d, k + u * T * d,
-                    v + u * T * d, alpha + u * T, eta + u * T, beta + u * T,
-                    c ? c + u * T : NULL, M0 + u * P, S0 + u * P, y + u * T * d,
-                    MT + u * P, ST + u * P);
+        oracle_unit(kind, d, h, chunk, c_mode, loss, delta, T, q + u * T * d,
+                    k + u * T * d, v + u * T * d, alpha + u * T, eta + u * T,
+                    beta + u * T, c ? c + u * T : NULL, M0 + u * P, S0 + u * P,
+                    y + u * T * d, MT + u * P, ST + u * P,
+                    surprise ? surprise + u * T : NULL);
     }
     return 0;
 }

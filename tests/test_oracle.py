@@ -389,3 +389,118 @@ def test_ragged_last_chunk_and_empty():
     ya, Ma, Sa = _run(oracle.LINEAR, d, 0, 4, oracle.C_ONE, q[:4], k[:4], v[:4], a[:4], e[:4], b[:4])
     yb, Mb, Sb = _run(oracle.LINEAR, d, 0, 3, oracle.C_ONE, q[4:], k[4:], v[4:], a[4:], e[4:], b[4:], M0=Ma, S0=Sa)
     assert np.array_equal(y, np.concatenate([ya, yb])) and np.array_equal(MT, Mb) and np.array_equal(ST, Sb)
+
+
+# ---------------------------------------------------------------- Huber loss (YAAD) and surprise norm
+# The YAAD variant uses a Huber loss (0h-n0.github.io explainer, "MIRASフレームワーク",
+# "3つの変種"; es.news.hada.io, "Modelos basados en MIRAS"); the pages give no formula
+# or threshold.  Reading: element-wise on r = M(k) - v with a given delta,
+# rho(r) = r^2 for |r| <= delta and 2 delta |r| - delta^2 beyond.  The surprise of a
+# token is the norm of the loss gradient with respect to the memory's parameters
+# (the same explainer, "Surprise機構"), here the Frobenius norm of the gradient the
+# update uses, taken at the chunk-start weights.
+
+def _huber_torch(r, delta):
+    a = r.abs()
+    return torch.where(a <= delta, r * r, 2 * delta * a - delta * delta).sum()
+
+
+@pytest.mark.parametrize("kind,d,hidden", [(oracle.LINEAR, 3, 0), (oracle.MLP2, 3, 5), (oracle.MLP2, 4, 8)])
+def test_huber_grad_finite_differences_and_library(kind, d, hidden):
+    """The Huber gradient against central differences of the Huber loss and
+    against torch autograd of the same loss written independently; delta is
+    set so that some residuals are clipped and none lies near the kink."""
+    rng = np.random.default_rng(31 + d + hidden)
+    P = oracle.param_count(kind, d, hidden)
+    checked_clip = False
+    for trial in range(6):
+        W = rng.normal(0, 0.7, P)
+        k = rng.normal(0, 1, d)
+        v = rng.normal(0, 1, d)
+        r = oracle.memory_apply(kind, d, hidden, W, k) - v
+        delta = float(np.median(np.abs(r)))
+        if np.min(np.abs(np.abs(r) - delta)) < 1e-3:
+            delta *= 1.01
+        if np.min(np.abs(np.abs(r) - delta)) < 1e-3:
+            continue
+        checked_clip |= bool(np.any(np.abs(r) > delta))
+        g = oracle.grad(kind, d, hidden, W, k, v, oracle.LOSS_HUBER, delta)
+        h = 1e-6
+        fd = np.zeros(P)
+        for p in range(P):
+            Wp = W.copy(); Wp[p] += h
+            Wm = W.copy(); Wm[p] -= h
+            fd[p] = (oracle.loss(kind, d, hidden, Wp, k, v, oracle.LOSS_HUBER, delta)
+                     - oracle.loss(kind, d, hidden, Wm, k, v, oracle.LOSS_HUBER, delta)) / (2 * h)
+        assert np.linalg.norm(g - fd) <= 1e-7 * np.linalg.norm(fd)
+        Wt = torch.tensor(W, requires_grad=True)
+        lt = _huber_torch(_torch_memory(kind, d, hidden, Wt, torch.tensor(k)) - torch.tensor(v), delta)
+        (gt,) = torch.autograd.grad(lt, Wt)
+        np.testing.assert_allclose(g, gt.numpy(), rtol=1e-12, atol=1e-13)
+        assert abs(oracle.loss(kind, d, hidden, W, k, v, oracle.LOSS_HUBER, delta) - float(lt)) <= 1e-12 * abs(float(lt))
+    assert checked_clip
+
+
+def test_huber_single_token_closed_form():
+    """Linear memory, M0 = S0 = 0, one token: r = -v, so
+    y = -eta c 2 clip(-v, -delta, delta) (k . q), M_T = -eta c 2 clip(-v) k^T."""
+    rng = np.random.default_rng(5)
+    d, delta = 4, 0.3
+    q, k = rng.normal(0, 1, (1, d)), rng.normal(0, 1, (1, d))
+    v = np.array([[0.1, -0.2, 0.9, -1.4]])
+    eta = 0.25
+    out = oracle.forward(oracle.LINEAR, d, 0, 1, oracle.C_ONE, q.reshape(1, 1, 1, d), k.reshape(1, 1, 1, d),
+                         v.reshape(1, 1, 1, d), np.full((1, 1, 1), 0.1), np.full((1, 1, 1), eta),
+                         np.full((1, 1, 1), 0.5), None, np.zeros((1, 1, d * d)), np.zeros((1, 1, d * d)),
+                         oracle.LOSS_HUBER, delta)
+    e = 2.0 * np.clip(-v[0], -delta, delta)        # [ -0.2, 0.4, -0.6, 0.6 ]
+    np.testing.assert_allclose(e, [-0.2, 0.4, -0.6, 0.6], rtol=0, atol=1e-15)
+    np.testing.assert_allclose(out[0][0, 0, 0], -eta * e * float(k[0] @ q[0]), rtol=1e-14, atol=1e-15)
+    np.testing.assert_allclose(out[1][0, 0].reshape(d, d), -eta * np.outer(e, k[0]), rtol=1e-14, atol=1e-15)
+
+
+@pytest.mark.parametrize("kind,d,hidden", [(oracle.LINEAR, 4, 0), (oracle.MLP2, 3, 6)])
+def test_huber_large_threshold_is_the_squared_loss(kind, d, hidden):
+    rng = np.random.default_rng(17)
+    T = 23
+    q, k, v = (rng.normal(0, 1, (1, 1, T, d)) for _ in range(3))
+    a, e, b = rng.uniform(0, .05, (1, 1, T)), rng.uniform(.01, .1, (1, 1, T)), rng.uniform(.8, .95, (1, 1, T))
+    P = oracle.param_count(kind, d, hidden)
+    M0 = rng.normal(0, 0.3, (1, 1, P))
+    S0 = np.zeros((1, 1, P))
+    ref = oracle.forward(kind, d, hidden, 5, oracle.C_ONE, q, k, v, a, e, b, None, M0, S0)
+    hub = oracle.forward(kind, d, hidden, 5, oracle.C_ONE, q, k, v, a, e, b, None, M0, S0, oracle.LOSS_HUBER, 1e30)
+    for x, y in zip(ref, hub):
+        np.testing.assert_array_equal(x, y)
+
+
+@pytest.mark.parametrize("kind,d,hidden,loss_kind", [(oracle.LINEAR, 4, 0, oracle.LOSS_L2),
+                                                     (oracle.LINEAR, 4, 0, oracle.LOSS_HUBER),
+                                                     (oracle.MLP2, 3, 6, oracle.LOSS_L2),
+                                                     (oracle.MLP2, 3, 6, oracle.LOSS_HUBER)])
+def test_surprise_is_the_gradient_norm_at_chunk_start(kind, d, hidden, loss_kind):
+    """Surprise of the first chunk's tokens against the norm of torch
+    autograd's gradient at M0 (the chunk-start weights); for the linear memory
+    also against the closed form ||rho'(M0 k - v)|| ||k||."""
+    rng = np.random.default_rng(23)
+    T, chunk, delta = 9, 6, 0.4
+    q, k, v = (rng.normal(0, 1, (1, 1, T, d)) for _ in range(3))
+    a, e, b = rng.uniform(0, .05, (1, 1, T)), rng.uniform(.01, .1, (1, 1, T)), rng.uniform(.8, .95, (1, 1, T))
+    P = oracle.param_count(kind, d, hidden)
+    M0 = rng.normal(0, 0.5, (1, 1, P))
+    out = oracle.forward(kind, d, hidden, chunk, oracle.C_ONE, q, k, v, a, e, b, None, M0, np.zeros((1, 1, P)),
+                         loss_kind, delta if loss_kind == oracle.LOSS_HUBER else np.inf, surprise=True)
+    sur = out[3][0, 0]
+    assert sur.shape == (T,)
+    for t in range(chunk):
+        Wt = torch.tensor(M0[0, 0], requires_grad=True)
+        r = _torch_memory(kind, d, hidden, Wt, torch.tensor(k[0, 0, t])) - torch.tensor(v[0, 0, t])
+        lt = _huber_torch(r, delta) if loss_kind == oracle.LOSS_HUBER else (r * r).sum()
+        (gt,) = torch.autograd.grad(lt, Wt)
+        assert abs(sur[t] - float(gt.norm())) <= 1e-12 * float(gt.norm())
+        if kind == oracle.LINEAR:
+            rr = M0[0, 0].reshape(d, d) @ k[0, 0, t] - v[0, 0, t]
+            ee = 2 * (np.clip(rr, -delta, delta) if loss_kind == oracle.LOSS_HUBER else rr)
+            assert abs(sur[t] - np.linalg.norm(ee) * np.linalg.norm(k[0, 0, t])) <= 1e-12 * sur[t]
+    # the later tokens take their gradients at the second chunk's start weights
+    assert np.all(sur[chunk:] > 0)
