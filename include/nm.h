@@ -10,7 +10,8 @@
  *   per (batch b, head h), for every chunk of `chunk` consecutive tokens
  *   (the chunk grid starts at token 0 of each call; the last chunk may be
  *   shorter), with W0 the memory at chunk start:
- *       g_t = grad_W || M_W0(k_t) - v_t ||^2          (no 1/2: factor 2 kept)
+ *       g_t = grad_W || M_W0(k_t) - v_t ||^2          (no 1/2: factor 2 kept;
+ *                                                      or the Huber loss, NM_LOSS_HUBER)
  *       S   = beta_t S + c_t g_t                       (momentum over surprise)
  *       M   = (1 - alpha_t) M - eta_t S                (forgetting + step)
  *       y_t = M(q_t)                                   (retrieval after the update)
@@ -61,6 +62,18 @@ extern "C" {
                                   S negated this is the form of "Meccanismo di
                                   Aggiornamento della Memoria")             */
 
+/* the associative loss (its gradient drives the update):
+ *   NM_LOSS_L2     l = ||M(k) - v||^2                   ("Funzione Obiettivo")
+ *   NM_LOSS_HUBER  l = sum_o rho(r_o), r = M(k) - v, rho(r) = r^2 for |r| <= delta,
+ *                  2 delta |r| - delta^2 beyond: the Huber loss of the YAAD variant
+ *                  (0h-n0.github.io explainer, "MIRASフレームワーク", "3つの変種";
+ *                  es.news.hada.io, "Modelos basados en MIRAS"), which the pages
+ *                  name without formula or threshold.  Element-wise, scaled to equal
+ *                  the squared loss inside the threshold, so e = 2 clip(r, -delta, delta)
+ *                  replaces e = 2 r.                                              */
+#define NM_LOSS_L2    0
+#define NM_LOSS_HUBER 1
+
 /* kernel family; AUTO picks the tensor-core path for bf16 inputs when one is
  * built for the shape, else the fp32 FFMA path */
 #define NM_PATH_AUTO 0
@@ -76,6 +89,9 @@ typedef struct nm_config {
     int out_dtype;  /* dtype of y: NM_F32 | NM_BF16                          */
     int c_mode;     /* NM_C_ONE | NM_C_ONE_MINUS_BETA | NM_C_PER_TOKEN       */
     int path;       /* NM_PATH_AUTO | NM_PATH_SIMT | NM_PATH_TC              */
+    int loss;       /* NM_LOSS_L2 | NM_LOSS_HUBER (a zeroed config means L2)  */
+    float huber_delta; /* Huber threshold delta: finite and > 0 for NM_LOSS_HUBER;
+                          ignored for NM_LOSS_L2                                 */
 } nm_config;
 
 typedef struct nm_handle* nm_handle_t;

@@ -33,6 +33,8 @@ C_PER_TOKEN = 2
 PATH_AUTO = 0
 PATH_SIMT = 1
 PATH_TC = 2
+LOSS_L2 = 0
+LOSS_HUBER = 1
 
 NM_OK = 0
 NM_ERR_ARG = 1
@@ -63,7 +65,8 @@ class NMError(RuntimeError):
 class _Config(ctypes.Structure):
     _fields_ = [("kind", ctypes.c_int), ("d", ctypes.c_int), ("hidden", ctypes.c_int),
                 ("chunk", ctypes.c_int), ("in_dtype", ctypes.c_int), ("out_dtype", ctypes.c_int),
-                ("c_mode", ctypes.c_int), ("path", ctypes.c_int)]
+                ("c_mode", ctypes.c_int), ("path", ctypes.c_int), ("loss", ctypes.c_int),
+                ("huber_delta", ctypes.c_float)]
 
 
 _lib = None
@@ -118,10 +121,11 @@ class NeuralMemory:
 
     def __init__(self, kind: int, d: int, hidden: int = 0, chunk: int = 64,
                  in_dtype: torch.dtype = torch.bfloat16, out_dtype: Optional[torch.dtype] = None,
-                 c_mode: int = C_ONE, path: int = PATH_AUTO, device: int = 0):
+                 c_mode: int = C_ONE, path: int = PATH_AUTO, device: int = 0,
+                 loss: int = LOSS_L2, huber_delta: float = 0.0):
         lib = load_library()
         out_dtype = in_dtype if out_dtype is None else out_dtype
-        self.cfg = _Config(kind, d, hidden, chunk, _DT[in_dtype], _DT[out_dtype], c_mode, path)
+        self.cfg = _Config(kind, d, hidden, chunk, _DT[in_dtype], _DT[out_dtype], c_mode, path, loss, huber_delta)
         self.kind, self.d, self.hidden, self.chunk = kind, d, hidden, chunk
         self.in_dtype, self.out_dtype, self.c_mode = in_dtype, out_dtype, c_mode
         self.device = device

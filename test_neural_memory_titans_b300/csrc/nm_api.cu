@@ -43,6 +43,8 @@ int check_config(const nm_config* c) {
     if (c->path < NM_PATH_AUTO || c->path > NM_PATH_TC) return NM_ERR_ARG;
     if (c->d <= 0 || c->chunk <= 0) return NM_ERR_ARG;
     if (c->kind == NM_MLP2 && c->hidden <= 0) return NM_ERR_ARG;
+    if (c->loss != NM_LOSS_L2 && c->loss != NM_LOSS_HUBER) return NM_ERR_ARG;
+    if (c->loss == NM_LOSS_HUBER && !(c->huber_delta > 0.0f && c->huber_delta <= 3.0e38f)) return NM_ERR_ARG;
     return NM_OK;
 }
 
@@ -204,6 +206,8 @@ int nm_forward(nm_handle_t h, int B, int H, int T, const void* q, const void* k,
     a.scratch_bytes = h->workspace_bytes;
     a.skip_first_load = h->inject_load_skip;
     h->inject_load_skip = 0;
+    a.e_clip = nm_err_clip(cfg);
+    a.surprise = nullptr;
     cudaError_t e = h->path == NM_PATH_TC ? nm_tc_launch(cfg, a, s, h->num_sms, &h->launches)
                                           : nm_simt_launch(cfg, a, s, &h->launches);
     if (e != cudaSuccess) {

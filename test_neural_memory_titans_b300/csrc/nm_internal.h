@@ -2,6 +2,7 @@
 // files.  Not part of the public ABI.
 #pragma once
 
+#include <math.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -27,7 +28,16 @@ struct nm_args {
     void* scratch;    // device workspace owned by the handle (may be NULL)
     size_t scratch_bytes;
     int skip_first_load;  // test hook: tensor-core kernels skip chunk 0's tile loads
+    float e_clip;     // |e| bound: 2 delta for the Huber loss, +inf for the squared loss
+    float* surprise;  // [B, H, T] per-token gradient norms, or NULL (not computed)
 };
+
+// The error e = d rho / d r of the loss at the residual r = M(k) - v, given
+// 2 r: unchanged for the squared loss (e_clip = +inf), clipped to
+// [-2 delta, 2 delta] for the Huber loss.  A NaN passes through unchanged.
+__host__ __device__ inline float nm_clip_err(float two_r, float e_clip) {
+    return two_r > e_clip ? e_clip : (two_r < -e_clip ? -e_clip : two_r);
+}
 
 struct nm_handle {
     nm_config cfg;
@@ -42,6 +52,11 @@ struct nm_handle {
     long long launches;
     int inject_load_skip;  // armed by nm_inject_missing_load, consumed by the next nm_forward
 };
+
+// The |e| bound of a configuration (see nm_clip_err).
+static inline float nm_err_clip(const nm_config& c) {
+    return c.loss == NM_LOSS_HUBER ? 2.0f * c.huber_delta : HUGE_VALF;
+}
 
 // Parameters per unit.
 static inline long long nm_param_count(const nm_config& c) {

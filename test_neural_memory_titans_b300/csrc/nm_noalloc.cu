@@ -73,6 +73,8 @@ extern "C" int nm_forward_mlp2_noalloc(const nm_config* cfg, int B, int H, int T
         return NM_ERR_ARG;
     if (cfg->c_mode < NM_C_ONE || cfg->c_mode > NM_C_PER_TOKEN) return NM_ERR_ARG;
     if (cfg->path != NM_PATH_AUTO && cfg->path != NM_PATH_SIMT) return NM_ERR_UNSUPPORTED;
+    if (cfg->loss != NM_LOSS_L2 && cfg->loss != NM_LOSS_HUBER) return NM_ERR_ARG;
+    if (cfg->loss == NM_LOSS_HUBER && !(cfg->huber_delta > 0.0f && cfg->huber_delta <= 3.0e38f)) return NM_ERR_ARG;
     nm_config run = *cfg;
     run.path = NM_PATH_SIMT;
     if (!nm_simt_supports(run)) return NM_ERR_UNSUPPORTED;
@@ -132,6 +134,8 @@ extern "C" int nm_forward_mlp2_noalloc(const nm_config* cfg, int B, int H, int T
     a.scratch = scratch;
     a.scratch_bytes = NM_NOALLOC_SCRATCH_BYTES;
     a.skip_first_load = 0;
+    a.e_clip = nm_err_clip(run);
+    a.surprise = nullptr;
     long long launched = 0;
     if (nm_simt_launch(run, a, s, &launched) != cudaSuccess) {
         cudaGetLastError();

@@ -121,14 +121,14 @@ __global__ void __launch_bounds__(D * LIN_R) simt_linear_kernel(nm_args a, int c
                 gc[i] = momentum_coef(c_mode, be[sb + i], cc, sb + i);
             }
             __syncthreads();
-            // e_t = 2 (W0 k_t - v_t): gradient of ||W0 k - v||^2 is e k^T
+            // e_t = 2 (W0 k_t - v_t): gradient of ||W0 k - v||^2 is e k^T (clipped for the Huber loss)
             for (int t = 0; t < n; ++t) {
                 float acc = 0.f;
 #pragma unroll
                 for (int j = 0; j < J; ++j) acc = fmaf(W0[j], Ks[t * D + j * R + s], acc);
 #pragma unroll
                 for (int o = R / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-                if (s == 0) Es[t * D + r] = 2.0f * (acc - ld_in(v + (sb + t) * D + r));
+                if (s == 0) Es[t * D + r] = nm_clip_err(2.0f * (acc - ld_in(v + (sb + t) * D + r)), a.e_clip);
             }
             __syncthreads();
             for (int t = 0; t < n; ++t) {
@@ -276,12 +276,12 @@ __global__ void __launch_bounds__(MLP_THREADS) simt_mlp_kernel(nm_args a, int d,
             Ak[idx] = silu_f(acc);
         }
         __syncthreads();
-        // e = 2 (W2 a - v)
+        // e = 2 (W2 a - v), clipped for the Huber loss
         for (int idx = tid; idx < n * d; idx += NT) {
             const int t = idx / d, o = idx % d;
             float acc = 0.f;
             for (int j = 0; j < hd; ++j) acc = fmaf(Ak[t * hd + j], W2[(long long)o * hd + j], acc);
-            E[idx] = 2.0f * (acc - Vf[idx]);
+            E[idx] = nm_clip_err(2.0f * (acc - Vf[idx]), a.e_clip);
         }
         __syncthreads();
         // delta = (W2^T e) * silu'(z);  Pm = Gamma (.) (Q K^T), lower triangle

@@ -390,7 +390,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             float vv[32], o[32];
             get_row32(sm + OFF_V, BC, t, c0, vv);
 #pragma unroll
-            for (int q = 0; q < 32; ++q) e0[q] = live ? 2.0f * (e0[q] - vv[q]) : 0.0f;
+            for (int q = 0; q < 32; ++q) e0[q] = live ? nm_clip_err(2.0f * (e0[q] - vv[q]), a.e_clip) : 0.0f;
             put_row32(sm + OFF_E, BC, t, c0, e0);
 #pragma unroll
             for (int q = 0; q < 32; ++q) o[q] = gm * e0[q];

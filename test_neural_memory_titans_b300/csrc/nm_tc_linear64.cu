@@ -394,7 +394,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 float vv[32], o[32];
                 get_row32(sm + OFF_V + stage * T64, t, c0, vv);
 #pragma unroll
-                for (int q = 0; q < 32; ++q) e[q] = live ? 2.0f * (e[q] - vv[q]) : 0.0f;
+                for (int q = 0; q < 32; ++q) e[q] = live ? nm_clip_err(2.0f * (e[q] - vv[q]), a.e_clip) : 0.0f;
                 put_row32(sm + OFF_E, 64, t, c0, e);
                 const float gm = sGl[t], uu = sU[t];
 #pragma unroll

@@ -546,6 +546,8 @@ __global__ void __launch_bounds__(128 * (64 / CW), 1)
 #pragma unroll
                 for (int q = 0; q < CW; ++q) ev[q] = fmaf(2.0f, px[q], ev[q]);
             }
+#pragma unroll
+            for (int q = 0; q < CW; ++q) ev[q] = nm_clip_err(ev[q], a.e_clip);  // the Huber loss clips e
             put_row<CW>(sm + OFF_E, 64, tr, CW * hq, ev);
             float o1[CW];
             const float gm = -sGl[tr], uu = sU[tr];

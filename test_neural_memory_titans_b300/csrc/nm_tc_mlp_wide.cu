@@ -487,7 +487,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
                         const int t = 4 * c4 + k;
-                        e[k] = t < n ? 2.0f * (sv[k] - __bfloat162float(vs[t * OR + row])) : 0.0f;
+                        e[k] = t < n ? nm_clip_err(2.0f * (sv[k] - __bfloat162float(vs[t * OR + row])), a.e_clip) : 0.0f;
                     }
                     const uint32_t w0 = pack_bf16(e[0], e[1]), w1 = pack_bf16(e[2], e[3]);
                     const uint32_t off = sw128_offset(own_lo + row, 4 * c4, 128);

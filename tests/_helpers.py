@@ -33,9 +33,11 @@ def f64(t: torch.Tensor) -> np.ndarray:
 
 
 def gpu_forward(wl: W.Workload, x: dict, path: int = nm.PATH_AUTO, M0=None, S0=None, c_mode=nm.C_ONE,
-                chunk=None, out_dtype=None):
+                chunk=None, out_dtype=None, huber_delta=None):
     mem = nm.NeuralMemory(wl.kind, wl.d, wl.hidden, wl.chunk if chunk is None else chunk, in_dtype=wl.dtype,
-                          out_dtype=out_dtype, c_mode=c_mode, path=path)
+                          out_dtype=out_dtype, c_mode=c_mode, path=path,
+                          loss=nm.LOSS_L2 if huber_delta is None else nm.LOSS_HUBER,
+                          huber_delta=0.0 if huber_delta is None else huber_delta)
     dev = torch.device("cuda", 0)
     g = lambda t: None if t is None else t.to(dev).contiguous()
     y, MT, ST = mem.forward(g(x["q"]), g(x["k"]), g(x["v"]), g(x["alpha"]), g(x["eta"]), g(x["beta"]),
@@ -48,7 +50,7 @@ def gpu_forward(wl: W.Workload, x: dict, path: int = nm.PATH_AUTO, M0=None, S0=N
 
 
 def oracle_forward(wl: W.Workload, x: dict, units=None, M0=None, S0=None, c_mode=oracle.C_ONE, chunk=None,
-                   T=None):
+                   T=None, huber_delta=None):
     """Oracle on the selected flat (batch*head) units and first T tokens."""
     B, H = wl.B, wl.H
     T = x["q"].shape[2] if T is None else T
@@ -67,7 +69,9 @@ def oracle_forward(wl: W.Workload, x: dict, units=None, M0=None, S0=None, c_mode
     S0 = x["S0"] if S0 is None else S0
     return oracle.forward(wl.kind, wl.d, wl.hidden, wl.chunk if chunk is None else chunk, c_mode,
                           sel(x["q"]), sel(x["k"]), sel(x["v"]), sel(x["alpha"]), sel(x["eta"]), sel(x["beta"]),
-                          sel(x.get("c")), sel(M0, False), sel(S0, False))
+                          sel(x.get("c")), sel(M0, False), sel(S0, False),
+                          oracle.LOSS_L2 if huber_delta is None else oracle.LOSS_HUBER,
+                          np.inf if huber_delta is None else huber_delta)
 
 
 def pick(t: torch.Tensor, wl: W.Workload, units=None, T=None) -> np.ndarray:

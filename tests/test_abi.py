@@ -55,7 +55,8 @@ def test_status_codes_match_header():
     for name, py in (("NM_LINEAR", "LINEAR"), ("NM_MLP2", "MLP2"), ("NM_F32", "F32"), ("NM_BF16", "BF16"),
                      ("NM_C_ONE", "C_ONE"), ("NM_C_ONE_MINUS_BETA", "C_ONE_MINUS_BETA"),
                      ("NM_C_PER_TOKEN", "C_PER_TOKEN"), ("NM_PATH_AUTO", "PATH_AUTO"),
-                     ("NM_PATH_SIMT", "PATH_SIMT"), ("NM_PATH_TC", "PATH_TC")):
+                     ("NM_PATH_SIMT", "PATH_SIMT"), ("NM_PATH_TC", "PATH_TC"), ("NM_LOSS_L2", "LOSS_L2"),
+                     ("NM_LOSS_HUBER", "LOSS_HUBER")):
         assert getattr(nm, py) == defs[name]
 
 
@@ -72,6 +73,13 @@ def test_null_handle_and_bad_config_without_gpu():
     big_chunk = nm._Config(nm.LINEAR, 64, 0, 1024, nm.BF16, nm.BF16, nm.C_ONE, nm.PATH_AUTO)
     assert lib.nm_create(ctypes.byref(big_chunk), 0, ctypes.byref(h)) == nm.NM_ERR_UNSUPPORTED
     assert lib.nm_create(None, 0, ctypes.byref(h)) == nm.NM_ERR_ARG
+    # the loss: an unknown kind, or a Huber threshold that is not finite and positive
+    for loss, delta in ((2, 1.0), (nm.LOSS_HUBER, 0.0), (nm.LOSS_HUBER, -1.0), (nm.LOSS_HUBER, float("inf")),
+                        (nm.LOSS_HUBER, float("nan"))):
+        cfg = nm._Config(nm.LINEAR, 64, 0, 64, nm.BF16, nm.BF16, nm.C_ONE, nm.PATH_AUTO, loss, delta)
+        assert lib.nm_create(ctypes.byref(cfg), 0, ctypes.byref(h)) == nm.NM_ERR_ARG
+        assert lib.nm_forward_mlp2_noalloc(ctypes.byref(cfg), 1, 1, 1, *([None] * 12), None) in (
+            nm.NM_ERR_ARG, nm.NM_ERR_UNSUPPORTED)
 
 
 # ------------------------------------------------------------------ on a GPU

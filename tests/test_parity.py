@@ -325,3 +325,55 @@ def test_linear_d64_momentum_forms(c_mode):
     M0, S0 = W.random_state(wl, "cuda", seed=96, scale=0.5)
     gpu = gpu_forward(wl, x, nm.PATH_TC, M0=M0, S0=S0, c_mode=c_mode)
     compare(wl, gpu, oracle_forward(wl, x, M0=M0, S0=S0, c_mode=c_mode))
+
+
+# ------------------------------------------------------------ Huber loss (YAAD reading)
+# e = 2 clip(M(k) - v, -delta, delta) replaces e = 2 (M(k) - v) in every kernel;
+# delta is chosen so that a good share of the first chunk's residuals is clipped.
+
+def _clipped_share(wl, x, M0, delta):
+    """Share of the first chunk's residuals M0(k) - v beyond delta (numpy, fp64)."""
+    k = f64(x["k"]).reshape(wl.B * wl.H, -1, wl.d)[:, :wl.chunk]
+    v = f64(x["v"]).reshape(wl.B * wl.H, -1, wl.d)[:, :wl.chunk]
+    W0 = f64(M0).reshape(wl.B * wl.H, -1)
+    share = []
+    for u in range(k.shape[0]):
+        r = np.stack([oracle.memory_apply(wl.kind, wl.d, wl.hidden, W0[u], kt) for kt in k[u]]) - v[u]
+        share.append(np.mean(np.abs(r) > delta))
+    return float(np.mean(share))
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("wid,T,chunk,delta", [(2, 300, 64, 0.08), (4, 700, 256, 0.08), (4, 130, 64, 0.08),
+                                               (0, 200, 16, 0.5)])
+def test_huber_linear(path, wid, T, chunk, delta):
+    wl = dataclasses.replace(W.WORKLOADS[wid].with_sizes(B=2, H=2, T=T, segment=0), chunk=chunk)
+    _skip_unsupported(wl, path)
+    x = W.make_inputs(wl, "cuda", seed=90 + T)
+    M0, S0 = W.random_state(wl, "cuda", seed=91, scale=0.5)
+    share = _clipped_share(wl, x, M0, delta)
+    assert 0.1 < share < 0.9, share
+    gpu = gpu_forward(wl, x, path, M0=M0, S0=S0, huber_delta=delta)
+    ref = oracle_forward(wl, x, M0=M0, S0=S0, huber_delta=delta)
+    compare(wl, gpu, ref)
+    # and it is not the squared loss's result
+    l2 = oracle_forward(wl, x, M0=M0, S0=S0)
+    assert rel_l2(l2[1], ref[1]) > 10 * TOL[wl.dtype]["M_T"]
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("hidden,d,T", [(256, 64, 100), (256, 64, 257), (128, 64, 130), (512, 128, 100)])
+def test_huber_mlp(path, hidden, d, T):
+    base = W.WORKLOADS[1] if d == 64 else W.WORKLOADS[3]
+    wl = dataclasses.replace(base, hidden=hidden).with_sizes(B=1, H=2, T=T)
+    _skip_unsupported(wl, path)
+    x = W.make_inputs(wl, "cuda", seed=95 + T + hidden)
+    M0, S0 = W.random_state(wl, "cuda", seed=96, scale=0.5)
+    delta = 0.5 if d == 64 else 0.05
+    share = _clipped_share(wl, x, M0, delta)
+    assert 0.1 < share < 0.9, share
+    gpu = gpu_forward(wl, x, path, M0=M0, S0=S0, huber_delta=delta)
+    ref = oracle_forward(wl, x, M0=M0, S0=S0, huber_delta=delta)
+    compare(wl, gpu, ref)
+    l2 = oracle_forward(wl, x, M0=M0, S0=S0)
+    assert rel_l2(l2[1], ref[1]) > 10 * TOL[wl.dtype]["M_T"]
