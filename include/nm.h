@@ -135,6 +135,28 @@ int nm_forward(nm_handle_t h, int B, int H, int T,
                void* y, float* M_T, float* S_T, void* stream);
 
 /*
+ * nm_forward_surprise - nm_forward that also writes each token's surprise,
+ *   the norm of the loss gradient with respect to the memory's parameters
+ *   (0h-n0.github.io explainer, "技術的詳細", "Surprise機構"):
+ *     surprise [B, H, T] fp32 (DEVICE, caller-owned, 16-byte aligned, written)
+ *       = || g_t ||_F over all parameters, with g_t the gradient the update
+ *         uses: at the chunk-start weights, of the configured loss.
+ *   Linear memory: ||e_t|| ||k_t||; MLP2: sqrt(||delta_t||^2 ||k_t||^2 +
+ *   ||e_t||^2 ||silu(W1 k_t)||^2).  Tokens are computed from the same fp32 e
+ *   (and delta) as the update, before any rounding to bf16.
+ *   Everything else is nm_forward's contract; `surprise` must not overlap any
+ *   other buffer (NM_ERR_ALIAS) and must not be NULL (NM_ERR_ARG).
+ *   Returns NM_ERR_UNSUPPORTED when the handle's kernel does not write it
+ *   (the tensor-core MLP2 kernels; the fp32 FFMA kernels and the tensor-core
+ *   linear kernels do).
+ */
+int nm_forward_surprise(nm_handle_t h, int B, int H, int T,
+                        const void* q, const void* k, const void* v,
+                        const float* alpha, const float* eta, const float* beta,
+                        const float* c, const float* M0, const float* S0,
+                        void* y, float* M_T, float* S_T, float* surprise, void* stream);
+
+/*
  * nm_forward_host - the same operation on HOST buffers (same layouts).
  *   Copies the inputs to the handle's device (into handle-owned buffers that
  *   grow on demand), runs nm_forward on `stream`, copies y, M_T, S_T back and

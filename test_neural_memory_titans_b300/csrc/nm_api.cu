@@ -142,9 +142,11 @@ int nm_inject_missing_load(nm_handle_t h) {
 
 long long nm_launch_count(nm_handle_t h) { return h ? h->launches : -1; }
 
-int nm_forward(nm_handle_t h, int B, int H, int T, const void* q, const void* k, const void* v,
-               const float* alpha, const float* eta, const float* beta, const float* c,
-               const float* M0, const float* S0, void* y, float* M_T, float* S_T, void* stream) {
+namespace {
+
+int forward_impl(nm_handle_t h, int B, int H, int T, const void* q, const void* k, const void* v,
+                 const float* alpha, const float* eta, const float* beta, const float* c, const float* M0,
+                 const float* S0, void* y, float* M_T, float* S_T, float* surprise, void* stream) {
     if (!h) return NM_ERR_ARG;
     const nm_config& cfg = h->cfg;
     if (B < 0 || H < 0 || T < 0) return NM_ERR_ARG;
@@ -156,9 +158,10 @@ int nm_forward(nm_handle_t h, int B, int H, int T, const void* q, const void* k,
     if (T > 0 && (!q || !k || !v || !alpha || !eta || !beta || !y)) return NM_ERR_ARG;
     if (T > 0 && need_c && !c) return NM_ERR_ARG;
     if (!need_c && c) return NM_ERR_ARG;
-    const void* ptrs[] = {q, k, v, alpha, eta, beta, c, M0, S0, y, M_T, S_T};
+    const void* ptrs[] = {q, k, v, alpha, eta, beta, c, M0, S0, y, M_T, S_T, surprise};
     for (const void* p : ptrs)
         if (p && !aligned16(p)) return NM_ERR_ALIGN;
+    if (surprise && !nm_supports_surprise(cfg, h->path)) return NM_ERR_UNSUPPORTED;
 
     const size_t tok = (size_t)units * (size_t)T;
     const size_t P = (size_t)nm_param_count(cfg);
@@ -171,14 +174,15 @@ int nm_forward(nm_handle_t h, int B, int H, int T, const void* q, const void* k,
                     {(const char*)eta, gate_b},           {(const char*)beta, gate_b},
                     {(const char*)c, need_c ? gate_b : 0}, {(const char*)M0, st_b},
                     {(const char*)S0, st_b}};
-    Range out_r[] = {{(const char*)y, T ? out_b : 0}, {(const char*)M_T, st_b}, {(const char*)S_T, st_b}};
-    for (int o = 0; o < 3; ++o) {
+    Range out_r[] = {{(const char*)y, T ? out_b : 0}, {(const char*)M_T, st_b}, {(const char*)S_T, st_b},
+                     {(const char*)surprise, T ? gate_b : 0}};
+    for (int o = 0; o < 4; ++o) {
         for (int i = 0; i < 9; ++i) {
             bool exact_ok = (o == 1 && i == 7) || (o == 2 && i == 8);
             if (exact_ok && out_r[o].p == in_r[i].p) continue;
             if (overlaps(out_r[o], in_r[i])) return NM_ERR_ALIAS;
         }
-        for (int o2 = o + 1; o2 < 3; ++o2)
+        for (int o2 = o + 1; o2 < 4; ++o2)
             if (overlaps(out_r[o], out_r[o2])) return NM_ERR_ALIAS;
     }
 
@@ -207,7 +211,7 @@ int nm_forward(nm_handle_t h, int B, int H, int T, const void* q, const void* k,
     a.skip_first_load = h->inject_load_skip;
     h->inject_load_skip = 0;
     a.e_clip = nm_err_clip(cfg);
-    a.surprise = nullptr;
+    a.surprise = surprise;
     cudaError_t e = h->path == NM_PATH_TC ? nm_tc_launch(cfg, a, s, h->num_sms, &h->launches)
                                           : nm_simt_launch(cfg, a, s, &h->launches);
     if (e != cudaSuccess) {
@@ -215,6 +219,22 @@ int nm_forward(nm_handle_t h, int B, int H, int T, const void* q, const void* k,
         return NM_ERR_CUDA;
     }
     return NM_OK;
+}
+
+}  // namespace
+
+int nm_forward(nm_handle_t h, int B, int H, int T, const void* q, const void* k, const void* v,
+               const float* alpha, const float* eta, const float* beta, const float* c,
+               const float* M0, const float* S0, void* y, float* M_T, float* S_T, void* stream) {
+    return forward_impl(h, B, H, T, q, k, v, alpha, eta, beta, c, M0, S0, y, M_T, S_T, nullptr, stream);
+}
+
+int nm_forward_surprise(nm_handle_t h, int B, int H, int T, const void* q, const void* k, const void* v,
+                        const float* alpha, const float* eta, const float* beta, const float* c,
+                        const float* M0, const float* S0, void* y, float* M_T, float* S_T, float* surprise,
+                        void* stream) {
+    if (!surprise) return NM_ERR_ARG;
+    return forward_impl(h, B, H, T, q, k, v, alpha, eta, beta, c, M0, S0, y, M_T, S_T, surprise, stream);
 }
 
 int nm_synchronize(nm_handle_t h) {

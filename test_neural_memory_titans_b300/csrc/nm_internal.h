@@ -70,5 +70,11 @@ cudaError_t nm_simt_launch(const nm_config& c, const nm_args& a, cudaStream_t s,
 
 // ---- tcgen05 tensor-core kernels (nm_tc_*.cu) -----------------------------
 bool nm_tc_supports(const nm_config& c);
+bool nm_tc_supports_surprise(const nm_config& c);
+
+// Whether the kernel family `path` writes the per-token surprise for `c`.
+static inline bool nm_supports_surprise(const nm_config& c, int path) {
+    return path == NM_PATH_SIMT || nm_tc_supports_surprise(c);
+}
 size_t nm_tc_scratch_bytes(const nm_config& c, int B, int H);
 cudaError_t nm_tc_launch(const nm_config& c, const nm_args& a, cudaStream_t s, int num_sms, long long* launches);

@@ -131,6 +131,17 @@ __global__ void __launch_bounds__(D * LIN_R) simt_linear_kernel(nm_args a, int c
                 if (s == 0) Es[t * D + r] = nm_clip_err(2.0f * (acc - ld_in(v + (sb + t) * D + r)), a.e_clip);
             }
             __syncthreads();
+            if (a.surprise) {  // surprise_t = ||e_t k_t^T||_F = ||e_t|| ||k_t||, one thread per token
+                for (int t = tid; t < n; t += NT) {
+                    float e2 = 0.f, k2 = 0.f;
+                    for (int o0 = 0; o0 < D; ++o0) {
+                        const int o = (o0 + t) % D;  // rotated: conflict-free across the warp
+                        e2 = fmaf(Es[t * D + o], Es[t * D + o], e2);
+                        k2 = fmaf(Ks[t * D + o], Ks[t * D + o], k2);
+                    }
+                    a.surprise[unit * T + sb + t] = sqrtf(e2) * sqrtf(k2);
+                }
+            }
             for (int t = 0; t < n; ++t) {
                 const float ce = gc[t] * Es[t * D + r];
                 const float at = ga[t], eh = ge[t], bt = gb[t];
@@ -301,6 +312,24 @@ __global__ void __launch_bounds__(MLP_THREADS) simt_mlp_kernel(nm_args a, int d,
             Pm[(size_t)t * b + i] = acc;
         }
         __syncthreads();
+        if (a.surprise) {
+            // surprise_t = ||(delta_t k_t^T, e_t a(k_t)^T)||_F
+            //            = sqrt(||delta_t||^2 ||k_t||^2 + ||e_t||^2 ||a(k_t)||^2), one thread per token
+            for (int t = tid; t < n; t += NT) {
+                float d2 = 0.f, a2 = 0.f, e2 = 0.f, k2 = 0.f;
+                for (int j0 = 0; j0 < hd; ++j0) {
+                    const int j = (j0 + t) % hd;  // rotated: conflict-free across the warp
+                    d2 = fmaf(Dl[t * hd + j], Dl[t * hd + j], d2);
+                    a2 = fmaf(Ak[t * hd + j], Ak[t * hd + j], a2);
+                }
+                for (int x0 = 0; x0 < d; ++x0) {
+                    const int x = (x0 + t) % d;
+                    e2 = fmaf(E[t * d + x], E[t * d + x], e2);
+                    k2 = fmaf(Kf[t * d + x], Kf[t * d + x], k2);
+                }
+                a.surprise[unit * T + t0 + t] = sqrtf(fmaf(d2, k2, e2 * a2));
+            }
+        }
         // layer 1 at token t: A_t W1 q - sigma_t S1 q - sum_i Gamma_{t,i} (k_i.q) delta_i
         for (int idx = tid; idx < n * hd; idx += NT) {
             const int t = idx / hd, j = idx % hd;

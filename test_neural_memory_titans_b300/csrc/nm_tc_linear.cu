@@ -64,7 +64,7 @@ constexpr uint32_t OFF_P = OFF_EU + TILE;        // [64 t][64 i] bf16
 constexpr int GS = 68;                           // padded fp32 row stride of Gamma
 constexpr uint32_t OFF_GM = OFF_P + HALF;
 constexpr uint32_t OFF_F = OFF_GM + 64 * GS * 4; // gates [2][4][64], A, B, sigma, gamma, u
-constexpr uint32_t N_F = 2 * 4 * BC + 5 * BC;
+constexpr uint32_t N_F = 2 * 4 * BC + 5 * BC + 4 * BC;  // + surprise partials [2 halves][e2, k2][64]
 constexpr uint32_t OFF_BAR = OFF_F + 4 * N_F;
 constexpr uint32_t SMEM_USED = OFF_BAR + 64;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;  // slack for 1024-byte alignment
@@ -133,6 +133,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     float* sSg = sBc + BC;
     float* sGl = sSg + BC;
     float* sU = sGl + BC;
+    float* sPart = sU + BC;  // surprise partial sums: [hf][||e||^2 | ||k||^2][64]
     float* Gm = reinterpret_cast<float*>(sm + OFF_GM);
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + OFF_BAR);  // 0,1: Q|K stages; 2: V; 3: mma
     __shared__ uint32_t s_tmem;
@@ -391,6 +392,21 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             get_row32(sm + OFF_V, BC, t, c0, vv);
 #pragma unroll
             for (int q = 0; q < 32; ++q) e0[q] = live ? nm_clip_err(2.0f * (e0[q] - vv[q]), a.e_clip) : 0.0f;
+            if (a.surprise) {  // partial ||e_t||^2 and ||k_t||^2 over this thread's 32 columns, summed over the row
+                float kv[32], e2 = 0.0f, k2 = 0.0f;
+                get_row32(sm + OFF_K + stage * TILE, BC, t, c0, kv);
+#pragma unroll
+                for (int q = 0; q < 32; ++q) {
+                    e2 = fmaf(e0[q], e0[q], e2);
+                    k2 = fmaf(kv[q], kv[q], k2);
+                }
+                e2 += __shfl_xor_sync(0xffffffffu, e2, 16);
+                k2 += __shfl_xor_sync(0xffffffffu, k2, 16);
+                if (!upper) {
+                    sPart[hf * 2 * BC + t] = e2;
+                    sPart[hf * 2 * BC + BC + t] = k2;
+                }
+            }
             put_row32(sm + OFF_E, BC, t, c0, e0);
 #pragma unroll
             for (int q = 0; q < 32; ++q) o[q] = gm * e0[q];
@@ -417,6 +433,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                               : c_mode == NM_C_PER_TOKEN ? nxt_c : 1.0f;
         }
         handoff();
+        if (a.surprise && hf == 0 && lane < 16) {  // surprise_t = ||e_t|| ||k_t||, token t = 16 qd + lane
+            const int t = 16 * qd + lane;
+            if (t < n)
+                a.surprise[unit * T + t0 + t] = sqrtf(sPart[t] + sPart[2 * BC + t]) *
+                                                 sqrtf(sPart[BC + t] + sPart[3 * BC + t]);
+        }
         // ---- batch 2: S0 Q^T, E^T P^T, M += (-gamma E)^T K, S += (u E)^T K; the next V tile
         const bool go2 = !failed;
         if (go2 && tid == 0) {

@@ -66,7 +66,7 @@ constexpr uint32_t OFF_GM = OFF_P + T64;           // fp32 Gamma [64][GS]
 constexpr uint32_t OFF_M0F = OFF_GM + 64 * GS * 4; // fp32 chunk-start M [64][GS]
 constexpr uint32_t OFF_S0F = OFF_M0F + 64 * GS * 4;
 constexpr uint32_t OFF_F = OFF_S0F + 64 * GS * 4;  // gates [2][4][64]; p, w, r, A, sigma, gamma, u [64]
-constexpr uint32_t N_F = 2 * 4 * SB + 7 * SB;
+constexpr uint32_t N_F = 2 * 4 * SB + 7 * SB + 4 * SB;  // + surprise partials [2 halves][e2, k2][64]
 constexpr uint32_t OFF_BAR = OFF_F + 4 * N_F;
 constexpr uint32_t SMEM_USED = OFF_BAR + 64;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;
@@ -140,6 +140,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     float* sSg = sA + SB;                                 // chunk-level sigma_t
     float* sGl = sSg + SB;                                // gamma_i of the block
     float* sU = sGl + SB;                                 // u_i of the block
+    float* sPart = sU + SB;                               // surprise partial sums: [hf][||e||^2 | ||k||^2][64]
     float* Gm = reinterpret_cast<float*>(sm + OFF_GM);
     float* M0f = reinterpret_cast<float*>(sm + OFF_M0F);
     float* S0f = reinterpret_cast<float*>(sm + OFF_S0F);
@@ -395,6 +396,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 get_row32(sm + OFF_V + stage * T64, t, c0, vv);
 #pragma unroll
                 for (int q = 0; q < 32; ++q) e[q] = live ? nm_clip_err(2.0f * (e[q] - vv[q]), a.e_clip) : 0.0f;
+                if (a.surprise) {  // partial ||e_t||^2, ||k_t||^2 over this thread's 32 columns
+                    float kv[32], e2 = 0.0f, k2 = 0.0f;
+                    get_row32(sm + OFF_K + stage * T64, t, c0, kv);
+#pragma unroll
+                    for (int q = 0; q < 32; ++q) {
+                        e2 = fmaf(e[q], e[q], e2);
+                        k2 = fmaf(kv[q], kv[q], k2);
+                    }
+                    sPart[hf * 2 * SB + t] = e2;
+                    sPart[hf * 2 * SB + SB + t] = k2;
+                }
                 put_row32(sm + OFF_E, 64, t, c0, e);
                 const float gm = sGl[t], uu = sU[t];
 #pragma unroll
@@ -422,6 +434,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                               : c_mode == NM_C_PER_TOKEN ? nxt_c : 1.0f;
         }
         handoff();
+        if (a.surprise && hf == 0 && r64 && rr < n)  // surprise_t = ||e_t|| ||k_t|| (gradient at the chunk start)
+            a.surprise[unit * T + t0 + rr] = sqrtf(sPart[rr] + sPart[2 * SB + rr]) * sqrtf(sPart[SB + rr] + sPart[3 * SB + rr]);
         // ---- batch 2: Q [M0 | S0 | CG | CU]^T, P E, CG += (gamma E)^T K, CU += (u E)^T K
         const bool go2 = !failed;
         if (go2 && tid == 0) {

@@ -63,6 +63,7 @@ def test_status_codes_match_header():
 def test_null_handle_and_bad_config_without_gpu():
     lib = nm.load_library()
     assert lib.nm_forward(None, 1, 1, 1, *([None] * 12), None) == nm.NM_ERR_ARG
+    assert lib.nm_forward_surprise(None, 1, 1, 1, *([None] * 13), None) == nm.NM_ERR_ARG
     assert lib.nm_synchronize(None) == nm.NM_ERR_ARG
     assert lib.nm_destroy(None) == nm.NM_OK
     h = ctypes.c_void_p()

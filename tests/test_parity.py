@@ -377,3 +377,59 @@ def test_huber_mlp(path, hidden, d, T):
     compare(wl, gpu, ref)
     l2 = oracle_forward(wl, x, M0=M0, S0=S0)
     assert rel_l2(l2[1], ref[1]) > 10 * TOL[wl.dtype]["M_T"]
+
+
+# ------------------------------------------------------------ surprise (per-token gradient norm)
+# nm_forward_surprise also writes ||g_t||_F, the norm of the gradient the update
+# uses (at the chunk-start weights).  Compared with the oracle's like y (relative
+# L2 over [B, H, T]); the other outputs must equal nm_forward's bit for bit.
+
+def _surprise_case(wl, x, path, M0, S0, huber_delta):
+    mem = nm.NeuralMemory(wl.kind, wl.d, wl.hidden, wl.chunk, in_dtype=wl.dtype, path=path,
+                          loss=nm.LOSS_L2 if huber_delta is None else nm.LOSS_HUBER,
+                          huber_delta=0.0 if huber_delta is None else huber_delta)
+    args = (x["q"], x["k"], x["v"], x["alpha"], x["eta"], x["beta"], M0, S0)
+    y, MT, ST, sur = mem.forward_surprise(*args)
+    y2, MT2, ST2 = mem.forward(*args)
+    assert mem.synchronize() == nm.NM_OK
+    assert mem.path == path or path == nm.PATH_AUTO
+    mem.close()
+    for a_, b_ in ((y, y2), (MT, MT2), (ST, ST2)):
+        assert torch.equal(a_, b_)
+    B, H, T = x["alpha"].shape
+    ref = oracle.forward(wl.kind, wl.d, wl.hidden, wl.chunk, oracle.C_ONE,
+                         *(f64(x[k_]) for k_ in ("q", "k", "v", "alpha", "eta", "beta")), None, f64(M0), f64(S0),
+                         oracle.LOSS_L2 if huber_delta is None else oracle.LOSS_HUBER,
+                         np.inf if huber_delta is None else huber_delta, surprise=True)
+    err = rel_l2(f64(sur), ref[3])
+    assert err <= TOL[wl.dtype]["y"], err
+    assert np.all(np.isfinite(f64(sur)))
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("wid,T,chunk,delta", [(2, 300, 64, None), (2, 130, 64, 0.08), (4, 700, 256, None),
+                                               (4, 300, 64, 0.08), (0, 200, 16, None), (0, 100, 16, 0.5)])
+def test_surprise_linear(path, wid, T, chunk, delta):
+    wl = dataclasses.replace(W.WORKLOADS[wid].with_sizes(B=2, H=2, T=T, segment=0), chunk=chunk)
+    _skip_unsupported(wl, path)
+    x = W.make_inputs(wl, "cuda", seed=120 + T)
+    M0, S0 = W.random_state(wl, "cuda", seed=121, scale=0.5)
+    _surprise_case(wl, x, path, M0, S0, delta)
+
+
+@pytest.mark.parametrize("hidden,d,T,delta", [(256, 64, 100, None), (128, 64, 70, 0.5)])
+def test_surprise_mlp_fp32_kernel(hidden, d, T, delta):
+    wl = dataclasses.replace(W.WORKLOADS[1], hidden=hidden).with_sizes(B=1, H=2, T=T)
+    x = W.make_inputs(wl, "cuda", seed=130 + T)
+    M0, S0 = W.random_state(wl, "cuda", seed=131, scale=0.5)
+    _surprise_case(wl, x, nm.PATH_SIMT, M0, S0, delta)
+
+
+def test_surprise_unsupported_on_tensor_core_mlp():
+    wl = W.WORKLOADS[1].with_sizes(B=1, H=1, T=64)
+    x = W.make_inputs(wl, "cuda", seed=3)
+    mem = nm.NeuralMemory(wl.kind, wl.d, wl.hidden, wl.chunk, in_dtype=wl.dtype, path=nm.PATH_TC)
+    with pytest.raises(nm.NMError) as ei:
+        mem.forward_surprise(x["q"], x["k"], x["v"], x["alpha"], x["eta"], x["beta"], x["M0"], x["S0"])
+    assert ei.value.status == nm.NM_ERR_UNSUPPORTED
+    mem.close()
