@@ -147,8 +147,8 @@ int nm_forward(nm_handle_t h, int B, int H, int T,
  *   Everything else is nm_forward's contract; `surprise` must not overlap any
  *   other buffer (NM_ERR_ALIAS) and must not be NULL (NM_ERR_ARG).
  *   Returns NM_ERR_UNSUPPORTED when the handle's kernel does not write it
- *   (the tensor-core MLP2 kernels; the fp32 FFMA kernels and the tensor-core
- *   linear kernels do).
+ *   (the tensor-core MLP2 kernel for d = 128; the fp32 FFMA kernels, the
+ *   tensor-core linear kernels and the tensor-core MLP2 kernel for d = 64 do).
  */
 int nm_forward_surprise(nm_handle_t h, int B, int H, int T,
                         const void* q, const void* k, const void* v,

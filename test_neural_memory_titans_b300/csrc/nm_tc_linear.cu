@@ -391,7 +391,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             float vv[32], o[32];
             get_row32(sm + OFF_V, BC, t, c0, vv);
 #pragma unroll
-            for (int q = 0; q < 32; ++q) e0[q] = live ? nm_clip_err(2.0f * (e0[q] - vv[q]), a.e_clip) : 0.0f;
+            for (int q = 0; q < 32; ++q) e0[q] = live ? 2.0f * (e0[q] - vv[q]) : 0.0f;
+            if (a.e_clip < HUGE_VALF) {  // the Huber loss clips e (uniform branch)
+#pragma unroll
+                for (int q = 0; q < 32; ++q) e0[q] = nm_clip_err(e0[q], a.e_clip);
+            }
             if (a.surprise) {  // partial ||e_t||^2 and ||k_t||^2 over this thread's 32 columns, summed over the row
                 float kv[32], e2 = 0.0f, k2 = 0.0f;
                 get_row32(sm + OFF_K + stage * TILE, BC, t, c0, kv);

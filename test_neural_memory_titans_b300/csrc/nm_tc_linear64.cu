@@ -395,7 +395,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 float vv[32], o[32];
                 get_row32(sm + OFF_V + stage * T64, t, c0, vv);
 #pragma unroll
-                for (int q = 0; q < 32; ++q) e[q] = live ? nm_clip_err(2.0f * (e[q] - vv[q]), a.e_clip) : 0.0f;
+                for (int q = 0; q < 32; ++q) e[q] = live ? 2.0f * (e[q] - vv[q]) : 0.0f;
+                if (a.e_clip < HUGE_VALF) {  // the Huber loss clips e (uniform branch)
+#pragma unroll
+                    for (int q = 0; q < 32; ++q) e[q] = nm_clip_err(e[q], a.e_clip);
+                }
                 if (a.surprise) {  // partial ||e_t||^2, ||k_t||^2 over this thread's 32 columns
                     float kv[32], e2 = 0.0f, k2 = 0.0f;
                     get_row32(sm + OFF_K + stage * T64, t, c0, kv);

@@ -83,7 +83,10 @@ constexpr uint32_t OFF_YX = OFF_GM + 2 * 64 * GS * 4;   // bf16 [64][XS] the pee
 constexpr uint32_t OFF_YR = OFF_YX + 64 * XS * 2;       // bf16 [64][RB] the peer's partial y (own columns)
 constexpr uint32_t OFF_F = OFF_YR + 64 * RB * 2;        // gates [2][4][64]; scan [2][A, B, sigma, gamma, u][64]
 constexpr uint32_t N_F = 2 * 4 * BC + 2 * 5 * BC;
-constexpr uint32_t OFF_BAR = OFF_F + 4 * N_F;
+constexpr uint32_t OFF_SP = OFF_F + 4 * N_F;  // surprise partials (fp32 [64] rows): ||a(k)||^2 [4 quadrants],
+constexpr uint32_t N_SP = 18 * BC;             // ||delta||^2 [4 quadrants], ||e||^2 [4 column groups],
+                                               // ||k||^2 [4 column groups], the peer's (||a||^2, ||delta||^2)
+constexpr uint32_t OFF_BAR = OFF_SP + 4 * N_SP;
 constexpr uint32_t SMEM_USED = OFF_BAR + 64;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;  // slack for the 1024-byte alignment
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
@@ -175,6 +178,9 @@ __device__ __forceinline__ void push_bf16(uint32_t dst, const float* v) {
                      "r"(pack_bf16(v[8 * q + 4], v[8 * q + 5])), "r"(pack_bf16(v[8 * q + 6], v[8 * q + 7]))
                      : "memory");
 }
+__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
 template <int W>
 __device__ __forceinline__ void pull_bf16(uint32_t src, float* v) {
 #pragma unroll
@@ -187,7 +193,29 @@ __device__ __forceinline__ void pull_bf16(uint32_t src, float* v) {
     }
 }
 
-template <int NC, int CW, typename Tout>
+// Sums v[0..15] (one value per lane per column) over the warp's 32 lanes by
+// halving exchanges; afterwards lane l holds the total of column
+// 8 b4 + 4 b3 + 2 b2 + b1 (b_i = bit i of l), which lanes l and l ^ 1 share.
+__device__ __forceinline__ float warp_colsum16(const float (&v)[16], int lane) {
+    float w8[8], w4[4], w2[2];
+    const bool h16 = lane & 16, h8 = lane & 8, h4 = lane & 4, h2 = lane & 2;
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        w8[i] = (h16 ? v[8 + i] : v[i]) + __shfl_xor_sync(0xffffffffu, h16 ? v[i] : v[8 + i], 16);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        w4[i] = (h8 ? w8[4 + i] : w8[i]) + __shfl_xor_sync(0xffffffffu, h8 ? w8[i] : w8[4 + i], 8);
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+        w2[i] = (h4 ? w4[2 + i] : w4[i]) + __shfl_xor_sync(0xffffffffu, h4 ? w4[i] : w4[2 + i], 4);
+    float w1 = (h2 ? w2[1] : w2[0]) + __shfl_xor_sync(0xffffffffu, h2 ? w2[0] : w2[1], 2);
+    return w1 + __shfl_xor_sync(0xffffffffu, w1, 1);
+}
+__device__ __forceinline__ int colsum16_column(int lane) {
+    return 8 * ((lane >> 4) & 1) + 4 * ((lane >> 3) & 1) + 2 * ((lane >> 2) & 1) + ((lane >> 1) & 1);
+}
+
+template <int NC, int CW, typename Tout, bool SURP>
 __global__ void __launch_bounds__(128 * (64 / CW), 1)
     tc_mlp_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, nm_args a, int c_mode) {
@@ -200,6 +228,12 @@ __global__ void __launch_bounds__(128 * (64 / CW), 1)
     __nv_bfloat16* Yx = reinterpret_cast<__nv_bfloat16*>(sm + OFF_YX);  // [64][XS]
     __nv_bfloat16* Yr = reinterpret_cast<__nv_bfloat16*>(sm + OFF_YR);  // [64][RB]
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + OFF_BAR);  // 0: tiles, 1: mma
+    // per-token surprise partial sums (written only when SURP)
+    float* sp_a2 = reinterpret_cast<float*>(sm + OFF_SP);  // [4 qd][64 t] ||a(k_t)||^2 over this CTA's hidden units
+    float* sp_d2 = sp_a2 + 4 * BC;                         // [4 qd][64 t] ||delta_t||^2, likewise
+    float* sp_e2 = sp_d2 + 4 * BC;                         // [4 hq][64 t] ||e_t||^2 over 16 columns each
+    float* sp_k2 = sp_e2 + 4 * BC;                         // [4][64 t]    ||k_t||^2 over 16 columns each
+    float* sp_peer = sp_k2 + 4 * BC;                       // [2][64 t]    the peer CTA's ||a||^2, ||delta||^2
     __shared__ uint32_t s_tmem;
 
     const int tid = threadIdx.x;
@@ -468,6 +502,12 @@ __global__ void __launch_bounds__(128 * (64 / CW), 1)
                 o1[q] = gm * kv[q];
                 o2[q] = uu * kv[q];
             }
+            if (SURP) {
+                float k2 = 0.0f;
+#pragma unroll
+                for (int q = 0; q < CW; ++q) k2 = fmaf(kv[q], kv[q], k2);
+                sp_k2[(tid >> 6) * BC + t] = k2;
+            }
             put_row<CW>(sm + OFF_KG, 64, t, c0, o1);
             put_row<CW>(sm + OFF_KU, 64, t, c0, o2);
         }
@@ -484,6 +524,13 @@ __global__ void __launch_bounds__(128 * (64 / CW), 1)
                 z[q] *= sg;
             }
             put_row<CW>(sm + OFF_AK, 128, jr, CW * hq, z);
+            if (SURP) {  // ||a(k_t)||^2 over this quadrant's 32 hidden units, for columns t of this thread
+                float sq[CW];
+#pragma unroll
+                for (int q = 0; q < CW; ++q) sq[q] = z[q] * z[q];
+                const float tot = warp_colsum16(sq, lane);
+                if (!(lane & 1)) sp_a2[qd * BC + CW * hq + colsum16_column(lane)] = tot;
+            }
             if (qd < 2) {
                 const float* gr = Gm + jr * GS + CW * hq;
 #pragma unroll
@@ -546,8 +593,16 @@ __global__ void __launch_bounds__(128 * (64 / CW), 1)
 #pragma unroll
                 for (int q = 0; q < CW; ++q) ev[q] = fmaf(2.0f, px[q], ev[q]);
             }
+            if (a.e_clip < HUGE_VALF) {  // the Huber loss clips e (uniform branch: free for the squared loss)
 #pragma unroll
-            for (int q = 0; q < CW; ++q) ev[q] = nm_clip_err(ev[q], a.e_clip);  // the Huber loss clips e
+                for (int q = 0; q < CW; ++q) ev[q] = nm_clip_err(ev[q], a.e_clip);
+            }
+            if (SURP) {
+                float e2 = 0.0f;
+#pragma unroll
+                for (int q = 0; q < CW; ++q) e2 = fmaf(ev[q], ev[q], e2);
+                sp_e2[hq * BC + tr] = e2;
+            }
             put_row<CW>(sm + OFF_E, 64, tr, CW * hq, ev);
             float o1[CW];
             const float gm = -sGl[tr], uu = sU[tr];
@@ -587,6 +642,13 @@ __global__ void __launch_bounds__(128 * (64 / CW), 1)
 #pragma unroll
             for (int q = 0; q < CW; ++q) xd[q] *= ds[q];
             put_row<CW>(sm + OFF_DT, 128, jr, CW * hq, xd);
+            if (SURP) {  // ||delta_t||^2 over this quadrant's 32 hidden units
+                float sq[CW];
+#pragma unroll
+                for (int q = 0; q < CW; ++q) sq[q] = xd[q] * xd[q];
+                const float tot = warp_colsum16(sq, lane);
+                if (!(lane & 1)) sp_d2[qd * BC + CW * hq + colsum16_column(lane)] = tot;
+            }
         }
         handoff();
         // ---- G4: state update and sum_i P1[t][i] delta_i
@@ -683,6 +745,13 @@ __global__ void __launch_bounds__(128 * (64 / CW), 1)
             // G5) become the next chunk's bf16 operands, or the result
             convert_state(2, c + 1 == nchunks);
             convert_state(3, c + 1 == nchunks);
+            if (SURP && NC > 1 && rank == 1 && tid < BC) {  // this CTA's ||a||^2, ||delta||^2 to rank 0
+                const int t = tid;
+                const float a2 = (sp_a2[t] + sp_a2[BC + t]) + (sp_a2[2 * BC + t] + sp_a2[3 * BC + t]);
+                const float d2 = (sp_d2[t] + sp_d2[BC + t]) + (sp_d2[2 * BC + t] + sp_d2[3 * BC + t]);
+                st_cluster_f32(map_to_rank(smem_u32(sp_peer + t), 0u), a2);
+                st_cluster_f32(map_to_rank(smem_u32(sp_peer + BC + t), 0u), d2);
+            }
             if (NC > 1) cluster_sync();
             if (r64 && own && tr < n) {
                 if (NC > 1) {
@@ -692,6 +761,19 @@ __global__ void __launch_bounds__(128 * (64 / CW), 1)
                     for (int q = 0; q < CW; ++q) yw[q] += pr[q];
                 }
                 store_y<CW>(y + (t0 + tr) * D + CW * hq, yw);
+            }
+            if (SURP && rank == 0 && tid < n) {
+                // surprise_t = sqrt(||delta_t||^2 ||k_t||^2 + ||e_t||^2 ||a(k_t)||^2) over all hidden units
+                const int t = tid;
+                float a2 = (sp_a2[t] + sp_a2[BC + t]) + (sp_a2[2 * BC + t] + sp_a2[3 * BC + t]);
+                float d2 = (sp_d2[t] + sp_d2[BC + t]) + (sp_d2[2 * BC + t] + sp_d2[3 * BC + t]);
+                if (NC > 1) {
+                    a2 += sp_peer[t];
+                    d2 += sp_peer[BC + t];
+                }
+                const float e2 = (sp_e2[t] + sp_e2[BC + t]) + (sp_e2[2 * BC + t] + sp_e2[3 * BC + t]);
+                const float k2 = (sp_k2[t] + sp_k2[BC + t]) + (sp_k2[2 * BC + t] + sp_k2[3 * BC + t]);
+                a.surprise[unit * T + t0 + t] = sqrtf(fmaf(d2, k2, e2 * a2));
             }
         }
         handoff();
@@ -707,14 +789,14 @@ __global__ void __launch_bounds__(128 * (64 / CW), 1)
     if (warp == 0) tmem_dealloc(tm, 512);
 }
 
-template <int NC, int CW, typename Tout>
+template <int NC, int CW, typename Tout, bool SURP>
 cudaError_t launch(const nm_config& c, const nm_args& a, cudaStream_t s) {
     CUtensorMap tq, tk, tv;
     const long long units = (long long)a.B * a.H;
     if (!make_token_map(&tq, a.q, D, a.T, units) || !make_token_map(&tk, a.k, D, a.T, units) ||
         !make_token_map(&tv, a.v, D, a.T, units))
         return cudaErrorInvalidValue;
-    auto kern = tc_mlp_kernel<NC, CW, Tout>;
+    auto kern = tc_mlp_kernel<NC, CW, Tout, SURP>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -736,8 +818,11 @@ cudaError_t launch(const nm_config& c, const nm_args& a, cudaStream_t s) {
 
 template <int NC>
 cudaError_t launch_nc(const nm_config& c, const nm_args& a, cudaStream_t s) {
-    return c.out_dtype == NM_BF16 ? launch<NC, CW_DEFAULT, __nv_bfloat16>(c, a, s)
-                                  : launch<NC, CW_DEFAULT, float>(c, a, s);
+    if (a.surprise)
+        return c.out_dtype == NM_BF16 ? launch<NC, CW_DEFAULT, __nv_bfloat16, true>(c, a, s)
+                                      : launch<NC, CW_DEFAULT, float, true>(c, a, s);
+    return c.out_dtype == NM_BF16 ? launch<NC, CW_DEFAULT, __nv_bfloat16, false>(c, a, s)
+                                  : launch<NC, CW_DEFAULT, float, false>(c, a, s);
 }
 
 }  // namespace

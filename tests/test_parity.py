@@ -417,16 +417,22 @@ def test_surprise_linear(path, wid, T, chunk, delta):
     _surprise_case(wl, x, path, M0, S0, delta)
 
 
-@pytest.mark.parametrize("hidden,d,T,delta", [(256, 64, 100, None), (128, 64, 70, 0.5)])
-def test_surprise_mlp_fp32_kernel(hidden, d, T, delta):
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("hidden,T,delta", [(256, 100, None), (256, 257, 0.5), (128, 70, 0.5), (128, 130, None)])
+def test_surprise_mlp(path, hidden, T, delta):
+    """fp32 FFMA kernel, and the tensor-core kernel with one CTA (hidden 128)
+    and a 2-CTA cluster (hidden 256, partial sums over the hidden units
+    crossing the cluster)."""
     wl = dataclasses.replace(W.WORKLOADS[1], hidden=hidden).with_sizes(B=1, H=2, T=T)
     x = W.make_inputs(wl, "cuda", seed=130 + T)
+    if T > 200:
+        x["eta"] *= 0.5
     M0, S0 = W.random_state(wl, "cuda", seed=131, scale=0.5)
-    _surprise_case(wl, x, nm.PATH_SIMT, M0, S0, delta)
+    _surprise_case(wl, x, path, M0, S0, delta)
 
 
-def test_surprise_unsupported_on_tensor_core_mlp():
-    wl = W.WORKLOADS[1].with_sizes(B=1, H=1, T=64)
+def test_surprise_unsupported_on_tensor_core_mlp_d128():
+    wl = W.WORKLOADS[3].with_sizes(B=1, H=1, T=64)
     x = W.make_inputs(wl, "cuda", seed=3)
     mem = nm.NeuralMemory(wl.kind, wl.d, wl.hidden, wl.chunk, in_dtype=wl.dtype, path=nm.PATH_TC)
     with pytest.raises(nm.NMError) as ei:
