@@ -35,8 +35,8 @@ METRIC = "memory-layer fwd tokens/sec (B*H*T/s) and % of roofline (TC FLOPs vs H
 # profiles/: workload -> (kernel sources, sha256 prefix of those sources when captured, bytes).
 # A capture describes the kernel it was taken on only: when the sources differ, traffic is null.
 NCU_TRAFFIC = {
-    "mlp_64x256_bf16_b4h8_t4096_c64": (("nm_tc_mlp.cu", "tc_common.cuh"), "028f9092d6e01339", 62.49e6),
-    "linear_d128_bf16_b8h16_t16384_c64": (("nm_tc_linear.cu", "tc_common.cuh"), "bd1e1accbb15e2c3", 2.121e9),
+    "mlp_64x256_bf16_b4h8_t4096_c64": (("nm_tc_mlp.cu", "tc_common.cuh"), "0c82da9d022d3f89", 62.415e6),
+    "linear_d128_bf16_b8h16_t16384_c64": (("nm_tc_linear.cu", "tc_common.cuh"), "4cddf53d9c0366eb", 2.114e9),
 }
 
 
