@@ -146,9 +146,8 @@ int nm_forward(nm_handle_t h, int B, int H, int T,
  *   (and delta) as the update, before any rounding to bf16.
  *   Everything else is nm_forward's contract; `surprise` must not overlap any
  *   other buffer (NM_ERR_ALIAS) and must not be NULL (NM_ERR_ARG).
- *   Returns NM_ERR_UNSUPPORTED when the handle's kernel does not write it
- *   (the tensor-core MLP2 kernel for d = 128; the fp32 FFMA kernels, the
- *   tensor-core linear kernels and the tensor-core MLP2 kernel for d = 64 do).
+ *   Every kernel family writes it (the tensor-core kernels through a variant
+ *   compiled for it, launched only when `surprise` is set).
  */
 int nm_forward_surprise(nm_handle_t h, int B, int H, int T,
                         const void* q, const void* k, const void* v,

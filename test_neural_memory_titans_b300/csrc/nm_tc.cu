@@ -17,7 +17,8 @@ bool nm_tc_supports(const nm_config& c) {
 
 // Kernels that can also write the per-token surprise (gradient norm).
 bool nm_tc_supports_surprise(const nm_config& c) {
-    return nm_tc_linear_supports(c) || nm_tc_linear64_supports(c) || nm_tc_mlp_supports(c);
+    return nm_tc_linear_supports(c) || nm_tc_linear64_supports(c) || nm_tc_mlp_supports(c) ||
+           nm_tc_mlp_wide_supports(c);
 }
 
 size_t nm_tc_scratch_bytes(const nm_config& c, int B, int H) {

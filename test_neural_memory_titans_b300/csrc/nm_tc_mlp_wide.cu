@@ -70,7 +70,9 @@ struct Layout {
     static constexpr uint32_t V = GM + 64 * GST * 2;              // bf16 [64 t][OR] this CTA's columns of v
     static constexpr uint32_t RX = V + 64 * OR * 2;               // bf16 [NC-1][OR][RBS] partials from the peers
     static constexpr uint32_t F = RX + (NC - 1) * OR * RBS * 2;   // gates [4][64], A, B, sigma, gamma, u
-    static constexpr uint32_t BAR = F + 4 * (4 * BC + 5 * BC);
+    static constexpr uint32_t SP = F + 4 * (4 * BC + 5 * BC);  // surprise: fp32 [4][64] this CTA's ||a||^2,
+                                                             // ||delta||^2, ||e||^2, ||k||^2; [2][3][64] cluster sums
+    static constexpr uint32_t BAR = SP + 4 * (10 * BC);
     static constexpr uint32_t USED = BAR + 64;
     static constexpr uint32_t BYTES = USED + 1024;  // slack for the 1024-byte alignment
     static_assert(BYTES <= 232448, "shared memory budget");
@@ -136,7 +138,11 @@ __device__ __forceinline__ void get_plain32(uint32_t addr, float* v) {
     }
 }
 
-template <int NC, typename Tout>
+__device__ __forceinline__ void red_cluster_add_f32(uint32_t addr, float v) {
+    asm volatile("red.shared::cluster.add.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+
+template <int NC, typename Tout, bool SURP>
 __global__ void __launch_bounds__(NTHREADS, 1)
     tc_mlpw_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                    const __grid_constant__ CUtensorMap tv, nm_args a, int c_mode) {
@@ -153,6 +159,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     __nv_bfloat16* Gm = reinterpret_cast<__nv_bfloat16*>(sm + L::GM);
     __nv_bfloat16* RX = reinterpret_cast<__nv_bfloat16*>(sm + L::RX);
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::BAR);  // 0: q|k tiles, 1: mma, 2: v slice
+    // per-token surprise sums (used only when SURP): this CTA's partials over its hidden units / owned
+    // output rows, and on rank 0 their cluster-wide sums for chunks of even / odd index
+    float* sp_loc = reinterpret_cast<float*>(sm + L::SP);  // [a2 | d2 | e2 | k2][64]
+    float* sp_acc = sp_loc + 4 * BC;                        // [2][a2 | d2 | e2][64]
     __shared__ uint32_t s_tmem;
 
     const int tid = threadIdx.x;
@@ -244,6 +254,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             put_row32(sm + (which ? L::S2 : L::W2), 128, lr, 32 * hf, r);
         }
     }
+    if (SURP)
+        for (int i = tid; i < 10 * BC; i += NTHREADS) sp_loc[i] = 0.0f;
     fence_proxy_async();
     tc_fence_before();
     cluster_sync();
@@ -429,6 +441,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     ds[q] = fmaf(v[q] * sg, 1.0f - sg, sg);  // silu'(z) = s + z s (1 - s)
                     v[q] *= sg;
                 }
+                if (SURP) {
+                    float a2 = 0.0f;
+#pragma unroll
+                    for (int q = 0; q < 32; ++q) a2 = fmaf(v[q], v[q], a2);
+                    atomicAdd(&sp_loc[t], a2);
+                }
                 put_row32(sm + L::AK, 64, t, 32 * hf, v);
 #pragma unroll
                 for (int q = 0; q < 32; ++q) o1[q] = gm * v[q];
@@ -488,6 +506,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     for (int k = 0; k < 4; ++k) {
                         const int t = 4 * c4 + k;
                         e[k] = t < n ? nm_clip_err(2.0f * (sv[k] - __bfloat162float(vs[t * OR + row])), a.e_clip) : 0.0f;
+                        if (SURP) atomicAdd(&sp_loc[2 * BC + t], e[k] * e[k]);
                     }
                     const uint32_t w0 = pack_bf16(e[0], e[1]), w1 = pack_bf16(e[2], e[3]);
                     const uint32_t off = sw128_offset(own_lo + row, 4 * c4, 128);
@@ -521,6 +540,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             const float gm = -sGl[t], uu = sU[t];
 #pragma unroll
             for (int q = 0; q < 32; ++q) x[q] *= ds[q];
+            if (SURP) {
+                float d2 = 0.0f;
+#pragma unroll
+                for (int q = 0; q < 32; ++q) d2 = fmaf(x[q], x[q], d2);
+                atomicAdd(&sp_loc[BC + t], d2);
+            }
             put_row32(sm + L::DT, 64, t, 32 * hf, x);
 #pragma unroll
             for (int q = 0; q < 32; ++q) o1[q] = gm * x[q];
@@ -528,8 +553,29 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
             for (int q = 0; q < 32; ++q) o1[q] = uu * x[q];
             put_row32(sm + L::DU, 64, t, 32 * hf, o1);
+        } else if (SURP) {  // ||k_t||^2: row t of the q|k tile's k half, 64 features per thread
+            const int t = lr - 64;
+            const uint32_t base = smem_u32(sm + L::KQ);
+            float k2 = 0.0f;
+#pragma unroll
+            for (int q8 = 0; q8 < 8; ++q8) {
+                const uint4 w = ld_shared_v4(base + sw128_offset(t, 64 * hf + 8 * q8, 128));
+                const float f[8] = {bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y),
+                                    bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w)};
+#pragma unroll
+                for (int i = 0; i < 8; ++i) k2 = fmaf(f[i], f[i], k2);
+            }
+            atomicAdd(&sp_loc[3 * BC + t], k2);
         }
         handoff();
+        if (SURP && tid < BC) {  // this CTA's partials onto rank 0's cluster sums for this chunk
+            float* acc = sp_acc + (c & 1) * 3 * BC;
+#pragma unroll
+            for (int m = 0; m < 3; ++m) {
+                red_cluster_add_f32(map_to_rank(smem_u32(acc + m * BC + tid), 0u), sp_loc[m * BC + tid]);
+                sp_loc[m * BC + tid] = 0.0f;
+            }
+        }
         // ---- G4: [DU; P1] delta -> rows 64..127 sum_i P1[t][i] delta_i; state updates
         //      W1^T += K^T (-gamma delta), S1^T += K^T (u delta), W2 += E^T (-gamma a(k)), S2 += E^T (u a(k))
         const bool go4 = !failed;
@@ -636,6 +682,19 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 }
             }
             cluster_sync();  // barrier C
+            if (SURP && tid < BC) {
+                // surprise_t = sqrt(||delta_t||^2 ||k_t||^2 + ||e_t||^2 ||a(k_t)||^2), sums over the cluster
+                float* acc = sp_acc + (c & 1) * 3 * BC;
+                if (rank == 0) {
+                    if (tid < n)
+                        a.surprise[unit * T + t0 + tid] =
+                            sqrtf(fmaf(acc[BC + tid], sp_loc[3 * BC + tid], acc[2 * BC + tid] * acc[tid]));
+                    acc[tid] = 0.0f;
+                    acc[BC + tid] = 0.0f;
+                    acc[2 * BC + tid] = 0.0f;
+                }
+                sp_loc[3 * BC + tid] = 0.0f;
+            }
             // every thread: 4 tokens of an owned row of y
             for (int task = tid; task < TASKS; task += NTHREADS) {
                 const int row = task % OR, c4 = task / OR;  // consecutive threads: consecutive rows
@@ -681,7 +740,7 @@ bool make_plain_map(CUtensorMap* m, const void* base, int d, long long T, long l
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int NC, typename Tout>
+template <int NC, typename Tout, bool SURP>
 cudaError_t launch(const nm_config& c, const nm_args& a, cudaStream_t s) {
     using L = Layout<NC>;
     CUtensorMap tq, tk, tv;
@@ -689,7 +748,7 @@ cudaError_t launch(const nm_config& c, const nm_args& a, cudaStream_t s) {
     if (!make_token_map(&tq, a.q, D, a.T, units) || !make_token_map(&tk, a.k, D, a.T, units) ||
         !make_plain_map(&tv, a.v, D, a.T, units, L::OR))
         return cudaErrorInvalidValue;
-    auto kern = tc_mlpw_kernel<NC, Tout>;
+    auto kern = tc_mlpw_kernel<NC, Tout, SURP>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::BYTES);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -711,7 +770,9 @@ cudaError_t launch(const nm_config& c, const nm_args& a, cudaStream_t s) {
 
 template <int NC>
 cudaError_t launch_nc(const nm_config& c, const nm_args& a, cudaStream_t s) {
-    return c.out_dtype == NM_BF16 ? launch<NC, __nv_bfloat16>(c, a, s) : launch<NC, float>(c, a, s);
+    if (a.surprise)
+        return c.out_dtype == NM_BF16 ? launch<NC, __nv_bfloat16, true>(c, a, s) : launch<NC, float, true>(c, a, s);
+    return c.out_dtype == NM_BF16 ? launch<NC, __nv_bfloat16, false>(c, a, s) : launch<NC, float, false>(c, a, s);
 }
 
 }  // namespace

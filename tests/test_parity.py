@@ -431,11 +431,13 @@ def test_surprise_mlp(path, hidden, T, delta):
     _surprise_case(wl, x, path, M0, S0, delta)
 
 
-def test_surprise_unsupported_on_tensor_core_mlp_d128():
-    wl = W.WORKLOADS[3].with_sizes(B=1, H=1, T=64)
-    x = W.make_inputs(wl, "cuda", seed=3)
-    mem = nm.NeuralMemory(wl.kind, wl.d, wl.hidden, wl.chunk, in_dtype=wl.dtype, path=nm.PATH_TC)
-    with pytest.raises(nm.NMError) as ei:
-        mem.forward_surprise(x["q"], x["k"], x["v"], x["alpha"], x["eta"], x["beta"], x["M0"], x["S0"])
-    assert ei.value.status == nm.NM_ERR_UNSUPPORTED
-    mem.close()
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("hidden,T,delta", [(512, 100, None), (256, 130, 0.05), (128, 64, None)])
+def test_surprise_mlp_d128(path, hidden, T, delta):
+    """The d = 128 kernel sums each token's partials over 2 to 8 CTAs of its
+    cluster (hidden 128 / 256 / 512) onto the first CTA."""
+    wl = dataclasses.replace(W.WORKLOADS[3], hidden=hidden).with_sizes(B=1, H=2, T=T)
+    _skip_unsupported(wl, path)
+    x = W.make_inputs(wl, "cuda", seed=140 + T + hidden)
+    M0, S0 = W.random_state(wl, "cuda", seed=141, scale=0.5)
+    _surprise_case(wl, x, path, M0, S0, delta)
