@@ -326,6 +326,38 @@ def run_ours(args, rank, world, local_rank):
     tokens = alg["tokens"]
     value = world * tokens / (ms * 1e-3)
 
+    # the same workload through the two optional forms of the method (Huber loss; surprise output),
+    # single-call workloads only, a few steps each, same L2 flush and event timing
+    variants = None
+    if seg == wl.T and not args.no_variants:
+        def time_calls(fn, n_steps):
+            for _ in range(2):
+                fn()
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_steps)]
+            for a_, b_ in ev:
+                flush.zero_()
+                a_.record(stream)
+                fn()
+                b_.record(stream)
+            torch.cuda.synchronize(dev)
+            return sum(a_.elapsed_time(b_) for a_, b_ in ev) / n_steps
+
+        n_var = max(3, min(args.steps, 30))
+        args8 = (x["q"], x["k"], x["v"], x["alpha"], x["eta"], x["beta"], x["M0"], x["S0"])
+        sur = torch.empty(x["alpha"].shape, dtype=torch.float32, device=dev)
+        mem_h = nm.NeuralMemory(wl.kind, wl.d, wl.hidden, wl.chunk, in_dtype=wl.dtype, path=args.path,
+                                device=local_rank, loss=nm.LOSS_HUBER, huber_delta=0.1)
+        v_h = time_calls(lambda: mem_h.forward(*args8, y=y, M_T=M, S_T=S, stream=stream), n_var)
+        v_s = time_calls(lambda: mem.forward_surprise(*args8, y=y, M_T=M, S_T=S, surprise=sur, stream=stream), n_var)
+        for m_ in (mem, mem_h):
+            st = m_.synchronize()
+            if st != nm.NM_OK:
+                raise RuntimeError("device status after the variants: %s" % nm.status_string(st))
+        mem_h.close()
+        variants = {"huber_loss": {"ms_per_step": v_h, "value": world * tokens / (v_h * 1e-3), "delta": 0.1},
+                    "surprise_output": {"ms_per_step": v_s, "value": world * tokens / (v_s * 1e-3)},
+                    "steps": n_var, "note": "nm_config.loss = NM_LOSS_HUBER; nm_forward_surprise"}
+
     # e2e through the host-buffer entry point (pinned), copies inside the timed region
     e2e = None
     if not args.no_e2e and seg == wl.T:
@@ -409,7 +441,8 @@ def run_ours(args, rank, world, local_rank):
                       "parallelism": "dp%d" % world,
                       "l2": "flushed between timed steps (256 MB write, outside the step's events)"},
            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
-           "clocks": clocks.summary(), "step_ms": {"min": min(step_ms), "max": max(step_ms)}}
+           "clocks": clocks.summary(), "step_ms": {"min": min(step_ms), "max": max(step_ms)},
+           "variants": variants}
     return out
 
 
@@ -452,6 +485,7 @@ def main():
                     help="DRAM bytes per launch of the dominant kernel from an ncu capture")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-variants", action="store_true", help="skip timing the Huber-loss and surprise forms")
     ap.add_argument("--cpu-budget", type=float, default=None,
                     help="seconds of oracle work per step of the reference arm (default: about 150 s in all)")
     ap.add_argument("--B", type=int, default=None, help="override the workload's batch (small profiling cases)")
