@@ -57,15 +57,15 @@ def _load():
         dp = ctypes.POINTER(ctypes.c_double)
         i = ctypes.c_int
         dd = ctypes.c_double
-        lib.oracle_forward.argtypes = [i, i, i, i, i, i, dd, i, i, i] + [dp] * 13
+        lib.oracle_forward.argtypes = [i, i, i, i, i, i, i, dd, i, i, i] + [dp] * 13
         lib.oracle_forward.restype = i
-        lib.oracle_grad.argtypes = [i, i, i, i, dd, dp, dp, dp, dp, dp]
+        lib.oracle_grad.argtypes = [i, i, i, i, i, dd, dp, dp, dp, dp, dp]
         lib.oracle_grad.restype = None
-        lib.oracle_loss.argtypes = [i, i, i, i, dd, dp, dp, dp, dp]
+        lib.oracle_loss.argtypes = [i, i, i, i, i, dd, dp, dp, dp, dp]
         lib.oracle_loss.restype = ctypes.c_double
-        lib.oracle_memory_apply.argtypes = [i, i, i, dp, dp, dp, dp]
+        lib.oracle_memory_apply.argtypes = [i, i, i, i, dp, dp, dp, dp]
         lib.oracle_memory_apply.restype = None
-        lib.oracle_param_count.argtypes = [i, i, i]
+        lib.oracle_param_count.argtypes = [i, i, i, i]
         lib.oracle_param_count.restype = ctypes.c_long
         _lib = lib
     return _lib
@@ -79,41 +79,43 @@ def _ptr(a: np.ndarray):
     return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
 
 
-def param_count(kind: int, d: int, hidden: int = 0) -> int:
-    return int(_load().oracle_param_count(kind, d, hidden))
+def param_count(kind: int, d: int, hidden: int = 0, layers: int = 2) -> int:
+    return int(_load().oracle_param_count(kind, d, hidden, layers))
 
 
-def memory_apply(kind: int, d: int, hidden: int, W, x) -> np.ndarray:
-    """y = M_W(x) for one memory (linear: M x; MLP2: W2 silu(W1 x))."""
+def memory_apply(kind: int, d: int, hidden: int, W, x, layers: int = 2) -> np.ndarray:
+    """y = M_W(x) for one memory (linear: M x; MLP2: W_L silu(... silu(W1 x)), L = layers)."""
     W, x = _f64(W), _f64(x)
     y = np.zeros(d)
-    work = np.zeros(max(hidden, 1) + 8)
-    _load().oracle_memory_apply(kind, d, hidden, _ptr(W), _ptr(x), _ptr(y), _ptr(work))
+    work = np.zeros(2 * max(hidden, 1) + 8)
+    _load().oracle_memory_apply(kind, d, hidden, layers, _ptr(W), _ptr(x), _ptr(y), _ptr(work))
     return y
 
 
-def loss(kind: int, d: int, hidden: int, W, k, v, loss_kind: int = LOSS_L2, huber_delta: float = np.inf) -> float:
+def loss(kind: int, d: int, hidden: int, W, k, v, loss_kind: int = LOSS_L2, huber_delta: float = np.inf,
+         layers: int = 2) -> float:
     """||M_W(k) - v||^2, or the element-wise Huber sum (rho(r) = r^2 inside delta,
     2 delta |r| - delta^2 beyond)."""
     W, k, v = _f64(W), _f64(k), _f64(v)
-    work = np.zeros(d + max(hidden, 1) + 8)
-    return float(_load().oracle_loss(kind, d, hidden, loss_kind, float(huber_delta), _ptr(W), _ptr(k), _ptr(v),
-                                     _ptr(work)))
+    work = np.zeros(d + 2 * max(hidden, 1) + 8)
+    return float(_load().oracle_loss(kind, d, hidden, layers, loss_kind, float(huber_delta), _ptr(W), _ptr(k),
+                                     _ptr(v), _ptr(work)))
 
 
-def grad(kind: int, d: int, hidden: int, W, k, v, loss_kind: int = LOSS_L2, huber_delta: float = np.inf) -> np.ndarray:
+def grad(kind: int, d: int, hidden: int, W, k, v, loss_kind: int = LOSS_L2, huber_delta: float = np.inf,
+         layers: int = 2) -> np.ndarray:
     """grad_W of the loss above by explicit backprop."""
     W, k, v = _f64(W), _f64(k), _f64(v)
-    g = np.zeros(param_count(kind, d, hidden))
-    work = np.zeros(3 * max(hidden, 1) + 2 * d + 8)
-    _load().oracle_grad(kind, d, hidden, loss_kind, float(huber_delta), _ptr(W), _ptr(k), _ptr(v), _ptr(g),
+    g = np.zeros(param_count(kind, d, hidden, layers))
+    work = np.zeros((2 * layers + 2) * max(hidden, 1) + 2 * d + 8)
+    _load().oracle_grad(kind, d, hidden, layers, loss_kind, float(huber_delta), _ptr(W), _ptr(k), _ptr(v), _ptr(g),
                         _ptr(work))
     return g
 
 
 def forward(kind: int, d: int, hidden: int, chunk: int, c_mode: int,
             q, k, v, alpha, eta, beta, c, M0, S0, loss_kind: int = LOSS_L2, huber_delta: float = np.inf,
-            surprise: bool = False):
+            surprise: bool = False, layers: int = 2):
     """The chunked forward on [B, H, T, d] inputs and [B, H, T] gates.
 
     Returns (y [B,H,T,d], M_T [B,H,P], S_T [B,H,P]) as float64 arrays, and with
@@ -124,7 +126,7 @@ def forward(kind: int, d: int, hidden: int, chunk: int, c_mode: int,
     assert dd == d and k.shape == q.shape and v.shape == q.shape
     alpha, eta, beta = _f64(alpha), _f64(eta), _f64(beta)
     assert alpha.shape == (B, H, T) and eta.shape == (B, H, T) and beta.shape == (B, H, T)
-    P = param_count(kind, d, hidden)
+    P = param_count(kind, d, hidden, layers)
     M0 = _f64(M0).reshape(B, H, P)
     S0 = _f64(S0).reshape(B, H, P)
     if c_mode == C_PER_TOKEN:
@@ -138,7 +140,7 @@ def forward(kind: int, d: int, hidden: int, chunk: int, c_mode: int,
     MT = np.zeros((B, H, P))
     ST = np.zeros((B, H, P))
     sp = np.zeros((B, H, T)) if surprise else None
-    rc = _load().oracle_forward(kind, d, hidden, chunk, c_mode, loss_kind, float(huber_delta), B, H, T,
+    rc = _load().oracle_forward(kind, d, hidden, layers, chunk, c_mode, loss_kind, float(huber_delta), B, H, T,
                                 _ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(eta), _ptr(beta),
                                 cp, _ptr(M0), _ptr(S0), _ptr(y), _ptr(MT), _ptr(ST),
                                 _ptr(sp) if surprise else None)

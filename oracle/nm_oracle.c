@@ -46,6 +46,11 @@
  *   MLP2  : M(x) = W2 silu(W1 x), W1 in R^{h x d}, W2 in R^{d x h}, no bias;
  *           parameters packed as W1 (row-major h x d) followed by W2
  *           (row-major d x h).
+ *           With `layers` = L > 2 (deeper memories, [JA] "ニューラル長期メモリモジュール":
+ *           the memory is an MLP of L_M >= 1 layers; [IT] reports that depth
+ *           helps): M(x) = W_L silu(W_{L-1} ... silu(W1 x)), W1 h x d,
+ *           W2 .. W_{L-1} h x h, W_L d x h, packed in that order; silu after
+ *           every layer but the last.
  *
  * Readings where the pages are silent or disagree:
  *   - the squared norm has no 1/2, so grad = 2 (M(k) - v) ... (kept);
@@ -99,15 +104,15 @@ static double or_dsilu(double z) {
     return s * (1.0 + z * (1.0 - s));
 }
 
-/* Number of parameters of one memory. */
-long oracle_param_count(int kind, int d, int h) {
+/* Number of parameters of one memory (layers: MLP depth, >= 2; ignored for LINEAR). */
+long oracle_param_count(int kind, int d, int h, int layers) {
     if (kind == OR_LINEAR) return (long)d * d;
-    if (kind == OR_MLP2) return 2L * h * d;
+    if (kind == OR_MLP2 && layers >= 2) return 2L * h * d + (long)(layers - 2) * h * h;
     return -1;
 }
 
-/* y = M_W(x).  work must hold h doubles for MLP2. */
-void oracle_memory_apply(int kind, int d, int h, const double* W,
+/* y = M_W(x).  work must hold 2h doubles for MLP2. */
+void oracle_memory_apply(int kind, int d, int h, int layers, const double* W,
                          const double* x, double* y, double* work) {
     if (kind == OR_LINEAR) {
         for (int o = 0; o < d; ++o) {
@@ -117,16 +122,27 @@ void oracle_memory_apply(int kind, int d, int h, const double* W,
         }
         return;
     }
-    const double* W1 = W;                 /* h x d */
-    const double* W2 = W + (long)h * d;   /* d x h */
+    double* cur = work;       /* h: activation of the current layer */
+    double* nxt = work + h;   /* h */
+    const double* W1 = W;     /* h x d */
     for (int j = 0; j < h; ++j) {
         double z = 0.0;
         for (int i = 0; i < d; ++i) z += W1[(long)j * d + i] * x[i];
-        work[j] = or_silu(z);
+        cur[j] = or_silu(z);
     }
-    for (int o = 0; o < d; ++o) {
+    const double* Wl = W + (long)h * d;
+    for (int l = 2; l < layers; ++l) {   /* hidden-to-hidden layers, h x h */
+        for (int j = 0; j < h; ++j) {
+            double z = 0.0;
+            for (int i = 0; i < h; ++i) z += Wl[(long)j * h + i] * cur[i];
+            nxt[j] = or_silu(z);
+        }
+        double* t = cur; cur = nxt; nxt = t;
+        Wl += (long)h * h;
+    }
+    for (int o = 0; o < d; ++o) {        /* last layer W_L, d x h, no activation */
         double acc = 0.0;
-        for (int j = 0; j < h; ++j) acc += W2[(long)o * h + j] * work[j];
+        for (int j = 0; j < h; ++j) acc += Wl[(long)o * h + j] * cur[j];
         y[o] = acc;
     }
 }
@@ -134,10 +150,10 @@ void oracle_memory_apply(int kind, int d, int h, const double* W,
 /* The associative loss l(W; k, v) = ||M_W(k) - v||_2^2 ([IT] "Funzione
  * Obiettivo"), or with loss = OR_LOSS_HUBER the sum of rho(r_o) above.
  * work: d + h doubles. */
-double oracle_loss(int kind, int d, int h, int loss, double delta, const double* W,
-                   const double* k, const double* v, double* work) {
+double oracle_loss(int kind, int d, int h, int layers, int loss, double delta,
+                   const double* W, const double* k, const double* v, double* work) {
     double* yhat = work;
-    oracle_memory_apply(kind, d, h, W, k, yhat, work + d);
+    oracle_memory_apply(kind, d, h, layers, W, k, yhat, work + d);
     double acc = 0.0;
     for (int o = 0; o < d; ++o) {
         double r = yhat[o] - v[o];
@@ -150,9 +166,10 @@ double oracle_loss(int kind, int d, int h, int loss, double delta, const double*
 }
 
 /* g = grad_W l(W; k, v), by an explicit forward and backward pass.
- * work: 3h + 2d doubles. */
-void oracle_grad(int kind, int d, int h, int loss, double delta, const double* W,
-                 const double* k, const double* v, double* g, double* work) {
+ * work: (2 layers + 2) h + 2d doubles. */
+void oracle_grad(int kind, int d, int h, int layers, int loss, double delta,
+                 const double* W, const double* k, const double* v, double* g,
+                 double* work) {
     if (kind == OR_LINEAR) {
         /* l = sum_o rho((M k - v)[o]),  rho(r) = r^2 for the squared loss
          * dl/dM[o][i] = rho'((M k - v)[o]) k[i]                              */
@@ -166,61 +183,86 @@ void oracle_grad(int kind, int d, int h, int loss, double delta, const double* W
             for (int i = 0; i < d; ++i) g[(long)o * d + i] = e[o] * k[i];
         return;
     }
-    const double* W1 = W;
-    const double* W2 = W + (long)h * d;
-    double* gW1 = g;
-    double* gW2 = g + (long)h * d;
-    double* z = work;          /* h */
-    double* a = work + h;      /* h */
-    double* da = work + 2 * h; /* h */
-    double* e = work + 3 * h;  /* d */
-    /* forward: z = W1 k, a = silu(z), yhat = W2 a */
-    for (int j = 0; j < h; ++j) {
-        double acc = 0.0;
-        for (int i = 0; i < d; ++i) acc += W1[(long)j * d + i] * k[i];
-        z[j] = acc;
-        a[j] = or_silu(acc);
+    const int L = layers;
+    /* per hidden layer l = 1 .. L-1: pre-activation z_l and activation a_l (h each) */
+    double* z = work;                         /* (L-1) x h */
+    double* a = work + (long)(L - 1) * h;     /* (L-1) x h */
+    double* da = work + 2L * (L - 1) * h;     /* h: dl/da of the current layer */
+    double* dz = da + h;                      /* h: dl/dz of the current layer */
+    double* e = dz + h;                       /* d */
+    /* offsets of each layer's weights in W (and of its gradient in g) */
+    long off[64];
+    off[1] = 0;
+    off[2] = (long)h * d;
+    for (int l = 3; l <= L; ++l) off[l] = off[l - 1] + (long)h * h;
+    /* forward: z_1 = W1 k, a_l = silu(z_l), z_l = W_l a_{l-1}, yhat = W_L a_{L-1} */
+    for (int l = 1; l < L; ++l) {
+        const double* Wl = W + off[l];
+        const int in = l == 1 ? d : h;
+        const double* x = l == 1 ? k : a + (long)(l - 2) * h;
+        for (int j = 0; j < h; ++j) {
+            double acc = 0.0;
+            for (int i = 0; i < in; ++i) acc += Wl[(long)j * in + i] * x[i];
+            z[(long)(l - 1) * h + j] = acc;
+            a[(long)(l - 1) * h + j] = or_silu(acc);
+        }
     }
+    const double* WL = W + off[L];
+    const double* aL = a + (long)(L - 2) * h;
     /* dl/dyhat = rho'(yhat - v): 2 (yhat - v) for the squared loss */
     for (int o = 0; o < d; ++o) {
         double acc = 0.0;
-        for (int j = 0; j < h; ++j) acc += W2[(long)o * h + j] * a[j];
+        for (int j = 0; j < h; ++j) acc += WL[(long)o * h + j] * aL[j];
         e[o] = or_dloss(loss, delta, acc - v[o]);
     }
-    /* dl/dW2[o][j] = e[o] a[j] */
+    /* dl/dW_L[o][j] = e[o] a_{L-1}[j] */
     for (int o = 0; o < d; ++o)
-        for (int j = 0; j < h; ++j) gW2[(long)o * h + j] = e[o] * a[j];
-    /* dl/da[j] = sum_o W2[o][j] e[o];  dl/dz[j] = dl/da[j] silu'(z[j]) */
+        for (int j = 0; j < h; ++j) g[off[L] + (long)o * h + j] = e[o] * aL[j];
+    /* dl/da_{L-1}[j] = sum_o W_L[o][j] e[o] */
     for (int j = 0; j < h; ++j) {
         double acc = 0.0;
-        for (int o = 0; o < d; ++o) acc += W2[(long)o * h + j] * e[o];
-        da[j] = acc * or_dsilu(z[j]);
+        for (int o = 0; o < d; ++o) acc += WL[(long)o * h + j] * e[o];
+        da[j] = acc;
     }
-    /* dl/dW1[j][i] = dl/dz[j] k[i] */
-    for (int j = 0; j < h; ++j)
-        for (int i = 0; i < d; ++i) gW1[(long)j * d + i] = da[j] * k[i];
+    /* down the hidden layers: dl/dz_l = dl/da_l silu'(z_l); dl/dW_l = dl/dz_l x_{l-1}^T;
+     * dl/da_{l-1} = W_l^T dl/dz_l */
+    for (int l = L - 1; l >= 1; --l) {
+        for (int j = 0; j < h; ++j) dz[j] = da[j] * or_dsilu(z[(long)(l - 1) * h + j]);
+        const int in = l == 1 ? d : h;
+        const double* x = l == 1 ? k : a + (long)(l - 2) * h;
+        for (int j = 0; j < h; ++j)
+            for (int i = 0; i < in; ++i) g[off[l] + (long)j * in + i] = dz[j] * x[i];
+        if (l > 1) {
+            const double* Wl = W + off[l];
+            for (int i = 0; i < h; ++i) {
+                double acc = 0.0;
+                for (int j = 0; j < h; ++j) acc += Wl[(long)j * h + i] * dz[j];
+                da[i] = acc;
+            }
+        }
+    }
 }
 
 /* One (batch, head) unit.  Pointers are already offset to the unit. */
-static void oracle_unit(int kind, int d, int h, int chunk, int c_mode, int loss,
+static void oracle_unit(int kind, int d, int h, int layers, int chunk, int c_mode, int loss,
                         double delta, int T, const double* q, const double* k,
                         const double* v, const double* alpha, const double* eta,
                         const double* beta, const double* c, const double* M0,
                         const double* S0, double* y, double* MT, double* ST,
                         double* surprise) {
-    long P = oracle_param_count(kind, d, h);
+    long P = oracle_param_count(kind, d, h, layers);
     double* M = (double*)malloc(sizeof(double) * P);
     double* S = (double*)malloc(sizeof(double) * P);
     double* W0 = (double*)malloc(sizeof(double) * P);
     double* g = (double*)malloc(sizeof(double) * P);
-    double* work = (double*)malloc(sizeof(double) * (3 * (long)h + 2 * (long)d + 8));
+    double* work = (double*)malloc(sizeof(double) * ((2 * (long)layers + 2) * h + 2 * (long)d + 8));
     memcpy(M, M0, sizeof(double) * P);
     memcpy(S, S0, sizeof(double) * P);
     for (int t0 = 0; t0 < T; t0 += chunk) {
         int t1 = t0 + chunk < T ? t0 + chunk : T;
         memcpy(W0, M, sizeof(double) * P); /* chunk-start weights */
         for (int t = t0; t < t1; ++t) {
-            oracle_grad(kind, d, h, loss, delta, W0, k + (long)t * d, v + (long)t * d, g, work);
+            oracle_grad(kind, d, h, layers, loss, delta, W0, k + (long)t * d, v + (long)t * d, g, work);
             if (surprise) {
                 double n2 = 0.0;
                 for (long p = 0; p < P; ++p) n2 += g[p] * g[p];
@@ -231,7 +273,7 @@ static void oracle_unit(int kind, int d, int h, int chunk, int c_mode, int loss,
             else if (c_mode == OR_C_PER_TOKEN) ct = c[t];
             for (long p = 0; p < P; ++p) S[p] = beta[t] * S[p] + ct * g[p];
             for (long p = 0; p < P; ++p) M[p] = (1.0 - alpha[t]) * M[p] - eta[t] * S[p];
-            oracle_memory_apply(kind, d, h, M, q + (long)t * d, y + (long)t * d, work);
+            oracle_memory_apply(kind, d, h, layers, M, q + (long)t * d, y + (long)t * d, work);
         }
     }
     memcpy(MT, M, sizeof(double) * P);
@@ -244,11 +286,12 @@ static void oracle_unit(int kind, int d, int h, int chunk, int c_mode, int loss,
  *   q, k, v, y : [B, H, T, d]      alpha, eta, beta, c, surprise : [B, H, T]
  *   M0, S0, MT, ST : [B, H, P]     (c may be NULL unless c_mode == PER_TOKEN;
  *                                   surprise may be NULL)
+ *   layers: MLP depth L >= 2 (ignored for LINEAR).
  *   loss: OR_LOSS_L2 or OR_LOSS_HUBER with threshold delta > 0.
  * Returns 0, or -1 on a bad argument.  Units run in parallel with OpenMP;
  * each unit's arithmetic is sequential and identical to a one-thread run.
  */
-int oracle_forward(int kind, int d, int h, int chunk, int c_mode, int loss,
+int oracle_forward(int kind, int d, int h, int layers, int chunk, int c_mode, int loss,
                    double delta, int B, int H, int T, const double* q,
                    const double* k, const double* v, const double* alpha,
                    const double* eta, const double* beta, const double* c,
@@ -258,13 +301,13 @@ int oracle_forward(int kind, int d, int h, int chunk, int c_mode, int loss,
         B < 0 || H < 0 || T < 0)
         return -1;
     if (loss != OR_LOSS_L2 && !(loss == OR_LOSS_HUBER && delta > 0.0)) return -1;
-    if (kind == OR_MLP2 && h <= 0) return -1;
+    if (kind == OR_MLP2 && (h <= 0 || layers < 2 || layers > 63)) return -1;
     if (c_mode == OR_C_PER_TOKEN && c == NULL) return -1;
-    long P = oracle_param_count(kind, d, h);
+    long P = oracle_param_count(kind, d, h, layers);
     long units = (long)B * H;
 #pragma omp parallel for schedule(dynamic, 1)
     for (long u = 0; u < units; ++u) {
-        oracle_unit(kind, d, h, chunk, c_mode, loss, delta, T, q + u * T * d,
+        oracle_unit(kind, d, h, layers, chunk, c_mode, loss, delta, T, q + u * T * d,
                     k + u * T * d, v + u * T * d, alpha + u * T, eta + u * T,
                     beta + u * T, c ? c + u * T : NULL, M0 + u * P, S0 + u * P,
                     y + u * T * d, MT + u * P, ST + u * P,

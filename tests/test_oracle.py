@@ -504,3 +504,86 @@ def test_surprise_is_the_gradient_norm_at_chunk_start(kind, d, hidden, loss_kind
             assert abs(sur[t] - np.linalg.norm(ee) * np.linalg.norm(k[0, 0, t])) <= 1e-12 * sur[t]
     # the later tokens take their gradients at the second chunk's start weights
     assert np.all(sur[chunk:] > 0)
+
+
+# ---------------------------------------------------------------- deeper memories (L >= 3 layers)
+# The memory is an MLP of L_M >= 1 layers (0h-n0.github.io explainer, "ニューラル長期メモリモジュール");
+# here M(x) = W_L silu(W_{L-1} ... silu(W1 x)), W1 h x d, W2 .. W_{L-1} h x h, W_L d x h, no bias,
+# packed in that order.
+
+def _torch_deep(d, hidden, layers, W, x):
+    """The L-layer memory written with library ops, independently of the oracle."""
+    sizes = [(hidden, d)] + [(hidden, hidden)] * (layers - 2) + [(d, hidden)]
+    off, h = 0, x
+    for li, (r, c) in enumerate(sizes):
+        Wl = W[off: off + r * c].reshape(r, c)
+        off += r * c
+        h = Wl @ h
+        if li < layers - 1:
+            h = torch.nn.functional.silu(h)
+    assert off == W.shape[0]
+    return h
+
+
+@pytest.mark.parametrize("d,hidden,layers", [(2, 3, 3), (3, 4, 4), (2, 5, 5)])
+def test_deep_grad_finite_differences_and_library(d, hidden, layers):
+    rng = np.random.default_rng(50 + layers)
+    P = oracle.param_count(oracle.MLP2, d, hidden, layers)
+    assert P == 2 * hidden * d + (layers - 2) * hidden * hidden
+    for _ in range(3):
+        W = rng.normal(0, 0.8, P)
+        k, v = rng.normal(0, 1, d), rng.normal(0, 1, d)
+        g = oracle.grad(oracle.MLP2, d, hidden, W, k, v, layers=layers)
+        h = 1e-6
+        fd = np.zeros(P)
+        for p in range(P):
+            Wp = W.copy(); Wp[p] += h
+            Wm = W.copy(); Wm[p] -= h
+            fd[p] = (oracle.loss(oracle.MLP2, d, hidden, Wp, k, v, layers=layers)
+                     - oracle.loss(oracle.MLP2, d, hidden, Wm, k, v, layers=layers)) / (2 * h)
+        assert np.linalg.norm(g - fd) <= 1e-7 * np.linalg.norm(fd)
+        Wt = torch.tensor(W, requires_grad=True)
+        yt = _torch_deep(d, hidden, layers, Wt, torch.tensor(k))
+        (gt,) = torch.autograd.grad(((yt - torch.tensor(v)) ** 2).sum(), Wt)
+        np.testing.assert_allclose(g, gt.numpy(), rtol=1e-12, atol=1e-13)
+        np.testing.assert_allclose(oracle.memory_apply(oracle.MLP2, d, hidden, W, k, layers=layers),
+                                   yt.detach().numpy(), rtol=1e-13, atol=1e-14)
+
+
+@pytest.mark.parametrize("layers", [3, 4])
+def test_deep_chunk1_equals_sequential_and_chunk_sums_gradients(layers):
+    """b = 1: the token-by-token rule (S = beta S + c g, M = (1 - alpha) M - eta S,
+    y = M(q) after the update) with autograd gradients of the L-layer memory;
+    one chunk with beta = 1: S_T is the gradient of the summed loss at the
+    chunk-start weights."""
+    rng = np.random.default_rng(60 + layers)
+    d, hidden, T = 3, 4, 7
+    P = oracle.param_count(oracle.MLP2, d, hidden, layers)
+    k = rng.normal(0, 1, (T, d)); v = rng.normal(0, 1, (T, d)); q = rng.normal(0, 1, (T, d))
+    alpha = rng.uniform(0, 0.2, T); eta = rng.uniform(0.05, 0.3, T); beta = rng.uniform(0.5, 0.9, T)
+    M = rng.normal(0, 0.5, P); S = rng.normal(0, 0.05, P)
+    M0, S0 = M.copy(), S.copy()
+
+    def grad_at(Wnp, t):
+        Wt = torch.tensor(Wnp, requires_grad=True)
+        l_ = ((_torch_deep(d, hidden, layers, Wt, torch.tensor(k[t])) - torch.tensor(v[t])) ** 2).sum()
+        return torch.autograd.grad(l_, Wt)[0].numpy()
+
+    ys = []
+    for t in range(T):
+        S = beta[t] * S + grad_at(M, t)
+        M = (1 - alpha[t]) * M - eta[t] * S
+        ys.append(_torch_deep(d, hidden, layers, torch.tensor(M), torch.tensor(q[t])).numpy())
+    out = oracle.forward(oracle.MLP2, d, hidden, 1, oracle.C_ONE, q[None, None], k[None, None], v[None, None],
+                         alpha[None, None], eta[None, None], beta[None, None], None, M0[None, None], S0[None, None],
+                         layers=layers)
+    np.testing.assert_allclose(out[0][0, 0], np.array(ys), rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(out[1][0, 0], M, rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(out[2][0, 0], S, rtol=1e-11, atol=1e-12)
+    # one chunk of all T tokens with beta = 1, alpha = eta = 0: S_T = S0 + sum_t g_t(M0)
+    out = oracle.forward(oracle.MLP2, d, hidden, T, oracle.C_ONE, q[None, None], k[None, None], v[None, None],
+                         np.zeros((1, 1, T)), np.zeros((1, 1, T)), np.ones((1, 1, T)), None, M0[None, None],
+                         S0[None, None], layers=layers)
+    gsum = sum(grad_at(M0, t) for t in range(T))
+    np.testing.assert_allclose(out[2][0, 0], S0 + gsum, rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(out[1][0, 0], M0, rtol=0, atol=0)
