@@ -20,7 +20,8 @@
  *                  NM_MLP2    M(x) = W2 silu(W1 x), W1 in R^{hidden x d},
  *                             W2 in R^{d x hidden}, no bias; parameters packed
  *                             as W1 (row-major) followed by W2 (row-major).
- *   P (parameters per unit) = d*d (LINEAR) or 2*hidden*d (MLP2).
+ *   P (parameters per unit) = d*d (LINEAR) or 2*hidden*d (MLP2; plus
+ *   (layers - 2)*hidden^2 for a deeper MLP2, see nm_config.layers).
  *
  * The library computes this in the chunked-parallel form (matrix products
  * plus a decay / momentum scan inside each chunk), with every unit's state
@@ -92,7 +93,15 @@ typedef struct nm_config {
     int loss;       /* NM_LOSS_L2 | NM_LOSS_HUBER (a zeroed config means L2)  */
     float huber_delta; /* Huber threshold delta: finite and > 0 for NM_LOSS_HUBER;
                           ignored for NM_LOSS_L2                                 */
+    int layers;     /* NM_MLP2 depth L, 2..NM_MAX_LAYERS (0 means 2); must be 0
+                       for NM_LINEAR.  L > 2 is the deeper memory
+                       W_L silu(W_{L-1} ... silu(W1 x)): W1 hidden x d,
+                       W2 .. W_{L-1} hidden x hidden, W_L d x hidden, packed in
+                       that order (P = 2 hidden d + (L - 2) hidden^2); it runs
+                       on the fp32 FFMA kernels (NM_PATH_TC is unsupported)    */
 } nm_config;
+
+#define NM_MAX_LAYERS 16
 
 typedef struct nm_handle* nm_handle_t;
 

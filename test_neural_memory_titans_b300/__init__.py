@@ -66,7 +66,7 @@ class _Config(ctypes.Structure):
     _fields_ = [("kind", ctypes.c_int), ("d", ctypes.c_int), ("hidden", ctypes.c_int),
                 ("chunk", ctypes.c_int), ("in_dtype", ctypes.c_int), ("out_dtype", ctypes.c_int),
                 ("c_mode", ctypes.c_int), ("path", ctypes.c_int), ("loss", ctypes.c_int),
-                ("huber_delta", ctypes.c_float)]
+                ("huber_delta", ctypes.c_float), ("layers", ctypes.c_int)]
 
 
 _lib = None
@@ -110,8 +110,8 @@ def status_string(status: int) -> str:
     return load_library().nm_status_string(status).decode()
 
 
-def param_count(kind: int, d: int, hidden: int = 0) -> int:
-    return d * d if kind == LINEAR else 2 * hidden * d
+def param_count(kind: int, d: int, hidden: int = 0, layers: int = 2) -> int:
+    return d * d if kind == LINEAR else 2 * hidden * d + (max(layers, 2) - 2) * hidden * hidden
 
 
 def _ptr(t: Optional[torch.Tensor]):
@@ -124,14 +124,15 @@ class NeuralMemory:
     def __init__(self, kind: int, d: int, hidden: int = 0, chunk: int = 64,
                  in_dtype: torch.dtype = torch.bfloat16, out_dtype: Optional[torch.dtype] = None,
                  c_mode: int = C_ONE, path: int = PATH_AUTO, device: int = 0,
-                 loss: int = LOSS_L2, huber_delta: float = 0.0):
+                 loss: int = LOSS_L2, huber_delta: float = 0.0, layers: int = 0):
         lib = load_library()
         out_dtype = in_dtype if out_dtype is None else out_dtype
-        self.cfg = _Config(kind, d, hidden, chunk, _DT[in_dtype], _DT[out_dtype], c_mode, path, loss, huber_delta)
+        self.cfg = _Config(kind, d, hidden, chunk, _DT[in_dtype], _DT[out_dtype], c_mode, path, loss, huber_delta,
+                           layers)
         self.kind, self.d, self.hidden, self.chunk = kind, d, hidden, chunk
         self.in_dtype, self.out_dtype, self.c_mode = in_dtype, out_dtype, c_mode
         self.device = device
-        self.P = param_count(kind, d, hidden)
+        self.P = param_count(kind, d, hidden, layers)
         h = ctypes.c_void_p()
         rc = lib.nm_create(ctypes.byref(self.cfg), device, ctypes.byref(h))
         if rc != NM_OK:

@@ -45,6 +45,7 @@ int check_config(const nm_config* c) {
     if (c->kind == NM_MLP2 && c->hidden <= 0) return NM_ERR_ARG;
     if (c->loss != NM_LOSS_L2 && c->loss != NM_LOSS_HUBER) return NM_ERR_ARG;
     if (c->loss == NM_LOSS_HUBER && !(c->huber_delta > 0.0f && c->huber_delta <= 3.0e38f)) return NM_ERR_ARG;
+    if (c->layers != 0 && (c->kind != NM_MLP2 || c->layers < 2 || c->layers > NM_MAX_LAYERS)) return NM_ERR_ARG;
     return NM_OK;
 }
 

@@ -58,9 +58,15 @@ static inline float nm_err_clip(const nm_config& c) {
     return c.loss == NM_LOSS_HUBER ? 2.0f * c.huber_delta : HUGE_VALF;
 }
 
+// Depth of an MLP2 memory (a zero `layers` means 2); 1 for the linear memory.
+static inline int nm_layers(const nm_config& c) {
+    return c.kind == NM_MLP2 ? (c.layers > 2 ? c.layers : 2) : 1;
+}
+
 // Parameters per unit.
 static inline long long nm_param_count(const nm_config& c) {
-    return c.kind == NM_LINEAR ? (long long)c.d * c.d : 2LL * c.hidden * c.d;
+    return c.kind == NM_LINEAR ? (long long)c.d * c.d
+                               : 2LL * c.hidden * c.d + (long long)(nm_layers(c) - 2) * c.hidden * c.hidden;
 }
 
 // ---- fp32 FFMA kernels (nm_simt.cu) ----------------------------------------

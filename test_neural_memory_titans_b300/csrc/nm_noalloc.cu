@@ -75,6 +75,7 @@ extern "C" int nm_forward_mlp2_noalloc(const nm_config* cfg, int B, int H, int T
     if (cfg->path != NM_PATH_AUTO && cfg->path != NM_PATH_SIMT) return NM_ERR_UNSUPPORTED;
     if (cfg->loss != NM_LOSS_L2 && cfg->loss != NM_LOSS_HUBER) return NM_ERR_ARG;
     if (cfg->loss == NM_LOSS_HUBER && !(cfg->huber_delta > 0.0f && cfg->huber_delta <= 3.0e38f)) return NM_ERR_ARG;
+    if (cfg->layers != 0 && (cfg->layers < 2 || cfg->layers > NM_MAX_LAYERS)) return NM_ERR_ARG;
     nm_config run = *cfg;
     run.path = NM_PATH_SIMT;
     if (!nm_simt_supports(run)) return NM_ERR_UNSUPPORTED;

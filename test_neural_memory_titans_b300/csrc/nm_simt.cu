@@ -397,6 +397,233 @@ __global__ void __launch_bounds__(MLP_THREADS) simt_mlp_kernel(nm_args a, int d,
     }
 }
 
+// ----------------------------------------------------------------- deeper MLP memories
+// M(x) = W_L silu(W_{L-1} ... silu(W1 x)), L >= 3 (the explainer's
+// "ニューラル長期メモリモジュール": an MLP of L_M >= 1 layers).  The chunked form of the
+// 2-layer kernel above, layer by layer: every token's gradient is taken at
+// the chunk-start weights, g_{l,i} = delta_{l,i} x_{l-1,i}^T with x_0 = k_i
+// and delta_L = e_i, so each layer's weights after token t are
+// W_l(t) = A_t W_l - sigma_t S_l - sum_{i<=t} Gamma_{t,i} delta_{l,i} x_{l-1,i}^T,
+// and retrieval runs the layers in order with
+// pre_l(t) = A_t W_l r - sigma_t S_l r - sum_i Gamma_{t,i} (x_{l-1,i} . r) delta_{l,i},
+// r the previous layer's retrieval activation (r = q_t for layer 1).
+
+__host__ __device__ inline size_t deep_unit_floats(int d, int h, int b, int L) {
+    return 2 * (size_t)b * b + 2 * (size_t)b + 4 * (size_t)b * d + (3 * (size_t)(L - 1) + 2) * (size_t)b * h;
+}
+__device__ __forceinline__ long long deep_off(int l, int d, int h) {  // offset of W_l in the packed parameters
+    return l == 1 ? 0 : (long long)h * d + (long long)(l - 2) * h * h;
+}
+
+template <typename Tin, typename Tout>
+__global__ void __launch_bounds__(MLP_THREADS) simt_deep_kernel(nm_args a, int d, int hd, int L, int chunk,
+                                                                int c_mode) {
+    __shared__ float sA[MLP_MAX_CHUNK], sB[MLP_MAX_CHUNK], sSg[MLP_MAX_CHUNK];
+    __shared__ float sa[MLP_MAX_CHUNK], se[MLP_MAX_CHUNK], sbt[MLP_MAX_CHUNK], sc[MLP_MAX_CHUNK];
+    const long long unit = blockIdx.x;
+    const int tid = threadIdx.x;
+    const int NT = blockDim.x;
+    const long long T = a.T;
+    const long long P = 2LL * hd * d + (long long)(L - 2) * hd * hd;
+    const int b = chunk;
+    const size_t bh = (size_t)b * hd;
+
+    float* ws = (float*)a.scratch + unit * deep_unit_floats(d, hd, b, L);
+    float* Gam = ws;                   // [b][b]   Gamma_{t,i}
+    float* ub = Gam + (size_t)b * b;   // [b]      u_{n-1,i}
+    float* gl = ub + b;                // [b]      Gamma_{n-1,i}
+    float* Kf = gl + b;                // [b][d]
+    float* Qf = Kf + (size_t)b * d;    // [b][d]
+    float* Vf = Qf + (size_t)b * d;    // [b][d]
+    float* E = Vf + (size_t)b * d;     // [b][d]   e_t (the output layer's delta)
+    float* Z = E + (size_t)b * d;      // [L-1][b][h] pre-activations of the keys' forward
+    float* X = Z + (L - 1) * bh;       // [L-1][b][h] activations x_l of the keys' forward
+    float* Dl = X + (L - 1) * bh;      // [L-1][b][h] delta_l of the hidden layers
+    float* R = Dl + (L - 1) * bh;      // [2][b][h]   retrieval activations (ping-pong)
+    float* Pm = R + 2 * bh;            // [b][b]   Gamma (.) inner products of the current layer
+
+    const Tin* q = (const Tin*)a.q + unit * T * d;
+    const Tin* k = (const Tin*)a.k + unit * T * d;
+    const Tin* v = (const Tin*)a.v + unit * T * d;
+    const float* al = a.alpha + unit * T;
+    const float* et = a.eta + unit * T;
+    const float* be = a.beta + unit * T;
+    const float* cc = a.c ? a.c + unit * T : nullptr;
+    Tout* y = (Tout*)a.y + unit * T * d;
+    float* Mw = a.M_T + unit * P;  // the state, updated in place chunk by chunk
+    float* Sw = a.S_T + unit * P;
+    if (a.M_T != a.M0)
+        for (long long i = tid; i < P; i += NT) Mw[i] = a.M0[unit * P + i];
+    if (a.S_T != a.S0)
+        for (long long i = tid; i < P; i += NT) Sw[i] = a.S0[unit * P + i];
+    __syncthreads();
+
+    for (long long t0 = 0; t0 < T; t0 += b) {
+        const int n = (int)min((long long)b, T - t0);
+        for (int i = tid; i < n * d; i += NT) {
+            Kf[i] = ld_in(k + t0 * d + i);
+            Qf[i] = ld_in(q + t0 * d + i);
+            Vf[i] = ld_in(v + t0 * d + i);
+        }
+        for (int i = tid; i < n; i += NT) {
+            sa[i] = 1.0f - al[t0 + i];
+            se[i] = et[t0 + i];
+            sbt[i] = be[t0 + i];
+            sc[i] = momentum_coef(c_mode, be[t0 + i], cc, t0 + i);
+        }
+        __syncthreads();
+        // decay / momentum scan, one column i of Gamma per thread
+        for (int i = tid; i < n; i += NT) {
+            float u = sc[i];
+            float G = se[i] * u;
+            Gam[(size_t)i * b + i] = G;
+            for (int t = i + 1; t < n; ++t) {
+                u *= sbt[t];
+                G = fmaf(sa[t], G, se[t] * u);
+                Gam[(size_t)t * b + i] = G;
+            }
+            ub[i] = u;
+            gl[i] = G;
+        }
+        if (tid == 0) {
+            float A = 1.f, Bc = 1.f, sg = 0.f;
+            for (int t = 0; t < n; ++t) {
+                A *= sa[t];
+                Bc *= sbt[t];
+                sg = fmaf(sa[t], sg, se[t] * Bc);
+                sA[t] = A;
+                sB[t] = Bc;
+                sSg[t] = sg;
+            }
+        }
+        __syncthreads();
+        // keys' forward at the chunk-start weights: z_l = W_l x_{l-1}, x_l = silu(z_l)
+        for (int l = 1; l < L; ++l) {
+            const int in = l == 1 ? d : hd;
+            const float* xin = l == 1 ? Kf : X + (l - 2) * bh;
+            const float* Wl = Mw + deep_off(l, d, hd);
+            for (int idx = tid; idx < n * hd; idx += NT) {
+                const int t = idx / hd, j = idx % hd;
+                float acc = 0.f;
+                for (int x = 0; x < in; ++x) acc = fmaf(xin[t * in + x], Wl[(long long)j * in + x], acc);
+                Z[(l - 1) * bh + idx] = acc;
+                X[(l - 1) * bh + idx] = silu_f(acc);
+            }
+            __syncthreads();
+        }
+        // e = 2 (W_L x_{L-1} - v), clipped for the Huber loss
+        {
+            const float* xl = X + (L - 2) * bh;
+            const float* WL = Mw + deep_off(L, d, hd);
+            for (int idx = tid; idx < n * d; idx += NT) {
+                const int t = idx / d, o = idx % d;
+                float acc = 0.f;
+                for (int j = 0; j < hd; ++j) acc = fmaf(xl[t * hd + j], WL[(long long)o * hd + j], acc);
+                E[idx] = nm_clip_err(2.0f * (acc - Vf[idx]), a.e_clip);
+            }
+            __syncthreads();
+        }
+        // backward: delta_l = (W_{l+1}^T delta_{l+1}) (.) silu'(z_l), delta_L = e
+        for (int l = L - 1; l >= 1; --l) {
+            const int up_n = l + 1 == L ? d : hd;
+            const float* up = l + 1 == L ? E : Dl + l * bh;
+            const float* Wn = Mw + deep_off(l + 1, d, hd);  // [up_n][h]
+            for (int idx = tid; idx < n * hd; idx += NT) {
+                const int t = idx / hd, j = idx % hd;
+                float acc = 0.f;
+                for (int o = 0; o < up_n; ++o) acc = fmaf(up[t * up_n + o], Wn[(long long)o * hd + j], acc);
+                Dl[(l - 1) * bh + idx] = acc * dsilu_f(Z[(l - 1) * bh + idx]);
+            }
+            __syncthreads();
+        }
+        if (a.surprise) {  // surprise_t = sqrt(sum_l ||delta_{l,t}||^2 ||x_{l-1,t}||^2), one thread per token
+            for (int t = tid; t < n; t += NT) {
+                float tot = 0.f;
+                for (int l = 1; l <= L; ++l) {
+                    const int in = l == 1 ? d : hd, out = l == L ? d : hd;
+                    const float* xin = l == 1 ? Kf : X + (l - 2) * bh;
+                    const float* dl = l == L ? E : Dl + (l - 1) * bh;
+                    float x2 = 0.f, d2 = 0.f;
+                    for (int x0 = 0; x0 < in; ++x0) {
+                        const int x = (x0 + t) % in;  // rotated: conflict-free across the warp
+                        x2 = fmaf(xin[t * in + x], xin[t * in + x], x2);
+                    }
+                    for (int o0 = 0; o0 < out; ++o0) {
+                        const int o = (o0 + t) % out;
+                        d2 = fmaf(dl[t * out + o], dl[t * out + o], d2);
+                    }
+                    tot = fmaf(d2, x2, tot);
+                }
+                a.surprise[unit * T + t0 + t] = sqrtf(tot);
+            }
+        }
+        // retrieval, layer by layer
+        const float* r = Qf;  // the previous layer's retrieval activation, [n][in]
+        for (int l = 1; l <= L; ++l) {
+            const int in = l == 1 ? d : hd, out = l == L ? d : hd;
+            const float* xin = l == 1 ? Kf : X + (l - 2) * bh;
+            const float* dl = l == L ? E : Dl + (l - 1) * bh;
+            for (int idx = tid; idx < n * n; idx += NT) {  // Pm = Gamma (.) (r_t . x_{l-1,i}), lower triangle
+                const int t = idx / n, i = idx % n;
+                float acc = 0.f;
+                if (i <= t) {
+                    for (int x = 0; x < in; ++x) acc = fmaf(r[t * in + x], xin[i * in + x], acc);
+                    acc *= Gam[(size_t)t * b + i];
+                }
+                Pm[(size_t)t * b + i] = acc;
+            }
+            __syncthreads();
+            const float* Wl = Mw + deep_off(l, d, hd);
+            const float* Sl = Sw + deep_off(l, d, hd);
+            float* rn = R + (l & 1) * bh;
+            for (int idx = tid; idx < n * out; idx += NT) {
+                const int t = idx / out, j = idx % out;
+                float m = 0.f, s = 0.f, g = 0.f;
+                for (int x = 0; x < in; ++x) {
+                    const float rx = r[t * in + x];
+                    m = fmaf(rx, Wl[(long long)j * in + x], m);
+                    s = fmaf(rx, Sl[(long long)j * in + x], s);
+                }
+                for (int i = 0; i <= t; ++i) g = fmaf(Pm[(size_t)t * b + i], dl[i * out + j], g);
+                const float pre = sA[t] * m - sSg[t] * s - g;
+                if (l < L) rn[idx] = silu_f(pre);
+                else st_out(y + (t0 + t) * d + j, pre);
+            }
+            __syncthreads();
+            r = rn;
+        }
+        // chunk-end state, layer by layer: W = A W0 - sigma S0 - sum_i gamma_i g_i, S = B S0 + sum_i u_i g_i
+        const float An = sA[n - 1], Bn = sB[n - 1], sn = sSg[n - 1];
+        for (int l = 1; l <= L; ++l) {
+            const int in = l == 1 ? d : hd, out = l == L ? d : hd;
+            const float* xin = l == 1 ? Kf : X + (l - 2) * bh;
+            const float* dl = l == L ? E : Dl + (l - 1) * bh;
+            float* Wl = Mw + deep_off(l, d, hd);
+            float* Sl = Sw + deep_off(l, d, hd);
+            for (int idx = tid; idx < out * in; idx += NT) {
+                const int j = idx / in, x = idx % in;
+                float gw = 0.f, gs = 0.f;
+                for (int i = 0; i < n; ++i) {
+                    const float gx = dl[i * out + j] * xin[i * in + x];
+                    gw = fmaf(gl[i], gx, gw);
+                    gs = fmaf(ub[i], gx, gs);
+                }
+                const float w = Wl[idx], sv = Sl[idx];
+                Wl[idx] = An * w - sn * sv - gw;
+                Sl[idx] = Bn * sv + gs;
+            }
+        }
+        __syncthreads();
+    }
+}
+
+template <typename Tin, typename Tout>
+cudaError_t launch_deep(const nm_config& c, const nm_args& a, cudaStream_t s) {
+    simt_deep_kernel<Tin, Tout><<<(unsigned)(a.B * a.H), MLP_THREADS, 0, s>>>(a, c.d, c.hidden, c.layers, c.chunk,
+                                                                            c.c_mode);
+    return cudaGetLastError();
+}
+
 template <typename Tin, typename Tout>
 cudaError_t launch_mlp(const nm_config& c, const nm_args& a, cudaStream_t s) {
     simt_mlp_kernel<Tin, Tout><<<(unsigned)(a.B * a.H), MLP_THREADS, 0, s>>>(a, c.d, c.hidden, c.chunk, c.c_mode);
@@ -408,6 +635,8 @@ cudaError_t dispatch_out(const nm_config& c, const nm_args& a, cudaStream_t s) {
     if (c.kind == NM_LINEAR)
         return c.out_dtype == NM_BF16 ? launch_linear_d<Tin, __nv_bfloat16>(c, a, s)
                                       : launch_linear_d<Tin, float>(c, a, s);
+    if (nm_layers(c) > 2)
+        return c.out_dtype == NM_BF16 ? launch_deep<Tin, __nv_bfloat16>(c, a, s) : launch_deep<Tin, float>(c, a, s);
     return c.out_dtype == NM_BF16 ? launch_mlp<Tin, __nv_bfloat16>(c, a, s) : launch_mlp<Tin, float>(c, a, s);
 }
 
@@ -423,6 +652,8 @@ bool nm_simt_supports(const nm_config& c) {
 
 size_t nm_simt_scratch_bytes(const nm_config& c, int B, int H) {
     if (c.kind == NM_LINEAR) return 0;
+    if (nm_layers(c) > 2)
+        return sizeof(float) * deep_unit_floats(c.d, c.hidden, c.chunk, nm_layers(c)) * (size_t)B * (size_t)H;
     return sizeof(float) * mlp_unit_floats(c.d, c.hidden, c.chunk) * (size_t)B * (size_t)H;
 }
 

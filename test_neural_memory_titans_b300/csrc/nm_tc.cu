@@ -11,12 +11,14 @@ cudaError_t nm_tc_linear64_launch(const nm_config& c, const nm_args& a, cudaStre
 cudaError_t nm_tc_mlp_wide_launch(const nm_config& c, const nm_args& a, cudaStream_t s);
 
 bool nm_tc_supports(const nm_config& c) {
+    if (nm_layers(c) > 2) return false;  // deeper MLP memories run on the fp32 FFMA kernel
     return nm_tc_linear_supports(c) || nm_tc_linear64_supports(c) || nm_tc_mlp_supports(c) ||
            nm_tc_mlp_wide_supports(c);
 }
 
 // Kernels that can also write the per-token surprise (gradient norm).
 bool nm_tc_supports_surprise(const nm_config& c) {
+    if (nm_layers(c) > 2) return false;
     return nm_tc_linear_supports(c) || nm_tc_linear64_supports(c) || nm_tc_mlp_supports(c) ||
            nm_tc_mlp_wide_supports(c);
 }

@@ -74,6 +74,10 @@ def test_null_handle_and_bad_config_without_gpu():
     big_chunk = nm._Config(nm.LINEAR, 64, 0, 1024, nm.BF16, nm.BF16, nm.C_ONE, nm.PATH_AUTO)
     assert lib.nm_create(ctypes.byref(big_chunk), 0, ctypes.byref(h)) == nm.NM_ERR_UNSUPPORTED
     assert lib.nm_create(None, 0, ctypes.byref(h)) == nm.NM_ERR_ARG
+    # the depth: only an MLP memory has layers, 2..16
+    for kind, layers in ((nm.LINEAR, 3), (nm.MLP2, 1), (nm.MLP2, 17), (nm.MLP2, -2)):
+        cfg = nm._Config(kind, 64, 128, 64, nm.BF16, nm.BF16, nm.C_ONE, nm.PATH_AUTO, nm.LOSS_L2, 0.0, layers)
+        assert lib.nm_create(ctypes.byref(cfg), 0, ctypes.byref(h)) == nm.NM_ERR_ARG
     # the loss: an unknown kind, or a Huber threshold that is not finite and positive
     for loss, delta in ((2, 1.0), (nm.LOSS_HUBER, 0.0), (nm.LOSS_HUBER, -1.0), (nm.LOSS_HUBER, float("inf")),
                         (nm.LOSS_HUBER, float("nan"))):

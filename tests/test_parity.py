@@ -441,3 +441,53 @@ def test_surprise_mlp_d128(path, hidden, T, delta):
     x = W.make_inputs(wl, "cuda", seed=140 + T + hidden)
     M0, S0 = W.random_state(wl, "cuda", seed=141, scale=0.5)
     _surprise_case(wl, x, path, M0, S0, delta)
+
+
+# ------------------------------------------------------------ deeper MLP memories (L >= 3), fp32 FFMA kernel
+
+def _deep_state(d, hidden, layers, seed, scale=0.5):
+    g = torch.Generator("cuda").manual_seed(seed)
+    parts_m, parts_s = [], []
+    for li in range(layers):
+        out_f = d if li == layers - 1 else hidden
+        in_f = d if li == 0 else hidden
+        std = (scale / in_f) ** 0.5
+        parts_m.append(std * torch.randn(out_f * in_f, generator=g, device="cuda"))
+        parts_s.append(0.1 * std * torch.randn(out_f * in_f, generator=g, device="cuda"))
+    return torch.cat(parts_m), torch.cat(parts_s)
+
+
+@pytest.mark.parametrize("layers,d,hidden,T,chunk,dtype,delta", [
+    (3, 64, 128, 100, 64, torch.bfloat16, None),
+    (4, 32, 64, 150, 16, torch.float32, None),
+    (3, 64, 96, 90, 64, torch.bfloat16, 0.5),
+    (5, 16, 32, 70, 8, torch.float32, 0.3),
+])
+def test_deep_memory(layers, d, hidden, T, chunk, dtype, delta):
+    wl = dataclasses.replace(W.WORKLOADS[1], d=d, hidden=hidden, chunk=chunk, dtype=dtype).with_sizes(B=1, H=2, T=T)
+    x = W.make_inputs(wl, "cuda", seed=150 + layers + T)
+    x["eta"] *= 0.5
+    P = nm.param_count(nm.MLP2, d, hidden, layers)
+    m0, s0 = zip(*(_deep_state(d, hidden, layers, seed=160 + u) for u in range(2)))
+    M0 = torch.stack(m0).reshape(1, 2, P).contiguous()
+    S0 = torch.stack(s0).reshape(1, 2, P).contiguous()
+    loss = nm.LOSS_L2 if delta is None else nm.LOSS_HUBER
+    mem = nm.NeuralMemory(nm.MLP2, d, hidden, chunk, in_dtype=dtype, layers=layers, loss=loss,
+                          huber_delta=0.0 if delta is None else delta)
+    assert mem.path == nm.PATH_SIMT
+    y, MT, ST, sur = mem.forward_surprise(x["q"], x["k"], x["v"], x["alpha"], x["eta"], x["beta"], M0, S0)
+    assert mem.synchronize() == nm.NM_OK
+    mem.close()
+    ref = oracle.forward(oracle.MLP2, d, hidden, chunk, oracle.C_ONE,
+                         *(f64(x[k_]) for k_ in ("q", "k", "v", "alpha", "eta", "beta")), None, f64(M0), f64(S0),
+                         oracle.LOSS_L2 if delta is None else oracle.LOSS_HUBER,
+                         np.inf if delta is None else delta, surprise=True, layers=layers)
+    tol = TOL[dtype]
+    assert rel_l2(f64(y), ref[0]) <= tol["y"]
+    assert rel_l2(f64(MT), ref[1]) <= tol["M_T"]
+    assert rel_l2(f64(ST), ref[2]) <= tol["S_T"]
+    assert rel_l2(f64(sur), ref[3]) <= tol["y"]
+    # a deeper memory is not built on the tensor-core path
+    with pytest.raises(nm.NMError) as ei:
+        nm.NeuralMemory(nm.MLP2, d, hidden, chunk, in_dtype=dtype, layers=layers, path=nm.PATH_TC)
+    assert ei.value.status == nm.NM_ERR_UNSUPPORTED
