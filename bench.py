@@ -63,7 +63,9 @@ def algorithmic(wl) -> dict:
     """Algorithmic tensor-core flops and HBM bytes of one full forward.
 
     flops per token: linear 10 d^2 + 2 (b+1) d, MLP 22 d h + 2 (b+1)(d+h)
-    (the b x b causal products counted as lower-triangular).
+    (the b x b causal products counted as lower-triangular); an MLP of L
+    layers: 11 P + 2 (b+1)(d + (L-1) h) with P = 2 d h + (L-2) h^2 (11 flops
+    per parameter and token, as for two layers).
     bytes per token: q, k, v in, y out, three fp32 gates; plus per unit the
     fp32 state read (M0, S0) and written (M_T, S_T) once per call.
     """
@@ -71,7 +73,7 @@ def algorithmic(wl) -> dict:
     if wl.kind == 0:
         f_tok = 10 * d * d + 2 * (b + 1) * d
     else:
-        f_tok = 22 * d * h + 2 * (b + 1) * (d + h)
+        f_tok = 11 * wl.P + 2 * (b + 1) * (d + (wl.layers - 1) * h)
     eb = 2 if wl.dtype == torch.bfloat16 else 4
     bytes_tok = 3 * d * eb + 12 + d * eb
     calls = (wl.T // wl.segment) if wl.segment else 1
@@ -211,7 +213,7 @@ def time_oracle(wl, x, budget_s: float = 15.0):
 
     def run(args):
         t0 = time.perf_counter()
-        oracle.forward(wl.kind, wl.d, wl.hidden, wl.chunk, oracle.C_ONE, *args)
+        oracle.forward(wl.kind, wl.d, wl.hidden, wl.chunk, oracle.C_ONE, *args, layers=wl.layers)
         return time.perf_counter() - t0
 
     # calibrate on one round of units (one per core) over a few chunks
@@ -245,6 +247,11 @@ def workload(args):
     from test_neural_memory_titans_b300 import workloads as W
 
     wl = W.WORKLOADS[args.workload]
+    if args.layers is not None and args.layers != wl.layers:
+        import dataclasses
+        if wl.kind != W.MLP2:
+            raise SystemExit("--layers applies to the MLP workloads (1 and 3)")
+        wl = dataclasses.replace(wl, layers=args.layers, name="%s_L%d" % (wl.name, args.layers))
     if args.B is None and args.H is None and args.T is None:
         return wl
     wl = wl.with_sizes(B=args.B, H=args.H, T=args.T)
@@ -262,7 +269,8 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.set_device(dev)
     wl = workload(args)
     x = W.make_inputs(wl, dev, seed=1000 + args.workload + 100 * rank)
-    mem = nm.NeuralMemory(wl.kind, wl.d, wl.hidden, wl.chunk, in_dtype=wl.dtype, path=args.path, device=local_rank)
+    mem = nm.NeuralMemory(wl.kind, wl.d, wl.hidden, wl.chunk, in_dtype=wl.dtype, path=args.path, device=local_rank,
+                          layers=wl.layers if wl.kind == nm.MLP2 else 0)
     stream = torch.cuda.current_stream(dev)
     y = torch.empty(x["q"].shape, dtype=wl.dtype, device=dev)
     M = torch.empty_like(x["M0"])
@@ -346,7 +354,8 @@ def run_ours(args, rank, world, local_rank):
         args8 = (x["q"], x["k"], x["v"], x["alpha"], x["eta"], x["beta"], x["M0"], x["S0"])
         sur = torch.empty(x["alpha"].shape, dtype=torch.float32, device=dev)
         mem_h = nm.NeuralMemory(wl.kind, wl.d, wl.hidden, wl.chunk, in_dtype=wl.dtype, path=args.path,
-                                device=local_rank, loss=nm.LOSS_HUBER, huber_delta=0.1)
+                                device=local_rank, loss=nm.LOSS_HUBER, huber_delta=0.1,
+                                layers=wl.layers if wl.kind == nm.MLP2 else 0)
         v_h = time_calls(lambda: mem_h.forward(*args8, y=y, M_T=M, S_T=S, stream=stream), n_var)
         v_s = time_calls(lambda: mem.forward_surprise(*args8, y=y, M_T=M, S_T=S, surprise=sur, stream=stream), n_var)
         for m_ in (mem, mem_h):
@@ -437,7 +446,7 @@ def run_ours(args, rank, world, local_rank):
            "vs_baseline": None, "dtype": "bf16" if mem.path == nm.PATH_TC else "f32", "data": "synthetic",
            "config": {"workload": wl.name, "memory": "linear" if wl.kind == 0 else "mlp2", "B": wl.B, "H": wl.H,
                       "T": wl.T, "d": wl.d, "hidden": wl.hidden, "chunk": wl.chunk,
-                      "segment": wl.segment or None, "in_dtype": str(wl.dtype).replace("torch.", ""),
+                      "layers": wl.layers if wl.kind == 1 else None, "segment": wl.segment or None, "in_dtype": str(wl.dtype).replace("torch.", ""),
                       "parallelism": "dp%d" % world,
                       "l2": "flushed between timed steps (256 MB write, outside the step's events)"},
            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
@@ -468,7 +477,8 @@ def run_reference(args, rank, world):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / len(runs),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": wl.name, "memory": "linear" if wl.kind == 0 else "mlp2", "B": wl.B, "H": wl.H,
-                       "T": wl.T, "d": wl.d, "hidden": wl.hidden, "chunk": wl.chunk},
+                       "T": wl.T, "d": wl.d, "hidden": wl.hidden, "chunk": wl.chunk,
+                       "layers": wl.layers if wl.kind == 1 else None},
             "cpu_baseline": cpu,
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
@@ -486,6 +496,8 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-variants", action="store_true", help="skip timing the Huber-loss and surprise forms")
+    ap.add_argument("--layers", type=int, default=None,
+                    help="MLP workloads: a memory of this many layers instead of 2 (fp32 FFMA kernel for > 2)")
     ap.add_argument("--cpu-budget", type=float, default=None,
                     help="seconds of oracle work per step of the reference arm (default: about 150 s in all)")
     ap.add_argument("--B", type=int, default=None, help="override the workload's batch (small profiling cases)")

@@ -45,10 +45,13 @@ class Workload:
     keys: str          # "gauss" | "orth_map" | "codebook" | "needles"
     segment: int = 0   # >0: processed as T/segment calls carrying (M, S)
     w_init_std: float = 0.0
+    layers: int = 2    # MLP depth (W1, L - 2 hidden-to-hidden layers, W_L); 2 for the configured workloads
 
     @property
     def P(self) -> int:
-        return self.d * self.d if self.kind == LINEAR else 2 * self.hidden * self.d
+        if self.kind == LINEAR:
+            return self.d * self.d
+        return 2 * self.hidden * self.d + (self.layers - 2) * self.hidden * self.hidden
 
     @property
     def tokens(self) -> int:
