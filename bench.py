@@ -35,8 +35,8 @@ METRIC = "memory-layer fwd tokens/sec (B*H*T/s) and % of roofline (TC FLOPs vs H
 # profiles/: workload -> (kernel sources, sha256 prefix of those sources when captured, bytes).
 # A capture describes the kernel it was taken on only: when the sources differ, traffic is null.
 NCU_TRAFFIC = {
-    "mlp_64x256_bf16_b4h8_t4096_c64": (("nm_tc_mlp.cu", "tc_common.cuh"), "0c82da9d022d3f89", 62.415e6),
-    "linear_d128_bf16_b8h16_t16384_c64": (("nm_tc_linear.cu", "tc_common.cuh"), "4cddf53d9c0366eb", 2.114e9),
+    "mlp_64x256_bf16_b4h8_t4096_c64": (("nm_tc_mlp.cu", "tc_common.cuh"), "90384118f1d61292", 61.86e6),
+    "linear_d128_bf16_b8h16_t16384_c64": (("nm_tc_linear.cu", "tc_common.cuh"), "a2afbc7a0329e8ae", 2.116e9),
 }
 
 

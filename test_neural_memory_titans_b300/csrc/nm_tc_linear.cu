@@ -120,7 +120,9 @@ __device__ __forceinline__ void store_y<__nv_bfloat16>(__nv_bfloat16* p, float x
 template <>
 __device__ __forceinline__ void store_y<float>(float* p, float x) { *p = x; }
 
-template <typename Tout>
+// OPT: bit 0 = write the surprise (a.surprise), bit 1 = Huber loss (clip e); compiled
+// variants, so that the plain forward carries neither.
+template <typename Tout, int OPT>
 __global__ void __launch_bounds__(NTHREADS, 1)
     tc_linear_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                      const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap ty, nm_args a,
@@ -392,11 +394,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             get_row32(sm + OFF_V, BC, t, c0, vv);
 #pragma unroll
             for (int q = 0; q < 32; ++q) e0[q] = live ? 2.0f * (e0[q] - vv[q]) : 0.0f;
-            if (a.e_clip < HUGE_VALF) {  // the Huber loss clips e (uniform branch)
+            if (OPT & 2) {  // the Huber loss clips e
 #pragma unroll
                 for (int q = 0; q < 32; ++q) e0[q] = nm_clip_err(e0[q], a.e_clip);
             }
-            if (a.surprise) {  // partial ||e_t||^2 and ||k_t||^2 over this thread's 32 columns, summed over the row
+            if (OPT & 1) {  // partial ||e_t||^2 and ||k_t||^2 over this thread's 32 columns, summed over the row
                 float kv[32], e2 = 0.0f, k2 = 0.0f;
                 get_row32(sm + OFF_K + stage * TILE, BC, t, c0, kv);
 #pragma unroll
@@ -437,7 +439,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                               : c_mode == NM_C_PER_TOKEN ? nxt_c : 1.0f;
         }
         handoff();
-        if (a.surprise && hf == 0 && lane < 16) {  // surprise_t = ||e_t|| ||k_t||, token t = 16 qd + lane
+        if ((OPT & 1) && hf == 0 && lane < 16) {  // surprise_t = ||e_t|| ||k_t||, token t = 16 qd + lane
             const int t = 16 * qd + lane;
             if (t < n)
                 a.surprise[unit * T + t0 + t] = sqrtf(sPart[t] + sPart[2 * BC + t]) *
@@ -518,7 +520,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (warp == 0) tmem_dealloc(tm, 512);
 }
 
-template <typename Tout>
+template <typename Tout, int OPT>
 cudaError_t launch(const nm_config& c, const nm_args& a, cudaStream_t s) {
     CUtensorMap tq, tk, tv, ty;
     const long long units = (long long)a.B * a.H;
@@ -526,7 +528,7 @@ cudaError_t launch(const nm_config& c, const nm_args& a, cudaStream_t s) {
         !make_token_map(&tv, a.v, D, a.T, units) ||
         !make_token_store_map(&ty, a.y, D, a.T, units, sizeof(Tout) == 2))
         return cudaErrorInvalidValue;
-    auto kern = tc_linear_kernel<Tout>;
+    auto kern = tc_linear_kernel<Tout, OPT>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
     if (e != cudaSuccess) return e;
     kern<<<(unsigned)units, NTHREADS, SMEM_BYTES, s>>>(tq, tk, tv, ty, a, c.c_mode);
@@ -540,5 +542,19 @@ bool nm_tc_linear_supports(const nm_config& c) {
 }
 
 cudaError_t nm_tc_linear_launch(const nm_config& c, const nm_args& a, cudaStream_t s) {
-    return c.out_dtype == NM_BF16 ? launch<__nv_bfloat16>(c, a, s) : launch<float>(c, a, s);
+    const int opt = (a.surprise ? 1 : 0) | (a.e_clip < HUGE_VALF ? 2 : 0);
+    if (c.out_dtype == NM_BF16) {
+        switch (opt) {
+            case 0: return launch<__nv_bfloat16, 0>(c, a, s);
+            case 1: return launch<__nv_bfloat16, 1>(c, a, s);
+            case 2: return launch<__nv_bfloat16, 2>(c, a, s);
+            default: return launch<__nv_bfloat16, 3>(c, a, s);
+        }
+    }
+    switch (opt) {
+        case 0: return launch<float, 0>(c, a, s);
+        case 1: return launch<float, 1>(c, a, s);
+        case 2: return launch<float, 2>(c, a, s);
+        default: return launch<float, 3>(c, a, s);
+    }
 }

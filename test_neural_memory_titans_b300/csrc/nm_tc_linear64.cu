@@ -126,7 +126,9 @@ __device__ __forceinline__ void store_row32<float>(float* p, const float* v) {
         reinterpret_cast<float4*>(p)[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
 }
 
-template <int NB, typename Tout>
+// OPT: bit 0 = write the surprise (a.surprise), bit 1 = Huber loss (clip e); compiled
+// variants, so that the plain forward carries neither.
+template <int NB, typename Tout, int OPT>
 __global__ void __launch_bounds__(NTHREADS, 1)
     tc_linear64_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                        const __grid_constant__ CUtensorMap tv, nm_args a, int c_mode) {
@@ -396,11 +398,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 get_row32(sm + OFF_V + stage * T64, t, c0, vv);
 #pragma unroll
                 for (int q = 0; q < 32; ++q) e[q] = live ? 2.0f * (e[q] - vv[q]) : 0.0f;
-                if (a.e_clip < HUGE_VALF) {  // the Huber loss clips e (uniform branch)
+                if (OPT & 2) {  // the Huber loss clips e
 #pragma unroll
                     for (int q = 0; q < 32; ++q) e[q] = nm_clip_err(e[q], a.e_clip);
                 }
-                if (a.surprise) {  // partial ||e_t||^2, ||k_t||^2 over this thread's 32 columns
+                if (OPT & 1) {  // partial ||e_t||^2, ||k_t||^2 over this thread's 32 columns
                     float kv[32], e2 = 0.0f, k2 = 0.0f;
                     get_row32(sm + OFF_K + stage * T64, t, c0, kv);
 #pragma unroll
@@ -438,7 +440,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                               : c_mode == NM_C_PER_TOKEN ? nxt_c : 1.0f;
         }
         handoff();
-        if (a.surprise && hf == 0 && r64 && rr < n)  // surprise_t = ||e_t|| ||k_t|| (gradient at the chunk start)
+        if ((OPT & 1) && hf == 0 && r64 && rr < n)  // surprise_t = ||e_t|| ||k_t|| (gradient at the chunk start)
             a.surprise[unit * T + t0 + rr] = sqrtf(sPart[rr] + sPart[2 * SB + rr]) * sqrtf(sPart[SB + rr] + sPart[3 * SB + rr]);
         // ---- batch 2: Q [M0 | S0 | CG | CU]^T, P E, CG += (gamma E)^T K, CU += (u E)^T K
         const bool go2 = !failed;
@@ -531,14 +533,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (warp == 0) tmem_dealloc(tm, 512);
 }
 
-template <int NB, typename Tout>
+template <int NB, typename Tout, int OPT>
 cudaError_t launch(const nm_config& c, const nm_args& a, cudaStream_t s) {
     CUtensorMap tq, tk, tv;
     const long long units = (long long)a.B * a.H;
     if (!make_token_map(&tq, a.q, D, a.T, units) || !make_token_map(&tk, a.k, D, a.T, units) ||
         !make_token_map(&tv, a.v, D, a.T, units))
         return cudaErrorInvalidValue;
-    auto kern = tc_linear64_kernel<NB, Tout>;
+    auto kern = tc_linear64_kernel<NB, Tout, OPT>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
     if (e != cudaSuccess) return e;
     kern<<<(unsigned)units, NTHREADS, SMEM_BYTES, s>>>(tq, tk, tv, a, c.c_mode);
@@ -547,7 +549,21 @@ cudaError_t launch(const nm_config& c, const nm_args& a, cudaStream_t s) {
 
 template <int NB>
 cudaError_t launch_nb(const nm_config& c, const nm_args& a, cudaStream_t s) {
-    return c.out_dtype == NM_BF16 ? launch<NB, __nv_bfloat16>(c, a, s) : launch<NB, float>(c, a, s);
+    const int opt = (a.surprise ? 1 : 0) | (a.e_clip < HUGE_VALF ? 2 : 0);
+    if (c.out_dtype == NM_BF16) {
+        switch (opt) {
+            case 0: return launch<NB, __nv_bfloat16, 0>(c, a, s);
+            case 1: return launch<NB, __nv_bfloat16, 1>(c, a, s);
+            case 2: return launch<NB, __nv_bfloat16, 2>(c, a, s);
+            default: return launch<NB, __nv_bfloat16, 3>(c, a, s);
+        }
+    }
+    switch (opt) {
+        case 0: return launch<NB, float, 0>(c, a, s);
+        case 1: return launch<NB, float, 1>(c, a, s);
+        case 2: return launch<NB, float, 2>(c, a, s);
+        default: return launch<NB, float, 3>(c, a, s);
+    }
 }
 
 }  // namespace

@@ -215,7 +215,9 @@ __device__ __forceinline__ int colsum16_column(int lane) {
     return 8 * ((lane >> 4) & 1) + 4 * ((lane >> 3) & 1) + 2 * ((lane >> 2) & 1) + ((lane >> 1) & 1);
 }
 
-template <int NC, int CW, typename Tout, bool SURP>
+// SURP: write the surprise (a.surprise); HUB: the Huber loss clips e.  Compiled
+// variants, so that the plain forward carries neither.
+template <int NC, int CW, typename Tout, bool SURP, bool HUB>
 __global__ void __launch_bounds__(128 * (64 / CW), 1)
     tc_mlp_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, nm_args a, int c_mode) {
@@ -593,7 +595,7 @@ __global__ void __launch_bounds__(128 * (64 / CW), 1)
 #pragma unroll
                 for (int q = 0; q < CW; ++q) ev[q] = fmaf(2.0f, px[q], ev[q]);
             }
-            if (a.e_clip < HUGE_VALF) {  // the Huber loss clips e (uniform branch: free for the squared loss)
+            if (HUB) {  // the Huber loss clips e
 #pragma unroll
                 for (int q = 0; q < CW; ++q) ev[q] = nm_clip_err(ev[q], a.e_clip);
             }
@@ -789,14 +791,14 @@ __global__ void __launch_bounds__(128 * (64 / CW), 1)
     if (warp == 0) tmem_dealloc(tm, 512);
 }
 
-template <int NC, int CW, typename Tout, bool SURP>
+template <int NC, int CW, typename Tout, bool SURP, bool HUB>
 cudaError_t launch(const nm_config& c, const nm_args& a, cudaStream_t s) {
     CUtensorMap tq, tk, tv;
     const long long units = (long long)a.B * a.H;
     if (!make_token_map(&tq, a.q, D, a.T, units) || !make_token_map(&tk, a.k, D, a.T, units) ||
         !make_token_map(&tv, a.v, D, a.T, units))
         return cudaErrorInvalidValue;
-    auto kern = tc_mlp_kernel<NC, CW, Tout, SURP>;
+    auto kern = tc_mlp_kernel<NC, CW, Tout, SURP, HUB>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -818,11 +820,17 @@ cudaError_t launch(const nm_config& c, const nm_args& a, cudaStream_t s) {
 
 template <int NC>
 cudaError_t launch_nc(const nm_config& c, const nm_args& a, cudaStream_t s) {
+    const bool hub = a.e_clip < HUGE_VALF;
+    if (c.out_dtype == NM_BF16) {
+        if (a.surprise)
+            return hub ? launch<NC, CW_DEFAULT, __nv_bfloat16, true, true>(c, a, s)
+                       : launch<NC, CW_DEFAULT, __nv_bfloat16, true, false>(c, a, s);
+        return hub ? launch<NC, CW_DEFAULT, __nv_bfloat16, false, true>(c, a, s)
+                   : launch<NC, CW_DEFAULT, __nv_bfloat16, false, false>(c, a, s);
+    }
     if (a.surprise)
-        return c.out_dtype == NM_BF16 ? launch<NC, CW_DEFAULT, __nv_bfloat16, true>(c, a, s)
-                                      : launch<NC, CW_DEFAULT, float, true>(c, a, s);
-    return c.out_dtype == NM_BF16 ? launch<NC, CW_DEFAULT, __nv_bfloat16, false>(c, a, s)
-                                  : launch<NC, CW_DEFAULT, float, false>(c, a, s);
+        return hub ? launch<NC, CW_DEFAULT, float, true, true>(c, a, s) : launch<NC, CW_DEFAULT, float, true, false>(c, a, s);
+    return hub ? launch<NC, CW_DEFAULT, float, false, true>(c, a, s) : launch<NC, CW_DEFAULT, float, false, false>(c, a, s);
 }
 
 }  // namespace
