@@ -435,7 +435,9 @@ def run_ours(args, rank, world, local_rank):
             "kernel": "nm_forward (%s path)" % ("tcgen05" if mem.path == nm.PATH_TC else "fp32 FFMA"),
             "per_launch_ms": per_launch_ms,
             "frac_tensor": alg["flops"] / (per_launch_ms * alg["calls"] * 1e-3) / (float(peaks["bf16_tflops"]) * 1e12),
-            "frac_hbm": alg["bytes"] / (per_launch_ms * alg["calls"] * 1e-3) / (float(peaks["hbm_gbs"]) * 1e9)}
+            "frac_hbm": alg["bytes"] / (per_launch_ms * alg["calls"] * 1e-3) / (float(peaks["hbm_gbs"]) * 1e9),
+            "frac_tensor_sustained": (alg["flops"] / (per_launch_ms * alg["calls"] * 1e-3)
+                                      / (float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])) * 1e12))}
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
         if seg != wl.T:
