@@ -13,6 +13,15 @@ inputs and device->host copies of y, M_T, S_T inside the timed region).
 
 ``--impl reference`` times the fp64 CPU oracle (the reference arm here) on
 the host cores, on a bounded sample of the same workload.
+
+Extra fields: ``roofline`` (the dominant kernel's algorithmic rate against the
+measured peak, with ``traffic`` from an ncu capture while the captured kernel
+source is unchanged), ``cpu_baseline`` (the oracle on a bounded sample),
+``clocks`` (SM clock and throttle reasons sampled during the timed region),
+``gpu_launches`` (this library's kernel launches in the timed region) and
+``variants`` (the same workload with the Huber loss and with the surprise
+output, a few steps each; ``--no-variants`` skips them).  ``--layers L`` runs
+an MLP workload with an L-layer memory.
 """
 from __future__ import annotations
 
