@@ -409,7 +409,8 @@ __global__ void __launch_bounds__(MLP_THREADS) simt_mlp_kernel(nm_args a, int d,
 // r the previous layer's retrieval activation (r = q_t for layer 1).
 
 __host__ __device__ inline size_t deep_unit_floats(int d, int h, int b, int L) {
-    return 2 * (size_t)b * b + 2 * (size_t)b + 4 * (size_t)b * d + (3 * (size_t)(L - 1) + 2) * (size_t)b * h;
+    const size_t P = 2 * (size_t)h * d + (size_t)(L - 2) * h * h;
+    return 2 * (size_t)b * b + 2 * (size_t)b + 4 * (size_t)b * d + (3 * (size_t)(L - 1) + 2) * (size_t)b * h + 2 * P;
 }
 __device__ __forceinline__ long long deep_off(int l, int d, int h) {  // offset of W_l in the packed parameters
     return l == 1 ? 0 : (long long)h * d + (long long)(l - 2) * h * h;
@@ -441,6 +442,9 @@ __global__ void __launch_bounds__(MLP_THREADS) simt_deep_kernel(nm_args a, int d
     float* Dl = X + (L - 1) * bh;      // [L-1][b][h] delta_l of the hidden layers
     float* R = Dl + (L - 1) * bh;      // [2][b][h]   retrieval activations (ping-pong)
     float* Pm = R + 2 * bh;            // [b][b]   Gamma (.) inner products of the current layer
+    float* Wt = Pm + (size_t)b * b;    // [P] the chunk-start weights, each layer transposed to [in][out],
+    float* St = Wt + P;                // [P] and the momentum likewise: consecutive threads (consecutive
+                                       //     outputs) then read consecutive addresses
 
     const Tin* q = (const Tin*)a.q + unit * T * d;
     const Tin* k = (const Tin*)a.k + unit * T * d;
@@ -497,15 +501,26 @@ __global__ void __launch_bounds__(MLP_THREADS) simt_deep_kernel(nm_args a, int d
             }
         }
         __syncthreads();
+        // the chunk-start W_l and S_l transposed ([out][in] -> [in][out])
+        for (int l = 1; l <= L; ++l) {
+            const int in = l == 1 ? d : hd, out = l == L ? d : hd;
+            const long long o0 = deep_off(l, d, hd);
+            for (int idx = tid; idx < out * in; idx += NT) {
+                const int j = idx / in, x = idx % in;
+                Wt[o0 + (long long)x * out + j] = Mw[o0 + idx];
+                St[o0 + (long long)x * out + j] = Sw[o0 + idx];
+            }
+        }
+        __syncthreads();
         // keys' forward at the chunk-start weights: z_l = W_l x_{l-1}, x_l = silu(z_l)
         for (int l = 1; l < L; ++l) {
             const int in = l == 1 ? d : hd;
             const float* xin = l == 1 ? Kf : X + (l - 2) * bh;
-            const float* Wl = Mw + deep_off(l, d, hd);
+            const float* Wtl = Wt + deep_off(l, d, hd);  // [in][h]
             for (int idx = tid; idx < n * hd; idx += NT) {
                 const int t = idx / hd, j = idx % hd;
                 float acc = 0.f;
-                for (int x = 0; x < in; ++x) acc = fmaf(xin[t * in + x], Wl[(long long)j * in + x], acc);
+                for (int x = 0; x < in; ++x) acc = fmaf(xin[t * in + x], Wtl[(long long)x * hd + j], acc);
                 Z[(l - 1) * bh + idx] = acc;
                 X[(l - 1) * bh + idx] = silu_f(acc);
             }
@@ -514,11 +529,11 @@ __global__ void __launch_bounds__(MLP_THREADS) simt_deep_kernel(nm_args a, int d
         // e = 2 (W_L x_{L-1} - v), clipped for the Huber loss
         {
             const float* xl = X + (L - 2) * bh;
-            const float* WL = Mw + deep_off(L, d, hd);
+            const float* WtL = Wt + deep_off(L, d, hd);  // [h][d]
             for (int idx = tid; idx < n * d; idx += NT) {
                 const int t = idx / d, o = idx % d;
                 float acc = 0.f;
-                for (int j = 0; j < hd; ++j) acc = fmaf(xl[t * hd + j], WL[(long long)o * hd + j], acc);
+                for (int j = 0; j < hd; ++j) acc = fmaf(xl[t * hd + j], WtL[(long long)j * d + o], acc);
                 E[idx] = nm_clip_err(2.0f * (acc - Vf[idx]), a.e_clip);
             }
             __syncthreads();
@@ -573,16 +588,16 @@ __global__ void __launch_bounds__(MLP_THREADS) simt_deep_kernel(nm_args a, int d
                 Pm[(size_t)t * b + i] = acc;
             }
             __syncthreads();
-            const float* Wl = Mw + deep_off(l, d, hd);
-            const float* Sl = Sw + deep_off(l, d, hd);
+            const float* Wtl = Wt + deep_off(l, d, hd);  // [in][out]
+            const float* Stl = St + deep_off(l, d, hd);
             float* rn = R + (l & 1) * bh;
             for (int idx = tid; idx < n * out; idx += NT) {
                 const int t = idx / out, j = idx % out;
                 float m = 0.f, s = 0.f, g = 0.f;
                 for (int x = 0; x < in; ++x) {
                     const float rx = r[t * in + x];
-                    m = fmaf(rx, Wl[(long long)j * in + x], m);
-                    s = fmaf(rx, Sl[(long long)j * in + x], s);
+                    m = fmaf(rx, Wtl[(long long)x * out + j], m);
+                    s = fmaf(rx, Stl[(long long)x * out + j], s);
                 }
                 for (int i = 0; i <= t; ++i) g = fmaf(Pm[(size_t)t * b + i], dl[i * out + j], g);
                 const float pre = sA[t] * m - sSg[t] * s - g;
