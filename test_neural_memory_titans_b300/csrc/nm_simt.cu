@@ -408,9 +408,12 @@ __global__ void __launch_bounds__(MLP_THREADS) simt_mlp_kernel(nm_args a, int d,
 // pre_l(t) = A_t W_l r - sigma_t S_l r - sum_i Gamma_{t,i} (x_{l-1,i} . r) delta_{l,i},
 // r the previous layer's retrieval activation (r = q_t for layer 1).
 
+// Every region of the deep kernel's workspace starts on a 16-byte boundary (float4 access).
+__host__ __device__ inline size_t round4(size_t n) { return (n + 3) & ~(size_t)3; }
 __host__ __device__ inline size_t deep_unit_floats(int d, int h, int b, int L) {
     const size_t P = 2 * (size_t)h * d + (size_t)(L - 2) * h * h;
-    return 2 * (size_t)b * b + 2 * (size_t)b + 4 * (size_t)b * d + (3 * (size_t)(L - 1) + 2) * (size_t)b * h + 2 * P;
+    return 2 * round4((size_t)b * b) + 2 * round4(b) + 4 * (size_t)b * d + (3 * (size_t)(L - 1) + 2) * (size_t)b * h +
+           2 * P;
 }
 __device__ __forceinline__ long long deep_off(int l, int d, int h) {  // offset of W_l in the packed parameters
     return l == 1 ? 0 : (long long)h * d + (long long)(l - 2) * h * h;
@@ -430,19 +433,19 @@ __global__ void __launch_bounds__(MLP_THREADS) simt_deep_kernel(nm_args a, int d
     const size_t bh = (size_t)b * hd;
 
     float* ws = (float*)a.scratch + unit * deep_unit_floats(d, hd, b, L);
-    float* Gam = ws;                   // [b][b]   Gamma_{t,i}
-    float* ub = Gam + (size_t)b * b;   // [b]      u_{n-1,i}
-    float* gl = ub + b;                // [b]      Gamma_{n-1,i}
-    float* Kf = gl + b;                // [b][d]
-    float* Qf = Kf + (size_t)b * d;    // [b][d]
-    float* Vf = Qf + (size_t)b * d;    // [b][d]
-    float* E = Vf + (size_t)b * d;     // [b][d]   e_t (the output layer's delta)
-    float* Z = E + (size_t)b * d;      // [L-1][b][h] pre-activations of the keys' forward
-    float* X = Z + (L - 1) * bh;       // [L-1][b][h] activations x_l of the keys' forward
-    float* Dl = X + (L - 1) * bh;      // [L-1][b][h] delta_l of the hidden layers
-    float* R = Dl + (L - 1) * bh;      // [2][b][h]   retrieval activations (ping-pong)
-    float* Pm = R + 2 * bh;            // [b][b]   Gamma (.) inner products of the current layer
-    float* Wt = Pm + (size_t)b * b;    // [P] the chunk-start weights, each layer transposed to [in][out],
+    float* Gam = ws;                          // [b][b]   Gamma_{t,i}
+    float* ub = Gam + round4((size_t)b * b);  // [b]      u_{n-1,i}
+    float* gl = ub + round4(b);               // [b]      Gamma_{n-1,i}
+    float* Kf = gl + round4(b);               // [b][d]
+    float* Qf = Kf + (size_t)b * d;           // [b][d]
+    float* Vf = Qf + (size_t)b * d;           // [b][d]
+    float* E = Vf + (size_t)b * d;            // [b][d]   e_t (the output layer's delta)
+    float* Z = E + (size_t)b * d;             // [L-1][b][h] pre-activations of the keys' forward
+    float* X = Z + (L - 1) * bh;              // [L-1][b][h] activations x_l of the keys' forward
+    float* Dl = X + (L - 1) * bh;             // [L-1][b][h] delta_l of the hidden layers
+    float* R = Dl + (L - 1) * bh;             // [2][b][h]   retrieval activations (ping-pong)
+    float* Pm = R + 2 * bh;                   // [b][b]   Gamma (.) inner products of the current layer
+    float* Wt = Pm + round4((size_t)b * b);   // [P] the chunk-start weights, each layer transposed to [in][out],
     float* St = Wt + P;                // [P] and the momentum likewise: consecutive threads (consecutive
                                        //     outputs) then read consecutive addresses
 
@@ -517,12 +520,20 @@ __global__ void __launch_bounds__(MLP_THREADS) simt_deep_kernel(nm_args a, int d
             const int in = l == 1 ? d : hd;
             const float* xin = l == 1 ? Kf : X + (l - 2) * bh;
             const float* Wtl = Wt + deep_off(l, d, hd);  // [in][h]
-            for (int idx = tid; idx < n * hd; idx += NT) {
-                const int t = idx / hd, j = idx % hd;
-                float acc = 0.f;
-                for (int x = 0; x < in; ++x) acc = fmaf(xin[t * in + x], Wtl[(long long)x * hd + j], acc);
-                Z[(l - 1) * bh + idx] = acc;
-                X[(l - 1) * bh + idx] = silu_f(acc);
+            const int h4 = hd / 4;
+            for (int idx = tid; idx < n * h4; idx += NT) {  // four consecutive outputs per thread
+                const int t = idx / h4, j = 4 * (idx % h4);
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int x = 0; x < in; ++x) {
+                    const float xv = xin[t * in + x];
+                    const float4 w = *reinterpret_cast<const float4*>(Wtl + (long long)x * hd + j);
+                    acc.x = fmaf(xv, w.x, acc.x); acc.y = fmaf(xv, w.y, acc.y);
+                    acc.z = fmaf(xv, w.z, acc.z); acc.w = fmaf(xv, w.w, acc.w);
+                }
+                float* zr = Z + (l - 1) * bh + (size_t)t * hd + j;
+                float* xr = X + (l - 1) * bh + (size_t)t * hd + j;
+                zr[0] = acc.x; zr[1] = acc.y; zr[2] = acc.z; zr[3] = acc.w;
+                xr[0] = silu_f(acc.x); xr[1] = silu_f(acc.y); xr[2] = silu_f(acc.z); xr[3] = silu_f(acc.w);
             }
             __syncthreads();
         }
@@ -530,11 +541,21 @@ __global__ void __launch_bounds__(MLP_THREADS) simt_deep_kernel(nm_args a, int d
         {
             const float* xl = X + (L - 2) * bh;
             const float* WtL = Wt + deep_off(L, d, hd);  // [h][d]
-            for (int idx = tid; idx < n * d; idx += NT) {
-                const int t = idx / d, o = idx % d;
-                float acc = 0.f;
-                for (int j = 0; j < hd; ++j) acc = fmaf(xl[t * hd + j], WtL[(long long)j * d + o], acc);
-                E[idx] = nm_clip_err(2.0f * (acc - Vf[idx]), a.e_clip);
+            const int d4 = d / 4;
+            for (int idx = tid; idx < n * d4; idx += NT) {  // four consecutive outputs per thread
+                const int t = idx / d4, o = 4 * (idx % d4);
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int j = 0; j < hd; ++j) {
+                    const float xv = xl[t * hd + j];
+                    const float4 w = *reinterpret_cast<const float4*>(WtL + (long long)j * d + o);
+                    acc.x = fmaf(xv, w.x, acc.x); acc.y = fmaf(xv, w.y, acc.y);
+                    acc.z = fmaf(xv, w.z, acc.z); acc.w = fmaf(xv, w.w, acc.w);
+                }
+                const int e0 = t * d + o;
+                E[e0] = nm_clip_err(2.0f * (acc.x - Vf[e0]), a.e_clip);
+                E[e0 + 1] = nm_clip_err(2.0f * (acc.y - Vf[e0 + 1]), a.e_clip);
+                E[e0 + 2] = nm_clip_err(2.0f * (acc.z - Vf[e0 + 2]), a.e_clip);
+                E[e0 + 3] = nm_clip_err(2.0f * (acc.w - Vf[e0 + 3]), a.e_clip);
             }
             __syncthreads();
         }
@@ -543,11 +564,21 @@ __global__ void __launch_bounds__(MLP_THREADS) simt_deep_kernel(nm_args a, int d
             const int up_n = l + 1 == L ? d : hd;
             const float* up = l + 1 == L ? E : Dl + l * bh;
             const float* Wn = Mw + deep_off(l + 1, d, hd);  // [up_n][h]
-            for (int idx = tid; idx < n * hd; idx += NT) {
-                const int t = idx / hd, j = idx % hd;
-                float acc = 0.f;
-                for (int o = 0; o < up_n; ++o) acc = fmaf(up[t * up_n + o], Wn[(long long)o * hd + j], acc);
-                Dl[(l - 1) * bh + idx] = acc * dsilu_f(Z[(l - 1) * bh + idx]);
+            const int h4 = hd / 4;
+            for (int idx = tid; idx < n * h4; idx += NT) {  // four consecutive outputs per thread
+                const int t = idx / h4, j = 4 * (idx % h4);
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int o = 0; o < up_n; ++o) {
+                    const float u = up[t * up_n + o];
+                    const float4 w = *reinterpret_cast<const float4*>(Wn + (long long)o * hd + j);
+                    acc.x = fmaf(u, w.x, acc.x); acc.y = fmaf(u, w.y, acc.y);
+                    acc.z = fmaf(u, w.z, acc.z); acc.w = fmaf(u, w.w, acc.w);
+                }
+                const size_t z0 = (l - 1) * bh + (size_t)t * hd + j;
+                Dl[z0] = acc.x * dsilu_f(Z[z0]);
+                Dl[z0 + 1] = acc.y * dsilu_f(Z[z0 + 1]);
+                Dl[z0 + 2] = acc.z * dsilu_f(Z[z0 + 2]);
+                Dl[z0 + 3] = acc.w * dsilu_f(Z[z0 + 3]);
             }
             __syncthreads();
         }
@@ -591,18 +622,31 @@ __global__ void __launch_bounds__(MLP_THREADS) simt_deep_kernel(nm_args a, int d
             const float* Wtl = Wt + deep_off(l, d, hd);  // [in][out]
             const float* Stl = St + deep_off(l, d, hd);
             float* rn = R + (l & 1) * bh;
-            for (int idx = tid; idx < n * out; idx += NT) {
-                const int t = idx / out, j = idx % out;
-                float m = 0.f, s = 0.f, g = 0.f;
+            const int o4 = out / 4;
+            for (int idx = tid; idx < n * o4; idx += NT) {  // four consecutive outputs per thread
+                const int t = idx / o4, j = 4 * (idx % o4);
+                float mv[4] = {0.f, 0.f, 0.f, 0.f}, sv[4] = {0.f, 0.f, 0.f, 0.f}, gv[4] = {0.f, 0.f, 0.f, 0.f};
                 for (int x = 0; x < in; ++x) {
                     const float rx = r[t * in + x];
-                    m = fmaf(rx, Wtl[(long long)x * out + j], m);
-                    s = fmaf(rx, Stl[(long long)x * out + j], s);
+                    const float4 w = *reinterpret_cast<const float4*>(Wtl + (long long)x * out + j);
+                    const float4 st = *reinterpret_cast<const float4*>(Stl + (long long)x * out + j);
+                    mv[0] = fmaf(rx, w.x, mv[0]); mv[1] = fmaf(rx, w.y, mv[1]);
+                    mv[2] = fmaf(rx, w.z, mv[2]); mv[3] = fmaf(rx, w.w, mv[3]);
+                    sv[0] = fmaf(rx, st.x, sv[0]); sv[1] = fmaf(rx, st.y, sv[1]);
+                    sv[2] = fmaf(rx, st.z, sv[2]); sv[3] = fmaf(rx, st.w, sv[3]);
                 }
-                for (int i = 0; i <= t; ++i) g = fmaf(Pm[(size_t)t * b + i], dl[i * out + j], g);
-                const float pre = sA[t] * m - sSg[t] * s - g;
-                if (l < L) rn[idx] = silu_f(pre);
-                else st_out(y + (t0 + t) * d + j, pre);
+                for (int i = 0; i <= t; ++i) {
+                    const float pm = Pm[(size_t)t * b + i];
+                    const float4 dv = *reinterpret_cast<const float4*>(dl + (size_t)i * out + j);
+                    gv[0] = fmaf(pm, dv.x, gv[0]); gv[1] = fmaf(pm, dv.y, gv[1]);
+                    gv[2] = fmaf(pm, dv.z, gv[2]); gv[3] = fmaf(pm, dv.w, gv[3]);
+                }
+#pragma unroll
+                for (int c4 = 0; c4 < 4; ++c4) {
+                    const float pre = sA[t] * mv[c4] - sSg[t] * sv[c4] - gv[c4];
+                    if (l < L) rn[(size_t)t * out + j + c4] = silu_f(pre);
+                    else st_out(y + (t0 + t) * d + j + c4, pre);
+                }
             }
             __syncthreads();
             r = rn;
@@ -615,17 +659,28 @@ __global__ void __launch_bounds__(MLP_THREADS) simt_deep_kernel(nm_args a, int d
             const float* dl = l == L ? E : Dl + (l - 1) * bh;
             float* Wl = Mw + deep_off(l, d, hd);
             float* Sl = Sw + deep_off(l, d, hd);
-            for (int idx = tid; idx < out * in; idx += NT) {
-                const int j = idx / in, x = idx % in;
-                float gw = 0.f, gs = 0.f;
+            const int in4 = in / 4;
+            for (int idx = tid; idx < out * in4; idx += NT) {  // four consecutive inputs per thread
+                const int j = idx / in4, x = 4 * (idx % in4);
+                float gw[4] = {0.f, 0.f, 0.f, 0.f}, gs[4] = {0.f, 0.f, 0.f, 0.f};
                 for (int i = 0; i < n; ++i) {
-                    const float gx = dl[i * out + j] * xin[i * in + x];
-                    gw = fmaf(gl[i], gx, gw);
-                    gs = fmaf(ub[i], gx, gs);
+                    const float dj = dl[i * out + j];
+                    const float4 xv = *reinterpret_cast<const float4*>(xin + (size_t)i * in + x);
+                    const float xs[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+                    for (int c4 = 0; c4 < 4; ++c4) {
+                        const float gx = dj * xs[c4];
+                        gw[c4] = fmaf(gl[i], gx, gw[c4]);
+                        gs[c4] = fmaf(ub[i], gx, gs[c4]);
+                    }
                 }
-                const float w = Wl[idx], sv = Sl[idx];
-                Wl[idx] = An * w - sn * sv - gw;
-                Sl[idx] = Bn * sv + gs;
+#pragma unroll
+                for (int c4 = 0; c4 < 4; ++c4) {
+                    const long long e = (long long)j * in + x + c4;
+                    const float w = Wl[e], sv = Sl[e];
+                    Wl[e] = An * w - sn * sv - gw[c4];
+                    Sl[e] = Bn * sv + gs[c4];
+                }
             }
         }
         __syncthreads();
