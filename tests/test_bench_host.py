@@ -1,0 +1,85 @@
+"""Host-side logic of bench.py, on the CPU: the work model behind the roofline
+fractions, the staleness rule of the ncu traffic table, and the workload
+selection (sizes and depth overrides)."""
+import argparse
+import dataclasses
+import importlib.util
+import os
+
+import pytest
+
+from test_neural_memory_titans_b300 import workloads as W
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _bench():
+    spec = importlib.util.spec_from_file_location("bench_under_test", os.path.join(ROOT, "bench.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod
+
+
+def _args(**over):
+    base = dict(workload=1, B=None, H=None, T=None, layers=None)
+    base.update(over)
+    return argparse.Namespace(**base)
+
+
+def test_flop_model_matches_the_per_token_formulas():
+    b = _bench()
+    for wid in range(5):
+        wl = W.WORKLOADS[wid]
+        alg = b.algorithmic(wl)
+        d, h, c = wl.d, wl.hidden, wl.chunk
+        per_tok = 10 * d * d + 2 * (c + 1) * d if wl.kind == W.LINEAR else 22 * d * h + 2 * (c + 1) * (d + h)
+        assert alg["flops"] == pytest.approx(per_tok * wl.B * wl.H * wl.T, rel=1e-12)
+        assert alg["tokens"] == wl.B * wl.H * wl.T
+        assert alg["bound"] == ("hbm" if wl.kind == W.LINEAR else "tensor")
+    # an L-layer memory: 11 flops per parameter and token plus the causal products of every layer input
+    wl3 = dataclasses.replace(W.WORKLOADS[1], layers=3)
+    d, h, c = wl3.d, wl3.hidden, wl3.chunk
+    P = 2 * h * d + h * h
+    assert wl3.P == P
+    assert b.algorithmic(wl3)["flops"] == pytest.approx((11 * P + 2 * (c + 1) * (d + 2 * h)) * wl3.tokens, rel=1e-12)
+
+
+def test_bytes_model_counts_inputs_outputs_gates_and_state():
+    b = _bench()
+    wl = W.WORKLOADS[2]
+    alg = b.algorithmic(wl)
+    per_tok = 3 * wl.d * 2 + 12 + wl.d * 2
+    assert alg["bytes"] == per_tok * wl.tokens + 4 * wl.P * 4 * wl.B * wl.H
+    wl4 = W.WORKLOADS[4]  # streamed: the state crosses HBM once per segment call
+    calls = wl4.T // wl4.segment
+    assert b.algorithmic(wl4)["calls"] == calls
+
+
+def test_ncu_traffic_only_for_the_captured_source():
+    b = _bench()
+    for name, (files, digest, nbytes) in b.NCU_TRAFFIC.items():
+        got = b.ncu_traffic(name)
+        assert got in (None, nbytes)
+    saved = dict(b.NCU_TRAFFIC)
+    try:
+        name = next(iter(saved))
+        files, digest, nbytes = saved[name]
+        b.NCU_TRAFFIC[name] = (files, "0" * 16, nbytes)  # a capture of some other source
+        assert b.ncu_traffic(name) is None
+    finally:
+        b.NCU_TRAFFIC.clear()
+        b.NCU_TRAFFIC.update(saved)
+    assert b.ncu_traffic("no such workload") is None
+
+
+def test_workload_overrides():
+    b = _bench()
+    assert b.workload(_args()) is W.WORKLOADS[1]
+    small = b.workload(_args(B=1, H=2, T=128))
+    assert (small.B, small.H, small.T) == (1, 2, 128) and small.name != W.WORKLOADS[1].name
+    deep = b.workload(_args(layers=4))
+    assert deep.layers == 4 and deep.name.endswith("_L4") and deep.P == 2 * 64 * 256 + 2 * 256 * 256
+    short = b.workload(_args(workload=4, T=4096))  # a streamed workload below one segment runs as one call
+    assert short.segment == 0
+    with pytest.raises(SystemExit):
+        b.workload(_args(workload=2, layers=3))
