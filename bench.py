@@ -461,7 +461,7 @@ def run_ours(args, rank, world, local_rank):
                       "parallelism": "dp%d" % world,
                       "l2": "flushed between timed steps (256 MB write, outside the step's events)"},
            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
-           "clocks": clocks.summary(), "step_ms": {"min": min(step_ms), "max": max(step_ms)},
+           "clocks": clocks.summary(), "step_ms": {"min": min(step_ms), "median": statistics.median(step_ms), "max": max(step_ms)},
            "variants": variants}
     return out
 
