@@ -239,7 +239,9 @@ int nm_inject_missing_load(nm_handle_t h);
  *   Workspace: one file-scope device array of NM_NOALLOC_SCRATCH_BYTES,
  *   present on every GPU that loads this library until the process exits.
  *   A call needing more than that (B*H units of
- *   4*(2b^2 + 2b + 4bd + 4bh) bytes each) returns NM_ERR_TOO_LARGE with
+ *   4*(2b^2 + 2b + 4bd + 4bh) bytes each for two layers; for L > 2 layers
+ *   4*(2 r4(b^2) + 2 r4(b) + 4bd + (3L - 1)bh + 2P) with r4 rounding up to a
+ *   multiple of 4 and P the parameter count) returns NM_ERR_TOO_LARGE with
  *   nothing launched.  The first call on a device looks up the array's device
  *   address (cudaGetSymbolAddress, with that device current); make that first
  *   call before any stream capture.  Every call shares the array, which keeps
