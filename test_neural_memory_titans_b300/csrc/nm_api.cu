@@ -1,6 +1,7 @@
 // Host side of the C ABI declared in include/nm.h: argument validation,
 // aliasing rules, handle-owned device memory, dispatch to the kernel files.
 // No arithmetic of the method happens here.
+#include <algorithm>
 #include <stdlib.h>
 #include <string.h>
 
@@ -57,6 +58,25 @@ int select_path(const nm_config& c) {
     if (tc) return NM_PATH_TC;
     if (simt) return NM_PATH_SIMT;
     return -1;
+}
+
+// Streams and events of nm_forward_host's copy / compute overlap, created once per handle.
+int ensure_pipe(nm_handle* h) {
+    if (h->pipe_ready) return NM_OK;
+    bool ok = cudaStreamCreateWithFlags(&h->s_in, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaStreamCreateWithFlags(&h->s_out, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaEventCreateWithFlags(&h->ev_start, cudaEventDisableTiming) == cudaSuccess &&
+              cudaEventCreateWithFlags(&h->ev_end, cudaEventDisableTiming) == cudaSuccess;
+    for (int i = 0; ok && i < 4; ++i)
+        ok = cudaStreamCreateWithFlags(&h->s_comp[i], cudaStreamNonBlocking) == cudaSuccess &&
+             cudaEventCreateWithFlags(&h->ev_in[i], cudaEventDisableTiming) == cudaSuccess &&
+             cudaEventCreateWithFlags(&h->ev_done[i], cudaEventDisableTiming) == cudaSuccess;
+    if (!ok) {
+        cudaGetLastError();
+        return NM_ERR_CUDA;
+    }
+    h->pipe_ready = 1;
+    return NM_OK;
 }
 
 int ensure_workspace(nm_handle* h, size_t bytes) {
@@ -306,6 +326,79 @@ int nm_forward_host(nm_handle_t h, int B, int H, int T, const void* q, const voi
     float* dST = (float*)carve(st_b);
     void* dy = carve(out_b);
     cudaStream_t s = (cudaStream_t)stream;
+    // Copy / compute overlap: the units are split into up to four groups; group g's inputs go up on one stream,
+    // its forward runs on a stream of its own as soon as they have landed (the groups' kernels run side by side,
+    // each unit's chain being independent), and its outputs come back on a third stream while later groups'
+    // inputs are still being copied.  Used on the tensor-core path (no shared workspace) when every group's slice
+    // of every buffer starts on a 16-byte boundary.
+    const int groups = (int)std::min<size_t>(4, units);
+    if (h->path == NM_PATH_TC && T > 0 && groups > 1 && (T % 4) == 0 && (P % 4) == 0 &&
+        in_b + out_b >= ((size_t)8 << 20)) {
+        int prc = ensure_pipe(h);
+        if (prc != NM_OK) return prc;
+        const size_t in_u = (size_t)T * cfg.d * dtype_bytes(cfg.in_dtype), out_u = (size_t)T * cfg.d * dtype_bytes(cfg.out_dtype);
+        const size_t gate_u = (size_t)T * sizeof(float), st_u = P * sizeof(float);
+        // the staging buffers carved above, as byte pointers
+        char* pq = (char*)dq;
+        char* pk = (char*)dk;
+        char* pv = (char*)dv;
+        char* pa = (char*)da;
+        char* pe = (char*)de;
+        char* pb = (char*)db;
+        char* pc = (char*)dc;
+        char* pM0 = (char*)dM0;
+        char* pS0 = (char*)dS0;
+        char* pMT = (char*)dMT;
+        char* pST = (char*)dST;
+        char* py = (char*)dy;
+        if (cudaEventRecord(h->ev_start, s) != cudaSuccess) return NM_ERR_CUDA;
+        if (cudaStreamWaitEvent(h->s_in, h->ev_start, 0) != cudaSuccess) return NM_ERR_CUDA;
+        if (cudaStreamWaitEvent(h->s_out, h->ev_start, 0) != cudaSuccess) return NM_ERR_CUDA;
+        size_t u0 = 0;
+        for (int gi = 0; gi < groups; ++gi) {
+            const size_t nu = units / groups + ((size_t)gi < units % groups ? 1 : 0);
+            struct Cp { char* dst; const char* src; size_t n; } cin[] = {
+                {pq + u0 * in_u, (const char*)q + u0 * in_u, nu * in_u},
+                {pk + u0 * in_u, (const char*)k + u0 * in_u, nu * in_u},
+                {pv + u0 * in_u, (const char*)v + u0 * in_u, nu * in_u},
+                {pa + u0 * gate_u, (const char*)alpha + u0 * gate_u, nu * gate_u},
+                {pe + u0 * gate_u, (const char*)eta + u0 * gate_u, nu * gate_u},
+                {pb + u0 * gate_u, (const char*)beta + u0 * gate_u, nu * gate_u},
+                {pc + u0 * gate_u, need_c ? (const char*)c + u0 * gate_u : nullptr, need_c ? nu * gate_u : 0},
+                {pM0 + u0 * st_u, (const char*)M0 + u0 * st_u, nu * st_u},
+                {pS0 + u0 * st_u, (const char*)S0 + u0 * st_u, nu * st_u}};
+            for (auto& cp : cin)
+                if (cp.n && cudaMemcpyAsync(cp.dst, cp.src, cp.n, cudaMemcpyHostToDevice, h->s_in) != cudaSuccess)
+                    return NM_ERR_CUDA;
+            if (cudaEventRecord(h->ev_in[gi], h->s_in) != cudaSuccess) return NM_ERR_CUDA;
+            if (cudaStreamWaitEvent(h->s_comp[gi], h->ev_in[gi], 0) != cudaSuccess) return NM_ERR_CUDA;
+            int rc = forward_impl(h, 1, (int)nu, T, pq + u0 * in_u, pk + u0 * in_u, pv + u0 * in_u,
+                                  (const float*)(pa + u0 * gate_u), (const float*)(pe + u0 * gate_u),
+                                  (const float*)(pb + u0 * gate_u), need_c ? (const float*)(pc + u0 * gate_u) : nullptr,
+                                  (const float*)(pM0 + u0 * st_u), (const float*)(pS0 + u0 * st_u), py + u0 * out_u,
+                                  (float*)(pMT + u0 * st_u), (float*)(pST + u0 * st_u), nullptr, h->s_comp[gi]);
+            if (rc != NM_OK) return rc;
+            if (cudaEventRecord(h->ev_done[gi], h->s_comp[gi]) != cudaSuccess) return NM_ERR_CUDA;
+            if (cudaStreamWaitEvent(h->s_out, h->ev_done[gi], 0) != cudaSuccess) return NM_ERR_CUDA;
+            struct Cp cout_[] = {{(char*)y + u0 * out_u, py + u0 * out_u, nu * out_u},
+                                 {(char*)M_T + u0 * st_u, pMT + u0 * st_u, nu * st_u},
+                                 {(char*)S_T + u0 * st_u, pST + u0 * st_u, nu * st_u}};
+            for (auto& cp : cout_)
+                if (cudaMemcpyAsync(cp.dst, cp.src, cp.n, cudaMemcpyDeviceToHost, h->s_out) != cudaSuccess)
+                    return NM_ERR_CUDA;
+            u0 += nu;
+        }
+        if (cudaEventRecord(h->ev_end, h->s_out) != cudaSuccess) return NM_ERR_CUDA;
+        if (cudaStreamWaitEvent(s, h->ev_end, 0) != cudaSuccess) return NM_ERR_CUDA;
+        if (cudaStreamSynchronize(h->s_out) != cudaSuccess || cudaStreamSynchronize(s) != cudaSuccess) {
+            cudaGetLastError();
+            return NM_ERR_CUDA;
+        }
+        int st = 0;
+        if (cudaMemcpy(&st, h->d_status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return NM_ERR_CUDA;
+        if (st != 0) cudaMemset(h->d_status, 0, sizeof(int));
+        return st;
+    }
     struct Cp { void* dst; const void* src; size_t n; } ins[] = {
         {dq, q, T ? in_b : 0}, {dk, k, T ? in_b : 0}, {dv, v, T ? in_b : 0},
         {da, alpha, T ? gate_b : 0}, {de, eta, T ? gate_b : 0}, {db, beta, T ? gate_b : 0},
@@ -342,6 +435,17 @@ int nm_destroy(nm_handle_t h) {
             }
             if (h->workspace) cudaFree(h->workspace);
             if (h->stage) cudaFree(h->stage);
+            if (h->pipe_ready) {
+                cudaStreamDestroy(h->s_in);
+                cudaStreamDestroy(h->s_out);
+                cudaEventDestroy(h->ev_start);
+                cudaEventDestroy(h->ev_end);
+                for (int i = 0; i < 4; ++i) {
+                    cudaStreamDestroy(h->s_comp[i]);
+                    cudaEventDestroy(h->ev_in[i]);
+                    cudaEventDestroy(h->ev_done[i]);
+                }
+            }
             if (h->d_status) cudaFree(h->d_status);
         } else {
             rc = NM_ERR_CUDA;

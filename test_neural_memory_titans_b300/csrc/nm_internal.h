@@ -51,6 +51,11 @@ struct nm_handle {
     size_t stage_bytes;
     long long launches;
     int inject_load_skip;  // armed by nm_inject_missing_load, consumed by the next nm_forward
+    // nm_forward_host's copy / compute overlap (created on first use): streams for the
+    // host->device and device->host copies and one compute stream per group of units
+    int pipe_ready;
+    cudaStream_t s_in, s_out, s_comp[4];
+    cudaEvent_t ev_start, ev_end, ev_in[4], ev_done[4];
 };
 
 // The |e| bound of a configuration (see nm_clip_err).
