@@ -2,14 +2,17 @@
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload I] [--impl ours|reference]
 
-A step is one full forward over the workload (for the streamed workload, all
-of its segment calls, carrying the state in place).  Inputs are resident in
-HBM before timing; L2 is flushed (a 256 MB write) between timed steps, outside
-each step's CUDA-event pair.  ``value`` is B*H*T tokens per second over all
-ranks (weak scaling: every rank runs its own copy of the workload with its own
-seed, no collective on the data path).  ``e2e`` measures the same metric
-through nm_forward_host with pinned host buffers (host->device copies of the
-inputs and device->host copies of y, M_T, S_T inside the timed region).
+The headline workload is the largest configuration (2-layer MLP memory
+128 -> 512 -> 128, B=2, H=16, T=131072, chunk 64).  A step is one full forward
+over the workload (for the streamed workload, all of its segment calls,
+carrying the state in place).  Inputs are resident in HBM before timing; L2 is
+flushed (a 256 MB write) between timed steps, outside each step's CUDA-event
+pair.  ``value`` is B*H*T tokens per second over all ranks (weak scaling:
+every rank runs its own copy of the workload with its own seed, no collective
+on the data path).  ``e2e`` measures the same metric through nm_forward_host
+with pinned host buffers (host->device copies of the inputs and device->host
+copies of y, M_T, S_T inside the timed region), with ``e2e.link`` the pinned
+copy bandwidth of the same byte counts measured alone in the same run.
 
 ``--impl reference`` times the fp64 CPU oracle (the reference arm here) on
 the host cores, on a bounded sample of the same workload.
@@ -18,10 +21,16 @@ Extra fields: ``roofline`` (the dominant kernel's algorithmic rate against the
 measured peak, with ``traffic`` from an ncu capture while the captured kernel
 source is unchanged), ``cpu_baseline`` (the oracle on a bounded sample),
 ``clocks`` (SM clock and throttle reasons sampled during the timed region),
-``gpu_launches`` (this library's kernel launches in the timed region) and
+``gpu_launches`` (this library's kernel launches in the timed region),
 ``variants`` (the same workload with the Huber loss and with the surprise
-output, a few steps each; ``--no-variants`` skips them).  ``--layers L`` runs
-an MLP workload with an L-layer memory.
+output, a few steps each; ``--no-variants`` skips them) and ``per_workload``
+(the other configurations timed in the same run, each with its own roofline
+fraction and clocks; the streamed one adds the needle-retrieval cosine;
+``--no-per-workload`` skips them).  ``--layers L`` runs an MLP workload with an
+L-layer memory.
+
+``--gpus N`` without a launcher starts N ranks itself (torch.distributed.run on
+127.0.0.1); under a launcher, N must equal WORLD_SIZE.
 """
 from __future__ import annotations
 
@@ -62,7 +71,7 @@ def ncu_traffic(workload_name: str):
                   "rb") as fh:
             h.update(fh.read())
     return nbytes if h.hexdigest()[:16] == digest else None
-DEFAULT_WORKLOAD = 1
+DEFAULT_WORKLOAD = 3
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 
 
@@ -270,57 +279,71 @@ def workload(args):
     return dataclasses.replace(wl, name="%s@B%dH%dT%d" % (wl.name, wl.B, wl.H, wl.T))
 
 
-def run_ours(args, rank, world, local_rank):
-    import test_neural_memory_titans_b300 as nm
-    from test_neural_memory_titans_b300 import workloads as W
+class Runner:
+    """One workload on one device: inputs resident in HBM, a handle, and a
+    ``step`` that runs one full forward (all segment calls of a streamed
+    workload, the state carried in place)."""
 
-    dev = torch.device("cuda", local_rank)
-    torch.cuda.set_device(dev)
-    wl = workload(args)
-    x = W.make_inputs(wl, dev, seed=1000 + args.workload + 100 * rank)
-    mem = nm.NeuralMemory(wl.kind, wl.d, wl.hidden, wl.chunk, in_dtype=wl.dtype, path=args.path, device=local_rank,
-                          layers=wl.layers if wl.kind == nm.MLP2 else 0)
-    stream = torch.cuda.current_stream(dev)
-    y = torch.empty(x["q"].shape, dtype=wl.dtype, device=dev)
-    M = torch.empty_like(x["M0"])
-    S = torch.empty_like(x["S0"])
-    seg = wl.segment if wl.segment else wl.T
+    def __init__(self, wl, dev, stream, seed, path, layers):
+        import test_neural_memory_titans_b300 as nm
+        from test_neural_memory_titans_b300 import workloads as W
 
-    def step():
-        if seg == wl.T:
-            mem.forward(x["q"], x["k"], x["v"], x["alpha"], x["eta"], x["beta"], x["M0"], x["S0"],
-                        y=y, M_T=M, S_T=S, stream=stream)
+        self.wl, self.dev, self.stream = wl, dev, stream
+        x = W.make_inputs(wl, dev, seed=seed)
+        self.x = x
+        self.mem = nm.NeuralMemory(wl.kind, wl.d, wl.hidden, wl.chunk, in_dtype=wl.dtype, path=path,
+                                   device=dev.index, layers=layers if wl.kind == nm.MLP2 else 0)
+        self.y = torch.empty(x["q"].shape, dtype=wl.dtype, device=dev)
+        self.M = torch.empty_like(x["M0"])
+        self.S = torch.empty_like(x["S0"])
+        self.seg = wl.segment if wl.segment else wl.T
+        self.segs = {}
+        if self.seg != wl.T:  # contiguous per-segment views prepared once, outside timing
+            for key in ("q", "k", "v", "alpha", "eta", "beta"):
+                self.segs[key] = {s0: x[key][:, :, s0:s0 + self.seg].contiguous() for s0 in range(0, wl.T, self.seg)}
+            self.segs["y"] = {s0: torch.empty((wl.B, wl.H, self.seg, wl.d), dtype=wl.dtype, device=dev)
+                              for s0 in range(0, wl.T, self.seg)}
+            del x["q"], x["k"], x["v"]
+
+    def step(self):
+        x, wl, segs = self.x, self.wl, self.segs
+        if self.seg == wl.T:
+            self.mem.forward(x["q"], x["k"], x["v"], x["alpha"], x["eta"], x["beta"], x["M0"], x["S0"],
+                             y=self.y, M_T=self.M, S_T=self.S, stream=self.stream)
         else:
-            M.copy_(x["M0"])
-            S.copy_(x["S0"])
-            for s0 in range(0, wl.T, seg):
-                sl = lambda t: t[:, :, s0:s0 + seg]
-                mem.forward(segs["q"][s0], segs["k"][s0], segs["v"][s0], segs["alpha"][s0], segs["eta"][s0],
-                            segs["beta"][s0], M, S, y=segs["y"][s0], M_T=M, S_T=S, stream=stream)
+            self.M.copy_(x["M0"])
+            self.S.copy_(x["S0"])
+            for s0 in range(0, wl.T, self.seg):
+                self.mem.forward(segs["q"][s0], segs["k"][s0], segs["v"][s0], segs["alpha"][s0], segs["eta"][s0],
+                                 segs["beta"][s0], self.M, self.S, y=segs["y"][s0], M_T=self.M, S_T=self.S,
+                                 stream=self.stream)
 
-    segs = {}
-    if seg != wl.T:  # contiguous per-segment views prepared once, outside timing
-        for key in ("q", "k", "v", "alpha", "eta", "beta"):
-            segs[key] = {s0: x[key][:, :, s0:s0 + seg].contiguous() for s0 in range(0, wl.T, seg)}
-        segs["y"] = {s0: torch.empty((wl.B, wl.H, seg, wl.d), dtype=wl.dtype, device=dev)
-                     for s0 in range(0, wl.T, seg)}
-        del x["q"], x["k"], x["v"]
+    def check_status(self, when: str):
+        import test_neural_memory_titans_b300 as nm
+        st = self.mem.synchronize()
+        if st != nm.NM_OK:
+            raise RuntimeError("device status %s: %s" % (when, nm.status_string(st)))
 
-    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
-    for _ in range(args.warmup):
+    def close(self):
+        self.mem.close()
+
+
+def time_steps(step, steps, warmup, flush, stream, dev, world, local_rank, check):
+    """W untimed warm-up steps, then K steps each bracketed by CUDA events on
+    the launching stream (L2 flushed before each, outside the events), with a
+    barrier and a device synchronisation on both sides of the timed region
+    and the SM clock sampled during it.  Returns the per-step times (ms) and
+    the clock summary."""
+    for _ in range(warmup):
         step()
-    st = mem.synchronize()
-    if st != nm.NM_OK:
-        raise RuntimeError("device status after warm-up: %s" % nm.status_string(st))
-
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    check("after warm-up")
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize(dev)
-    l0 = mem.launches
     with ClockSampler(local_rank) as clocks:
-        for i in range(args.steps):
+        for i in range(steps):
             flush.zero_()
             starts[i].record(stream)
             step()
@@ -328,11 +351,113 @@ def run_ours(args, rank, world, local_rank):
         torch.cuda.synchronize(dev)
     if world > 1:
         torch.distributed.barrier()
+    check("after timing")
+    return [s_.elapsed_time(e_) for s_, e_ in zip(starts, ends)], clocks.summary()
+
+
+def roofline(wl, ms, path_tc, peaks, peak_src, traffic):
+    """The dominant kernel's algorithmic rate per launch against the measured peak."""
+    alg = algorithmic(wl)
+    per_launch_ms = ms / alg["calls"]
+    if alg["bound"] == "tensor":
+        achieved = alg["flops"] / alg["calls"] / (per_launch_ms * 1e-3) / 1e12
+        peak = float(peaks["bf16_tflops"])
+        unit = "TFLOP/s"
+    else:
+        achieved = alg["bytes"] / alg["calls"] / (per_launch_ms * 1e-3) / 1e9
+        peak = float(peaks["hbm_gbs"])
+        unit = "GB/s"
+    secs = per_launch_ms * alg["calls"] * 1e-3
+    return {"bound": "hbm" if alg["bound"] == "hbm" else "tensor", "achieved": achieved, "peak": peak, "unit": unit,
+            "frac": achieved / peak, "traffic": traffic,
+            "peak_source": peak_src + " (burst)",
+            "kernel": "nm_forward (%s path)" % ("tcgen05" if path_tc else "fp32 FFMA"),
+            "per_launch_ms": per_launch_ms,
+            "algorithmic_flops_per_launch": alg["flops"] / alg["calls"],
+            "algorithmic_bytes_per_launch": alg["bytes"] / alg["calls"],
+            "frac_tensor": alg["flops"] / secs / (float(peaks["bf16_tflops"]) * 1e12),
+            "frac_hbm": alg["bytes"] / secs / (float(peaks["hbm_gbs"]) * 1e9),
+            "frac_tensor_sustained": (alg["flops"] / secs
+                                      / (float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])) * 1e12))}
+
+
+def needle_cosine(r) -> dict:
+    """Retrieval diagnostic of the streamed workload: for every needle
+    (position p, later probe p' whose query is k_p), the cosine between the
+    memory's output y_{p'} and the stored value v_p, from the last step's y."""
+    pos, probe = r.x["needles"]
+    wl = r.wl
+    y = torch.cat([r.segs["y"][s0] for s0 in sorted(r.segs["y"])], dim=2).reshape(wl.B * wl.H, wl.T, wl.d)
+    v = torch.cat([r.segs["v"][s0] for s0 in sorted(r.segs["v"])], dim=2).reshape(wl.B * wl.H, wl.T, wl.d)
+    pos = pos.reshape(wl.B * wl.H, -1)
+    probe = probe.reshape(wl.B * wl.H, -1)
+    rows = torch.arange(wl.B * wl.H, device=y.device).unsqueeze(1).expand_as(pos)
+    yp = y[rows, probe].float()
+    vp = v[rows, pos].float()
+    cos = torch.nn.functional.cosine_similarity(yp, vp, dim=-1)
+    # the same cosine against a value that was never stored at that key (a random other needle's value)
+    perm = torch.roll(torch.arange(pos.shape[1], device=y.device), 1)
+    cos0 = torch.nn.functional.cosine_similarity(yp, vp[:, perm], dim=-1)
+    return {"needles": int(cos.numel()), "mean_cosine": float(cos.mean()), "median_cosine": float(cos.median()),
+            "mean_cosine_unrelated_value": float(cos0.mean())}
+
+
+def link_bandwidth(dev, stream, h2d_bytes, d2h_bytes, reps=3):
+    """Pinned host <-> device copy rate for the e2e byte counts, measured alone:
+    one cudaMemcpyAsync per direction (torch copy_ from / to pinned memory),
+    each direction alone and both at once on two streams."""
+    hsrc = torch.empty(h2d_bytes, dtype=torch.uint8, pin_memory=True)
+    ddst = torch.empty(h2d_bytes, dtype=torch.uint8, device=dev)
+    dsrc = torch.empty(d2h_bytes, dtype=torch.uint8, device=dev)
+    hdst = torch.empty(d2h_bytes, dtype=torch.uint8, pin_memory=True)
+    s2 = torch.cuda.Stream(dev)
+
+    def timed(fn):
+        best = None
+        for _ in range(reps):
+            torch.cuda.synchronize(dev)
+            t0 = time.perf_counter()
+            fn()
+            torch.cuda.synchronize(dev)
+            dt = time.perf_counter() - t0
+            best = dt if best is None else min(best, dt)
+        return best
+
+    def h2d():
+        with torch.cuda.stream(stream):
+            ddst.copy_(hsrc, non_blocking=True)
+
+    def d2h():
+        with torch.cuda.stream(s2):
+            hdst.copy_(dsrc, non_blocking=True)
+
+    def both():
+        h2d()
+        d2h()
+
+    t_in, t_out, t_both = timed(h2d), timed(d2h), timed(both)
+    return {"h2d_gbs": h2d_bytes / t_in / 1e9, "d2h_gbs": d2h_bytes / t_out / 1e9,
+            "both_directions_ms": t_both * 1e3, "h2d_ms": t_in * 1e3, "d2h_ms": t_out * 1e3,
+            "note": "pinned copies of the e2e byte counts alone (best of %d); the e2e step cannot be faster "
+                    "than both_directions_ms" % reps}
+
+
+def run_ours(args, rank, world, local_rank):
+    import test_neural_memory_titans_b300 as nm
+    from test_neural_memory_titans_b300 import workloads as W
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    wl = workload(args)
+    r = Runner(wl, dev, stream, 1000 + args.workload + 100 * rank, args.path, wl.layers)
+    mem, x, y, M, S, seg = r.mem, r.x, r.y, r.M, r.S, r.seg
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+
+    l0 = mem.launches
+    step_ms, clocks = time_steps(r.step, args.steps, args.warmup, flush, stream, dev, world, local_rank,
+                                 r.check_status)
     launches = mem.launches - l0
-    st = mem.synchronize()
-    if st != nm.NM_OK:
-        raise RuntimeError("device status after timing: %s" % nm.status_string(st))
-    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     ms = sum(step_ms) / len(step_ms)
     if world > 1:
         t = torch.tensor([ms], dtype=torch.float64, device=dev)
@@ -372,6 +497,7 @@ def run_ours(args, rank, world, local_rank):
             if st != nm.NM_OK:
                 raise RuntimeError("device status after the variants: %s" % nm.status_string(st))
         mem_h.close()
+        del sur
         variants = {"huber_loss": {"ms_per_step": v_h, "value": world * tokens / (v_h * 1e-3), "delta": 0.1},
                     "surprise_output": {"ms_per_step": v_s, "value": world * tokens / (v_s * 1e-3)},
                     "steps": n_var, "note": "nm_config.loss = NM_LOSS_HUBER; nm_forward_surprise"}
@@ -394,9 +520,12 @@ def run_ours(args, rank, world, local_rank):
         h2d = sum(t.numel() * t.element_size() for t in hargs)
         d2h = hy.numel() * hy.element_size() + hM.numel() * 4 + hS.numel() * 4
         e2e = {"value": world * tokens / e_s, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h, "ms_per_step": e_s * 1e3}
+               "d2h_bytes_per_step": d2h, "ms_per_step": e_s * 1e3,
+               "link": link_bandwidth(dev, stream, h2d, d2h)}
+        del hx, hy, hM, hS, hargs
     elif not args.no_e2e:
         # streamed: one host-buffer call per segment, the state carried on the host from call to call
+        segs = r.segs
         keys = ("q", "k", "v", "alpha", "eta", "beta")
         hseg = {k: {s0: segs[k][s0].cpu().pin_memory() for s0 in segs[k]} for k in keys}
         hy = {s0: torch.empty(segs["y"][s0].shape, dtype=wl.dtype, pin_memory=True) for s0 in segs["y"]}
@@ -424,45 +553,65 @@ def run_ours(args, rank, world, local_rank):
         d2h = sum(t.numel() * t.element_size() for t in hy.values()) + n_seg * (hM0.numel() + hS0.numel()) * 4
         e2e = {"value": world * tokens / e_s, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": e_s * 1e3,
-               "note": "one host-buffer call per segment; the state is carried on the host"}
+               "note": "one host-buffer call per segment; the state is carried on the host",
+               "link": link_bandwidth(dev, stream, h2d, d2h)}
+        del hseg, hy
 
     peaks, peak_src = load_peaks()
-    per_launch_ms = ms / alg["calls"]
-    if alg["bound"] == "tensor":
-        achieved = alg["flops"] / alg["calls"] / (per_launch_ms * 1e-3) / 1e12
-        peak = float(peaks["bf16_tflops"])
-        unit = "TFLOP/s"
-    else:
-        achieved = alg["bytes"] / alg["calls"] / (per_launch_ms * 1e-3) / 1e9
-        peak = float(peaks["hbm_gbs"])
-        unit = "GB/s"
-    roof = {"bound": "hbm" if alg["bound"] == "hbm" else "tensor", "achieved": achieved, "peak": peak, "unit": unit,
-            "frac": achieved / peak,
-            "traffic": args.traffic if args.traffic is not None else
-            (ncu_traffic(wl.name) if mem.path == nm.PATH_TC and (args.B, args.H, args.T) == (None, None, None) else None),
-            "peak_source": peak_src + " (burst)",
-            "kernel": "nm_forward (%s path)" % ("tcgen05" if mem.path == nm.PATH_TC else "fp32 FFMA"),
-            "per_launch_ms": per_launch_ms,
-            "frac_tensor": alg["flops"] / (per_launch_ms * alg["calls"] * 1e-3) / (float(peaks["bf16_tflops"]) * 1e12),
-            "frac_hbm": alg["bytes"] / (per_launch_ms * alg["calls"] * 1e-3) / (float(peaks["hbm_gbs"]) * 1e9),
-            "frac_tensor_sustained": (alg["flops"] / (per_launch_ms * alg["calls"] * 1e-3)
-                                      / (float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])) * 1e12))}
+    full_size = (args.B, args.H, args.T) == (None, None, None)
+    traffic = args.traffic if args.traffic is not None else (
+        ncu_traffic(wl.name) if mem.path == nm.PATH_TC and full_size else None)
+    roof = roofline(wl, ms, mem.path == nm.PATH_TC, peaks, peak_src, traffic)
+    needles = needle_cosine(r) if wl.keys == "needles" and seg != wl.T else None
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
         if seg != wl.T:
-            x["q"], x["k"], x["v"] = (torch.cat([segs[k][s] for s in sorted(segs[k])], dim=2) for k in ("q", "k", "v"))
+            x["q"], x["k"], x["v"] = (torch.cat([r.segs[k][s] for s in sorted(r.segs[k])], dim=2)
+                                      for k in ("q", "k", "v"))
         cpu = time_oracle(wl, x)
     out = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
            "vs_baseline": None, "dtype": "bf16" if mem.path == nm.PATH_TC else "f32", "data": "synthetic",
            "config": {"workload": wl.name, "memory": "linear" if wl.kind == 0 else "mlp2", "B": wl.B, "H": wl.H,
                       "T": wl.T, "d": wl.d, "hidden": wl.hidden, "chunk": wl.chunk,
-                      "layers": wl.layers if wl.kind == 1 else None, "segment": wl.segment or None, "in_dtype": str(wl.dtype).replace("torch.", ""),
+                      "layers": wl.layers if wl.kind == 1 else None, "segment": wl.segment or None,
+                      "in_dtype": str(wl.dtype).replace("torch.", ""),
                       "parallelism": "dp%d" % world,
                       "l2": "flushed between timed steps (256 MB write, outside the step's events)"},
            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
-           "clocks": clocks.summary(), "step_ms": {"min": min(step_ms), "median": statistics.median(step_ms), "max": max(step_ms)},
+           "clocks": clocks, "step_ms": {"min": min(step_ms), "median": statistics.median(step_ms),
+                                         "max": max(step_ms)},
            "variants": variants}
+    if needles is not None:
+        out["needle_retrieval"] = needles
+    r.close()
+    del r, x, y, M, S, mem
+
+    # the other configurations, timed in the same run (full size, same timing rules), rank 0 alone at N = 1
+    if world == 1 and not args.no_per_workload and full_size and args.layers is None:
+        per = []
+        for wid in sorted(W.WORKLOADS):
+            if wid == args.workload:
+                continue
+            wl2 = W.WORKLOADS[wid]
+            torch.cuda.empty_cache()
+            r2 = Runner(wl2, dev, stream, 1000 + wid, args.path, wl2.layers)
+            n_steps = max(3, min(args.steps, 200 if not wl2.segment else 10))
+            l0 = r2.mem.launches
+            ms2, clk2 = time_steps(r2.step, n_steps, max(3, min(args.warmup, 5)), flush, stream, dev, 1,
+                                   local_rank, r2.check_status)
+            m2 = sum(ms2) / len(ms2)
+            entry = {"workload": wl2.name, "ms_per_step": m2, "value": wl2.tokens / (m2 * 1e-3), "unit": "tokens/s",
+                     "steps": n_steps, "gpu_launches": r2.mem.launches - l0,
+                     "roofline": roofline(wl2, m2, r2.mem.path == nm.PATH_TC, peaks, peak_src,
+                                          ncu_traffic(wl2.name) if r2.mem.path == nm.PATH_TC else None),
+                     "clocks": clk2, "path": "tcgen05" if r2.mem.path == nm.PATH_TC else "fp32 FFMA"}
+            if wl2.keys == "needles" and r2.seg != wl2.T:
+                entry["needle_retrieval"] = needle_cosine(r2)
+            per.append(entry)
+            r2.close()
+            del r2
+        out["per_workload"] = per
     return out
 
 
@@ -507,6 +656,7 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-variants", action="store_true", help="skip timing the Huber-loss and surprise forms")
+    ap.add_argument("--no-per-workload", action="store_true", help="skip timing the other configurations")
     ap.add_argument("--layers", type=int, default=None,
                     help="MLP workloads: a memory of this many layers instead of 2 (fp32 FFMA kernel for > 2)")
     ap.add_argument("--cpu-budget", type=float, default=None,
@@ -518,9 +668,21 @@ def main():
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
 
+    if "WORLD_SIZE" not in os.environ and args.gpus > 1:
+        # no launcher: start one rank per GPU on this node and wait for them
+        import socket
+        import subprocess
+        with socket.socket() as so:
+            so.bind(("127.0.0.1", 0))
+            port = so.getsockname()[1]
+        cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", str(args.gpus),
+               "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.abspath(__file__)] + sys.argv[1:]
+        raise SystemExit(subprocess.call(cmd))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if world != args.gpus:
+        raise SystemExit("bench.py: --gpus %d but the launcher started %d rank(s) (WORLD_SIZE)" % (args.gpus, world))
     if world > 1:
         backend = "nccl" if args.impl == "ours" else "gloo"
         if args.impl == "ours":

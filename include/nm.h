@@ -242,9 +242,11 @@ int nm_inject_missing_load(nm_handle_t h);
  *   4*(2b^2 + 2b + 4bd + 4bh) bytes each for two layers; for L > 2 layers
  *   4*(2 r4(b^2) + 2 r4(b) + 4bd + (3L - 1)bh + 2P) with r4 rounding up to a
  *   multiple of 4 and P the parameter count) returns NM_ERR_TOO_LARGE with
- *   nothing launched.  The first call on a device looks up the array's device
- *   address (cudaGetSymbolAddress, with that device current); make that first
- *   call before any stream capture.  Every call shares the array, which keeps
+ *   nothing launched.  Every call looks up the array's device address on the
+ *   current device (cudaGetSymbolAddress); the first call on a device may load
+ *   the library's module there, so make that first call before any stream
+ *   capture.  The address is not cached, so calls stay correct after
+ *   cudaDeviceReset (which may move the array).  Every call shares the array, which keeps
  *   the previous call's contents (the kernel writes each workspace element
  *   before reading it, so nothing needs clearing); calls whose kernels overlap
  *   on the GPU race on it, so the caller must order them.  Bounded-wait

@@ -352,8 +352,18 @@ int nm_forward_host(nm_handle_t h, int B, int H, int T, const void* q, const voi
         char* pST = (char*)dST;
         char* py = (char*)dy;
         if (cudaEventRecord(h->ev_start, s) != cudaSuccess) return NM_ERR_CUDA;
-        if (cudaStreamWaitEvent(h->s_in, h->ev_start, 0) != cudaSuccess) return NM_ERR_CUDA;
-        if (cudaStreamWaitEvent(h->s_out, h->ev_start, 0) != cudaSuccess) return NM_ERR_CUDA;
+        // On an error after this point, earlier groups' copies and kernels may still be queued on the
+        // handle's streams, reading and writing the caller's host buffers and the staging buffer: wait
+        // for all of them before returning, so that nothing outlives the call.
+        auto drain = [&](int rc, int used) {
+            cudaStreamSynchronize(h->s_in);
+            for (int i = 0; i < used; ++i) cudaStreamSynchronize(h->s_comp[i]);
+            cudaStreamSynchronize(h->s_out);
+            cudaGetLastError();
+            return rc;
+        };
+        if (cudaStreamWaitEvent(h->s_in, h->ev_start, 0) != cudaSuccess) return drain(NM_ERR_CUDA, 0);
+        if (cudaStreamWaitEvent(h->s_out, h->ev_start, 0) != cudaSuccess) return drain(NM_ERR_CUDA, 0);
         size_t u0 = 0;
         for (int gi = 0; gi < groups; ++gi) {
             const size_t nu = units / groups + ((size_t)gi < units % groups ? 1 : 0);
@@ -369,27 +379,27 @@ int nm_forward_host(nm_handle_t h, int B, int H, int T, const void* q, const voi
                 {pS0 + u0 * st_u, (const char*)S0 + u0 * st_u, nu * st_u}};
             for (auto& cp : cin)
                 if (cp.n && cudaMemcpyAsync(cp.dst, cp.src, cp.n, cudaMemcpyHostToDevice, h->s_in) != cudaSuccess)
-                    return NM_ERR_CUDA;
-            if (cudaEventRecord(h->ev_in[gi], h->s_in) != cudaSuccess) return NM_ERR_CUDA;
-            if (cudaStreamWaitEvent(h->s_comp[gi], h->ev_in[gi], 0) != cudaSuccess) return NM_ERR_CUDA;
+                    return drain(NM_ERR_CUDA, gi);
+            if (cudaEventRecord(h->ev_in[gi], h->s_in) != cudaSuccess) return drain(NM_ERR_CUDA, gi);
+            if (cudaStreamWaitEvent(h->s_comp[gi], h->ev_in[gi], 0) != cudaSuccess) return drain(NM_ERR_CUDA, gi);
             int rc = forward_impl(h, 1, (int)nu, T, pq + u0 * in_u, pk + u0 * in_u, pv + u0 * in_u,
                                   (const float*)(pa + u0 * gate_u), (const float*)(pe + u0 * gate_u),
                                   (const float*)(pb + u0 * gate_u), need_c ? (const float*)(pc + u0 * gate_u) : nullptr,
                                   (const float*)(pM0 + u0 * st_u), (const float*)(pS0 + u0 * st_u), py + u0 * out_u,
                                   (float*)(pMT + u0 * st_u), (float*)(pST + u0 * st_u), nullptr, h->s_comp[gi]);
-            if (rc != NM_OK) return rc;
-            if (cudaEventRecord(h->ev_done[gi], h->s_comp[gi]) != cudaSuccess) return NM_ERR_CUDA;
-            if (cudaStreamWaitEvent(h->s_out, h->ev_done[gi], 0) != cudaSuccess) return NM_ERR_CUDA;
+            if (rc != NM_OK) return drain(rc, gi + 1);
+            if (cudaEventRecord(h->ev_done[gi], h->s_comp[gi]) != cudaSuccess) return drain(NM_ERR_CUDA, gi + 1);
+            if (cudaStreamWaitEvent(h->s_out, h->ev_done[gi], 0) != cudaSuccess) return drain(NM_ERR_CUDA, gi + 1);
             struct Cp cout_[] = {{(char*)y + u0 * out_u, py + u0 * out_u, nu * out_u},
                                  {(char*)M_T + u0 * st_u, pMT + u0 * st_u, nu * st_u},
                                  {(char*)S_T + u0 * st_u, pST + u0 * st_u, nu * st_u}};
             for (auto& cp : cout_)
                 if (cudaMemcpyAsync(cp.dst, cp.src, cp.n, cudaMemcpyDeviceToHost, h->s_out) != cudaSuccess)
-                    return NM_ERR_CUDA;
+                    return drain(NM_ERR_CUDA, gi + 1);
             u0 += nu;
         }
-        if (cudaEventRecord(h->ev_end, h->s_out) != cudaSuccess) return NM_ERR_CUDA;
-        if (cudaStreamWaitEvent(s, h->ev_end, 0) != cudaSuccess) return NM_ERR_CUDA;
+        if (cudaEventRecord(h->ev_end, h->s_out) != cudaSuccess) return drain(NM_ERR_CUDA, groups);
+        if (cudaStreamWaitEvent(s, h->ev_end, 0) != cudaSuccess) return drain(NM_ERR_CUDA, groups);
         if (cudaStreamSynchronize(h->s_out) != cudaSuccess || cudaStreamSynchronize(s) != cudaSuccess) {
             cudaGetLastError();
             return NM_ERR_CUDA;

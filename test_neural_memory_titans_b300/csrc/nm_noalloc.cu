@@ -13,42 +13,33 @@
 //
 // The array is NM_NOALLOC_SCRATCH_BYTES (16 MiB) and lives on every GPU that
 // loads this library until the process exits.  Host code must not pass the
-// array's name to a kernel: on the host the name is only a stand-in, so the
-// device address is looked up once per device with cudaGetSymbolAddress, with
-// that device current, on the first call made on that device.
+// array's name to a kernel: on the host the name is only a stand-in, so every
+// call looks the device address up with cudaGetSymbolAddress on the current
+// device.  The first call on a device may load the module there; later calls
+// are a host-side lookup that allocates nothing.  Looking it up every time
+// (rather than caching it) keeps the address right after cudaDeviceReset,
+// which rebuilds the context and may place the array elsewhere.
 //
 // Every call shares the array and it keeps the previous call's contents.  The
 // kernel writes every workspace element of a chunk before it reads it, so
 // nothing has to start at zero and no clearing is done.  Two calls whose
 // kernels overlap on the GPU (different streams, or different host threads on
 // the same device) race on the array: callers must order them.
-#include <mutex>
-
 #include "nm_internal.h"
 
 static __device__ __align__(256) unsigned char nm_noalloc_scratch[NM_NOALLOC_SCRATCH_BYTES];
 
 namespace {
 
-constexpr int kMaxDevices = 64;
-std::mutex g_mutex;
-void* g_scratch_addr[kMaxDevices];  // device address of the array, per device
-
-// Looks up the array's device address on the current device (first call per
-// device only).
-int scratch_address(int dev, void** out) {
-    if (dev < 0 || dev >= kMaxDevices) return NM_ERR_UNSUPPORTED;
-    std::lock_guard<std::mutex> lock(g_mutex);
-    if (!g_scratch_addr[dev]) {
-        void* p = nullptr;
-        cudaError_t e = cudaGetSymbolAddress(&p, nm_noalloc_scratch);
-        if (e != cudaSuccess || p == nullptr) {
-            cudaGetLastError();
-            return NM_ERR_CUDA;
-        }
-        g_scratch_addr[dev] = p;
+// The array's device address on the current device.
+int scratch_address(void** out) {
+    void* p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, nm_noalloc_scratch);
+    if (e != cudaSuccess || p == nullptr) {
+        cudaGetLastError();
+        return NM_ERR_CUDA;
     }
-    *out = g_scratch_addr[dev];
+    *out = p;
     return NM_OK;
 }
 
@@ -117,13 +108,8 @@ extern "C" int nm_forward_mlp2_noalloc(const nm_config* cfg, int B, int H, int T
         if (S_T != S0 && cudaMemcpyAsync(S_T, S0, st_b, cudaMemcpyDeviceToDevice, s) != cudaSuccess) return NM_ERR_CUDA;
         return NM_OK;
     }
-    int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess) {
-        cudaGetLastError();
-        return NM_ERR_CUDA;
-    }
     void* scratch = nullptr;
-    int rc = scratch_address(dev, &scratch);
+    int rc = scratch_address(&scratch);
     if (rc != NM_OK) return rc;
 
     nm_args a;

@@ -83,15 +83,36 @@ def pick(t: torch.Tensor, wl: W.Workload, units=None, T=None) -> np.ndarray:
     return f64(a)[None]
 
 
+def rel_l2_per_unit(x, ref) -> np.ndarray:
+    """Relative L2 of each unit (axis 1 of [1, U, ...] arrays) on its own."""
+    x = np.asarray(x, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    x = x.reshape(x.shape[0] * x.shape[1], -1)
+    ref = ref.reshape(ref.shape[0] * ref.shape[1], -1)
+    den = np.linalg.norm(ref, axis=1)
+    num = np.linalg.norm(x - ref, axis=1)
+    return np.where(den == 0.0, num, num / np.where(den == 0.0, 1.0, den))
+
+
 def compare(wl, gpu, ref, units=None, T=None, tol=None):
-    """Relative L2 of y, M_T, S_T; returns dict and asserts tolerances."""
+    """Relative L2 of y, M_T, S_T over the whole tensor and for the worst
+    unit (batch, head) on its own; returns both and asserts the tolerances
+    on each, so one bad unit cannot hide inside a whole-tensor norm."""
     tol = TOL[wl.dtype] if tol is None else tol
     y, MT, ST = gpu[:3]
-    out = {"y": rel_l2(pick(y, wl, units, T), ref[0]),
-           "M_T": rel_l2(pick(MT, wl, units), ref[1]),
-           "S_T": rel_l2(pick(ST, wl, units), ref[2])}
-    for key, val in out.items():
-        assert val <= tol[key], "%s rel L2 %.3e > %.1e (%s)" % (key, val, tol[key], out)
+    got = {"y": pick(y, wl, units, T), "M_T": pick(MT, wl, units), "S_T": pick(ST, wl, units)}
+    refs = {"y": ref[0], "M_T": ref[1], "S_T": ref[2]}
+    out = {key: rel_l2(got[key], refs[key]) for key in got}
+    worst = {}
+    for key in got:
+        per = rel_l2_per_unit(got[key], refs[key])
+        i = int(np.nanargmax(per)) if per.size and not np.all(np.isnan(per)) else 0
+        worst[key] = (float(per[i]) if per.size else 0.0, i)
+    out["worst_unit"] = worst
+    for key in ("y", "M_T", "S_T"):
+        assert out[key] <= tol[key], "%s rel L2 %.3e > %.1e (%s)" % (key, out[key], tol[key], out)
+        assert worst[key][0] <= tol[key], "%s worst-unit rel L2 %.3e (unit %d) > %.1e (%s)" % (
+            key, worst[key][0], worst[key][1], tol[key], out)
     return out
 
 
@@ -110,3 +131,43 @@ def chunks_as_units(wl: W.Workload, x: dict, chunk_ids, span: int, seed: int = 7
     M0, S0 = W.random_state(wl2, device=x["q"].device, seed=seed)
     out["M0"], out["S0"], out["c"] = M0, S0, None
     return wl2, out
+
+
+class ParityAccumulator:
+    """Relative L2 accumulated over pieces of a large comparison (groups of
+    units, or successive segments of the same units), so that the oracle can
+    run piece by piece: per unit the squared error and squared reference norm
+    are summed; ``check`` asserts the whole-tensor and worst-unit values."""
+
+    def __init__(self, n_units: int):
+        self.n = n_units
+        self.num = {}
+        self.den = {}
+
+    def add(self, key: str, got, ref, unit_ids) -> None:
+        got = np.asarray(got, dtype=np.float64)
+        ref = np.asarray(ref, dtype=np.float64)
+        u = len(unit_ids)
+        g = got.reshape(u, -1)
+        r = ref.reshape(u, -1)
+        if key not in self.num:
+            self.num[key] = np.zeros(self.n)
+            self.den[key] = np.zeros(self.n)
+        idx = np.asarray(unit_ids)
+        self.num[key][idx] += np.sum((g - r) ** 2, axis=1)
+        self.den[key][idx] += np.sum(r ** 2, axis=1)
+
+    def check(self, tol: dict) -> dict:
+        out, worst = {}, {}
+        for key in self.num:
+            num, den = self.num[key], self.den[key]
+            out[key] = float(np.sqrt(num.sum() / den.sum())) if den.sum() > 0 else float(np.sqrt(num.sum()))
+            per = np.sqrt(num / np.where(den > 0, den, 1.0))
+            i = int(np.argmax(per))
+            worst[key] = (float(per[i]), i)
+        out["worst_unit"] = worst
+        for key in self.num:
+            assert out[key] <= tol[key], "%s rel L2 %.3e > %.1e (%s)" % (key, out[key], tol[key], out)
+            assert worst[key][0] <= tol[key], "%s worst-unit rel L2 %.3e (unit %d) > %.1e (%s)" % (
+                key, worst[key][0], worst[key][1], tol[key], out)
+        return out

@@ -30,3 +30,28 @@ def test_reference_arm_two_gloo_ranks():
     assert out["impl"] == "reference" and out["n_gpus"] == 2 and out["steps"] == 2
     assert out["value"] > 0 and out["cpu_baseline"]["kind"] == "oracle"
     assert out["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_gpus_flag_starts_its_own_ranks():
+    """``--gpus 2`` without a launcher starts two ranks itself; rank 0 alone
+    prints the line, with n_gpus = 2."""
+    cmd = [sys.executable, "bench.py", "--impl", "reference", "--gpus", "2", "--steps", "1", "--warmup", "1",
+           "--workload", "0", "--cpu-budget", "0.2"]
+    env = {k: v for k, v in os.environ.items() if k not in ("WORLD_SIZE", "RANK", "LOCAL_RANK")}
+    env["OMP_NUM_THREADS"] = "2"
+    r = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=300, env=env)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    assert json.loads(lines[0])["n_gpus"] == 2
+
+
+def test_gpus_flag_must_match_the_launcher():
+    """Under a launcher whose WORLD_SIZE differs from --gpus, the bench fails
+    loudly instead of reporting another rank count."""
+    cmd = [sys.executable, "bench.py", "--impl", "reference", "--gpus", "2", "--steps", "1", "--workload", "0"]
+    env = dict(os.environ, WORLD_SIZE="1", RANK="0", LOCAL_RANK="0")
+    r = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=300, env=env)
+    assert r.returncode != 0
+    assert "WORLD_SIZE" in r.stderr
+    assert not [l for l in r.stdout.splitlines() if l.startswith("{")]

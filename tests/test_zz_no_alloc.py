@@ -3,11 +3,15 @@ allocate device memory (a host that owns the whole device through its own
 pool, or a loop that cannot take cudaMalloc's device-wide synchronisation).
 
 It runs the fp32 FFMA MLP kernel with its workspace in a fixed file-scope
-device array instead of a handle's allocation.  The test calls it through the
-C ABI and checks it against the handle-based nm_forward on the same inputs,
-within the bf16 tolerances the parity tests use, on two calls in a row (the
-second on other inputs, over the array left behind by the first).  It also
-checks that a call needing more than the array returns NM_ERR_TOO_LARGE.
+device array instead of a handle's allocation.  The kernel and its arithmetic
+are the same as nm_forward's on the fp32 FFMA path, so the tests call it
+through the C ABI and require the result to equal nm_forward's bit for bit
+(a workspace-offset mistake that perturbs the result slightly would not pass
+a tolerance-free comparison): two calls in a row on different inputs (the
+second over the array left behind by the first), then a deeper (3-layer)
+memory, whose workspace per unit is laid out differently.  They also check
+that calls needing more than the array return NM_ERR_TOO_LARGE, for the two-
+and the three-layer sizes.
 
 This file is named so that pytest collects it last.
 """
@@ -18,8 +22,6 @@ import torch
 
 import test_neural_memory_titans_b300 as nm
 from test_neural_memory_titans_b300 import workloads as W
-
-from _helpers import TOL, rel_l2
 
 pytestmark = pytest.mark.gpu
 
@@ -52,11 +54,31 @@ def _noalloc(cfg, x, M0, S0):
     return y, MT, ST
 
 
+def _deep_state(B, H, d, hidden, layers, seed):
+    """W_l ~ N(0, 0.5 / fan_in), S_l ~ 0.1 of that, packed W1, W2 .. W_L."""
+    g = torch.Generator("cuda").manual_seed(seed)
+    n = B * H
+    ms, ss = [], []
+    for li in range(layers):
+        out_f = d if li == layers - 1 else hidden
+        in_f = d if li == 0 else hidden
+        std = (0.5 / in_f) ** 0.5
+        ms.append(std * torch.randn((n, out_f * in_f), generator=g, device="cuda"))
+        ss.append(0.1 * std * torch.randn((n, out_f * in_f), generator=g, device="cuda"))
+    P = nm.param_count(nm.MLP2, d, hidden, layers)
+    return (torch.cat(ms, 1).reshape(B, H, P).contiguous(), torch.cat(ss, 1).reshape(B, H, P).contiguous())
+
+
+def _assert_bit_equal(got, ref, what):
+    for name, g, r in zip(("y", "M_T", "S_T"), got, ref):
+        assert torch.equal(g, r), "%s: %s differs from nm_forward (max |diff| %.3e)" % (
+            what, name, (g.float() - r.float()).abs().max().item())
+
+
 def test_noalloc_matches_nm_forward_twice():
     wl = W.WORKLOADS[1]
     cfg = nm._Config(nm.MLP2, wl.d, wl.hidden, wl.chunk, nm.BF16, nm.BF16, nm.C_ONE, nm.PATH_AUTO)
     mem = nm.NeuralMemory(wl.kind, wl.d, wl.hidden, wl.chunk, in_dtype=wl.dtype, path=nm.PATH_SIMT)
-    tol = TOL[torch.bfloat16]
     for call, (B, H, T, seed) in enumerate([(1, 3, 150, 1), (2, 2, 200, 2)]):
         w = wl.with_sizes(B=B, H=H, T=T)
         x = W.make_inputs(w, "cuda", seed=seed)
@@ -64,23 +86,56 @@ def test_noalloc_matches_nm_forward_twice():
         got = _noalloc(cfg, x, M0, S0)
         ref = mem.forward(x["q"], x["k"], x["v"], x["alpha"], x["eta"], x["beta"], M0, S0)
         assert mem.synchronize() == nm.NM_OK
-        for name, g, r in zip(("y", "M_T", "S_T"), got, ref):
-            err = rel_l2(g.double().cpu().numpy(), r.double().cpu().numpy())
-            assert err <= tol[name], "call %d: %s rel L2 %.3e" % (call, name, err)
+        _assert_bit_equal(got, ref, "call %d" % call)
     mem.close()
 
 
-def test_noalloc_rejects_calls_beyond_its_workspace():
-    wl = W.WORKLOADS[1]
-    per_unit = 4 * (2 * wl.chunk ** 2 + 2 * wl.chunk + 4 * wl.chunk * wl.d + 4 * wl.chunk * wl.hidden)
+def test_noalloc_deep_memory_matches_nm_forward():
+    """A 3-layer memory (64 -> 128 -> 128 -> 64) through the same entry point."""
+    d, hidden, chunk, layers = 64, 128, 64, 3
+    cfg = nm._Config(nm.MLP2, d, hidden, chunk, nm.BF16, nm.BF16, nm.C_ONE, nm.PATH_AUTO, nm.LOSS_L2, 0.0, layers)
+    mem = nm.NeuralMemory(nm.MLP2, d, hidden, chunk, in_dtype=torch.bfloat16, path=nm.PATH_SIMT, layers=layers)
+    w = W.WORKLOADS[1].with_sizes(B=1, H=3, T=130)
+    x = W.make_inputs(w, "cuda", seed=5)
+    x["eta"] *= 0.5
+    M0, S0 = _deep_state(1, 3, d, hidden, layers, seed=6)
+    got = _noalloc(cfg, x, M0, S0)
+    ref = mem.forward(x["q"], x["k"], x["v"], x["alpha"], x["eta"], x["beta"], M0, S0)
+    assert mem.synchronize() == nm.NM_OK
+    mem.close()
+    assert torch.isfinite(got[0].float()).all()
+    _assert_bit_equal(got, ref, "3-layer memory")
+
+
+def _round4(n):
+    return (n + 3) // 4 * 4
+
+
+@pytest.mark.parametrize("layers", [2, 3])
+def test_noalloc_rejects_calls_beyond_its_workspace(layers):
+    d, hidden, b = 64, 256 if layers == 2 else 128, 64
+    if layers == 2:
+        per_unit = 4 * (2 * b ** 2 + 2 * b + 4 * b * d + 4 * b * hidden)
+    else:
+        P = nm.param_count(nm.MLP2, d, hidden, layers)
+        per_unit = 4 * (2 * _round4(b * b) + 2 * _round4(b) + 4 * b * d + (3 * layers - 1) * b * hidden + 2 * P)
     H = SCRATCH_BYTES // per_unit + 1
-    w = wl.with_sizes(B=1, H=H, T=1)
+    w = W.WORKLOADS[1].with_sizes(B=1, H=H, T=1)
     x = W.make_inputs(w, "cuda", seed=3)
+    P = nm.param_count(nm.MLP2, d, hidden, layers)
+    M0 = torch.zeros((1, H, P), device="cuda")
+    S0 = torch.zeros_like(M0)
     y = torch.empty(x["q"].shape, dtype=torch.bfloat16, device="cuda")
-    MT = torch.empty_like(x["M0"])
-    ST = torch.empty_like(x["S0"])
-    cfg = nm._Config(nm.MLP2, wl.d, wl.hidden, wl.chunk, nm.BF16, nm.BF16, nm.C_ONE, nm.PATH_AUTO)
-    rc = _entry()(ctypes.byref(cfg), 1, H, 1, _p(x["q"]), _p(x["k"]), _p(x["v"]), _p(x["alpha"]), _p(x["eta"]),
-                  _p(x["beta"]), None, _p(x["M0"]), _p(x["S0"]), _p(y), _p(MT), _p(ST), None)
+    MT = torch.empty_like(M0)
+    ST = torch.empty_like(S0)
+    cfg = nm._Config(nm.MLP2, d, hidden, b, nm.BF16, nm.BF16, nm.C_ONE, nm.PATH_AUTO, nm.LOSS_L2, 0.0,
+                     0 if layers == 2 else layers)
+    args = (_p(x["q"]), _p(x["k"]), _p(x["v"]), _p(x["alpha"]), _p(x["eta"]), _p(x["beta"]), None)
+    rc = _entry()(ctypes.byref(cfg), 1, H, 1, *args, _p(M0), _p(S0), _p(y), _p(MT), _p(ST), None)
     assert rc == NM_ERR_TOO_LARGE
     assert "workspace" in nm.status_string(rc)
+    # one unit fewer fits
+    rc = _entry()(ctypes.byref(cfg), 1, H - 1, 1, *args, _p(M0[:, :H - 1]), _p(S0[:, :H - 1]), _p(y[:, :H - 1]),
+                  _p(MT[:, :H - 1]), _p(ST[:, :H - 1]), None)
+    assert rc == nm.NM_OK, nm.status_string(rc)
+    torch.cuda.synchronize()
