@@ -45,6 +45,29 @@
 // and sum_i P1 delta_i -> h, a_t -> G5 W2 a_t | S2 a_t, a_t . a(k_i) -> P2 ->
 // G6 P2 E -> y partials -> exchange -> y.  Then the new state becomes the
 // next chunk's bf16 operands.
+//
+// Precision of the gradient path.  Each operand of the products that build
+// the gradient and the state update (the chunk-start W1, W2 in the key
+// forward and backward, a(k), e, delta and the gamma / u scaled k and e) is
+// taken as a hi/lo pair of bf16 tiles, x = hi + lo with lo = bf16(x -
+// bf16(x)), and a product A B becomes A_hi B_hi + A_lo B_hi + A_hi B_lo
+// (three tensor-core products into one fp32 accumulator; q and k are exact in
+// bf16 and need no lo half).  The key forward W2 a(k) splits W2 only: the
+// a(k) lo term changes the state by two orders of magnitude less than the
+// others in the emulation.  The memory's own dynamics amplify rounding in
+// this path: with single bf16 operands, runs of a few thousand tokens leave
+// the fp32 tolerance of the state far behind (an fp64 emulation of the
+// rounding points put every one of these six operands at about the same
+// share).  Retrieval-only products (S1 q, W2 a_t, S2 a_t, the Gamma-weighted
+// inner products) keep single bf16 operands.  The lo tiles reuse regions
+// that are dead while they live: W1 lo in the a(k) tile (end of the previous
+// chunk .. G1), W2 lo and then delta lo in the S1 copy (dead after G1), a(k)
+// lo in the q|k tile and e lo in the v tile (the next chunk's tiles load
+// after G4), -gamma e lo and u e lo in the W1 copy (dead after G1, rewritten
+// after G4), and -gamma k lo, u k lo in their own tiles (room made by
+// keeping Gamma in bf16: it only enters the bf16 P tiles).  The W2 / S2
+// updates are issued right behind G3 and run while E3 does, so that only the
+// W1 / S1 updates stand between delta and retrieval.
 #include <cuda_bf16.h>
 
 #include "nm_internal.h"
@@ -75,12 +98,22 @@ constexpr uint32_t OFF_E = OFF_KU + T64;      // [64 t][64 o]   e_t
 constexpr uint32_t OFF_EG = OFF_E + T64;      // -gamma_t e_t
 constexpr uint32_t OFF_EU = OFF_EG + T64;     // u_t e_t
 constexpr uint32_t OFF_P = OFF_EU + T64;      // [64 t][64 i]   Gamma (.) inner products
-constexpr int GS = 68;                        // padded fp32 row stride (conflict-free row reads)
-constexpr uint32_t OFF_GM = OFF_P + T64;                // fp32 Gamma [2 stages][64][GS]
-constexpr int XS = 72;                                  // bf16 row stride of the key-forward exchange
-constexpr int RB = 40;                                  // bf16 row stride of the y exchange
-constexpr uint32_t OFF_YX = OFF_GM + 2 * 64 * GS * 4;   // bf16 [64][XS] the peer's partial key forward
-constexpr uint32_t OFF_YR = OFF_YX + 64 * XS * 2;       // bf16 [64][RB] the peer's partial y (own columns)
+constexpr uint32_t OFF_KLO = OFF_P + T64;     // [2][64 t][64 x] lo halves of -gamma_t k_t, u_t k_t
+constexpr int XS = 72;                        // bf16 row stride of the key-forward exchange
+constexpr int RB = 40;                        // bf16 row stride of the y exchange
+constexpr uint32_t OFF_YX = OFF_KLO + 2 * T64;  // bf16 [64][XS] the peer's partial key forward (E2);
+                                                // then the u e lo tile [64 t][64 o] (E3 .. G4)
+constexpr int GST = 72;                         // bf16 row stride of Gamma
+constexpr uint32_t OFF_GM = OFF_YX + 64 * XS * 2;       // bf16 Gamma [2 stages][64][GST]
+constexpr uint32_t OFF_YR = OFF_GM + 2 * 64 * GST * 2;  // bf16 [64][RB] the peer's partial y (own columns)
+// lo halves living in regions that are dead meanwhile (see the file header)
+constexpr uint32_t OFF_W1LO = OFF_AK;   // [128 j][64 x]  W1 lo: E6 of the previous chunk .. G1
+constexpr uint32_t OFF_W2LO = OFF_S1;   // [128 j][64 o]  W2 lo (transposed): E1 .. G3
+constexpr uint32_t OFF_AKLO = OFF_QK;   // [128 j][64 t]  a(k) lo: E1 .. G4
+constexpr uint32_t OFF_ELO = OFF_V;     // [64 t][64 o]   e lo: E2 .. G3
+constexpr uint32_t OFF_EGLO = OFF_W1;   // [64 t][64 o]   -gamma e lo: E2 .. G4
+constexpr uint32_t OFF_EULO = OFF_W1 + T64;  // [64 t][64 o]   u e lo: E2 .. G4
+constexpr uint32_t OFF_DTLO = OFF_S1;   // [128 j][64 t]  delta lo: E3 .. G4
 constexpr uint32_t OFF_F = OFF_YR + 64 * RB * 2;        // gates [2][4][64]; scan [2][A, B, sigma, gamma, u][64]
 constexpr uint32_t N_F = 2 * 4 * BC + 2 * 5 * BC;
 constexpr uint32_t OFF_SP = OFF_F + 4 * N_F;  // surprise partials (fp32 [64] rows): ||a(k)||^2 [4 quadrants],
@@ -91,6 +124,8 @@ constexpr uint32_t SMEM_USED = OFF_BAR + 64;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;  // slack for the 1024-byte alignment
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 static_assert(OFF_S2 == OFF_W2 + T128, "W2 and S2 copies form one N=128 operand");
+static_assert(OFF_YX % 1024 == 0, "exchange buffer alignment");
+static_assert(OFF_GM % 16 == 0 && (GST * 2) % 16 == 0, "Gamma rows are read 16 bytes at a time");
 
 // TMEM columns
 constexpr uint32_t COL_W1 = 0, COL_S1 = 64, COL_W2 = 128, COL_S2 = 192;
@@ -146,6 +181,20 @@ __device__ __forceinline__ void get_row(const unsigned char* tile, uint32_t rows
 #pragma unroll
     for (int q = 0; q < W / 8; ++q) {
         const uint4 w = ld_shared_v4(base + sw128_offset(r, c0 + 8 * q, rows));
+        v[8 * q + 0] = bf16_lo(w.x); v[8 * q + 1] = bf16_hi(w.x);
+        v[8 * q + 2] = bf16_lo(w.y); v[8 * q + 3] = bf16_hi(w.y);
+        v[8 * q + 4] = bf16_lo(w.z); v[8 * q + 5] = bf16_hi(w.z);
+        v[8 * q + 6] = bf16_lo(w.w); v[8 * q + 7] = bf16_hi(w.w);
+    }
+}
+
+// W bf16 of a plain row-major row (16-byte aligned), as floats.
+template <int W>
+__device__ __forceinline__ void get_plain(const __nv_bfloat16* p, float* v) {
+    const uint32_t base = smem_u32(p);
+#pragma unroll
+    for (int q = 0; q < W / 8; ++q) {
+        const uint4 w = ld_shared_v4(base + 16 * q);
         v[8 * q + 0] = bf16_lo(w.x); v[8 * q + 1] = bf16_hi(w.x);
         v[8 * q + 2] = bf16_lo(w.y); v[8 * q + 3] = bf16_hi(w.y);
         v[8 * q + 4] = bf16_lo(w.z); v[8 * q + 5] = bf16_hi(w.z);
@@ -225,7 +274,7 @@ __global__ void __launch_bounds__(128 * (64 / CW), 1)
     unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     float* gates = reinterpret_cast<float*>(sm + OFF_F);  // [2 stages][a, eta, beta, c][64]
     float* scan_out = gates + 2 * 4 * BC;                 // [2 stages][A, B, sigma, gamma, u][64]
-    float* gamma_all = reinterpret_cast<float*>(sm + OFF_GM);  // [2 stages][64][GS]
+    __nv_bfloat16* gamma_all = reinterpret_cast<__nv_bfloat16*>(sm + OFF_GM);  // [2 stages][64][GST]
     // exchange buffers: the peer's partial sums as bf16 (summed here in fp32)
     __nv_bfloat16* Yx = reinterpret_cast<__nv_bfloat16*>(sm + OFF_YX);  // [64][XS]
     __nv_bfloat16* Yr = reinterpret_cast<__nv_bfloat16*>(sm + OFF_YR);  // [64][RB]
@@ -311,7 +360,7 @@ __global__ void __launch_bounds__(128 * (64 / CW), 1)
         const float* g = gates + st * 4 * BC;
         float* so = scan_out + st * 5 * BC;
         if (tid >= 128 && tid < 128 + BC) {
-            float* Gm = gamma_all + st * 64 * GS;
+            __nv_bfloat16* Gm = gamma_all + st * 64 * GST;
             const int i = tid - 128;
             const float ci = g[3 * BC + i];
             float u = 0.0f, G = 0.0f;
@@ -331,7 +380,7 @@ __global__ void __launch_bounds__(128 * (64 / CW), 1)
                     const int t = 4 * t4 + k;
                     u = fmaf(gb[k], u, t == i ? ci : 0.0f);
                     G = fmaf(ga[k], G, ge[k] * u);
-                    Gm[t * GS + i] = G;
+                    Gm[t * GST + i] = __float2bfloat16_rn(G);
                 }
             }
             so[3 * BC + i] = G;
@@ -413,6 +462,7 @@ __global__ void __launch_bounds__(128 * (64 / CW), 1)
             }
             tmem_st_n(tl + (which ? COL_S1 : COL_W1) + CW * hq, r);
             put_row<CW>(sm + (which ? OFF_S1 : OFF_W1), 128, jr, CW * hq, r);
+            if (!which) put_row_lo<CW>(sm + OFF_W1LO, 128, jr, CW * hq, r);
             // W2 (or S2) transposed: [j][o] = W2[o][j_glob], o = 32 hf + q
             const float* w2 = src + (long long)hid * D + j_glob;
 #pragma unroll
@@ -430,6 +480,9 @@ __global__ void __launch_bounds__(128 * (64 / CW), 1)
     const uint32_t aW2 = smem_u32(sm + OFF_W2), aAK = smem_u32(sm + OFF_AK), aDT = smem_u32(sm + OFF_DT);
     const uint32_t aKG = smem_u32(sm + OFF_KG), aKU = smem_u32(sm + OFF_KU), aE = smem_u32(sm + OFF_E);
     const uint32_t aEG = smem_u32(sm + OFF_EG), aEU = smem_u32(sm + OFF_EU), aP = smem_u32(sm + OFF_P);
+    const uint32_t aW1lo = smem_u32(sm + OFF_W1LO), aW2lo = smem_u32(sm + OFF_W2LO), aAKlo = smem_u32(sm + OFF_AKLO);
+    const uint32_t aElo = smem_u32(sm + OFF_ELO), aEGlo = smem_u32(sm + OFF_EGLO), aEUlo = smem_u32(sm + OFF_EULO);
+    const uint32_t aDTlo = smem_u32(sm + OFF_DTLO), aKGlo = smem_u32(sm + OFF_KLO), aKUlo = smem_u32(sm + OFF_KLO + T64);
     const int peer = rank ^ 1;
 
     bool failed = false;
@@ -459,7 +512,7 @@ __global__ void __launch_bounds__(128 * (64 / CW), 1)
         // this chunk's scan (computed during the previous chunk)
         const float* so = scan_out + stage * 5 * BC;
         const float *sA = so, *sBc = so + BC, *sSg = so + 2 * BC, *sGl = so + 3 * BC, *sU = so + 4 * BC;
-        const float* Gm = gamma_all + stage * 64 * GS;
+        const __nv_bfloat16* Gm = gamma_all + stage * 64 * GST;
         // the next chunk's gates: warps 2-3 load them now (raw, so that nothing
         // waits for the loads until they are stored to shared memory after E2)
         const int gi = tid - 64;
@@ -480,10 +533,12 @@ __global__ void __launch_bounds__(128 * (64 / CW), 1)
             if (tiles_ok) {
                 tc_fence_after();
                 const uint64_t dW1 = kdesc(aW1), dS1 = kdesc(aS1), dQK = kdesc(aQK), dK = kdesc(aQK + T64);
+                const uint64_t dW1lo = kdesc(aW1lo);
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks) {
                     const uint32_t acc = ks ? 1u : 0u;
                     mma_bf16(tm + COL_XA, dW1 + KS_K * ks, dQK + KS_K * ks, ID_XA, acc);
+                    mma_bf16(tm + COL_Z, dW1lo + KS_K * ks, dK + KS_K * ks, ID_M128N64, 1u);  // z only
                     mma_bf16(tm + COL_XB, dS1 + KS_K * ks, dQK + KS_K * ks, ID_M128N64, acc);
                     mma_bf16(tm + COL_QK, dQK + KS_K * ks, dK + KS_K * ks, ID_M128N64, acc);
                 }
@@ -512,6 +567,8 @@ __global__ void __launch_bounds__(128 * (64 / CW), 1)
             }
             put_row<CW>(sm + OFF_KG, 64, t, c0, o1);
             put_row<CW>(sm + OFF_KU, 64, t, c0, o2);
+            put_row_lo<CW>(sm + OFF_KLO, 64, t, c0, o1);
+            put_row_lo<CW>(sm + OFF_KLO + T64, 64, t, c0, o2);
         }
         mma_wait(go1);
         // ---- E1: a(k) and silu'(z) from z = W1 k; P1 = Gamma (.) Q K^T
@@ -526,6 +583,12 @@ __global__ void __launch_bounds__(128 * (64 / CW), 1)
                 z[q] *= sg;
             }
             put_row<CW>(sm + OFF_AK, 128, jr, CW * hq, z);
+            put_row_lo<CW>(sm + OFF_AKLO, 128, jr, CW * hq, z);  // q|k is dead after G1
+            {  // the chunk-start W2 (the state is rescaled only in E2) as the lo tile for G2 and G3
+                float w[CW];
+                tmem_ld_n(tl + COL_W2 + CW * hq, w);
+                put_row_lo<CW>(sm + OFF_W2LO, 128, jr, CW * hq, w);  // the S1 copy is dead after G1
+            }
             if (SURP) {  // ||a(k_t)||^2 over this quadrant's 32 hidden units, for columns t of this thread
                 float sq[CW];
 #pragma unroll
@@ -534,12 +597,10 @@ __global__ void __launch_bounds__(128 * (64 / CW), 1)
                 if (!(lane & 1)) sp_a2[qd * BC + CW * hq + colsum16_column(lane)] = tot;
             }
             if (qd < 2) {
-                const float* gr = Gm + jr * GS + CW * hq;
+                float gr[CW];
+                get_plain<CW>(Gm + jr * GST + CW * hq, gr);
 #pragma unroll
-                for (int q = 0; q < CW; q += 4) {
-                    const float4 gg = *reinterpret_cast<const float4*>(gr + q);
-                    p[q] *= gg.x; p[q + 1] *= gg.y; p[q + 2] *= gg.z; p[q + 3] *= gg.w;
-                }
+                for (int q = 0; q < CW; ++q) p[q] *= gr[q];
                 put_row<CW>(sm + OFF_P, 64, jr, CW * hq, p);
             }
         }
@@ -548,9 +609,12 @@ __global__ void __launch_bounds__(128 * (64 / CW), 1)
         const bool go2 = !failed;
         if (go2 && tid == 0) {
             const uint64_t dAK = mdesc(aAK, T128), dW2 = mdesc(aW2, T128);
+            const uint64_t dW2lo = mdesc(aW2lo, T128);
 #pragma unroll
-            for (int ks = 0; ks < 8; ++ks)
+            for (int ks = 0; ks < 8; ++ks) {
                 mma_bf16(tm + COL_YH, dAK + KS_M * ks, dW2 + KS_M * ks, ID_M64N64_TT, ks ? 1u : 0u);
+                mma_bf16(tm + COL_YH, dAK + KS_M * ks, dW2lo + KS_M * ks, ID_M64N64_TT, 1u);
+            }
             mma_commit(&bars[1]);
         }
         mma_wait(go2);
@@ -606,14 +670,18 @@ __global__ void __launch_bounds__(128 * (64 / CW), 1)
                 sp_e2[hq * BC + tr] = e2;
             }
             put_row<CW>(sm + OFF_E, 64, tr, CW * hq, ev);
+            // e lo over this thread's own v elements (read above, before the cluster barrier)
+            put_row_lo<CW>(sm + OFF_ELO, 64, tr, CW * hq, ev);
             float o1[CW];
             const float gm = -sGl[tr], uu = sU[tr];
 #pragma unroll
             for (int q = 0; q < CW; ++q) o1[q] = gm * ev[q];
             put_row<CW>(sm + OFF_EG, 64, tr, CW * hq, o1);
+            put_row_lo<CW>(sm + OFF_EGLO, 64, tr, CW * hq, o1);  // the W1 copy is dead after G1
 #pragma unroll
             for (int q = 0; q < CW; ++q) o1[q] = uu * ev[q];
             put_row<CW>(sm + OFF_EU, 64, tr, CW * hq, o1);
+            put_row_lo<CW>(sm + OFF_EULO, 64, tr, CW * hq, o1);
         }
         if (gi >= 0 && gi < BC && c + 1 < nchunks) {
             // tokens past T change nothing: a = 1, eta = 0, beta = 1, c = 0
@@ -626,15 +694,29 @@ __global__ void __launch_bounds__(128 * (64 / CW), 1)
                               : c_mode == NM_C_PER_TOKEN ? nxt_c : 1.0f;
         }
         handoff();
-        // ---- G3: W2^T e (the next chunk's tiles start loading: Q|K and V are free)
+        // ---- G3: W2^T e; then the W2 / S2 updates, which complete while E3 runs (the commit of G4
+        //      covers them): W2 += (-gamma e)^T a(k), S2 += (u e)^T a(k) into the rescaled state
         const bool go3 = !failed;
         if (go3 && tid == 0) {
-            const uint64_t dW2 = kdesc(aW2), dE = kdesc(aE);
+            const uint64_t dW2 = kdesc(aW2), dE = kdesc(aE), dW2lo = kdesc(aW2lo), dElo = kdesc(aElo);
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
+            for (int ks = 0; ks < 4; ++ks) {
                 mma_bf16(tm + COL_XD, dW2 + KS_K * ks, dE + KS_K * ks, ID_M128N64, ks ? 1u : 0u);
+                mma_bf16(tm + COL_XD, dW2lo + KS_K * ks, dE + KS_K * ks, ID_M128N64, 1u);
+                mma_bf16(tm + COL_XD, dW2 + KS_K * ks, dElo + KS_K * ks, ID_M128N64, 1u);
+            }
             mma_commit(&bars[1]);
-            if (c + 1 < nchunks) issue_tiles(c + 1);
+            const uint64_t dAK = kdesc(aAK), dAKlo = kdesc(aAKlo);
+            const uint64_t dEG = mdesc(aEG, T64), dEU = mdesc(aEU, T64), dEGlo = mdesc(aEGlo, T64), dEUlo = mdesc(aEUlo, T64);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
+                mma_bf16(tm + COL_W2, dAK + KS_K * ks, dEG + KS_M * ks, ID_UPD, 1u);
+                mma_bf16(tm + COL_W2, dAKlo + KS_K * ks, dEG + KS_M * ks, ID_UPD, 1u);
+                mma_bf16(tm + COL_W2, dAK + KS_K * ks, dEGlo + KS_M * ks, ID_UPD, 1u);
+                mma_bf16(tm + COL_S2, dAK + KS_K * ks, dEU + KS_M * ks, ID_UPD, 1u);
+                mma_bf16(tm + COL_S2, dAKlo + KS_K * ks, dEU + KS_M * ks, ID_UPD, 1u);
+                mma_bf16(tm + COL_S2, dAK + KS_K * ks, dEUlo + KS_M * ks, ID_UPD, 1u);
+            }
         }
         mma_wait(go3);
         // ---- E3: delta = (W2^T e) (.) silu'(z)
@@ -644,6 +726,7 @@ __global__ void __launch_bounds__(128 * (64 / CW), 1)
 #pragma unroll
             for (int q = 0; q < CW; ++q) xd[q] *= ds[q];
             put_row<CW>(sm + OFF_DT, 128, jr, CW * hq, xd);
+            put_row_lo<CW>(sm + OFF_DTLO, 128, jr, CW * hq, xd);  // the S1 copy is dead after G1
             if (SURP) {  // ||delta_t||^2 over this quadrant's 32 hidden units
                 float sq[CW];
 #pragma unroll
@@ -656,27 +739,30 @@ __global__ void __launch_bounds__(128 * (64 / CW), 1)
         // ---- G4: state update and sum_i P1[t][i] delta_i
         const bool go4 = !failed;
         if (go4 && tid == 0) {
-            const uint64_t dDT = kdesc(aDT), dAK = kdesc(aAK), dP = kdesc(aP);
-            const uint64_t dKG = mdesc(aKG, T64), dKU = mdesc(aKU, T64), dEG = mdesc(aEG, T64), dEU = mdesc(aEU, T64);
-            // R1 and the W1 / S1 updates first (E4 overwrites delta, which they
-            // read, with a_t); the W2 / S2 updates complete behind them (the next
-            // commit covers them)
+            const uint64_t dDT = kdesc(aDT), dP = kdesc(aP);
+            const uint64_t dKG = mdesc(aKG, T64), dKU = mdesc(aKU, T64);
+            const uint64_t dDTlo = kdesc(aDTlo);
+            const uint64_t dKGlo = mdesc(aKGlo, T64), dKUlo = mdesc(aKUlo, T64);
+            // R1 and the W1 / S1 updates (E4 overwrites delta, which they read, with a_t); this
+            // commit also covers the W2 / S2 updates issued behind G3
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) {
                 mma_bf16(tm + COL_R1, dDT + KS_K * ks, dP + KS_K * ks, ID_M128N64, ks ? 1u : 0u);
                 mma_bf16(tm + COL_W1, dDT + KS_K * ks, dKG + KS_M * ks, ID_UPD, 1u);
+                mma_bf16(tm + COL_W1, dDTlo + KS_K * ks, dKG + KS_M * ks, ID_UPD, 1u);
+                mma_bf16(tm + COL_W1, dDT + KS_K * ks, dKGlo + KS_M * ks, ID_UPD, 1u);
                 mma_bf16(tm + COL_S1, dDT + KS_K * ks, dKU + KS_M * ks, ID_UPD, 1u);
+                mma_bf16(tm + COL_S1, dDTlo + KS_K * ks, dKU + KS_M * ks, ID_UPD, 1u);
+                mma_bf16(tm + COL_S1, dDT + KS_K * ks, dKUlo + KS_M * ks, ID_UPD, 1u);
             }
             mma_commit(&bars[1]);
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks) {
-                mma_bf16(tm + COL_W2, dAK + KS_K * ks, dEG + KS_M * ks, ID_UPD, 1u);
-                mma_bf16(tm + COL_S2, dAK + KS_K * ks, dEU + KS_M * ks, ID_UPD, 1u);
-            }
         }
         // while G4 runs: the next chunk's scan (its gates were stored in E2)
         if (c + 1 < nchunks) scan(stage ^ 1);
         mma_wait(go4);
+        // every product reading the q|k tile (a(k) lo) and the v tile (e lo) has completed: the next
+        // chunk's tiles start loading
+        if (tid == 0 && !failed && c + 1 < nchunks) issue_tiles(c + 1);
         // ---- E4: h_t = A_t W1 q_t - sigma_t S1 q_t - sum_i P1[t][i] delta_i, a_t = silu(h_t)
         {
             float xa[CW], xb[CW], r1[CW];
@@ -709,12 +795,10 @@ __global__ void __launch_bounds__(128 * (64 / CW), 1)
             float p[CW];
             tmem_ld_n(tl + COL_AA + CW * hq, p);
             if (r64) {
-                const float* gr = Gm + tr * GS + CW * hq;
+                float gr[CW];
+                get_plain<CW>(Gm + tr * GST + CW * hq, gr);
 #pragma unroll
-                for (int q = 0; q < CW; q += 4) {
-                    const float4 gg = *reinterpret_cast<const float4*>(gr + q);
-                    p[q] *= gg.x; p[q + 1] *= gg.y; p[q + 2] *= gg.z; p[q + 3] *= gg.w;
-                }
+                for (int q = 0; q < CW; ++q) p[q] *= gr[q];
                 put_row<CW>(sm + OFF_P, 64, tr, CW * hq, p);
             }
         }
@@ -747,6 +831,11 @@ __global__ void __launch_bounds__(128 * (64 / CW), 1)
             // G5) become the next chunk's bf16 operands, or the result
             convert_state(2, c + 1 == nchunks);
             convert_state(3, c + 1 == nchunks);
+            if (c + 1 < nchunks) {  // the new W1 as the next G1's lo tile (a(k) is dead: G4 and G5 are done)
+                float w[CW];
+                tmem_ld_n(tl + COL_W1 + CW * hq, w);
+                put_row_lo<CW>(sm + OFF_W1LO, 128, jr, CW * hq, w);
+            }
             if (SURP && NC > 1 && rank == 1 && tid < BC) {  // this CTA's ||a||^2, ||delta||^2 to rank 0
                 const int t = tid;
                 const float a2 = (sp_a2[t] + sp_a2[BC + t]) + (sp_a2[2 * BC + t] + sp_a2[3 * BC + t]);

@@ -30,6 +30,24 @@
 //     and each owner writes its rows of y.
 // Four cluster barriers per chunk order the exchanges (one receive buffer
 // serves both reduce-scatters).
+//
+// Precision of the gradient path.  Operands are hi/lo pairs of bf16 tiles
+// (x = hi + lo, lo = bf16(x - bf16(x)); a product takes A_hi B_hi + A_lo B_hi +
+// A_hi B_lo into one fp32 accumulator; k is exact in bf16) wherever they feed
+// the gradient or the state update: the chunk-start W1 and W2 in the key
+// forward, e^T in the backward and in the W2 / S2 updates, and the gamma / u
+// scaled a(k) and delta of the updates.  With single bf16 operands the state
+// after a few thousand tokens misses the fp32 state tolerance even in stable
+// runs (an fp64 emulation of the rounding points: the updates' own rounding
+// sets a floor near 1e-2 relative).  The backward's W2 and the
+// retrieval-only products keep single bf16 operands: there is no room for
+// their lo tiles.  The lo tiles live in regions that are dead at the time:
+// W1_lo in the -gamma a(k) / u a(k) tiles from the end of the previous chunk
+// until G1, W2_lo in the delta tiles from the state rescale until G2, the
+// scaled a(k) lo tiles in the q rows of the q|k tile (q is read by G1 only;
+// the next q|k tiles load after G4), e^T lo in the W1 copy and the scaled
+// delta lo tiles in the S1 copy (both read by G1 only, rewritten for the next
+// chunk after G6).
 #include <cuda_bf16.h>
 
 #include "nm_internal.h"
@@ -67,6 +85,14 @@ struct Layout {
     static constexpr uint32_t DU = DG + T64;        // u_t delta_t
     static constexpr uint32_t P = DU + T64;         // [64 t][64 i] Gamma (.) inner products (follows DU: stacked operand)
     static constexpr uint32_t GM = P + T64;         // bf16 Gamma [64][GST]
+    // lo halves of the chunk-start weights for the key forward, in tiles that are dead meanwhile:
+    static constexpr uint32_t W1LO = AKG;           // [128 x][64 j] W1^T lo: end of the previous chunk .. G1
+    static constexpr uint32_t W2LO = DT;            // [128 o][64 j] W2 lo: state rescale .. G2
+    static constexpr uint32_t AKGLO = KQ + T64;     // [64 t][64 j] -gamma a(k) lo (q rows, block 0): E1 .. G4
+    static constexpr uint32_t AKULO = KQ + T128 + T64;  // [64 t][64 j] u a(k) lo (q rows, block 1): E1 .. G4
+    static constexpr uint32_t ETLO = W1;            // [128 o][64 t] e^T lo: exchange 1 .. G4
+    static constexpr uint32_t DGLO = S1;            // [64 t][64 j] -gamma delta lo: E3 .. G4
+    static constexpr uint32_t DULO = S1 + T64;      // [64 t][64 j] u delta lo: E3 .. G4
     static constexpr uint32_t V = GM + 64 * GST * 2;              // bf16 [64 t][OR] this CTA's columns of v
     static constexpr uint32_t RX = V + 64 * OR * 2;               // bf16 [NC-1][OR][RBS] partials from the peers
     static constexpr uint32_t F = RX + (NC - 1) * OR * RBS * 2;   // gates [4][64], A, B, sigma, gamma, u
@@ -77,6 +103,7 @@ struct Layout {
     static constexpr uint32_t BYTES = USED + 1024;  // slack for the 1024-byte alignment
     static_assert(BYTES <= 232448, "shared memory budget");
     static_assert(AQ == AK + T64 && P == DU + T64, "stacked operands");
+    static_assert(AKU == AKG + T64 && DG == DT + T64, "the lo tiles span two consecutive 64-row tiles");
     static_assert(GM % 128 == 0 && V % 128 == 0 && RX % 16 == 0 && (RBS * 2) % 16 == 0, "alignment");
     // the owner's own partial rows (fp32 [OR][RXS]) during an exchange live in
     // the delta tiles, which are dead at both exchange points
@@ -244,6 +271,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             for (int q = 0; q < 32; ++q) r[q] = w1[(long long)q * D];
             tmem_st32(tl + (which ? COL_S1 : COL_W1) + 32 * hf, r);
             put_row32(sm + (which ? L::S1 : L::W1), 128, lr, 32 * hf, r);
+            if (!which) put_row32_lo(sm + L::W1LO, 128, lr, 32 * hf, r);
             const float* w2 = src + (long long)hid * D + (long long)lr * hid + jg0 + 32 * hf;
 #pragma unroll
             for (int q = 0; q < 32; q += 4) {
@@ -266,6 +294,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const uint32_t aAQ = smem_u32(sm + L::AQ), aAKG = smem_u32(sm + L::AKG), aAKU = smem_u32(sm + L::AKU);
     const uint32_t aET = smem_u32(sm + L::ET), aDT = smem_u32(sm + L::DT), aDG = smem_u32(sm + L::DG);
     const uint32_t aDU = smem_u32(sm + L::DU), aP = smem_u32(sm + L::P);
+    const uint32_t aW1lo = smem_u32(sm + L::W1LO), aW2lo = smem_u32(sm + L::W2LO);
+    const uint32_t aAKGlo = smem_u32(sm + L::AKGLO), aAKUlo = smem_u32(sm + L::AKULO), aETlo = smem_u32(sm + L::ETLO);
+    const uint32_t aDGlo = smem_u32(sm + L::DGLO), aDUlo = smem_u32(sm + L::DULO);
 
     bool failed = false;
     uint32_t mma_phase = 0;
@@ -343,11 +374,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             if (tiles_ok) {
                 tc_fence_after();
                 const uint64_t dKQ = kdesc(aKQ), dW1 = mdesc(aW1, T128), dS1 = mdesc(aS1, T128);
+                const uint64_t dW1lo = mdesc(aW1lo, T128);
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {  // 16 features per k-step
                     const uint32_t acc = ks ? 1u : 0u;
                     const uint64_t ka = (ks >> 2) * (T128 >> 4) + KS_K * (ks & 3);
                     mma_bf16(tm + COL_XA, dKQ + ka, dW1 + KS_M * ks, ID_KB, acc);
+                    mma_bf16(tm + COL_XA, dKQ + ka, dW1lo + KS_M * ks, ID_KB, 1u);
                     mma_bf16(tm + COL_XB, dKQ + ka, dS1 + KS_M * ks, ID_KB, acc);
                     mma_bf16(tm + COL_QK, dKQ + ka, dKQ + ka, ID_KK, acc);
                 }
@@ -416,6 +449,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             for (int pr = 0; pr < 2; ++pr) {
                 const uint32_t cw = (pr ? COL_W2 : COL_W1) + 32 * hf, cs = (pr ? COL_S2 : COL_S1) + 32 * hf;
                 tmem_ld_n(tl + cw, tl + cs, w, s);
+                // the chunk-start W2 (read before the rescale) as the lo half for G2
+                if (pr) put_row32_lo(sm + L::W2LO, 128, lr, 32 * hf, w);
 #pragma unroll
                 for (int q = 0; q < 32; ++q) {
                     w[q] = fmaf(An, w[q], -sn * s[q]);
@@ -451,9 +486,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
                 for (int q = 0; q < 32; ++q) o1[q] = gm * v[q];
                 put_row32(sm + L::AKG, 64, t, 32 * hf, o1);
+                put_row32_lo(sm + L::AKGLO, 64, t, 32 * hf, o1);
 #pragma unroll
                 for (int q = 0; q < 32; ++q) o1[q] = uu * v[q];
                 put_row32(sm + L::AKU, 64, t, 32 * hf, o1);
+                put_row32_lo(sm + L::AKULO, 64, t, 32 * hf, o1);
             } else {
                 tmem_ld32(tl + COL_QK + 32 * hf, v);
                 const int t = lr - 64;
@@ -468,10 +505,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         // ---- G2: partial key forward [o][t] = sum_{j in slice} W2[o][j] a(k_t)[j]
         const bool go2 = !failed;
         if (go2 && tid == 0) {
-            const uint64_t dW2 = kdesc(aW2), dAK = kdesc(aAK);
+            const uint64_t dW2 = kdesc(aW2), dAK = kdesc(aAK), dW2lo = kdesc(aW2lo);
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
+            for (int ks = 0; ks < 4; ++ks) {
                 mma_bf16(tm + COL_YH, dW2 + KS_K * ks, dAK + KS_K * ks, ID_KK, ks ? 1u : 0u);
+                mma_bf16(tm + COL_YH, dW2lo + KS_K * ks, dAK + KS_K * ks, ID_KK, 1u);
+            }
             mma_commit(&bars[1]);
         }
         // the next chunk's gates (this chunk's are scanned)
@@ -509,11 +548,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         if (SURP) atomicAdd(&sp_loc[2 * BC + t], e[k] * e[k]);
                     }
                     const uint32_t w0 = pack_bf16(e[0], e[1]), w1 = pack_bf16(e[2], e[3]);
+                    const uint32_t l0 = pack_bf16(bf16_residual(e[0]), bf16_residual(e[1]));
+                    const uint32_t l1 = pack_bf16(bf16_residual(e[2]), bf16_residual(e[3]));
                     const uint32_t off = sw128_offset(own_lo + row, 4 * c4, 128);
 #pragma unroll
-                    for (int p = 0; p < NC; ++p) {
+                    for (int p = 0; p < NC; ++p) {  // (every CTA's W1 copy is dead: barrier A follows its G1)
                         const uint32_t dst = map_to_rank(aET + off, (uint32_t)p);
                         asm volatile("st.shared::cluster.v2.b32 [%0], {%1, %2};" ::"r"(dst), "r"(w0), "r"(w1) : "memory");
+                        const uint32_t dlo = map_to_rank(aETlo + off, (uint32_t)p);
+                        asm volatile("st.shared::cluster.v2.b32 [%0], {%1, %2};" ::"r"(dlo), "r"(l0), "r"(l1) : "memory");
                     }
                 }
             }
@@ -524,10 +567,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         //      the upper 64 rows of the stacked operand are not read); the next v slice
         const bool go3 = !failed;
         if (go3 && tid == 0) {
-            const uint64_t dE = mdesc(aET, T128), dW2 = mdesc(aW2, T128);
+            const uint64_t dE = mdesc(aET, T128), dW2 = mdesc(aW2, T128), dElo = mdesc(aETlo, T128);
 #pragma unroll
-            for (int ks = 0; ks < 8; ++ks)  // 16 output features per k-step
+            for (int ks = 0; ks < 8; ++ks) {  // 16 output features per k-step
                 mma_bf16(tm + COL_X, dE + KS_M * ks, dW2 + KS_M * ks, ID_MB, ks ? 1u : 0u);
+                mma_bf16(tm + COL_X, dElo + KS_M * ks, dW2 + KS_M * ks, ID_MB, 1u);
+            }
             mma_commit(&bars[1]);
             if (c + 1 < nchunks) issue_v(c + 1);
         }
@@ -550,9 +595,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
             for (int q = 0; q < 32; ++q) o1[q] = gm * x[q];
             put_row32(sm + L::DG, 64, t, 32 * hf, o1);
+            put_row32_lo(sm + L::DGLO, 64, t, 32 * hf, o1);
 #pragma unroll
             for (int q = 0; q < 32; ++q) o1[q] = uu * x[q];
             put_row32(sm + L::DU, 64, t, 32 * hf, o1);
+            put_row32_lo(sm + L::DULO, 64, t, 32 * hf, o1);
         } else if (SURP) {  // ||k_t||^2: row t of the q|k tile's k half, 64 features per thread
             const int t = lr - 64;
             const uint32_t base = smem_u32(sm + L::KQ);
@@ -583,13 +630,21 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             const uint64_t dDUP = kdesc(aDU), dDT = mdesc(aDT, T64);
             const uint64_t dKt = mdesc(aKQ, T128), dDG = mdesc(aDG, T64), dDU = mdesc(aDU, T64);
             const uint64_t dET = kdesc(aET), dAKG = mdesc(aAKG, T64), dAKU = mdesc(aAKU, T64);
+            const uint64_t dDGlo = mdesc(aDGlo, T64), dDUlo = mdesc(aDUlo, T64), dETlo = kdesc(aETlo);
+            const uint64_t dAKGlo = mdesc(aAKGlo, T64), dAKUlo = mdesc(aAKUlo, T64);
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) {  // 16 tokens per k-step
                 mma_bf16(tm + COL_R1, dDUP + KS_K * ks, dDT + KS_M * ks, ID_KB, ks ? 1u : 0u);
                 mma_bf16(tm + COL_W1, dKt + KS_M * ks, dDG + KS_M * ks, ID_MB, 1u);
+                mma_bf16(tm + COL_W1, dKt + KS_M * ks, dDGlo + KS_M * ks, ID_MB, 1u);
                 mma_bf16(tm + COL_S1, dKt + KS_M * ks, dDU + KS_M * ks, ID_MB, 1u);
+                mma_bf16(tm + COL_S1, dKt + KS_M * ks, dDUlo + KS_M * ks, ID_MB, 1u);
                 mma_bf16(tm + COL_W2, dET + KS_K * ks, dAKG + KS_M * ks, ID_KB, 1u);
+                mma_bf16(tm + COL_W2, dETlo + KS_K * ks, dAKG + KS_M * ks, ID_KB, 1u);
+                mma_bf16(tm + COL_W2, dET + KS_K * ks, dAKGlo + KS_M * ks, ID_KB, 1u);
                 mma_bf16(tm + COL_S2, dET + KS_K * ks, dAKU + KS_M * ks, ID_KB, 1u);
+                mma_bf16(tm + COL_S2, dETlo + KS_K * ks, dAKU + KS_M * ks, ID_KB, 1u);
+                mma_bf16(tm + COL_S2, dET + KS_K * ks, dAKUlo + KS_M * ks, ID_KB, 1u);
             }
             mma_commit(&bars[1]);
         }
@@ -666,6 +721,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     if (!last) {
                         const uint32_t off = m == 0 ? L::W1 : m == 1 ? L::S1 : m == 2 ? L::W2 : L::S2;
                         put_row32(sm + off, 128, lr, 32 * hf, w);
+                        if (m == 0) put_row32_lo(sm + L::W1LO, 128, lr, 32 * hf, w);  // read by the next G1
                     } else {
                         float* dst = ((m & 1) ? a.S_T : a.M_T) + unit * P;
                         if (m < 2) {  // W1[jg0 + j][x] for x = lr

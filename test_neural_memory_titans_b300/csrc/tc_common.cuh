@@ -86,6 +86,32 @@ __device__ __forceinline__ void put_row(unsigned char* tile, uint32_t rows, uint
     }
 }
 
+// The part of x that bf16 rounding drops, x - bf16(x) (exact in fp32).  Rounded
+// to bf16 in turn it is the "lo" half of a hi/lo pair: hi + lo carries about 16
+// significant bits, so a product taken as hi * B + lo * B (two tensor-core
+// products into one fp32 accumulator) keeps fp32-like accuracy in the operand
+// that was split.
+__device__ __forceinline__ float bf16_residual(float x) {
+    return x - __bfloat162float(__float2bfloat16_rn(x));
+}
+
+// put_row32 of the residuals x - bf16(x) of 32 values (the lo halves).
+__device__ __forceinline__ void put_row32_lo(unsigned char* tile, uint32_t rows, uint32_t r, uint32_t c0, const float* v) {
+    float lo[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) lo[i] = bf16_residual(v[i]);
+    put_row32(tile, rows, r, c0, lo);
+}
+
+// put_row<W> of the residuals x - bf16(x) of W values.
+template <int W>
+__device__ __forceinline__ void put_row_lo(unsigned char* tile, uint32_t rows, uint32_t r, uint32_t c0, const float* v) {
+    float lo[W];
+#pragma unroll
+    for (int i = 0; i < W; ++i) lo[i] = bf16_residual(v[i]);
+    put_row<W>(tile, rows, r, c0, lo);
+}
+
 // ------------------------------------------------------------------ mbarrier
 
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
