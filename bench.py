@@ -22,8 +22,9 @@ measured peak, with ``traffic`` from an ncu capture while the captured kernel
 source is unchanged), ``cpu_baseline`` (the oracle on a bounded sample),
 ``clocks`` (SM clock and throttle reasons sampled during the timed region),
 ``gpu_launches`` (this library's kernel launches in the timed region),
-``variants`` (the same workload with the Huber loss and with the surprise
-output, a few steps each; ``--no-variants`` skips them) and ``per_workload``
+``variants`` (the same workload with the Huber loss, with the surprise
+output and with the Memory-as-Gate output, a few steps each;
+``--no-variants`` skips them) and ``per_workload``
 (the other configurations timed in the same run, each with its own roofline
 fraction and clocks; the streamed one adds the needle-retrieval cosine;
 ``--no-per-workload`` skips them).  ``--layers L`` runs an MLP workload with an
@@ -502,15 +503,20 @@ def run_ours(args, rank, world, local_rank):
                                 layers=wl.layers if wl.kind == nm.MLP2 else 0)
         v_h = time_calls(lambda: mem_h.forward(*args8, y=y, M_T=M, S_T=S, stream=stream), n_var)
         v_s = time_calls(lambda: mem.forward_surprise(*args8, y=y, M_T=M, S_T=S, surprise=sur, stream=stream), n_var)
+        y_attn = torch.randn(y.shape, device=dev).to(y.dtype)
+        v_g = time_calls(lambda: mem.forward_gated(*args8, y_attn, o=y, M_T=M, S_T=S, stream=stream), n_var)
         for m_ in (mem, mem_h):
             st = m_.synchronize()
             if st != nm.NM_OK:
                 raise RuntimeError("device status after the variants: %s" % nm.status_string(st))
         mem_h.close()
-        del sur
+        del sur, y_attn
         variants = {"huber_loss": {"ms_per_step": v_h, "value": world * tokens / (v_h * 1e-3), "delta": 0.1},
                     "surprise_output": {"ms_per_step": v_s, "value": world * tokens / (v_s * 1e-3)},
-                    "steps": n_var, "note": "nm_config.loss = NM_LOSS_HUBER; nm_forward_surprise"}
+                    "mag_gate": {"ms_per_step": v_g, "value": world * tokens / (v_g * 1e-3)},
+                    "steps": n_var,
+                    "note": "nm_config.loss = NM_LOSS_HUBER; nm_forward_surprise; nm_forward_gated (o = sigmoid(y) * "
+                            "y_attn written in place of y)"}
 
     # e2e through the host-buffer entry point (pinned), copies inside the timed region
     e2e = None

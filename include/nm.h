@@ -165,6 +165,31 @@ int nm_forward_surprise(nm_handle_t h, int B, int H, int T,
                         void* y, float* M_T, float* S_T, float* surprise, void* stream);
 
 /*
+ * nm_forward_gated - nm_forward with the memory's output combined with an
+ *   attention branch's output by the Memory-as-Gate rule (0h-n0.github.io
+ *   explainer, "3つのアーキテクチャ変種", MAG: o_t = sigmoid(y_t^mem) (.)
+ *   y_t^attn; "Titans: Imparare a Memorizzare al Tempo di Test", "Varianti
+ *   dell'Architettura Titans", "Memory as Gate (MAG)": the two branches'
+ *   outputs combined by a gate):
+ *     y_attn [B, H, T, d] out_dtype (DEVICE, caller-owned, 16-byte aligned,
+ *            read): the other branch's output (e.g. sliding-window attention)
+ *     o      [B, H, T, d] out_dtype (written) = sigmoid(y) * y_attn element by
+ *            element, y the memory's retrieval M_t(q_t) that nm_forward writes
+ *   The sigmoid is 1 / (1 + exp(-y)), applied to y in fp32 before the output
+ *   is rounded.  y itself is not written.  M_T and S_T are nm_forward's, bit
+ *   for bit.  o == y_attn (exact aliasing) is allowed, gating the attention
+ *   output in place; any other overlap of y_attn with an output returns
+ *   NM_ERR_ALIAS.  y_attn must not be NULL when T > 0 (NM_ERR_ARG).
+ *   Everything else is nm_forward's contract.  Every kernel family writes it
+ *   from its retrieval epilogue.
+ */
+int nm_forward_gated(nm_handle_t h, int B, int H, int T,
+                     const void* q, const void* k, const void* v,
+                     const float* alpha, const float* eta, const float* beta,
+                     const float* c, const float* M0, const float* S0,
+                     const void* y_attn, void* o, float* M_T, float* S_T, void* stream);
+
+/*
  * nm_forward_host - the same operation on HOST buffers (same layouts).
  *   Copies the inputs to the handle's device (into handle-owned buffers that
  *   grow on demand), runs nm_forward on `stream`, copies y, M_T, S_T back and

@@ -113,6 +113,19 @@ def grad(kind: int, d: int, hidden: int, W, k, v, loss_kind: int = LOSS_L2, hube
     return g
 
 
+def mag_gate(y_mem, y_attn) -> np.ndarray:
+    """The Memory-as-Gate combination of the memory's output with another
+    branch's output, element by element: o = sigmoid(y_mem) * y_attn with the
+    logistic sigmoid 1 / (1 + exp(-y)), in fp64 (0h-n0.github.io explainer,
+    "3つのアーキテクチャ変種", MAG: o_t = sigma(y_t^mem) (.) y_t^attn;
+    "Titans: Imparare a Memorizzare al Tempo di Test", "Varianti
+    dell'Architettura Titans", "Memory as Gate (MAG)")."""
+    y_mem, y_attn = _f64(y_mem), _f64(y_attn)
+    assert y_mem.shape == y_attn.shape
+    with np.errstate(over="ignore"):
+        return y_attn / (1.0 + np.exp(-y_mem))
+
+
 def forward(kind: int, d: int, hidden: int, chunk: int, c_mode: int,
             q, k, v, alpha, eta, beta, c, M0, S0, loss_kind: int = LOSS_L2, huber_delta: float = np.inf,
             surprise: bool = False, layers: int = 2):

@@ -50,7 +50,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libnm.so")
 EXPORTED = ("nm_create", "nm_forward", "nm_forward_host", "nm_synchronize", "nm_destroy",
             "nm_status_string", "nm_selected_path", "nm_launch_count", "nm_inject_missing_load",
-            "nm_forward_mlp2_noalloc", "nm_forward_surprise")
+            "nm_forward_mlp2_noalloc", "nm_forward_surprise", "nm_forward_gated")
 
 _DT = {torch.float32: F32, torch.bfloat16: BF16}
 _TORCH_DT = {F32: torch.float32, BF16: torch.bfloat16}
@@ -90,6 +90,8 @@ def load_library() -> ctypes.CDLL:
         lib.nm_forward_host.restype = i
         lib.nm_forward_surprise.argtypes = fwd[:-1] + [vp, vp]
         lib.nm_forward_surprise.restype = i
+        lib.nm_forward_gated.argtypes = fwd[:13] + [vp, vp, f, f, vp]
+        lib.nm_forward_gated.restype = i
         lib.nm_synchronize.argtypes = [vp]
         lib.nm_synchronize.restype = i
         lib.nm_destroy.argtypes = [vp]
@@ -223,6 +225,31 @@ class NeuralMemory:
         if rc != NM_OK:
             raise NMError(rc, "nm_forward_surprise")
         return y, M_T, S_T, surprise
+
+    def forward_gated(self, q, k, v, alpha, eta, beta, M0, S0, y_attn, c=None, o=None, M_T=None, S_T=None,
+                      stream: Optional[torch.cuda.Stream] = None):
+        """forward() whose output is combined with another branch's output by
+        the Memory-as-Gate rule, o = sigmoid(y) * y_attn (y_attn of the output
+        dtype and y's shape; o may be y_attn itself): returns (o, M_T, S_T)."""
+        B, H, T = self._check(q, k, v, alpha, eta, beta, c, M0, S0, host=False)
+        dev = q.device
+        if y_attn.shape != (B, H, T, self.d) or y_attn.dtype != self.out_dtype or not y_attn.is_contiguous():
+            raise ValueError("y_attn must be a contiguous %s [B, H, T, %d] tensor" % (self.out_dtype, self.d))
+        if not y_attn.is_cuda or y_attn.device.index != self.device:
+            raise ValueError("forward_gated takes tensors on cuda:%d" % self.device)
+        if o is None:
+            o = torch.empty((B, H, T, self.d), dtype=self.out_dtype, device=dev)
+        if M_T is None:
+            M_T = torch.empty_like(M0)
+        if S_T is None:
+            S_T = torch.empty_like(S0)
+        s = stream if stream is not None else torch.cuda.current_stream(dev)
+        rc = load_library().nm_forward_gated(self._h, B, H, T, _ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(eta),
+                                             _ptr(beta), _ptr(c), _ptr(M0), _ptr(S0), _ptr(y_attn), _ptr(o),
+                                             _ptr(M_T), _ptr(S_T), ctypes.c_void_p(s.cuda_stream))
+        if rc != NM_OK:
+            raise NMError(rc, "nm_forward_gated")
+        return o, M_T, S_T
 
     def forward_host(self, q, k, v, alpha, eta, beta, M0, S0, c=None, y=None, M_T=None, S_T=None,
                      stream: Optional[torch.cuda.Stream] = None):

@@ -167,7 +167,8 @@ namespace {
 
 int forward_impl(nm_handle_t h, int B, int H, int T, const void* q, const void* k, const void* v,
                  const float* alpha, const float* eta, const float* beta, const float* c, const float* M0,
-                 const float* S0, void* y, float* M_T, float* S_T, float* surprise, void* stream) {
+                 const float* S0, void* y, float* M_T, float* S_T, float* surprise, void* stream,
+                 const void* y_attn = nullptr) {
     if (!h) return NM_ERR_ARG;
     const nm_config& cfg = h->cfg;
     if (B < 0 || H < 0 || T < 0) return NM_ERR_ARG;
@@ -179,7 +180,7 @@ int forward_impl(nm_handle_t h, int B, int H, int T, const void* q, const void* 
     if (T > 0 && (!q || !k || !v || !alpha || !eta || !beta || !y)) return NM_ERR_ARG;
     if (T > 0 && need_c && !c) return NM_ERR_ARG;
     if (!need_c && c) return NM_ERR_ARG;
-    const void* ptrs[] = {q, k, v, alpha, eta, beta, c, M0, S0, y, M_T, S_T, surprise};
+    const void* ptrs[] = {q, k, v, alpha, eta, beta, c, M0, S0, y, M_T, S_T, surprise, y_attn};
     for (const void* p : ptrs)
         if (p && !aligned16(p)) return NM_ERR_ALIGN;
     if (surprise && !nm_supports_surprise(cfg, h->path)) return NM_ERR_UNSUPPORTED;
@@ -194,12 +195,13 @@ int forward_impl(nm_handle_t h, int B, int H, int T, const void* q, const void* 
                     {(const char*)v, T ? in_b : 0},       {(const char*)alpha, gate_b},
                     {(const char*)eta, gate_b},           {(const char*)beta, gate_b},
                     {(const char*)c, need_c ? gate_b : 0}, {(const char*)M0, st_b},
-                    {(const char*)S0, st_b}};
+                    {(const char*)S0, st_b},              {(const char*)y_attn, T ? out_b : 0}};
     Range out_r[] = {{(const char*)y, T ? out_b : 0}, {(const char*)M_T, st_b}, {(const char*)S_T, st_b},
                      {(const char*)surprise, T ? gate_b : 0}};
     for (int o = 0; o < 4; ++o) {
-        for (int i = 0; i < 9; ++i) {
-            bool exact_ok = (o == 1 && i == 7) || (o == 2 && i == 8);
+        for (int i = 0; i < 10; ++i) {
+            // in-place carry of the state, and the gated output over the attention branch's buffer
+            bool exact_ok = (o == 1 && i == 7) || (o == 2 && i == 8) || (o == 0 && i == 9);
             if (exact_ok && out_r[o].p == in_r[i].p) continue;
             if (overlaps(out_r[o], in_r[i])) return NM_ERR_ALIAS;
         }
@@ -233,6 +235,7 @@ int forward_impl(nm_handle_t h, int B, int H, int T, const void* q, const void* 
     h->inject_load_skip = 0;
     a.e_clip = nm_err_clip(cfg);
     a.surprise = surprise;
+    a.y_attn = y_attn;
     cudaError_t e = h->path == NM_PATH_TC ? nm_tc_launch(cfg, a, s, h->num_sms, &h->launches)
                                           : nm_simt_launch(cfg, a, s, &h->launches);
     if (e != cudaSuccess) {
@@ -256,6 +259,15 @@ int nm_forward_surprise(nm_handle_t h, int B, int H, int T, const void* q, const
                         void* stream) {
     if (!surprise) return NM_ERR_ARG;
     return forward_impl(h, B, H, T, q, k, v, alpha, eta, beta, c, M0, S0, y, M_T, S_T, surprise, stream);
+}
+
+int nm_forward_gated(nm_handle_t h, int B, int H, int T, const void* q, const void* k, const void* v,
+                     const float* alpha, const float* eta, const float* beta, const float* c,
+                     const float* M0, const float* S0, const void* y_attn, void* o, float* M_T, float* S_T,
+                     void* stream) {
+    if (T > 0 && !y_attn) return NM_ERR_ARG;
+    return forward_impl(h, B, H, T, q, k, v, alpha, eta, beta, c, M0, S0, o, M_T, S_T, nullptr, stream,
+                        T > 0 ? y_attn : nullptr);
 }
 
 int nm_synchronize(nm_handle_t h) {

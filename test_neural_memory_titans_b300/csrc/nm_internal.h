@@ -3,6 +3,7 @@
 #pragma once
 
 #include <math.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -30,6 +31,8 @@ struct nm_args {
     int skip_first_load;  // test hook: tensor-core kernels skip chunk 0's tile loads
     float e_clip;     // |e| bound: 2 delta for the Huber loss, +inf for the squared loss
     float* surprise;  // [B, H, T] per-token gradient norms, or NULL (not computed)
+    const void* y_attn;  // [B, H, T, d] of y's type: when set, the call writes o = sigmoid(y) * y_attn
+                         // (the Memory-as-Gate combination) in place of y; NULL for the plain forward
 };
 
 // The error e = d rho / d r of the loss at the residual r = M(k) - v, given
@@ -38,6 +41,62 @@ struct nm_args {
 __host__ __device__ inline float nm_clip_err(float two_r, float e_clip) {
     return two_r > e_clip ? e_clip : (two_r < -e_clip ? -e_clip : two_r);
 }
+
+#ifdef __CUDACC__
+__device__ __forceinline__ float nm_to_f32(float x) { return x; }
+__device__ __forceinline__ float nm_to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+// The value a kernel writes at output element p (a pointer into a.y) for the
+// memory's retrieval y there: y itself, or with a.y_attn set the
+// Memory-as-Gate combination o = sigmoid(y) * y_attn at the same index
+// (0h-n0.github.io explainer, "3つのアーキテクチャ変種", MAG; "Titans:
+// Imparare a Memorizzare al Tempo di Test", "Varianti dell'Architettura
+// Titans", "Memory as Gate (MAG)").  Each element of y_attn is read by the
+// thread that writes the same element of o, before it writes it, so o may be
+// y_attn itself.
+template <typename Tout>
+__device__ __forceinline__ float nm_gated(const nm_args& a, const Tout* p, float y) {
+    if (!a.y_attn) return y;
+    const Tout* ya = reinterpret_cast<const Tout*>(a.y_attn) + (p - reinterpret_cast<const Tout*>(a.y));
+    return nm_to_f32(*ya) / (1.0f + expf(-y));
+}
+
+// W consecutive elements y_attn[idx .. idx + W) as floats, with 16-byte loads
+// (idx a multiple of 8 for bf16, of 4 for fp32, and y_attn 16-byte aligned),
+// all issued before any is used.
+template <int W>
+__device__ __forceinline__ void nm_load_row(const __nv_bfloat16* p, float* v) {
+#pragma unroll
+    for (int i = 0; i < W / 8; ++i) {
+        const uint4 w = reinterpret_cast<const uint4*>(p)[i];
+        const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            v[8 * i + 2 * j] = __uint_as_float(u[j] << 16);
+            v[8 * i + 2 * j + 1] = __uint_as_float(u[j] & 0xFFFF0000u);
+        }
+    }
+}
+template <int W>
+__device__ __forceinline__ void nm_load_row(const float* p, float* v) {
+#pragma unroll
+    for (int i = 0; i < W / 4; ++i) {
+        const float4 w = reinterpret_cast<const float4*>(p)[i];
+        v[4 * i] = w.x; v[4 * i + 1] = w.y; v[4 * i + 2] = w.z; v[4 * i + 3] = w.w;
+    }
+}
+
+// The Memory-as-Gate combination over W consecutive outputs starting at p
+// (a pointer into a.y, its element index a multiple of 8): v <- sigmoid(v) *
+// y_attn, the y_attn row loaded first.  Call it only when a.y_attn is set.
+template <int W, typename Tout>
+__device__ __forceinline__ void nm_gate_row(const nm_args& a, const Tout* p, float* v) {
+    float ya[W];
+    nm_load_row<W>(reinterpret_cast<const Tout*>(a.y_attn) + (p - reinterpret_cast<const Tout*>(a.y)), ya);
+#pragma unroll
+    for (int i = 0; i < W; ++i) v[i] = ya[i] / (1.0f + expf(-v[i]));
+}
+#endif
 
 struct nm_handle {
     nm_config cfg;

@@ -123,6 +123,7 @@ extern "C" int nm_forward_mlp2_noalloc(const nm_config* cfg, int B, int H, int T
     a.skip_first_load = 0;
     a.e_clip = nm_err_clip(run);
     a.surprise = nullptr;
+    a.y_attn = nullptr;
     long long launched = 0;
     if (nm_simt_launch(run, a, s, &launched) != cudaSuccess) {
         cudaGetLastError();

@@ -155,7 +155,7 @@ __global__ void __launch_bounds__(D * LIN_R) simt_linear_kernel(nm_args a, int c
                 }
 #pragma unroll
                 for (int o = R / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-                if (s == 0) st_out(y + (sb + t) * D + r, acc);
+                if (s == 0) st_out(y + (sb + t) * D + r, nm_gated(a, y + (sb + t) * D + r, acc));
             }
         }
     }
@@ -364,7 +364,7 @@ __global__ void __launch_bounds__(MLP_THREADS) simt_mlp_kernel(nm_args a, int d,
                 s2 = fmaf(aj, S2[(long long)o * hd + j], s2);
             }
             for (int i = 0; i <= t; ++i) g = fmaf(Pm[(size_t)t * b + i], E[i * d + o], g);
-            st_out(y + (t0 + t) * d + o, sA[t] * m2 - sSg[t] * s2 - g);
+            st_out(y + (t0 + t) * d + o, nm_gated(a, y + (t0 + t) * d + o, sA[t] * m2 - sSg[t] * s2 - g));
         }
         __syncthreads();
         // chunk-end state: W = A W0 - sigma S0 - sum_i Gamma_{n-1,i} g_i, S = B S0 + sum_i u_{n-1,i} g_i
@@ -645,7 +645,7 @@ __global__ void __launch_bounds__(MLP_THREADS) simt_deep_kernel(nm_args a, int d
                 for (int c4 = 0; c4 < 4; ++c4) {
                     const float pre = sA[t] * mv[c4] - sSg[t] * sv[c4] - gv[c4];
                     if (l < L) rn[(size_t)t * out + j + c4] = silu_f(pre);
-                    else st_out(y + (t0 + t) * d + j + c4, pre);
+                    else st_out(y + (t0 + t) * d + j + c4, nm_gated(a, y + (t0 + t) * d + j + c4, pre));
                 }
             }
             __syncthreads();

@@ -474,10 +474,29 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             float y1[32], y2[32], pe[32];
             tmem_ld_n(tl + COL_Y1 + 32 * hf, tl + COL_Y2 + 32 * hf, tl + COL_PE + 32 * hf, y1, y2, pe);
             Tout* yt = reinterpret_cast<Tout*>(sm + OFF_EG);
+            if (!a.y_attn) {
 #pragma unroll
-            for (int q = 0; q < 32; ++q) {
-                const int t = 32 * hf + q;
-                store_y(yt + t * D + orow, fmaf(sA[t], y1[q], -fmaf(sSg[t], y2[q], pe[q])));
+                for (int q = 0; q < 32; ++q) {
+                    const int t = 32 * hf + q;
+                    store_y(yt + t * D + orow, fmaf(sA[t], y1[q], -fmaf(sSg[t], y2[q], pe[q])));
+                }
+            } else {  // the gated output: this output row's y_attn of 8 tokens at a time, loaded first
+                const Tout* ya = reinterpret_cast<const Tout*>(a.y_attn) + (unit * T + t0) * D + orow;
+#pragma unroll
+                for (int g8 = 0; g8 < 4; ++g8) {
+                    float yv[8];
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        const int t = 32 * hf + 8 * g8 + q;
+                        yv[q] = t < n ? nm_to_f32(ya[t * D]) : 0.0f;  // rows past T are not stored
+                    }
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        const int t = 32 * hf + 8 * g8 + q, qq = 8 * g8 + q;
+                        const float v = fmaf(sA[t], y1[qq], -fmaf(sSg[t], y2[qq], pe[qq]));
+                        store_y(yt + t * D + orow, yv[q] / (1.0f + expf(-v)));
+                    }
+                }
             }
         }
         // ---- the new state: bf16 operand copies for the next chunk, or the result

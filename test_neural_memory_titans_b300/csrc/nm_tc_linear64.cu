@@ -469,7 +469,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             tmem_ld32x2(tl + COL_Y4 + 192 + c0, tl + COL_PE + c0, y2, y3);
 #pragma unroll
             for (int q = 0; q < 32; ++q) y1[q] -= fmaf(rt, y2[q], y3[q]);
-            if (r64 && t < n) store_row32<Tout>(y + (t0 + t) * D + c0, y1);
+            if (r64 && t < n) {
+                if (a.y_attn) nm_gate_row<32>(a, y + (t0 + t) * D + c0, y1);
+                store_row32<Tout>(y + (t0 + t) * D + c0, y1);
+            }
         }
         // ---- CG, CU become the next block's operands; at the chunk's end, the new state
         {

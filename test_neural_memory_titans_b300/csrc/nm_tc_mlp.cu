@@ -851,6 +851,7 @@ __global__ void __launch_bounds__(128 * (64 / CW), 1)
 #pragma unroll
                     for (int q = 0; q < CW; ++q) yw[q] += pr[q];
                 }
+                if (a.y_attn) nm_gate_row<CW>(a, y + (t0 + tr) * D + CW * hq, yw);
                 store_y<CW>(y + (t0 + tr) * D + CW * hq, yw);
             }
             if (SURP && rank == 0 && tid < n) {

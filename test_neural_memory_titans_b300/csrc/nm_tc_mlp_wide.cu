@@ -755,7 +755,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             for (int task = tid; task < TASKS; task += NTHREADS) {
                 const int row = task % OR, c4 = task / OR;  // consecutive threads: consecutive rows
                 const float4 sum = reduce4(row, c4);
-                const float sv[4] = {sum.x, sum.y, sum.z, sum.w};
+                float sv[4] = {sum.x, sum.y, sum.z, sum.w};
+                if (a.y_attn) {  // the gated output: the four y_attn values loaded first
+                    const Tout* ya = reinterpret_cast<const Tout*>(a.y_attn) + (unit * T + t0) * D + own_lo + row;
+                    float yv[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) yv[k] = 4 * c4 + k < n ? nm_to_f32(ya[(4 * c4 + k) * D]) : 0.0f;
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) sv[k] = yv[k] / (1.0f + expf(-sv[k]));
+                }
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
                     const int t = 4 * c4 + k;

@@ -64,6 +64,7 @@ def test_null_handle_and_bad_config_without_gpu():
     lib = nm.load_library()
     assert lib.nm_forward(None, 1, 1, 1, *([None] * 12), None) == nm.NM_ERR_ARG
     assert lib.nm_forward_surprise(None, 1, 1, 1, *([None] * 13), None) == nm.NM_ERR_ARG
+    assert lib.nm_forward_gated(None, 1, 1, 1, *([None] * 13), None) == nm.NM_ERR_ARG
     assert lib.nm_synchronize(None) == nm.NM_ERR_ARG
     assert lib.nm_destroy(None) == nm.NM_OK
     h = ctypes.c_void_p()
@@ -160,3 +161,30 @@ def test_binding_rejects_wrong_tensors():
         mem.forward(x["q"].cpu(), x["k"], x["v"], x["alpha"], x["eta"], x["beta"], x["M0"], x["S0"])
     with pytest.raises(ValueError):
         mem.forward(x["q"], x["k"], x["v"], x["alpha"], x["eta"], x["beta"], x["M0"][..., :-1], x["S0"])
+
+
+@pytest.mark.gpu
+def test_gated_validation():
+    """nm_forward_gated: y_attn required, aligned, and apart from the outputs
+    except o == y_attn (gating in place); nothing launched on an error."""
+    wl = W.WORKLOADS[2].with_sizes(B=2, H=2, T=128)
+    x, y, MT, ST = _args(wl)
+    ya = torch.randn(y.shape, device="cuda").to(wl.dtype)
+    mem = nm.NeuralMemory(wl.kind, wl.d, 0, wl.chunk, in_dtype=wl.dtype)
+    lib = nm.load_library()
+    n0 = mem.launches
+
+    def call(y_attn, o, M_T=MT, S_T=ST):
+        p = lambda t: None if t is None else ctypes.c_void_p(t if isinstance(t, int) else t.data_ptr())
+        return lib.nm_forward_gated(mem._h, 2, 2, 128, p(x["q"]), p(x["k"]), p(x["v"]), p(x["alpha"]),
+                                    p(x["eta"]), p(x["beta"]), None, p(x["M0"]), p(x["S0"]), p(y_attn), p(o),
+                                    p(M_T), p(S_T), None)
+    assert call(None, y) == nm.NM_ERR_ARG
+    assert call(ya.data_ptr() + 2, y) == nm.NM_ERR_ALIGN
+    assert call(ya, ya.data_ptr() + 16) == nm.NM_ERR_ALIAS        # o partly over y_attn
+    assert call(ya, y, M_T=ya) == nm.NM_ERR_ALIAS                 # a state output over y_attn
+    assert call(x["q"], x["q"]) == nm.NM_ERR_ALIAS                # o over q (even as y_attn)
+    assert mem.launches == n0
+    assert call(ya, ya) == nm.NM_OK                               # in place
+    assert mem.synchronize() == nm.NM_OK
+    assert mem.launches == n0 + 1

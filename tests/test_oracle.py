@@ -587,3 +587,28 @@ def test_deep_chunk1_equals_sequential_and_chunk_sums_gradients(layers):
     gsum = sum(grad_at(M0, t) for t in range(T))
     np.testing.assert_allclose(out[2][0, 0], S0 + gsum, rtol=1e-11, atol=1e-12)
     np.testing.assert_allclose(out[1][0, 0], M0, rtol=0, atol=0)
+
+
+# ------------------------------------------------------------ Memory-as-Gate combination
+
+def test_mag_gate_hand_worked():
+    """Rational points of the sigmoid (y = ln r gives r / (r + 1)), worked by
+    hand in tests/golden/mag_gate_worked.txt."""
+    g = _read_golden("mag_gate_worked.txt")
+    y = np.log(_fl(g["r"]))
+    o = oracle.mag_gate(y, _fl(g["y_attn"]))
+    assert np.allclose(o, _fl(g["o"]), rtol=1e-15, atol=0)
+
+
+def test_mag_gate_symmetry_limits_and_library():
+    """sigmoid(-y) = 1 - sigmoid(y), so o(y) + o(-y) = y_attn; o -> y_attn for
+    y -> +inf and -> 0 for y -> -inf; and the library logistic function."""
+    from scipy.special import expit
+    rng = np.random.default_rng(0)
+    y = rng.normal(size=(3, 5, 7)) * 4
+    ya = rng.normal(size=y.shape)
+    assert np.allclose(oracle.mag_gate(y, ya) + oracle.mag_gate(-y, ya), ya, rtol=1e-14, atol=1e-15)
+    assert np.allclose(oracle.mag_gate(y, ya), expit(y) * ya, rtol=1e-14, atol=0)
+    big = np.full(4, 800.0)
+    assert np.array_equal(oracle.mag_gate(big, ya.ravel()[:4]), ya.ravel()[:4])
+    assert np.array_equal(oracle.mag_gate(-big, np.ones(4)), np.zeros(4))

@@ -631,3 +631,52 @@ def test_deep_memory(layers, d, hidden, T, chunk, dtype, delta):
     with pytest.raises(nm.NMError) as ei:
         nm.NeuralMemory(nm.MLP2, d, hidden, chunk, in_dtype=dtype, layers=layers, path=nm.PATH_TC)
     assert ei.value.status == nm.NM_ERR_UNSUPPORTED
+
+
+# ------------------------------------------------------------ Memory-as-Gate output
+# nm_forward_gated writes o = sigmoid(y) * y_attn from the retrieval epilogue of
+# every kernel family; o is compared with the oracle's y gated the same way (in
+# fp64), the state must equal nm_forward's bit for bit, and gating y_attn in
+# place must give the same o.
+
+@pytest.mark.parametrize("wid,T,chunk,path,layers", [
+    (0, 200, 16, nm.PATH_SIMT, 2), (2, 300, 64, nm.PATH_SIMT, 2), (2, 300, 64, nm.PATH_TC, 2),
+    (4, 700, 256, nm.PATH_TC, 2), (4, 130, 64, nm.PATH_TC, 2), (1, 150, 64, nm.PATH_SIMT, 2),
+    (1, 150, 64, nm.PATH_TC, 2), (3, 100, 64, nm.PATH_TC, 2), (1, 90, 64, nm.PATH_SIMT, 3)])
+def test_mag_gate(wid, T, chunk, path, layers):
+    wl = dataclasses.replace(W.WORKLOADS[wid].with_sizes(B=2, H=2, T=T, segment=0), chunk=chunk, layers=layers)
+    if layers > 2:
+        wl = dataclasses.replace(wl, hidden=128)
+    _skip_unsupported(wl, path)
+    x = W.make_inputs(wl, "cuda", seed=170 + T)
+    if wl.kind == nm.MLP2 and layers == 2:
+        M0, S0 = W.random_state(wl, "cuda", seed=171, scale=0.5)
+    elif wl.kind == nm.MLP2:
+        g = torch.Generator("cuda").manual_seed(172)
+        M0 = (0.5 / wl.hidden) ** 0.5 * torch.randn((wl.B, wl.H, wl.P), generator=g, device="cuda")
+        S0 = 0.1 * M0.flip(-1).contiguous()
+        x["eta"] *= 0.5
+    else:
+        M0, S0 = W.random_state(wl, "cuda", seed=171, scale=0.5)
+    g = torch.Generator("cuda").manual_seed(173)
+    y_attn = torch.randn(x["q"].shape, generator=g, device="cuda").to(wl.dtype)
+    mem = nm.NeuralMemory(wl.kind, wl.d, wl.hidden, wl.chunk, in_dtype=wl.dtype, path=path,
+                          layers=layers if wl.kind == nm.MLP2 else 0)
+    args = (x["q"], x["k"], x["v"], x["alpha"], x["eta"], x["beta"], M0, S0)
+    o, MT, ST = mem.forward_gated(*args, y_attn)
+    y, MT2, ST2 = mem.forward(*args)
+    inplace = y_attn.clone()
+    o2, _, _ = mem.forward_gated(*args, inplace, o=inplace)
+    assert mem.synchronize() == nm.NM_OK
+    assert mem.path == path
+    mem.close()
+    assert torch.equal(MT, MT2) and torch.equal(ST, ST2)
+    assert torch.equal(o2, o)
+    ref = oracle.forward(wl.kind, wl.d, wl.hidden, wl.chunk, oracle.C_ONE,
+                         *(f64(x[k_]) for k_ in ("q", "k", "v", "alpha", "eta", "beta")), None, f64(M0), f64(S0),
+                         layers=layers)
+    n = wl.B * wl.H
+    o_ref = oracle.mag_gate(ref[0], f64(y_attn)).reshape(1, n, T, wl.d)
+    compare(wl, (o, MT, ST), (o_ref, ref[1].reshape(1, n, -1), ref[2].reshape(1, n, -1)))
+    # and it is not y itself
+    assert rel_l2(f64(o), ref[0]) > 0.1
