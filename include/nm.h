@@ -190,6 +190,39 @@ int nm_forward_gated(nm_handle_t h, int B, int H, int T,
                      const void* y_attn, void* o, float* M_T, float* S_T, void* stream);
 
 /*
+ * nm_backward - gradients of a loss of the forward's outputs with respect to
+ *   every input, for training what surrounds the memory ("Titans: Imparare a
+ *   Memorizzare al Tempo di Test", "Addestramento Parallelizzato": the inner
+ *   loop is written with matrix products so that the outer loop trains
+ *   fast).  Given the upstream gradients of L with respect to y, M_T and S_T,
+ *   it writes dL/d(every input) of nm_forward on the same inputs:
+ *     inputs: q, k, v, alpha, eta, beta, c, M0, S0 as for nm_forward (DEVICE)
+ *     Gy      [B, H, T, d] fp32   dL/dy
+ *     GM, GS  [B, H, P]    fp32   dL/dM_T, dL/dS_T
+ *     outputs (fp32, written): dq, dk, dv [B, H, T, d]; dalpha, deta, dbeta
+ *     [B, H, T]; dc [B, H, T] for NM_C_PER_TOKEN (must be NULL otherwise;
+ *     with NM_C_ONE_MINUS_BETA the dependence of c on beta is in dbeta);
+ *     dM0, dS0 [B, H, P].
+ *   Memory kinds: NM_LINEAR (d 16..128, chunk <= 256, fp32 or bf16 inputs,
+ *   either loss); others return NM_ERR_UNSUPPORTED.  The gradient is that of
+ *   the chunked forward in fp32 arithmetic: the call first runs the forward
+ *   once more on the fp32 FFMA kernel, recording every chunk's start state in
+ *   a handle-owned workspace (B*H*ceil(T/chunk)*2*P floats plus per-unit
+ *   scratch; it grows on demand, so a first call at a larger size
+ *   allocates), then sweeps the chunks from last to first.  No output may
+ *   overlap any input or another output (NM_ERR_ALIAS).  Asynchronous on
+ *   `stream`; host-side errors return with nothing launched.
+ */
+int nm_backward(nm_handle_t h, int B, int H, int T,
+                const void* q, const void* k, const void* v,
+                const float* alpha, const float* eta, const float* beta,
+                const float* c, const float* M0, const float* S0,
+                const float* Gy, const float* GM, const float* GS,
+                float* dq, float* dk, float* dv,
+                float* dalpha, float* deta, float* dbeta, float* dc,
+                float* dM0, float* dS0, void* stream);
+
+/*
  * nm_forward_host - the same operation on HOST buffers (same layouts).
  *   Copies the inputs to the handle's device (into handle-owned buffers that
  *   grow on demand), runs nm_forward on `stream`, copies y, M_T, S_T back and

@@ -50,7 +50,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libnm.so")
 EXPORTED = ("nm_create", "nm_forward", "nm_forward_host", "nm_synchronize", "nm_destroy",
             "nm_status_string", "nm_selected_path", "nm_launch_count", "nm_inject_missing_load",
-            "nm_forward_mlp2_noalloc", "nm_forward_surprise", "nm_forward_gated")
+            "nm_forward_mlp2_noalloc", "nm_forward_surprise", "nm_forward_gated", "nm_backward")
 
 _DT = {torch.float32: F32, torch.bfloat16: BF16}
 _TORCH_DT = {F32: torch.float32, BF16: torch.bfloat16}
@@ -92,6 +92,8 @@ def load_library() -> ctypes.CDLL:
         lib.nm_forward_surprise.restype = i
         lib.nm_forward_gated.argtypes = fwd[:13] + [vp, vp, f, f, vp]
         lib.nm_forward_gated.restype = i
+        lib.nm_backward.argtypes = [vp, i, i, i] + [vp] * 22
+        lib.nm_backward.restype = i
         lib.nm_synchronize.argtypes = [vp]
         lib.nm_synchronize.restype = i
         lib.nm_destroy.argtypes = [vp]
@@ -250,6 +252,39 @@ class NeuralMemory:
         if rc != NM_OK:
             raise NMError(rc, "nm_forward_gated")
         return o, M_T, S_T
+
+    def backward(self, q, k, v, alpha, eta, beta, M0, S0, Gy, GM, GS, c=None,
+                 stream: Optional[torch.cuda.Stream] = None) -> dict:
+        """Gradients of a loss with upstream gradients Gy = dL/dy [B,H,T,d],
+        GM = dL/dM_T, GS = dL/dS_T [B,H,P] (fp32 device tensors) with respect
+        to every input of forward() on the same inputs: a dict with q, k, v,
+        alpha, eta, beta, M0, S0 (and c for C_PER_TOKEN), all fp32."""
+        B, H, T = self._check(q, k, v, alpha, eta, beta, c, M0, S0, host=False)
+        dev = q.device
+        if Gy.shape != (B, H, T, self.d) or Gy.dtype != torch.float32 or not Gy.is_contiguous():
+            raise ValueError("Gy must be a contiguous float32 [B, H, T, %d] tensor" % self.d)
+        for t in (GM, GS):
+            if t.shape != (B, H, self.P) or t.dtype != torch.float32 or not t.is_contiguous():
+                raise ValueError("GM, GS must be contiguous float32 [B, H, %d] tensors" % self.P)
+        for t in (Gy, GM, GS):
+            if not t.is_cuda or t.device.index != self.device:
+                raise ValueError("backward takes tensors on cuda:%d" % self.device)
+        f = lambda shape: torch.empty(shape, dtype=torch.float32, device=dev)
+        out = {"q": f((B, H, T, self.d)), "k": f((B, H, T, self.d)), "v": f((B, H, T, self.d)),
+               "alpha": f((B, H, T)), "eta": f((B, H, T)), "beta": f((B, H, T)),
+               "c": f((B, H, T)) if self.c_mode == C_PER_TOKEN else None,
+               "M0": f((B, H, self.P)), "S0": f((B, H, self.P))}
+        s = stream if stream is not None else torch.cuda.current_stream(dev)
+        rc = load_library().nm_backward(self._h, B, H, T, _ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(eta),
+                                        _ptr(beta), _ptr(c), _ptr(M0), _ptr(S0), _ptr(Gy), _ptr(GM), _ptr(GS),
+                                        _ptr(out["q"]), _ptr(out["k"]), _ptr(out["v"]), _ptr(out["alpha"]),
+                                        _ptr(out["eta"]), _ptr(out["beta"]), _ptr(out["c"]), _ptr(out["M0"]),
+                                        _ptr(out["S0"]), ctypes.c_void_p(s.cuda_stream))
+        if rc != NM_OK:
+            raise NMError(rc, "nm_backward")
+        if out["c"] is None:
+            del out["c"]
+        return out
 
     def forward_host(self, q, k, v, alpha, eta, beta, M0, S0, c=None, y=None, M_T=None, S_T=None,
                      stream: Optional[torch.cuda.Stream] = None):

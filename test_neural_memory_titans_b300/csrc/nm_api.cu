@@ -236,6 +236,7 @@ int forward_impl(nm_handle_t h, int B, int H, int T, const void* q, const void* 
     a.e_clip = nm_err_clip(cfg);
     a.surprise = surprise;
     a.y_attn = y_attn;
+    a.ckpt = nullptr;
     cudaError_t e = h->path == NM_PATH_TC ? nm_tc_launch(cfg, a, s, h->num_sms, &h->launches)
                                           : nm_simt_launch(cfg, a, s, &h->launches);
     if (e != cudaSuccess) {
@@ -268,6 +269,120 @@ int nm_forward_gated(nm_handle_t h, int B, int H, int T, const void* q, const vo
     if (T > 0 && !y_attn) return NM_ERR_ARG;
     return forward_impl(h, B, H, T, q, k, v, alpha, eta, beta, c, M0, S0, o, M_T, S_T, nullptr, stream,
                         T > 0 ? y_attn : nullptr);
+}
+
+int nm_backward(nm_handle_t h, int B, int H, int T, const void* q, const void* k, const void* v,
+                const float* alpha, const float* eta, const float* beta, const float* c, const float* M0,
+                const float* S0, const float* Gy, const float* GM, const float* GS, float* dq, float* dk,
+                float* dv, float* dalpha, float* deta, float* dbeta, float* dc, float* dM0, float* dS0,
+                void* stream) {
+    if (!h) return NM_ERR_ARG;
+    const nm_config& cfg = h->cfg;
+    if (B < 0 || H < 0 || T < 0) return NM_ERR_ARG;
+    const long long units = (long long)B * H;
+    if (units == 0) return NM_OK;
+    if (units > (1LL << 31) - 1 || (long long)T * cfg.d > (1LL << 40)) return NM_ERR_ARG;
+    if (!nm_bwd_supports(cfg)) return NM_ERR_UNSUPPORTED;
+    const bool need_c = cfg.c_mode == NM_C_PER_TOKEN;
+    if (!M0 || !S0 || !GM || !GS || !dM0 || !dS0) return NM_ERR_ARG;
+    if (T > 0 && (!q || !k || !v || !alpha || !eta || !beta || !Gy || !dq || !dk || !dv || !dalpha || !deta || !dbeta))
+        return NM_ERR_ARG;
+    if (T > 0 && need_c != (c != nullptr)) return NM_ERR_ARG;
+    if (T > 0 && need_c != (dc != nullptr)) return NM_ERR_ARG;
+    if (T == 0 && (c || dc)) return NM_ERR_ARG;
+    const void* ptrs[] = {q, k, v, alpha, eta, beta, c, M0, S0, Gy, GM, GS, dq, dk, dv, dalpha, deta, dbeta, dc,
+                          dM0, dS0};
+    for (const void* p : ptrs)
+        if (p && !aligned16(p)) return NM_ERR_ALIGN;
+    const size_t tok = (size_t)units * (size_t)T;
+    const size_t P = (size_t)nm_param_count(cfg);
+    const size_t in_b = tok * cfg.d * dtype_bytes(cfg.in_dtype), g_b = tok * sizeof(float);
+    const size_t tf_b = tok * cfg.d * sizeof(float), st_b = (size_t)units * P * sizeof(float);
+    Range in_r[] = {{(const char*)q, T ? in_b : 0}, {(const char*)k, T ? in_b : 0}, {(const char*)v, T ? in_b : 0},
+                    {(const char*)alpha, T ? g_b : 0}, {(const char*)eta, T ? g_b : 0},
+                    {(const char*)beta, T ? g_b : 0}, {(const char*)c, need_c && T ? g_b : 0},
+                    {(const char*)M0, st_b}, {(const char*)S0, st_b}, {(const char*)Gy, T ? tf_b : 0},
+                    {(const char*)GM, st_b}, {(const char*)GS, st_b}};
+    Range out_r[] = {{(const char*)dq, T ? tf_b : 0}, {(const char*)dk, T ? tf_b : 0},
+                     {(const char*)dv, T ? tf_b : 0}, {(const char*)dalpha, T ? g_b : 0},
+                     {(const char*)deta, T ? g_b : 0}, {(const char*)dbeta, T ? g_b : 0},
+                     {(const char*)dc, need_c && T ? g_b : 0}, {(const char*)dM0, st_b}, {(const char*)dS0, st_b}};
+    for (const Range& o : out_r) {
+        for (const Range& i : in_r)
+            if (overlaps(o, i)) return NM_ERR_ALIAS;
+        for (const Range& o2 : out_r)
+            if (&o2 != &o && overlaps(o, o2)) return NM_ERR_ALIAS;
+    }
+
+    DeviceGuard g(h->device);
+    if (!g.ok) return NM_ERR_CUDA;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (T == 0) {  // nothing happens between the inputs and the outputs: the state's adjoints pass through
+        if (cudaMemcpyAsync(dM0, GM, st_b, cudaMemcpyDeviceToDevice, s) != cudaSuccess ||
+            cudaMemcpyAsync(dS0, GS, st_b, cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+            return NM_ERR_CUDA;
+        return NM_OK;
+    }
+    // workspace: the chunk-start states of every unit, the forward's final state (not returned), and the
+    // reverse sweep's per-unit scratch
+    const long long nch = ((long long)T + cfg.chunk - 1) / cfg.chunk;
+    auto up = [](size_t n) { return (n + 255) & ~(size_t)255; };
+    const size_t ck_b = up((size_t)units * nch * 2 * P * sizeof(float));
+    const size_t fin_b = up(2 * st_b);
+    const size_t sc_b = up((size_t)units * nm_bwd_linear_ws_floats(cfg.d, cfg.chunk) * sizeof(float));
+    const size_t need = ck_b + fin_b + sc_b;
+    if (need > h->bwd_ws_bytes) {
+        if (h->bwd_ws) cudaFree(h->bwd_ws);
+        h->bwd_ws = nullptr;
+        h->bwd_ws_bytes = 0;
+        if (cudaMalloc(&h->bwd_ws, need) != cudaSuccess) {
+            cudaGetLastError();
+            return NM_ERR_NOMEM;
+        }
+        h->bwd_ws_bytes = need;
+    }
+    char* w = (char*)h->bwd_ws;
+    float* ckpt = (float*)w;
+    float* fin = (float*)(w + ck_b);
+    float* scratch = (float*)(w + ck_b + fin_b);
+
+    // the forward once more, on the fp32 FFMA kernel, recording each chunk's start state (y is not written)
+    nm_config fc = cfg;
+    fc.path = NM_PATH_SIMT;
+    nm_args a;
+    a.B = B; a.H = H; a.T = T;
+    a.q = q; a.k = k; a.v = v;
+    a.alpha = alpha; a.eta = eta; a.beta = beta; a.c = c;
+    a.M0 = M0; a.S0 = S0; a.y = nullptr; a.M_T = fin; a.S_T = fin + units * P;
+    a.status = h->d_status;
+    a.scratch = nullptr;
+    a.scratch_bytes = 0;
+    a.skip_first_load = 0;
+    a.e_clip = nm_err_clip(cfg);
+    a.surprise = nullptr;
+    a.y_attn = nullptr;
+    a.ckpt = ckpt;
+    if (nm_simt_launch(fc, a, s, &h->launches) != cudaSuccess) {
+        cudaGetLastError();
+        return NM_ERR_CUDA;
+    }
+    nm_bwd_call bc;
+    bc.units = units; bc.T = T;
+    bc.q = q; bc.k = k; bc.v = v;
+    bc.alpha = alpha; bc.eta = eta; bc.beta = beta; bc.c = c;
+    bc.ckpt = ckpt;
+    bc.Gy = Gy; bc.GM = GM; bc.GS = GS;
+    bc.dq = dq; bc.dk = dk; bc.dv = dv;
+    bc.dalpha = dalpha; bc.deta = deta; bc.dbeta = dbeta; bc.dc = dc;
+    bc.dM0 = dM0; bc.dS0 = dS0;
+    bc.ws = scratch;
+    bc.e_clip = nm_err_clip(cfg);
+    if (nm_bwd_launch(cfg, bc, s) != cudaSuccess) {
+        cudaGetLastError();
+        return NM_ERR_CUDA;
+    }
+    h->launches += 1;
+    return NM_OK;
 }
 
 int nm_synchronize(nm_handle_t h) {
@@ -457,6 +572,7 @@ int nm_destroy(nm_handle_t h) {
             }
             if (h->workspace) cudaFree(h->workspace);
             if (h->stage) cudaFree(h->stage);
+            if (h->bwd_ws) cudaFree(h->bwd_ws);
             if (h->pipe_ready) {
                 cudaStreamDestroy(h->s_in);
                 cudaStreamDestroy(h->s_out);

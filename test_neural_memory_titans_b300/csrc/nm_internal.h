@@ -33,6 +33,8 @@ struct nm_args {
     float* surprise;  // [B, H, T] per-token gradient norms, or NULL (not computed)
     const void* y_attn;  // [B, H, T, d] of y's type: when set, the call writes o = sigmoid(y) * y_attn
                          // (the Memory-as-Gate combination) in place of y; NULL for the plain forward
+    float* ckpt;         // [B*H][ceil(T / chunk)][2][P] fp32: when set (fp32 FFMA linear kernel, for the
+                         // backward pass), every chunk's start state (M, S); y may then be NULL (not written)
 };
 
 // The error e = d rho / d r of the loss at the residual r = M(k) - v, given
@@ -108,6 +110,8 @@ struct nm_handle {
     size_t workspace_bytes;
     void* stage;       // device staging for nm_forward_host
     size_t stage_bytes;
+    void* bwd_ws;      // device workspace of nm_backward (checkpoints, per-unit scratch), grows on demand
+    size_t bwd_ws_bytes;
     long long launches;
     int inject_load_skip;  // armed by nm_inject_missing_load, consumed by the next nm_forward
     // nm_forward_host's copy / compute overlap (created on first use): streams for the
@@ -132,6 +136,37 @@ static inline long long nm_param_count(const nm_config& c) {
     return c.kind == NM_LINEAR ? (long long)c.d * c.d
                                : 2LL * c.hidden * c.d + (long long)(nm_layers(c) - 2) * c.hidden * c.hidden;
 }
+
+// ---- backward pass (nm_backward.cu) ----------------------------------------
+// One backward call's device pointers, validated on the host.
+struct nm_bwd_call {
+    long long units, T;
+    const void* q;
+    const void* k;
+    const void* v;
+    const float* alpha;
+    const float* eta;
+    const float* beta;
+    const float* c;
+    const float* ckpt;  // chunk-start states from the checkpointing forward
+    const float* Gy;
+    const float* GM;
+    const float* GS;
+    float* dq;
+    float* dk;
+    float* dv;
+    float* dalpha;
+    float* deta;
+    float* dbeta;
+    float* dc;
+    float* dM0;
+    float* dS0;
+    float* ws;
+    float e_clip;
+};
+bool nm_bwd_supports(const nm_config& c);
+size_t nm_bwd_linear_ws_floats(int d, int b);
+cudaError_t nm_bwd_launch(const nm_config& c, const nm_bwd_call& call, cudaStream_t s);
 
 // ---- fp32 FFMA kernels (nm_simt.cu) ----------------------------------------
 bool nm_simt_supports(const nm_config& c);

@@ -124,6 +124,7 @@ extern "C" int nm_forward_mlp2_noalloc(const nm_config* cfg, int B, int H, int T
     a.e_clip = nm_err_clip(run);
     a.surprise = nullptr;
     a.y_attn = nullptr;
+    a.ckpt = nullptr;
     long long launched = 0;
     if (nm_simt_launch(run, a, s, &launched) != cudaSuccess) {
         cudaGetLastError();

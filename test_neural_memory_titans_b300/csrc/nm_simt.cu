@@ -107,6 +107,14 @@ __global__ void __launch_bounds__(D * LIN_R) simt_linear_kernel(nm_args a, int c
         const long long t1 = min(t0 + (long long)chunk, T);
 #pragma unroll
         for (int j = 0; j < J; ++j) W0[j] = M[j];
+        if (a.ckpt) {  // the chunk-start state, for the backward pass
+            float* ck = a.ckpt + (unit * ((T + chunk - 1) / chunk) + t0 / chunk) * 2 * P + (long long)r * D;
+#pragma unroll
+            for (int j = 0; j < J; ++j) {
+                ck[j * R + s] = M[j];
+                ck[P + j * R + s] = S[j];
+            }
+        }
         for (long long sb = t0; sb < t1; sb += LIN_SB) {
             const int n = (int)min((long long)LIN_SB, t1 - sb);
             __syncthreads();
@@ -155,7 +163,7 @@ __global__ void __launch_bounds__(D * LIN_R) simt_linear_kernel(nm_args a, int c
                 }
 #pragma unroll
                 for (int o = R / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-                if (s == 0) st_out(y + (sb + t) * D + r, nm_gated(a, y + (sb + t) * D + r, acc));
+                if (s == 0 && a.y) st_out(y + (sb + t) * D + r, nm_gated(a, y + (sb + t) * D + r, acc));
             }
         }
     }
