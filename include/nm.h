@@ -203,8 +203,9 @@ int nm_forward_gated(nm_handle_t h, int B, int H, int T,
  *     [B, H, T]; dc [B, H, T] for NM_C_PER_TOKEN (must be NULL otherwise;
  *     with NM_C_ONE_MINUS_BETA the dependence of c on beta is in dbeta);
  *     dM0, dS0 [B, H, P].
- *   Memory kinds: NM_LINEAR (d 16..128, chunk <= 256, fp32 or bf16 inputs,
- *   either loss); others return NM_ERR_UNSUPPORTED.  The gradient is that of
+ *   Memory kinds: NM_LINEAR and the 2-layer NM_MLP2 (d 16..128, hidden <= 1024
+ *   a multiple of 32, chunk <= 256, fp32 or bf16 inputs, either loss); deeper
+ *   MLP memories return NM_ERR_UNSUPPORTED.  The gradient is that of
  *   the chunked forward in fp32 arithmetic: the call first runs the forward
  *   once more on the fp32 FFMA kernel, recording every chunk's start state in
  *   a handle-owned workspace (B*H*ceil(T/chunk)*2*P floats plus per-unit

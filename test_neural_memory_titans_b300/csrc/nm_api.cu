@@ -329,8 +329,11 @@ int nm_backward(nm_handle_t h, int B, int H, int T, const void* q, const void* k
     auto up = [](size_t n) { return (n + 255) & ~(size_t)255; };
     const size_t ck_b = up((size_t)units * nch * 2 * P * sizeof(float));
     const size_t fin_b = up(2 * st_b);
-    const size_t sc_b = up((size_t)units * nm_bwd_linear_ws_floats(cfg.d, cfg.chunk) * sizeof(float));
-    const size_t need = ck_b + fin_b + sc_b;
+    const size_t sc_b = up((size_t)units * nm_bwd_ws_floats(cfg) * sizeof(float));
+    nm_config fc = cfg;
+    fc.path = NM_PATH_SIMT;
+    const size_t fw_b = up(nm_simt_scratch_bytes(fc, B, H));  // the forward kernel's own workspace
+    const size_t need = ck_b + fin_b + sc_b + fw_b;
     if (need > h->bwd_ws_bytes) {
         if (h->bwd_ws) cudaFree(h->bwd_ws);
         h->bwd_ws = nullptr;
@@ -345,18 +348,17 @@ int nm_backward(nm_handle_t h, int B, int H, int T, const void* q, const void* k
     float* ckpt = (float*)w;
     float* fin = (float*)(w + ck_b);
     float* scratch = (float*)(w + ck_b + fin_b);
+    void* fw_scratch = fw_b ? (void*)(w + ck_b + fin_b + sc_b) : nullptr;
 
     // the forward once more, on the fp32 FFMA kernel, recording each chunk's start state (y is not written)
-    nm_config fc = cfg;
-    fc.path = NM_PATH_SIMT;
     nm_args a;
     a.B = B; a.H = H; a.T = T;
     a.q = q; a.k = k; a.v = v;
     a.alpha = alpha; a.eta = eta; a.beta = beta; a.c = c;
     a.M0 = M0; a.S0 = S0; a.y = nullptr; a.M_T = fin; a.S_T = fin + units * P;
     a.status = h->d_status;
-    a.scratch = nullptr;
-    a.scratch_bytes = 0;
+    a.scratch = fw_scratch;
+    a.scratch_bytes = fw_b;
     a.skip_first_load = 0;
     a.e_clip = nm_err_clip(cfg);
     a.surprise = nullptr;

@@ -166,6 +166,7 @@ struct nm_bwd_call {
 };
 bool nm_bwd_supports(const nm_config& c);
 size_t nm_bwd_linear_ws_floats(int d, int b);
+size_t nm_bwd_ws_floats(const nm_config& c);  // per-unit scratch of the reverse sweep
 cudaError_t nm_bwd_launch(const nm_config& c, const nm_bwd_call& call, cudaStream_t s);
 
 // ---- fp32 FFMA kernels (nm_simt.cu) ----------------------------------------

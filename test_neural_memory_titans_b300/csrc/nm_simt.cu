@@ -249,6 +249,13 @@ __global__ void __launch_bounds__(MLP_THREADS) simt_mlp_kernel(nm_args a, int d,
 
     for (long long t0 = 0; t0 < T; t0 += b) {
         const int n = (int)min((long long)b, T - t0);
+        if (a.ckpt) {  // the chunk-start state (W1 | W2, S1 | S2), for the backward pass
+            float* ck = a.ckpt + (unit * ((T + b - 1) / b) + t0 / b) * 2 * P;
+            for (long long i = tid; i < P; i += NT) {
+                ck[i] = W1[i];
+                ck[P + i] = S1[i];
+            }
+        }
         for (int i = tid; i < n * d; i += NT) {
             Kf[i] = ld_in(k + t0 * d + i);
             Qf[i] = ld_in(q + t0 * d + i);
@@ -372,7 +379,7 @@ __global__ void __launch_bounds__(MLP_THREADS) simt_mlp_kernel(nm_args a, int d,
                 s2 = fmaf(aj, S2[(long long)o * hd + j], s2);
             }
             for (int i = 0; i <= t; ++i) g = fmaf(Pm[(size_t)t * b + i], E[i * d + o], g);
-            st_out(y + (t0 + t) * d + o, nm_gated(a, y + (t0 + t) * d + o, sA[t] * m2 - sSg[t] * s2 - g));
+            if (a.y) st_out(y + (t0 + t) * d + o, nm_gated(a, y + (t0 + t) * d + o, sA[t] * m2 - sSg[t] * s2 - g));
         }
         __syncthreads();
         // chunk-end state: W = A W0 - sigma S0 - sum_i Gamma_{n-1,i} g_i, S = B S0 + sum_i u_{n-1,i} g_i

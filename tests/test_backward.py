@@ -9,7 +9,7 @@ rounded, where the inputs are bf16) values; the GPU works in fp32.  Each
 gradient is a sum over a chunk of products of fp32-rounded terms (unit
 roundoff 6e-8) carried through ceil(T / chunk) chunks of the reverse sweep,
 whose adjoint recursion contracts by the forgetting factor, so a relative L2
-error of a few 1e-7 is expected (measured: 1e-7 to 5.5e-7 over these cases);
+error of a few 1e-7 is expected (measured: 8e-8 to 1.3e-6 over these cases);
 the bound is 1e-5, ten times tighter than the fp32 forward's 1e-4.
 """
 import dataclasses
@@ -91,12 +91,58 @@ def test_backward_zero_tokens_passes_the_state_adjoints():
     assert torch.equal(got["M0"], up["GM"]) and torch.equal(got["S0"], up["GS"])
 
 
-def test_backward_mlp_is_not_built():
+@pytest.mark.parametrize("d,hidden,T,chunk,dtype,c_mode,delta", [
+    (16, 32, 37, 8, torch.float32, nm.C_ONE, None),
+    (64, 128, 130, 64, torch.bfloat16, nm.C_PER_TOKEN, None),
+    (64, 256, 100, 64, torch.bfloat16, nm.C_ONE_MINUS_BETA, 0.5),
+    (32, 64, 75, 16, torch.float32, nm.C_ONE, 0.3),
+    (128, 256, 70, 64, torch.bfloat16, nm.C_ONE, None),
+])
+def test_backward_mlp_matches_reference(d, hidden, T, chunk, dtype, c_mode, delta):
+    """The 2-layer SiLU MLP memory (the workloads' recipe at these sizes, from
+    random states W ~ N(0, 0.5 / fan_in), step eta halved)."""
+    wl = dataclasses.replace(W.WORKLOADS[1], d=d, hidden=hidden, chunk=chunk, dtype=dtype).with_sizes(B=1, H=2, T=T)
+    seed = 300 + T
+    x = W.make_inputs(wl, "cuda", seed=seed)
+    x["eta"] *= 0.5
+    x["M0"], x["S0"] = W.random_state(wl, "cuda", seed=seed + 1, scale=0.5)
+    if c_mode == nm.C_PER_TOKEN:
+        x["c"] = torch.rand(x["alpha"].shape, device="cuda", generator=torch.Generator("cuda").manual_seed(seed + 2))
+    g = torch.Generator("cuda").manual_seed(seed + 3)
+    up = {"Gy": torch.randn((1, 2, T, d), generator=g, device="cuda"),
+          "GM": torch.randn((1, 2, wl.P), generator=g, device="cuda"),
+          "GS": torch.randn((1, 2, wl.P), generator=g, device="cuda")}
+    loss = nm.LOSS_L2 if delta is None else nm.LOSS_HUBER
+    mem = nm.NeuralMemory(nm.MLP2, d, hidden, chunk, in_dtype=dtype, c_mode=c_mode, loss=loss,
+                          huber_delta=0.0 if delta is None else delta)
+    got = mem.backward(x["q"], x["k"], x["v"], x["alpha"], x["eta"], x["beta"], x["M0"], x["S0"],
+                       up["Gy"], up["GM"], up["GS"], c=x.get("c"))
+    assert mem.synchronize() == nm.NM_OK
+    mem.close()
+    names = NAMES + (("c",) if c_mode == nm.C_PER_TOKEN else ())
+    errs = {}
+    for u in range(2):
+        sel = lambda t: None if t is None else f64(t[0, u])
+        ref = ob.backward(oracle.MLP2, d, hidden, chunk, c_mode, sel(x["q"]), sel(x["k"]), sel(x["v"]),
+                          sel(x["alpha"]), sel(x["eta"]), sel(x["beta"]), sel(x.get("c")), sel(x["M0"]),
+                          sel(x["S0"]), sel(up["Gy"]), sel(up["GM"]), sel(up["GS"]),
+                          oracle.LOSS_L2 if delta is None else oracle.LOSS_HUBER,
+                          np.inf if delta is None else delta)
+        for n_ in names:
+            errs[(n_, u)] = rel_l2(f64(got[n_][0, u]), ref[n_])
+    print({k_: "%.2e" % v_ for k_, v_ in errs.items()})
+    bad = {k_: v_ for k_, v_ in errs.items() if not v_ <= TOL}
+    assert not bad, bad
+
+
+def test_backward_deeper_mlp_is_not_built():
     wl = W.WORKLOADS[1].with_sizes(B=1, H=1, T=64)
     x = W.make_inputs(wl, "cuda")
-    mem = nm.NeuralMemory(nm.MLP2, 64, 256, 64, in_dtype=torch.bfloat16)
+    mem = nm.NeuralMemory(nm.MLP2, 64, 128, 64, in_dtype=torch.bfloat16, layers=3)
+    P = nm.param_count(nm.MLP2, 64, 128, 3)
     Gy = torch.zeros((1, 1, 64, 64), device="cuda")
-    G = torch.zeros((1, 1, wl.P), device="cuda")
+    G = torch.zeros((1, 1, P), device="cuda")
+    M0 = torch.zeros((1, 1, P), device="cuda")
     with pytest.raises(nm.NMError) as ei:
-        mem.backward(x["q"], x["k"], x["v"], x["alpha"], x["eta"], x["beta"], x["M0"], x["S0"], Gy, G, G)
+        mem.backward(x["q"], x["k"], x["v"], x["alpha"], x["eta"], x["beta"], M0, M0, Gy, G, G)
     assert ei.value.status == nm.NM_ERR_UNSUPPORTED
