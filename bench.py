@@ -53,9 +53,18 @@ METRIC = "memory-layer fwd tokens/sec (B*H*T/s) and % of roofline (TC FLOPs vs H
 # DRAM bytes (read + write) per launch of the dominant kernel, from ncu captures summarised under
 # profiles/: workload -> (kernel sources, sha256 prefix of those sources when captured, bytes).
 # A capture describes the kernel it was taken on only: when the sources differ, traffic is null.
+# The 128->512->128 figure is scaled from a capture of a 16384-token slice of the workload (token
+# traffic x 8, plus the state read and written once per call); the streamed workload's is one
+# 65536-token segment call, which is what one launch of its bench step processes.
 NCU_TRAFFIC = {
-    "mlp_64x256_bf16_b4h8_t4096_c64": (("nm_tc_mlp.cu", "tc_common.cuh"), "90384118f1d61292", 61.86e6),
-    "linear_d128_bf16_b8h16_t16384_c64": (("nm_tc_linear.cu", "tc_common.cuh"), "a2afbc7a0329e8ae", 2.116e9),
+    "mlp_64x256_bf16_b4h8_t4096_c64": (("nm_tc_mlp.cu", "tc_common.cuh", "nm_internal.h"), "28bac25edc957911",
+                                       62.58e6),
+    "linear_d128_bf16_b8h16_t16384_c64": (("nm_tc_linear.cu", "tc_common.cuh", "nm_internal.h"), "225ccbed532f1500",
+                                          2.173e9),
+    "mlp_128x512_bf16_b2h16_t131072_c64": (("nm_tc_mlp_wide.cu", "tc_common.cuh", "nm_internal.h"),
+                                           "113046ade5ad0aa9", 4.179e9),
+    "linear_d64_bf16_b1h8_t2097152_c256_seg65536": (("nm_tc_linear64.cu", "tc_common.cuh", "nm_internal.h"),
+                                                    "5c4248d3e888dc17", 256.7e6),
 }
 
 
@@ -100,6 +109,23 @@ def algorithmic(wl) -> dict:
     tokens = wl.B * wl.H * wl.T
     return {"flops": float(f_tok) * tokens, "bytes": float(bytes_tok) * tokens + state_bytes,
             "tokens": tokens, "calls": calls, "bound": "tensor" if wl.kind == 1 else "hbm"}
+
+
+def backward_algorithmic(wl) -> dict:
+    """Algorithmic fp32 flops of one nm_backward call: the reverse sweep's
+    products (linear: 13 d^2 + 5 b d multiply-adds per token; 2-layer MLP:
+    29 d h + 3 b (d + h) per token) plus the checkpointing forward that
+    records the chunk-start states (linear 3 d^2, MLP 11 d h per token)."""
+    d, h, b = wl.d, wl.hidden, wl.chunk
+    if wl.kind == 0:
+        fma_tok = 13 * d * d + 5 * b * d + 3 * d * d
+    else:
+        fma_tok = 29 * d * h + 3 * b * (d + h) + 11 * d * h
+    return {"flops": 2.0 * fma_tok * wl.tokens, "tokens": wl.tokens}
+
+
+# the fp32 FFMA peak of a B300 from its unit counts and clock: 148 SMs x 128 fp32 lanes x 2 flops x 2032 MHz
+FP32_PEAK_TFLOPS = 148 * 128 * 2 * 2.032e9 / 1e12
 
 
 def load_peaks():
@@ -455,6 +481,58 @@ def link_bandwidth(dev, stream, h2d_bytes, d2h_bytes, reps=3):
                     "than both_directions_ms" % reps}
 
 
+def run_backward(args, rank, world, local_rank):
+    """Times nm_backward (gradients of <Gy, y> + <GM, M_T> + <GS, S_T> with
+    respect to every input) on the selected workload: one step = one call
+    over the whole workload (a streamed workload as one call over T)."""
+    import test_neural_memory_titans_b300 as nm
+    from test_neural_memory_titans_b300 import workloads as W
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    wl = workload(args)
+    x = W.make_inputs(wl, dev, seed=1000 + args.workload + 100 * rank)
+    g = torch.Generator(device=dev).manual_seed(7)
+    Gy = torch.randn((wl.B, wl.H, wl.T, wl.d), generator=g, device=dev)
+    GM = torch.randn((wl.B, wl.H, wl.P), generator=g, device=dev)
+    GS = torch.randn((wl.B, wl.H, wl.P), generator=g, device=dev)
+    mem = nm.NeuralMemory(wl.kind, wl.d, wl.hidden, wl.chunk, in_dtype=wl.dtype, device=local_rank)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+
+    def step():
+        mem.backward(x["q"], x["k"], x["v"], x["alpha"], x["eta"], x["beta"], x["M0"], x["S0"], Gy, GM, GS,
+                     stream=stream)
+
+    def check(when):
+        st = mem.synchronize()
+        if st != nm.NM_OK:
+            raise RuntimeError("device status %s: %s" % (when, nm.status_string(st)))
+
+    step_ms, clocks, launches = time_steps(step, args.steps, args.warmup, flush, stream, dev, world, local_rank,
+                                           check, lambda: mem.launches)
+    ms = sum(step_ms) / len(step_ms)
+    if world > 1:
+        t = torch.tensor([ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    alg = backward_algorithmic(wl)
+    achieved = alg["flops"] / (ms * 1e-3) / 1e12
+    mem.close()
+    return {"metric": "memory-layer backward tokens/sec (B*H*T/s)", "value": world * alg["tokens"] / (ms * 1e-3),
+            "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": wl.name, "pass": "backward", "B": wl.B, "H": wl.H, "T": wl.T, "d": wl.d,
+                       "hidden": wl.hidden, "chunk": wl.chunk, "parallelism": "dp%d" % world,
+                       "l2": "flushed between timed steps (256 MB write, outside the step's events)"},
+            "roofline": {"bound": "alu", "achieved": achieved, "peak": FP32_PEAK_TFLOPS, "unit": "TFLOP/s",
+                         "frac": achieved / FP32_PEAK_TFLOPS, "traffic": None,
+                         "peak_source": "derived: 148 SMs x 128 fp32 lanes x 2 flops x 2032 MHz",
+                         "kernel": "nm_backward (fp32 FFMA checkpointing forward + reverse sweep)"},
+            "gpu_launches": launches, "clocks": clocks,
+            "step_ms": {"min": min(step_ms), "median": statistics.median(step_ms), "max": max(step_ms)}}
+
+
 def run_ours(args, rank, world, local_rank):
     import test_neural_memory_titans_b300 as nm
     from test_neural_memory_titans_b300 import workloads as W
@@ -672,6 +750,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-variants", action="store_true", help="skip timing the Huber-loss and surprise forms")
     ap.add_argument("--no-per-workload", action="store_true", help="skip timing the other configurations")
+    ap.add_argument("--backward", action="store_true",
+                    help="time nm_backward (gradients of every input) on the workload instead of the forward")
     ap.add_argument("--layers", type=int, default=None,
                     help="MLP workloads: a memory of this many layers instead of 2 (fp32 FFMA kernel for > 2)")
     ap.add_argument("--cpu-budget", type=float, default=None,
@@ -706,6 +786,8 @@ def main():
     try:
         if args.impl == "reference":
             out = run_reference(args, rank, world)
+        elif args.backward:
+            out = run_backward(args, rank, world, local_rank)
         else:
             out = run_ours(args, rank, world, local_rank)
         if rank == 0 and out is not None:
