@@ -88,6 +88,69 @@ __device__ float block_sum(float v, float* red) {
     return s;
 }
 
+// ---------------------------------------------------------------- block GEMM (fp32 FFMA)
+// C(m, n) = alpha sum_k A(m, k) B(k, n) [+ C(m, n) if accumulate], m < M, n < N, over the whole block.
+// A(m, k) = A[m am + k ak], B(k, n) = B[k bk + n bn], C(m, n) = C[m cm + n].  Tiles of 64 x 64 outputs,
+// K in steps of 16 staged in shared memory (loaded along whichever dimension is contiguous, so the global
+// reads coalesce), 4 x 4 outputs per thread.  Ends with the block synchronised.
+constexpr int GM_T = 64, GK_T = 16;
+constexpr int GEMM_SMEM_FLOATS = 2 * GM_T * GK_T;
+
+__device__ void block_gemm(int M, int N, int K, const float* A, long long am, long long ak, const float* B,
+                           long long bk, long long bn, float* C, long long cm, float alpha, bool accumulate,
+                           float* sh) {
+    float* As = sh;                 // [GK_T][GM_T]
+    float* Bs = sh + GM_T * GK_T;   // [GK_T][GM_T]
+    const int tid = threadIdx.x;
+    const int tr = tid >> 4, tc = tid & 15;
+    for (int m0 = 0; m0 < M; m0 += GM_T) {
+        for (int n0 = 0; n0 < N; n0 += GM_T) {
+            float acc[4][4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+            for (int k0 = 0; k0 < K; k0 += GK_T) {
+                __syncthreads();
+                for (int e = tid; e < GM_T * GK_T; e += BW_THREADS) {
+                    int mm, kk;
+                    if (ak == 1) { mm = e / GK_T; kk = e % GK_T; } else { kk = e / GM_T; mm = e % GM_T; }
+                    const int m = m0 + mm, k = k0 + kk;
+                    As[kk * GM_T + mm] = (m < M && k < K) ? A[m * am + k * ak] : 0.f;
+                    int nn, kb;
+                    if (bn == 1) { kb = e / GM_T; nn = e % GM_T; } else { nn = e / GK_T; kb = e % GK_T; }
+                    const int n = n0 + nn, kq = k0 + kb;
+                    Bs[kb * GM_T + nn] = (n < N && kq < K) ? B[kq * bk + n * bn] : 0.f;
+                }
+                __syncthreads();
+#pragma unroll
+                for (int kk = 0; kk < GK_T; ++kk) {
+                    const float4 a4 = *reinterpret_cast<const float4*>(As + kk * GM_T + 4 * tr);
+                    const float4 b4 = *reinterpret_cast<const float4*>(Bs + kk * GM_T + 4 * tc);
+                    const float av[4] = {a4.x, a4.y, a4.z, a4.w}, bv[4] = {b4.x, b4.y, b4.z, b4.w};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int m = m0 + 4 * tr + i;
+                if (m >= M) continue;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int n = n0 + 4 * tc + j;
+                    if (n >= N) continue;
+                    float* c = C + m * cm + n;
+                    *c = accumulate ? fmaf(alpha, acc[i][j], *c) : alpha * acc[i][j];
+                }
+            }
+        }
+    }
+    __syncthreads();
+}
+
 template <typename Tin>
 __global__ void __launch_bounds__(BW_THREADS) bwd_linear_kernel(bwd_args a, int d, int b, int c_mode) {
     __shared__ float s_a[BW_MAX_CHUNK], s_e[BW_MAX_CHUNK], s_b[BW_MAX_CHUNK], s_c[BW_MAX_CHUNK];
@@ -96,6 +159,7 @@ __global__ void __launch_bounds__(BW_THREADS) bwd_linear_kernel(bwd_args a, int 
     __shared__ float s_gA[BW_MAX_CHUNK], s_gS[BW_MAX_CHUNK], s_hg[BW_MAX_CHUNK], s_hu[BW_MAX_CHUNK];
     __shared__ float s_da[BW_MAX_CHUNK], s_de[BW_MAX_CHUNK], s_db[BW_MAX_CHUNK], s_dc[BW_MAX_CHUNK];
     __shared__ float red[BW_THREADS / 32];
+    __shared__ __align__(16) float gsh[GEMM_SMEM_FLOATS];
 
     const long long unit = blockIdx.x;
     const int tid = threadIdx.x;
@@ -111,24 +175,28 @@ __global__ void __launch_bounds__(BW_THREADS) bwd_linear_kernel(bwd_args a, int 
     const float* cc = a.c ? a.c + unit * T : nullptr;
     const float* Gy_u = a.Gy + unit * T * d;
 
-    float* GM = a.ws + unit * a.ws_unit;  // [d][d] running adjoint of M (of the current chunk's end state)
-    float* GS = GM + P;                  // [d][d] running adjoint of S
-    float* Kf = GS + P;                  // [b][d] the chunk's k, q, v, Gy in fp32
-    float* Qf = Kf + (size_t)b * d;
-    float* Vf = Qf + (size_t)b * d;
-    float* Gyf = Vf + (size_t)b * d;
-    float* E = Gyf + (size_t)b * d;      // [b][d] e_i
-    float* LR = E + (size_t)b * d;       // [b][d] 2 (Mc k_i - v_i), then lambda_r_i
-    float* Mq = LR + (size_t)b * d;      // [b][d] Mc q_t
-    float* Sq = Mq + (size_t)b * d;      // [b][d] Sc q_t
-    float* GMk = Sq + (size_t)b * d;     // [b][d] GM k_i
-    float* GSk = GMk + (size_t)b * d;    // [b][d] GS k_i
-    float* GMtE = GSk + (size_t)b * d;   // [b][d] GM^T e_i
-    float* GStE = GMtE + (size_t)b * d;  // [b][d] GS^T e_i
-    float* Gam = GStE + (size_t)b * d;   // [b][b] Gamma_{t,i}
-    float* U = Gam + (size_t)b * b;      // [b][b] u_{t,i}
-    float* QK = U + (size_t)b * b;       // [b][b] q_t . k_i
-    float* Z = QK + (size_t)b * b;       // [b][b] Gy_t . e_i (i <= t)
+    float* p_ = a.ws + unit * a.ws_unit;
+    auto take = [&](size_t n_) { float* r_ = p_; p_ += n_; return r_; };
+    const size_t bd = (size_t)b * d, bb = (size_t)b * b;
+    float* GM = take(P);   // [d][d] running adjoint of M (of the current chunk's end state)
+    float* GS = take(P);   // [d][d] running adjoint of S
+    float* TM = take(P);   // [d][d] the chunk's products for dMc, dSc
+    float* TS = take(P);
+    float *Kf = take(bd), *Qf = take(bd), *Vf = take(bd), *Gyf = take(bd);  // the chunk's k, q, v, Gy in fp32
+    float* E = take(bd);     // e_i
+    float* LR = take(bd);    // 2 (Mc k_i - v_i), then lambda_r_i
+    float* Mq = take(bd);    // Mc q_t
+    float* Sq = take(bd);    // Sc q_t
+    float* GMk = take(bd);   // GM k_i
+    float* GSk = take(bd);   // GS k_i
+    float* GMtE = take(bd);  // GM^T e_i
+    float* GStE = take(bd);  // GS^T e_i
+    float* DK = take(bd);    // dk accumulator
+    float* DQ1 = take(bd);   // Gy_t Mc (as rows: (Mc^T Gy_t)^T)
+    float* DQ2 = take(bd);   // Gy_t Sc
+    float* LE = take(bd);    // -(Gamma (.) QK)^T Gy, then (Gamma (.) Z) K
+    float* SG = take(bd);    // A_t Gy_t, then sigma_t Gy_t
+    float *Gam = take(bb), *U = take(bb), *QK = take(bb), *Z = take(bb), *PQ = take(bb), *PZ = take(bb);
 
     for (int i = tid; i < P; i += BW_THREADS) {
         GM[i] = a.GM[unit * P + i];
@@ -177,80 +245,56 @@ __global__ void __launch_bounds__(BW_THREADS) bwd_linear_kernel(bwd_args a, int 
                 sA[t] = A; sB[t] = Bc; sS[t] = sg;
             }
         }
-        // ---- r_i = Mc k_i - v_i (as 2 r in LR), e_i, Mc q_t, Sc q_t
+        // ---- Mc k_i, Mc q_t, Sc q_t, q_t . k_i  (B(x, o) = Mc[o][x])
+        block_gemm(n, d, d, Kf, d, 1, Mc, 1, d, LR, d, 1.0f, false, gsh);
+        block_gemm(n, d, d, Qf, d, 1, Mc, 1, d, Mq, d, 1.0f, false, gsh);
+        block_gemm(n, d, d, Qf, d, 1, Sc, 1, d, Sq, d, 1.0f, false, gsh);
+        block_gemm(n, n, d, Qf, d, 1, Kf, 1, d, QK, b, 1.0f, false, gsh);
+        // ---- e_i = clip(2 (Mc k_i - v_i)); P_Q = Gamma (.) QK (lower triangle)
         for (int idx = tid; idx < n * d; idx += BW_THREADS) {
-            const int i = idx / d, o = idx % d;
-            const float* mr = Mc + (size_t)o * d;
-            const float* sr = Sc + (size_t)o * d;
-            const float* kr = Kf + (size_t)i * d;
-            const float* qr = Qf + (size_t)i * d;
-            float rk = 0.f, mq = 0.f, sq = 0.f;
-            for (int x = 0; x < d; ++x) {
-                rk = fmaf(mr[x], kr[x], rk);
-                mq = fmaf(mr[x], qr[x], mq);
-                sq = fmaf(sr[x], qr[x], sq);
-            }
-            const float r2 = 2.0f * (rk - Vf[idx]);
+            const float r2 = 2.0f * (LR[idx] - Vf[idx]);
             LR[idx] = r2;
             E[idx] = nm_clip_err(r2, a.e_clip);
-            Mq[idx] = mq;
-            Sq[idx] = sq;
         }
-        __syncthreads();
-        // ---- QK, Z; GM k_i, GS k_i, GM^T e_i, GS^T e_i
         for (int idx = tid; idx < n * n; idx += BW_THREADS) {
             const int t = idx / n, i = idx % n;
-            float qk = 0.f, z = 0.f;
-            for (int x = 0; x < d; ++x) {
-                qk = fmaf(Qf[t * d + x], Kf[i * d + x], qk);
-                z = fmaf(Gyf[t * d + x], E[i * d + x], z);
-            }
-            QK[t * b + i] = qk;
-            Z[t * b + i] = i <= t ? z : 0.0f;
-        }
-        for (int idx = tid; idx < n * d; idx += BW_THREADS) {
-            const int i = idx / d, o = idx % d;
-            float gmk = 0.f, gsk = 0.f, gme = 0.f, gse = 0.f;
-            for (int x = 0; x < d; ++x) {
-                const float kx = Kf[i * d + x], ex = E[i * d + x];
-                gmk = fmaf(GM[o * d + x], kx, gmk);
-                gsk = fmaf(GS[o * d + x], kx, gsk);
-                gme = fmaf(GM[x * d + o], ex, gme);  // (GM^T e_i)[o]
-                gse = fmaf(GS[x * d + o], ex, gse);
-            }
-            GMk[idx] = gmk;
-            GSk[idx] = gsk;
-            GMtE[idx] = gme;
-            GStE[idx] = gse;
+            PQ[t * b + i] = i <= t ? Gam[t * b + i] * QK[t * b + i] : 0.0f;
         }
         __syncthreads();
-        // ---- lambda_e, lambda_r = 2 [inside the clip] lambda_e, dv = -lambda_r
+        // ---- Z = Gy E^T; GM k_i, GS k_i (B(x, o) = G[o][x]); GM^T e_i, GS^T e_i (B(o, x) = G[o][x])
+        block_gemm(n, n, d, Gyf, d, 1, E, 1, d, Z, b, 1.0f, false, gsh);
+        block_gemm(n, d, d, Kf, d, 1, GM, 1, d, GMk, d, 1.0f, false, gsh);
+        block_gemm(n, d, d, Kf, d, 1, GS, 1, d, GSk, d, 1.0f, false, gsh);
+        block_gemm(n, d, d, E, d, 1, GM, d, 1, GMtE, d, 1.0f, false, gsh);
+        block_gemm(n, d, d, E, d, 1, GS, d, 1, GStE, d, 1.0f, false, gsh);
+        // ---- lambda_e (first part): -(Gamma (.) QK)^T Gy   (A(i, t) = P_Q[t][i])
+        block_gemm(n, d, n, PQ, 1, b, Gyf, d, 1, LE, d, -1.0f, false, gsh);
+        for (int idx = tid; idx < n * n; idx += BW_THREADS) {
+            const int t = idx / n, i = idx % n;
+            const float z = i <= t ? Z[t * b + i] : 0.0f;
+            Z[t * b + i] = z;
+            PZ[t * b + i] = Gam[t * b + i] * z;
+        }
+        // ---- lambda_e = ... - gamma_i GM k_i + u_i GS k_i; lambda_r = 2 [inside the clip] lambda_e; dv = -lambda_r
         for (int idx = tid; idx < n * d; idx += BW_THREADS) {
-            const int i = idx / d, o = idx % d;
-            float le = -s_gam[i] * GMk[idx] + s_u[i] * GSk[idx];
-            for (int t = i; t < n; ++t) le = fmaf(-Gam[t * b + i] * QK[t * b + i], Gyf[t * d + o], le);
+            const int i = idx / d;
+            const float le = LE[idx] - s_gam[i] * GMk[idx] + s_u[i] * GSk[idx];
             const float r2 = LR[idx];
             const float lr = (r2 <= a.e_clip && r2 >= -a.e_clip) ? 2.0f * le : 0.0f;
             LR[idx] = lr;
             a.dv[(unit * T + t0) * d + idx] = -lr;
         }
         __syncthreads();
-        // ---- dk, dq
+        // ---- dk = -(Gamma (.) Z)^T Q + lambda_r Mc (...) ; dq parts Gy Mc, Gy Sc, (Gamma (.) Z) K
+        block_gemm(n, d, n, PZ, 1, b, Qf, d, 1, DK, d, -1.0f, false, gsh);
+        block_gemm(n, d, d, LR, d, 1, Mc, d, 1, DK, d, 1.0f, true, gsh);
+        block_gemm(n, d, d, Gyf, d, 1, Mc, d, 1, DQ1, d, 1.0f, false, gsh);
+        block_gemm(n, d, d, Gyf, d, 1, Sc, d, 1, DQ2, d, 1.0f, false, gsh);
+        block_gemm(n, d, n, PZ, b, 1, Kf, d, 1, LE, d, 1.0f, false, gsh);
         for (int idx = tid; idx < n * d; idx += BW_THREADS) {
-            const int i = idx / d, x = idx % d;
-            float g = -s_gam[i] * GMtE[idx] + s_u[i] * GStE[idx];
-            for (int t = i; t < n; ++t) g = fmaf(-Gam[t * b + i] * Z[t * b + i], Qf[t * d + x], g);
-            for (int o = 0; o < d; ++o) g = fmaf(Mc[o * d + x], LR[i * d + o], g);
-            a.dk[(unit * T + t0) * d + idx] = g;
-            const int t = i;  // the same index as a token t for dq
-            float mg = 0.f, sgy = 0.f;
-            for (int o = 0; o < d; ++o) {
-                mg = fmaf(Mc[o * d + x], Gyf[t * d + o], mg);
-                sgy = fmaf(Sc[o * d + x], Gyf[t * d + o], sgy);
-            }
-            float dqv = sA[t] * mg - sS[t] * sgy;
-            for (int i2 = 0; i2 <= t; ++i2) dqv = fmaf(-Gam[t * b + i2] * Z[t * b + i2], Kf[i2 * d + x], dqv);
-            a.dq[(unit * T + t0) * d + idx] = dqv;
+            const int i = idx / d;  // also the token t of dq
+            a.dk[(unit * T + t0) * d + idx] = DK[idx] - s_gam[i] * GMtE[idx] + s_u[i] * GStE[idx];
+            a.dq[(unit * T + t0) * d + idx] = sA[i] * DQ1[idx] - sS[i] * DQ2[idx] - LE[idx];
         }
         // ---- scalar adjoints of A, sigma (per token) and of the chunk-end gamma, u (per column)
         for (int t = tid; t < n; t += BW_THREADS) {
@@ -292,6 +336,8 @@ __global__ void __launch_bounds__(BW_THREADS) bwd_linear_kernel(bwd_args a, int 
                 cU = s_b[t] * gu;
             }
         }
+        // ---- A_t Gy_t as rows, for dMc
+        for (int idx = tid; idx < n * d; idx += BW_THREADS) SG[idx] = sA[idx / d] * Gyf[idx];
         __syncthreads();
         // ---- reverse of A_t = a_t A_{t-1}, B_t = beta_t B_{t-1}, sigma_t = a_t sigma_{t-1} + eta_t B_t
         if (tid == 0) {
@@ -310,7 +356,9 @@ __global__ void __launch_bounds__(BW_THREADS) bwd_linear_kernel(bwd_args a, int 
                 cB = s_b[t] * gB;
             }
         }
-        __syncthreads();
+        // ---- dMc = sum_t A_t Gy_t q_t^T + sum_i lambda_r_i k_i^T (+ A GM below)   (A(o, t) = SG[t][o])
+        block_gemm(d, d, n, SG, 1, d, Qf, d, 1, TM, d, 1.0f, false, gsh);
+        block_gemm(d, d, n, LR, 1, d, Kf, d, 1, TM, d, 1.0f, true, gsh);
         for (int t = tid; t < n; t += BW_THREADS) {
             const long long g = unit * T + t0 + t;
             a.dalpha[g] = -s_da[t];  // a_t = 1 - alpha_t
@@ -318,20 +366,16 @@ __global__ void __launch_bounds__(BW_THREADS) bwd_linear_kernel(bwd_args a, int 
             a.dbeta[g] = s_db[t] + (c_mode == NM_C_ONE_MINUS_BETA ? -s_dc[t] : 0.0f);
             if (a.dc) a.dc[g] = s_dc[t];
         }
+        for (int idx = tid; idx < n * d; idx += BW_THREADS) SG[idx] = sS[idx / d] * Gyf[idx];
+        __syncthreads();
+        // ---- dSc = - sum_t sigma_t Gy_t q_t^T (- sigma GM + B GS below)
+        block_gemm(d, d, n, SG, 1, d, Qf, d, 1, TS, d, -1.0f, false, gsh);
         // ---- the chunk-start state's adjoint becomes the previous chunk's (GM, GS), in place
         const float An = sA[n - 1], Bn = sB[n - 1], Sn = sS[n - 1];
         for (int idx = tid; idx < P; idx += BW_THREADS) {
-            const int o = idx / d, x = idx % d;
-            float aq = 0.f, sq = 0.f, lk = 0.f;
-            for (int t = 0; t < n; ++t) {
-                const float gq = Gyf[t * d + o] * Qf[t * d + x];
-                aq = fmaf(sA[t], gq, aq);
-                sq = fmaf(sS[t], gq, sq);
-                lk = fmaf(LR[t * d + o], Kf[t * d + x], lk);
-            }
             const float gm = GM[idx], gs = GS[idx];
-            GS[idx] = -sq - Sn * gm + Bn * gs;
-            GM[idx] = aq + An * gm + lk;
+            GS[idx] = TS[idx] - Sn * gm + Bn * gs;
+            GM[idx] = TM[idx] + An * gm;
         }
     }
     __syncthreads();
@@ -340,6 +384,14 @@ __global__ void __launch_bounds__(BW_THREADS) bwd_linear_kernel(bwd_args a, int 
         a.dS0[unit * P + i] = GS[i];
     }
 }
+
+}  // namespace
+
+size_t nm_bwd_linear_ws_floats(int d, int b) {
+    return 4 * (size_t)d * d + 17 * (size_t)b * d + 6 * (size_t)b * b;
+}
+
+namespace {
 
 // ---------------------------------------------------------------- 2-layer MLP memory
 // M(x) = W2 silu(W1 x).  Per chunk, with the chunk-start (W1, S1, W2, S2):
@@ -367,7 +419,7 @@ __global__ void __launch_bounds__(BW_THREADS) bwd_linear_kernel(bwd_args a, int 
 __device__ __forceinline__ float sig_f(float z) { return 1.0f / (1.0f + expf(-z)); }
 
 __host__ __device__ inline size_t bwd_mlp_ws_floats(int d, int h, int b) {
-    return 4 * (size_t)h * d + 14 * (size_t)b * d + 17 * (size_t)b * h + 6 * (size_t)b * b;
+    return 8 * (size_t)h * d + 18 * (size_t)b * d + 21 * (size_t)b * h + 10 * (size_t)b * b;
 }
 
 template <typename Tin>
@@ -378,6 +430,7 @@ __global__ void __launch_bounds__(BW_THREADS) bwd_mlp_kernel(bwd_args a, int d, 
     __shared__ float s_gA[BW_MAX_CHUNK], s_gS[BW_MAX_CHUNK], s_hg[BW_MAX_CHUNK], s_hu[BW_MAX_CHUNK];
     __shared__ float s_da[BW_MAX_CHUNK], s_de[BW_MAX_CHUNK], s_db[BW_MAX_CHUNK], s_dc[BW_MAX_CHUNK];
     __shared__ float red[BW_THREADS / 32];
+    __shared__ __align__(16) float gsh[GEMM_SMEM_FLOATS];
 
     const long long unit = blockIdx.x;
     const int tid = threadIdx.x;
@@ -394,21 +447,24 @@ __global__ void __launch_bounds__(BW_THREADS) bwd_mlp_kernel(bwd_args a, int d, 
     const float* cc = a.c ? a.c + unit * T : nullptr;
     const float* Gy_u = a.Gy + unit * T * d;
 
-    // running adjoints of the end state, in the packed order: [dL/dW1 | dL/dW2] then [dL/dS1 | dL/dS2]
-    float* GW1 = a.ws + unit * a.ws_unit;  // [h][d]
-    float* GW2 = GW1 + HD;                 // [d][h]
-    float* GS1 = GW2 + HD;                 // [h][d]
-    float* GS2 = GS1 + HD;                 // [d][h]
-    float* p_ = GS2 + HD;
+    float* p_ = a.ws + unit * a.ws_unit;
     auto take = [&](size_t n_) { float* r_ = p_; p_ += n_; return r_; };
+    // running adjoints of the end state, in the packed order: [dL/dW1 | dL/dW2] then [dL/dS1 | dL/dS2]
+    float* GW1 = take(HD);  // [h][d]
+    float* GW2 = take(HD);  // [d][h]
+    float* GS1 = take(HD);  // [h][d]
+    float* GS2 = take(HD);  // [d][h]
+    float *TW1 = take(HD), *TW2 = take(HD), *TS1 = take(HD), *TS2 = take(HD);  // the chunk's products for them
     const size_t bd = (size_t)b * d, bh = (size_t)b * hd, bb = (size_t)b * b;
     float *Kf = take(bd), *Qf = take(bd), *Vf = take(bd), *Gyf = take(bd), *E = take(bd), *R2 = take(bd);
     float *W2b = take(bd), *S2b = take(bd), *G2a = take(bd), *H2a = take(bd), *G1td = take(bd), *H1td = take(bd);
-    float *DE = take(bd), *DK = take(bd);
+    float *DE = take(bd), *DK = take(bd), *SGy = take(bd), *DHW1 = take(bd), *DHS1 = take(bd), *PZhK = take(bd);
     float *Zs = take(bh), *Ak = take(bh), *PH = take(bh), *PP = take(bh), *DL = take(bh), *PSI = take(bh);
     float *Bt = take(bh), *W1q = take(bh), *S1q = take(bh), *DH = take(bh), *DP = take(bh), *DAk = take(bh);
-    float *G1k = take(bh), *H1k = take(bh), *G2te = take(bh), *H2te = take(bh), *DZ = take(bh);
+    float *G1k = take(bh), *H1k = take(bh), *G2te = take(bh), *H2te = take(bh), *DZ = take(bh), *C1 = take(bh);
+    float *GyW2 = take(bh), *GyS2 = take(bh), *SGh = take(bh);
     float *Gam = take(bb), *U = take(bb), *QK = take(bb), *AA = take(bb), *Zy = take(bb), *Zh = take(bb);
+    float *PQ = take(bb), *PZy = take(bb), *PA = take(bb), *PZh = take(bb);
 
     for (long long i = tid; i < P; i += BW_THREADS) {
         GW1[i] = a.GM[unit * P + i];
@@ -458,195 +514,124 @@ __global__ void __launch_bounds__(BW_THREADS) bwd_mlp_kernel(bwd_args a, int d, 
                 sA[t] = A; sB[t] = Bc; sS[t] = sg;
             }
         }
-        // ---- F1: z, a(k), silu'(z); W1 q, S1 q; QK
+        // ---- F1: z = W1 k_i, W1 q_t, S1 q_t (B(x, j) = W1[j][x]); QK
+        block_gemm(n, hd, d, Kf, d, 1, W1c, 1, d, Zs, hd, 1.0f, false, gsh);
+        block_gemm(n, hd, d, Qf, d, 1, W1c, 1, d, W1q, hd, 1.0f, false, gsh);
+        block_gemm(n, hd, d, Qf, d, 1, S1c, 1, d, S1q, hd, 1.0f, false, gsh);
+        block_gemm(n, n, d, Qf, d, 1, Kf, 1, d, QK, b, 1.0f, false, gsh);
         for (int idx = tid; idx < n * hd; idx += BW_THREADS) {
-            const int i = idx / hd, j = idx % hd;
-            const float* w1 = W1c + (size_t)j * d;
-            const float* s1 = S1c + (size_t)j * d;
-            float z = 0.f, wq = 0.f, sq = 0.f;
-            for (int x = 0; x < d; ++x) {
-                z = fmaf(w1[x], Kf[i * d + x], z);
-                wq = fmaf(w1[x], Qf[i * d + x], wq);
-                sq = fmaf(s1[x], Qf[i * d + x], sq);
-            }
-            const float s = sig_f(z);
-            Zs[idx] = z;
+            const float z = Zs[idx], s = sig_f(z);
             Ak[idx] = z * s;
             PH[idx] = s * (1.0f + z * (1.0f - s));
-            W1q[idx] = wq;
-            S1q[idx] = sq;
         }
         for (int idx = tid; idx < n * n; idx += BW_THREADS) {
             const int t = idx / n, i = idx % n;
-            float qk = 0.f;
-            for (int x = 0; x < d; ++x) qk = fmaf(Qf[t * d + x], Kf[i * d + x], qk);
-            QK[t * b + i] = qk;
+            PQ[t * b + i] = i <= t ? Gam[t * b + i] * QK[t * b + i] : 0.0f;
         }
         __syncthreads();
-        // ---- F2: e = clip(2 (W2 a - v))
+        // ---- F2: e = clip(2 (W2 a - v))   (B(j, o) = W2[o][j])
+        block_gemm(n, d, hd, Ak, hd, 1, W2c, 1, hd, R2, d, 1.0f, false, gsh);
         for (int idx = tid; idx < n * d; idx += BW_THREADS) {
-            const int i = idx / d, o = idx % d;
-            const float* w2 = W2c + (size_t)o * hd;
-            float yh = 0.f;
-            for (int j = 0; j < hd; ++j) yh = fmaf(w2[j], Ak[i * hd + j], yh);
-            const float r2 = 2.0f * (yh - Vf[idx]);
+            const float r2 = 2.0f * (R2[idx] - Vf[idx]);
             R2[idx] = r2;
             E[idx] = nm_clip_err(r2, a.e_clip);
         }
         __syncthreads();
-        // ---- F3: p = W2^T e, delta = p (.) silu'(z)
-        for (int idx = tid; idx < n * hd; idx += BW_THREADS) {
-            const int i = idx / hd, j = idx % hd;
-            float p = 0.f;
-            for (int o = 0; o < d; ++o) p = fmaf(W2c[(size_t)o * hd + j], E[i * d + o], p);
-            PP[idx] = p;
-            DL[idx] = p * PH[idx];
-        }
+        // ---- F3: p = W2^T e (B(o, j) = W2[o][j]), delta = p (.) silu'(z)
+        block_gemm(n, hd, d, E, d, 1, W2c, hd, 1, PP, hd, 1.0f, false, gsh);
+        for (int idx = tid; idx < n * hd; idx += BW_THREADS) DL[idx] = PP[idx] * PH[idx];
         __syncthreads();
-        // ---- F4: h_t, b_t = silu(h_t), silu'(h_t)
+        // ---- F4: h_t = A_t W1 q_t - sigma_t S1 q_t - sum_{i<=t} Gamma QK delta_i; b_t = silu(h_t)
+        block_gemm(n, hd, n, PQ, b, 1, DL, hd, 1, C1, hd, 1.0f, false, gsh);
         for (int idx = tid; idx < n * hd; idx += BW_THREADS) {
-            const int t = idx / hd, j = idx % hd;
-            float hh = sA[t] * W1q[idx] - sS[t] * S1q[idx];
-            for (int i = 0; i <= t; ++i) hh = fmaf(-Gam[t * b + i] * QK[t * b + i], DL[i * hd + j], hh);
+            const int t = idx / hd;
+            const float hh = sA[t] * W1q[idx] - sS[t] * S1q[idx] - C1[idx];
             const float s = sig_f(hh);
             Bt[idx] = hh * s;
             PSI[idx] = s * (1.0f + hh * (1.0f - s));
         }
         __syncthreads();
-        // ---- F5: AA, Zy; W2 b_t, S2 b_t
+        // ---- F5: AA = b a^T, Zy = Gy e^T; W2 b_t, S2 b_t
+        block_gemm(n, n, hd, Bt, hd, 1, Ak, 1, hd, AA, b, 1.0f, false, gsh);
+        block_gemm(n, n, d, Gyf, d, 1, E, 1, d, Zy, b, 1.0f, false, gsh);
+        block_gemm(n, d, hd, Bt, hd, 1, W2c, 1, hd, W2b, d, 1.0f, false, gsh);
+        block_gemm(n, d, hd, Bt, hd, 1, S2c, 1, hd, S2b, d, 1.0f, false, gsh);
         for (int idx = tid; idx < n * n; idx += BW_THREADS) {
             const int t = idx / n, i = idx % n;
-            float aa = 0.f, zy = 0.f;
-            for (int j = 0; j < hd; ++j) aa = fmaf(Bt[t * hd + j], Ak[i * hd + j], aa);
-            for (int o = 0; o < d; ++o) zy = fmaf(Gyf[t * d + o], E[i * d + o], zy);
-            AA[t * b + i] = aa;
-            Zy[t * b + i] = i <= t ? zy : 0.0f;
-        }
-        for (int idx = tid; idx < n * d; idx += BW_THREADS) {
-            const int t = idx / d, o = idx % d;
-            const float* w2 = W2c + (size_t)o * hd;
-            const float* s2 = S2c + (size_t)o * hd;
-            float wb = 0.f, sb = 0.f;
-            for (int j = 0; j < hd; ++j) {
-                wb = fmaf(w2[j], Bt[t * hd + j], wb);
-                sb = fmaf(s2[j], Bt[t * hd + j], sb);
-            }
-            W2b[idx] = wb;
-            S2b[idx] = sb;
+            const float zy = i <= t ? Zy[t * b + i] : 0.0f;
+            Zy[t * b + i] = zy;
+            PZy[t * b + i] = Gam[t * b + i] * zy;
+            PA[t * b + i] = i <= t ? Gam[t * b + i] * AA[t * b + i] : 0.0f;
         }
         __syncthreads();
-        // ---- B2: db_t and dh_t = db_t (.) silu'(h_t)
+        // ---- B2: db_t = A_t W2^T Gy_t - sigma_t S2^T Gy_t - sum_i Gamma Zy a_i;  dh_t = db_t (.) silu'(h_t)
+        block_gemm(n, hd, d, Gyf, d, 1, W2c, hd, 1, GyW2, hd, 1.0f, false, gsh);
+        block_gemm(n, hd, d, Gyf, d, 1, S2c, hd, 1, GyS2, hd, 1.0f, false, gsh);
+        block_gemm(n, hd, n, PZy, b, 1, Ak, hd, 1, C1, hd, 1.0f, false, gsh);
         for (int idx = tid; idx < n * hd; idx += BW_THREADS) {
-            const int t = idx / hd, j = idx % hd;
-            float wg = 0.f, sg = 0.f;
-            for (int o = 0; o < d; ++o) {
-                wg = fmaf(W2c[(size_t)o * hd + j], Gyf[t * d + o], wg);
-                sg = fmaf(S2c[(size_t)o * hd + j], Gyf[t * d + o], sg);
-            }
-            float db = sA[t] * wg - sS[t] * sg;
-            for (int i = 0; i <= t; ++i) db = fmaf(-Gam[t * b + i] * Zy[t * b + i], Ak[i * hd + j], db);
-            DH[idx] = db * PSI[idx];
+            const int t = idx / hd;
+            DH[idx] = (sA[t] * GyW2[idx] - sS[t] * GyS2[idx] - C1[idx]) * PSI[idx];
         }
         // ---- B5: the end state's adjoints against the chunk's vectors
-        for (int idx = tid; idx < n * hd; idx += BW_THREADS) {
-            const int i = idx / hd, j = idx % hd;
-            float g1k = 0.f, h1k = 0.f, g2e = 0.f, h2e = 0.f;
-            for (int x = 0; x < d; ++x) {
-                g1k = fmaf(GW1[(size_t)j * d + x], Kf[i * d + x], g1k);
-                h1k = fmaf(GS1[(size_t)j * d + x], Kf[i * d + x], h1k);
-            }
-            for (int o = 0; o < d; ++o) {
-                g2e = fmaf(GW2[(size_t)o * hd + j], E[i * d + o], g2e);
-                h2e = fmaf(GS2[(size_t)o * hd + j], E[i * d + o], h2e);
-            }
-            G1k[idx] = g1k; H1k[idx] = h1k; G2te[idx] = g2e; H2te[idx] = h2e;
-        }
-        for (int idx = tid; idx < n * d; idx += BW_THREADS) {
-            const int i = idx / d, o = idx % d;
-            float g2a = 0.f, h2a = 0.f, g1d = 0.f, h1d = 0.f;
-            for (int j = 0; j < hd; ++j) {
-                g2a = fmaf(GW2[(size_t)o * hd + j], Ak[i * hd + j], g2a);
-                h2a = fmaf(GS2[(size_t)o * hd + j], Ak[i * hd + j], h2a);
-                g1d = fmaf(GW1[(size_t)j * d + o], DL[i * hd + j], g1d);  // (G1^T delta_i)[x = o]
-                h1d = fmaf(GS1[(size_t)j * d + o], DL[i * hd + j], h1d);
-            }
-            G2a[idx] = g2a; H2a[idx] = h2a; G1td[idx] = g1d; H1td[idx] = h1d;
-        }
-        __syncthreads();
-        // ---- B3: Zh; B4: dq
+        block_gemm(n, hd, d, Kf, d, 1, GW1, 1, d, G1k, hd, 1.0f, false, gsh);   // G1 k_i
+        block_gemm(n, hd, d, Kf, d, 1, GS1, 1, d, H1k, hd, 1.0f, false, gsh);   // H1 k_i
+        block_gemm(n, hd, d, E, d, 1, GW2, hd, 1, G2te, hd, 1.0f, false, gsh);  // G2^T e_i
+        block_gemm(n, hd, d, E, d, 1, GS2, hd, 1, H2te, hd, 1.0f, false, gsh);  // H2^T e_i
+        block_gemm(n, d, hd, Ak, hd, 1, GW2, 1, hd, G2a, d, 1.0f, false, gsh);  // G2 a_i
+        block_gemm(n, d, hd, Ak, hd, 1, GS2, 1, hd, H2a, d, 1.0f, false, gsh);  // H2 a_i
+        block_gemm(n, d, hd, DL, hd, 1, GW1, d, 1, G1td, d, 1.0f, false, gsh); // G1^T delta_i
+        block_gemm(n, d, hd, DL, hd, 1, GS1, d, 1, H1td, d, 1.0f, false, gsh); // H1^T delta_i
+        // ---- B3: Zh = dh delta^T; B4: dq
+        block_gemm(n, n, hd, DH, hd, 1, DL, 1, hd, Zh, b, 1.0f, false, gsh);
         for (int idx = tid; idx < n * n; idx += BW_THREADS) {
             const int t = idx / n, i = idx % n;
-            float zh = 0.f;
-            for (int j = 0; j < hd; ++j) zh = fmaf(DH[t * hd + j], DL[i * hd + j], zh);
-            Zh[t * b + i] = i <= t ? zh : 0.0f;
+            const float zh = i <= t ? Zh[t * b + i] : 0.0f;
+            Zh[t * b + i] = zh;
+            PZh[t * b + i] = Gam[t * b + i] * zh;
         }
         __syncthreads();
+        block_gemm(n, d, hd, DH, hd, 1, W1c, d, 1, DHW1, d, 1.0f, false, gsh);
+        block_gemm(n, d, hd, DH, hd, 1, S1c, d, 1, DHS1, d, 1.0f, false, gsh);
+        block_gemm(n, d, n, PZh, b, 1, Kf, d, 1, PZhK, d, 1.0f, false, gsh);
         for (int idx = tid; idx < n * d; idx += BW_THREADS) {
-            const int t = idx / d, x = idx % d;
-            float wd = 0.f, sd = 0.f;
-            for (int j = 0; j < hd; ++j) {
-                wd = fmaf(W1c[(size_t)j * d + x], DH[t * hd + j], wd);
-                sd = fmaf(S1c[(size_t)j * d + x], DH[t * hd + j], sd);
-            }
-            float g = sA[t] * wd - sS[t] * sd;
-            for (int i = 0; i <= t; ++i) g = fmaf(-Gam[t * b + i] * Zh[t * b + i], Kf[i * d + x], g);
-            a.dq[(unit * T + t0) * d + idx] = g;
+            const int t = idx / d;
+            a.dq[(unit * T + t0) * d + idx] = sA[t] * DHW1[idx] - sS[t] * DHS1[idx] - PZhK[idx];
         }
-        // ---- B6: ddelta -> dp and the silu'' part of dz; the direct parts of de, da, dk
+        // ---- B6: ddelta -> dp and the silu'' part of dz; the direct parts of da, de, dk
+        block_gemm(n, hd, n, PQ, 1, b, DH, hd, 1, C1, hd, -1.0f, false, gsh);    // -sum_t Gamma QK dh_t
+        block_gemm(n, hd, n, PZy, 1, b, Bt, hd, 1, DAk, hd, -1.0f, false, gsh);  // -sum_t Gamma Zy b_t
+        block_gemm(n, d, n, PA, 1, b, Gyf, d, 1, DE, d, -1.0f, false, gsh);      // -sum_t Gamma AA Gy_t
+        block_gemm(n, d, n, PZh, 1, b, Qf, d, 1, DK, d, -1.0f, false, gsh);     // -sum_t Gamma Zh q_t
         for (int idx = tid; idx < n * hd; idx += BW_THREADS) {
-            const int i = idx / hd, j = idx % hd;
-            float dd = -s_gam[i] * G1k[idx] + s_u[i] * H1k[idx];
-            float da = -s_gam[i] * G2te[idx] + s_u[i] * H2te[idx];
-            for (int t = i; t < n; ++t) {
-                const float gm = Gam[t * b + i];
-                dd = fmaf(-gm * QK[t * b + i], DH[t * hd + j], dd);
-                da = fmaf(-gm * Zy[t * b + i], Bt[t * hd + j], da);
-            }
+            const int i = idx / hd;
+            const float dd = C1[idx] - s_gam[i] * G1k[idx] + s_u[i] * H1k[idx];
             const float z = Zs[idx], s = sig_f(z);
             DP[idx] = dd * PH[idx];
             DZ[idx] = dd * PP[idx] * (s * (1.0f - s) * (2.0f + z * (1.0f - 2.0f * s)));
-            DAk[idx] = da;
+            DAk[idx] += -s_gam[i] * G2te[idx] + s_u[i] * H2te[idx];
         }
         for (int idx = tid; idx < n * d; idx += BW_THREADS) {
-            const int i = idx / d, o = idx % d;
-            float de = -s_gam[i] * G2a[idx] + s_u[i] * H2a[idx];
-            float dk = -s_gam[i] * G1td[idx] + s_u[i] * H1td[idx];
-            for (int t = i; t < n; ++t) {
-                const float gm = Gam[t * b + i];
-                de = fmaf(-gm * AA[t * b + i], Gyf[t * d + o], de);
-                dk = fmaf(-gm * Zh[t * b + i], Qf[t * d + o], dk);
-            }
-            DE[idx] = de;
-            DK[idx] = dk;
+            const int i = idx / d;
+            DE[idx] += -s_gam[i] * G2a[idx] + s_u[i] * H2a[idx];
+            DK[idx] += -s_gam[i] * G1td[idx] + s_u[i] * H1td[idx];
         }
         __syncthreads();
-        // ---- B7: de += W2 dp; dr = 2 [inside the clip] de; dv = -dr
+        // ---- B7: de += W2 dp (B(j, o) = W2[o][j]); dr = 2 [inside the clip] de; dv = -dr
+        block_gemm(n, d, hd, DP, hd, 1, W2c, 1, hd, DE, d, 1.0f, true, gsh);
         for (int idx = tid; idx < n * d; idx += BW_THREADS) {
-            const int i = idx / d, o = idx % d;
-            const float* w2 = W2c + (size_t)o * hd;
-            float de = DE[idx];
-            for (int j = 0; j < hd; ++j) de = fmaf(w2[j], DP[i * hd + j], de);
             const float r2 = R2[idx];
-            const float dr = (r2 <= a.e_clip && r2 >= -a.e_clip) ? 2.0f * de : 0.0f;
+            const float dr = (r2 <= a.e_clip && r2 >= -a.e_clip) ? 2.0f * DE[idx] : 0.0f;
             R2[idx] = dr;
             a.dv[(unit * T + t0) * d + idx] = -dr;
         }
         __syncthreads();
-        // ---- B8: da += W2^T dr; dz += da (.) silu'(z)
-        for (int idx = tid; idx < n * hd; idx += BW_THREADS) {
-            const int i = idx / hd, j = idx % hd;
-            float da = DAk[idx];
-            for (int o = 0; o < d; ++o) da = fmaf(W2c[(size_t)o * hd + j], R2[i * d + o], da);
-            DZ[idx] = fmaf(da, PH[idx], DZ[idx]);
-        }
+        // ---- B8: da += W2^T dr (B(o, j) = W2[o][j]); dz += da (.) silu'(z)
+        block_gemm(n, hd, d, R2, d, 1, W2c, hd, 1, DAk, hd, 1.0f, true, gsh);
+        for (int idx = tid; idx < n * hd; idx += BW_THREADS) DZ[idx] = fmaf(DAk[idx], PH[idx], DZ[idx]);
         __syncthreads();
-        // ---- B9: dk += W1^T dz
-        for (int idx = tid; idx < n * d; idx += BW_THREADS) {
-            const int i = idx / d, x = idx % d;
-            float g = DK[idx];
-            for (int j = 0; j < hd; ++j) g = fmaf(W1c[(size_t)j * d + x], DZ[i * hd + j], g);
-            a.dk[(unit * T + t0) * d + idx] = g;
-        }
+        // ---- B9: dk += W1^T dz (B(j, x) = W1[j][x])
+        block_gemm(n, d, hd, DZ, hd, 1, W1c, d, 1, DK, d, 1.0f, true, gsh);
+        for (int idx = tid; idx < n * d; idx += BW_THREADS) a.dk[(unit * T + t0) * d + idx] = DK[idx];
         // ---- B10: scalar adjoints of A, sigma and of the chunk-end gamma, u
         for (int t = tid; t < n; t += BW_THREADS) {
             float ga = 0.f, gs = 0.f, hg = 0.f, hu = 0.f;
@@ -692,6 +677,8 @@ __global__ void __launch_bounds__(BW_THREADS) bwd_mlp_kernel(bwd_args a, int d, 
                 cU = s_b[t] * gu;
             }
         }
+        for (int idx = tid; idx < n * hd; idx += BW_THREADS) SGh[idx] = sA[idx / hd] * DH[idx];
+        for (int idx = tid; idx < n * d; idx += BW_THREADS) SGy[idx] = sA[idx / d] * Gyf[idx];
         __syncthreads();
         if (tid == 0) {
             float cA = 0.f, cS = 0.f, cB = 0.f;
@@ -709,7 +696,13 @@ __global__ void __launch_bounds__(BW_THREADS) bwd_mlp_kernel(bwd_args a, int d, 
                 cB = s_b[t] * gB;
             }
         }
-        __syncthreads();
+        // ---- B11: the chunk's products for the chunk-start state's adjoints
+        //      dW1 = sum_t A_t dh_t q_t^T + sum_i dz_i k_i^T; dW2 = sum_t A_t Gy_t b_t^T + sum_i (e_i dp_i^T + dr_i a_i^T)
+        block_gemm(hd, d, n, SGh, 1, hd, Qf, d, 1, TW1, d, 1.0f, false, gsh);
+        block_gemm(hd, d, n, DZ, 1, hd, Kf, d, 1, TW1, d, 1.0f, true, gsh);
+        block_gemm(d, hd, n, SGy, 1, d, Bt, hd, 1, TW2, hd, 1.0f, false, gsh);
+        block_gemm(d, hd, n, E, 1, d, DP, hd, 1, TW2, hd, 1.0f, true, gsh);
+        block_gemm(d, hd, n, R2, 1, d, Ak, hd, 1, TW2, hd, 1.0f, true, gsh);
         for (int t = tid; t < n; t += BW_THREADS) {
             const long long g = unit * T + t0 + t;
             a.dalpha[g] = -s_da[t];
@@ -717,34 +710,19 @@ __global__ void __launch_bounds__(BW_THREADS) bwd_mlp_kernel(bwd_args a, int d, 
             a.dbeta[g] = s_db[t] + (c_mode == NM_C_ONE_MINUS_BETA ? -s_dc[t] : 0.0f);
             if (a.dc) a.dc[g] = s_dc[t];
         }
-        // ---- B11: the chunk-start state's adjoints, in place
+        for (int idx = tid; idx < n * hd; idx += BW_THREADS) SGh[idx] = sS[idx / hd] * DH[idx];
+        for (int idx = tid; idx < n * d; idx += BW_THREADS) SGy[idx] = sS[idx / d] * Gyf[idx];
+        __syncthreads();
+        //      dS1 = - sum_t sigma_t dh_t q_t^T, dS2 = - sum_t sigma_t Gy_t b_t^T  (the state terms below)
+        block_gemm(hd, d, n, SGh, 1, hd, Qf, d, 1, TS1, d, -1.0f, false, gsh);
+        block_gemm(d, hd, n, SGy, 1, d, Bt, hd, 1, TS2, hd, -1.0f, false, gsh);
         const float An = sA[n - 1], Bn = sB[n - 1], Sn = sS[n - 1];
-        for (long long idx = tid; idx < HD; idx += BW_THREADS) {  // W1, S1 [h][d]
-            const int j = (int)(idx / d), x = (int)(idx % d);
-            float aq = 0.f, sq = 0.f, zk = 0.f;
-            for (int t = 0; t < n; ++t) {
-                const float hq = DH[t * hd + j] * Qf[t * d + x];
-                aq = fmaf(sA[t], hq, aq);
-                sq = fmaf(sS[t], hq, sq);
-                zk = fmaf(DZ[t * hd + j], Kf[t * d + x], zk);
-            }
-            const float gw = GW1[idx], gs = GS1[idx];
-            GS1[idx] = -sq - Sn * gw + Bn * gs;
-            GW1[idx] = aq + An * gw + zk;
-        }
-        for (long long idx = tid; idx < HD; idx += BW_THREADS) {  // W2, S2 [d][h]
-            const int o = (int)(idx / hd), j = (int)(idx % hd);
-            float ab = 0.f, sb = 0.f, ed = 0.f;
-            for (int t = 0; t < n; ++t) {
-                const float gb = Gyf[t * d + o] * Bt[t * hd + j];
-                ab = fmaf(sA[t], gb, ab);
-                sb = fmaf(sS[t], gb, sb);
-                ed = fmaf(E[t * d + o], DP[t * hd + j], ed);
-                ed = fmaf(R2[t * d + o], Ak[t * hd + j], ed);
-            }
-            const float gw = GW2[idx], gs = GS2[idx];
-            GS2[idx] = -sb - Sn * gw + Bn * gs;
-            GW2[idx] = ab + An * gw + ed;
+        for (long long idx = tid; idx < HD; idx += BW_THREADS) {
+            const float g1 = GW1[idx], h1 = GS1[idx], g2 = GW2[idx], h2 = GS2[idx];
+            GS1[idx] = TS1[idx] - Sn * g1 + Bn * h1;
+            GW1[idx] = TW1[idx] + An * g1;
+            GS2[idx] = TS2[idx] - Sn * g2 + Bn * h2;
+            GW2[idx] = TW2[idx] + An * g2;
         }
     }
     __syncthreads();
@@ -755,10 +733,6 @@ __global__ void __launch_bounds__(BW_THREADS) bwd_mlp_kernel(bwd_args a, int d, 
 }
 
 }  // namespace
-
-size_t nm_bwd_linear_ws_floats(int d, int b) {
-    return 2 * (size_t)d * d + 12 * (size_t)b * d + 4 * (size_t)b * b;
-}
 
 size_t nm_bwd_ws_floats(const nm_config& c) {
     return c.kind == NM_LINEAR ? nm_bwd_linear_ws_floats(c.d, c.chunk) : bwd_mlp_ws_floats(c.d, c.hidden, c.chunk);
