@@ -28,8 +28,16 @@
 //     e for its rows and all-gathers e^T as bf16 into every CTA;
 //   * the retrieval y: the partials [o][t] are reduce-scattered the same way
 //     and each owner writes its rows of y.
-// Four cluster barriers per chunk order the exchanges (one receive buffer
-// serves both reduce-scatters).
+// The exchanges use st.async: each 16- or 8-byte store into a peer's shared
+// memory counts its bytes on the peer's mbarrier when it lands, so a sender
+// never waits (a release fence or cluster barrier stalls each thread until its
+// remote stores are acknowledged) and a receiver waits, bounded, on its own
+// mbarrier for exactly the bytes the peers owe it in this chunk.  The two
+// reduce-scatters have separate receive buffers; with the causal order of the
+// exchanges (a peer's next stores into a buffer depend on data that this CTA
+// sent after reading it) no cluster barrier is needed inside the chunk loop.
+// Each pair of products that shares its A operand (W1 | S1, W2 | S2, and the
+// W1 / S1 query projections) is one N = 128 product over two adjacent B tiles.
 //
 // Precision of the gradient path.  Operands are hi/lo pairs of bf16 tiles
 // (x = hi + lo, lo = bf16(x - bf16(x)); a product takes A_hi B_hi + A_lo B_hi +
@@ -94,8 +102,9 @@ struct Layout {
     static constexpr uint32_t DGLO = S1;            // [64 t][64 j] -gamma delta lo: E3 .. G4
     static constexpr uint32_t DULO = S1 + T64;      // [64 t][64 j] u delta lo: E3 .. G4
     static constexpr uint32_t V = GM + 64 * GST * 2;              // bf16 [64 t][OR] this CTA's columns of v
-    static constexpr uint32_t RX = V + 64 * OR * 2;               // bf16 [NC-1][OR][RBS] partials from the peers
-    static constexpr uint32_t F = RX + (NC - 1) * OR * RBS * 2;   // gates [4][64], A, B, sigma, gamma, u
+    static constexpr uint32_t RX = V + 64 * OR * 2;               // bf16 [NC-1][OR][RBS] key-forward partials
+    static constexpr uint32_t RX2 = RX + (NC - 1) * OR * RBS * 2; // bf16 [NC-1][OR][RBS] retrieval partials
+    static constexpr uint32_t F = RX2 + (NC - 1) * OR * RBS * 2;  // gates [4][64], A, B, sigma, gamma, u
     static constexpr uint32_t SP = F + 4 * (4 * BC + 5 * BC);  // surprise: fp32 [4][64] this CTA's ||a||^2,
                                                              // ||delta||^2, ||e||^2, ||k||^2; [2][3][64] cluster sums
     static constexpr uint32_t BAR = SP + 4 * (10 * BC);
@@ -104,7 +113,13 @@ struct Layout {
     static_assert(BYTES <= 232448, "shared memory budget");
     static_assert(AQ == AK + T64 && P == DU + T64, "stacked operands");
     static_assert(AKU == AKG + T64 && DG == DT + T64, "the lo tiles span two consecutive 64-row tiles");
-    static_assert(GM % 128 == 0 && V % 128 == 0 && RX % 16 == 0 && (RBS * 2) % 16 == 0, "alignment");
+    // paired B operands of the N = 128 products
+    static_assert(S1 == W1 + T128 && DU == DG + T64 && DULO == DGLO + T64 && AKULO == AKGLO + T128, "pairs");
+    static_assert(GM % 128 == 0 && V % 128 == 0 && RX % 16 == 0 && RX2 % 16 == 0 && (RBS * 2) % 16 == 0, "alignment");
+    // transaction bytes each CTA receives per chunk: the peers' partials of its
+    // owned rows (either exchange), and the peers' rows of e^T (hi and lo)
+    static constexpr uint32_t TX_PART = (NC - 1) * OR * BC * 2;
+    static constexpr uint32_t TX_E = (NC - 1) * OR * BC * 4;
     // the owner's own partial rows (fp32 [OR][RXS]) during an exchange live in
     // the delta tiles, which are dead at both exchange points
     static_assert(OR * RXS * 4 <= 3 * T64, "own partial fits the delta tiles");
@@ -126,6 +141,11 @@ constexpr uint32_t COL_PE = 384;   // G6: [o][t] partial sum_i P2[t][i] e_i
 constexpr uint32_t ID_KB = idesc_bf16_f32(128, 64, false, true);  // A K-major, B MN-major
 constexpr uint32_t ID_KK = idesc_bf16_f32(128, 64, false, false);
 constexpr uint32_t ID_MB = idesc_bf16_f32(128, 64, true, true);   // A MN-major, B MN-major
+// N = 128: two 64-column accumulators side by side (W1 | S1, W2 | S2, XA | XB)
+// from two B tiles whose 64-element MN blocks lie `lbo` bytes apart
+constexpr uint32_t ID_KB2 = idesc_bf16_f32(128, 128, false, true);
+constexpr uint32_t ID_MB2 = idesc_bf16_f32(128, 128, true, true);
+static_assert(COL_S1 == COL_W1 + 64 && COL_S2 == COL_W2 + 64 && COL_XB == COL_XA + 64, "paired accumulators");
 constexpr uint64_t WAIT_NS = 2000000000ull;  // 2 s
 
 // Shared-memory descriptors (sw128_desc fields): K-major, and MN-major with
@@ -185,7 +205,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     float* sU = sGl + BC;
     __nv_bfloat16* Gm = reinterpret_cast<__nv_bfloat16*>(sm + L::GM);
     __nv_bfloat16* RX = reinterpret_cast<__nv_bfloat16*>(sm + L::RX);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::BAR);  // 0: q|k tiles, 1: mma, 2: v slice
+    __nv_bfloat16* RX2 = reinterpret_cast<__nv_bfloat16*>(sm + L::RX2);
+    // 0: q|k tiles, 1: mma, 2: v slice; bytes from the peers: 3 key-forward partials,
+    // 4 rows of e^T, 5 retrieval partials (one phase per chunk each)
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::BAR);
     // per-token surprise sums (used only when SURP): this CTA's partials over its hidden units / owned
     // output rows, and on rank 0 their cluster-wide sums for chunks of even / odd index
     float* sp_loc = reinterpret_cast<float*>(sm + L::SP);  // [a2 | d2 | e2 | k2][64]
@@ -214,8 +237,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int jg0 = HS * rank;            // this CTA's first hidden unit
 
     if (tid == 0) {
-        for (int i = 0; i < 3; ++i) mbar_init(&bars[i], 1);
+        for (int i = 0; i < 6; ++i) mbar_init(&bars[i], 1);
         fence_mbar_init();
+        if (nchunks > 0) {  // chunk 0's expected bytes (the cluster barrier below precedes any peer's stores)
+            mbar_arrive_expect_tx(&bars[3], L::TX_PART);
+            mbar_arrive_expect_tx(&bars[4], L::TX_E);
+            mbar_arrive_expect_tx(&bars[5], L::TX_PART);
+        }
         prefetch_tmap(&tq);
         prefetch_tmap(&tk);
         prefetch_tmap(&tv);
@@ -289,14 +317,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     cluster_sync();
     tc_fence_after();
 
-    const uint32_t aKQ = smem_u32(sm + L::KQ), aW1 = smem_u32(sm + L::W1), aS1 = smem_u32(sm + L::S1);
+    const uint32_t aKQ = smem_u32(sm + L::KQ), aW1 = smem_u32(sm + L::W1);
     const uint32_t aW2 = smem_u32(sm + L::W2), aS2 = smem_u32(sm + L::S2), aAK = smem_u32(sm + L::AK);
-    const uint32_t aAQ = smem_u32(sm + L::AQ), aAKG = smem_u32(sm + L::AKG), aAKU = smem_u32(sm + L::AKU);
+    const uint32_t aAQ = smem_u32(sm + L::AQ), aAKG = smem_u32(sm + L::AKG);
     const uint32_t aET = smem_u32(sm + L::ET), aDT = smem_u32(sm + L::DT), aDG = smem_u32(sm + L::DG);
     const uint32_t aDU = smem_u32(sm + L::DU), aP = smem_u32(sm + L::P);
     const uint32_t aW1lo = smem_u32(sm + L::W1LO), aW2lo = smem_u32(sm + L::W2LO);
-    const uint32_t aAKGlo = smem_u32(sm + L::AKGLO), aAKUlo = smem_u32(sm + L::AKULO), aETlo = smem_u32(sm + L::ETLO);
-    const uint32_t aDGlo = smem_u32(sm + L::DGLO), aDUlo = smem_u32(sm + L::DULO);
+    const uint32_t aAKGlo = smem_u32(sm + L::AKGLO), aETlo = smem_u32(sm + L::ETLO);
+    const uint32_t aDGlo = smem_u32(sm + L::DGLO);
 
     bool failed = false;
     uint32_t mma_phase = 0;
@@ -316,39 +344,51 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tc_fence_after();
     };
     // Sends this thread's 32 partial values of row lr (columns 32 hf ..) to the
-    // CTA owning the row (its exchange slot for this CTA), or keeps them.
+    // CTA owning the row (its slot for this CTA in the receive buffer `rx`,
+    // counted on the owner's mbarrier `xb`), or keeps them.  A CTA whose wait
+    // has given up sends nothing more: it no longer expects bytes itself, and
+    // each peer then gives up at its next wait for this CTA's data.
     float* OWN = reinterpret_cast<float*>(sm + L::DT);  // fp32 [OR][RXS] during an exchange
-    auto scatter_row = [&](const float* v) {
+    auto scatter_row = [&](const float* v, __nv_bfloat16* rx, int xb) {
         const int q_own = lr / OR;
         if (q_own == rank) {
             float* dst = OWN + (size_t)(lr - own_lo) * RXS + 32 * hf;
 #pragma unroll
             for (int q = 0; q < 32; q += 4) *reinterpret_cast<float4*>(dst + q) = make_float4(v[q], v[q + 1], v[q + 2], v[q + 3]);
-        } else {
+        } else if (!failed) {
             // partial sums travel as bf16 (the sums themselves are taken in fp32)
             const int slot = rank < q_own ? rank : rank - 1;
             const uint32_t dst =
-                map_to_rank(smem_u32(RX + ((size_t)slot * OR + (lr - OR * q_own)) * RBS + 32 * hf), (uint32_t)q_own);
+                map_to_rank(smem_u32(rx + ((size_t)slot * OR + (lr - OR * q_own)) * RBS + 32 * hf), (uint32_t)q_own);
+            const uint32_t bar = map_to_rank(smem_u32(&bars[xb]), (uint32_t)q_own);
 #pragma unroll
             for (int q = 0; q < 4; ++q)
-                asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst + 16 * q),
-                             "r"(pack_bf16(v[8 * q], v[8 * q + 1])), "r"(pack_bf16(v[8 * q + 2], v[8 * q + 3])),
-                             "r"(pack_bf16(v[8 * q + 4], v[8 * q + 5])), "r"(pack_bf16(v[8 * q + 6], v[8 * q + 7]))
-                             : "memory");
+                st_async_v4(dst + 16 * q, pack_bf16(v[8 * q], v[8 * q + 1]), pack_bf16(v[8 * q + 2], v[8 * q + 3]),
+                            pack_bf16(v[8 * q + 4], v[8 * q + 5]), pack_bf16(v[8 * q + 6], v[8 * q + 7]), bar);
         }
     };
-    // After the barrier: the sum over the cluster of 4 consecutive columns
-    // (tokens 4 c4 .. 4 c4 + 3) of owned row `row` (own partial + the peers').
-    auto reduce4 = [&](int row, int c4) {
+    // Once the peers' partials have landed: the sum over the cluster of 4
+    // consecutive columns (tokens 4 c4 .. 4 c4 + 3) of owned row `row` (own
+    // partial + the peers' in `rx`).
+    auto reduce4 = [&](int row, int c4, const __nv_bfloat16* rx) {
         float4 acc = *reinterpret_cast<const float4*>(OWN + (size_t)row * RXS + 4 * c4);
 #pragma unroll
         for (int sl = 0; sl < NC - 1; ++sl) {
-            const uint2 w = *reinterpret_cast<const uint2*>(RX + ((size_t)sl * OR + row) * RBS + 4 * c4);
+            const uint2 w = *reinterpret_cast<const uint2*>(rx + ((size_t)sl * OR + row) * RBS + 4 * c4);
             acc.x += bf16_lo(w.x); acc.y += bf16_hi(w.x); acc.z += bf16_lo(w.y); acc.w += bf16_hi(w.y);
         }
         return acc;
     };
     constexpr int TASKS = OR * 16;  // owned rows x 16 groups of 4 tokens
+    // Every thread: this chunk's bytes from the peers on mbarrier `xb` (bounded
+    // wait; `extra` folds in another condition); then thread 0 expects the next
+    // chunk's.  The CTA barrier also completes the own partial rows.
+    auto receive = [&](int xb, uint32_t bytes, int c, bool extra) {
+        bool ok = extra;
+        if (!failed) ok = ok && mbar_wait_cluster(&bars[xb], (uint32_t)(c & 1), WAIT_NS);
+        failed = __syncthreads_or(!ok) || failed;
+        if (tid == 0 && !failed && c + 1 < nchunks) mbar_arrive_expect_tx(&bars[xb], bytes);
+    };
 
     float ds[32];  // silu'(z) of this thread's token row (rows 0..63), kept from E1 to E3
     for (int c = 0; c < nchunks; ++c) {
@@ -373,15 +413,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             tiles_ok = mbar_wait(&bars[0], (uint32_t)(c & 1), WAIT_NS);
             if (tiles_ok) {
                 tc_fence_after();
-                const uint64_t dKQ = kdesc(aKQ), dW1 = mdesc(aW1, T128), dS1 = mdesc(aS1, T128);
-                const uint64_t dW1lo = mdesc(aW1lo, T128);
+                const uint64_t dKQ = kdesc(aKQ), dW1S1 = mdesc(aW1, T128), dW1lo = mdesc(aW1lo, T128);
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {  // 16 features per k-step
                     const uint32_t acc = ks ? 1u : 0u;
                     const uint64_t ka = (ks >> 2) * (T128 >> 4) + KS_K * (ks & 3);
-                    mma_bf16(tm + COL_XA, dKQ + ka, dW1 + KS_M * ks, ID_KB, acc);
+                    mma_bf16(tm + COL_XA, dKQ + ka, dW1S1 + KS_M * ks, ID_KB2, acc);  // [XA | XB]
                     mma_bf16(tm + COL_XA, dKQ + ka, dW1lo + KS_M * ks, ID_KB, 1u);
-                    mma_bf16(tm + COL_XB, dKQ + ka, dS1 + KS_M * ks, ID_KB, acc);
                     mma_bf16(tm + COL_QK, dKQ + ka, dKQ + ka, ID_KK, acc);
                 }
                 mma_commit(&bars[1]);
@@ -528,17 +566,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         {
             float v[32];
             tmem_ld32(tl + COL_YH + 32 * hf, v);
-            scatter_row(v);
+            scatter_row(v, RX, 3);
             bool okv = true;  // the owners read this chunk's v slice
             if (owner && !failed) okv = mbar_wait(&bars[2], (uint32_t)(c & 1), WAIT_NS);
-            failed = __syncthreads_or(!okv) || failed;
-            cluster_sync();  // barrier A
+            receive(3, L::TX_PART, c, okv);
             // every thread: e = 2 (yhat - v) for 4 tokens of an owned row, all-gathered as bf16
             {
                 const __nv_bfloat16* vs = reinterpret_cast<const __nv_bfloat16*>(sm + L::V);
                 for (int task = tid; task < TASKS; task += NTHREADS) {
                     const int row = task >> 4, c4 = task & 15;  // consecutive threads: one row's tokens
-                    const float4 sum = reduce4(row, c4);
+                    const float4 sum = reduce4(row, c4, RX);
                     const float sv[4] = {sum.x, sum.y, sum.z, sum.w};
                     float e[4];
 #pragma unroll
@@ -551,16 +588,20 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     const uint32_t l0 = pack_bf16(bf16_residual(e[0]), bf16_residual(e[1]));
                     const uint32_t l1 = pack_bf16(bf16_residual(e[2]), bf16_residual(e[3]));
                     const uint32_t off = sw128_offset(own_lo + row, 4 * c4, 128);
+                    *reinterpret_cast<uint2*>(sm + L::ET + off) = make_uint2(w0, w1);
+                    *reinterpret_cast<uint2*>(sm + L::ETLO + off) = make_uint2(l0, l1);
+                    // (every peer's W1 copy is dead: its partials, which this row needed, follow its G1)
 #pragma unroll
-                    for (int p = 0; p < NC; ++p) {  // (every CTA's W1 copy is dead: barrier A follows its G1)
-                        const uint32_t dst = map_to_rank(aET + off, (uint32_t)p);
-                        asm volatile("st.shared::cluster.v2.b32 [%0], {%1, %2};" ::"r"(dst), "r"(w0), "r"(w1) : "memory");
-                        const uint32_t dlo = map_to_rank(aETlo + off, (uint32_t)p);
-                        asm volatile("st.shared::cluster.v2.b32 [%0], {%1, %2};" ::"r"(dlo), "r"(l0), "r"(l1) : "memory");
+                    for (int p = 1; p < NC; ++p) {
+                        if (failed) break;
+                        const uint32_t q = (uint32_t)((rank + p) % NC);
+                        const uint32_t bar = map_to_rank(smem_u32(&bars[4]), q);
+                        st_async_v2(map_to_rank(aET + off, q), w0, w1, bar);
+                        st_async_v2(map_to_rank(aETlo + off, q), l0, l1, bar);
                     }
                 }
             }
-            cluster_sync();  // barrier B: e^T complete everywhere
+            receive(4, L::TX_E, c, true);  // e^T complete
         }
         handoff();
         // ---- G3: rows 0..63: (W2^T e_t)[j] (A = e as [t][o] via the e^T tile, MN-major;
@@ -628,23 +669,19 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const bool go4 = !failed;
         if (go4 && tid == 0) {
             const uint64_t dDUP = kdesc(aDU), dDT = mdesc(aDT, T64);
-            const uint64_t dKt = mdesc(aKQ, T128), dDG = mdesc(aDG, T64), dDU = mdesc(aDU, T64);
-            const uint64_t dET = kdesc(aET), dAKG = mdesc(aAKG, T64), dAKU = mdesc(aAKU, T64);
-            const uint64_t dDGlo = mdesc(aDGlo, T64), dDUlo = mdesc(aDUlo, T64), dETlo = kdesc(aETlo);
-            const uint64_t dAKGlo = mdesc(aAKGlo, T64), dAKUlo = mdesc(aAKUlo, T64);
+            const uint64_t dKt = mdesc(aKQ, T128), dDGU = mdesc(aDG, T64), dDGUlo = mdesc(aDGlo, T64);
+            const uint64_t dET = kdesc(aET), dETlo = kdesc(aETlo);
+            const uint64_t dAKGU = mdesc(aAKG, T64), dAKGUlo = mdesc(aAKGlo, T128);
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) {  // 16 tokens per k-step
                 mma_bf16(tm + COL_R1, dDUP + KS_K * ks, dDT + KS_M * ks, ID_KB, ks ? 1u : 0u);
-                mma_bf16(tm + COL_W1, dKt + KS_M * ks, dDG + KS_M * ks, ID_MB, 1u);
-                mma_bf16(tm + COL_W1, dKt + KS_M * ks, dDGlo + KS_M * ks, ID_MB, 1u);
-                mma_bf16(tm + COL_S1, dKt + KS_M * ks, dDU + KS_M * ks, ID_MB, 1u);
-                mma_bf16(tm + COL_S1, dKt + KS_M * ks, dDUlo + KS_M * ks, ID_MB, 1u);
-                mma_bf16(tm + COL_W2, dET + KS_K * ks, dAKG + KS_M * ks, ID_KB, 1u);
-                mma_bf16(tm + COL_W2, dETlo + KS_K * ks, dAKG + KS_M * ks, ID_KB, 1u);
-                mma_bf16(tm + COL_W2, dET + KS_K * ks, dAKGlo + KS_M * ks, ID_KB, 1u);
-                mma_bf16(tm + COL_S2, dET + KS_K * ks, dAKU + KS_M * ks, ID_KB, 1u);
-                mma_bf16(tm + COL_S2, dETlo + KS_K * ks, dAKU + KS_M * ks, ID_KB, 1u);
-                mma_bf16(tm + COL_S2, dET + KS_K * ks, dAKUlo + KS_M * ks, ID_KB, 1u);
+                // [W1^T | S1^T] += K^T [-gamma delta | u delta], hi and lo halves of the right factor
+                mma_bf16(tm + COL_W1, dKt + KS_M * ks, dDGU + KS_M * ks, ID_MB2, 1u);
+                mma_bf16(tm + COL_W1, dKt + KS_M * ks, dDGUlo + KS_M * ks, ID_MB2, 1u);
+                // [W2 | S2] += E^T [-gamma a(k) | u a(k)]: hi x hi, lo x hi, hi x lo
+                mma_bf16(tm + COL_W2, dET + KS_K * ks, dAKGU + KS_M * ks, ID_KB2, 1u);
+                mma_bf16(tm + COL_W2, dETlo + KS_K * ks, dAKGU + KS_M * ks, ID_KB2, 1u);
+                mma_bf16(tm + COL_W2, dET + KS_K * ks, dAKGUlo + KS_M * ks, ID_KB2, 1u);
             }
             mma_commit(&bars[1]);
         }
@@ -710,8 +747,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 const int t = 32 * hf + q;
                 yw[q] = fmaf(sA[t], yw[q], -fmaf(sSg[t], ys[q], pe[q]));
             }
-            scatter_row(yw);
-            {
+            scatter_row(yw, RX2, 5);
+            {  // the new state's bf16 copies meanwhile
                 const bool last = c + 1 == nchunks;
                 float w[32];
 #pragma unroll
@@ -737,7 +774,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     }
                 }
             }
-            cluster_sync();  // barrier C
+            receive(5, L::TX_PART, c, true);
+            if (SURP) cluster_sync();  // rank 0's surprise sums of this chunk are complete
             if (SURP && tid < BC) {
                 // surprise_t = sqrt(||delta_t||^2 ||k_t||^2 + ||e_t||^2 ||a(k_t)||^2), sums over the cluster
                 float* acc = sp_acc + (c & 1) * 3 * BC;
@@ -754,7 +792,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             // every thread: 4 tokens of an owned row of y
             for (int task = tid; task < TASKS; task += NTHREADS) {
                 const int row = task % OR, c4 = task / OR;  // consecutive threads: consecutive rows
-                const float4 sum = reduce4(row, c4);
+                const float4 sum = reduce4(row, c4, RX2);
                 float sv[4] = {sum.x, sum.y, sum.z, sum.w};
                 if (a.y_attn) {  // the gated output: the four y_attn values loaded first
                     const Tout* ya = reinterpret_cast<const Tout*>(a.y_attn) + (unit * T + t0) * D + own_lo + row;
@@ -771,12 +809,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 }
             }
         }
-        // barrier D: the exchange buffer has been read before any peer refills it
-        // for the next chunk; the bf16 state copies are visible to the tensor cores
-        fence_proxy_async();
-        tc_fence_before();
-        cluster_sync();
-        tc_fence_after();
+        // the bf16 state copies are visible to the tensor cores and the own partial
+        // has been read before the next chunk rewrites its tile.  No peer refills a
+        // receive buffer before this CTA has read it: a peer's next key-forward
+        // partials follow its own retrieval sums, which needed this CTA's partials
+        // (sent after it read the key-forward buffer), and its next retrieval
+        // partials follow this CTA's next rows of e^T (sent after it read the
+        // retrieval buffer).
+        handoff();
     }
     if (failed) {
         if (tid == 0 && a.status) atomicExch(a.status, NM_ERR_DEVICE_TIMEOUT);

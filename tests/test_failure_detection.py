@@ -1,8 +1,9 @@
 """Device-side failure detection, tested without a GPU fault.
 
-Every wait of the tensor-core kernels (TMA tiles, tensor-core completion) is
-bounded (2 s).  The test hook nm_inject_missing_load makes the next launch
-skip its first tile loads, so that wait expires: the kernel must record
+Every wait of the tensor-core kernels (TMA tiles, tensor-core completion, the
+peers' bytes of an exchange inside a cluster) is bounded (2 s).  The test hook
+nm_inject_missing_load makes the next launch skip its first tile loads, so
+that wait expires: the kernel must record
 NM_ERR_DEVICE_TIMEOUT in the handle's status word, skip the rest of its
 tensor-core work, exit normally, and leave the context usable, so that the
 next call on the same handle is correct again.
@@ -20,7 +21,7 @@ from _helpers import compare, oracle_forward
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("wid", [2, 1], ids=["linear_d128", "mlp_64x256_cluster"])
+@pytest.mark.parametrize("wid", [2, 1, 3], ids=["linear_d128", "mlp_64x256_cluster", "mlp_128x512_cluster"])
 def test_missing_tile_load_times_out_and_the_handle_recovers(wid):
     wl = W.WORKLOADS[wid].with_sizes(B=1, H=2, T=192)
     x = W.make_inputs(wl, "cuda", seed=3)
