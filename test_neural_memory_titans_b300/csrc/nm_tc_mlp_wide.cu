@@ -105,7 +105,7 @@ struct Layout {
     static constexpr uint32_t RX = V + 64 * OR * 2;               // bf16 [NC-1][OR][RBS] key-forward partials
     static constexpr uint32_t RX2 = RX + (NC - 1) * OR * RBS * 2; // bf16 [NC-1][OR][RBS] retrieval partials
     static constexpr uint32_t F = RX2 + (NC - 1) * OR * RBS * 2;  // gates [4][64], A, B, sigma, gamma, u
-    static constexpr uint32_t SP = F + 4 * (4 * BC + 5 * BC);  // surprise: fp32 [4][64] this CTA's ||a||^2,
+    static constexpr uint32_t SP = F + 4 * (4 * BC + 5 * BC + 4);  // (+ A_n, B_n, sigma_n) surprise: fp32 [4][64] this CTA's ||a||^2,
                                                              // ||delta||^2, ||e||^2, ||k||^2; [2][3][64] cluster sums
     static constexpr uint32_t BAR = SP + 4 * (10 * BC);
     static constexpr uint32_t USED = BAR + 64;
@@ -203,11 +203,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     float* sSg = sBc + BC;
     float* sGl = sSg + BC;
     float* sU = sGl + BC;
+    float* sEnd = sU + BC;  // A_n, B_n, sigma_n of the chunk (computed during the previous chunk)
     __nv_bfloat16* Gm = reinterpret_cast<__nv_bfloat16*>(sm + L::GM);
     __nv_bfloat16* RX = reinterpret_cast<__nv_bfloat16*>(sm + L::RX);
     __nv_bfloat16* RX2 = reinterpret_cast<__nv_bfloat16*>(sm + L::RX2);
     // 0: q|k tiles, 1: mma, 2: v slice; bytes from the peers: 3 key-forward partials,
-    // 4 rows of e^T, 5 retrieval partials (one phase per chunk each)
+    // 4 rows of e^T, 5 retrieval partials (one phase per chunk each); 6: the state
+    // updates are done with the q|k tiles; 7: the products in flight when a wait has given up
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::BAR);
     // per-token surprise sums (used only when SURP): this CTA's partials over its hidden units / owned
     // output rows, and on rank 0 their cluster-wide sums for chunks of even / odd index
@@ -237,7 +239,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int jg0 = HS * rank;            // this CTA's first hidden unit
 
     if (tid == 0) {
-        for (int i = 0; i < 6; ++i) mbar_init(&bars[i], 1);
+        for (int i = 0; i < 8; ++i) mbar_init(&bars[i], 1);
         fence_mbar_init();
         if (nchunks > 0) {  // chunk 0's expected bytes (the cluster barrier below precedes any peer's stores)
             mbar_arrive_expect_tx(&bars[3], L::TX_PART);
@@ -277,10 +279,27 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
     };
 
+    // A_n, B_n, sigma_n (the products and the sigma recursion of the gate scan,
+    // in the scan's order) of the chunk whose gates are staged
+    auto chunk_end = [&]() {
+        float A = 1.f, Bc = 1.f, sg = 0.f;
+#pragma unroll 8
+        for (int t = 0; t < BC; ++t) {
+            const float ga = gates[t], ge = gates[BC + t], gb = gates[2 * BC + t];
+            A *= ga;
+            Bc *= gb;
+            sg = fmaf(ga, sg, ge * Bc);
+        }
+        sEnd[0] = A;
+        sEnd[1] = Bc;
+        sEnd[2] = sg;
+    };
+
     load_gates(0);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    if (tid == 224) chunk_end();  // (visible after the cluster barrier below)
     const uint32_t tm = s_tmem;
     const uint32_t tl = tm + ((uint32_t)(32 * qd) << 16);
     if (tid == 0 && nchunks > 0 && !a.skip_first_load) {  // (the test hook leaves chunk 0 unloaded)
@@ -298,8 +317,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
             for (int q = 0; q < 32; ++q) r[q] = w1[(long long)q * D];
             tmem_st32(tl + (which ? COL_S1 : COL_W1) + 32 * hf, r);
-            put_row32(sm + (which ? L::S1 : L::W1), 128, lr, 32 * hf, r);
-            if (!which) put_row32_lo(sm + L::W1LO, 128, lr, 32 * hf, r);
+            if (which) put_row32(sm + L::S1, 128, lr, 32 * hf, r);
+            else put_row32_hilo(sm + L::W1, sm + L::W1LO, 128, lr, 32 * hf, r);
             const float* w2 = src + (long long)hid * D + (long long)lr * hid + jg0 + 32 * hf;
 #pragma unroll
             for (int q = 0; q < 32; q += 4) {
@@ -425,6 +444,29 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 mma_commit(&bars[1]);
             }
         }
+        // rescale the fp32 state for this chunk, W <- A_n W - sigma_n S, S <- B_n S,
+        // while G1 runs (it reads the bf16 copies, not these TMEM columns).  Thread 0
+        // is issuing G1, so warp 4 (the same TMEM lanes) takes warp 0's 32 columns too.
+        auto rescale = [&](int h) {
+            const float An = sEnd[0], Bn = sEnd[1], sn = sEnd[2];
+            float w[32], s[32];
+#pragma unroll
+            for (int pr = 0; pr < 2; ++pr) {
+                const uint32_t cw = (pr ? COL_W2 : COL_W1) + 32 * h, cs = (pr ? COL_S2 : COL_S1) + 32 * h;
+                tmem_ld_n(tl + cw, tl + cs, w, s);
+                // the chunk-start W2 (read before the rescale) as the lo half for G2
+                if (pr) put_row32_lo(sm + L::W2LO, 128, lr, 32 * h, w);
+#pragma unroll
+                for (int q = 0; q < 32; ++q) {
+                    w[q] = fmaf(An, w[q], -sn * s[q]);
+                    s[q] = Bn * s[q];
+                }
+                tmem_st_n(tl + cw, w);
+                tmem_st_n(tl + cs, s);
+            }
+        };
+        if (warp != 0) rescale(hf);
+        if (warp == 4) rescale(0);
         if (tid >= 128 && tid < 128 + BC) {
             // column i of Gamma: Gamma_{t,i} = a_t Gamma_{t-1,i} + eta_t u_{t,i}, zero above the diagonal
             const int i = tid - 128;
@@ -479,35 +521,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         const bool go1 = !failed && !__syncthreads_or(!tiles_ok);
         if (!go1 && !failed) failed = true;
-        // rescale the fp32 state for this chunk: W <- A_n W - sigma_n S, S <- B_n S
-        {
-            const float An = sA[BC - 1], Bn = sBc[BC - 1], sn = sSg[BC - 1];
-            float w[32], s[32];
-#pragma unroll
-            for (int pr = 0; pr < 2; ++pr) {
-                const uint32_t cw = (pr ? COL_W2 : COL_W1) + 32 * hf, cs = (pr ? COL_S2 : COL_S1) + 32 * hf;
-                tmem_ld_n(tl + cw, tl + cs, w, s);
-                // the chunk-start W2 (read before the rescale) as the lo half for G2
-                if (pr) put_row32_lo(sm + L::W2LO, 128, lr, 32 * hf, w);
-#pragma unroll
-                for (int q = 0; q < 32; ++q) {
-                    w[q] = fmaf(An, w[q], -sn * s[q]);
-                    s[q] = Bn * s[q];
-                }
-                tmem_st_n(tl + cw, w);
-                tmem_st_n(tl + cs, s);
-            }
-        }
         mma_wait(go1);
-        // ---- E1: rows 0..63: a(k) = silu(z), silu'(z), and the gamma / u scaled
-        //      a(k); rows 64..127: P1 = Gamma (.) Q K^T
+        // ---- E1: rows 0..63: a(k) = silu(z) (the G2 operand, and in fp32 back into
+        //      the z columns for the scaled copies below) and silu'(z);
+        //      rows 64..127: P1 = Gamma (.) Q K^T
         {
             float v[32];
             if (qd < 2) {
                 tmem_ld32(tl + COL_XA + 32 * hf, v);
                 const int t = lr;
-                const float gm = -sGl[t], uu = sU[t];
-                float o1[32];
 #pragma unroll
                 for (int q = 0; q < 32; ++q) {
                     const float sg = sigmoid_f(v[q]);
@@ -521,14 +543,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     atomicAdd(&sp_loc[t], a2);
                 }
                 put_row32(sm + L::AK, 64, t, 32 * hf, v);
-#pragma unroll
-                for (int q = 0; q < 32; ++q) o1[q] = gm * v[q];
-                put_row32(sm + L::AKG, 64, t, 32 * hf, o1);
-                put_row32_lo(sm + L::AKGLO, 64, t, 32 * hf, o1);
-#pragma unroll
-                for (int q = 0; q < 32; ++q) o1[q] = uu * v[q];
-                put_row32(sm + L::AKU, 64, t, 32 * hf, o1);
-                put_row32_lo(sm + L::AKULO, 64, t, 32 * hf, o1);
+                tmem_st32(tl + COL_XA + 32 * hf, v);
             } else {
                 tmem_ld32(tl + COL_QK + 32 * hf, v);
                 const int t = lr - 64;
@@ -550,6 +565,19 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 mma_bf16(tm + COL_YH, dW2lo + KS_K * ks, dAK + KS_K * ks, ID_KK, 1u);
             }
             mma_commit(&bars[1]);
+        }
+        // ---- E1b while G2 runs (rows 0..63): the gamma / u scaled a(k), hi and lo, for the updates
+        if (qd < 2) {
+            float v[32], o1[32];
+            tmem_ld32(tl + COL_XA + 32 * hf, v);
+            const int t = lr;
+            const float gm = -sGl[t], uu = sU[t];
+#pragma unroll
+            for (int q = 0; q < 32; ++q) o1[q] = gm * v[q];
+            put_row32_hilo(sm + L::AKG, sm + L::AKGLO, 64, t, 32 * hf, o1);
+#pragma unroll
+            for (int q = 0; q < 32; ++q) o1[q] = uu * v[q];
+            put_row32_hilo(sm + L::AKU, sm + L::AKULO, 64, t, 32 * hf, o1);
         }
         // the next chunk's gates (this chunk's are scanned)
         if (gi >= 0 && gi < BC && c + 1 < nchunks) {
@@ -584,13 +612,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         e[k] = t < n ? nm_clip_err(2.0f * (sv[k] - __bfloat162float(vs[t * OR + row])), a.e_clip) : 0.0f;
                         if (SURP) atomicAdd(&sp_loc[2 * BC + t], e[k] * e[k]);
                     }
-                    const uint32_t w0 = pack_bf16(e[0], e[1]), w1 = pack_bf16(e[2], e[3]);
-                    const uint32_t l0 = pack_bf16(bf16_residual(e[0]), bf16_residual(e[1]));
-                    const uint32_t l1 = pack_bf16(bf16_residual(e[2]), bf16_residual(e[3]));
+                    uint32_t w0, w1;
+                    const uint32_t l0 = pack_hi_lo(e[0], e[1], w0), l1 = pack_hi_lo(e[2], e[3], w1);
                     const uint32_t off = sw128_offset(own_lo + row, 4 * c4, 128);
                     *reinterpret_cast<uint2*>(sm + L::ET + off) = make_uint2(w0, w1);
                     *reinterpret_cast<uint2*>(sm + L::ETLO + off) = make_uint2(l0, l1);
-                    // (every peer's W1 copy is dead: its partials, which this row needed, follow its G1)
+                    // (every peer's W1 copy, where e^T lo lands, is dead: its partials,
+                    // which this row needed, follow its G1)
 #pragma unroll
                     for (int p = 1; p < NC; ++p) {
                         if (failed) break;
@@ -617,6 +645,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             mma_commit(&bars[1]);
             if (c + 1 < nchunks) issue_v(c + 1);
         }
+        if (tid == 224 && c + 1 < nchunks) chunk_end();  // the next chunk's gates are staged (G2)
         mma_wait(go3);
         // ---- E3: delta = (W2^T e) (.) silu'(z) and its gamma / u scaled copies (rows 0..63)
         if (qd < 2) {
@@ -635,12 +664,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             put_row32(sm + L::DT, 64, t, 32 * hf, x);
 #pragma unroll
             for (int q = 0; q < 32; ++q) o1[q] = gm * x[q];
-            put_row32(sm + L::DG, 64, t, 32 * hf, o1);
-            put_row32_lo(sm + L::DGLO, 64, t, 32 * hf, o1);
+            put_row32_hilo(sm + L::DG, sm + L::DGLO, 64, t, 32 * hf, o1);
 #pragma unroll
             for (int q = 0; q < 32; ++q) o1[q] = uu * x[q];
-            put_row32(sm + L::DU, 64, t, 32 * hf, o1);
-            put_row32_lo(sm + L::DULO, 64, t, 32 * hf, o1);
+            put_row32_hilo(sm + L::DU, sm + L::DULO, 64, t, 32 * hf, o1);
         } else if (SURP) {  // ||k_t||^2: row t of the q|k tile's k half, 64 features per thread
             const int t = lr - 64;
             const uint32_t base = smem_u32(sm + L::KQ);
@@ -673,23 +700,37 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             const uint64_t dET = kdesc(aET), dETlo = kdesc(aETlo);
             const uint64_t dAKGU = mdesc(aAKG, T64), dAKGUlo = mdesc(aAKGlo, T128);
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks) {  // 16 tokens per k-step
+            for (int ks = 0; ks < 4; ++ks)  // 16 tokens per k-step
                 mma_bf16(tm + COL_R1, dDUP + KS_K * ks, dDT + KS_M * ks, ID_KB, ks ? 1u : 0u);
-                // [W1^T | S1^T] += K^T [-gamma delta | u delta], hi and lo halves of the right factor
+            mma_commit(&bars[1]);  // E4 needs R1 only
+            // the state updates run on behind E4 (G5's commit covers them):
+            // [W1^T | S1^T] += K^T [-gamma delta | u delta], hi and lo halves of the right factor
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
                 mma_bf16(tm + COL_W1, dKt + KS_M * ks, dDGU + KS_M * ks, ID_MB2, 1u);
                 mma_bf16(tm + COL_W1, dKt + KS_M * ks, dDGUlo + KS_M * ks, ID_MB2, 1u);
-                // [W2 | S2] += E^T [-gamma a(k) | u a(k)]: hi x hi, lo x hi, hi x lo
+            }
+            // [W2 | S2] += E^T [-gamma a(k) | u a(k)]: hi x hi, lo x hi, hi x lo
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
                 mma_bf16(tm + COL_W2, dET + KS_K * ks, dAKGU + KS_M * ks, ID_KB2, 1u);
                 mma_bf16(tm + COL_W2, dETlo + KS_K * ks, dAKGU + KS_M * ks, ID_KB2, 1u);
                 mma_bf16(tm + COL_W2, dET + KS_K * ks, dAKGUlo + KS_M * ks, ID_KB2, 1u);
             }
-            mma_commit(&bars[1]);
+            // the q|k tiles are free once the updates have read K^T and the scaled
+            // a(k) lo tiles (in the q rows): the next chunk's tiles may load
+            mma_commit(&bars[6]);
         }
-        mma_wait(go4);
-        // the next chunk's q|k tiles (K^T and Q have been read)
-        if (tid == 0 && !failed && c + 1 < nchunks) issue_kq(c + 1);
-        // ---- E4 (rows 64..127): h_t = A_t W1 q_t - sigma_t S1 q_t - R1, a_t = silu(h_t)
-        if (qd >= 2) {
+        // ---- E4 (rows 64..127): h_t = A_t W1 q_t - sigma_t S1 q_t - R1, a_t = silu(h_t),
+        //      by the warps of lanes 64..127 as soon as R1 is done (thread 0 may still be
+        //      issuing the updates; the CTA barrier below also carries a failed wait)
+        bool ok4 = true;
+        if (qd >= 2 && go4) {
+            ok4 = mbar_wait(&bars[1], mma_phase, WAIT_NS);
+            tc_fence_after();
+        }
+        if (go4) mma_phase ^= 1u;
+        if (qd >= 2 && ok4) {
             float xa[32], xb[32], r1[32];
             tmem_ld32x3(tl + COL_XA + 32 * hf, tl + COL_XB + 32 * hf, tl + COL_R1 + 32 * hf, xa, xb, r1);
             const int t = lr - 64;
@@ -701,10 +742,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             }
             put_row32(sm + L::AQ, 64, t, 32 * hf, xa);
         }
-        handoff();
+        fence_proxy_async();
+        tc_fence_before();
+        failed = __syncthreads_or(!ok4) || failed;
+        tc_fence_after();
         // ---- G5: [AK; AQ] AK^T -> rows 64..127 a_t . a(k_i); [o][t] partial W2 a_t and S2 a_t
         const bool go5 = !failed;
         if (go5 && tid == 0) {
+            // the next chunk's q|k tiles once the updates are done with them; if this bounded
+            // wait gives up, the next chunk's wait for the tiles fails
+            if (c + 1 < nchunks && mbar_wait(&bars[6], (uint32_t)(c & 1), WAIT_NS)) issue_kq(c + 1);
             const uint64_t dAK = kdesc(aAK), dAQ = kdesc(aAQ), dW2 = kdesc(aW2), dS2 = kdesc(aS2);
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks)
@@ -748,17 +795,18 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 yw[q] = fmaf(sA[t], yw[q], -fmaf(sSg[t], ys[q], pe[q]));
             }
             scatter_row(yw, RX2, 5);
-            {  // the new state's bf16 copies meanwhile
+            // the new state as the next chunk's operands (the bf16 copies) or the output
+            auto copy_state = [&](int m) {
                 const bool last = c + 1 == nchunks;
                 float w[32];
-#pragma unroll
-                for (int m = 0; m < 4; ++m) {
+                {
                     const uint32_t col = (m == 0 ? COL_W1 : m == 1 ? COL_S1 : m == 2 ? COL_W2 : COL_S2) + 32 * hf;
                     tmem_ld32(tl + col, w);
                     if (!last) {
-                        const uint32_t off = m == 0 ? L::W1 : m == 1 ? L::S1 : m == 2 ? L::W2 : L::S2;
-                        put_row32(sm + off, 128, lr, 32 * hf, w);
-                        if (m == 0) put_row32_lo(sm + L::W1LO, 128, lr, 32 * hf, w);  // read by the next G1
+                        if (m == 0)  // W1 and its lo half, read by the next G1
+                            put_row32_hilo(sm + L::W1, sm + L::W1LO, 128, lr, 32 * hf, w);
+                        else
+                            put_row32(sm + (m == 1 ? L::S1 : m == 2 ? L::W2 : L::S2), 128, lr, 32 * hf, w);
                     } else {
                         float* dst = ((m & 1) ? a.S_T : a.M_T) + unit * P;
                         if (m < 2) {  // W1[jg0 + j][x] for x = lr
@@ -773,7 +821,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         }
                     }
                 }
-            }
+            };
+#pragma unroll 1
+            for (int m = 0; m < 4; ++m) copy_state(m);  // meanwhile
             receive(5, L::TX_PART, c, true);
             if (SURP) cluster_sync();  // rank 0's surprise sums of this chunk are complete
             if (SURP && tid < BC) {
@@ -824,6 +874,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         mbar_wait(&bars[0], (uint32_t)(nchunks & 1), WAIT_NS / 4);
         mbar_wait(&bars[2], (uint32_t)(nchunks & 1), WAIT_NS / 4);
         mbar_wait(&bars[1], mma_phase, WAIT_NS);
+        if (tid == 0) {  // a fresh commit tracks every product this thread has issued
+            mma_commit(&bars[7]);
+            mbar_wait(&bars[7], 0u, WAIT_NS);
+        }
     }
     tc_fence_before();
     cluster_sync();

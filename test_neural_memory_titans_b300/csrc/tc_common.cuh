@@ -95,21 +95,62 @@ __device__ __forceinline__ float bf16_residual(float x) {
     return x - __bfloat162float(__float2bfloat16_rn(x));
 }
 
-// put_row32 of the residuals x - bf16(x) of 32 values (the lo halves).
-__device__ __forceinline__ void put_row32_lo(unsigned char* tile, uint32_t rows, uint32_t r, uint32_t c0, const float* v) {
-    float lo[32];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) lo[i] = bf16_residual(v[i]);
-    put_row32(tile, rows, r, c0, lo);
+// The bf16 pair of (x0, x1) in `hi` and the pair of their residuals
+// x - bf16(x) in the return value: one bf16x2 conversion for each pair (the
+// rounded values are read back from the packed word by bit operations).
+__device__ __forceinline__ uint32_t pack_hi_lo(float x0, float x1, uint32_t& hi) {
+    hi = pack_bf16(x0, x1);
+    return pack_bf16(x0 - __uint_as_float(hi << 16), x1 - __uint_as_float(hi & 0xFFFF0000u));
 }
 
-// put_row<W> of the residuals x - bf16(x) of W values.
+// put_row<W> of W values into `hi_tile` and of their residuals (the lo
+// halves) into `lo_tile`, at the same row and columns.
+template <int W>
+__device__ __forceinline__ void put_row_hilo(unsigned char* hi_tile, unsigned char* lo_tile, uint32_t rows, uint32_t r,
+                                             uint32_t c0, const float* v) {
+    const uint32_t bh = smem_u32(hi_tile), bl = smem_u32(lo_tile);
+#pragma unroll
+    for (int q = 0; q < W / 8; ++q) {
+        uint32_t h[4], l[4];
+#pragma unroll
+        for (int p = 0; p < 4; ++p) l[p] = pack_hi_lo(v[8 * q + 2 * p], v[8 * q + 2 * p + 1], h[p]);
+        const uint32_t off = sw128_offset(r, c0 + 8 * q, rows);
+        st_shared_v4(bh + off, h[0], h[1], h[2], h[3]);
+        st_shared_v4(bl + off, l[0], l[1], l[2], l[3]);
+    }
+}
+
+__device__ __forceinline__ void put_row32_hilo(unsigned char* hi_tile, unsigned char* lo_tile, uint32_t rows,
+                                               uint32_t r, uint32_t c0, const float* v) {
+    put_row_hilo<32>(hi_tile, lo_tile, rows, r, c0, v);
+}
+
+// put_row<W> of the residuals x - bf16(x) of W values (the lo halves only).
 template <int W>
 __device__ __forceinline__ void put_row_lo(unsigned char* tile, uint32_t rows, uint32_t r, uint32_t c0, const float* v) {
-    float lo[W];
+    const uint32_t base = smem_u32(tile);
 #pragma unroll
-    for (int i = 0; i < W; ++i) lo[i] = bf16_residual(v[i]);
-    put_row<W>(tile, rows, r, c0, lo);
+    for (int q = 0; q < W / 8; ++q) {
+        uint32_t h[4], l[4];
+#pragma unroll
+        for (int p = 0; p < 4; ++p) l[p] = pack_hi_lo(v[8 * q + 2 * p], v[8 * q + 2 * p + 1], h[p]);
+        st_shared_v4(base + sw128_offset(r, c0 + 8 * q, rows), l[0], l[1], l[2], l[3]);
+    }
+}
+
+__device__ __forceinline__ void put_row32_lo(unsigned char* tile, uint32_t rows, uint32_t r, uint32_t c0, const float* v) {
+    put_row_lo<32>(tile, rows, r, c0, v);
+}
+
+// Bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned) from
+// this CTA's shared memory at `src` into a cluster peer's at `dst` (`dst` and
+// `bar` mapped to the peer), counted on the peer's mbarrier `bar` as
+// transaction bytes.  The source must be visible to the async proxy
+// (fence_proxy_async by its writers, then a CTA barrier).
+__device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst, uint32_t src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "r"(src), "r"(bytes), "r"(bar)
+                 : "memory");
 }
 
 // ------------------------------------------------------------------ mbarrier
