@@ -72,8 +72,10 @@ constexpr int NTHREADS = 256;
 constexpr uint32_t T64 = 64 * 128;    // [64 rows][64 bf16] swizzled tile (8 KB)
 constexpr uint32_t T128 = 128 * 128;  // [128 rows][64 bf16] (16 KB)
 constexpr int GST = 72;               // Gamma row stride (bf16 elements)
-constexpr int RXS = 68;               // row stride of the own partial (floats)
-constexpr int RBS = 72;               // row stride of the peers' partials (bf16 elements)
+// An exchanged partial row holds 64 tokens: fp32 (256 bytes) for the rows a CTA
+// owns, bf16 (128 bytes) for the rows it sends or receives.  Both keep their
+// 16-byte chunks XOR-swizzled by the row (chunk ^ (row & 15), chunk ^ (row & 7))
+// so that reading four tokens of 16 rows or of one row is free of bank conflicts.
 
 template <int NC>
 struct Layout {
@@ -102,9 +104,16 @@ struct Layout {
     static constexpr uint32_t DGLO = S1;            // [64 t][64 j] -gamma delta lo: E3 .. G4
     static constexpr uint32_t DULO = S1 + T64;      // [64 t][64 j] u delta lo: E3 .. G4
     static constexpr uint32_t V = GM + 64 * GST * 2;              // bf16 [64 t][OR] this CTA's columns of v
-    static constexpr uint32_t RX = V + 64 * OR * 2;               // bf16 [NC-1][OR][RBS] key-forward partials
-    static constexpr uint32_t RX2 = RX + (NC - 1) * OR * RBS * 2; // bf16 [NC-1][OR][RBS] retrieval partials
-    static constexpr uint32_t F = RX2 + (NC - 1) * OR * RBS * 2;  // gates [4][64], A, B, sigma, gamma, u
+    static constexpr uint32_t PART = (NC - 1) * OR * 128;  // bytes of the peers' partials of the owned rows
+    static constexpr uint32_t RX = V + 64 * OR * 2;        // bf16 [NC-1][OR][64] key-forward partials
+    static constexpr uint32_t RX2 = RX + PART;             // bf16 [NC-1][OR][64] retrieval partials
+    static constexpr uint32_t F = RX2 + PART;              // gates [4][64], A, B, sigma, gamma, u
+    // the rows sent to the peers, staged as bf16 [NC-1][OR][64] (peer p at p OR rows,
+    // p = (owner - rank - 1) mod NC) for one bulk copy per peer: the key forward's
+    // at the end of the delta tiles (dead from G2 until E3), the retrieval's in
+    // the e^T tile (dead after G6)
+    static constexpr uint32_t STG1 = DT + 3 * T64 - PART;
+    static constexpr uint32_t STG2 = ET;
     static constexpr uint32_t SP = F + 4 * (4 * BC + 5 * BC + 4);  // (+ A_n, B_n, sigma_n) surprise: fp32 [4][64] this CTA's ||a||^2,
                                                              // ||delta||^2, ||e||^2, ||k||^2; [2][3][64] cluster sums
     static constexpr uint32_t BAR = SP + 4 * (10 * BC);
@@ -115,14 +124,14 @@ struct Layout {
     static_assert(AKU == AKG + T64 && DG == DT + T64, "the lo tiles span two consecutive 64-row tiles");
     // paired B operands of the N = 128 products
     static_assert(S1 == W1 + T128 && DU == DG + T64 && DULO == DGLO + T64 && AKULO == AKGLO + T128, "pairs");
-    static_assert(GM % 128 == 0 && V % 128 == 0 && RX % 16 == 0 && RX2 % 16 == 0 && (RBS * 2) % 16 == 0, "alignment");
+    static_assert(GM % 128 == 0 && V % 128 == 0 && RX % 16 == 0 && RX2 % 16 == 0 && STG1 % 16 == 0, "alignment");
     // transaction bytes each CTA receives per chunk: the peers' partials of its
     // owned rows (either exchange), and the peers' rows of e^T (hi and lo)
-    static constexpr uint32_t TX_PART = (NC - 1) * OR * BC * 2;
+    static constexpr uint32_t TX_PART = PART;
     static constexpr uint32_t TX_E = (NC - 1) * OR * BC * 4;
-    // the owner's own partial rows (fp32 [OR][RXS]) during an exchange live in
+    // the owner's own partial rows (fp32 [OR][64]) during an exchange live in
     // the delta tiles, which are dead at both exchange points
-    static_assert(OR * RXS * 4 <= 3 * T64, "own partial fits the delta tiles");
+    static_assert(OR * 256 <= STG1 - DT && PART <= T128, "own partial and staging fit the delta tiles; staging fits e^T");
 };
 
 // TMEM columns
@@ -205,8 +214,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     float* sU = sGl + BC;
     float* sEnd = sU + BC;  // A_n, B_n, sigma_n of the chunk (computed during the previous chunk)
     __nv_bfloat16* Gm = reinterpret_cast<__nv_bfloat16*>(sm + L::GM);
-    __nv_bfloat16* RX = reinterpret_cast<__nv_bfloat16*>(sm + L::RX);
-    __nv_bfloat16* RX2 = reinterpret_cast<__nv_bfloat16*>(sm + L::RX2);
+    const unsigned char* RX = sm + L::RX;
+    const unsigned char* RX2 = sm + L::RX2;
     // 0: q|k tiles, 1: mma, 2: v slice; bytes from the peers: 3 key-forward partials,
     // 4 rows of e^T, 5 retrieval partials (one phase per chunk each); 6: the state
     // updates are done with the q|k tiles; 7: the products in flight when a wait has given up
@@ -362,38 +371,54 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         __syncthreads();
         tc_fence_after();
     };
-    // Sends this thread's 32 partial values of row lr (columns 32 hf ..) to the
-    // CTA owning the row (its slot for this CTA in the receive buffer `rx`,
-    // counted on the owner's mbarrier `xb`), or keeps them.  A CTA whose wait
-    // has given up sends nothing more: it no longer expects bytes itself, and
-    // each peer then gives up at its next wait for this CTA's data.
-    float* OWN = reinterpret_cast<float*>(sm + L::DT);  // fp32 [OR][RXS] during an exchange
-    auto scatter_row = [&](const float* v, __nv_bfloat16* rx, int xb) {
+    // Stages this thread's 32 partial values of row lr (tokens 32 hf ..): a row
+    // this CTA owns stays fp32 in OWN, any other goes as bf16 into the staging
+    // tile `stg` at its owner's peer slot.
+    unsigned char* OWN = sm + L::DT;  // fp32 [OR][64] during an exchange
+    auto stage_row = [&](const float* v, unsigned char* stg) {
         const int q_own = lr / OR;
+        const int r = lr - OR * q_own;  // row within the owner's block
         if (q_own == rank) {
-            float* dst = OWN + (size_t)(lr - own_lo) * RXS + 32 * hf;
+            const uint32_t base = smem_u32(OWN) + (uint32_t)r * 256u;
 #pragma unroll
-            for (int q = 0; q < 32; q += 4) *reinterpret_cast<float4*>(dst + q) = make_float4(v[q], v[q + 1], v[q + 2], v[q + 3]);
-        } else if (!failed) {
-            // partial sums travel as bf16 (the sums themselves are taken in fp32)
-            const int slot = rank < q_own ? rank : rank - 1;
-            const uint32_t dst =
-                map_to_rank(smem_u32(rx + ((size_t)slot * OR + (lr - OR * q_own)) * RBS + 32 * hf), (uint32_t)q_own);
-            const uint32_t bar = map_to_rank(smem_u32(&bars[xb]), (uint32_t)q_own);
+            for (int m = 0; m < 8; ++m) {
+                const uint32_t off = ((uint32_t)((8 * hf + m) ^ (r & 15))) << 4;
+                st_shared_v4(base + off, __float_as_uint(v[4 * m]), __float_as_uint(v[4 * m + 1]),
+                             __float_as_uint(v[4 * m + 2]), __float_as_uint(v[4 * m + 3]));
+            }
+        } else {  // partial sums travel as bf16 (the sums themselves are taken in fp32)
+            const int p = (q_own - rank - 1 + NC) % NC;
+            const uint32_t base = smem_u32(stg) + (uint32_t)(p * OR + r) * 128u;
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
-                st_async_v4(dst + 16 * q, pack_bf16(v[8 * q], v[8 * q + 1]), pack_bf16(v[8 * q + 2], v[8 * q + 3]),
-                            pack_bf16(v[8 * q + 4], v[8 * q + 5]), pack_bf16(v[8 * q + 6], v[8 * q + 7]), bar);
+            for (int m = 0; m < 4; ++m) {
+                const uint32_t off = ((uint32_t)((4 * hf + m) ^ (r & 7))) << 4;
+                st_shared_v4(base + off, pack_bf16(v[8 * m], v[8 * m + 1]), pack_bf16(v[8 * m + 2], v[8 * m + 3]),
+                             pack_bf16(v[8 * m + 4], v[8 * m + 5]), pack_bf16(v[8 * m + 6], v[8 * m + 7]));
+            }
+        }
+    };
+    // Threads 0 .. NC-2, once the staging is visible to the async proxy: one bulk
+    // copy per peer of the rows it owns, into this CTA's slot of its receive
+    // buffer `rx`, counted on its mbarrier `xb`.  A CTA whose wait has given up
+    // sends nothing more: it no longer expects bytes itself, and each peer then
+    // gives up at its next wait for this CTA's data.
+    auto send_rows = [&](const unsigned char* stg, const unsigned char* rx, int xb) {
+        if (tid < NC - 1 && !failed) {
+            const uint32_t q = (uint32_t)((rank + 1 + tid) % NC);
+            const uint32_t slot = (uint32_t)(rank < (int)q ? rank : rank - 1);
+            bulk_copy_to_peer(map_to_rank(smem_u32(rx) + slot * OR * 128u, q), smem_u32(stg) + (uint32_t)tid * OR * 128u,
+                              OR * 128u, map_to_rank(smem_u32(&bars[xb]), q));
         }
     };
     // Once the peers' partials have landed: the sum over the cluster of 4
     // consecutive columns (tokens 4 c4 .. 4 c4 + 3) of owned row `row` (own
     // partial + the peers' in `rx`).
-    auto reduce4 = [&](int row, int c4, const __nv_bfloat16* rx) {
-        float4 acc = *reinterpret_cast<const float4*>(OWN + (size_t)row * RXS + 4 * c4);
+    auto reduce4 = [&](int row, int c4, const unsigned char* rx) {
+        float4 acc = *reinterpret_cast<const float4*>(OWN + row * 256 + (((c4 ^ (row & 15))) << 4));
+        const int off = row * 128 + (((c4 >> 1) ^ (row & 7)) << 4) + (c4 & 1) * 8;
 #pragma unroll
         for (int sl = 0; sl < NC - 1; ++sl) {
-            const uint2 w = *reinterpret_cast<const uint2*>(rx + ((size_t)sl * OR + row) * RBS + 4 * c4);
+            const uint2 w = *reinterpret_cast<const uint2*>(rx + sl * OR * 128 + off);
             acc.x += bf16_lo(w.x); acc.y += bf16_hi(w.x); acc.z += bf16_lo(w.y); acc.w += bf16_hi(w.y);
         }
         return acc;
@@ -467,9 +492,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         };
         if (warp != 0) rescale(hf);
         if (warp == 4) rescale(0);
-        if (tid >= 128 && tid < 128 + BC) {
+        if (tid >= 160 && tid < 160 + BC) {  // (warps 5 and 6: warp 4 rescales for warp 0)
             // column i of Gamma: Gamma_{t,i} = a_t Gamma_{t-1,i} + eta_t u_{t,i}, zero above the diagonal
-            const int i = tid - 128;
+            const int i = tid - 160;
             // from row 0 with u = Gamma = 0 and the start injected,
             // u_t = beta_t u_{t-1} + [t = i] c_i: zero above the diagonal, no branch per row;
             // the next four gates are loaded before this group's stores
@@ -594,10 +619,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         {
             float v[32];
             tmem_ld32(tl + COL_YH + 32 * hf, v);
-            scatter_row(v, RX, 3);
+            stage_row(v, sm + L::STG1);
             bool okv = true;  // the owners read this chunk's v slice
             if (owner && !failed) okv = mbar_wait(&bars[2], (uint32_t)(c & 1), WAIT_NS);
-            receive(3, L::TX_PART, c, okv);
+            fence_proxy_async();
+            failed = __syncthreads_or(!okv) || failed;
+            send_rows(sm + L::STG1, RX, 3);
+            receive(3, L::TX_PART, c, true);
             // every thread: e = 2 (yhat - v) for 4 tokens of an owned row, all-gathered as bf16
             {
                 const __nv_bfloat16* vs = reinterpret_cast<const __nv_bfloat16*>(sm + L::V);
@@ -794,7 +822,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 const int t = 32 * hf + q;
                 yw[q] = fmaf(sA[t], yw[q], -fmaf(sSg[t], ys[q], pe[q]));
             }
-            scatter_row(yw, RX2, 5);
+            stage_row(yw, sm + L::STG2);
+            fence_proxy_async();
+            __syncthreads();
+            send_rows(sm + L::STG2, RX2, 5);
             // the new state as the next chunk's operands (the bf16 copies) or the output
             auto copy_state = [&](int m) {
                 const bool last = c + 1 == nchunks;
@@ -860,12 +891,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             }
         }
         // the bf16 state copies are visible to the tensor cores and the own partial
-        // has been read before the next chunk rewrites its tile.  No peer refills a
-        // receive buffer before this CTA has read it: a peer's next key-forward
-        // partials follow its own retrieval sums, which needed this CTA's partials
-        // (sent after it read the key-forward buffer), and its next retrieval
-        // partials follow this CTA's next rows of e^T (sent after it read the
-        // retrieval buffer).
+        // has been read before the next chunk rewrites its tile.  Nothing is
+        // rewritten while a copy may still read or fill it.  Receive buffers: a
+        // peer's next key-forward partials follow its own retrieval sums, which
+        // needed this CTA's partials (sent after it read the key-forward buffer),
+        // and its next retrieval partials follow this CTA's next rows of e^T (sent
+        // after it read the retrieval buffer).  Staging: the key forward's (in the
+        // delta tiles, next written by E3) is read by copies that every peer has
+        // received before it sends its rows of e^T, which E3 waits for; the
+        // retrieval's (in e^T, next written once the next key-forward partials are
+        // in) is read by copies that every peer has received before it sends those.
         handoff();
     }
     if (failed) {
