@@ -124,11 +124,17 @@ constexpr uint32_t SMEM_USED = OFF_BAR + 64;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;  // slack for the 1024-byte alignment
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 static_assert(OFF_S2 == OFF_W2 + T128, "W2 and S2 copies form one N=128 operand");
+static_assert(OFF_EU == OFF_EG + T64 && OFF_EULO == OFF_EGLO + T64 && OFF_KU == OFF_KG + T64, "paired update operands");
 static_assert(OFF_YX % 1024 == 0, "exchange buffer alignment");
+// bytes the peer sends per chunk: its whole partial key forward [64 t][64 o], and
+// its partial y of this CTA's 32 output columns
+constexpr uint32_t XCH_KEY_BYTES = 64 * 64 * 2;
+constexpr uint32_t XCH_Y_BYTES = 64 * 32 * 2;
 static_assert(OFF_GM % 16 == 0 && (GST * 2) % 16 == 0, "Gamma rows are read 16 bytes at a time");
 
 // TMEM columns
 constexpr uint32_t COL_W1 = 0, COL_S1 = 64, COL_W2 = 128, COL_S2 = 192;
+static_assert(COL_S1 == COL_W1 + 64 && COL_S2 == COL_W2 + 64, "paired update accumulators");
 constexpr uint32_t COL_XA = 256;  // G1: [j][t] W1 q_t (256..319), W1 k_t = z_t (320..383)
 constexpr uint32_t COL_Z = 320;
 constexpr uint32_t COL_XB = 384;  // G1: [j][t] S1 q_t
@@ -142,9 +148,9 @@ constexpr uint32_t COL_PE = 448;  // G6: M=64 [t][o] sum_i P2[t][i] e_i
 
 constexpr uint32_t ID_XA = idesc_bf16_f32(128, 128, false, false);
 constexpr uint32_t ID_M128N64 = idesc_bf16_f32(128, 64, false, false);
-constexpr uint32_t ID_UPD = idesc_bf16_f32(128, 64, false, true);
+// the W | S updates as one N = 128 product over two adjacent B tiles (T64 apart)
+constexpr uint32_t ID_UPD2 = idesc_bf16_f32(128, 128, false, true);
 constexpr uint32_t ID_M64N64_TT = idesc_bf16_f32(64, 64, true, true);
-constexpr uint32_t ID_M64N128_TT = idesc_bf16_f32(64, 128, true, true);
 constexpr uint32_t ID_M64N192_TT = idesc_bf16_f32(64, 192, true, true);
 static_assert(OFF_AK == OFF_S2 + T128 && COL_AA == COL_YW + 128, "N=192 operand and accumulator");
 constexpr uint32_t ID_M64N64_BT = idesc_bf16_f32(64, 64, false, true);
@@ -217,15 +223,14 @@ __device__ __forceinline__ void store_y(float* p, const float* v) {
         reinterpret_cast<float4*>(p)[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
 }
 
-// W values as bf16 into a peer's shared memory (16-byte stores) / back to floats.
+// W values as bf16 into a peer's shared memory (st.async, 16 bytes at a time,
+// counted on the peer's mbarrier `bar`) / back to floats.
 template <int W>
-__device__ __forceinline__ void push_bf16(uint32_t dst, const float* v) {
+__device__ __forceinline__ void push_bf16(uint32_t dst, const float* v, uint32_t bar) {
 #pragma unroll
     for (int q = 0; q < W / 8; ++q)
-        asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst + 16 * q),
-                     "r"(pack_bf16(v[8 * q], v[8 * q + 1])), "r"(pack_bf16(v[8 * q + 2], v[8 * q + 3])),
-                     "r"(pack_bf16(v[8 * q + 4], v[8 * q + 5])), "r"(pack_bf16(v[8 * q + 6], v[8 * q + 7]))
-                     : "memory");
+        st_async_v4(dst + 16 * q, pack_bf16(v[8 * q], v[8 * q + 1]), pack_bf16(v[8 * q + 2], v[8 * q + 3]),
+                    pack_bf16(v[8 * q + 4], v[8 * q + 5]), pack_bf16(v[8 * q + 6], v[8 * q + 7]), bar);
 }
 __device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
     asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
@@ -278,7 +283,8 @@ __global__ void __launch_bounds__(128 * (64 / CW), 1)
     // exchange buffers: the peer's partial sums as bf16 (summed here in fp32)
     __nv_bfloat16* Yx = reinterpret_cast<__nv_bfloat16*>(sm + OFF_YX);  // [64][XS]
     __nv_bfloat16* Yr = reinterpret_cast<__nv_bfloat16*>(sm + OFF_YR);  // [64][RB]
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + OFF_BAR);  // 0: tiles, 1: mma
+    // 0: tiles, 1: mma; the peer's bytes (one phase per chunk each): 2 partial key forward, 3 partial y
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
     // per-token surprise partial sums (written only when SURP)
     float* sp_a2 = reinterpret_cast<float*>(sm + OFF_SP);  // [4 qd][64 t] ||a(k_t)||^2 over this CTA's hidden units
     float* sp_d2 = sp_a2 + 4 * BC;                         // [4 qd][64 t] ||delta_t||^2, likewise
@@ -310,9 +316,12 @@ __global__ void __launch_bounds__(128 * (64 / CW), 1)
     const int j_glob = HS * rank + jr;       // hidden unit of row jr
 
     if (tid == 0) {
-        mbar_init(&bars[0], 1);
-        mbar_init(&bars[1], 1);
+        for (int i = 0; i < 4; ++i) mbar_init(&bars[i], 1);
         fence_mbar_init();
+        if (NC > 1 && nchunks > 0) {  // chunk 0's bytes from the peer (the cluster barrier below precedes them)
+            mbar_arrive_expect_tx(&bars[2], XCH_KEY_BYTES);
+            mbar_arrive_expect_tx(&bars[3], XCH_Y_BYTES);
+        }
         prefetch_tmap(&tq);
         prefetch_tmap(&tk);
         prefetch_tmap(&tv);
@@ -478,11 +487,11 @@ __global__ void __launch_bounds__(128 * (64 / CW), 1)
 
     const uint32_t aQK = smem_u32(sm + OFF_QK), aW1 = smem_u32(sm + OFF_W1), aS1 = smem_u32(sm + OFF_S1);
     const uint32_t aW2 = smem_u32(sm + OFF_W2), aAK = smem_u32(sm + OFF_AK), aDT = smem_u32(sm + OFF_DT);
-    const uint32_t aKG = smem_u32(sm + OFF_KG), aKU = smem_u32(sm + OFF_KU), aE = smem_u32(sm + OFF_E);
-    const uint32_t aEG = smem_u32(sm + OFF_EG), aEU = smem_u32(sm + OFF_EU), aP = smem_u32(sm + OFF_P);
+    const uint32_t aKG = smem_u32(sm + OFF_KG), aE = smem_u32(sm + OFF_E);
+    const uint32_t aEG = smem_u32(sm + OFF_EG), aP = smem_u32(sm + OFF_P);
     const uint32_t aW1lo = smem_u32(sm + OFF_W1LO), aW2lo = smem_u32(sm + OFF_W2LO), aAKlo = smem_u32(sm + OFF_AKLO);
-    const uint32_t aElo = smem_u32(sm + OFF_ELO), aEGlo = smem_u32(sm + OFF_EGLO), aEUlo = smem_u32(sm + OFF_EULO);
-    const uint32_t aDTlo = smem_u32(sm + OFF_DTLO), aKGlo = smem_u32(sm + OFF_KLO), aKUlo = smem_u32(sm + OFF_KLO + T64);
+    const uint32_t aElo = smem_u32(sm + OFF_ELO), aEGlo = smem_u32(sm + OFF_EGLO);
+    const uint32_t aDTlo = smem_u32(sm + OFF_DTLO), aKGlo = smem_u32(sm + OFF_KLO);
     const int peer = rank ^ 1;
 
     bool failed = false;
@@ -496,6 +505,21 @@ __global__ void __launch_bounds__(128 * (64 / CW), 1)
         }
         failed = __syncthreads_or(!ok) || failed;
         tc_fence_after();
+    };
+    // Every thread: this chunk's bytes from the peer on mbarrier `xb` (bounded
+    // wait); then thread 0 expects the next chunk's.  No cluster barrier orders
+    // the exchanges: the peer's next stores into a buffer depend on data that
+    // this CTA sent after reading it (its next key-forward partial follows its
+    // y sum, which needed this CTA's y partial, sent after this CTA read the
+    // key-forward buffer; its next y partial follows its e, which needed this
+    // CTA's next key-forward partial, sent after this CTA read the y buffer).
+    // A CTA whose wait has given up sends nothing more, and the peer then gives
+    // up at its next wait.
+    auto receive = [&](int xb, uint32_t bytes, int c) {
+        bool ok = true;
+        if (!failed) ok = mbar_wait_cluster(&bars[xb], (uint32_t)(c & 1), WAIT_NS);
+        failed = __syncthreads_or(!ok) || failed;
+        if (tid == 0 && !failed && c + 1 < nchunks) mbar_arrive_expect_tx(&bars[xb], bytes);
     };
     auto handoff = [&]() {  // epilogue smem / TMEM writes -> tensor-core reads
         fence_proxy_async();
@@ -565,10 +589,8 @@ __global__ void __launch_bounds__(128 * (64 / CW), 1)
                 for (int q = 0; q < CW; ++q) k2 = fmaf(kv[q], kv[q], k2);
                 sp_k2[(tid >> 6) * BC + t] = k2;
             }
-            put_row<CW>(sm + OFF_KG, 64, t, c0, o1);
-            put_row<CW>(sm + OFF_KU, 64, t, c0, o2);
-            put_row_lo<CW>(sm + OFF_KLO, 64, t, c0, o1);
-            put_row_lo<CW>(sm + OFF_KLO + T64, 64, t, c0, o2);
+            put_row_hilo<CW>(sm + OFF_KG, sm + OFF_KLO, 64, t, c0, o1);
+            put_row_hilo<CW>(sm + OFF_KU, sm + OFF_KLO + T64, 64, t, c0, o2);
         }
         mma_wait(go1);
         // ---- E1: a(k) and silu'(z) from z = W1 k; P1 = Gamma (.) Q K^T
@@ -582,8 +604,7 @@ __global__ void __launch_bounds__(128 * (64 / CW), 1)
                 ds[q] = fmaf(z[q] * sg, 1.0f - sg, sg);  // silu'(z) = s + z s (1 - s)
                 z[q] *= sg;
             }
-            put_row<CW>(sm + OFF_AK, 128, jr, CW * hq, z);
-            put_row_lo<CW>(sm + OFF_AKLO, 128, jr, CW * hq, z);  // q|k is dead after G1
+            put_row_hilo<CW>(sm + OFF_AK, sm + OFF_AKLO, 128, jr, CW * hq, z);  // (q|k is dead after G1)
             {  // the chunk-start W2 (the state is rescaled only in E2) as the lo tile for G2 and G3
                 float w[CW];
                 tmem_ld_n(tl + COL_W2 + CW * hq, w);
@@ -623,9 +644,9 @@ __global__ void __launch_bounds__(128 * (64 / CW), 1)
         {
             tmem_ld_n(tl + COL_YH + CW * hq, ev);
             if (r64) {
-                if (NC > 1) {
+                if (NC > 1 && !failed) {
                     const uint32_t dst = map_to_rank(smem_u32(Yx + tr * XS + CW * hq), (uint32_t)peer);
-                    push_bf16<CW>(dst, ev);
+                    push_bf16<CW>(dst, ev, map_to_rank(smem_u32(&bars[2]), (uint32_t)peer));
                 }
                 float vv[CW];
                 get_row<CW>(sm + OFF_V, 64, tr, CW * hq, vv);
@@ -651,7 +672,7 @@ __global__ void __launch_bounds__(128 * (64 / CW), 1)
                 tmem_st_n(tl + cs, s);
             }
         }
-        if (NC > 1) cluster_sync();
+        if (NC > 1) receive(2, XCH_KEY_BYTES, c);
         if (r64) {
             if (NC > 1) {
                 float px[CW];
@@ -669,19 +690,16 @@ __global__ void __launch_bounds__(128 * (64 / CW), 1)
                 for (int q = 0; q < CW; ++q) e2 = fmaf(ev[q], ev[q], e2);
                 sp_e2[hq * BC + tr] = e2;
             }
-            put_row<CW>(sm + OFF_E, 64, tr, CW * hq, ev);
-            // e lo over this thread's own v elements (read above, before the cluster barrier)
-            put_row_lo<CW>(sm + OFF_ELO, 64, tr, CW * hq, ev);
+            // (e lo lands on this thread's own elements of the v tile, read above)
+            put_row_hilo<CW>(sm + OFF_E, sm + OFF_ELO, 64, tr, CW * hq, ev);
             float o1[CW];
             const float gm = -sGl[tr], uu = sU[tr];
 #pragma unroll
             for (int q = 0; q < CW; ++q) o1[q] = gm * ev[q];
-            put_row<CW>(sm + OFF_EG, 64, tr, CW * hq, o1);
-            put_row_lo<CW>(sm + OFF_EGLO, 64, tr, CW * hq, o1);  // the W1 copy is dead after G1
+            put_row_hilo<CW>(sm + OFF_EG, sm + OFF_EGLO, 64, tr, CW * hq, o1);  // (the W1 copy is dead after G1)
 #pragma unroll
             for (int q = 0; q < CW; ++q) o1[q] = uu * ev[q];
-            put_row<CW>(sm + OFF_EU, 64, tr, CW * hq, o1);
-            put_row_lo<CW>(sm + OFF_EULO, 64, tr, CW * hq, o1);
+            put_row_hilo<CW>(sm + OFF_EU, sm + OFF_EULO, 64, tr, CW * hq, o1);
         }
         if (gi >= 0 && gi < BC && c + 1 < nchunks) {
             // tokens past T change nothing: a = 1, eta = 0, beta = 1, c = 0
@@ -706,16 +724,14 @@ __global__ void __launch_bounds__(128 * (64 / CW), 1)
                 mma_bf16(tm + COL_XD, dW2 + KS_K * ks, dElo + KS_K * ks, ID_M128N64, 1u);
             }
             mma_commit(&bars[1]);
+            // [W2^T | S2^T] += a(k) [-gamma e | u e]: hi x hi, lo x hi, hi x lo
             const uint64_t dAK = kdesc(aAK), dAKlo = kdesc(aAKlo);
-            const uint64_t dEG = mdesc(aEG, T64), dEU = mdesc(aEU, T64), dEGlo = mdesc(aEGlo, T64), dEUlo = mdesc(aEUlo, T64);
+            const uint64_t dEGU = mdesc(aEG, T64), dEGUlo = mdesc(aEGlo, T64);
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) {
-                mma_bf16(tm + COL_W2, dAK + KS_K * ks, dEG + KS_M * ks, ID_UPD, 1u);
-                mma_bf16(tm + COL_W2, dAKlo + KS_K * ks, dEG + KS_M * ks, ID_UPD, 1u);
-                mma_bf16(tm + COL_W2, dAK + KS_K * ks, dEGlo + KS_M * ks, ID_UPD, 1u);
-                mma_bf16(tm + COL_S2, dAK + KS_K * ks, dEU + KS_M * ks, ID_UPD, 1u);
-                mma_bf16(tm + COL_S2, dAKlo + KS_K * ks, dEU + KS_M * ks, ID_UPD, 1u);
-                mma_bf16(tm + COL_S2, dAK + KS_K * ks, dEUlo + KS_M * ks, ID_UPD, 1u);
+                mma_bf16(tm + COL_W2, dAK + KS_K * ks, dEGU + KS_M * ks, ID_UPD2, 1u);
+                mma_bf16(tm + COL_W2, dAKlo + KS_K * ks, dEGU + KS_M * ks, ID_UPD2, 1u);
+                mma_bf16(tm + COL_W2, dAK + KS_K * ks, dEGUlo + KS_M * ks, ID_UPD2, 1u);
             }
         }
         mma_wait(go3);
@@ -725,8 +741,7 @@ __global__ void __launch_bounds__(128 * (64 / CW), 1)
             tmem_ld_n(tl + COL_XD + CW * hq, xd);
 #pragma unroll
             for (int q = 0; q < CW; ++q) xd[q] *= ds[q];
-            put_row<CW>(sm + OFF_DT, 128, jr, CW * hq, xd);
-            put_row_lo<CW>(sm + OFF_DTLO, 128, jr, CW * hq, xd);  // the S1 copy is dead after G1
+            put_row_hilo<CW>(sm + OFF_DT, sm + OFF_DTLO, 128, jr, CW * hq, xd);  // (the S1 copy is dead after G1)
             if (SURP) {  // ||delta_t||^2 over this quadrant's 32 hidden units
                 float sq[CW];
 #pragma unroll
@@ -740,20 +755,16 @@ __global__ void __launch_bounds__(128 * (64 / CW), 1)
         const bool go4 = !failed;
         if (go4 && tid == 0) {
             const uint64_t dDT = kdesc(aDT), dP = kdesc(aP);
-            const uint64_t dKG = mdesc(aKG, T64), dKU = mdesc(aKU, T64);
-            const uint64_t dDTlo = kdesc(aDTlo);
-            const uint64_t dKGlo = mdesc(aKGlo, T64), dKUlo = mdesc(aKUlo, T64);
+            const uint64_t dKGU = mdesc(aKG, T64), dDTlo = kdesc(aDTlo), dKGUlo = mdesc(aKGlo, T64);
             // R1 and the W1 / S1 updates (E4 overwrites delta, which they read, with a_t); this
             // commit also covers the W2 / S2 updates issued behind G3
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) {
                 mma_bf16(tm + COL_R1, dDT + KS_K * ks, dP + KS_K * ks, ID_M128N64, ks ? 1u : 0u);
-                mma_bf16(tm + COL_W1, dDT + KS_K * ks, dKG + KS_M * ks, ID_UPD, 1u);
-                mma_bf16(tm + COL_W1, dDTlo + KS_K * ks, dKG + KS_M * ks, ID_UPD, 1u);
-                mma_bf16(tm + COL_W1, dDT + KS_K * ks, dKGlo + KS_M * ks, ID_UPD, 1u);
-                mma_bf16(tm + COL_S1, dDT + KS_K * ks, dKU + KS_M * ks, ID_UPD, 1u);
-                mma_bf16(tm + COL_S1, dDTlo + KS_K * ks, dKU + KS_M * ks, ID_UPD, 1u);
-                mma_bf16(tm + COL_S1, dDT + KS_K * ks, dKUlo + KS_M * ks, ID_UPD, 1u);
+                // [W1 | S1] += delta [-gamma k | u k]: hi x hi, lo x hi, hi x lo
+                mma_bf16(tm + COL_W1, dDT + KS_K * ks, dKGU + KS_M * ks, ID_UPD2, 1u);
+                mma_bf16(tm + COL_W1, dDTlo + KS_K * ks, dKGU + KS_M * ks, ID_UPD2, 1u);
+                mma_bf16(tm + COL_W1, dDT + KS_K * ks, dKGUlo + KS_M * ks, ID_UPD2, 1u);
             }
             mma_commit(&bars[1]);
         }
@@ -822,9 +833,9 @@ __global__ void __launch_bounds__(128 * (64 / CW), 1)
                 const float At = sA[tr], st = sSg[tr];
 #pragma unroll
                 for (int q = 0; q < CW; ++q) yw[q] = fmaf(At, yw[q], -fmaf(st, ys[q], pe[q]));
-                if (!own) {
+                if (!own && !failed) {
                     const uint32_t dst = map_to_rank(smem_u32(Yr + tr * RB + (CW * hq) % 32), (uint32_t)peer);
-                    push_bf16<CW>(dst, yw);
+                    push_bf16<CW>(dst, yw, map_to_rank(smem_u32(&bars[3]), (uint32_t)peer));
                 }
             }
             // while the peer's partial y arrives: W2 and S2 (no longer read by
@@ -843,7 +854,8 @@ __global__ void __launch_bounds__(128 * (64 / CW), 1)
                 st_cluster_f32(map_to_rank(smem_u32(sp_peer + t), 0u), a2);
                 st_cluster_f32(map_to_rank(smem_u32(sp_peer + BC + t), 0u), d2);
             }
-            if (NC > 1) cluster_sync();
+            if (NC > 1) receive(3, XCH_Y_BYTES, c);
+            if (SURP && NC > 1) cluster_sync();  // the peer's surprise partials are here
             if (r64 && own && tr < n) {
                 if (NC > 1) {
                     float pr[CW];

@@ -108,12 +108,12 @@ struct Layout {
     static constexpr uint32_t RX = V + 64 * OR * 2;        // bf16 [NC-1][OR][64] key-forward partials
     static constexpr uint32_t RX2 = RX + PART;             // bf16 [NC-1][OR][64] retrieval partials
     static constexpr uint32_t F = RX2 + PART;              // gates [4][64], A, B, sigma, gamma, u
-    // the rows sent to the peers, staged as bf16 [NC-1][OR][64] (peer p at p OR rows,
-    // p = (owner - rank - 1) mod NC) for one bulk copy per peer: the key forward's
-    // at the end of the delta tiles (dead from G2 until E3), the retrieval's in
-    // the e^T tile (dead after G6)
+    // the rows sent to the peers, staged as bf16 [NC-1][OR][64] (owner q at the slot
+    // that q fills in this CTA's receive buffers) for one bulk copy per peer: the
+    // key forward's at the end of the delta tiles (dead from G2 until E3), the
+    // retrieval's in the key-forward receive buffer (dead after the e reduce)
     static constexpr uint32_t STG1 = DT + 3 * T64 - PART;
-    static constexpr uint32_t STG2 = ET;
+    static constexpr uint32_t STG2 = RX;
     static constexpr uint32_t SP = F + 4 * (4 * BC + 5 * BC + 4);  // (+ A_n, B_n, sigma_n) surprise: fp32 [4][64] this CTA's ||a||^2,
                                                              // ||delta||^2, ||e||^2, ||k||^2; [2][3][64] cluster sums
     static constexpr uint32_t BAR = SP + 4 * (10 * BC);
@@ -131,7 +131,7 @@ struct Layout {
     static constexpr uint32_t TX_E = (NC - 1) * OR * BC * 4;
     // the owner's own partial rows (fp32 [OR][64]) during an exchange live in
     // the delta tiles, which are dead at both exchange points
-    static_assert(OR * 256 <= STG1 - DT && PART <= T128, "own partial and staging fit the delta tiles; staging fits e^T");
+    static_assert(OR * 256 <= STG1 - DT, "own partial and staging fit the delta tiles");
 };
 
 // TMEM columns
@@ -387,7 +387,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                              __float_as_uint(v[4 * m + 2]), __float_as_uint(v[4 * m + 3]));
             }
         } else {  // partial sums travel as bf16 (the sums themselves are taken in fp32)
-            const int p = (q_own - rank - 1 + NC) % NC;
+            const int p = q_own < rank ? q_own : q_own - 1;
             const uint32_t base = smem_u32(stg) + (uint32_t)(p * OR + r) * 128u;
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
@@ -399,15 +399,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     };
     // Threads 0 .. NC-2, once the staging is visible to the async proxy: one bulk
     // copy per peer of the rows it owns, into this CTA's slot of its receive
-    // buffer `rx`, counted on its mbarrier `xb`.  A CTA whose wait has given up
-    // sends nothing more: it no longer expects bytes itself, and each peer then
-    // gives up at its next wait for this CTA's data.
+    // buffer `rx`, counted on its mbarrier `xb`.  (A staged block sits where the
+    // same peer's partials land in this CTA's buffers, so the only later writer
+    // of a block is a peer that has received the copy reading it.)  A CTA whose
+    // wait has given up sends nothing more: it no longer expects bytes itself,
+    // and each peer then gives up at its next wait for this CTA's data.
     auto send_rows = [&](const unsigned char* stg, const unsigned char* rx, int xb) {
         if (tid < NC - 1 && !failed) {
-            const uint32_t q = (uint32_t)((rank + 1 + tid) % NC);
-            const uint32_t slot = (uint32_t)(rank < (int)q ? rank : rank - 1);
-            bulk_copy_to_peer(map_to_rank(smem_u32(rx) + slot * OR * 128u, q), smem_u32(stg) + (uint32_t)tid * OR * 128u,
-                              OR * 128u, map_to_rank(smem_u32(&bars[xb]), q));
+            const int q = (rank + 1 + tid) % NC;
+            const uint32_t dslot = (uint32_t)(rank < q ? rank : rank - 1), sslot = (uint32_t)(q < rank ? q : q - 1);
+            bulk_copy_to_peer(map_to_rank(smem_u32(rx) + dslot * OR * 128u, (uint32_t)q),
+                              smem_u32(stg) + sslot * OR * 128u, OR * 128u, map_to_rank(smem_u32(&bars[xb]), (uint32_t)q));
         }
     };
     // Once the peers' partials have landed: the sum over the cluster of 4
@@ -645,17 +647,18 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     const uint32_t off = sw128_offset(own_lo + row, 4 * c4, 128);
                     *reinterpret_cast<uint2*>(sm + L::ET + off) = make_uint2(w0, w1);
                     *reinterpret_cast<uint2*>(sm + L::ETLO + off) = make_uint2(l0, l1);
-                    // (every peer's W1 copy, where e^T lo lands, is dead: its partials,
-                    // which this row needed, follow its G1)
-#pragma unroll
-                    for (int p = 1; p < NC; ++p) {
-                        if (failed) break;
-                        const uint32_t q = (uint32_t)((rank + p) % NC);
-                        const uint32_t bar = map_to_rank(smem_u32(&bars[4]), q);
-                        st_async_v2(map_to_rank(aET + off, q), w0, w1, bar);
-                        st_async_v2(map_to_rank(aETlo + off, q), l0, l1, bar);
-                    }
                 }
+            }
+            // the owned rows of e^T (hi and lo) are one contiguous block of each
+            // swizzled tile, at the same place in every CTA: two bulk copies per
+            // peer.  (Every peer's W1 copy, where e^T lo lands, is dead: its
+            // partials, which these rows needed, follow its G1.)
+            fence_proxy_async();
+            __syncthreads();
+            if (tid < 2 * (NC - 1) && !failed) {
+                const uint32_t q = (uint32_t)((rank + 1 + (tid >> 1)) % NC);
+                const uint32_t src = ((tid & 1) ? aETlo : aET) + (uint32_t)own_lo * 128u;
+                bulk_copy_to_peer(map_to_rank(src, q), src, OR * 128u, map_to_rank(smem_u32(&bars[4]), q));
             }
             receive(4, L::TX_E, c, true);  // e^T complete
         }
@@ -854,8 +857,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 }
             };
 #pragma unroll 1
-            for (int m = 0; m < 4; ++m) copy_state(m);  // meanwhile
+            for (int m = 1; m < 4; ++m) copy_state(m);  // meanwhile
             receive(5, L::TX_PART, c, true);
+            // the W1 copy shares its tile with e^T lo, whose owned rows this CTA's bulk
+            // copies read: every peer has received them once its retrieval partials are here
+            copy_state(0);
             if (SURP) cluster_sync();  // rank 0's surprise sums of this chunk are complete
             if (SURP && tid < BC) {
                 // surprise_t = sqrt(||delta_t||^2 ||k_t||^2 + ||e_t||^2 ||a(k_t)||^2), sums over the cluster
