@@ -64,7 +64,8 @@ constexpr uint32_t OFF_P = OFF_EU + TILE;        // [64 t][64 i] bf16
 constexpr int GS = 68;                           // padded fp32 row stride of Gamma
 constexpr uint32_t OFF_GM = OFF_P + HALF;
 constexpr uint32_t OFF_F = OFF_GM + 64 * GS * 4; // gates [2][4][64], A, B, sigma, gamma, u
-constexpr uint32_t N_F = 2 * 4 * BC + 5 * BC + 4 * BC;  // + surprise partials [2 halves][e2, k2][64]
+constexpr uint32_t N_F = 2 * 4 * BC + 5 * BC + 4 * BC + 4;  // + surprise partials [2 halves][e2, k2][64]
+                                                             // + the next chunk's A_n, B_n, sigma_n
 constexpr uint32_t OFF_BAR = OFF_F + 4 * N_F;
 constexpr uint32_t SMEM_USED = OFF_BAR + 64;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;  // slack for 1024-byte alignment
@@ -136,6 +137,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     float* sGl = sSg + BC;
     float* sU = sGl + BC;
     float* sPart = sU + BC;  // surprise partial sums: [hf][||e||^2 | ||k||^2][64]
+    float* sEnd = sPart + 4 * BC;  // A_n, B_n, sigma_n of the chunk (computed during the previous chunk)
     float* Gm = reinterpret_cast<float*>(sm + OFF_GM);
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + OFF_BAR);  // 0,1: Q|K stages; 2: V; 3: mma
     __shared__ uint32_t s_tmem;
@@ -182,6 +184,21 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
         for (int h = 0; h < 2; ++h) tma_load_3d(sm + OFF_V + h * HALF, &tv, &bars[2], h * 64, t0, (int)unit);
     };
+    // A_n, B_n, sigma_n (the products and the sigma recursion of the gate scan,
+    // in the scan's order) of the gates staged at `g`
+    auto chunk_end = [&](const float* g) {
+        float A = 1.f, Bc = 1.f, sg = 0.f;
+#pragma unroll 8
+        for (int t = 0; t < BC; ++t) {
+            const float ga = g[t], ge = g[BC + t], gb = g[2 * BC + t];
+            A *= ga;
+            Bc *= gb;
+            sg = fmaf(ga, sg, ge * Bc);
+        }
+        sEnd[0] = A;
+        sEnd[1] = Bc;
+        sEnd[2] = sg;
+    };
     if (tid < BC) {  // gates of chunk 0; tokens past T change nothing: a = 1, eta = 0, beta = 1, c = 0
         const long long t = tid;
         float* g = gates;
@@ -203,6 +220,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             issue_v(0);
         }
     }
+    if (tid == 224) chunk_end(gates);  // (visible after the barrier below)
 
     // initial state: TMEM fp32 (lane o = row o of M, S) and bf16 operand copies
     {
@@ -274,8 +292,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         //      then the next chunk's Q|K tiles; meanwhile the gate scan
         bool tiles_ok = true;
         if (tid == 0 && !failed) {
-            tiles_ok = mbar_wait(&bars[stage], (uint32_t)((c >> 1) & 1), WAIT_NS) &&
-                       mbar_wait(&bars[2], (uint32_t)(c & 1), WAIT_NS);
+            tiles_ok = mbar_wait(&bars[stage], (uint32_t)((c >> 1) & 1), WAIT_NS);
             if (tiles_ok) {
                 tc_fence_after();
                 const uint64_t dQ = kdesc(aQ), dK = kdesc(aK), dM = kdesc(aMH);
@@ -292,11 +309,34 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 mma_commit(&bars[3]);
                 if (c + 1 < nchunks) issue_qk(c + 1, stage ^ 1);
             }
+            // V is read only after batch 1: its wait overlaps the products
+            tiles_ok = tiles_ok && mbar_wait(&bars[2], (uint32_t)(c & 1), WAIT_NS);
             bulk_wait_read();  // the previous chunk's y tile (in EG / EU) has been read by its store
         }
-        if (tid >= 128 && tid < 128 + BC) {
+        // rescale the fp32 state for this chunk (batch 1 does not touch it) while batch 1
+        // runs: M <- A_n M - sigma_n S, S <- B_n S.  Thread 0 is issuing, so warp 4 (the
+        // same TMEM lanes) takes warp 0's columns too.
+        auto rescale = [&](int h) {
+            const float An = sEnd[0], Bn = sEnd[1], sn = sEnd[2];
+            float m[32], s[32];
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const uint32_t c0 = 64 * h + 32 * j;
+                tmem_ld_n(tl + COL_M + c0, tl + COL_S + c0, m, s);
+#pragma unroll
+                for (int q = 0; q < 32; ++q) {
+                    m[q] = fmaf(An, m[q], -sn * s[q]);
+                    s[q] = Bn * s[q];
+                }
+                tmem_st_n(tl + COL_M + c0, m);
+                tmem_st_n(tl + COL_S + c0, s);
+            }
+        };
+        if (warp != 0) rescale(hf);
+        if (warp == 4) rescale(0);
+        if (tid >= 160 && tid < 160 + BC) {  // (warps 5 and 6: warp 4 rescales for warp 0)
             // column i of Gamma: Gamma_{t,i} = a_t Gamma_{t-1,i} + eta_t u_{t,i}, zero above the diagonal
-            const int i = tid - 128;
+            const int i = tid - 160;
             // from row 0 with u = Gamma = 0 and the start injected,
             // u_t = beta_t u_{t-1} + [t = i] c_i: zero above the diagonal, no branch per row;
             // the next four gates are loaded before this group's stores
@@ -348,24 +388,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         const bool go1 = !failed && !__syncthreads_or(!tiles_ok);
         if (!go1 && !failed) failed = true;
-        // rescale the fp32 state for this chunk (batch 1 does not touch it):
-        // M <- A_n M - sigma_n S, S <- B_n S
-        {
-            const float An = sA[BC - 1], Bn = sBc[BC - 1], sn = sSg[BC - 1];
-            float m[32], s[32];
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                const uint32_t c0 = 64 * hf + 32 * j;
-                tmem_ld_n(tl + COL_M + c0, tl + COL_S + c0, m, s);
-#pragma unroll
-                for (int q = 0; q < 32; ++q) {
-                    m[q] = fmaf(An, m[q], -sn * s[q]);
-                    s[q] = Bn * s[q];
-                }
-                tmem_st_n(tl + COL_M + c0, m);
-                tmem_st_n(tl + COL_S + c0, s);
-            }
-        }
         mma_wait(go1);
         // ---- e_t = 2 (M0 k_t - v_t) and its gamma / u scaled copies, and
         //      P = Gamma (.) Q K^T.  The M=64 accumulators hold token t in lane
@@ -466,6 +488,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             mma_commit(&bars[3]);
             if (c + 1 < nchunks) issue_v(c + 1);
         }
+        if (tid == 224 && c + 1 < nchunks) chunk_end(gates + (stage ^ 1) * 4 * BC);  // (staged before batch 2)
         mma_wait(go2);
         // ---- y_t[o] = A_t (M0 q_t)[o] - sigma_t (S0 q_t)[o] - (E^T P^T)[o][t], tokens 32 hf ..,
         //      into a row-major [64 t][128 o] tile in the EG / EU space (free after batch 2),
