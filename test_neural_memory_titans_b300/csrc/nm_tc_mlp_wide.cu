@@ -397,7 +397,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             }
         }
     };
-    // Threads 0 .. NC-2, once the staging is visible to the async proxy: one bulk
+    // Lane 0 of warps 0 .. NC-2 (copies issued from separate warps go out in
+    // parallel), once the staging is visible to the async proxy: one bulk
     // copy per peer of the rows it owns, into this CTA's slot of its receive
     // buffer `rx`, counted on its mbarrier `xb`.  (A staged block sits where the
     // same peer's partials land in this CTA's buffers, so the only later writer
@@ -405,8 +406,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // wait has given up sends nothing more: it no longer expects bytes itself,
     // and each peer then gives up at its next wait for this CTA's data.
     auto send_rows = [&](const unsigned char* stg, const unsigned char* rx, int xb) {
-        if (tid < NC - 1 && !failed) {
-            const int q = (rank + 1 + tid) % NC;
+        if (lane == 0 && warp < NC - 1 && !failed) {
+            const int q = (rank + 1 + warp) % NC;
             const uint32_t dslot = (uint32_t)(rank < q ? rank : rank - 1), sslot = (uint32_t)(q < rank ? q : q - 1);
             bulk_copy_to_peer(map_to_rank(smem_u32(rx) + dslot * OR * 128u, (uint32_t)q),
                               smem_u32(stg) + sslot * OR * 128u, OR * 128u, map_to_rank(smem_u32(&bars[xb]), (uint32_t)q));
@@ -632,7 +633,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             {
                 const __nv_bfloat16* vs = reinterpret_cast<const __nv_bfloat16*>(sm + L::V);
                 for (int task = tid; task < TASKS; task += NTHREADS) {
-                    const int row = task >> 4, c4 = task & 15;  // consecutive threads: one row's tokens
+                    const int row = task % OR, c4 = task / OR;  // consecutive threads: consecutive rows
                     const float4 sum = reduce4(row, c4, RX);
                     const float sv[4] = {sum.x, sum.y, sum.z, sum.w};
                     float e[4];
@@ -655,9 +656,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             // partials, which these rows needed, follow its G1.)
             fence_proxy_async();
             __syncthreads();
-            if (tid < 2 * (NC - 1) && !failed) {
-                const uint32_t q = (uint32_t)((rank + 1 + (tid >> 1)) % NC);
-                const uint32_t src = ((tid & 1) ? aETlo : aET) + (uint32_t)own_lo * 128u;
+            if ((lane & 15) == 0 && warp < NC - 1 && !failed) {  // hi from lane 0, lo from lane 16 of warp p
+                const uint32_t q = (uint32_t)((rank + 1 + warp) % NC);
+                const uint32_t src = ((lane >> 4) ? aETlo : aET) + (uint32_t)own_lo * 128u;
                 bulk_copy_to_peer(map_to_rank(src, q), src, OR * 128u, map_to_rank(smem_u32(&bars[4]), q));
             }
             receive(4, L::TX_E, c, true);  // e^T complete
