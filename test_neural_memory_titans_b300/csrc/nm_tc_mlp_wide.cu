@@ -427,6 +427,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         return acc;
     };
     constexpr int TASKS = OR * 16;  // owned rows x 16 groups of 4 tokens
+    static_assert(TASKS % NTHREADS == 0, "every task loop runs in full warps");
     // Every thread: this chunk's bytes from the peers on mbarrier `xb` (bounded
     // wait; `extra` folds in another condition); then thread 0 expects the next
     // chunk's.  The CTA barrier also completes the own partial rows.
@@ -641,7 +642,21 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     for (int k = 0; k < 4; ++k) {
                         const int t = 4 * c4 + k;
                         e[k] = t < n ? nm_clip_err(2.0f * (sv[k] - __bfloat162float(vs[t * OR + row])), a.e_clip) : 0.0f;
-                        if (SURP) atomicAdd(&sp_loc[2 * BC + t], e[k] * e[k]);
+                    }
+                    if (SURP) {  // ||e_t||^2 over the owned rows: summed across the lanes that share
+                                 // these tokens (TASKS is a multiple of the block: full warps), then
+                                 // one shared-memory atomic per group
+                        constexpr int G = OR < 32 ? OR : 32;
+                        float e2[4];
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) e2[k] = e[k] * e[k];
+#pragma unroll
+                        for (int off = G / 2; off > 0; off >>= 1)
+#pragma unroll
+                            for (int k = 0; k < 4; ++k) e2[k] += __shfl_xor_sync(0xffffffffu, e2[k], off);
+                        if ((lane & (G - 1)) == 0)
+#pragma unroll
+                            for (int k = 0; k < 4; ++k) atomicAdd(&sp_loc[2 * BC + 4 * c4 + k], e2[k]);
                     }
                     uint32_t w0, w1;
                     const uint32_t l0 = pack_hi_lo(e[0], e[1], w0), l1 = pack_hi_lo(e[2], e[3], w1);
