@@ -228,7 +228,13 @@ int nm_backward(nm_handle_t h, int B, int H, int T,
  *   Copies the inputs to the handle's device (into handle-owned buffers that
  *   grow on demand), runs nm_forward on `stream`, copies y, M_T, S_T back and
  *   synchronises the stream before returning.  Pinned host memory gives
- *   asynchronous copies; pageable memory works but is slower.
+ *   asynchronous copies; pageable memory works but is slower.  On the
+ *   tensor-core path, when one input tensor plus y hold 8 MiB or more, the
+ *   units run in groups (one per 16 MiB of q + y, at least 2, at most 16 and
+ *   at most one per unit), each group's forward starting on a stream of its
+ *   own as soon as its inputs are in, its outputs copied back while later
+ *   groups' inputs are still going up; the results equal nm_forward's bit
+ *   for bit, and each group counts as one launch in nm_launch_count.
  *   Returns the first host-side error, or the device status word as
  *   nm_synchronize would.
  */

@@ -67,7 +67,7 @@ int ensure_pipe(nm_handle* h) {
               cudaStreamCreateWithFlags(&h->s_out, cudaStreamNonBlocking) == cudaSuccess &&
               cudaEventCreateWithFlags(&h->ev_start, cudaEventDisableTiming) == cudaSuccess &&
               cudaEventCreateWithFlags(&h->ev_end, cudaEventDisableTiming) == cudaSuccess;
-    for (int i = 0; ok && i < 4; ++i)
+    for (int i = 0; ok && i < NM_HOST_MAX_GROUPS; ++i)
         ok = cudaStreamCreateWithFlags(&h->s_comp[i], cudaStreamNonBlocking) == cudaSuccess &&
              cudaEventCreateWithFlags(&h->ev_in[i], cudaEventDisableTiming) == cudaSuccess &&
              cudaEventCreateWithFlags(&h->ev_done[i], cudaEventDisableTiming) == cudaSuccess;
@@ -455,12 +455,17 @@ int nm_forward_host(nm_handle_t h, int B, int H, int T, const void* q, const voi
     float* dST = (float*)carve(st_b);
     void* dy = carve(out_b);
     cudaStream_t s = (cudaStream_t)stream;
-    // Copy / compute overlap: the units are split into up to four groups; group g's inputs go up on one stream,
-    // its forward runs on a stream of its own as soon as they have landed (the groups' kernels run side by side,
+    // Copy / compute overlap: the units are split into groups; group g's inputs go up on one stream, its
+    // forward runs on a stream of its own as soon as they have landed (the groups' kernels run side by side,
     // each unit's chain being independent), and its outputs come back on a third stream while later groups'
-    // inputs are still being copied.  Used on the tensor-core path (no shared workspace) when every group's slice
-    // of every buffer starts on a 16-byte boundary.
-    const int groups = (int)std::min<size_t>(4, units);
+    // inputs are still being copied.  One group per NM_HOST_GROUP_BYTES of q + y, at least 2 and at most
+    // NM_HOST_MAX_GROUPS and the number of units: a group's forward starts once its own inputs are in, so small
+    // groups keep the kernels busy behind the copies (and few CTAs in flight at once), while each group costs a
+    // dozen copy calls.  Used on the tensor-core path (no shared workspace) when every group's slice of every
+    // buffer starts on a 16-byte boundary.
+    const size_t by_bytes = (in_b + out_b + NM_HOST_GROUP_BYTES - 1) / NM_HOST_GROUP_BYTES;
+    const int groups = (int)std::min<size_t>(std::min<size_t>((size_t)NM_HOST_MAX_GROUPS, units),
+                                             std::max<size_t>(2, by_bytes));
     if (h->path == NM_PATH_TC && T > 0 && groups > 1 && (T % 4) == 0 && (P % 4) == 0 &&
         in_b + out_b >= ((size_t)8 << 20)) {
         int prc = ensure_pipe(h);
@@ -580,7 +585,7 @@ int nm_destroy(nm_handle_t h) {
                 cudaStreamDestroy(h->s_out);
                 cudaEventDestroy(h->ev_start);
                 cudaEventDestroy(h->ev_end);
-                for (int i = 0; i < 4; ++i) {
+                for (int i = 0; i < NM_HOST_MAX_GROUPS; ++i) {
                     cudaStreamDestroy(h->s_comp[i]);
                     cudaEventDestroy(h->ev_in[i]);
                     cudaEventDestroy(h->ev_done[i]);

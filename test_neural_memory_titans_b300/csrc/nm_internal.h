@@ -100,6 +100,11 @@ __device__ __forceinline__ void nm_gate_row(const nm_args& a, const Tout* p, flo
 }
 #endif
 
+// nm_forward_host's copy / compute overlap: at most this many unit groups, each
+// on a compute stream of its own, and one group per NM_HOST_GROUP_BYTES of q + y.
+constexpr int NM_HOST_MAX_GROUPS = 16;
+constexpr size_t NM_HOST_GROUP_BYTES = (size_t)16 << 20;
+
 struct nm_handle {
     nm_config cfg;
     int device;
@@ -117,8 +122,8 @@ struct nm_handle {
     // nm_forward_host's copy / compute overlap (created on first use): streams for the
     // host->device and device->host copies and one compute stream per group of units
     int pipe_ready;
-    cudaStream_t s_in, s_out, s_comp[4];
-    cudaEvent_t ev_start, ev_end, ev_in[4], ev_done[4];
+    cudaStream_t s_in, s_out, s_comp[NM_HOST_MAX_GROUPS];
+    cudaEvent_t ev_start, ev_end, ev_in[NM_HOST_MAX_GROUPS], ev_done[NM_HOST_MAX_GROUPS];
 };
 
 // The |e| bound of a configuration (see nm_clip_err).

@@ -283,18 +283,26 @@ def test_simt_path_fp32_mlp_tight():
     compare(wl, gpu, oracle_forward(wl, x, M0=M0, S0=S0))
 
 
-# The copy / compute overlap of nm_forward_host takes units in up to four groups when the
-# tensor-core path runs and one input tensor (q) plus y hold at least this many bytes.
+# The copy / compute overlap of nm_forward_host takes units in groups when the tensor-core
+# path runs and one input tensor (q) plus y hold at least this many bytes: one group per
+# HOST_GROUP_BYTES of q + y, at least 2, at most 16 and at most one per unit.
 HOST_GROUPED_MIN_BYTES = 8 << 20
+HOST_GROUP_BYTES = 16 << 20
+
+
+def _host_groups(units, qy_bytes):
+    return min(16, units, max(2, -(-qy_bytes // HOST_GROUP_BYTES)))
 
 
 @pytest.mark.parametrize("wid,B,H,T,grouped", [(2, 2, 2, 300, False), (2, 2, 8, 4096, True),
-                                               (4, 1, 5, 8192, True), (1, 1, 177, 192, True)])
+                                               (4, 1, 5, 8192, True), (1, 1, 177, 192, True),
+                                               (2, 4, 8, 8192, True)])
 def test_forward_host_matches_device(wid, B, H, T, grouped):
     """nm_forward_host equals nm_forward bit for bit.  The larger cases take
-    its copy / compute overlap (units in four groups on their own streams),
-    with even groups (16 units) and uneven ones (5 units as 2 + 1 + 1 + 1, 177
-    MLP units as 45 + 44 + 44 + 44); the launch counter shows which path ran.
+    its copy / compute overlap (units in groups on their own streams), with
+    even groups (16 units in 2, 32 units in 8) and uneven ones (5 units as
+    3 + 2, 177 MLP units as 89 + 88); the launch counter shows which path ran
+    and how many groups it used.
     The MLP case runs three chunks of the literal workload, before its
     weights diverge, so every output is finite."""
     wl = W.WORKLOADS[wid].with_sizes(B=B, H=H, T=T, segment=0)
@@ -307,7 +315,7 @@ def test_forward_host_matches_device(wid, B, H, T, grouped):
     l0 = mem.launches
     yh, Mh, Sh = mem.forward_host(pin["q"], pin["k"], pin["v"], pin["alpha"], pin["eta"], pin["beta"],
                                   pin["M0"], pin["S0"])
-    assert mem.launches - l0 == (min(4, B * H) if grouped else 1)
+    assert mem.launches - l0 == (_host_groups(B * H, 2 * B * H * T * wl.d * eb) if grouped else 1)
     g = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
     yd, Md, Sd = mem.forward(g["q"], g["k"], g["v"], g["alpha"], g["eta"], g["beta"], g["M0"], g["S0"])
     assert mem.synchronize() == nm.NM_OK
