@@ -63,6 +63,24 @@ __device__ __forceinline__ float nm_gated(const nm_args& a, const Tout* p, float
     return nm_to_f32(*ya) / (1.0f + expf(-y));
 }
 
+// o = sigmoid(y) * y_attn for the tensor-core kernels' epilogues, with the
+// fast exponential and division (a few ulp of fp32, far below the bf16
+// rounding of their outputs; for y below about -88 the exponential
+// overflows and o is 0, the limit).  The fp32 FFMA kernels keep the exact form.
+__device__ __forceinline__ float nm_gate_fast(float y_attn, float y) {
+    return __fdividef(y_attn, 1.0f + __expf(-y));
+}
+
+// The gated output's y_attn bytes [off, off + bytes) into L2, one 128-byte line
+// per thread (thread `tid` of `nthreads`): issued at a chunk's start so that the
+// epilogue's loads of the chunk's y_attn find them there.  Nothing is read.
+__device__ __forceinline__ void nm_prefetch_attn(const nm_args& a, long long off, long long bytes, int tid,
+                                                 int nthreads) {
+    const char* base = reinterpret_cast<const char*>(a.y_attn) + off;
+    for (long long i = tid; i * 128 < bytes; i += nthreads)
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(base + i * 128));
+}
+
 // W consecutive elements y_attn[idx .. idx + W) as floats, with 16-byte loads
 // (idx a multiple of 8 for bf16, of 4 for fp32, and y_attn 16-byte aligned),
 // all issued before any is used.
@@ -96,7 +114,7 @@ __device__ __forceinline__ void nm_gate_row(const nm_args& a, const Tout* p, flo
     float ya[W];
     nm_load_row<W>(reinterpret_cast<const Tout*>(a.y_attn) + (p - reinterpret_cast<const Tout*>(a.y)), ya);
 #pragma unroll
-    for (int i = 0; i < W; ++i) v[i] = ya[i] / (1.0f + expf(-v[i]));
+    for (int i = 0; i < W; ++i) v[i] = nm_gate_fast(ya[i], v[i]);
 }
 #endif
 

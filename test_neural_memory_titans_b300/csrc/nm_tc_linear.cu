@@ -121,7 +121,8 @@ __device__ __forceinline__ void store_y<__nv_bfloat16>(__nv_bfloat16* p, float x
 template <>
 __device__ __forceinline__ void store_y<float>(float* p, float x) { *p = x; }
 
-// OPT: bit 0 = write the surprise (a.surprise), bit 1 = Huber loss (clip e); compiled
+// OPT: bit 0 = write the surprise (a.surprise), bit 1 = Huber loss (clip e), bit 2 = the
+// gated output o = sigmoid(y) (.) y_attn (a.y_attn); compiled
 // variants, so that the plain forward carries neither.
 template <typename Tout, int OPT>
 __global__ void __launch_bounds__(NTHREADS, 1)
@@ -288,6 +289,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             if (c_mode == NM_C_PER_TOKEN) nxt_c = cc[t];
         }
 
+        // the gated output: the chunk's y_attn rows into L2 now, for the loads before the y epilogue
+        if (OPT & 4) nm_prefetch_attn(a, (unit * T + t0) * D * (long long)sizeof(Tout), (long long)n * D * sizeof(Tout),
+                                      tid, NTHREADS);
         // ---- batch 1 (thread 0, as soon as the tiles land): yhat = K M0^T, Q K^T, M0 Q^T;
         //      then the next chunk's Q|K tiles; meanwhile the gate scan
         bool tiles_ok = true;
@@ -489,6 +493,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             if (c + 1 < nchunks) issue_v(c + 1);
         }
         if (tid == 224 && c + 1 < nchunks) chunk_end(gates + (stage ^ 1) * 4 * BC);  // (staged before batch 2)
+        // the gated output: y_attn of this thread's output row and 32 tokens, loaded while batch 2 runs
+        // (consecutive lanes read consecutive features of a token: coalesced)
+        Tout yatt[(OPT & 4) ? 32 : 1];
+        if (OPT & 4) {
+            const Tout* ya = reinterpret_cast<const Tout*>(a.y_attn) + (unit * T + t0) * D + orow;
+#pragma unroll
+            for (int q = 0; q < 32; ++q) {
+                const int t = 32 * hf + q;
+                yatt[q] = ya[(t < n ? t : 0) * D];  // (rows past T are not stored)
+            }
+        }
         mma_wait(go2);
         // ---- y_t[o] = A_t (M0 q_t)[o] - sigma_t (S0 q_t)[o] - (E^T P^T)[o][t], tokens 32 hf ..,
         //      into a row-major [64 t][128 o] tile in the EG / EU space (free after batch 2),
@@ -497,28 +512,18 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             float y1[32], y2[32], pe[32];
             tmem_ld_n(tl + COL_Y1 + 32 * hf, tl + COL_Y2 + 32 * hf, tl + COL_PE + 32 * hf, y1, y2, pe);
             Tout* yt = reinterpret_cast<Tout*>(sm + OFF_EG);
-            if (!a.y_attn) {
+            if (!(OPT & 4)) {
 #pragma unroll
                 for (int q = 0; q < 32; ++q) {
                     const int t = 32 * hf + q;
                     store_y(yt + t * D + orow, fmaf(sA[t], y1[q], -fmaf(sSg[t], y2[q], pe[q])));
                 }
-            } else {  // the gated output: this output row's y_attn of 8 tokens at a time, loaded first
-                const Tout* ya = reinterpret_cast<const Tout*>(a.y_attn) + (unit * T + t0) * D + orow;
+            } else {  // o = sigmoid(y) (.) y_attn with the y_attn loaded above
 #pragma unroll
-                for (int g8 = 0; g8 < 4; ++g8) {
-                    float yv[8];
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        const int t = 32 * hf + 8 * g8 + q;
-                        yv[q] = t < n ? nm_to_f32(ya[t * D]) : 0.0f;  // rows past T are not stored
-                    }
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        const int t = 32 * hf + 8 * g8 + q, qq = 8 * g8 + q;
-                        const float v = fmaf(sA[t], y1[qq], -fmaf(sSg[t], y2[qq], pe[qq]));
-                        store_y(yt + t * D + orow, yv[q] / (1.0f + expf(-v)));
-                    }
+                for (int q = 0; q < 32; ++q) {
+                    const int t = 32 * hf + q;
+                    const float v = fmaf(sA[t], y1[q], -fmaf(sSg[t], y2[q], pe[q]));
+                    store_y(yt + t * D + orow, nm_gate_fast(nm_to_f32(yatt[q]), v));
                 }
             }
         }
@@ -577,6 +582,20 @@ cudaError_t launch(const nm_config& c, const nm_args& a, cudaStream_t s) {
     return cudaGetLastError();
 }
 
+template <typename Tout>
+cudaError_t launch_opt(int opt, const nm_config& c, const nm_args& a, cudaStream_t s) {
+    switch (opt) {
+        case 0: return launch<Tout, 0>(c, a, s);
+        case 1: return launch<Tout, 1>(c, a, s);
+        case 2: return launch<Tout, 2>(c, a, s);
+        case 3: return launch<Tout, 3>(c, a, s);
+        case 4: return launch<Tout, 4>(c, a, s);
+        case 5: return launch<Tout, 5>(c, a, s);
+        case 6: return launch<Tout, 6>(c, a, s);
+        default: return launch<Tout, 7>(c, a, s);
+    }
+}
+
 }  // namespace
 
 bool nm_tc_linear_supports(const nm_config& c) {
@@ -584,19 +603,6 @@ bool nm_tc_linear_supports(const nm_config& c) {
 }
 
 cudaError_t nm_tc_linear_launch(const nm_config& c, const nm_args& a, cudaStream_t s) {
-    const int opt = (a.surprise ? 1 : 0) | (a.e_clip < HUGE_VALF ? 2 : 0);
-    if (c.out_dtype == NM_BF16) {
-        switch (opt) {
-            case 0: return launch<__nv_bfloat16, 0>(c, a, s);
-            case 1: return launch<__nv_bfloat16, 1>(c, a, s);
-            case 2: return launch<__nv_bfloat16, 2>(c, a, s);
-            default: return launch<__nv_bfloat16, 3>(c, a, s);
-        }
-    }
-    switch (opt) {
-        case 0: return launch<float, 0>(c, a, s);
-        case 1: return launch<float, 1>(c, a, s);
-        case 2: return launch<float, 2>(c, a, s);
-        default: return launch<float, 3>(c, a, s);
-    }
+    const int opt = (a.surprise ? 1 : 0) | (a.e_clip < HUGE_VALF ? 2 : 0) | (a.y_attn ? 4 : 0);
+    return c.out_dtype == NM_BF16 ? launch_opt<__nv_bfloat16>(opt, c, a, s) : launch_opt<float>(opt, c, a, s);
 }

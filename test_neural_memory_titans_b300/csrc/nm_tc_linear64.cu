@@ -269,6 +269,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const bool chunk_end = s == NB - 1 || g + 1 == nblocks;
         const long long t0 = (long long)g * SB;
         const int n = (int)min((long long)SB, T - t0);
+        // the gated output: this block's y_attn rows into L2 for the epilogue's loads
+        if (a.y_attn) nm_prefetch_attn(a, (unit * T + t0) * D * (long long)sizeof(Tout), (long long)n * D * sizeof(Tout),
+                                       tid, NTHREADS);
         const float* gt = gates + stage * 4 * SB;
         const uint32_t aQ = smem_u32(sm + OFF_Q + stage * T64), aK = smem_u32(sm + OFF_K + stage * T64);
 

@@ -533,6 +533,9 @@ __global__ void __launch_bounds__(128 * (64 / CW), 1)
         const int stage = c & 1;
         const long long t0 = (long long)c * BC;
         const int n = (int)min((long long)BC, T - t0);
+        // the gated output: this chunk's y_attn rows into L2 for the epilogue's loads
+        if (a.y_attn) nm_prefetch_attn(a, (unit * T + t0) * D * (long long)sizeof(Tout), (long long)n * D * sizeof(Tout),
+                                       tid, (int)blockDim.x);
         // this chunk's scan (computed during the previous chunk)
         const float* so = scan_out + stage * 5 * BC;
         const float *sA = so, *sBc = so + BC, *sSg = so + 2 * BC, *sGl = so + 3 * BC, *sU = so + 4 * BC;

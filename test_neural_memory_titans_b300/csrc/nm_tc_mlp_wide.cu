@@ -442,6 +442,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     for (int c = 0; c < nchunks; ++c) {
         const long long t0 = (long long)c * BC;
         const int n = (int)min((long long)BC, T - t0);
+        // the gated output: this chunk's y_attn rows into L2 for the epilogue's loads
+        if (a.y_attn) nm_prefetch_attn(a, (unit * T + t0) * D * (long long)sizeof(Tout), (long long)n * D * sizeof(Tout),
+                                       tid, NTHREADS);
 
         // the next chunk's gates (warps 2-3), stored after this chunk's scan
         const int gi = tid - 64;
@@ -903,7 +906,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
                     for (int k = 0; k < 4; ++k) yv[k] = 4 * c4 + k < n ? nm_to_f32(ya[(4 * c4 + k) * D]) : 0.0f;
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) sv[k] = yv[k] / (1.0f + expf(-sv[k]));
+                    for (int k = 0; k < 4; ++k) sv[k] = nm_gate_fast(yv[k], sv[k]);
                 }
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
