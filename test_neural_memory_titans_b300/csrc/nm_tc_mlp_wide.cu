@@ -115,9 +115,10 @@ struct Layout {
     static constexpr uint32_t STG1 = DT + 3 * T64 - PART;
     static constexpr uint32_t STG2 = RX;
     static constexpr uint32_t SP = F + 4 * (4 * BC + 5 * BC + 4);  // (+ A_n, B_n, sigma_n) surprise: fp32 [4][64] this CTA's ||a||^2,
-                                                             // ||delta||^2, ||e||^2, ||k||^2; [2][3][64] cluster sums
-    static constexpr uint32_t BAR = SP + 4 * (10 * BC);
-    static constexpr uint32_t USED = BAR + 64;
+                                                             // ||delta||^2, ||e||^2, ||k||^2; on rank 0 [NC][3][64] every CTA's first three
+    static constexpr uint32_t BAR = SP + 4 * (4 * BC + 3 * BC * NC);
+    static constexpr uint32_t USED = BAR + 128;
+    static constexpr uint32_t SP_BYTES = (NC - 1) * 3 * BC * 4;  // the peers' partial norms per chunk (rank 0)
     static constexpr uint32_t BYTES = USED + 1024;  // slack for the 1024-byte alignment
     static_assert(BYTES <= 232448, "shared memory budget");
     static_assert(AQ == AK + T64 && P == DU + T64, "stacked operands");
@@ -218,12 +219,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const unsigned char* RX2 = sm + L::RX2;
     // 0: q|k tiles, 1: mma, 2: v slice; bytes from the peers: 3 key-forward partials,
     // 4 rows of e^T, 5 retrieval partials (one phase per chunk each); 6: the state
-    // updates are done with the q|k tiles; 7: the products in flight when a wait has given up
+    // updates are done with the q|k tiles; 7: the products in flight when a wait has given up;
+    // 8 (rank 0, with the surprise output): the peers' partial norms (one phase per chunk)
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::BAR);
     // per-token surprise sums (used only when SURP): this CTA's partials over its hidden units / owned
     // output rows, and on rank 0 their cluster-wide sums for chunks of even / odd index
     float* sp_loc = reinterpret_cast<float*>(sm + L::SP);  // [a2 | d2 | e2 | k2][64]
-    float* sp_acc = sp_loc + 4 * BC;                        // [2][a2 | d2 | e2][64]
+    float* sp_slot = sp_loc + 4 * BC;                       // on rank 0: [NC][a2 | d2 | e2][64]
     __shared__ uint32_t s_tmem;
 
     const int tid = threadIdx.x;
@@ -248,8 +250,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int jg0 = HS * rank;            // this CTA's first hidden unit
 
     if (tid == 0) {
-        for (int i = 0; i < 8; ++i) mbar_init(&bars[i], 1);
+        for (int i = 0; i < 9; ++i) mbar_init(&bars[i], 1);
         fence_mbar_init();
+        if (SURP && rank == 0 && nchunks > 0) mbar_arrive_expect_tx(&bars[8], L::SP_BYTES);
         if (nchunks > 0) {  // chunk 0's expected bytes (the cluster barrier below precedes any peer's stores)
             mbar_arrive_expect_tx(&bars[3], L::TX_PART);
             mbar_arrive_expect_tx(&bars[4], L::TX_E);
@@ -339,7 +342,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
     }
     if (SURP)
-        for (int i = tid; i < 10 * BC; i += NTHREADS) sp_loc[i] = 0.0f;
+        for (int i = tid; i < 4 * BC; i += NTHREADS) sp_loc[i] = 0.0f;
     fence_proxy_async();
     tc_fence_before();
     cluster_sync();
@@ -733,12 +736,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             atomicAdd(&sp_loc[3 * BC + t], k2);
         }
         handoff();
-        if (SURP && tid < BC) {  // this CTA's partials onto rank 0's cluster sums for this chunk
-            float* acc = sp_acc + (c & 1) * 3 * BC;
+        if (SURP && tid < BC) {  // this CTA's partial norms into its slot on rank 0 (counted there)
 #pragma unroll
             for (int m = 0; m < 3; ++m) {
-                red_cluster_add_f32(map_to_rank(smem_u32(acc + m * BC + tid), 0u), sp_loc[m * BC + tid]);
+                const float v = sp_loc[m * BC + tid];
                 sp_loc[m * BC + tid] = 0.0f;
+                if (rank == 0) sp_slot[m * BC + tid] = v;
+                else if (!failed)
+                    st_async_b32(map_to_rank(smem_u32(sp_slot + (rank * 3 + m) * BC + tid), 0u), __float_as_uint(v),
+                                 map_to_rank(smem_u32(&bars[8]), 0u));
             }
         }
         // ---- G4: [DU; P1] delta -> rows 64..127 sum_i P1[t][i] delta_i; state updates
@@ -881,17 +887,22 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             // the W1 copy shares its tile with e^T lo, whose owned rows this CTA's bulk
             // copies read: every peer has received them once its retrieval partials are here
             copy_state(0);
-            if (SURP) cluster_sync();  // rank 0's surprise sums of this chunk are complete
+            if (SURP) {  // rank 0: the peers' partial norms of this chunk (no cluster barrier: a peer's
+                         // next ones follow its next E3, which needed rank 0's next rows of e^T)
+                bool ok = true;
+                if (rank == 0 && !failed) ok = mbar_wait_cluster(&bars[8], (uint32_t)(c & 1), WAIT_NS);
+                failed = __syncthreads_or(!ok) || failed;
+                if (rank == 0 && tid == 0 && !failed && c + 1 < nchunks) mbar_arrive_expect_tx(&bars[8], L::SP_BYTES);
+            }
             if (SURP && tid < BC) {
                 // surprise_t = sqrt(||delta_t||^2 ||k_t||^2 + ||e_t||^2 ||a(k_t)||^2), sums over the cluster
-                float* acc = sp_acc + (c & 1) * 3 * BC;
-                if (rank == 0) {
-                    if (tid < n)
-                        a.surprise[unit * T + t0 + tid] =
-                            sqrtf(fmaf(acc[BC + tid], sp_loc[3 * BC + tid], acc[2 * BC + tid] * acc[tid]));
-                    acc[tid] = 0.0f;
-                    acc[BC + tid] = 0.0f;
-                    acc[2 * BC + tid] = 0.0f;
+                if (rank == 0 && tid < n) {
+                    float s[3] = {0.0f, 0.0f, 0.0f};
+#pragma unroll
+                    for (int p = 0; p < NC; ++p)
+#pragma unroll
+                        for (int m = 0; m < 3; ++m) s[m] += sp_slot[(p * 3 + m) * BC + tid];
+                    a.surprise[unit * T + t0 + tid] = sqrtf(fmaf(s[1], sp_loc[3 * BC + tid], s[2] * s[0]));
                 }
                 sp_loc[3 * BC + tid] = 0.0f;
             }
