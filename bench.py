@@ -57,14 +57,14 @@ METRIC = "memory-layer fwd tokens/sec (B*H*T/s) and % of roofline (TC FLOPs vs H
 # traffic x 8, plus the state read and written once per call); the streamed workload's is one
 # 65536-token segment call, which is what one launch of its bench step processes.
 NCU_TRAFFIC = {
-    "mlp_64x256_bf16_b4h8_t4096_c64": (("nm_tc_mlp.cu", "tc_common.cuh", "nm_internal.h"), "ce6578f7977bfa19",
-                                       62.12e6),
-    "linear_d128_bf16_b8h16_t16384_c64": (("nm_tc_linear.cu", "tc_common.cuh", "nm_internal.h"), "1023aaf0415483b9",
+    "mlp_64x256_bf16_b4h8_t4096_c64": (("nm_tc_mlp.cu", "tc_common.cuh", "nm_internal.h"), "810ad16e5ee50003",
+                                       62.45e6),
+    "linear_d128_bf16_b8h16_t16384_c64": (("nm_tc_linear.cu", "tc_common.cuh", "nm_internal.h"), "f6f951c6577d621c",
                                           2.173e9),
     "mlp_128x512_bf16_b2h16_t131072_c64": (("nm_tc_mlp_wide.cu", "tc_common.cuh", "nm_internal.h"),
-                                           "94ec2fe9a90624d6", 4.179e9),
+                                           "d70d351ebd9b6b93", 4.178e9),
     "linear_d64_bf16_b1h8_t2097152_c256_seg65536": (("nm_tc_linear64.cu", "tc_common.cuh", "nm_internal.h"),
-                                                    "a3372d2aa55b45e2", 254.7e6),
+                                                    "cd0494a3b25f3211", 254.6e6),
 }
 
 
