@@ -753,7 +753,7 @@ def main():
     ap.add_argument("--backward", action="store_true",
                     help="time nm_backward (gradients of every input) on the workload instead of the forward")
     ap.add_argument("--layers", type=int, default=None,
-                    help="MLP workloads: a memory of this many layers instead of 2 (fp32 FFMA kernel for > 2)")
+                    help="MLP workloads: a memory of this many layers instead of 2")
     ap.add_argument("--cpu-budget", type=float, default=None,
                     help="seconds of oracle work per step of the reference arm (default: about 150 s in all)")
     ap.add_argument("--B", type=int, default=None, help="override the workload's batch (small profiling cases)")

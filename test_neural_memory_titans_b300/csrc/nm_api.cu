@@ -461,13 +461,13 @@ int nm_forward_host(nm_handle_t h, int B, int H, int T, const void* q, const voi
     // inputs are still being copied.  One group per NM_HOST_GROUP_BYTES of q + y, at least 2 and at most
     // NM_HOST_MAX_GROUPS and the number of units: a group's forward starts once its own inputs are in, so small
     // groups keep the kernels busy behind the copies (and few CTAs in flight at once), while each group costs a
-    // dozen copy calls.  Used on the tensor-core path (no shared workspace) when every group's slice of every
-    // buffer starts on a 16-byte boundary.
+    // dozen copy calls.  Used on the tensor-core path when its kernel needs no workspace (the groups' kernels
+    // would share it) and every group's slice of every buffer starts on a 16-byte boundary.
     const size_t by_bytes = (in_b + out_b + NM_HOST_GROUP_BYTES - 1) / NM_HOST_GROUP_BYTES;
     const int groups = (int)std::min<size_t>(std::min<size_t>((size_t)NM_HOST_MAX_GROUPS, units),
                                              std::max<size_t>(2, by_bytes));
-    if (h->path == NM_PATH_TC && T > 0 && groups > 1 && (T % 4) == 0 && (P % 4) == 0 &&
-        in_b + out_b >= ((size_t)8 << 20)) {
+    if (h->path == NM_PATH_TC && nm_tc_scratch_bytes(cfg, B, H) == 0 && T > 0 && groups > 1 && (T % 4) == 0 &&
+        (P % 4) == 0 && in_b + out_b >= ((size_t)8 << 20)) {
         int prc = ensure_pipe(h);
         if (prc != NM_OK) return prc;
         const size_t in_u = (size_t)T * cfg.d * dtype_bytes(cfg.in_dtype), out_u = (size_t)T * cfg.d * dtype_bytes(cfg.out_dtype);

@@ -591,7 +591,7 @@ def test_surprise_mlp_d128(path, hidden, T, delta):
     _surprise_case(wl, x, path, M0, S0, delta)
 
 
-# ------------------------------------------------------------ deeper MLP memories (L >= 3), fp32 FFMA kernel
+# ------------------------------------------------------------ deeper MLP memories (L >= 3)
 
 def _deep_state(d, hidden, layers, seed, scale=0.5):
     g = torch.Generator("cuda").manual_seed(seed)
@@ -610,8 +610,17 @@ def _deep_state(d, hidden, layers, seed, scale=0.5):
     (4, 32, 64, 150, 16, torch.float32, None),
     (3, 64, 96, 90, 64, torch.bfloat16, 0.5),
     (5, 16, 32, 70, 8, torch.float32, 0.3),
+    (4, 32, 64, 150, 16, torch.bfloat16, None),
+    (3, 128, 256, 130, 64, torch.bfloat16, None),
+    (3, 64, 512, 70, 64, torch.bfloat16, 0.5),
+    (3, 128, 384, 65, 32, torch.bfloat16, None),
 ])
-def test_deep_memory(layers, d, hidden, T, chunk, dtype, delta):
+@pytest.mark.parametrize("path", PATHS)
+def test_deep_memory(layers, d, hidden, T, chunk, dtype, delta, path):
+    """L >= 3 layers on both kernel families: the tf32 tensor-core kernel
+    takes bf16 inputs (hidden widths of one to four 128-row tiles, state
+    updates in column blocks of 256), the fp32 FFMA kernel both input types;
+    y, the state and the surprise against the oracle."""
     wl = dataclasses.replace(W.WORKLOADS[1], d=d, hidden=hidden, chunk=chunk, dtype=dtype).with_sizes(B=1, H=2, T=T)
     x = W.make_inputs(wl, "cuda", seed=150 + layers + T)
     x["eta"] *= 0.5
@@ -620,9 +629,20 @@ def test_deep_memory(layers, d, hidden, T, chunk, dtype, delta):
     M0 = torch.stack(m0).reshape(1, 2, P).contiguous()
     S0 = torch.stack(s0).reshape(1, 2, P).contiguous()
     loss = nm.LOSS_L2 if delta is None else nm.LOSS_HUBER
-    mem = nm.NeuralMemory(nm.MLP2, d, hidden, chunk, in_dtype=dtype, layers=layers, loss=loss,
-                          huber_delta=0.0 if delta is None else delta)
-    assert mem.path == nm.PATH_SIMT
+    kw = dict(in_dtype=dtype, layers=layers, loss=loss, huber_delta=0.0 if delta is None else delta)
+    if path == nm.PATH_TC and dtype == torch.float32:
+        # the tensor-core kernel takes bf16 inputs only
+        with pytest.raises(nm.NMError) as ei:
+            nm.NeuralMemory(nm.MLP2, d, hidden, chunk, path=path, **kw)
+        assert ei.value.status == nm.NM_ERR_UNSUPPORTED
+        return
+    if path == nm.PATH_SIMT and hidden > 128 and T > 100:
+        pytest.skip("the fp32 FFMA kernel is covered by the smaller shapes")
+    mem = nm.NeuralMemory(nm.MLP2, d, hidden, chunk, path=path, **kw)
+    assert mem.path == path
+    auto = nm.NeuralMemory(nm.MLP2, d, hidden, chunk, **kw)
+    assert auto.path == (nm.PATH_TC if dtype == torch.bfloat16 and d >= 32 else nm.PATH_SIMT)
+    auto.close()
     y, MT, ST, sur = mem.forward_surprise(x["q"], x["k"], x["v"], x["alpha"], x["eta"], x["beta"], M0, S0)
     assert mem.synchronize() == nm.NM_OK
     mem.close()
@@ -635,10 +655,73 @@ def test_deep_memory(layers, d, hidden, T, chunk, dtype, delta):
     assert rel_l2(f64(MT), ref[1]) <= tol["M_T"]
     assert rel_l2(f64(ST), ref[2]) <= tol["S_T"]
     assert rel_l2(f64(sur), ref[3]) <= tol["y"]
-    # a deeper memory is not built on the tensor-core path
-    with pytest.raises(nm.NMError) as ei:
-        nm.NeuralMemory(nm.MLP2, d, hidden, chunk, in_dtype=dtype, layers=layers, path=nm.PATH_TC)
-    assert ei.value.status == nm.NM_ERR_UNSUPPORTED
+    for u in range(2):  # every unit on its own
+        assert rel_l2(f64(y[0, u]), ref[0][0, u]) <= tol["y"]
+        assert rel_l2(f64(MT[0, u]), ref[1][0, u]) <= tol["M_T"]
+
+
+@pytest.mark.parametrize("c_mode", [nm.C_ONE_MINUS_BETA, nm.C_PER_TOKEN])
+def test_deep_memory_tc_momentum_forms(c_mode):
+    """The tensor-core deep kernel with the pages' other momentum forms."""
+    d, hidden, layers, T = 64, 128, 3, 150
+    wl = dataclasses.replace(W.WORKLOADS[1], hidden=hidden).with_sizes(B=1, H=2, T=T)
+    x = W.make_inputs(wl, "cuda", seed=181)
+    x["eta"] *= 0.5
+    P = nm.param_count(nm.MLP2, d, hidden, layers)
+    m0, s0 = zip(*(_deep_state(d, hidden, layers, seed=182 + u) for u in range(2)))
+    M0 = torch.stack(m0).reshape(1, 2, P).contiguous()
+    S0 = torch.stack(s0).reshape(1, 2, P).contiguous()
+    c = None
+    if c_mode == nm.C_PER_TOKEN:
+        g = torch.Generator("cuda").manual_seed(183)
+        c = torch.rand((1, 2, T), generator=g, device="cuda")
+    mem = nm.NeuralMemory(nm.MLP2, d, hidden, 64, in_dtype=torch.bfloat16, layers=layers, c_mode=c_mode,
+                          path=nm.PATH_TC)
+    y, MT, ST = mem.forward(x["q"], x["k"], x["v"], x["alpha"], x["eta"], x["beta"], M0, S0, c=c)
+    assert mem.synchronize() == nm.NM_OK
+    mem.close()
+    ref = oracle.forward(oracle.MLP2, d, hidden, 64, c_mode,
+                         *(f64(x[k_]) for k_ in ("q", "k", "v", "alpha", "eta", "beta")),
+                         None if c is None else f64(c), f64(M0), f64(S0), layers=layers)
+    tol = TOL[torch.bfloat16]
+    assert rel_l2(f64(y), ref[0]) <= tol["y"]
+    assert rel_l2(f64(MT), ref[1]) <= tol["M_T"]
+    assert rel_l2(f64(ST), ref[2]) <= tol["S_T"]
+
+
+def test_deep_memory_tc_long_run():
+    """4096 tokens of a 64 -> 256 -> 256 -> 64 memory on the tensor-core
+    kernel from random states, every unit at the bf16 tolerances: the
+    state's rounding (tf32 operands) does not accumulate past them over 64
+    chunks.  With the workload's gates this memory diverges (eta x 0.5,
+    alpha x 0.1) or its weights decay towards zero (eta x 0.25); eta x 0.2
+    with alpha x 0.05 keeps them finite, moving and away from zero (the
+    oracle's regime is checked first; in a CPU probe of the same recipe
+    max |W| was about 8e-3 and a 1e-9 perturbation of v grew about 3 times
+    in the state)."""
+    d, hidden, layers, T = 64, 256, 3, 4096
+    wl = dataclasses.replace(W.WORKLOADS[1], hidden=hidden).with_sizes(B=1, H=4, T=T)
+    x = W.make_inputs(wl, "cuda", seed=191)
+    x["eta"] *= 0.2
+    x["alpha"] *= 0.05
+    P = nm.param_count(nm.MLP2, d, hidden, layers)
+    m0, s0 = zip(*(_deep_state(d, hidden, layers, seed=192 + u) for u in range(4)))
+    M0 = torch.stack(m0).reshape(1, 4, P).contiguous()
+    S0 = torch.stack(s0).reshape(1, 4, P).contiguous()
+    mem = nm.NeuralMemory(nm.MLP2, d, hidden, 64, in_dtype=torch.bfloat16, layers=layers, path=nm.PATH_TC)
+    y, MT, ST = mem.forward(x["q"], x["k"], x["v"], x["alpha"], x["eta"], x["beta"], M0, S0)
+    assert mem.synchronize() == nm.NM_OK
+    mem.close()
+    ref = oracle.forward(oracle.MLP2, d, hidden, 64, oracle.C_ONE,
+                         *(f64(x[k_]) for k_ in ("q", "k", "v", "alpha", "eta", "beta")), None, f64(M0), f64(S0),
+                         layers=layers)
+    assert np.isfinite(ref[1]).all() and 1e-4 < np.abs(ref[1]).max() < 1e3
+    assert rel_l2(ref[1], f64(M0)) > 1e-2  # the state moved
+    tol = TOL[torch.bfloat16]
+    for u in range(4):
+        assert rel_l2(f64(y[0, u]), ref[0][0, u]) <= tol["y"]
+        assert rel_l2(f64(MT[0, u]), ref[1][0, u]) <= tol["M_T"]
+        assert rel_l2(f64(ST[0, u]), ref[2][0, u]) <= tol["S_T"]
 
 
 # ------------------------------------------------------------ Memory-as-Gate output
@@ -650,7 +733,8 @@ def test_deep_memory(layers, d, hidden, T, chunk, dtype, delta):
 @pytest.mark.parametrize("wid,T,chunk,path,layers", [
     (0, 200, 16, nm.PATH_SIMT, 2), (2, 300, 64, nm.PATH_SIMT, 2), (2, 300, 64, nm.PATH_TC, 2),
     (4, 700, 256, nm.PATH_TC, 2), (4, 130, 64, nm.PATH_TC, 2), (1, 150, 64, nm.PATH_SIMT, 2),
-    (1, 150, 64, nm.PATH_TC, 2), (3, 100, 64, nm.PATH_TC, 2), (1, 90, 64, nm.PATH_SIMT, 3)])
+    (1, 150, 64, nm.PATH_TC, 2), (3, 100, 64, nm.PATH_TC, 2), (1, 90, 64, nm.PATH_SIMT, 3),
+    (1, 90, 64, nm.PATH_TC, 3)])
 def test_mag_gate(wid, T, chunk, path, layers):
     wl = dataclasses.replace(W.WORKLOADS[wid].with_sizes(B=2, H=2, T=T, segment=0), chunk=chunk, layers=layers)
     if layers > 2:
