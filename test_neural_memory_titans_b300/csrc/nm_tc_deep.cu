@@ -20,28 +20,38 @@
 // Design.  One CTA (8 warps) per (batch, head) unit walks the sequence.  The
 // fp32 state of a deep memory (2 P floats, 768 KB for 64 -> 256 -> 256 -> 64)
 // exceeds one SM's TMEM and shared memory, so it stays in the caller's M_T /
-// S_T buffers, updated in place once per chunk, where the L2 (126 MB) holds it
-// for every unit at once; the chunk's activations go to a per-unit workspace
-// the same way.  Every contraction of a chunk (the keys' forward per layer,
-// the output error, the backward per layer, the Gamma-masked inner products,
-// the retrieval per layer and the two state updates per layer) is one
-// tensor-core GEMM C[M x N] += sum_k A[m][k] B[n][k] with the accumulator in
-// TMEM: its operands are read from L2 by all threads in blocks of 32 k,
-// scaled where the formula scales them (A_t, -sigma_t, gamma_i, u_i), rounded
-// to tf32 (round to nearest) and written into shared memory in the 128-byte
-// swizzled K-major layout, double-buffered so that the next block is staged
-// while the tensor cores work on the current one; one thread issues
-// tcgen05.mma kind::tf32 (M = 128 rows per tile, K = 8 per instruction).
-// Transposed operands (W^T in the backward, delta^T and x^T in the updates)
-// are the same loads with the strides swapped, so no transposed copy is ever
-// stored.  Operands are fp32 rounded once to tf32 (11 significant bits):
-// finer than a single bf16 rounding by a factor of 8, which the memory's
-// sensitivity to gradient-path rounding needs, at half the bf16 rate and
-// without the extra products of a hi/lo split.
+// S_T buffers, updated in place once per chunk, where the L2 (126 MB) holds it.
+// Every contraction of a chunk (the keys' forward per layer, the output error,
+// the backward per layer, the Gamma-masked inner products, the retrieval per
+// layer and the two state updates per layer) is one tensor-core GEMM
+// C[M x N] += sum_k A[m][k] B[n][k], tcgen05.mma kind::tf32 (M = 128 rows per
+// tile, K = 8 per instruction) with the accumulator in TMEM.
 //
-// Every wait (the MMA completions) gives up after 2 s of %globaltimer; the
-// CTA then records NM_ERR_DEVICE_TIMEOUT, issues nothing more, drains with
-// bounded waits, frees its TMEM and exits.
+// Its operands come from a per-unit workspace of operand tiles: tf32 values
+// (rounded to nearest) already in the 128-byte-swizzled K-major layout the
+// tensor cores read, in blocks of 32 k (a block of R rows is R x 128 bytes).
+// Each producer writes its results there in every form a later product
+// consumes: the keys' forward epilogue writes x_l as [t][j] (a B operand) and
+// as [j][t] (the update's B operand), the backward epilogue delta_l as [t][j]
+// and as [j][t] three times (plain, times gamma_t, times u_t), the retrieval
+// epilogue r_l three times (plain, times A_t, times -sigma_t), the inner-product
+// epilogue -G, and the update epilogue, next to the fp32 state, W_l and S_l as
+// [o][i] and W_l as [i][o] for the backward.  A block of a product is then one
+// or two bulk copies (cp.async.bulk) into shared memory, issued by one thread,
+// which also issues the MMAs: the copies run up to 3 blocks ahead over a ring
+// of stages (full / empty mbarriers), and no thread stages operands.  The
+// scalings of the formula (A_t, -sigma_t, gamma_i, u_i) live in those copies,
+// so each of retrieval's three chains and each update adds into its
+// accumulator directly.  Transposes cost nothing extra: a thread that holds a
+// row of an accumulator writes a row of one form and a column of the other.
+// fp32 rounded once to tf32 (11 significant bits) is finer than a single
+// bf16 rounding by a factor of 8, which the memory's sensitivity to
+// gradient-path rounding needs, at half the bf16 rate and without the extra
+// products of a hi/lo split.
+//
+// Every wait (bulk copies, MMA completions) gives up after 2 s of
+// %globaltimer; the CTA then records NM_ERR_DEVICE_TIMEOUT, issues nothing
+// more, drains what it issued with bounded waits, frees its TMEM and exits.
 #include <cuda_bf16.h>
 
 #include "nm_internal.h"
@@ -56,6 +66,9 @@ constexpr int NTOK = 64;           // token rows of a chunk tile (chunks of at m
 constexpr int GSTR = NTOK + 1;     // padded row stride of Gamma in shared memory
 constexpr uint32_t ATILE = 128 * 128;   // one M = 128 tile of 32 fp32 k: 16 KB
 constexpr uint32_t BSTAGE = 256 * 128;  // up to 256 B rows of 32 fp32 k: 32 KB
+constexpr int MAX_STAGES = 4;
+constexpr uint32_t EPI_TBUF_BYTES = 36864;                          // 8 warps x 32 x 33 floats, rounded up
+constexpr uint32_t EPI_BYTES = EPI_TBUF_BYTES + (NT / 32) * 3 * 4096;  // + three 4 KB block buffers per warp
 constexpr uint64_t WAIT_NS = 2000000000ull;  // 2 s
 
 // Instruction descriptor of tcgen05.mma kind::tf32: tf32 A and B (format 2),
@@ -97,203 +110,326 @@ __device__ __forceinline__ float momentum_c(int mode, float beta, const float* c
     return 1.0f;
 }
 
-// One GEMM operand: element (r, k) is p[r * sr + k * sk] (fp32 or bf16) times
-// rs[r] (if set) times ks[k] (if set) times mul.  Rows r >= rlim are not
-// staged (the products in their row or column are never read); k >= klim
-// stages as zero (it would add to products that are read).
-struct Src {
-    const void* p;
-    long long sr, sk;
-    const float* rs;
-    const float* ks;
-    float mul;
-    int rlim, klim;
-    int bf16;
+
+// ---- operand tiles in global memory
+// A matrix of R rows and K columns (K a multiple of 32) stored as K / 32
+// blocks of R x 32 tf32 values, each block R 128-byte rows with the 16-byte
+// chunks of row r permuted by (chunk ^ (r % 8)): the K-major 128-byte swizzle,
+// so that any 8-row-aligned run of rows of a block, copied verbatim to a
+// 1024-byte-aligned shared-memory address, is a tensor-core operand.
+struct Tile {
+    float* p;
+    int R;
 };
 
-__device__ __forceinline__ Src src(const void* p, long long sr, long long sk, int rlim, int klim, int bf16 = 0,
-                                   const float* rs = nullptr, const float* ks = nullptr, float mul = 1.0f) {
-    Src s;
-    s.p = p; s.sr = sr; s.sk = sk; s.rs = rs; s.ks = ks; s.mul = mul; s.rlim = rlim; s.klim = klim; s.bf16 = bf16;
-    return s;
+// Float offset of element (r, k).
+__device__ __forceinline__ uint32_t toff(int R, int r, int k) {
+    return (uint32_t)(k >> 5) * (uint32_t)R * 32u + (uint32_t)r * 32u +
+           (((((uint32_t)k & 31u) >> 2) ^ ((uint32_t)r & 7u)) << 2) + ((uint32_t)k & 3u);
 }
 
-// One chain of products into one accumulator: sum over K (a multiple of 32)
-// of A (mt tiles of 128 rows) times B (N rows).  `fresh` starts the
-// accumulator at zero.
+// Per-unit workspace (floats), every region a multiple of 64 floats.
+struct Layout {
+    size_t tw[NM_MAX_LAYERS + 1], ts[NM_MAX_LAYERS + 1], twt[NM_MAX_LAYERS + 1];  // state tiles per layer
+    size_t tk, tkt, tq, tqa, tqs;                                              // this chunk's keys and queries
+    size_t tx[NM_MAX_LAYERS], txt[NM_MAX_LAYERS], z[NM_MAX_LAYERS];            // hidden layers 1 .. L-1
+    size_t td[NM_MAX_LAYERS + 1], tdt[NM_MAX_LAYERS + 1], tdg[NM_MAX_LAYERS + 1], tdu[NM_MAX_LAYERS + 1];
+    size_t tr[NM_MAX_LAYERS], tra[NM_MAX_LAYERS], trs[NM_MAX_LAYERS];
+    size_t tg;
+    size_t total;
+};
+
+__host__ __device__ inline Layout deep_layout(int d, int h, int L) {
+    Layout o;
+    size_t at = 0;
+    auto take = [&](size_t n) { const size_t r = at; at += (n + 63) & ~(size_t)63; return r; };
+    for (int l = 1; l <= L; ++l) {
+        const size_t in = l == 1 ? d : h, out = l == L ? d : h;
+        o.tw[l] = take(out * in);
+        o.ts[l] = take(out * in);
+        o.twt[l] = l >= 2 ? take(in * out) : 0;
+    }
+    o.tk = take((size_t)NTOK * d);
+    o.tkt = take((size_t)d * NTOK);
+    o.tq = take((size_t)NTOK * d);
+    o.tqa = take((size_t)NTOK * d);
+    o.tqs = take((size_t)NTOK * d);
+    for (int l = 1; l < L; ++l) {
+        o.tx[l] = take((size_t)NTOK * h);
+        o.txt[l] = take((size_t)h * NTOK);
+        o.z[l] = take((size_t)NTOK * h);
+        o.tr[l] = take((size_t)NTOK * h);
+        o.tra[l] = take((size_t)NTOK * h);
+        o.trs[l] = take((size_t)NTOK * h);
+    }
+    for (int l = 1; l <= L; ++l) {  // delta_l (delta_L = e): [t][j] and [j][t] plain, x gamma_t, x u_t
+        const size_t w = l == L ? d : h;
+        o.td[l] = take((size_t)NTOK * w);
+        o.tdt[l] = take(w * NTOK);
+        o.tdg[l] = take(w * NTOK);
+        o.tdu[l] = take(w * NTOK);
+    }
+    o.tg = take((size_t)NTOK * NTOK);
+    o.total = at;
+    return o;
+}
+
+// Shared memory: `ns` stages of (mt_max A tiles + one B block), Gamma, the
+// gate vectors, the mbarriers and flags.
+__host__ __device__ inline uint32_t deep_stage_bytes(int mt_max) { return (uint32_t)mt_max * ATILE + BSTAGE; }
+__host__ __device__ inline uint32_t deep_smem_bytes(int mt_max, int ns) {
+    return (uint32_t)ns * deep_stage_bytes(mt_max) + NTOK * GSTR * 4 + 9 * NTOK * 4 + 256 + 1024;
+}
+__host__ inline int deep_stages(int mt_max) {
+    int ns = MAX_STAGES;
+    while (ns > 2 && deep_smem_bytes(mt_max, ns) > 232448) --ns;
+    return ns;
+}
+// the smallest operand-stage area of any launch is 2 stages of 3 A tiles (hidden 384)
+static_assert(2 * (3 * ATILE + BSTAGE) >= EPI_BYTES, "the epilogues' buffers fit in the operand stages");
+
+// ---- the product pipeline: one thread copies operand blocks and issues the MMAs
+
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+
+// Makes this thread's generic-proxy global writes visible to later bulk copies.
+__device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+
+// One chain of products into one accumulator: K (a multiple of 32) of A
+// (rows a_row0 .. of tile set a, mt tiles of 128 rows) times B (rows
+// b_row0 .. b_row0 + N - 1 of tile set b).  `fresh` starts at zero.
 struct Seg {
-    Src a, b;
+    const float* a;
+    int a_R, a_row0;
+    const float* b;
+    int b_R, b_row0;
     int K;
     uint32_t col;  // TMEM column of M-tile 0's accumulator; tile m at col + m * N
     int fresh;
 };
 
-__device__ __forceinline__ float ld_elem(const Src& s, long long off) {
-    if (s.bf16) return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(s.p)[off]);
-    return reinterpret_cast<const float*>(s.p)[off];
+__device__ __forceinline__ Seg seg(const Tile& a, int a_row0, const Tile& b, int b_row0, int K, uint32_t col,
+                                   int fresh) {
+    Seg s;
+    s.a = a.p; s.a_R = a.R; s.a_row0 = a_row0;
+    s.b = b.p; s.b_R = b.R; s.b_row0 = b_row0;
+    s.K = K; s.col = col; s.fresh = fresh;
+    return s;
 }
 
-// Stages columns k0 .. k0 + 31 of rows 0 .. R - 1 of operand s into a tile of
-// R 128-byte rows (16-byte chunk kc of row r at r * 128 + ((kc ^ (r % 8)) * 16)),
-// as tf32.  Consecutive threads take consecutive 16-byte chunks of a row when
-// k is contiguous in memory, consecutive rows otherwise, so that the global
-// loads of a warp are coalesced either way.
-__device__ __forceinline__ void stage(uint32_t tile, int R, const Src& s, int k0, int tid) {
-    const int rows = min(R, s.rlim);
-    const int n = rows * 8;
-    const bool kfast = s.sk == 1;
-    for (int idx = tid; idx < n; idx += NT) {
-        int r, kc;
-        if (kfast) {
-            r = idx >> 3;
-            kc = idx & 7;
-        } else {
-            r = idx % rows;
-            kc = idx / rows;
-        }
-        const int k = k0 + 4 * kc;
-        float v[4];
-        const long long base = (long long)r * s.sr + (long long)k * s.sk;
-        if (kfast && k + 3 < s.klim) {
-            if (s.bf16) {
-                const uint2 w = *reinterpret_cast<const uint2*>(reinterpret_cast<const __nv_bfloat16*>(s.p) + base);
-                v[0] = bf16_lo(w.x); v[1] = bf16_hi(w.x); v[2] = bf16_lo(w.y); v[3] = bf16_hi(w.y);
-            } else {
-                const float4 w = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(s.p) + base);
-                v[0] = w.x; v[1] = w.y; v[2] = w.z; v[3] = w.w;
-            }
-        } else {
-#pragma unroll
-            for (int j = 0; j < 4; ++j) v[j] = k + j < s.klim ? ld_elem(s, base + (long long)j * s.sk) : 0.0f;
-        }
-        const float rf = (s.rs ? s.rs[r] : 1.0f) * s.mul;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            float f = v[j] * rf;
-            if (s.ks) f *= k + j < s.klim ? s.ks[k + j] : 0.0f;
-            v[j] = f;
-        }
-        st_shared_v4(tile + (uint32_t)r * 128u + (((uint32_t)kc ^ ((uint32_t)r & 7u)) << 4), to_tf32(v[0]),
-                     to_tf32(v[1]), to_tf32(v[2]), to_tf32(v[3]));
-    }
-}
-
-// The double-buffered product pipeline of one CTA: two operand stages, one
-// mbarrier per stage that the MMA commit of the stage's block arrives on.
 struct Pipe {
-    uint32_t a_st[2], b_st[2];  // shared-memory addresses of the A and B stages
-    uint64_t* bars;             // [2]
-    uint32_t ph[2];             // completions of each barrier waited for so far
-    uint32_t pending[2];        // a commit on the barrier not yet waited for
-    uint32_t tm;                // TMEM base address (lane 0, column 0)
-    int failed;                 // a wait gave up: nothing more is issued
+    uint32_t st[MAX_STAGES];  // stage base addresses: A tiles, then the B block at + boff
+    uint32_t boff;
+    int ns;
+    uint64_t* full;   // [ns] a stage's copies landed
+    uint64_t* empty;  // [ns] the products that read a stage completed
+    uint64_t* done;   // all products of a GEMM completed (or the producer gave up)
+    int* s_fail;
+    uint32_t tm;
+    uint32_t g;       // operand blocks issued so far (thread 0)
+    uint32_t ndone;   // GEMMs finished (every thread)
+    uint32_t pend_full, pend_empty;  // bit per stage: a phase issued and not yet waited for (thread 0)
+    int failed;
 };
 
-__device__ __forceinline__ bool pipe_wait(Pipe& p, int st) {
-    if (!p.pending[st]) return true;
-    const bool ok = mbar_wait(&p.bars[st], p.ph[st] & 1u, WAIT_NS);
-    p.ph[st] += 1;
-    p.pending[st] = 0;
-    return ok;
-}
-
-// Runs the products of `nseg` segments (all threads of the CTA), each over
-// its K in blocks of 32: block kb is staged into stage kb % 2 once the
-// products of block kb - 2 have completed, then thread 0 issues its
-// mt x 4 MMAs (K = 8 each) and commits them.  Returns with every product
-// complete (or p.failed set).
-__device__ void gemm(Pipe& p, const Seg* segs, int nseg, int mt, int N, int tid) {
-    if (p.failed) return;
+// Thread 0: the copies and products of one GEMM.  Block b of the GEMM goes
+// to stage (g + b) % ns.  The copies of ns - 1 blocks are issued first; after
+// the products of block b are issued, the copies of block b + ns - 1 follow,
+// into the stage that block b - 1's products read (waited for on its empty
+// barrier, while block b's products keep the tensor cores busy).
+__device__ __noinline__ void run_gemm(Pipe& p, const Seg* segs, int nseg, int mt, int N) {
+    int total = 0;
+    for (int s = 0; s < nseg; ++s) total += segs[s].K >> 5;
     const uint32_t idesc = idesc_tf32((uint32_t)N);
-    int kb = 0;
-    bool bad = false;
-    for (int s = 0; s < nseg && !p.failed; ++s) {
-        const Seg& g = segs[s];
-        for (int k0 = 0; k0 < g.K; k0 += 32, ++kb) {
-            const int st = kb & 1;
-            if (!pipe_wait(p, st)) bad = true;
-            stage(p.a_st[st], 128 * mt, g.a, k0, tid);
-            stage(p.b_st[st], N, g.b, k0, tid);
-            fence_proxy_async();
-            if (__syncthreads_or(bad)) {
-                p.failed = 1;
-                break;
-            }
-            if (tid == 0) {
-                tc_fence_after();
-                for (int m = 0; m < mt; ++m) {
+    const uint32_t ns = (uint32_t)p.ns;
+    bool ok = true;
+    int issued = 0, is = 0, ikb = 0;  // next block to copy: its segment and block within the segment
+    auto issue_next = [&]() {
+        const uint32_t gb = p.g + (uint32_t)issued;
+        const int st = (int)(gb % ns);
+        if (p.pend_empty >> st & 1u) {
+            ok = mbar_wait(&p.empty[st], ((gb / ns) - 1u) & 1u, WAIT_NS);
+            p.pend_empty &= ~(1u << st);
+            if (!ok) return;
+        }
+        const Seg& g = segs[is];
+        const uint32_t arows = (uint32_t)min(128 * mt, g.a_R - g.a_row0);
+        const uint32_t ab = arows * 128u, bb = (uint32_t)N * 128u;
+        mbar_arrive_expect_tx(&p.full[st], ab + bb);
+        bulk_g2s(p.st[st], g.a + ((size_t)ikb * g.a_R + g.a_row0) * 32, ab, &p.full[st]);
+        bulk_g2s(p.st[st] + p.boff, g.b + ((size_t)ikb * g.b_R + g.b_row0) * 32, bb, &p.full[st]);
+        p.pend_full |= 1u << st;
+        ++issued;
+        if (++ikb == (g.K >> 5)) {
+            ikb = 0;
+            ++is;
+        }
+    };
+    while (ok && issued < total && issued < p.ns - 1) issue_next();
+    for (int b = 0, cs = 0, ckb = 0; b < total && ok; ++b) {
+        const uint32_t gb = p.g + (uint32_t)b;
+        const int st = (int)(gb % ns);
+        ok = mbar_wait(&p.full[st], (gb / ns) & 1u, WAIT_NS);
+        p.pend_full &= ~(1u << st);
+        if (!ok) break;
+        tc_fence_after();
+        const Seg& g = segs[cs];
+        for (int m = 0; m < mt; ++m) {
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        mma_tf32(p.tm + g.col + (uint32_t)(m * N), kdesc(p.a_st[st] + m * ATILE + kk * 32),
-                                 kdesc(p.b_st[st] + kk * 32), idesc, (g.fresh && k0 == 0 && kk == 0) ? 0u : 1u);
-                }
-                mma_commit(&p.bars[st]);
-            }
-            p.pending[st] = 1;
+            for (int kk = 0; kk < 4; ++kk)
+                mma_tf32(p.tm + g.col + (uint32_t)(m * N), kdesc(p.st[st] + (uint32_t)m * ATILE + kk * 32),
+                         kdesc(p.st[st] + p.boff + kk * 32), idesc, (g.fresh && ckb == 0 && kk == 0) ? 0u : 1u);
         }
+        mma_commit(&p.empty[st]);
+        p.pend_empty |= 1u << st;
+        if (++ckb == (g.K >> 5)) {
+            ckb = 0;
+            ++cs;
+        }
+        if (issued < total) issue_next();
     }
-    if (!pipe_wait(p, kb & 1)) bad = true;
-    if (!pipe_wait(p, (kb + 1) & 1)) bad = true;
-    if (__syncthreads_or(bad)) p.failed = 1;
+    p.g += (uint32_t)total;
+    if (ok) {
+        mma_commit(p.done);
+    } else {
+        *reinterpret_cast<volatile int*>(p.s_fail) = 1;
+        mbar_arrive(p.done);
+    }
+}
+
+// Every thread: run one GEMM (thread 0 drives it) and wait for it.  Returns
+// false once any wait has given up.
+__device__ __forceinline__ bool gemm(Pipe& p, const Seg* segs, int nseg, int mt, int N, int tid) {
+    if (p.failed) return false;
+    if (tid < 32) {  // the producer's warp-mates wait at a warp barrier, not on the mbarrier: a
+                     // try_wait may suspend the whole warp and with it the producer
+        if (tid == 0) run_gemm(p, segs, nseg, mt, N);
+        __syncwarp();
+    }
+    const bool ok = mbar_wait(p.done, p.ndone & 1u, 2 * WAIT_NS);
+    p.ndone += 1;
+    if (__syncthreads_or(!ok || *reinterpret_cast<volatile int*>(p.s_fail))) p.failed = 1;
     tc_fence_after();
+    return !p.failed;
 }
 
-// Reads an M = 128 x N accumulator (mt tiles, tile m at column col + m N)
-// out of TMEM: warp w takes lanes 32 (w % 4) .. + 31 and half w / 4 of the
-// columns, 16 at a time, and calls f(row, first column, values[16]) for rows
-// below `rows`.
+// Visits an M = 128 x N accumulator (mt tiles, tile m at column col + m N,
+// N / 2 a multiple of 32) in blocks of 32 rows x 32 columns read from TMEM:
+// warp w takes the rows of lanes 32 (w % 4) .. + 31 (its TMEM sub-partition)
+// and column half w / 4, and calls f(first row, first column, v) with v this
+// lane's row (row first row + lane), for row blocks below `rows` (a multiple
+// of 32).
 template <typename F>
-__device__ __forceinline__ void epilogue(const Pipe& p, uint32_t col, int mt, int N, int rows, int warp, int lane,
-                                         F&& f) {
+__device__ __forceinline__ void epi32(const Pipe& p, uint32_t col, int mt, int N, int rows, int warp, F&& f) {
     if (p.failed) return;
-    const int q = warp & 3, hf = warp >> 2;
-    const int half = N / 2;
+    const int q = warp & 3, hf = warp >> 2, half = N / 2;
     for (int m = 0; m < mt; ++m) {
-        const int row = 128 * m + 32 * q + lane;
-        for (int c0 = hf * half; c0 < (hf + 1) * half; c0 += 16) {
-            float v[16];
+        const int jb = 128 * m + 32 * q;
+        if (jb >= rows) continue;  // the same for the whole warp
+        for (int c0 = hf * half; c0 < (hf + 1) * half; c0 += 32) {
+            float v[32];
             tmem_ld_n(p.tm + ((uint32_t)(32 * q) << 16) + col + (uint32_t)(m * N + c0), v);
-            if (row < rows) f(row, c0, v);
+            f(jb, c0, v);
         }
     }
 }
 
-// The same over two accumulators of one tile (columns col0 and col1), read together.
+// The same for two accumulators of one tile (columns col0 and col1), read together.
 template <typename F>
-__device__ __forceinline__ void epilogue2(const Pipe& p, uint32_t col0, uint32_t col1, int N, int rows, int warp,
-                                          int lane, F&& f) {
+__device__ __forceinline__ void epi32x2(const Pipe& p, uint32_t col0, uint32_t col1, int N, int rows, int warp,
+                                        F&& f) {
     if (p.failed) return;
-    const int q = warp & 3, hf = warp >> 2;
-    const int half = N / 2;
-    const int row = 32 * q + lane;
-    for (int c0 = hf * half; c0 < (hf + 1) * half; c0 += 16) {
-        float v0[16], v1[16];
+    const int q = warp & 3, hf = warp >> 2, half = N / 2;
+    const int jb = 32 * q;
+    if (jb >= rows) return;
+    for (int c0 = hf * half; c0 < (hf + 1) * half; c0 += 32) {
+        float v0[32], v1[32];
         const uint32_t base = p.tm + ((uint32_t)(32 * q) << 16) + (uint32_t)c0;
         tmem_ld_n(base + col0, base + col1, v0, v1);
-        if (row < rows) f(row, c0, v0, v1);
+        f(jb, c0, v0, v1);
     }
 }
 
-// Per-unit workspace, in floats: Z_l, x_l, delta_l for the hidden layers
-// ([64][h] each), e ([64][d]), two retrieval activation buffers ([64][h]) and
-// the Gamma-masked inner products G ([64][64]).
-__host__ __device__ inline size_t deep_ws_floats(int d, int h, int L) {
-    return (size_t)NTOK * (3 * (size_t)(L - 1) * h + 2 * (size_t)h + d + NTOK);
+// A 32 x 32 block held one row per lane (v) as one column per lane (u, u[r]
+// = row r of the block at column `lane`), through 32 x 33 floats of this
+// warp's shared memory (conflict-free both ways).
+__device__ __forceinline__ void transpose32(float* buf, const float (&v)[32], float (&u)[32], int lane) {
+#pragma unroll
+    for (int c = 0; c < 32; ++c) buf[lane * 33 + c] = v[c];
+    __syncwarp();
+#pragma unroll
+    for (int r = 0; r < 32; ++r) u[r] = buf[r * 33 + lane];
+    __syncwarp();
 }
 
-// Shared-memory bytes of a launch with mt_max M tiles of the hidden width.
-__host__ __device__ inline uint32_t deep_smem_bytes(int mt_max) {
-    return 2 * (uint32_t)mt_max * ATILE + 2 * BSTAGE + NTOK * GSTR * 4 + 9 * NTOK * 4 + 64 + 1024;
+// Block writes of operand tiles.  A 32 x 32 block of a tile (rows r0 ..
+// r0 + 31, r0 a multiple of 32, and the 32 k of one block) is one contiguous
+// 4 KB piece of global memory: the warp that holds it (lane = k - k0, one
+// value per row) writes it into one of three 4 KB buffers of its own in shared
+// memory, in the tile's swizzled layout, and lane 0 sends it with one bulk
+// copy.  A buffer is reused once at most one later copy is still reading it
+// (so two blocks may be open at once).
+__device__ __forceinline__ void st_shared_f32(uint32_t addr, float v) {
+    asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+__device__ __forceinline__ void bulk_s2g(void* dst, uint32_t src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(reinterpret_cast<uint64_t>(dst)),
+                 "r"(src), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_wait_read1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+
+struct Stager {
+    uint32_t base;  // this warp's three 4 KB buffers
+    int cnt;        // blocks begun so far
+};
+
+__device__ __forceinline__ uint32_t blk_begin(Stager& sg, int lane) {
+    const uint32_t buf = sg.base + (uint32_t)(sg.cnt % 3) * 4096u;
+    ++sg.cnt;
+    if (lane == 0) bulk_wait_read1();
+    __syncwarp();
+    return buf;
+}
+// value v of block row i (0..31) at k = k0 + lane
+__device__ __forceinline__ void blk_put(uint32_t buf, int i, float v, int lane) {
+    st_shared_f32(buf + (uint32_t)i * 128u + ((((uint32_t)lane >> 2) ^ ((uint32_t)i & 7u)) << 4) + ((uint32_t)lane & 3u) * 4u,
+                  __uint_as_float(to_tf32(v)));
+}
+__device__ __forceinline__ void blk_end(uint32_t buf, const Tile& t, int r0, int k0, int lane) {
+    fence_proxy_async();
+    __syncwarp();
+    if (lane == 0) {
+        bulk_s2g(t.p + ((size_t)(k0 >> 5) * t.R + r0) * 32, buf, 4096u);
+        bulk_commit();
+    }
+}
+// the whole block from one array: v[i] = row r0 + i at k = k0 + lane
+__device__ __forceinline__ void put_block(Stager& sg, const Tile& t, int r0, int k0, const float (&v)[32], int lane) {
+    const uint32_t buf = blk_begin(sg, lane);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) blk_put(buf, i, v[i], lane);
+    blk_end(buf, t, r0, k0, lane);
 }
 
 template <typename Tout>
 __global__ void __launch_bounds__(NT, 1)
-    tc_deep_kernel(nm_args a, int d, int hd, int L, int chunk, int c_mode, int mt_max) {
+    tc_deep_kernel(nm_args a, int d, int hd, int L, int chunk, int c_mode, int mt_max, int nstages) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const uint32_t astage = (uint32_t)mt_max * ATILE;
-    float* sG = reinterpret_cast<float*>(sm + 2 * astage + 2 * BSTAGE);  // Gamma [t][i], row stride GSTR
+    const uint32_t stage_bytes = deep_stage_bytes(mt_max);
+    // this warp's 32 x 33 transpose buffer and three 4 KB block buffers, in the
+    // operand stages (idle while the epilogues run; 132 KB of the at least 160 KB)
+    float* tbuf = reinterpret_cast<float*>(sm) + warp * 32 * 33;
+    Stager sg;
+    sg.base = smem_u32(sm) + EPI_TBUF_BYTES + (uint32_t)warp * 3u * 4096u;
+    sg.cnt = 0;
+    float* sG = reinterpret_cast<float*>(sm + (size_t)nstages * stage_bytes);  // Gamma [t][i], row stride GSTR
     float* ga = sG + NTOK * GSTR;  // 1 - alpha_t
     float* ge = ga + NTOK;         // eta_t
     float* gb = ge + NTOK;         // beta_t
@@ -303,28 +439,35 @@ __global__ void __launch_bounds__(NT, 1)
     float* sSg = sB + NTOK;        // sigma_t
     float* gl = sSg + NTOK;        // gamma_i = Gamma_{n-1,i}
     float* ub = gl + NTOK;         // u_i = u_{n-1,i}
-    uint64_t* bars = reinterpret_cast<uint64_t*>(ub + NTOK);
-    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 2);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(ub + NTOK);  // full[4], empty[4], done
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 2 * MAX_STAGES + 1);
+    int* s_fail = reinterpret_cast<int*>(s_tmem + 1);
 
     const long long unit = blockIdx.x;
     const long long T = a.T;
     const int h = hd;
     const long long P = 2LL * h * d + (long long)(L - 2) * h * h;
     const int b = chunk;
-    const size_t th = (size_t)NTOK * h;
-
-    float* ws = reinterpret_cast<float*>(a.scratch) + (size_t)unit * deep_ws_floats(d, h, L);
-    float* Zw = ws;                       // [L-1][64][h]
-    float* Xw = Zw + (L - 1) * th;        // [L-1][64][h]
-    float* Dw = Xw + (L - 1) * th;        // [L-1][64][h]
-    float* Ew = Dw + (L - 1) * th;        // [64][d]
-    float* Rw = Ew + (size_t)NTOK * d;    // [2][64][h]
-    float* Gw = Rw + 2 * th;              // [64][64]
-    auto Z = [&](int l) { return Zw + (size_t)(l - 1) * th; };
-    auto X = [&](int l) { return Xw + (size_t)(l - 1) * th; };
-    auto Dl = [&](int l) { return l == L ? Ew : Dw + (size_t)(l - 1) * th; };
-    auto woff = [&](int l) { return l == 1 ? 0LL : (long long)h * d + (long long)(l - 2) * h * h; };
+    const Layout lo = deep_layout(d, h, L);
+    float* ws = reinterpret_cast<float*>(a.scratch) + (size_t)unit * lo.total;
     auto dim = [&](int l) { return (l == 0 || l == L) ? d : h; };  // width of x_l (x_L: the output)
+    auto woff = [&](int l) { return l == 1 ? 0LL : (long long)h * d + (long long)(l - 2) * h * h; };
+    auto TW = [&](int l) { return Tile{ws + lo.tw[l], dim(l)}; };      // W_l [o][i]
+    auto TS = [&](int l) { return Tile{ws + lo.ts[l], dim(l)}; };      // S_l [o][i]
+    auto TWt = [&](int l) { return Tile{ws + lo.twt[l], dim(l - 1)}; };  // W_l [i][o], l >= 2
+    const Tile TK{ws + lo.tk, NTOK}, TKt{ws + lo.tkt, d};               // k [t][x], [x][t]
+    const Tile TQ{ws + lo.tq, NTOK}, TQa{ws + lo.tqa, NTOK}, TQs{ws + lo.tqs, NTOK};  // q, A_t q, -sigma_t q
+    auto TX = [&](int l) { return Tile{ws + lo.tx[l], NTOK}; };   // x_l [t][j]
+    auto TXt = [&](int l) { return Tile{ws + lo.txt[l], h}; };    // x_l [j][t]
+    auto Zp = [&](int l) { return ws + lo.z[l]; };                 // z_l [t][j], fp32
+    auto TR = [&](int l) { return Tile{ws + lo.tr[l], NTOK}; };   // r_l [t][j], times A_t, times -sigma_t
+    auto TRa = [&](int l) { return Tile{ws + lo.tra[l], NTOK}; };
+    auto TRs = [&](int l) { return Tile{ws + lo.trs[l], NTOK}; };
+    auto TD = [&](int l) { return Tile{ws + lo.td[l], NTOK}; };   // delta_l [t][j]
+    auto TDt = [&](int l) { return Tile{ws + lo.tdt[l], dim(l)}; };  // delta_l [j][t], times gamma_t, times u_t
+    auto TDg = [&](int l) { return Tile{ws + lo.tdg[l], dim(l)}; };
+    auto TDu = [&](int l) { return Tile{ws + lo.tdu[l], dim(l)}; };
+    const Tile TG{ws + lo.tg, NTOK};  // -Gamma_{t,i} (r_t . x_i) [t][i]
 
     const __nv_bfloat16* qp = reinterpret_cast<const __nv_bfloat16*>(a.q) + unit * T * d;
     const __nv_bfloat16* kp = reinterpret_cast<const __nv_bfloat16*>(a.k) + unit * T * d;
@@ -334,51 +477,75 @@ __global__ void __launch_bounds__(NT, 1)
     const float* be = a.beta + unit * T;
     const float* cc = a.c ? a.c + unit * T : nullptr;
     Tout* y = reinterpret_cast<Tout*>(a.y) + unit * T * d;
-    float* Mw = a.M_T + unit * P;  // the state, updated in place chunk by chunk
+    float* Mw = a.M_T + unit * P;  // the fp32 state, updated in place chunk by chunk
     float* Sw = a.S_T + unit * P;
 
     Pipe p;
-    p.bars = bars;
-    p.a_st[0] = smem_u32(sm);
-    p.a_st[1] = smem_u32(sm + astage);
-    p.b_st[0] = smem_u32(sm + 2 * astage);
-    p.b_st[1] = smem_u32(sm + 2 * astage + BSTAGE);
-    p.ph[0] = p.ph[1] = 0;
-    p.pending[0] = p.pending[1] = 0;
+    for (int s = 0; s < MAX_STAGES; ++s) p.st[s] = smem_u32(sm) + (uint32_t)min(s, nstages - 1) * stage_bytes;
+    p.boff = (uint32_t)mt_max * ATILE;
+    p.ns = nstages;
+    p.full = bars;
+    p.empty = bars + MAX_STAGES;
+    p.done = bars + 2 * MAX_STAGES;
+    p.s_fail = s_fail;
+    p.g = 0;
+    p.ndone = 0;
+    p.pend_full = p.pend_empty = 0;
     p.failed = 0;
 
     if (tid == 0) {
-        mbar_init(&bars[0], 1);
-        mbar_init(&bars[1], 1);
+        for (int i = 0; i < 2 * MAX_STAGES + 1; ++i) mbar_init(&bars[i], 1);
+        *s_fail = 0;
         fence_mbar_init();
     }
     if (warp == 0) {
         tmem_alloc(s_tmem, 512);
         tmem_relinquish();
     }
-    if (a.M_T != a.M0)
-        for (long long i = tid; i < P; i += NT) Mw[i] = a.M0[unit * P + i];
-    if (a.S_T != a.S0)
-        for (long long i = tid; i < P; i += NT) Sw[i] = a.S0[unit * P + i];
+    // the state: fp32 copy into M_T / S_T, and its operand tiles
+    for (int l = 1; l <= L; ++l) {
+        const int in = dim(l - 1), out = dim(l);
+        const Tile tw = TW(l), tsl = TS(l), twt = TWt(l);
+        for (int idx = tid; idx < out * in; idx += NT) {
+            const int j = idx / in, x = idx - j * in;
+            const long long e = woff(l) + idx;
+            const float w = a.M0[unit * P + e], sv = a.S0[unit * P + e];
+            if (a.M_T != a.M0) Mw[e] = w;
+            if (a.S_T != a.S0) Sw[e] = sv;
+            tw.p[toff(out, j, x)] = __uint_as_float(to_tf32(w));
+            tsl.p[toff(out, j, x)] = __uint_as_float(to_tf32(sv));
+            if (l >= 2) twt.p[toff(in, x, j)] = __uint_as_float(to_tf32(w));
+        }
+    }
+    fence_proxy_async_global();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     p.tm = *s_tmem;
 
-    // ends an epilogue: its TMEM reads and workspace writes are done before
-    // the next products are staged and issued
+    // ends an epilogue: its TMEM reads are done, its tile writes visible to the
+    // bulk copies of the next products, and its use of the stages (the
+    // transposes) ordered before those copies land there
     auto handoff = [&]() {
+        if (lane == 0) bulk_wait_all();  // this warp's block copies have landed
+        fence_proxy_async_global();
+        fence_proxy_async();
         tc_fence_before();
         __syncthreads();
     };
 
     for (long long t0 = 0; t0 < T && !p.failed; t0 += b) {
         const int n = (int)min((long long)b, T - t0);
-        if (tid < n) {
-            ga[tid] = 1.0f - al[t0 + tid];
-            ge[tid] = et[t0 + tid];
-            gb[tid] = be[t0 + tid];
-            gc[tid] = momentum_c(c_mode, be[t0 + tid], cc, t0 + tid);
+        if (tid < NTOK) {
+            const bool in_chunk = tid < n;
+            ga[tid] = in_chunk ? 1.0f - al[t0 + tid] : 0.0f;
+            ge[tid] = in_chunk ? et[t0 + tid] : 0.0f;
+            gb[tid] = in_chunk ? be[t0 + tid] : 0.0f;
+            gc[tid] = in_chunk ? momentum_c(c_mode, be[t0 + tid], cc, t0 + tid) : 0.0f;
+            gl[tid] = 0.0f;
+            ub[tid] = 0.0f;
+            sA[tid] = 0.0f;
+            sSg[tid] = 0.0f;
         }
         __syncthreads();
         // gate scan: column i of Gamma per thread (division-free recursion), A, B, sigma by one thread
@@ -406,70 +573,104 @@ __global__ void __launch_bounds__(NT, 1)
             }
         }
         __syncthreads();
-        const __nv_bfloat16* kc = kp + t0 * d;  // this chunk's keys [t][x]
+        const __nv_bfloat16* kc = kp + t0 * d;  // this chunk's keys and queries [t][x]
         const __nv_bfloat16* qc = qp + t0 * d;
+        // their operand tiles (zero past the chunk's end)
+        for (int idx = tid; idx < NTOK * d; idx += NT) {
+            const int t = idx / d, x = idx - t * d;
+            const bool in_chunk = t < n;
+            const float kv = in_chunk ? __bfloat162float(kc[(size_t)t * d + x]) : 0.0f;
+            const float qv = in_chunk ? __bfloat162float(qc[(size_t)t * d + x]) : 0.0f;
+            TK.p[toff(NTOK, t, x)] = kv;  // bf16 values are exact in tf32
+            TKt.p[toff(d, x, t)] = kv;
+            TQ.p[toff(NTOK, t, x)] = qv;
+            TQa.p[toff(NTOK, t, x)] = __uint_as_float(to_tf32(sA[t] * qv));
+            TQs.p[toff(NTOK, t, x)] = __uint_as_float(to_tf32(-sSg[t] * qv));
+        }
+        handoff();
 
         // keys' forward at the chunk-start weights: z_l = W_l x_{l-1}, x_l = silu(z_l)
         for (int l = 1; l < L; ++l) {
             const int in = dim(l - 1);
-            Seg s[1];
-            s[0].a = src(Mw + woff(l), in, 1, h, in);
-            s[0].b = l == 1 ? src(kc, d, 1, n, in, 1) : src(X(l - 1), h, 1, n, in);
-            s[0].K = in; s[0].col = 0; s[0].fresh = 1;
             const int mt = (h + 127) / 128;
+            Seg s[1] = {seg(TW(l), 0, l == 1 ? TK : TX(l - 1), 0, in, 0, 1)};
             gemm(p, s, 1, mt, NTOK, tid);
-            float* z = Z(l);
-            float* x = X(l);
-            epilogue(p, 0, mt, NTOK, h, warp, lane, [&](int j, int c0, const float* v) {
+            float* z = Zp(l);
+            const Tile tx = TX(l), txt = TXt(l);
+            epi32(p, 0, mt, NTOK, h, warp, [&](int jb, int tb, const float (&v)[32]) {
+                float xv[32], xu[32];
 #pragma unroll
-                for (int c = 0; c < 16; ++c) {
-                    const int t = c0 + c;
-                    if (t < n) {
-                        z[(size_t)t * h + j] = v[c];
-                        x[(size_t)t * h + j] = silu_e(v[c]);
-                    }
+                for (int c = 0; c < 32; ++c) {  // lane = feature j = jb + lane, c = token tb + c
+                    const int t = tb + c;
+                    xv[c] = t < n ? silu_e(v[c]) : 0.0f;
+                    if (t < n) z[(size_t)t * h + jb + lane] = v[c];
                 }
+                put_block(sg, tx, tb, jb, xv, lane);  // x_l [t][j]
+                transpose32(tbuf, xv, xu, lane);
+                put_block(sg, txt, jb, tb, xu, lane);  // x_l [j][t]
             });
             handoff();
         }
-        // e = 2 (W_L x_{L-1} - v), clipped for the Huber loss
+        // e = 2 (W_L x_{L-1} - v), clipped for the Huber loss: delta_L
         {
-            Seg s[1];
-            s[0].a = src(Mw + woff(L), h, 1, d, h);
-            s[0].b = src(X(L - 1), h, 1, n, h);
-            s[0].K = h; s[0].col = 0; s[0].fresh = 1;
+            Seg s[1] = {seg(TW(L), 0, TX(L - 1), 0, h, 0, 1)};
             gemm(p, s, 1, 1, NTOK, tid);
             const __nv_bfloat16* vc = vp + t0 * d;
-            epilogue(p, 0, 1, NTOK, d, warp, lane, [&](int o, int c0, const float* v) {
+            const Tile td = TD(L), tdt = TDt(L), tdg = TDg(L), tdu = TDu(L);
+            epi32(p, 0, 1, NTOK, d, warp, [&](int ob, int tb, const float (&v)[32]) {
+                float e[32], eu_[32];
+                const int o = ob + lane;
 #pragma unroll
-                for (int c = 0; c < 16; ++c) {
-                    const int t = c0 + c;
-                    if (t < n) Ew[(size_t)t * d + o] = nm_clip_err(2.0f * (v[c] - __bfloat162float(vc[(size_t)t * d + o])), a.e_clip);
+                for (int c = 0; c < 32; ++c) {
+                    const int t = tb + c;
+                    e[c] = t < n ? nm_clip_err(2.0f * (v[c] - __bfloat162float(vc[(size_t)t * d + o])), a.e_clip) : 0.0f;
                 }
+                put_block(sg, td, tb, ob, e, lane);  // e [t][o]
+                transpose32(tbuf, e, eu_, lane);      // eu_[r] = e of output ob + r at token tb + lane
+                put_block(sg, tdt, ob, tb, eu_, lane);
+                const float g = gl[tb + lane], u = ub[tb + lane];
+                float sc[32];
+#pragma unroll
+                for (int r = 0; r < 32; ++r) sc[r] = eu_[r] * g;
+                put_block(sg, tdg, ob, tb, sc, lane);
+#pragma unroll
+                for (int r = 0; r < 32; ++r) sc[r] = eu_[r] * u;
+                put_block(sg, tdu, ob, tb, sc, lane);
             });
             handoff();
         }
         // backward: delta_l = (W_{l+1}^T delta_{l+1}) (.) silu'(z_l)
         for (int l = L - 1; l >= 1; --l) {
             const int up = dim(l + 1);
-            Seg s[1];
-            s[0].a = src(Mw + woff(l + 1), 1, h, h, up);  // (j, o) -> W_{l+1}[o][j]
-            s[0].b = src(Dl(l + 1), up, 1, n, up);
-            s[0].K = up; s[0].col = 0; s[0].fresh = 1;
             const int mt = (h + 127) / 128;
+            Seg s[1] = {seg(TWt(l + 1), 0, TD(l + 1), 0, up, 0, 1)};
             gemm(p, s, 1, mt, NTOK, tid);
-            const float* z = Z(l);
-            float* dl = Dl(l);
-            epilogue(p, 0, mt, NTOK, h, warp, lane, [&](int j, int c0, const float* v) {
+            const float* z = Zp(l);
+            const Tile td = TD(l), tdt = TDt(l), tdg = TDg(l), tdu = TDu(l);
+            epi32(p, 0, mt, NTOK, h, warp, [&](int jb, int tb, const float (&v)[32]) {
+                float dl[32], du_[32];
+                const int j = jb + lane;
 #pragma unroll
-                for (int c = 0; c < 16; ++c) {
-                    const int t = c0 + c;
-                    if (t < n) dl[(size_t)t * h + j] = v[c] * dsilu_e(z[(size_t)t * h + j]);
+                for (int c = 0; c < 32; ++c) {
+                    const int t = tb + c;
+                    dl[c] = t < n ? v[c] * dsilu_e(z[(size_t)t * h + j]) : 0.0f;
                 }
+                put_block(sg, td, tb, jb, dl, lane);  // delta_l [t][j]
+                transpose32(tbuf, dl, du_, lane);
+                put_block(sg, tdt, jb, tb, du_, lane);
+                const float g = gl[tb + lane], u = ub[tb + lane];
+                float sc[32];
+#pragma unroll
+                for (int r = 0; r < 32; ++r) sc[r] = du_[r] * g;
+                put_block(sg, tdg, jb, tb, sc, lane);
+#pragma unroll
+                for (int r = 0; r < 32; ++r) sc[r] = du_[r] * u;
+                put_block(sg, tdu, jb, tb, sc, lane);
             });
             handoff();
         }
-        // surprise_t = sqrt(sum_l ||delta_{l,t}||^2 ||x_{l-1,t}||^2): one warp per token
+        // surprise_t = sqrt(sum_l ||delta_{l,t}||^2 ||x_{l-1,t}||^2): one warp per token, from the
+        // [t][.] tiles (the order of a row's values inside a block does not matter to a sum)
         if (a.surprise && !p.failed) {
             for (int t = warp; t < n; t += NT / 32) {
                 float tot = 0.f;
@@ -477,11 +678,15 @@ __global__ void __launch_bounds__(NT, 1)
                     const int in = dim(l - 1), out = dim(l);
                     float x2 = 0.f, d2 = 0.f;
                     for (int x = lane; x < in; x += 32) {
-                        const float xv = l == 1 ? __bfloat162float(kc[(size_t)t * d + x]) : X(l - 1)[(size_t)t * h + x];
+                        const float xv = l == 1 ? __bfloat162float(kc[(size_t)t * d + x])
+                                                : TX(l - 1).p[(size_t)(x >> 5) * NTOK * 32 + (size_t)t * 32 + (x & 31)];
                         x2 = fmaf(xv, xv, x2);
                     }
-                    const float* dl = Dl(l);
-                    for (int o = lane; o < out; o += 32) d2 = fmaf(dl[(size_t)t * out + o], dl[(size_t)t * out + o], d2);
+                    const float* dl = TD(l).p;
+                    for (int o = lane; o < out; o += 32) {
+                        const float dv = dl[(size_t)(o >> 5) * NTOK * 32 + (size_t)t * 32 + (o & 31)];
+                        d2 = fmaf(dv, dv, d2);
+                    }
 #pragma unroll
                     for (int sh = 16; sh > 0; sh >>= 1) {
                         x2 += __shfl_xor_sync(0xffffffffu, x2, sh);
@@ -492,52 +697,53 @@ __global__ void __launch_bounds__(NT, 1)
                 if (lane == 0) a.surprise[unit * T + t0 + t] = sqrtf(tot);
             }
         }
-        // retrieval, layer by layer
+        // retrieval, layer by layer (r_0 = q)
         for (int l = 1; l <= L && !p.failed; ++l) {
             const int in = dim(l - 1), out = dim(l);
-            const void* xin = l == 1 ? (const void*)kc : (const void*)X(l - 1);
-            const void* rin = l == 1 ? (const void*)qc : (const void*)(Rw + (size_t)((l - 1) & 1) * th);
-            const long long xs = l == 1 ? d : h;
-            const int bf = l == 1 ? 1 : 0;
-            // G[t][i] = Gamma_{t,i} (r_t . x_{l-1,i}) for i <= t, from P^T[i][t] = x_{l-1,i} . r_t
+            const Tile xin = l == 1 ? TK : TX(l - 1);
+            // -G[t][i] = -Gamma_{t,i} (r_t . x_{l-1,i}) for i <= t, from P^T[i][t] = x_{l-1,i} . r_t
             {
-                Seg s[1];
-                s[0].a = src(xin, xs, 1, n, in, bf);
-                s[0].b = src(rin, xs, 1, n, in, bf);
-                s[0].K = in; s[0].col = 0; s[0].fresh = 1;
+                Seg s[1] = {seg(xin, 0, l == 1 ? TQ : TR(l - 1), 0, in, 0, 1)};
                 gemm(p, s, 1, 1, NTOK, tid);
-                epilogue(p, 0, 1, NTOK, n, warp, lane, [&](int i, int c0, const float* v) {
+                epi32(p, 0, 1, NTOK, NTOK, warp, [&](int ib, int tb, const float (&v)[32]) {
+                    float g[32];
+                    const int i = ib + lane;
 #pragma unroll
-                    for (int c = 0; c < 16; ++c) {
-                        const int t = c0 + c;
-                        Gw[t * NTOK + i] = (i <= t && t < n) ? sG[t * GSTR + i] * v[c] : 0.0f;
+                    for (int c = 0; c < 32; ++c) {
+                        const int t = tb + c;
+                        g[c] = (i <= t && t < n) ? -sG[t * GSTR + i] * v[c] : 0.0f;
                     }
+                    put_block(sg, TG, tb, ib, g, lane);  // -G [t][i]
                 });
                 handoff();
             }
-            // pre_l^T[j][t] = A_t (W_l r_t)_j - sigma_t (S_l r_t)_j - sum_i delta_{l,i,j} G[t][i], one accumulator
+            // pre_l^T[j][t] = (W_l (A_t r_t))_j + (S_l (-sigma_t r_t))_j + sum_i delta_{l,i,j} (-G[t][i])
             {
                 const int mt = (out + 127) / 128;
-                Seg s[3];
-                s[0].a = src(Mw + woff(l), in, 1, out, in);
-                s[0].b = src(rin, xs, 1, n, in, bf, sA);
-                s[0].K = in; s[0].col = 0; s[0].fresh = 1;
-                s[1].a = src(Sw + woff(l), in, 1, out, in);
-                s[1].b = src(rin, xs, 1, n, in, bf, sSg, nullptr, -1.0f);
-                s[1].K = in; s[1].col = 0; s[1].fresh = 0;
-                s[2].a = src(Dl(l), 1, out, out, n);  // (j, i) -> delta_l[i][j]
-                s[2].b = src(Gw, NTOK, 1, n, n, 0, nullptr, nullptr, -1.0f);
-                s[2].K = NTOK; s[2].col = 0; s[2].fresh = 0;
+                Seg s[3] = {seg(TW(l), 0, l == 1 ? TQa : TRa(l - 1), 0, in, 0, 1),
+                            seg(TS(l), 0, l == 1 ? TQs : TRs(l - 1), 0, in, 0, 0),
+                            seg(TDt(l), 0, TG, 0, NTOK, 0, 0)};
                 gemm(p, s, 3, mt, NTOK, tid);
-                float* rn = Rw + (size_t)(l & 1) * th;
-                epilogue(p, 0, mt, NTOK, out, warp, lane, [&](int j, int c0, const float* v) {
+                const Tile tr = l < L ? TR(l) : TK, tra = l < L ? TRa(l) : TK, trs = l < L ? TRs(l) : TK;
+                epi32(p, 0, mt, NTOK, out, warp, [&](int jb, int tb, const float (&v)[32]) {
+                    const int j = jb + lane;
+                    if (l < L) {
+                        float r[32];
 #pragma unroll
-                    for (int c = 0; c < 16; ++c) {
-                        const int t = c0 + c;
-                        if (t < n) {
-                            if (l < L) {
-                                rn[(size_t)t * h + j] = silu_e(v[c]);
-                            } else {
+                        for (int c = 0; c < 32; ++c) r[c] = tb + c < n ? silu_e(v[c]) : 0.0f;
+                        put_block(sg, tr, tb, jb, r, lane);  // r_l [t][j]
+                        float sc[32];
+#pragma unroll
+                        for (int c = 0; c < 32; ++c) sc[c] = r[c] * sA[tb + c];
+                        put_block(sg, tra, tb, jb, sc, lane);
+#pragma unroll
+                        for (int c = 0; c < 32; ++c) sc[c] = -r[c] * sSg[tb + c];
+                        put_block(sg, trs, tb, jb, sc, lane);
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < 32; ++c) {
+                            const int t = tb + c;
+                            if (t < n) {
                                 Tout* yp = y + (t0 + t) * d + j;
                                 const float o = nm_gated(a, yp, v[c]);
                                 if constexpr (sizeof(Tout) == 2) *yp = __float2bfloat16_rn(o);
@@ -550,46 +756,59 @@ __global__ void __launch_bounds__(NT, 1)
             }
         }
         // chunk-end state, layer by layer, in tiles of 128 rows x up to 256 columns:
-        // W_l <- A_n W_l - sigma_n S_l - sum_i gamma_i delta_{l,i} x_{l-1,i}^T, S_l <- B_n S_l + sum_i u_i (same)
+        // W_l <- A_n W_l - sigma_n S_l - sum_i gamma_i delta_{l,i} x_{l-1,i}^T, S_l <- B_n S_l + sum_i u_i (same),
+        // written as fp32 and as the next chunk's operand tiles
         const float An = sA[n - 1], Bn = sB[n - 1], sn = sSg[n - 1];
         for (int l = 1; l <= L && !p.failed; ++l) {
             const int in = dim(l - 1), out = dim(l);
-            const void* xin = l == 1 ? (const void*)kc : (const void*)X(l - 1);
-            const long long xs = l == 1 ? d : h;
-            const int bf = l == 1 ? 1 : 0;
             float* Wl = Mw + woff(l);
             float* Sl = Sw + woff(l);
+            const Tile tw = TW(l), tsl = TS(l), twt = TWt(l);
+            const Tile xt = l == 1 ? TKt : TXt(l - 1);
             for (int m0 = 0; m0 < out; m0 += 128) {
                 for (int x0 = 0; x0 < in; x0 += 256) {
                     const int N = min(256, in - x0);
-                    Seg s[2];
-                    s[0].a = src(Dl(l) + m0, 1, out, out - m0, n, 0, nullptr, gl);  // (j, i) -> gamma_i delta_l[i][m0 + j]
-                    s[0].b = l == 1 ? src(kc + x0, 1, xs, N, n, bf) : src(X(l - 1) + x0, 1, xs, N, n, bf);
-                    s[0].K = NTOK; s[0].col = 0; s[0].fresh = 1;
-                    s[1].a = src(Dl(l) + m0, 1, out, out - m0, n, 0, nullptr, ub);
-                    s[1].b = s[0].b;
-                    s[1].K = NTOK; s[1].col = 256; s[1].fresh = 1;
-                    (void)xin;
+                    Seg s[2] = {seg(TDg(l), m0, xt, x0, NTOK, 0, 1), seg(TDu(l), m0, xt, x0, NTOK, 256, 1)};
                     gemm(p, s, 2, 1, N, tid);
-                    epilogue2(p, 0, 256, N, out - m0, warp, lane, [&](int j, int c0, const float* gw, const float* gs) {
-                        float* wr = Wl + (size_t)(m0 + j) * in + x0 + c0;
-                        float* sr = Sl + (size_t)(m0 + j) * in + x0 + c0;
+                    epi32x2(p, 0, 256, N, out - m0, warp, [&](int jb, int cb, const float (&gw)[32], const float (&gs)[32]) {
+                        // column-mapped: lane = input x = x0 + cb + lane, r = output row m0 + jb + r
+                        float gwu[32], gsu[32];
+                        transpose32(tbuf, gw, gwu, lane);
+                        transpose32(tbuf, gs, gsu, lane);
+                        const int x = x0 + cb + lane, rb = m0 + jb;
+                        const uint32_t bw = blk_begin(sg, lane), bs = blk_begin(sg, lane);
 #pragma unroll
-                        for (int c = 0; c < 16; c += 4) {
-                            const float4 w = *reinterpret_cast<const float4*>(wr + c);
-                            const float4 sv = *reinterpret_cast<const float4*>(sr + c);
-                            float4 wn, sn4;
-                            wn.x = An * w.x - sn * sv.x - gw[c];
-                            wn.y = An * w.y - sn * sv.y - gw[c + 1];
-                            wn.z = An * w.z - sn * sv.z - gw[c + 2];
-                            wn.w = An * w.w - sn * sv.w - gw[c + 3];
-                            sn4.x = Bn * sv.x + gs[c];
-                            sn4.y = Bn * sv.y + gs[c + 1];
-                            sn4.z = Bn * sv.z + gs[c + 2];
-                            sn4.w = Bn * sv.w + gs[c + 3];
-                            *reinterpret_cast<float4*>(wr + c) = wn;
-                            *reinterpret_cast<float4*>(sr + c) = sn4;
+                        for (int r0 = 0; r0 < 32; r0 += 16) {  // the loads of 16 rows issued before any store
+                            float w[16], sv[16];
+#pragma unroll
+                            for (int r = 0; r < 16; ++r) {
+                                const size_t e = (size_t)(rb + r0 + r) * in + x;
+                                w[r] = Wl[e];
+                                sv[r] = Sl[e];
+                            }
+#pragma unroll
+                            for (int r = 0; r < 16; ++r) {
+                                const size_t e = (size_t)(rb + r0 + r) * in + x;
+                                const float wnew = An * w[r] - sn * sv[r] - gwu[r0 + r];
+                                const float snew = Bn * sv[r] + gsu[r0 + r];
+                                Wl[e] = wnew;
+                                Sl[e] = snew;
+                                blk_put(bw, r0 + r, wnew, lane);
+                                blk_put(bs, r0 + r, snew, lane);
+                                tbuf[(r0 + r) * 33 + lane] = wnew;
+                            }
                         }
+                        blk_end(bw, tw, rb, x0 + cb, lane);  // W_l, S_l [o][i]
+                        blk_end(bs, tsl, rb, x0 + cb, lane);
+                        if (l >= 2) {  // W_l [x][o]: back to one row per lane, then one 128-byte row per store
+                            __syncwarp();
+                            float wv[32];
+#pragma unroll
+                            for (int c = 0; c < 32; ++c) wv[c] = tbuf[lane * 33 + c];
+                            __syncwarp();
+                            put_block(sg, twt, x0 + cb, rb, wv, lane);
+                        }
+                        __syncwarp();
                     });
                     handoff();
                 }
@@ -597,10 +816,16 @@ __global__ void __launch_bounds__(NT, 1)
         }
     }
     if (p.failed) {
-        if (tid == 0 && a.status) atomicExch(a.status, NM_ERR_DEVICE_TIMEOUT);
-        // let products still in flight land before the CTA leaves
-        for (int st = 0; st < 2; ++st)
-            if (p.pending[st]) mbar_wait(&bars[st], p.ph[st] & 1u, WAIT_NS);
+        if (tid == 0) {
+            if (a.status) atomicExch(a.status, NM_ERR_DEVICE_TIMEOUT);
+            // let copies and products still in flight land before the CTA leaves
+            for (int st = 0; st < nstages; ++st) {
+                const uint32_t uses = (p.g + (uint32_t)nstages - 1u - (uint32_t)st) / (uint32_t)nstages;
+                if (uses == 0) continue;
+                if (p.pend_full >> st & 1u) mbar_wait(&bars[st], (uses - 1u) & 1u, WAIT_NS);
+                if (p.pend_empty >> st & 1u) mbar_wait(&bars[MAX_STAGES + st], (uses - 1u) & 1u, WAIT_NS);
+            }
+        }
     }
     tc_fence_before();
     __syncthreads();
@@ -610,24 +835,25 @@ __global__ void __launch_bounds__(NT, 1)
 template <typename Tout>
 cudaError_t launch(const nm_config& c, const nm_args& a, cudaStream_t s) {
     const int mt_max = (c.hidden + 127) / 128;
-    const uint32_t smem = deep_smem_bytes(mt_max);
+    const int ns = deep_stages(mt_max);
+    const uint32_t smem = deep_smem_bytes(mt_max, ns);
     auto kern = tc_deep_kernel<Tout>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     kern<<<(unsigned)((long long)a.B * a.H), NT, smem, s>>>(a, c.d, c.hidden, nm_layers(c), c.chunk, c.c_mode,
-                                                            mt_max);
+                                                            mt_max, ns);
     return cudaGetLastError();
 }
 
 }  // namespace
 
 bool nm_tc_deep_supports(const nm_config& c) {
-    return c.kind == NM_MLP2 && nm_layers(c) > 2 && c.in_dtype == NM_BF16 && (c.d == 32 || c.d == 64 || c.d == 128) &&
-           c.hidden >= 32 && c.hidden <= 512 && c.hidden % 32 == 0 && c.chunk >= 1 && c.chunk <= NTOK;
+    return c.kind == NM_MLP2 && nm_layers(c) > 2 && c.in_dtype == NM_BF16 && (c.d == 64 || c.d == 128) &&
+           c.hidden >= 64 && c.hidden <= 512 && c.hidden % 64 == 0 && c.chunk >= 1 && c.chunk <= NTOK;
 }
 
 size_t nm_tc_deep_scratch_bytes(const nm_config& c, int B, int H) {
-    return sizeof(float) * deep_ws_floats(c.d, c.hidden, nm_layers(c)) * (size_t)B * (size_t)H;
+    return sizeof(float) * deep_layout(c.d, c.hidden, nm_layers(c)).total * (size_t)B * (size_t)H;
 }
 
 cudaError_t nm_tc_deep_launch(const nm_config& c, const nm_args& a, cudaStream_t s) {

@@ -614,13 +614,15 @@ def _deep_state(d, hidden, layers, seed, scale=0.5):
     (3, 128, 256, 130, 64, torch.bfloat16, None),
     (3, 64, 512, 70, 64, torch.bfloat16, 0.5),
     (3, 128, 384, 65, 32, torch.bfloat16, None),
+    (3, 128, 128, 90, 64, torch.bfloat16, 0.5),
 ])
 @pytest.mark.parametrize("path", PATHS)
 def test_deep_memory(layers, d, hidden, T, chunk, dtype, delta, path):
     """L >= 3 layers on both kernel families: the tf32 tensor-core kernel
-    takes bf16 inputs (hidden widths of one to four 128-row tiles, state
-    updates in column blocks of 256), the fp32 FFMA kernel both input types;
-    y, the state and the surprise against the oracle."""
+    takes bf16 inputs with d = 64 or 128 and hidden widths that are
+    multiples of 64 (one to four 128-row tiles, state updates in column
+    blocks of 256), the fp32 FFMA kernel every shape here; y, the state and
+    the surprise against the oracle."""
     wl = dataclasses.replace(W.WORKLOADS[1], d=d, hidden=hidden, chunk=chunk, dtype=dtype).with_sizes(B=1, H=2, T=T)
     x = W.make_inputs(wl, "cuda", seed=150 + layers + T)
     x["eta"] *= 0.5
@@ -630,8 +632,8 @@ def test_deep_memory(layers, d, hidden, T, chunk, dtype, delta, path):
     S0 = torch.stack(s0).reshape(1, 2, P).contiguous()
     loss = nm.LOSS_L2 if delta is None else nm.LOSS_HUBER
     kw = dict(in_dtype=dtype, layers=layers, loss=loss, huber_delta=0.0 if delta is None else delta)
-    if path == nm.PATH_TC and dtype == torch.float32:
-        # the tensor-core kernel takes bf16 inputs only
+    tc_ok = dtype == torch.bfloat16 and d in (64, 128) and hidden % 64 == 0
+    if path == nm.PATH_TC and not tc_ok:
         with pytest.raises(nm.NMError) as ei:
             nm.NeuralMemory(nm.MLP2, d, hidden, chunk, path=path, **kw)
         assert ei.value.status == nm.NM_ERR_UNSUPPORTED
@@ -641,7 +643,7 @@ def test_deep_memory(layers, d, hidden, T, chunk, dtype, delta, path):
     mem = nm.NeuralMemory(nm.MLP2, d, hidden, chunk, path=path, **kw)
     assert mem.path == path
     auto = nm.NeuralMemory(nm.MLP2, d, hidden, chunk, **kw)
-    assert auto.path == (nm.PATH_TC if dtype == torch.bfloat16 and d >= 32 else nm.PATH_SIMT)
+    assert auto.path == (nm.PATH_TC if tc_ok else nm.PATH_SIMT)
     auto.close()
     y, MT, ST, sur = mem.forward_surprise(x["q"], x["k"], x["v"], x["alpha"], x["eta"], x["beta"], M0, S0)
     assert mem.synchronize() == nm.NM_OK
