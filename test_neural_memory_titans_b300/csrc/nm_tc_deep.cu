@@ -65,8 +65,8 @@ constexpr int NT = 256;            // threads per CTA
 constexpr int NTOK = 64;           // token rows of a chunk tile (chunks of at most 64 tokens)
 constexpr int GSTR = NTOK + 1;     // padded row stride of Gamma in shared memory
 constexpr uint32_t ATILE = 128 * 128;   // one M = 128 tile of 32 fp32 k: 16 KB
-constexpr uint32_t BSTAGE = 256 * 128;  // up to 256 B rows of 32 fp32 k: 32 KB
-constexpr int MAX_STAGES = 4;
+constexpr uint32_t STAGE_AREA = 196608; // operand stages: 192 KB, cut per GEMM into stages of its block size
+constexpr int MAX_STAGES = 8;
 constexpr uint32_t EPI_TBUF_BYTES = 36864;                          // 8 warps x 32 x 33 floats, rounded up
 constexpr uint32_t EPI_BYTES = EPI_TBUF_BYTES + (NT / 32) * 3 * 4096;  // + three 4 KB block buffers per warp
 constexpr uint64_t WAIT_NS = 2000000000ull;  // 2 s
@@ -98,9 +98,11 @@ __device__ __forceinline__ uint32_t to_tf32(float x) {
     return r;
 }
 
-__device__ __forceinline__ float silu_e(float z) { return z / (1.0f + expf(-z)); }
+// silu and its derivative with the hardware-tanh sigmoid (relative error about
+// 2^-11, the size of the tf32 rounding every result goes through next).
+__device__ __forceinline__ float silu_e(float z) { return z * sigmoid_f(z); }
 __device__ __forceinline__ float dsilu_e(float z) {
-    const float s = 1.0f / (1.0f + expf(-z));
+    const float s = sigmoid_f(z);
     return s * (1.0f + z * (1.0f - s));
 }
 
@@ -174,19 +176,12 @@ __host__ __device__ inline Layout deep_layout(int d, int h, int L) {
     return o;
 }
 
-// Shared memory: `ns` stages of (mt_max A tiles + one B block), Gamma, the
-// gate vectors, the mbarriers and flags.
-__host__ __device__ inline uint32_t deep_stage_bytes(int mt_max) { return (uint32_t)mt_max * ATILE + BSTAGE; }
-__host__ __device__ inline uint32_t deep_smem_bytes(int mt_max, int ns) {
-    return (uint32_t)ns * deep_stage_bytes(mt_max) + NTOK * GSTR * 4 + 9 * NTOK * 4 + 256 + 1024;
-}
-__host__ inline int deep_stages(int mt_max) {
-    int ns = MAX_STAGES;
-    while (ns > 2 && deep_smem_bytes(mt_max, ns) > 232448) --ns;
-    return ns;
-}
-// the smallest operand-stage area of any launch is 2 stages of 3 A tiles (hidden 384)
-static_assert(2 * (3 * ATILE + BSTAGE) >= EPI_BYTES, "the epilogues' buffers fit in the operand stages");
+// Shared memory: the operand stages, Gamma, the gate vectors, the mbarriers and flags.
+constexpr uint32_t MISC_BYTES = 4096;  // producer state, segments, workspace layout
+constexpr uint32_t DEEP_SMEM_BYTES = STAGE_AREA + NTOK * GSTR * 4 + 9 * NTOK * 4 + 256 + MISC_BYTES + 1024;
+static_assert(DEEP_SMEM_BYTES <= 232448, "shared memory budget");
+static_assert(STAGE_AREA >= EPI_BYTES, "the epilogues' buffers fit in the operand stages");
+static_assert(STAGE_AREA >= 2 * (4 * ATILE + 256 * 128), "two stages of the largest one-atom block fit");
 
 // ---- the product pipeline: one thread copies operand blocks and issues the MMAs
 
@@ -199,7 +194,7 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
 // Makes this thread's generic-proxy global writes visible to later bulk copies.
 __device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
 
-// One chain of products into one accumulator: K (a multiple of 32) of A
+// One chain of products into one accumulator: K (a multiple of 64) of A
 // (rows a_row0 .. of tile set a, mt tiles of 128 rows) times B (rows
 // b_row0 .. b_row0 + N - 1 of tile set b).  `fresh` starts at zero.
 struct Seg {
@@ -221,83 +216,135 @@ __device__ __forceinline__ Seg seg(const Tile& a, int a_row0, const Tile& b, int
     return s;
 }
 
-struct Pipe {
-    uint32_t st[MAX_STAGES];  // stage base addresses: A tiles, then the B block at + boff
-    uint32_t boff;
-    int ns;
-    uint64_t* full;   // [ns] a stage's copies landed
-    uint64_t* empty;  // [ns] the products that read a stage completed
+// What the producer (thread 0) works from, in shared memory: the stage area,
+// barriers and TMEM base, its barrier bookkeeping (held in registers inside
+// a GEMM) and the segments of the GEMM being run.
+struct Prod {
+    uint32_t area, tm;
+    uint64_t* full;   // [MAX_STAGES] a stage's copies landed
+    uint64_t* empty;  // [MAX_STAGES] the products that read a stage completed
     uint64_t* done;   // all products of a GEMM completed (or the producer gave up)
     int* s_fail;
+    uint32_t fph, eph;               // bit s: parity of the next phase of full[s] / empty[s]
+    uint32_t pend_full, pend_empty;  // bit s: a phase of full[s] / empty[s] not yet waited for
+    Seg segs[3];
+};
+
+struct Pipe {
+    uint32_t area;    // shared address of the operand stages
+    uint64_t* full;   // [MAX_STAGES] a stage's copies landed
+    uint64_t* empty;  // [MAX_STAGES] the products that read a stage completed
+    uint64_t* done;   // all products of a GEMM completed (or the producer gave up)
+    int* s_fail;
+    Prod* prod;       // shared
     uint32_t tm;
-    uint32_t g;       // operand blocks issued so far (thread 0)
     uint32_t ndone;   // GEMMs finished (every thread)
-    uint32_t pend_full, pend_empty;  // bit per stage: a phase issued and not yet waited for (thread 0)
     int failed;
 };
 
-// Thread 0: the copies and products of one GEMM.  Block b of the GEMM goes
-// to stage (g + b) % ns.  The copies of ns - 1 blocks are issued first; after
-// the products of block b are issued, the copies of block b + ns - 1 follow,
-// into the stage that block b - 1's products read (waited for on its empty
-// barrier, while block b's products keep the tensor cores busy).
-__device__ __noinline__ void run_gemm(Pipe& p, const Seg* segs, int nseg, int mt, int N) {
+// Thread 0: the copies and products of one GEMM.  A block is 64 k (two
+// 32-k swizzle atoms; one atom where two such stages would not fit) of A
+// rows (up to mt tiles) and N B rows; the blocks cut
+// the stage area into ns = area / block stages (at most MAX_STAGES) and block
+// b goes to stage b % ns.  The copies of ns - 1 blocks are issued first;
+// after the products of block b are issued, the copies of block b + ns - 1
+// follow, into the stage that block b - 1's products read (waited for on its
+// empty barrier while block b's products keep the tensor cores busy).  Each
+// barrier's phase parity is tracked on its own, so the stage count may change
+// from one GEMM to the next.
+__device__ __noinline__ void run_gemm(Prod* prod, int nseg, int mt, int N) {
+    const uint32_t area = prod->area, tm = prod->tm;
+    uint64_t* const full = prod->full;
+    uint64_t* const empty = prod->empty;
+    uint64_t* const done = prod->done;
+    const Seg* segs = prod->segs;
+    uint32_t fph = prod->fph, eph = prod->eph, pend_full = prod->pend_full, pend_empty = prod->pend_empty;
+    uint32_t amax = 0;
+    for (int s = 0; s < nseg; ++s) amax = max(amax, (uint32_t)min(128 * mt, segs[s].a_R - segs[s].a_row0) * 128u);
+    const uint32_t bb = (uint32_t)N * 128u;  // one 32-k atom of B (a multiple of 1024: N % 8 == 0)
+    const uint32_t na = 2u * 2u * (amax + bb) <= STAGE_AREA ? 2u : 1u;  // atoms per block
+    const int lk = na == 2u ? 6 : 5;         // log2 of the k per block
     int total = 0;
-    for (int s = 0; s < nseg; ++s) total += segs[s].K >> 5;
+    for (int s = 0; s < nseg; ++s) total += segs[s].K >> lk;
+    const uint32_t boff = na * amax;         // amax is a multiple of 1024 (rows % 8 == 0)
+    const uint32_t sbytes = boff + na * bb;
+    const int ns = (int)min((uint32_t)MAX_STAGES, STAGE_AREA / sbytes);
     const uint32_t idesc = idesc_tf32((uint32_t)N);
-    const uint32_t ns = (uint32_t)p.ns;
     bool ok = true;
-    int issued = 0, is = 0, ikb = 0;  // next block to copy: its segment and block within the segment
+    int issued = 0, is = 0, ikb = 0;  // next block to copy: its segment and 64-k block within the segment
     auto issue_next = [&]() {
-        const uint32_t gb = p.g + (uint32_t)issued;
-        const int st = (int)(gb % ns);
-        if (p.pend_empty >> st & 1u) {
-            ok = mbar_wait(&p.empty[st], ((gb / ns) - 1u) & 1u, WAIT_NS);
-            p.pend_empty &= ~(1u << st);
+        const int st = issued % ns;
+        const uint32_t bit = 1u << st;
+        if (pend_empty & bit) {
+            ok = mbar_wait(&empty[st], (eph & bit) ? 1u : 0u, WAIT_NS);
+            eph ^= bit;
+            pend_empty &= ~bit;
             if (!ok) return;
         }
         const Seg& g = segs[is];
-        const uint32_t arows = (uint32_t)min(128 * mt, g.a_R - g.a_row0);
-        const uint32_t ab = arows * 128u, bb = (uint32_t)N * 128u;
-        mbar_arrive_expect_tx(&p.full[st], ab + bb);
-        bulk_g2s(p.st[st], g.a + ((size_t)ikb * g.a_R + g.a_row0) * 32, ab, &p.full[st]);
-        bulk_g2s(p.st[st] + p.boff, g.b + ((size_t)ikb * g.b_R + g.b_row0) * 32, bb, &p.full[st]);
-        p.pend_full |= 1u << st;
+        const int arows = min(128 * mt, g.a_R - g.a_row0);
+        const uint32_t ab = (uint32_t)arows * 128u;
+        const uint32_t sa = area + (uint32_t)st * sbytes;
+        const float* ga0 = g.a + ((size_t)(na * ikb) * g.a_R + g.a_row0) * 32;
+        const float* gb0 = g.b + ((size_t)(na * ikb) * g.b_R + g.b_row0) * 32;
+        mbar_arrive_expect_tx(&full[st], na * (ab + bb));
+        if (na == 1u || (g.a_row0 == 0 && arows == g.a_R)) {  // the atoms of A are one contiguous run
+            bulk_g2s(sa, ga0, na * ab, &full[st]);
+        } else {
+            bulk_g2s(sa, ga0, ab, &full[st]);
+            bulk_g2s(sa + ab, ga0 + (size_t)g.a_R * 32, ab, &full[st]);
+        }
+        if (na == 1u || (g.b_row0 == 0 && N == g.b_R)) {
+            bulk_g2s(sa + boff, gb0, na * bb, &full[st]);
+        } else {
+            bulk_g2s(sa + boff, gb0, bb, &full[st]);
+            bulk_g2s(sa + boff + bb, gb0 + (size_t)g.b_R * 32, bb, &full[st]);
+        }
+        pend_full |= bit;
         ++issued;
-        if (++ikb == (g.K >> 5)) {
+        if (++ikb == (g.K >> lk)) {
             ikb = 0;
             ++is;
         }
     };
-    while (ok && issued < total && issued < p.ns - 1) issue_next();
+    while (ok && issued < total && issued < ns - 1) issue_next();
     for (int b = 0, cs = 0, ckb = 0; b < total && ok; ++b) {
-        const uint32_t gb = p.g + (uint32_t)b;
-        const int st = (int)(gb % ns);
-        ok = mbar_wait(&p.full[st], (gb / ns) & 1u, WAIT_NS);
-        p.pend_full &= ~(1u << st);
+        const int st = b % ns;
+        const uint32_t bit = 1u << st;
+        ok = mbar_wait(&full[st], (fph & bit) ? 1u : 0u, WAIT_NS);
+        fph ^= bit;
+        pend_full &= ~bit;
         if (!ok) break;
         tc_fence_after();
         const Seg& g = segs[cs];
-        for (int m = 0; m < mt; ++m) {
+        const uint32_t ab = (uint32_t)min(128 * mt, g.a_R - g.a_row0) * 128u;
+        const uint32_t sa = area + (uint32_t)st * sbytes;
+        for (uint32_t hk = 0; hk < na; ++hk) {
+            for (int m = 0; m < mt; ++m) {
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-                mma_tf32(p.tm + g.col + (uint32_t)(m * N), kdesc(p.st[st] + (uint32_t)m * ATILE + kk * 32),
-                         kdesc(p.st[st] + p.boff + kk * 32), idesc, (g.fresh && ckb == 0 && kk == 0) ? 0u : 1u);
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_tf32(tm + g.col + (uint32_t)(m * N), kdesc(sa + hk * ab + (uint32_t)m * ATILE + kk * 32),
+                             kdesc(sa + boff + hk * bb + kk * 32), idesc,
+                             (g.fresh && ckb == 0 && hk == 0 && kk == 0) ? 0u : 1u);
+            }
         }
-        mma_commit(&p.empty[st]);
-        p.pend_empty |= 1u << st;
-        if (++ckb == (g.K >> 5)) {
+        mma_commit(&empty[st]);
+        pend_empty |= bit;
+        if (++ckb == (g.K >> lk)) {
             ckb = 0;
             ++cs;
         }
         if (issued < total) issue_next();
     }
-    p.g += (uint32_t)total;
+    prod->fph = fph;
+    prod->eph = eph;
+    prod->pend_full = pend_full;
+    prod->pend_empty = pend_empty;
     if (ok) {
-        mma_commit(p.done);
+        mma_commit(done);
     } else {
-        *reinterpret_cast<volatile int*>(p.s_fail) = 1;
-        mbar_arrive(p.done);
+        *reinterpret_cast<volatile int*>(prod->s_fail) = 1;
+        mbar_arrive(done);
     }
 }
 
@@ -307,7 +354,10 @@ __device__ __forceinline__ bool gemm(Pipe& p, const Seg* segs, int nseg, int mt,
     if (p.failed) return false;
     if (tid < 32) {  // the producer's warp-mates wait at a warp barrier, not on the mbarrier: a
                      // try_wait may suspend the whole warp and with it the producer
-        if (tid == 0) run_gemm(p, segs, nseg, mt, N);
+        if (tid == 0) {
+            for (int i = 0; i < nseg; ++i) p.prod->segs[i] = segs[i];
+            run_gemm(p.prod, nseg, mt, N);
+        }
         __syncwarp();
     }
     const bool ok = mbar_wait(p.done, p.ndone & 1u, 2 * WAIT_NS);
@@ -418,18 +468,17 @@ __device__ __forceinline__ void put_block(Stager& sg, const Tile& t, int r0, int
 
 template <typename Tout>
 __global__ void __launch_bounds__(NT, 1)
-    tc_deep_kernel(nm_args a, int d, int hd, int L, int chunk, int c_mode, int mt_max, int nstages) {
+    tc_deep_kernel(nm_args a, int d, int hd, int L, int chunk, int c_mode) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const uint32_t stage_bytes = deep_stage_bytes(mt_max);
     // this warp's 32 x 33 transpose buffer and three 4 KB block buffers, in the
-    // operand stages (idle while the epilogues run; 132 KB of the at least 160 KB)
+    // operand stages (idle while the epilogues run; 132 KB of the 192 KB)
     float* tbuf = reinterpret_cast<float*>(sm) + warp * 32 * 33;
     Stager sg;
     sg.base = smem_u32(sm) + EPI_TBUF_BYTES + (uint32_t)warp * 3u * 4096u;
     sg.cnt = 0;
-    float* sG = reinterpret_cast<float*>(sm + (size_t)nstages * stage_bytes);  // Gamma [t][i], row stride GSTR
+    float* sG = reinterpret_cast<float*>(sm + STAGE_AREA);  // Gamma [t][i], row stride GSTR
     float* ga = sG + NTOK * GSTR;  // 1 - alpha_t
     float* ge = ga + NTOK;         // eta_t
     float* gb = ge + NTOK;         // beta_t
@@ -442,13 +491,18 @@ __global__ void __launch_bounds__(NT, 1)
     uint64_t* bars = reinterpret_cast<uint64_t*>(ub + NTOK);  // full[4], empty[4], done
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 2 * MAX_STAGES + 1);
     int* s_fail = reinterpret_cast<int*>(s_tmem + 1);
+    unsigned char* misc = reinterpret_cast<unsigned char*>(bars) + 256;
+    Prod* s_prod = reinterpret_cast<Prod*>(misc);
+    Layout* s_lo = reinterpret_cast<Layout*>(misc + ((sizeof(Prod) + 15) & ~(size_t)15));
 
     const long long unit = blockIdx.x;
     const long long T = a.T;
     const int h = hd;
     const long long P = 2LL * h * d + (long long)(L - 2) * h * h;
     const int b = chunk;
-    const Layout lo = deep_layout(d, h, L);
+    if (tid == 0) *s_lo = deep_layout(d, h, L);
+    __syncthreads();
+    const volatile Layout& lo = *s_lo;  // read where used (a shared load), not held in registers
     float* ws = reinterpret_cast<float*>(a.scratch) + (size_t)unit * lo.total;
     auto dim = [&](int l) { return (l == 0 || l == L) ? d : h; };  // width of x_l (x_L: the output)
     auto woff = [&](int l) { return l == 1 ? 0LL : (long long)h * d + (long long)(l - 2) * h * h; };
@@ -481,21 +535,24 @@ __global__ void __launch_bounds__(NT, 1)
     float* Sw = a.S_T + unit * P;
 
     Pipe p;
-    for (int s = 0; s < MAX_STAGES; ++s) p.st[s] = smem_u32(sm) + (uint32_t)min(s, nstages - 1) * stage_bytes;
-    p.boff = (uint32_t)mt_max * ATILE;
-    p.ns = nstages;
+    p.area = smem_u32(sm);
     p.full = bars;
     p.empty = bars + MAX_STAGES;
     p.done = bars + 2 * MAX_STAGES;
     p.s_fail = s_fail;
-    p.g = 0;
+    p.prod = s_prod;
     p.ndone = 0;
-    p.pend_full = p.pend_empty = 0;
     p.failed = 0;
 
     if (tid == 0) {
         for (int i = 0; i < 2 * MAX_STAGES + 1; ++i) mbar_init(&bars[i], 1);
         *s_fail = 0;
+        s_prod->fph = s_prod->eph = s_prod->pend_full = s_prod->pend_empty = 0;
+        s_prod->area = smem_u32(sm);
+        s_prod->full = bars;
+        s_prod->empty = bars + MAX_STAGES;
+        s_prod->done = bars + 2 * MAX_STAGES;
+        s_prod->s_fail = s_fail;
         fence_mbar_init();
     }
     if (warp == 0) {
@@ -522,6 +579,7 @@ __global__ void __launch_bounds__(NT, 1)
     __syncthreads();
     tc_fence_after();
     p.tm = *s_tmem;
+    if (tid == 0) s_prod->tm = p.tm;
 
     // ends an epilogue: its TMEM reads are done, its tile writes visible to the
     // bulk copies of the next products, and its use of the stages (the
@@ -546,6 +604,26 @@ __global__ void __launch_bounds__(NT, 1)
             ub[tid] = 0.0f;
             sA[tid] = 0.0f;
             sSg[tid] = 0.0f;
+        }
+        if (t0 + b < T) {  // the next chunk's q, k, v and gates into L2 (one 128-byte line per thread)
+            const long long nb = min((long long)b, T - t0 - b);
+            const long long qkv_lines = (nb * d * 2 + 127) / 128, g_lines = (nb * 4 + 127) / 128;
+            const long long tot = 3 * qkv_lines + 3 * g_lines;
+            for (long long i = tid; i < tot; i += NT) {
+                const char* base;
+                long long li = i;
+                if (li < 3 * qkv_lines) {
+                    const int which = (int)(li / qkv_lines);
+                    li -= which * qkv_lines;
+                    base = reinterpret_cast<const char*>((which == 0 ? qp : which == 1 ? kp : vp) + (t0 + b) * d);
+                } else {
+                    li -= 3 * qkv_lines;
+                    const int which = (int)(li / g_lines);
+                    li -= which * g_lines;
+                    base = reinterpret_cast<const char*>((which == 0 ? al : which == 1 ? et : be) + t0 + b);
+                }
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(base + li * 128));
+            }
         }
         __syncthreads();
         // gate scan: column i of Gamma per thread (division-free recursion), A, B, sigma by one thread
@@ -575,17 +653,35 @@ __global__ void __launch_bounds__(NT, 1)
         __syncthreads();
         const __nv_bfloat16* kc = kp + t0 * d;  // this chunk's keys and queries [t][x]
         const __nv_bfloat16* qc = qp + t0 * d;
-        // their operand tiles (zero past the chunk's end)
-        for (int idx = tid; idx < NTOK * d; idx += NT) {
-            const int t = idx / d, x = idx - t * d;
-            const bool in_chunk = t < n;
-            const float kv = in_chunk ? __bfloat162float(kc[(size_t)t * d + x]) : 0.0f;
-            const float qv = in_chunk ? __bfloat162float(qc[(size_t)t * d + x]) : 0.0f;
-            TK.p[toff(NTOK, t, x)] = kv;  // bf16 values are exact in tf32
-            TKt.p[toff(d, x, t)] = kv;
-            TQ.p[toff(NTOK, t, x)] = qv;
-            TQa.p[toff(NTOK, t, x)] = __uint_as_float(to_tf32(sA[t] * qv));
-            TQs.p[toff(NTOK, t, x)] = __uint_as_float(to_tf32(-sSg[t] * qv));
+        // their operand tiles (zero past the chunk's end), in 32 x 32 blocks: k as [t][x] and [x][t],
+        // q plain, times A_t and times -sigma_t (bf16 values are exact in tf32)
+        {
+            const int nxb = d / 32;
+            for (int blk = warp; blk < 4 * nxb; blk += NT / 32) {
+                const bool isq = blk >= 2 * nxb;
+                const int bi = isq ? blk - 2 * nxb : blk;
+                const int tb = (bi / nxb) * 32, xb = (bi % nxb) * 32;
+                const __nv_bfloat16* src = isq ? qc : kc;
+                float v[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    v[i] = tb + i < n ? __bfloat162float(src[(size_t)(tb + i) * d + xb + lane]) : 0.0f;
+                if (!isq) {
+                    put_block(sg, TK, tb, xb, v, lane);
+                    float u[32];
+                    transpose32(tbuf, v, u, lane);
+                    put_block(sg, TKt, xb, tb, u, lane);
+                } else {
+                    put_block(sg, TQ, tb, xb, v, lane);
+                    float sc[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) sc[i] = v[i] * sA[tb + i];
+                    put_block(sg, TQa, tb, xb, sc, lane);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) sc[i] = -v[i] * sSg[tb + i];
+                    put_block(sg, TQs, tb, xb, sc, lane);
+                }
+            }
         }
         handoff();
 
@@ -819,11 +915,11 @@ __global__ void __launch_bounds__(NT, 1)
         if (tid == 0) {
             if (a.status) atomicExch(a.status, NM_ERR_DEVICE_TIMEOUT);
             // let copies and products still in flight land before the CTA leaves
-            for (int st = 0; st < nstages; ++st) {
-                const uint32_t uses = (p.g + (uint32_t)nstages - 1u - (uint32_t)st) / (uint32_t)nstages;
-                if (uses == 0) continue;
-                if (p.pend_full >> st & 1u) mbar_wait(&bars[st], (uses - 1u) & 1u, WAIT_NS);
-                if (p.pend_empty >> st & 1u) mbar_wait(&bars[MAX_STAGES + st], (uses - 1u) & 1u, WAIT_NS);
+            const Prod pr = *s_prod;
+            for (int st = 0; st < MAX_STAGES; ++st) {
+                const uint32_t bit = 1u << st;
+                if (pr.pend_full & bit) mbar_wait(&bars[st], (pr.fph & bit) ? 1u : 0u, WAIT_NS);
+                if (pr.pend_empty & bit) mbar_wait(&bars[MAX_STAGES + st], (pr.eph & bit) ? 1u : 0u, WAIT_NS);
             }
         }
     }
@@ -834,14 +930,11 @@ __global__ void __launch_bounds__(NT, 1)
 
 template <typename Tout>
 cudaError_t launch(const nm_config& c, const nm_args& a, cudaStream_t s) {
-    const int mt_max = (c.hidden + 127) / 128;
-    const int ns = deep_stages(mt_max);
-    const uint32_t smem = deep_smem_bytes(mt_max, ns);
     auto kern = tc_deep_kernel<Tout>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)DEEP_SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    kern<<<(unsigned)((long long)a.B * a.H), NT, smem, s>>>(a, c.d, c.hidden, nm_layers(c), c.chunk, c.c_mode,
-                                                            mt_max, ns);
+    kern<<<(unsigned)((long long)a.B * a.H), NT, DEEP_SMEM_BYTES, s>>>(a, c.d, c.hidden, nm_layers(c), c.chunk,
+                                                                       c.c_mode);
     return cudaGetLastError();
 }
 
