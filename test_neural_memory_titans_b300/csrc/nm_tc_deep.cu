@@ -216,17 +216,19 @@ __device__ __forceinline__ Seg seg(const Tile& a, int a_row0, const Tile& b, int
     return s;
 }
 
-// What the producer (thread 0) works from, in shared memory: the stage area,
-// barriers and TMEM base, its barrier bookkeeping (held in registers inside
-// a GEMM) and the segments of the GEMM being run.
+// What the two producer threads work from, in shared memory: the stage
+// area, barriers and TMEM base, the segments of the GEMM being run, and per
+// stage the copies issued into it (by the copy thread) and the products that
+// read it (by the MMA thread).  Stage s's n-th copy completes phase n of
+// full[s], the products that read it phase n of empty[s].
 struct Prod {
     uint32_t area, tm;
     uint64_t* full;   // [MAX_STAGES] a stage's copies landed
     uint64_t* empty;  // [MAX_STAGES] the products that read a stage completed
-    uint64_t* done;   // all products of a GEMM completed (or the producer gave up)
+    uint64_t* done;   // all products of a GEMM completed (or a producer gave up)
     int* s_fail;
-    uint32_t fph, eph;               // bit s: parity of the next phase of full[s] / empty[s]
-    uint32_t pend_full, pend_empty;  // bit s: a phase of full[s] / empty[s] not yet waited for
+    uint32_t ncopy[MAX_STAGES];  // copies issued into stage s so far (copy thread)
+    uint32_t nmma[MAX_STAGES];   // products issued from stage s so far (MMA thread)
     Seg segs[3];
 };
 
@@ -242,122 +244,126 @@ struct Pipe {
     int failed;
 };
 
-// Thread 0: the copies and products of one GEMM.  A block is 64 k (two
-// 32-k swizzle atoms; one atom where two such stages would not fit) of A
-// rows (up to mt tiles) and N B rows; the blocks cut
-// the stage area into ns = area / block stages (at most MAX_STAGES) and block
-// b goes to stage b % ns.  The copies of ns - 1 blocks are issued first;
-// after the products of block b are issued, the copies of block b + ns - 1
-// follow, into the stage that block b - 1's products read (waited for on its
-// empty barrier while block b's products keep the tensor cores busy).  Each
-// barrier's phase parity is tracked on its own, so the stage count may change
-// from one GEMM to the next.
-__device__ __noinline__ void run_gemm(Prod* prod, int nseg, int mt, int N) {
-    const uint32_t area = prod->area, tm = prod->tm;
-    uint64_t* const full = prod->full;
-    uint64_t* const empty = prod->empty;
-    uint64_t* const done = prod->done;
-    const Seg* segs = prod->segs;
-    uint32_t fph = prod->fph, eph = prod->eph, pend_full = prod->pend_full, pend_empty = prod->pend_empty;
+// The block geometry of one GEMM.  A block is 64 k (two 32-k swizzle atoms;
+// one atom where two such stages would not fit) of A rows (up to mt tiles)
+// and N B rows; the blocks cut the stage area into ns = area / block stages
+// (at most MAX_STAGES) and block b goes to stage b % ns.
+struct Geo {
+    uint32_t na, boff, bb, sbytes;
+    int lk, ns, total;
+};
+__device__ __forceinline__ Geo geometry(const Seg* segs, int nseg, int mt, int N) {
+    Geo g;
     uint32_t amax = 0;
     for (int s = 0; s < nseg; ++s) amax = max(amax, (uint32_t)min(128 * mt, segs[s].a_R - segs[s].a_row0) * 128u);
-    const uint32_t bb = (uint32_t)N * 128u;  // one 32-k atom of B (a multiple of 1024: N % 8 == 0)
-    const uint32_t na = 2u * 2u * (amax + bb) <= STAGE_AREA ? 2u : 1u;  // atoms per block
-    const int lk = na == 2u ? 6 : 5;         // log2 of the k per block
-    int total = 0;
-    for (int s = 0; s < nseg; ++s) total += segs[s].K >> lk;
-    const uint32_t boff = na * amax;         // amax is a multiple of 1024 (rows % 8 == 0)
-    const uint32_t sbytes = boff + na * bb;
-    const int ns = (int)min((uint32_t)MAX_STAGES, STAGE_AREA / sbytes);
-    const uint32_t idesc = idesc_tf32((uint32_t)N);
+    g.bb = (uint32_t)N * 128u;  // one 32-k atom of B (a multiple of 1024: N % 8 == 0)
+    g.na = 2u * 2u * (amax + g.bb) <= STAGE_AREA ? 2u : 1u;
+    g.lk = g.na == 2u ? 6 : 5;  // log2 of the k per block
+    g.total = 0;
+    for (int s = 0; s < nseg; ++s) g.total += segs[s].K >> g.lk;
+    g.boff = g.na * amax;       // amax is a multiple of 1024 (rows % 8 == 0)
+    g.sbytes = g.boff + g.na * g.bb;
+    g.ns = (int)min((uint32_t)MAX_STAGES, STAGE_AREA / g.sbytes);
+    return g;
+}
+
+// The copy thread (warp 0, lane 0): block b's operands into stage b % ns,
+// once the products that read the stage's previous block completed (its
+// empty barrier), so that the copies run up to ns blocks ahead of the
+// products.
+__device__ __noinline__ void run_copies(Prod* prod, int nseg, int mt, int N) {
+    const Seg* segs = prod->segs;
+    const Geo geo = geometry(segs, nseg, mt, N);
     bool ok = true;
-    int issued = 0, is = 0, ikb = 0;  // next block to copy: its segment and 64-k block within the segment
-    auto issue_next = [&]() {
-        const int st = issued % ns;
-        const uint32_t bit = 1u << st;
-        if (pend_empty & bit) {
-            ok = mbar_wait(&empty[st], (eph & bit) ? 1u : 0u, WAIT_NS);
-            eph ^= bit;
-            pend_empty &= ~bit;
-            if (!ok) return;
+    for (int b = 0, is = 0, ikb = 0; b < geo.total; ++b) {
+        const int st = b % geo.ns;
+        const uint32_t n = prod->ncopy[st];
+        if (n > 0) {
+            ok = mbar_wait(&prod->empty[st], (n - 1u) & 1u, WAIT_NS);
+            if (!ok) break;
         }
         const Seg& g = segs[is];
         const int arows = min(128 * mt, g.a_R - g.a_row0);
-        const uint32_t ab = (uint32_t)arows * 128u;
-        const uint32_t sa = area + (uint32_t)st * sbytes;
+        const uint32_t ab = (uint32_t)arows * 128u, bb = geo.bb, na = geo.na;
+        const uint32_t sa = prod->area + (uint32_t)st * geo.sbytes;
         const float* ga0 = g.a + ((size_t)(na * ikb) * g.a_R + g.a_row0) * 32;
         const float* gb0 = g.b + ((size_t)(na * ikb) * g.b_R + g.b_row0) * 32;
-        mbar_arrive_expect_tx(&full[st], na * (ab + bb));
+        uint64_t* fb = &prod->full[st];
+        mbar_arrive_expect_tx(fb, na * (ab + bb));
         if (na == 1u || (g.a_row0 == 0 && arows == g.a_R)) {  // the atoms of A are one contiguous run
-            bulk_g2s(sa, ga0, na * ab, &full[st]);
+            bulk_g2s(sa, ga0, na * ab, fb);
         } else {
-            bulk_g2s(sa, ga0, ab, &full[st]);
-            bulk_g2s(sa + ab, ga0 + (size_t)g.a_R * 32, ab, &full[st]);
+            bulk_g2s(sa, ga0, ab, fb);
+            bulk_g2s(sa + ab, ga0 + (size_t)g.a_R * 32, ab, fb);
         }
         if (na == 1u || (g.b_row0 == 0 && N == g.b_R)) {
-            bulk_g2s(sa + boff, gb0, na * bb, &full[st]);
+            bulk_g2s(sa + geo.boff, gb0, na * bb, fb);
         } else {
-            bulk_g2s(sa + boff, gb0, bb, &full[st]);
-            bulk_g2s(sa + boff + bb, gb0 + (size_t)g.b_R * 32, bb, &full[st]);
+            bulk_g2s(sa + geo.boff, gb0, bb, fb);
+            bulk_g2s(sa + geo.boff + bb, gb0 + (size_t)g.b_R * 32, bb, fb);
         }
-        pend_full |= bit;
-        ++issued;
-        if (++ikb == (g.K >> lk)) {
+        prod->ncopy[st] = n + 1u;
+        if (++ikb == (g.K >> geo.lk)) {
             ikb = 0;
             ++is;
         }
-    };
-    while (ok && issued < total && issued < ns - 1) issue_next();
-    for (int b = 0, cs = 0, ckb = 0; b < total && ok; ++b) {
-        const int st = b % ns;
-        const uint32_t bit = 1u << st;
-        ok = mbar_wait(&full[st], (fph & bit) ? 1u : 0u, WAIT_NS);
-        fph ^= bit;
-        pend_full &= ~bit;
+    }
+    if (!ok) *reinterpret_cast<volatile int*>(prod->s_fail) = 1;
+}
+
+// The MMA thread (warp 1, lane 0): waits for each block's copies, issues its
+// products (M = 128 per tile, K = 8 each) and commits them to the stage's
+// empty barrier; the last commit goes to `done`.  A wait that gives up marks
+// the failure and arrives on `done` so that nobody waits longer.
+__device__ __noinline__ void run_mmas(Prod* prod, int nseg, int mt, int N) {
+    const Seg* segs = prod->segs;
+    const Geo geo = geometry(segs, nseg, mt, N);
+    const uint32_t idesc = idesc_tf32((uint32_t)N);
+    bool ok = true;
+    for (int b = 0, cs = 0, ckb = 0; b < geo.total; ++b) {
+        const int st = b % geo.ns;
+        const uint32_t n = prod->nmma[st];
+        ok = mbar_wait(&prod->full[st], n & 1u, WAIT_NS);
         if (!ok) break;
         tc_fence_after();
         const Seg& g = segs[cs];
         const uint32_t ab = (uint32_t)min(128 * mt, g.a_R - g.a_row0) * 128u;
-        const uint32_t sa = area + (uint32_t)st * sbytes;
-        for (uint32_t hk = 0; hk < na; ++hk) {
+        const uint32_t sa = prod->area + (uint32_t)st * geo.sbytes;
+        for (uint32_t hk = 0; hk < geo.na; ++hk) {
             for (int m = 0; m < mt; ++m) {
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    mma_tf32(tm + g.col + (uint32_t)(m * N), kdesc(sa + hk * ab + (uint32_t)m * ATILE + kk * 32),
-                             kdesc(sa + boff + hk * bb + kk * 32), idesc,
+                    mma_tf32(prod->tm + g.col + (uint32_t)(m * N), kdesc(sa + hk * ab + (uint32_t)m * ATILE + kk * 32),
+                             kdesc(sa + geo.boff + hk * geo.bb + kk * 32), idesc,
                              (g.fresh && ckb == 0 && hk == 0 && kk == 0) ? 0u : 1u);
             }
         }
-        mma_commit(&empty[st]);
-        pend_empty |= bit;
-        if (++ckb == (g.K >> lk)) {
+        mma_commit(&prod->empty[st]);
+        prod->nmma[st] = n + 1u;
+        if (++ckb == (g.K >> geo.lk)) {
             ckb = 0;
             ++cs;
         }
-        if (issued < total) issue_next();
     }
-    prod->fph = fph;
-    prod->eph = eph;
-    prod->pend_full = pend_full;
-    prod->pend_empty = pend_empty;
-    if (ok) {
-        mma_commit(done);
+    if (ok && !*reinterpret_cast<volatile int*>(prod->s_fail)) {
+        mma_commit(prod->done);
     } else {
         *reinterpret_cast<volatile int*>(prod->s_fail) = 1;
-        mbar_arrive(done);
+        mbar_arrive(prod->done);
     }
 }
 
-// Every thread: run one GEMM (thread 0 drives it) and wait for it.  Returns
+// Every thread: run one GEMM (threads 0 and 32 drive it) and wait for it.  Returns
 // false once any wait has given up.
 __device__ __forceinline__ bool gemm(Pipe& p, const Seg* segs, int nseg, int mt, int N, int tid) {
     if (p.failed) return false;
-    if (tid < 32) {  // the producer's warp-mates wait at a warp barrier, not on the mbarrier: a
+    if (tid < 64) {  // the producers' warp-mates wait at a warp barrier, not on the mbarrier: a
                      // try_wait may suspend the whole warp and with it the producer
-        if (tid == 0) {
+        if (tid == 0)
             for (int i = 0; i < nseg; ++i) p.prod->segs[i] = segs[i];
-            run_gemm(p.prod, nseg, mt, N);
-        }
+        asm volatile("bar.sync 1, 64;" ::: "memory");  // warps 0 and 1: the segments are in place
+        if (tid == 0) run_copies(p.prod, nseg, mt, N);
+        if (tid == 32) run_mmas(p.prod, nseg, mt, N);
         __syncwarp();
     }
     const bool ok = mbar_wait(p.done, p.ndone & 1u, 2 * WAIT_NS);
@@ -547,7 +553,7 @@ __global__ void __launch_bounds__(NT, 1)
     if (tid == 0) {
         for (int i = 0; i < 2 * MAX_STAGES + 1; ++i) mbar_init(&bars[i], 1);
         *s_fail = 0;
-        s_prod->fph = s_prod->eph = s_prod->pend_full = s_prod->pend_empty = 0;
+        for (int i = 0; i < MAX_STAGES; ++i) s_prod->ncopy[i] = s_prod->nmma[i] = 0;
         s_prod->area = smem_u32(sm);
         s_prod->full = bars;
         s_prod->empty = bars + MAX_STAGES;
@@ -587,6 +593,15 @@ __global__ void __launch_bounds__(NT, 1)
     auto handoff = [&]() {
         if (lane == 0) bulk_wait_all();  // this warp's block copies have landed
         fence_proxy_async_global();
+        fence_proxy_async();
+        tc_fence_before();
+        __syncthreads();
+    };
+    // the same where the block copies just sent are read only in the next chunk (the state's tiles): they
+    // need only have read their shared-memory buffers, which the next products' copies reuse; the next
+    // chunk's first handoff waits for them to land
+    auto handoff_light = [&]() {
+        if (lane == 0) bulk_wait_read();
         fence_proxy_async();
         tc_fence_before();
         __syncthreads();
@@ -906,7 +921,7 @@ __global__ void __launch_bounds__(NT, 1)
                         }
                         __syncwarp();
                     });
-                    handoff();
+                    handoff_light();
                 }
             }
         }
@@ -915,14 +930,14 @@ __global__ void __launch_bounds__(NT, 1)
         if (tid == 0) {
             if (a.status) atomicExch(a.status, NM_ERR_DEVICE_TIMEOUT);
             // let copies and products still in flight land before the CTA leaves
-            const Prod pr = *s_prod;
             for (int st = 0; st < MAX_STAGES; ++st) {
-                const uint32_t bit = 1u << st;
-                if (pr.pend_full & bit) mbar_wait(&bars[st], (pr.fph & bit) ? 1u : 0u, WAIT_NS);
-                if (pr.pend_empty & bit) mbar_wait(&bars[MAX_STAGES + st], (pr.eph & bit) ? 1u : 0u, WAIT_NS);
+                const uint32_t nc = s_prod->ncopy[st], nm = s_prod->nmma[st];
+                if (nc > nm) mbar_wait(&bars[st], nm & 1u, WAIT_NS);                      // a copy not consumed
+                if (nm > 0) mbar_wait(&bars[MAX_STAGES + st], (nm - 1u) & 1u, WAIT_NS);  // the last products
             }
         }
     }
+    if (lane == 0) bulk_wait_all();  // every block copy has read its buffer and landed before the CTA exits
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(p.tm, 512);
