@@ -36,6 +36,7 @@ L-layer memory.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import os
 import statistics
@@ -293,7 +294,6 @@ def workload(args):
 
     wl = W.WORKLOADS[args.workload]
     if args.layers is not None and args.layers != wl.layers:
-        import dataclasses
         if wl.kind != W.MLP2:
             raise SystemExit("--layers applies to the MLP workloads (1 and 3)")
         wl = dataclasses.replace(wl, layers=args.layers, name="%s_L%d" % (wl.name, args.layers))
@@ -302,7 +302,6 @@ def workload(args):
     wl = wl.with_sizes(B=args.B, H=args.H, T=args.T)
     if wl.segment and (wl.T % wl.segment or wl.T < wl.segment):
         wl = wl.with_sizes(segment=0)
-    import dataclasses
     return dataclasses.replace(wl, name="%s@B%dH%dT%d" % (wl.name, wl.B, wl.H, wl.T))
 
 
@@ -385,13 +384,21 @@ def time_steps(step, steps, warmup, flush, stream, dev, world, local_rank, check
     return [s_.elapsed_time(e_) for s_, e_ in zip(starts, ends)], clocks.summary(), n_launch
 
 
+# Nominal dense tf32 / bf16 tensor rate of a B300 (1.1 / 2.25 PFLOP/s): the
+# tf32 peak is the measured bf16 peak times this ratio.
+TF32_PER_BF16 = 1.1 / 2.25
+
+
 def roofline(wl, ms, path_tc, peaks, peak_src, traffic):
-    """The dominant kernel's algorithmic rate per launch against the measured peak."""
+    """The dominant kernel's algorithmic rate per launch against the measured
+    peak of its own operand type (the deeper-memory kernel's products are
+    tf32, the other tensor-core kernels' bf16)."""
     alg = algorithmic(wl)
     per_launch_ms = ms / alg["calls"]
+    tf32 = path_tc and wl.kind == 1 and wl.layers > 2  # the MLP memory
     if alg["bound"] == "tensor":
         achieved = alg["flops"] / alg["calls"] / (per_launch_ms * 1e-3) / 1e12
-        peak = float(peaks["bf16_tflops"])
+        peak = float(peaks["bf16_tflops"]) * (TF32_PER_BF16 if tf32 else 1.0)
         unit = "TFLOP/s"
     else:
         achieved = alg["bytes"] / alg["calls"] / (per_launch_ms * 1e-3) / 1e9
@@ -400,7 +407,7 @@ def roofline(wl, ms, path_tc, peaks, peak_src, traffic):
     secs = per_launch_ms * alg["calls"] * 1e-3
     return {"bound": "hbm" if alg["bound"] == "hbm" else "tensor", "achieved": achieved, "peak": peak, "unit": unit,
             "frac": achieved / peak, "traffic": traffic,
-            "peak_source": peak_src + " (burst)",
+            "peak_source": peak_src + (" (burst bf16 x 1.1/2.25, the nominal tf32 ratio)" if tf32 else " (burst)"),
             "kernel": "nm_forward (%s path)" % ("tcgen05" if path_tc else "fp32 FFMA"),
             "per_launch_ms": per_launch_ms,
             "algorithmic_flops_per_launch": alg["flops"] / alg["calls"],
@@ -704,6 +711,20 @@ def run_ours(args, rank, world, local_rank):
             per.append(entry)
             r2.close()
             del r2
+        # the deeper memory (3 layers) on the 64 -> 256 -> 64 workload's shape and inputs
+        wl3 = dataclasses.replace(W.WORKLOADS[1], layers=3, name=W.WORKLOADS[1].name + "_L3")
+        torch.cuda.empty_cache()
+        r3 = Runner(wl3, dev, stream, 1001, args.path, 3)
+        n3 = max(3, min(args.steps, 20))
+        ms3, clk3, l3 = time_steps(r3.step, n3, max(3, min(args.warmup, 5)), flush, stream, dev, 1, local_rank,
+                                   r3.check_status, lambda: r3.mem.launches)
+        m3 = sum(ms3) / len(ms3)
+        per.append({"workload": wl3.name, "ms_per_step": m3, "value": wl3.tokens / (m3 * 1e-3), "unit": "tokens/s",
+                    "steps": n3, "gpu_launches": l3,
+                    "roofline": roofline(wl3, m3, r3.mem.path == nm.PATH_TC, peaks, peak_src, None),
+                    "clocks": clk3, "path": "tcgen05 tf32" if r3.mem.path == nm.PATH_TC else "fp32 FFMA"})
+        r3.close()
+        del r3
         out["per_workload"] = per
     return out
 
