@@ -97,8 +97,11 @@ typedef struct nm_config {
                        for NM_LINEAR.  L > 2 is the deeper memory
                        W_L silu(W_{L-1} ... silu(W1 x)): W1 hidden x d,
                        W2 .. W_{L-1} hidden x hidden, W_L d x hidden, packed in
-                       that order (P = 2 hidden d + (L - 2) hidden^2); it runs
-                       on the fp32 FFMA kernels (NM_PATH_TC is unsupported)    */
+                       that order (P = 2 hidden d + (L - 2) hidden^2).  On
+                       NM_PATH_TC (tf32 tensor-core kernel) for bf16 inputs,
+                       d = 64 or 128, hidden a multiple of 64 up to 512 and
+                       chunk <= 64, with a per-unit workspace the handle
+                       allocates; every shape on the fp32 FFMA kernels        */
 } nm_config;
 
 #define NM_MAX_LAYERS 16
