@@ -56,7 +56,8 @@ METRIC = "memory-layer fwd tokens/sec (B*H*T/s) and % of roofline (TC FLOPs vs H
 # A capture describes the kernel it was taken on only: when the sources differ, traffic is null.
 # The 128->512->128 figure is scaled from a capture of a 16384-token slice of the workload (token
 # traffic x 8, plus the state read and written once per call); the streamed workload's is one
-# 65536-token segment call, which is what one launch of its bench step processes.
+# 65536-token segment call, which is what one launch of its bench step processes; the 3-layer memory's
+# from a 512-token capture (8 of the 64 chunks: its per-chunk traffic x 64, plus the state once).
 NCU_TRAFFIC = {
     "mlp_64x256_bf16_b4h8_t4096_c64": (("nm_tc_mlp.cu", "tc_common.cuh", "nm_internal.h"), "810ad16e5ee50003",
                                        62.45e6),
@@ -66,6 +67,8 @@ NCU_TRAFFIC = {
                                            "d70d351ebd9b6b93", 4.178e9),
     "linear_d64_bf16_b1h8_t2097152_c256_seg65536": (("nm_tc_linear64.cu", "tc_common.cuh", "nm_internal.h"),
                                                     "cd0494a3b25f3211", 254.6e6),
+    "mlp_64x256_bf16_b4h8_t4096_c64_L3": (("nm_tc_deep.cu", "tc_common.cuh", "nm_internal.h"), "8340c6d6e7fd91c1",
+                                          8.446e9),
 }
 
 
@@ -721,7 +724,8 @@ def run_ours(args, rank, world, local_rank):
         m3 = sum(ms3) / len(ms3)
         per.append({"workload": wl3.name, "ms_per_step": m3, "value": wl3.tokens / (m3 * 1e-3), "unit": "tokens/s",
                     "steps": n3, "gpu_launches": l3,
-                    "roofline": roofline(wl3, m3, r3.mem.path == nm.PATH_TC, peaks, peak_src, None),
+                    "roofline": roofline(wl3, m3, r3.mem.path == nm.PATH_TC, peaks, peak_src,
+                                         ncu_traffic(wl3.name) if r3.mem.path == nm.PATH_TC else None),
                     "clocks": clk3, "path": "tcgen05 tf32" if r3.mem.path == nm.PATH_TC else "fp32 FFMA"})
         r3.close()
         del r3
