@@ -227,6 +227,7 @@ struct Prod {
     uint64_t* empty;  // [MAX_STAGES] the products that read a stage completed
     uint64_t* done;   // all products of a GEMM completed (or a producer gave up)
     int* s_fail;
+    int skip;                    // test hook: the call's first GEMM gets no copies (its products' wait expires)
     uint32_t ncopy[MAX_STAGES];  // copies issued into stage s so far (copy thread)
     uint32_t nmma[MAX_STAGES];   // products issued from stage s so far (MMA thread)
     Seg segs[3];
@@ -272,6 +273,10 @@ __device__ __forceinline__ Geo geometry(const Seg* segs, int nseg, int mt, int N
 // empty barrier), so that the copies run up to ns blocks ahead of the
 // products.
 __device__ __noinline__ void run_copies(Prod* prod, int nseg, int mt, int N) {
+    if (prod->skip) {  // (the test hook: nothing is copied, so the MMA thread's first wait gives up)
+        prod->skip = 0;
+        return;
+    }
     const Seg* segs = prod->segs;
     const Geo geo = geometry(segs, nseg, mt, N);
     bool ok = true;
@@ -554,6 +559,7 @@ __global__ void __launch_bounds__(NT, 1)
         for (int i = 0; i < 2 * MAX_STAGES + 1; ++i) mbar_init(&bars[i], 1);
         *s_fail = 0;
         for (int i = 0; i < MAX_STAGES; ++i) s_prod->ncopy[i] = s_prod->nmma[i] = 0;
+        s_prod->skip = a.skip_first_load;
         s_prod->area = smem_u32(sm);
         s_prod->full = bars;
         s_prod->empty = bars + MAX_STAGES;

@@ -40,6 +40,40 @@ def test_missing_tile_load_times_out_and_the_handle_recovers(wid):
     mem.close()
 
 
+def test_missing_load_deep_memory_times_out_and_the_handle_recovers():
+    """The deeper-memory kernel (3 layers, tf32 tensor cores): the hook makes
+    its copy thread issue nothing for the call's first product, so the MMA
+    thread's wait for those operands gives up after 2 s."""
+    import dataclasses
+    import numpy as np
+    import oracle
+    from _helpers import TOL, f64, rel_l2
+    d, hidden, layers, T = 64, 128, 3, 130
+    wl = dataclasses.replace(W.WORKLOADS[1], hidden=hidden, layers=layers).with_sizes(B=1, H=2, T=T)
+    x = W.make_inputs(wl, "cuda", seed=5)
+    x["eta"] *= 0.5
+    g = torch.Generator("cuda").manual_seed(6)
+    M0 = (0.5 / hidden) ** 0.5 * torch.randn((1, 2, wl.P), generator=g, device="cuda")
+    S0 = 0.1 * M0.flip(-1).contiguous()
+    mem = nm.NeuralMemory(nm.MLP2, d, hidden, 64, in_dtype=torch.bfloat16, layers=layers, path=nm.PATH_TC)
+    args = (x["q"], x["k"], x["v"], x["alpha"], x["eta"], x["beta"], M0, S0)
+    assert mem.inject_missing_load() == nm.NM_OK
+    t0 = time.time()
+    mem.forward(*args)
+    assert mem.synchronize() == nm.NM_ERR_DEVICE_TIMEOUT
+    assert time.time() - t0 < 60
+    y, MT, ST = mem.forward(*args)
+    assert mem.synchronize() == nm.NM_OK
+    mem.close()
+    ref = oracle.forward(oracle.MLP2, d, hidden, 64, oracle.C_ONE,
+                         *(f64(x[k_]) for k_ in ("q", "k", "v", "alpha", "eta", "beta")), None, f64(M0), f64(S0),
+                         layers=layers)
+    tol = TOL[torch.bfloat16]
+    assert rel_l2(f64(y), ref[0]) <= tol["y"]
+    assert rel_l2(f64(MT), ref[1]) <= tol["M_T"]
+    assert rel_l2(f64(ST), ref[2]) <= tol["S_T"]
+
+
 def test_injection_needs_the_tensor_core_path():
     wl = W.WORKLOADS[0]
     mem = nm.NeuralMemory(wl.kind, wl.d, 0, wl.chunk, in_dtype=torch.float32, path=nm.PATH_SIMT)
