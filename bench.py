@@ -507,7 +507,8 @@ def run_backward(args, rank, world, local_rank):
     Gy = torch.randn((wl.B, wl.H, wl.T, wl.d), generator=g, device=dev)
     GM = torch.randn((wl.B, wl.H, wl.P), generator=g, device=dev)
     GS = torch.randn((wl.B, wl.H, wl.P), generator=g, device=dev)
-    mem = nm.NeuralMemory(wl.kind, wl.d, wl.hidden, wl.chunk, in_dtype=wl.dtype, device=local_rank)
+    mem = nm.NeuralMemory(wl.kind, wl.d, wl.hidden, wl.chunk, in_dtype=wl.dtype, device=local_rank, path=args.path)
+    tc = mem.path == nm.PATH_TC  # the reverse sweep's contractions on the tensor cores (tf32)
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
 
     def step():
@@ -529,17 +530,25 @@ def run_backward(args, rank, world, local_rank):
     alg = backward_algorithmic(wl)
     achieved = alg["flops"] / (ms * 1e-3) / 1e12
     mem.close()
+    if tc:
+        peaks, peak_src = load_peaks()
+        peak = float(peaks["bf16_tflops"]) * TF32_PER_BF16
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                "traffic": None, "peak_source": peak_src + " (burst bf16 x 1.1/2.25, the nominal tf32 ratio)",
+                "kernel": "nm_backward (fp32 FFMA checkpointing forward + reverse sweep with tcgen05 tf32 contractions)"}
+    else:
+        roof = {"bound": "alu", "achieved": achieved, "peak": FP32_PEAK_TFLOPS, "unit": "TFLOP/s",
+                "frac": achieved / FP32_PEAK_TFLOPS, "traffic": None,
+                "peak_source": "derived: 148 SMs x 128 fp32 lanes x 2 flops x 2032 MHz",
+                "kernel": "nm_backward (fp32 FFMA checkpointing forward + reverse sweep)"}
     return {"metric": "memory-layer backward tokens/sec (B*H*T/s)", "value": world * alg["tokens"] / (ms * 1e-3),
             "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "tf32" if tc else "f32",
+            "data": "synthetic",
             "config": {"workload": wl.name, "pass": "backward", "B": wl.B, "H": wl.H, "T": wl.T, "d": wl.d,
                        "hidden": wl.hidden, "chunk": wl.chunk, "parallelism": "dp%d" % world,
                        "l2": "flushed between timed steps (256 MB write, outside the step's events)"},
-            "roofline": {"bound": "alu", "achieved": achieved, "peak": FP32_PEAK_TFLOPS, "unit": "TFLOP/s",
-                         "frac": achieved / FP32_PEAK_TFLOPS, "traffic": None,
-                         "peak_source": "derived: 148 SMs x 128 fp32 lanes x 2 flops x 2032 MHz",
-                         "kernel": "nm_backward (fp32 FFMA checkpointing forward + reverse sweep)"},
-            "gpu_launches": launches, "clocks": clocks,
+            "roofline": roof, "gpu_launches": launches, "clocks": clocks,
             "step_ms": {"min": min(step_ms), "median": statistics.median(step_ms), "max": max(step_ms)}}
 
 

@@ -213,9 +213,15 @@ int nm_forward_gated(nm_handle_t h, int B, int H, int T,
  *   once more on the fp32 FFMA kernel, recording every chunk's start state in
  *   a handle-owned workspace (B*H*ceil(T/chunk)*2*P floats plus per-unit
  *   scratch; it grows on demand, so a first call at a larger size
- *   allocates), then sweeps the chunks from last to first.  No output may
- *   overlap any input or another output (NM_ERR_ALIAS).  Asynchronous on
- *   `stream`; host-side errors return with nothing launched.
+ *   allocates), then sweeps the chunks from last to first.  The sweep's
+ *   chunk-sized contractions run as fp32 FFMA products, or, on a handle
+ *   created with path NM_PATH_TC (bf16 inputs, a shape the forward's
+ *   tensor-core kernels take), as tcgen05 tf32 products (fp32 accumulation;
+ *   gradients then within the bf16-input tolerances instead of fp32 ones,
+ *   and a timed-out product wait is reported by nm_synchronize as
+ *   NM_ERR_DEVICE_TIMEOUT).  No output may overlap any input or another
+ *   output (NM_ERR_ALIAS).  Asynchronous on `stream`; host-side errors return
+ *   with nothing launched.
  */
 int nm_backward(nm_handle_t h, int B, int H, int T,
                 const void* q, const void* k, const void* v,

@@ -7,6 +7,9 @@
 
 #include "nm_internal.h"
 
+// The backward pass's reverse sweep with tensor-core contractions (nm_backward.cu).
+cudaError_t nm_bwd_launch_tc(const nm_config& c, const nm_bwd_call& call, int* status, cudaStream_t s);
+
 namespace {
 
 // Makes `dev` current for the scope and restores the caller's device after.
@@ -379,7 +382,10 @@ int nm_backward(nm_handle_t h, int B, int H, int T, const void* q, const void* k
     bc.dM0 = dM0; bc.dS0 = dS0;
     bc.ws = scratch;
     bc.e_clip = nm_err_clip(cfg);
-    if (nm_bwd_launch(cfg, bc, s) != cudaSuccess) {
+    // the reverse sweep's contractions on the tensor cores (tf32) when the handle asked for NM_PATH_TC, else
+    // fp32 FFMA (NM_PATH_AUTO: the same speed, since the sweep is bound by its other steps, at fp32 accuracy)
+    const cudaError_t be = cfg.path == NM_PATH_TC ? nm_bwd_launch_tc(cfg, bc, h->d_status, s) : nm_bwd_launch(cfg, bc, s);
+    if (be != cudaSuccess) {
         cudaGetLastError();
         return NM_ERR_CUDA;
     }

@@ -30,10 +30,13 @@
 // start states come from a forward pass that records them (the fp32 FFMA
 // forward kernel with a checkpoint array).
 //
-// This is an fp32 FFMA kernel: one CTA per unit, every step a block-wide loop
-// over its output elements, matrices in a per-unit global workspace (read
-// through L1 / L2).
+// One CTA per unit, every step a block-wide loop over its output elements,
+// matrices in a per-unit global workspace (read through L1 / L2).  The
+// chunk-sized contractions run either as fp32 FFMA block GEMMs or, on the
+// tensor-core path, as tcgen05 kind::tf32 products (operands rounded to tf32,
+// fp32 accumulation in TMEM); everything else is the same fp32 code.
 #include "nm_internal.h"
+#include "tc_common.cuh"
 
 namespace {
 
@@ -65,6 +68,7 @@ struct bwd_args {
     float* ws;          // per-unit workspace
     size_t ws_unit;     // floats per unit
     float e_clip;
+    int* status;        // device status word (a timed-out wait of the tensor-core contractions)
 };
 
 __device__ __forceinline__ float ld_f(const float* p) { return *p; }
@@ -151,7 +155,191 @@ __device__ void block_gemm(int M, int N, int K, const float* A, long long am, lo
     __syncthreads();
 }
 
-template <typename Tin>
+// ---------------------------------------------------------------- tensor-core contractions
+// C(m, n) = alpha sum_k A(m, k) B(k, n) [+ C(m, n)] as tcgen05.mma kind::tf32
+// products, the same contract as block_gemm: per pass up to 256 x 256
+// outputs (two M = 128 tiles, N a multiple of 32) in TMEM; K in blocks of 32,
+// each staged by all threads into shared memory as tf32 (rounded to nearest)
+// in the 128-byte-swizzled K-major layout, double-buffered so that a block is
+// staged while the previous one's products run; thread 0 issues the products
+// (K = 8 each) and commits them to the stage's mbarrier; the epilogue reads
+// the accumulators (row = TMEM lane) and writes C.  Every wait gives up after
+// 2 s; the CTA then stops issuing products and reports NM_ERR_DEVICE_TIMEOUT.
+constexpr uint32_t TG_ATILE = 128 * 128;               // 128 rows x 32 fp32 k
+constexpr uint32_t TG_ASTAGE = 2 * TG_ATILE;           // up to 256 A rows
+constexpr uint32_t TG_BSTAGE = 256 * 128;              // up to 256 B rows
+constexpr uint32_t TG_SMEM = 2 * (TG_ASTAGE + TG_BSTAGE) + 64 + 1024;  // two stages, barriers, alignment
+constexpr uint64_t TG_WAIT_NS = 2000000000ull;
+constexpr int TG_U = 4;  // 16-byte chunks per thread whose loads are issued together
+
+// tcgen05 instruction descriptor, kind::tf32: tf32 A and B (format 2), fp32
+// accumulator, both K-major, M = 128.
+__host__ __device__ constexpr uint32_t tg_idesc(uint32_t N) {
+    return (1u << 4) | (2u << 7) | (2u << 10) | ((N >> 3) << 17) | ((128u >> 4) << 24);
+}
+__device__ __forceinline__ void tg_mma(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                       uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ uint32_t tg_tf32(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
+}
+
+struct TcCtx {
+    uint32_t a_st[2], b_st[2];  // shared addresses of the stages
+    uint64_t* bars;             // [2] products of a stage completed
+    uint32_t ph[2];             // completions waited per barrier
+    uint32_t pending;           // bit s: a commit on bars[s] not waited for
+    uint32_t tm;                // TMEM base
+    int failed;
+};
+
+// Dynamic shared memory, barriers and 512 TMEM columns (every thread calls it).
+__device__ void tg_setup(TcCtx& x) {
+    extern __shared__ unsigned char tg_raw[];
+    unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(tg_raw) + 1023) & ~(uintptr_t)1023);
+    x.a_st[0] = tc::smem_u32(sm);
+    x.a_st[1] = x.a_st[0] + TG_ASTAGE;
+    x.b_st[0] = x.a_st[1] + TG_ASTAGE;
+    x.b_st[1] = x.b_st[0] + TG_BSTAGE;
+    x.bars = reinterpret_cast<uint64_t*>(sm + 2 * (TG_ASTAGE + TG_BSTAGE));
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(x.bars + 2);
+    if (threadIdx.x == 0) {
+        tc::mbar_init(&x.bars[0], 1);
+        tc::mbar_init(&x.bars[1], 1);
+        tc::fence_mbar_init();
+    }
+    if (threadIdx.x < 32) {
+        tc::tmem_alloc(s_tmem, 512);
+        tc::tmem_relinquish();
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    x.tm = *s_tmem;
+    x.ph[0] = x.ph[1] = 0;
+    x.pending = 0;
+    x.failed = 0;
+}
+
+__device__ void tg_teardown(TcCtx& x, int* status) {
+    if (x.failed && threadIdx.x == 0 && status) atomicExch(status, NM_ERR_DEVICE_TIMEOUT);
+    tc::tc_fence_before();
+    __syncthreads();
+    if (threadIdx.x < 32) tc::tmem_dealloc(x.tm, 512);
+}
+
+// Stages columns k0 .. k0 + 31 of rows 0 .. R - 1 of an operand (element
+// (r, k) = p[r sr + k sk], zero for r >= rv or k >= K) into a tile of R
+// 128-byte rows, 16-byte chunk kc of row r at r * 128 + ((kc ^ (r % 8)) * 16).
+// Consecutive threads take consecutive chunks of a row when k is contiguous,
+// consecutive rows otherwise (coalesced loads either way).
+__device__ __forceinline__ void tg_stage(uint32_t tile, int R, int rv, const float* p, long long sr, long long sk,
+                                         int k0, int K, int tid) {
+    const int n = R * 8;
+    const bool kfast = sk == 1;
+    for (int base = 0; base < n; base += BW_THREADS * TG_U) {
+        float v[TG_U][4];
+        int rr[TG_U], kc[TG_U];
+#pragma unroll
+        for (int u = 0; u < TG_U; ++u) {
+            const int idx = base + u * BW_THREADS + tid;
+            rr[u] = kfast ? idx >> 3 : idx % R;
+            kc[u] = kfast ? idx & 7 : idx / R;
+            const int k = k0 + 4 * kc[u];
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                v[u][j] = (idx < n && rr[u] < rv && k + j < K) ? p[(long long)rr[u] * sr + (long long)(k + j) * sk] : 0.0f;
+        }
+#pragma unroll
+        for (int u = 0; u < TG_U; ++u) {
+            const int idx = base + u * BW_THREADS + tid;
+            if (idx < n)
+                tc::st_shared_v4(tile + (uint32_t)rr[u] * 128u + (((uint32_t)kc[u] ^ ((uint32_t)rr[u] & 7u)) << 4),
+                                 tg_tf32(v[u][0]), tg_tf32(v[u][1]), tg_tf32(v[u][2]), tg_tf32(v[u][3]));
+        }
+    }
+}
+
+__device__ __forceinline__ bool tg_wait(TcCtx& x, int st) {
+    if (!(x.pending >> st & 1u)) return true;
+    const bool ok = tc::mbar_wait(&x.bars[st], x.ph[st] & 1u, TG_WAIT_NS);
+    x.ph[st] += 1;
+    x.pending &= ~(1u << st);
+    return ok;
+}
+
+__device__ __noinline__ void tc_gemm(TcCtx& x, int M, int N, int K, const float* A, long long am, long long ak, const float* B,
+                        long long bk, long long bn, float* C, long long cm, float alpha, bool accumulate) {
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    for (int m0 = 0; m0 < M; m0 += 256) {
+        const int mr = min(256, M - m0), mt = (mr + 127) >> 7;
+        for (int n0 = 0; n0 < N; n0 += 256) {
+            const int nr = min(256, N - n0), np = (nr + 31) & ~31;
+            const uint32_t idesc = tg_idesc((uint32_t)np);
+            bool bad = false;
+            int kb = 0;
+            for (int k0 = 0; k0 < K && !x.failed; k0 += 32, ++kb) {
+                const int st = kb & 1;
+                if (!tg_wait(x, st)) bad = true;
+                tg_stage(x.a_st[st], 128 * mt, mr, A + (long long)m0 * am, am, ak, k0, K, tid);
+                tg_stage(x.b_st[st], np, nr, B + (long long)n0 * bn, bn, bk, k0, K, tid);
+                tc::fence_proxy_async();
+                if (__syncthreads_or(bad)) {
+                    x.failed = 1;
+                    break;
+                }
+                if (tid == 0) {
+                    tc::tc_fence_after();
+                    for (int m = 0; m < mt; ++m) {
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            tg_mma(x.tm + (uint32_t)(m * np),
+                                   tc::sw128_desc(x.a_st[st] + (uint32_t)m * TG_ATILE + kk * 32, 16, 1024),
+                                   tc::sw128_desc(x.b_st[st] + kk * 32, 16, 1024), idesc, (k0 > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    tc::mma_commit(&x.bars[st]);
+                }
+                x.pending |= 1u << st;
+            }
+            if (!tg_wait(x, 0)) bad = true;
+            if (!tg_wait(x, 1)) bad = true;
+            if (__syncthreads_or(bad)) x.failed = 1;
+            tc::tc_fence_after();
+            if (!x.failed) {
+                const int q = warp & 3, hf = warp >> 2, half = np / 2;
+                for (int m = 0; m < mt; ++m) {
+                    const int gm = m0 + 128 * m + 32 * q + lane;
+                    for (int c0 = hf * half; c0 < (hf + 1) * half; c0 += 16) {
+                        float v[16];
+                        tc::tmem_ld_n(x.tm + ((uint32_t)(32 * q) << 16) + (uint32_t)(m * np + c0), v);
+                        if (gm < M) {
+#pragma unroll
+                            for (int c = 0; c < 16; ++c) {
+                                const int gn = n0 + c0 + c;
+                                if (gn < N) {
+                                    float* cp = C + (long long)gm * cm + gn;
+                                    *cp = accumulate ? fmaf(alpha, v[c], *cp) : alpha * v[c];
+                                }
+                            }
+                        }
+                    }
+                }
+            }
+            tc::tc_fence_before();
+            __syncthreads();
+        }
+    }
+}
+
+template <typename Tin, bool TC>
 __global__ void __launch_bounds__(BW_THREADS) bwd_linear_kernel(bwd_args a, int d, int b, int c_mode) {
     __shared__ float s_a[BW_MAX_CHUNK], s_e[BW_MAX_CHUNK], s_b[BW_MAX_CHUNK], s_c[BW_MAX_CHUNK];
     __shared__ float sA[BW_MAX_CHUNK], sB[BW_MAX_CHUNK], sS[BW_MAX_CHUNK];
@@ -160,6 +348,14 @@ __global__ void __launch_bounds__(BW_THREADS) bwd_linear_kernel(bwd_args a, int 
     __shared__ float s_da[BW_MAX_CHUNK], s_de[BW_MAX_CHUNK], s_db[BW_MAX_CHUNK], s_dc[BW_MAX_CHUNK];
     __shared__ float red[BW_THREADS / 32];
     __shared__ __align__(16) float gsh[GEMM_SMEM_FLOATS];
+    TcCtx tcx;
+    if constexpr (TC) tg_setup(tcx);
+    // every chunk-sized contraction: tcgen05 tf32 products or fp32 FFMA block GEMMs
+    auto gemm_ = [&](int M_, int N_, int K_, const float* A_, long long am_, long long ak_, const float* B_, long long bk_,
+                     long long bn_, float* C_, long long cm_, float alpha_, bool acc_, float* sh_) {
+        if constexpr (TC) tc_gemm(tcx, M_, N_, K_, A_, am_, ak_, B_, bk_, bn_, C_, cm_, alpha_, acc_);
+        else block_gemm(M_, N_, K_, A_, am_, ak_, B_, bk_, bn_, C_, cm_, alpha_, acc_, sh_);
+    };
 
     const long long unit = blockIdx.x;
     const int tid = threadIdx.x;
@@ -246,10 +442,10 @@ __global__ void __launch_bounds__(BW_THREADS) bwd_linear_kernel(bwd_args a, int 
             }
         }
         // ---- Mc k_i, Mc q_t, Sc q_t, q_t . k_i  (B(x, o) = Mc[o][x])
-        block_gemm(n, d, d, Kf, d, 1, Mc, 1, d, LR, d, 1.0f, false, gsh);
-        block_gemm(n, d, d, Qf, d, 1, Mc, 1, d, Mq, d, 1.0f, false, gsh);
-        block_gemm(n, d, d, Qf, d, 1, Sc, 1, d, Sq, d, 1.0f, false, gsh);
-        block_gemm(n, n, d, Qf, d, 1, Kf, 1, d, QK, b, 1.0f, false, gsh);
+        gemm_(n, d, d, Kf, d, 1, Mc, 1, d, LR, d, 1.0f, false, gsh);
+        gemm_(n, d, d, Qf, d, 1, Mc, 1, d, Mq, d, 1.0f, false, gsh);
+        gemm_(n, d, d, Qf, d, 1, Sc, 1, d, Sq, d, 1.0f, false, gsh);
+        gemm_(n, n, d, Qf, d, 1, Kf, 1, d, QK, b, 1.0f, false, gsh);
         // ---- e_i = clip(2 (Mc k_i - v_i)); P_Q = Gamma (.) QK (lower triangle)
         for (int idx = tid; idx < n * d; idx += BW_THREADS) {
             const float r2 = 2.0f * (LR[idx] - Vf[idx]);
@@ -262,13 +458,13 @@ __global__ void __launch_bounds__(BW_THREADS) bwd_linear_kernel(bwd_args a, int 
         }
         __syncthreads();
         // ---- Z = Gy E^T; GM k_i, GS k_i (B(x, o) = G[o][x]); GM^T e_i, GS^T e_i (B(o, x) = G[o][x])
-        block_gemm(n, n, d, Gyf, d, 1, E, 1, d, Z, b, 1.0f, false, gsh);
-        block_gemm(n, d, d, Kf, d, 1, GM, 1, d, GMk, d, 1.0f, false, gsh);
-        block_gemm(n, d, d, Kf, d, 1, GS, 1, d, GSk, d, 1.0f, false, gsh);
-        block_gemm(n, d, d, E, d, 1, GM, d, 1, GMtE, d, 1.0f, false, gsh);
-        block_gemm(n, d, d, E, d, 1, GS, d, 1, GStE, d, 1.0f, false, gsh);
+        gemm_(n, n, d, Gyf, d, 1, E, 1, d, Z, b, 1.0f, false, gsh);
+        gemm_(n, d, d, Kf, d, 1, GM, 1, d, GMk, d, 1.0f, false, gsh);
+        gemm_(n, d, d, Kf, d, 1, GS, 1, d, GSk, d, 1.0f, false, gsh);
+        gemm_(n, d, d, E, d, 1, GM, d, 1, GMtE, d, 1.0f, false, gsh);
+        gemm_(n, d, d, E, d, 1, GS, d, 1, GStE, d, 1.0f, false, gsh);
         // ---- lambda_e (first part): -(Gamma (.) QK)^T Gy   (A(i, t) = P_Q[t][i])
-        block_gemm(n, d, n, PQ, 1, b, Gyf, d, 1, LE, d, -1.0f, false, gsh);
+        gemm_(n, d, n, PQ, 1, b, Gyf, d, 1, LE, d, -1.0f, false, gsh);
         for (int idx = tid; idx < n * n; idx += BW_THREADS) {
             const int t = idx / n, i = idx % n;
             const float z = i <= t ? Z[t * b + i] : 0.0f;
@@ -286,11 +482,11 @@ __global__ void __launch_bounds__(BW_THREADS) bwd_linear_kernel(bwd_args a, int 
         }
         __syncthreads();
         // ---- dk = -(Gamma (.) Z)^T Q + lambda_r Mc (...) ; dq parts Gy Mc, Gy Sc, (Gamma (.) Z) K
-        block_gemm(n, d, n, PZ, 1, b, Qf, d, 1, DK, d, -1.0f, false, gsh);
-        block_gemm(n, d, d, LR, d, 1, Mc, d, 1, DK, d, 1.0f, true, gsh);
-        block_gemm(n, d, d, Gyf, d, 1, Mc, d, 1, DQ1, d, 1.0f, false, gsh);
-        block_gemm(n, d, d, Gyf, d, 1, Sc, d, 1, DQ2, d, 1.0f, false, gsh);
-        block_gemm(n, d, n, PZ, b, 1, Kf, d, 1, LE, d, 1.0f, false, gsh);
+        gemm_(n, d, n, PZ, 1, b, Qf, d, 1, DK, d, -1.0f, false, gsh);
+        gemm_(n, d, d, LR, d, 1, Mc, d, 1, DK, d, 1.0f, true, gsh);
+        gemm_(n, d, d, Gyf, d, 1, Mc, d, 1, DQ1, d, 1.0f, false, gsh);
+        gemm_(n, d, d, Gyf, d, 1, Sc, d, 1, DQ2, d, 1.0f, false, gsh);
+        gemm_(n, d, n, PZ, b, 1, Kf, d, 1, LE, d, 1.0f, false, gsh);
         for (int idx = tid; idx < n * d; idx += BW_THREADS) {
             const int i = idx / d;  // also the token t of dq
             a.dk[(unit * T + t0) * d + idx] = DK[idx] - s_gam[i] * GMtE[idx] + s_u[i] * GStE[idx];
@@ -357,8 +553,8 @@ __global__ void __launch_bounds__(BW_THREADS) bwd_linear_kernel(bwd_args a, int 
             }
         }
         // ---- dMc = sum_t A_t Gy_t q_t^T + sum_i lambda_r_i k_i^T (+ A GM below)   (A(o, t) = SG[t][o])
-        block_gemm(d, d, n, SG, 1, d, Qf, d, 1, TM, d, 1.0f, false, gsh);
-        block_gemm(d, d, n, LR, 1, d, Kf, d, 1, TM, d, 1.0f, true, gsh);
+        gemm_(d, d, n, SG, 1, d, Qf, d, 1, TM, d, 1.0f, false, gsh);
+        gemm_(d, d, n, LR, 1, d, Kf, d, 1, TM, d, 1.0f, true, gsh);
         for (int t = tid; t < n; t += BW_THREADS) {
             const long long g = unit * T + t0 + t;
             a.dalpha[g] = -s_da[t];  // a_t = 1 - alpha_t
@@ -369,7 +565,7 @@ __global__ void __launch_bounds__(BW_THREADS) bwd_linear_kernel(bwd_args a, int 
         for (int idx = tid; idx < n * d; idx += BW_THREADS) SG[idx] = sS[idx / d] * Gyf[idx];
         __syncthreads();
         // ---- dSc = - sum_t sigma_t Gy_t q_t^T (- sigma GM + B GS below)
-        block_gemm(d, d, n, SG, 1, d, Qf, d, 1, TS, d, -1.0f, false, gsh);
+        gemm_(d, d, n, SG, 1, d, Qf, d, 1, TS, d, -1.0f, false, gsh);
         // ---- the chunk-start state's adjoint becomes the previous chunk's (GM, GS), in place
         const float An = sA[n - 1], Bn = sB[n - 1], Sn = sS[n - 1];
         for (int idx = tid; idx < P; idx += BW_THREADS) {
@@ -383,6 +579,7 @@ __global__ void __launch_bounds__(BW_THREADS) bwd_linear_kernel(bwd_args a, int 
         a.dM0[unit * P + i] = GM[i];
         a.dS0[unit * P + i] = GS[i];
     }
+    if constexpr (TC) tg_teardown(tcx, a.status);
 }
 
 }  // namespace
@@ -422,7 +619,7 @@ __host__ __device__ inline size_t bwd_mlp_ws_floats(int d, int h, int b) {
     return 8 * (size_t)h * d + 18 * (size_t)b * d + 21 * (size_t)b * h + 10 * (size_t)b * b;
 }
 
-template <typename Tin>
+template <typename Tin, bool TC>
 __global__ void __launch_bounds__(BW_THREADS) bwd_mlp_kernel(bwd_args a, int d, int hd, int b, int c_mode) {
     __shared__ float s_a[BW_MAX_CHUNK], s_e[BW_MAX_CHUNK], s_b[BW_MAX_CHUNK], s_c[BW_MAX_CHUNK];
     __shared__ float sA[BW_MAX_CHUNK], sB[BW_MAX_CHUNK], sS[BW_MAX_CHUNK];
@@ -431,6 +628,14 @@ __global__ void __launch_bounds__(BW_THREADS) bwd_mlp_kernel(bwd_args a, int d, 
     __shared__ float s_da[BW_MAX_CHUNK], s_de[BW_MAX_CHUNK], s_db[BW_MAX_CHUNK], s_dc[BW_MAX_CHUNK];
     __shared__ float red[BW_THREADS / 32];
     __shared__ __align__(16) float gsh[GEMM_SMEM_FLOATS];
+    TcCtx tcx;
+    if constexpr (TC) tg_setup(tcx);
+    // every chunk-sized contraction: tcgen05 tf32 products or fp32 FFMA block GEMMs
+    auto gemm_ = [&](int M_, int N_, int K_, const float* A_, long long am_, long long ak_, const float* B_, long long bk_,
+                     long long bn_, float* C_, long long cm_, float alpha_, bool acc_, float* sh_) {
+        if constexpr (TC) tc_gemm(tcx, M_, N_, K_, A_, am_, ak_, B_, bk_, bn_, C_, cm_, alpha_, acc_);
+        else block_gemm(M_, N_, K_, A_, am_, ak_, B_, bk_, bn_, C_, cm_, alpha_, acc_, sh_);
+    };
 
     const long long unit = blockIdx.x;
     const int tid = threadIdx.x;
@@ -515,10 +720,10 @@ __global__ void __launch_bounds__(BW_THREADS) bwd_mlp_kernel(bwd_args a, int d, 
             }
         }
         // ---- F1: z = W1 k_i, W1 q_t, S1 q_t (B(x, j) = W1[j][x]); QK
-        block_gemm(n, hd, d, Kf, d, 1, W1c, 1, d, Zs, hd, 1.0f, false, gsh);
-        block_gemm(n, hd, d, Qf, d, 1, W1c, 1, d, W1q, hd, 1.0f, false, gsh);
-        block_gemm(n, hd, d, Qf, d, 1, S1c, 1, d, S1q, hd, 1.0f, false, gsh);
-        block_gemm(n, n, d, Qf, d, 1, Kf, 1, d, QK, b, 1.0f, false, gsh);
+        gemm_(n, hd, d, Kf, d, 1, W1c, 1, d, Zs, hd, 1.0f, false, gsh);
+        gemm_(n, hd, d, Qf, d, 1, W1c, 1, d, W1q, hd, 1.0f, false, gsh);
+        gemm_(n, hd, d, Qf, d, 1, S1c, 1, d, S1q, hd, 1.0f, false, gsh);
+        gemm_(n, n, d, Qf, d, 1, Kf, 1, d, QK, b, 1.0f, false, gsh);
         for (int idx = tid; idx < n * hd; idx += BW_THREADS) {
             const float z = Zs[idx], s = sig_f(z);
             Ak[idx] = z * s;
@@ -530,7 +735,7 @@ __global__ void __launch_bounds__(BW_THREADS) bwd_mlp_kernel(bwd_args a, int d, 
         }
         __syncthreads();
         // ---- F2: e = clip(2 (W2 a - v))   (B(j, o) = W2[o][j])
-        block_gemm(n, d, hd, Ak, hd, 1, W2c, 1, hd, R2, d, 1.0f, false, gsh);
+        gemm_(n, d, hd, Ak, hd, 1, W2c, 1, hd, R2, d, 1.0f, false, gsh);
         for (int idx = tid; idx < n * d; idx += BW_THREADS) {
             const float r2 = 2.0f * (R2[idx] - Vf[idx]);
             R2[idx] = r2;
@@ -538,11 +743,11 @@ __global__ void __launch_bounds__(BW_THREADS) bwd_mlp_kernel(bwd_args a, int d, 
         }
         __syncthreads();
         // ---- F3: p = W2^T e (B(o, j) = W2[o][j]), delta = p (.) silu'(z)
-        block_gemm(n, hd, d, E, d, 1, W2c, hd, 1, PP, hd, 1.0f, false, gsh);
+        gemm_(n, hd, d, E, d, 1, W2c, hd, 1, PP, hd, 1.0f, false, gsh);
         for (int idx = tid; idx < n * hd; idx += BW_THREADS) DL[idx] = PP[idx] * PH[idx];
         __syncthreads();
         // ---- F4: h_t = A_t W1 q_t - sigma_t S1 q_t - sum_{i<=t} Gamma QK delta_i; b_t = silu(h_t)
-        block_gemm(n, hd, n, PQ, b, 1, DL, hd, 1, C1, hd, 1.0f, false, gsh);
+        gemm_(n, hd, n, PQ, b, 1, DL, hd, 1, C1, hd, 1.0f, false, gsh);
         for (int idx = tid; idx < n * hd; idx += BW_THREADS) {
             const int t = idx / hd;
             const float hh = sA[t] * W1q[idx] - sS[t] * S1q[idx] - C1[idx];
@@ -552,10 +757,10 @@ __global__ void __launch_bounds__(BW_THREADS) bwd_mlp_kernel(bwd_args a, int d, 
         }
         __syncthreads();
         // ---- F5: AA = b a^T, Zy = Gy e^T; W2 b_t, S2 b_t
-        block_gemm(n, n, hd, Bt, hd, 1, Ak, 1, hd, AA, b, 1.0f, false, gsh);
-        block_gemm(n, n, d, Gyf, d, 1, E, 1, d, Zy, b, 1.0f, false, gsh);
-        block_gemm(n, d, hd, Bt, hd, 1, W2c, 1, hd, W2b, d, 1.0f, false, gsh);
-        block_gemm(n, d, hd, Bt, hd, 1, S2c, 1, hd, S2b, d, 1.0f, false, gsh);
+        gemm_(n, n, hd, Bt, hd, 1, Ak, 1, hd, AA, b, 1.0f, false, gsh);
+        gemm_(n, n, d, Gyf, d, 1, E, 1, d, Zy, b, 1.0f, false, gsh);
+        gemm_(n, d, hd, Bt, hd, 1, W2c, 1, hd, W2b, d, 1.0f, false, gsh);
+        gemm_(n, d, hd, Bt, hd, 1, S2c, 1, hd, S2b, d, 1.0f, false, gsh);
         for (int idx = tid; idx < n * n; idx += BW_THREADS) {
             const int t = idx / n, i = idx % n;
             const float zy = i <= t ? Zy[t * b + i] : 0.0f;
@@ -565,24 +770,24 @@ __global__ void __launch_bounds__(BW_THREADS) bwd_mlp_kernel(bwd_args a, int d, 
         }
         __syncthreads();
         // ---- B2: db_t = A_t W2^T Gy_t - sigma_t S2^T Gy_t - sum_i Gamma Zy a_i;  dh_t = db_t (.) silu'(h_t)
-        block_gemm(n, hd, d, Gyf, d, 1, W2c, hd, 1, GyW2, hd, 1.0f, false, gsh);
-        block_gemm(n, hd, d, Gyf, d, 1, S2c, hd, 1, GyS2, hd, 1.0f, false, gsh);
-        block_gemm(n, hd, n, PZy, b, 1, Ak, hd, 1, C1, hd, 1.0f, false, gsh);
+        gemm_(n, hd, d, Gyf, d, 1, W2c, hd, 1, GyW2, hd, 1.0f, false, gsh);
+        gemm_(n, hd, d, Gyf, d, 1, S2c, hd, 1, GyS2, hd, 1.0f, false, gsh);
+        gemm_(n, hd, n, PZy, b, 1, Ak, hd, 1, C1, hd, 1.0f, false, gsh);
         for (int idx = tid; idx < n * hd; idx += BW_THREADS) {
             const int t = idx / hd;
             DH[idx] = (sA[t] * GyW2[idx] - sS[t] * GyS2[idx] - C1[idx]) * PSI[idx];
         }
         // ---- B5: the end state's adjoints against the chunk's vectors
-        block_gemm(n, hd, d, Kf, d, 1, GW1, 1, d, G1k, hd, 1.0f, false, gsh);   // G1 k_i
-        block_gemm(n, hd, d, Kf, d, 1, GS1, 1, d, H1k, hd, 1.0f, false, gsh);   // H1 k_i
-        block_gemm(n, hd, d, E, d, 1, GW2, hd, 1, G2te, hd, 1.0f, false, gsh);  // G2^T e_i
-        block_gemm(n, hd, d, E, d, 1, GS2, hd, 1, H2te, hd, 1.0f, false, gsh);  // H2^T e_i
-        block_gemm(n, d, hd, Ak, hd, 1, GW2, 1, hd, G2a, d, 1.0f, false, gsh);  // G2 a_i
-        block_gemm(n, d, hd, Ak, hd, 1, GS2, 1, hd, H2a, d, 1.0f, false, gsh);  // H2 a_i
-        block_gemm(n, d, hd, DL, hd, 1, GW1, d, 1, G1td, d, 1.0f, false, gsh); // G1^T delta_i
-        block_gemm(n, d, hd, DL, hd, 1, GS1, d, 1, H1td, d, 1.0f, false, gsh); // H1^T delta_i
+        gemm_(n, hd, d, Kf, d, 1, GW1, 1, d, G1k, hd, 1.0f, false, gsh);   // G1 k_i
+        gemm_(n, hd, d, Kf, d, 1, GS1, 1, d, H1k, hd, 1.0f, false, gsh);   // H1 k_i
+        gemm_(n, hd, d, E, d, 1, GW2, hd, 1, G2te, hd, 1.0f, false, gsh);  // G2^T e_i
+        gemm_(n, hd, d, E, d, 1, GS2, hd, 1, H2te, hd, 1.0f, false, gsh);  // H2^T e_i
+        gemm_(n, d, hd, Ak, hd, 1, GW2, 1, hd, G2a, d, 1.0f, false, gsh);  // G2 a_i
+        gemm_(n, d, hd, Ak, hd, 1, GS2, 1, hd, H2a, d, 1.0f, false, gsh);  // H2 a_i
+        gemm_(n, d, hd, DL, hd, 1, GW1, d, 1, G1td, d, 1.0f, false, gsh); // G1^T delta_i
+        gemm_(n, d, hd, DL, hd, 1, GS1, d, 1, H1td, d, 1.0f, false, gsh); // H1^T delta_i
         // ---- B3: Zh = dh delta^T; B4: dq
-        block_gemm(n, n, hd, DH, hd, 1, DL, 1, hd, Zh, b, 1.0f, false, gsh);
+        gemm_(n, n, hd, DH, hd, 1, DL, 1, hd, Zh, b, 1.0f, false, gsh);
         for (int idx = tid; idx < n * n; idx += BW_THREADS) {
             const int t = idx / n, i = idx % n;
             const float zh = i <= t ? Zh[t * b + i] : 0.0f;
@@ -590,18 +795,18 @@ __global__ void __launch_bounds__(BW_THREADS) bwd_mlp_kernel(bwd_args a, int d, 
             PZh[t * b + i] = Gam[t * b + i] * zh;
         }
         __syncthreads();
-        block_gemm(n, d, hd, DH, hd, 1, W1c, d, 1, DHW1, d, 1.0f, false, gsh);
-        block_gemm(n, d, hd, DH, hd, 1, S1c, d, 1, DHS1, d, 1.0f, false, gsh);
-        block_gemm(n, d, n, PZh, b, 1, Kf, d, 1, PZhK, d, 1.0f, false, gsh);
+        gemm_(n, d, hd, DH, hd, 1, W1c, d, 1, DHW1, d, 1.0f, false, gsh);
+        gemm_(n, d, hd, DH, hd, 1, S1c, d, 1, DHS1, d, 1.0f, false, gsh);
+        gemm_(n, d, n, PZh, b, 1, Kf, d, 1, PZhK, d, 1.0f, false, gsh);
         for (int idx = tid; idx < n * d; idx += BW_THREADS) {
             const int t = idx / d;
             a.dq[(unit * T + t0) * d + idx] = sA[t] * DHW1[idx] - sS[t] * DHS1[idx] - PZhK[idx];
         }
         // ---- B6: ddelta -> dp and the silu'' part of dz; the direct parts of da, de, dk
-        block_gemm(n, hd, n, PQ, 1, b, DH, hd, 1, C1, hd, -1.0f, false, gsh);    // -sum_t Gamma QK dh_t
-        block_gemm(n, hd, n, PZy, 1, b, Bt, hd, 1, DAk, hd, -1.0f, false, gsh);  // -sum_t Gamma Zy b_t
-        block_gemm(n, d, n, PA, 1, b, Gyf, d, 1, DE, d, -1.0f, false, gsh);      // -sum_t Gamma AA Gy_t
-        block_gemm(n, d, n, PZh, 1, b, Qf, d, 1, DK, d, -1.0f, false, gsh);     // -sum_t Gamma Zh q_t
+        gemm_(n, hd, n, PQ, 1, b, DH, hd, 1, C1, hd, -1.0f, false, gsh);    // -sum_t Gamma QK dh_t
+        gemm_(n, hd, n, PZy, 1, b, Bt, hd, 1, DAk, hd, -1.0f, false, gsh);  // -sum_t Gamma Zy b_t
+        gemm_(n, d, n, PA, 1, b, Gyf, d, 1, DE, d, -1.0f, false, gsh);      // -sum_t Gamma AA Gy_t
+        gemm_(n, d, n, PZh, 1, b, Qf, d, 1, DK, d, -1.0f, false, gsh);     // -sum_t Gamma Zh q_t
         for (int idx = tid; idx < n * hd; idx += BW_THREADS) {
             const int i = idx / hd;
             const float dd = C1[idx] - s_gam[i] * G1k[idx] + s_u[i] * H1k[idx];
@@ -617,7 +822,7 @@ __global__ void __launch_bounds__(BW_THREADS) bwd_mlp_kernel(bwd_args a, int d, 
         }
         __syncthreads();
         // ---- B7: de += W2 dp (B(j, o) = W2[o][j]); dr = 2 [inside the clip] de; dv = -dr
-        block_gemm(n, d, hd, DP, hd, 1, W2c, 1, hd, DE, d, 1.0f, true, gsh);
+        gemm_(n, d, hd, DP, hd, 1, W2c, 1, hd, DE, d, 1.0f, true, gsh);
         for (int idx = tid; idx < n * d; idx += BW_THREADS) {
             const float r2 = R2[idx];
             const float dr = (r2 <= a.e_clip && r2 >= -a.e_clip) ? 2.0f * DE[idx] : 0.0f;
@@ -626,11 +831,11 @@ __global__ void __launch_bounds__(BW_THREADS) bwd_mlp_kernel(bwd_args a, int d, 
         }
         __syncthreads();
         // ---- B8: da += W2^T dr (B(o, j) = W2[o][j]); dz += da (.) silu'(z)
-        block_gemm(n, hd, d, R2, d, 1, W2c, hd, 1, DAk, hd, 1.0f, true, gsh);
+        gemm_(n, hd, d, R2, d, 1, W2c, hd, 1, DAk, hd, 1.0f, true, gsh);
         for (int idx = tid; idx < n * hd; idx += BW_THREADS) DZ[idx] = fmaf(DAk[idx], PH[idx], DZ[idx]);
         __syncthreads();
         // ---- B9: dk += W1^T dz (B(j, x) = W1[j][x])
-        block_gemm(n, d, hd, DZ, hd, 1, W1c, d, 1, DK, d, 1.0f, true, gsh);
+        gemm_(n, d, hd, DZ, hd, 1, W1c, d, 1, DK, d, 1.0f, true, gsh);
         for (int idx = tid; idx < n * d; idx += BW_THREADS) a.dk[(unit * T + t0) * d + idx] = DK[idx];
         // ---- B10: scalar adjoints of A, sigma and of the chunk-end gamma, u
         for (int t = tid; t < n; t += BW_THREADS) {
@@ -698,11 +903,11 @@ __global__ void __launch_bounds__(BW_THREADS) bwd_mlp_kernel(bwd_args a, int d, 
         }
         // ---- B11: the chunk's products for the chunk-start state's adjoints
         //      dW1 = sum_t A_t dh_t q_t^T + sum_i dz_i k_i^T; dW2 = sum_t A_t Gy_t b_t^T + sum_i (e_i dp_i^T + dr_i a_i^T)
-        block_gemm(hd, d, n, SGh, 1, hd, Qf, d, 1, TW1, d, 1.0f, false, gsh);
-        block_gemm(hd, d, n, DZ, 1, hd, Kf, d, 1, TW1, d, 1.0f, true, gsh);
-        block_gemm(d, hd, n, SGy, 1, d, Bt, hd, 1, TW2, hd, 1.0f, false, gsh);
-        block_gemm(d, hd, n, E, 1, d, DP, hd, 1, TW2, hd, 1.0f, true, gsh);
-        block_gemm(d, hd, n, R2, 1, d, Ak, hd, 1, TW2, hd, 1.0f, true, gsh);
+        gemm_(hd, d, n, SGh, 1, hd, Qf, d, 1, TW1, d, 1.0f, false, gsh);
+        gemm_(hd, d, n, DZ, 1, hd, Kf, d, 1, TW1, d, 1.0f, true, gsh);
+        gemm_(d, hd, n, SGy, 1, d, Bt, hd, 1, TW2, hd, 1.0f, false, gsh);
+        gemm_(d, hd, n, E, 1, d, DP, hd, 1, TW2, hd, 1.0f, true, gsh);
+        gemm_(d, hd, n, R2, 1, d, Ak, hd, 1, TW2, hd, 1.0f, true, gsh);
         for (int t = tid; t < n; t += BW_THREADS) {
             const long long g = unit * T + t0 + t;
             a.dalpha[g] = -s_da[t];
@@ -714,8 +919,8 @@ __global__ void __launch_bounds__(BW_THREADS) bwd_mlp_kernel(bwd_args a, int d, 
         for (int idx = tid; idx < n * d; idx += BW_THREADS) SGy[idx] = sS[idx / d] * Gyf[idx];
         __syncthreads();
         //      dS1 = - sum_t sigma_t dh_t q_t^T, dS2 = - sum_t sigma_t Gy_t b_t^T  (the state terms below)
-        block_gemm(hd, d, n, SGh, 1, hd, Qf, d, 1, TS1, d, -1.0f, false, gsh);
-        block_gemm(d, hd, n, SGy, 1, d, Bt, hd, 1, TS2, hd, -1.0f, false, gsh);
+        gemm_(hd, d, n, SGh, 1, hd, Qf, d, 1, TS1, d, -1.0f, false, gsh);
+        gemm_(d, hd, n, SGy, 1, d, Bt, hd, 1, TS2, hd, -1.0f, false, gsh);
         const float An = sA[n - 1], Bn = sB[n - 1], Sn = sS[n - 1];
         for (long long idx = tid; idx < HD; idx += BW_THREADS) {
             const float g1 = GW1[idx], h1 = GS1[idx], g2 = GW2[idx], h2 = GS2[idx];
@@ -730,6 +935,7 @@ __global__ void __launch_bounds__(BW_THREADS) bwd_mlp_kernel(bwd_args a, int d, 
         a.dM0[unit * P + i] = GW1[i];
         a.dS0[unit * P + i] = GS1[i];
     }
+    if constexpr (TC) tg_teardown(tcx, a.status);
 }
 
 }  // namespace
@@ -745,7 +951,10 @@ bool nm_bwd_supports(const nm_config& c) {
     return common && c.kind == NM_MLP2 && nm_layers(c) == 2 && c.hidden > 0 && c.hidden <= 1024 && c.hidden % 32 == 0;
 }
 
-cudaError_t nm_bwd_launch(const nm_config& c, const nm_bwd_call& call, cudaStream_t s) {
+namespace {
+
+template <bool TC>
+cudaError_t bwd_launch(const nm_config& c, const nm_bwd_call& call, int* status, cudaStream_t s) {
     bwd_args a;
     a.T = call.T;
     a.q = call.q; a.k = call.k; a.v = call.v;
@@ -758,16 +967,34 @@ cudaError_t nm_bwd_launch(const nm_config& c, const nm_bwd_call& call, cudaStrea
     a.ws = call.ws;
     a.ws_unit = nm_bwd_ws_floats(c);
     a.e_clip = call.e_clip;
+    a.status = status;
     const unsigned units = (unsigned)call.units;
+    const unsigned smem = TC ? TG_SMEM : 0;
+    auto run = [&](auto kern, auto... args) {
+        if (TC) {
+            cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            if (e != cudaSuccess) return e;
+        }
+        kern<<<units, BW_THREADS, smem, s>>>(a, args...);
+        return cudaGetLastError();
+    };
     if (c.kind == NM_MLP2) {
-        if (c.in_dtype == NM_BF16)
-            bwd_mlp_kernel<__nv_bfloat16><<<units, BW_THREADS, 0, s>>>(a, c.d, c.hidden, c.chunk, c.c_mode);
-        else
-            bwd_mlp_kernel<float><<<units, BW_THREADS, 0, s>>>(a, c.d, c.hidden, c.chunk, c.c_mode);
-    } else if (c.in_dtype == NM_BF16) {
-        bwd_linear_kernel<__nv_bfloat16><<<units, BW_THREADS, 0, s>>>(a, c.d, c.chunk, c.c_mode);
-    } else {
-        bwd_linear_kernel<float><<<units, BW_THREADS, 0, s>>>(a, c.d, c.chunk, c.c_mode);
+        if (c.in_dtype == NM_BF16) return run(bwd_mlp_kernel<__nv_bfloat16, TC>, c.d, c.hidden, c.chunk, c.c_mode);
+        return run(bwd_mlp_kernel<float, TC>, c.d, c.hidden, c.chunk, c.c_mode);
     }
-    return cudaGetLastError();
+    if (c.in_dtype == NM_BF16) return run(bwd_linear_kernel<__nv_bfloat16, TC>, c.d, c.chunk, c.c_mode);
+    return run(bwd_linear_kernel<float, TC>, c.d, c.chunk, c.c_mode);
+}
+
+}  // namespace
+
+// The reverse sweep with fp32 FFMA contractions.
+cudaError_t nm_bwd_launch(const nm_config& c, const nm_bwd_call& call, cudaStream_t s) {
+    return bwd_launch<false>(c, call, nullptr, s);
+}
+
+// The reverse sweep with tensor-core (tcgen05 kind::tf32) contractions; a
+// timed-out wait is reported in `status`.
+cudaError_t nm_bwd_launch_tc(const nm_config& c, const nm_bwd_call& call, int* status, cudaStream_t s) {
+    return bwd_launch<true>(c, call, status, s);
 }

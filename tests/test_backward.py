@@ -11,6 +11,12 @@ roundoff 6e-8) carried through ceil(T / chunk) chunks of the reverse sweep,
 whose adjoint recursion contracts by the forgetting factor, so a relative L2
 error of a few 1e-7 is expected (measured: 8e-8 to 1.3e-6 over these cases);
 the bound is 1e-5, ten times tighter than the fp32 forward's 1e-4.
+
+On a tensor-core handle (NM_PATH_TC) the reverse sweep's contractions run as
+tf32 tensor-core products (operands rounded to 11 significant bits, fp32
+accumulation): those cases are held to the bf16-input tolerances of the
+forward (relative L2 1e-2 on the state's gradients dM0, dS0, 2e-2 on the
+others).
 """
 import dataclasses
 
@@ -28,7 +34,22 @@ from _helpers import f64, rel_l2
 pytestmark = pytest.mark.gpu
 
 TOL = 1e-5
+TOL_TC = {"M0": 1e-2, "S0": 1e-2}  # every other gradient: 2e-2
 NAMES = ("q", "k", "v", "alpha", "eta", "beta", "M0", "S0")
+
+
+def _tol(path, name):
+    return TOL if path == nm.PATH_SIMT else TOL_TC.get(name, 2e-2)
+
+
+def _handle(path, *args, **kw):
+    """A handle on the given path, or a skip where that path is not built for the shape."""
+    try:
+        return nm.NeuralMemory(*args, path=path, **kw)
+    except nm.NMError as e:
+        if e.status == nm.NM_ERR_UNSUPPORTED and path == nm.PATH_TC:
+            pytest.skip("no tensor-core kernel for this shape")
+        raise
 
 
 def _case(wid, d, T, chunk, dtype, seed, c_mode, units=2):
@@ -54,11 +75,12 @@ def _case(wid, d, T, chunk, dtype, seed, c_mode, units=2):
     (2, 128, 130, 64, torch.bfloat16, nm.C_ONE_MINUS_BETA, 0.08),
     (2, 32, 75, 32, torch.float32, nm.C_PER_TOKEN, 0.05),
 ])
-def test_backward_linear_matches_reference(wid, d, T, chunk, dtype, c_mode, delta):
+@pytest.mark.parametrize("path", [nm.PATH_SIMT, nm.PATH_TC])
+def test_backward_linear_matches_reference(wid, d, T, chunk, dtype, c_mode, delta, path):
     wl, x, up = _case(wid, d, T, chunk, dtype, seed=200 + T, c_mode=c_mode)
     loss = nm.LOSS_L2 if delta is None else nm.LOSS_HUBER
-    mem = nm.NeuralMemory(nm.LINEAR, d, 0, chunk, in_dtype=dtype, c_mode=c_mode, loss=loss,
-                          huber_delta=0.0 if delta is None else delta)
+    mem = _handle(path, nm.LINEAR, d, 0, chunk, in_dtype=dtype, c_mode=c_mode, loss=loss,
+                  huber_delta=0.0 if delta is None else delta)
     got = mem.backward(x["q"], x["k"], x["v"], x["alpha"], x["eta"], x["beta"], x["M0"], x["S0"],
                        up["Gy"], up["GM"], up["GS"], c=x.get("c"))
     assert mem.synchronize() == nm.NM_OK
@@ -75,7 +97,7 @@ def test_backward_linear_matches_reference(wid, d, T, chunk, dtype, c_mode, delt
         for n_ in names:
             errs[(n_, u)] = rel_l2(f64(got[n_][0, u]), ref[n_])
     print({k_: "%.2e" % v_ for k_, v_ in errs.items()})
-    bad = {k_: v_ for k_, v_ in errs.items() if not v_ <= TOL}
+    bad = {k_: v_ for k_, v_ in errs.items() if not v_ <= _tol(path, k_[0])}
     assert not bad, bad
 
 
@@ -98,7 +120,8 @@ def test_backward_zero_tokens_passes_the_state_adjoints():
     (32, 64, 75, 16, torch.float32, nm.C_ONE, 0.3),
     (128, 256, 70, 64, torch.bfloat16, nm.C_ONE, None),
 ])
-def test_backward_mlp_matches_reference(d, hidden, T, chunk, dtype, c_mode, delta):
+@pytest.mark.parametrize("path", [nm.PATH_SIMT, nm.PATH_TC])
+def test_backward_mlp_matches_reference(d, hidden, T, chunk, dtype, c_mode, delta, path):
     """The 2-layer SiLU MLP memory (the workloads' recipe at these sizes, from
     random states W ~ N(0, 0.5 / fan_in), step eta halved)."""
     wl = dataclasses.replace(W.WORKLOADS[1], d=d, hidden=hidden, chunk=chunk, dtype=dtype).with_sizes(B=1, H=2, T=T)
@@ -113,8 +136,8 @@ def test_backward_mlp_matches_reference(d, hidden, T, chunk, dtype, c_mode, delt
           "GM": torch.randn((1, 2, wl.P), generator=g, device="cuda"),
           "GS": torch.randn((1, 2, wl.P), generator=g, device="cuda")}
     loss = nm.LOSS_L2 if delta is None else nm.LOSS_HUBER
-    mem = nm.NeuralMemory(nm.MLP2, d, hidden, chunk, in_dtype=dtype, c_mode=c_mode, loss=loss,
-                          huber_delta=0.0 if delta is None else delta)
+    mem = _handle(path, nm.MLP2, d, hidden, chunk, in_dtype=dtype, c_mode=c_mode, loss=loss,
+                  huber_delta=0.0 if delta is None else delta)
     got = mem.backward(x["q"], x["k"], x["v"], x["alpha"], x["eta"], x["beta"], x["M0"], x["S0"],
                        up["Gy"], up["GM"], up["GS"], c=x.get("c"))
     assert mem.synchronize() == nm.NM_OK
@@ -131,7 +154,7 @@ def test_backward_mlp_matches_reference(d, hidden, T, chunk, dtype, c_mode, delt
         for n_ in names:
             errs[(n_, u)] = rel_l2(f64(got[n_][0, u]), ref[n_])
     print({k_: "%.2e" % v_ for k_, v_ in errs.items()})
-    bad = {k_: v_ for k_, v_ in errs.items() if not v_ <= TOL}
+    bad = {k_: v_ for k_, v_ in errs.items() if not v_ <= _tol(path, k_[0])}
     assert not bad, bad
 
 
