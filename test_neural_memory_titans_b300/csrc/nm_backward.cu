@@ -80,6 +80,13 @@ __device__ __forceinline__ float momentum_c(int mode, float beta, const float* c
     return 1.0f;
 }
 
+// Sum over the warp, returned to every lane (all 32 lanes must call it).
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int sh = 16; sh > 0; sh >>= 1) v += __shfl_xor_sync(0xffffffffu, v, sh);
+    return v;
+}
+
 // Sum over the block (every thread passes its partial); the result is returned to all threads.
 __device__ float block_sum(float v, float* red) {
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -404,12 +411,28 @@ __global__ void __launch_bounds__(BW_THREADS) bwd_linear_kernel(bwd_args a, int 
         const float* Mc = a.ckpt + (unit * nch + c) * 2 * (long long)P;
         const float* Sc = Mc + P;
         __syncthreads();
-        // ---- the chunk's tokens and gates
-        for (int i = tid; i < n * d; i += BW_THREADS) {
-            Kf[i] = ld_f(k + t0 * d + i);
-            Qf[i] = ld_f(q + t0 * d + i);
-            Vf[i] = ld_f(v + t0 * d + i);
-            Gyf[i] = Gy_u[t0 * d + i];
+        // ---- the chunk's tokens and gates (four iterations' loads issued before their stores)
+        for (int i0 = tid; i0 < n * d; i0 += 4 * BW_THREADS) {
+            float kv[4], qv[4], vv[4], gv[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int i = i0 + j * BW_THREADS;
+                const bool in = i < n * d;
+                kv[j] = in ? ld_f(k + t0 * d + i) : 0.f;
+                qv[j] = in ? ld_f(q + t0 * d + i) : 0.f;
+                vv[j] = in ? ld_f(v + t0 * d + i) : 0.f;
+                gv[j] = in ? Gy_u[t0 * d + i] : 0.f;
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int i = i0 + j * BW_THREADS;
+                if (i < n * d) {
+                    Kf[i] = kv[j];
+                    Qf[i] = qv[j];
+                    Vf[i] = vv[j];
+                    Gyf[i] = gv[j];
+                }
+            }
         }
         for (int i = tid; i < n; i += BW_THREADS) {
             const float bt = be[t0 + i];
@@ -493,18 +516,31 @@ __global__ void __launch_bounds__(BW_THREADS) bwd_linear_kernel(bwd_args a, int 
             a.dq[(unit * T + t0) * d + idx] = sA[i] * DQ1[idx] - sS[i] * DQ2[idx] - LE[idx];
         }
         // ---- scalar adjoints of A, sigma (per token) and of the chunk-end gamma, u (per column)
-        for (int t = tid; t < n; t += BW_THREADS) {
+        // (four threads per token, each over every fourth feature, summed by shuffles)
+        for (int base = 0; base < n; base += BW_THREADS / 4) {
+            const int t = base + (tid >> 2), part = tid & 3;
             float ga = 0.f, gs = 0.f, hg = 0.f, hu = 0.f;
-            for (int o = 0; o < d; ++o) {
-                ga = fmaf(Gyf[t * d + o], Mq[t * d + o], ga);
-                gs = fmaf(Gyf[t * d + o], Sq[t * d + o], gs);
-                hg = fmaf(E[t * d + o], GMk[t * d + o], hg);
-                hu = fmaf(E[t * d + o], GSk[t * d + o], hu);
+            if (t < n) {
+                for (int o = part; o < d; o += 4) {
+                    ga = fmaf(Gyf[t * d + o], Mq[t * d + o], ga);
+                    gs = fmaf(Gyf[t * d + o], Sq[t * d + o], gs);
+                    hg = fmaf(E[t * d + o], GMk[t * d + o], hg);
+                    hu = fmaf(E[t * d + o], GSk[t * d + o], hu);
+                }
             }
-            s_gA[t] = ga;
-            s_gS[t] = -gs;
-            s_hg[t] = -hg;  // dL/dgamma_t (token t as a column i)
-            s_hu[t] = hu;   // dL/du_t
+#pragma unroll
+            for (int sh = 1; sh < 4; sh <<= 1) {
+                ga += __shfl_xor_sync(0xffffffffu, ga, sh);
+                gs += __shfl_xor_sync(0xffffffffu, gs, sh);
+                hg += __shfl_xor_sync(0xffffffffu, hg, sh);
+                hu += __shfl_xor_sync(0xffffffffu, hu, sh);
+            }
+            if (t < n && part == 0) {
+                s_gA[t] = ga;
+                s_gS[t] = -gs;
+                s_hg[t] = -hg;  // dL/dgamma_t (token t as a column i)
+                s_hu[t] = hu;   // dL/du_t
+            }
         }
         float pmm = 0.f, pms = 0.f, pss = 0.f;
         for (int i = tid; i < P; i += BW_THREADS) {
@@ -518,18 +554,50 @@ __global__ void __launch_bounds__(BW_THREADS) bwd_linear_kernel(bwd_args a, int 
         __syncthreads();
         // ---- reverse of the column recursions Gamma_{t,i} = a_t Gamma_{t-1,i} + eta_t u_{t,i},
         //      u_{t,i} = beta_t u_{t-1,i} (+ c_i at t = i)
-        for (int i = tid; i < n; i += BW_THREADS) {
+        // One column i per thread (chunks of at most BW_THREADS tokens).  The adjoints of a_t, eta_t, beta_t
+        // gather every column's step-t term: each warp sums its lanes' terms by shuffles and one lane adds them
+        // (steps run from the last token down to the warp's first column, the same for all its lanes); the
+        // column's values for 8 steps are loaded before those steps are computed.
+        {
+            const int i = tid, lane = tid & 31, wmin = tid & ~31;
+            const bool col = i < n;
             float cG = 0.f, cU = 0.f;  // a_{t+1} gGamma_{t+1}, beta_{t+1} gu_{t+1}
-            for (int t = n - 1; t >= i; --t) {
-                const float gG = -QK[t * b + i] * Z[t * b + i] + (t == n - 1 ? s_hg[i] : 0.0f) + cG;
-                const float gu = (t == n - 1 ? s_hu[i] : 0.0f) + s_e[t] * gG + cU;
-                const float Gprev = t > i ? Gam[(t - 1) * b + i] : 0.0f;
-                atomicAdd(&s_da[t], gG * Gprev);
-                atomicAdd(&s_de[t], gG * U[t * b + i]);
-                if (t > i) atomicAdd(&s_db[t], gu * U[(t - 1) * b + i]);
-                else atomicAdd(&s_dc[i], gu);
-                cG = s_a[t] * gG;
-                cU = s_b[t] * gu;
+            for (int th = n - 1; th >= wmin; th -= 8) {
+                float qk[8], zz[8], gp[8], u0[8], u1[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int t = th - j;
+                    const bool in = col && t >= i;
+                    qk[j] = in ? QK[t * b + i] : 0.0f;
+                    zz[j] = in ? Z[t * b + i] : 0.0f;
+                    gp[j] = in && t > i ? Gam[(t - 1) * b + i] : 0.0f;
+                    u0[j] = in ? U[t * b + i] : 0.0f;
+                    u1[j] = in && t > i ? U[(t - 1) * b + i] : 0.0f;
+                }
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int t = th - j;
+                    if (t < wmin) break;  // the same for the whole warp
+                    float ta = 0.f, te = 0.f, tb = 0.f;
+                    if (col && t >= i) {
+                        const float gG = -qk[j] * zz[j] + (t == n - 1 ? s_hg[i] : 0.0f) + cG;
+                        const float gu = (t == n - 1 ? s_hu[i] : 0.0f) + s_e[t] * gG + cU;
+                        ta = gG * gp[j];
+                        te = gG * u0[j];
+                        if (t > i) tb = gu * u1[j];
+                        else s_dc[i] += gu;
+                        cG = s_a[t] * gG;
+                        cU = s_b[t] * gu;
+                    }
+                    ta = warp_sum(ta);
+                    te = warp_sum(te);
+                    tb = warp_sum(tb);
+                    if (lane == 0) {
+                        atomicAdd(&s_da[t], ta);
+                        atomicAdd(&s_de[t], te);
+                        atomicAdd(&s_db[t], tb);
+                    }
+                }
             }
         }
         // ---- A_t Gy_t as rows, for dMc
@@ -684,11 +752,27 @@ __global__ void __launch_bounds__(BW_THREADS) bwd_mlp_kernel(bwd_args a, int d, 
         const float* S1c = W1c + P;
         const float* S2c = S1c + HD;
         __syncthreads();
-        for (int i = tid; i < n * d; i += BW_THREADS) {
-            Kf[i] = ld_f(k + t0 * d + i);
-            Qf[i] = ld_f(q + t0 * d + i);
-            Vf[i] = ld_f(v + t0 * d + i);
-            Gyf[i] = Gy_u[t0 * d + i];
+        for (int i0 = tid; i0 < n * d; i0 += 4 * BW_THREADS) {  // four iterations' loads before their stores
+            float kv[4], qv[4], vv[4], gv[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int i = i0 + j * BW_THREADS;
+                const bool in = i < n * d;
+                kv[j] = in ? ld_f(k + t0 * d + i) : 0.f;
+                qv[j] = in ? ld_f(q + t0 * d + i) : 0.f;
+                vv[j] = in ? ld_f(v + t0 * d + i) : 0.f;
+                gv[j] = in ? Gy_u[t0 * d + i] : 0.f;
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int i = i0 + j * BW_THREADS;
+                if (i < n * d) {
+                    Kf[i] = kv[j];
+                    Qf[i] = qv[j];
+                    Vf[i] = vv[j];
+                    Gyf[i] = gv[j];
+                }
+            }
         }
         for (int i = tid; i < n; i += BW_THREADS) {
             const float bt = be[t0 + i];
@@ -838,24 +922,37 @@ __global__ void __launch_bounds__(BW_THREADS) bwd_mlp_kernel(bwd_args a, int d, 
         gemm_(n, d, hd, DZ, hd, 1, W1c, d, 1, DK, d, 1.0f, true, gsh);
         for (int idx = tid; idx < n * d; idx += BW_THREADS) a.dk[(unit * T + t0) * d + idx] = DK[idx];
         // ---- B10: scalar adjoints of A, sigma and of the chunk-end gamma, u
-        for (int t = tid; t < n; t += BW_THREADS) {
+        // (four threads per token, each over every fourth feature, summed by shuffles)
+        for (int base = 0; base < n; base += BW_THREADS / 4) {
+            const int t = base + (tid >> 2), part = tid & 3;
             float ga = 0.f, gs = 0.f, hg = 0.f, hu = 0.f;
-            for (int o = 0; o < d; ++o) {
-                ga = fmaf(Gyf[t * d + o], W2b[t * d + o], ga);
-                gs = fmaf(Gyf[t * d + o], S2b[t * d + o], gs);
-                hg = fmaf(E[t * d + o], G2a[t * d + o], hg);
-                hu = fmaf(E[t * d + o], H2a[t * d + o], hu);
+            if (t < n) {
+                for (int o = part; o < d; o += 4) {
+                    ga = fmaf(Gyf[t * d + o], W2b[t * d + o], ga);
+                    gs = fmaf(Gyf[t * d + o], S2b[t * d + o], gs);
+                    hg = fmaf(E[t * d + o], G2a[t * d + o], hg);
+                    hu = fmaf(E[t * d + o], H2a[t * d + o], hu);
+                }
+                for (int j = part; j < hd; j += 4) {
+                    ga = fmaf(DH[t * hd + j], W1q[t * hd + j], ga);
+                    gs = fmaf(DH[t * hd + j], S1q[t * hd + j], gs);
+                    hg = fmaf(DL[t * hd + j], G1k[t * hd + j], hg);
+                    hu = fmaf(DL[t * hd + j], H1k[t * hd + j], hu);
+                }
             }
-            for (int j = 0; j < hd; ++j) {
-                ga = fmaf(DH[t * hd + j], W1q[t * hd + j], ga);
-                gs = fmaf(DH[t * hd + j], S1q[t * hd + j], gs);
-                hg = fmaf(DL[t * hd + j], G1k[t * hd + j], hg);
-                hu = fmaf(DL[t * hd + j], H1k[t * hd + j], hu);
+#pragma unroll
+            for (int sh = 1; sh < 4; sh <<= 1) {
+                ga += __shfl_xor_sync(0xffffffffu, ga, sh);
+                gs += __shfl_xor_sync(0xffffffffu, gs, sh);
+                hg += __shfl_xor_sync(0xffffffffu, hg, sh);
+                hu += __shfl_xor_sync(0xffffffffu, hu, sh);
             }
-            s_gA[t] = ga;
-            s_gS[t] = -gs;
-            s_hg[t] = -hg;
-            s_hu[t] = hu;
+            if (t < n && part == 0) {
+                s_gA[t] = ga;
+                s_gS[t] = -gs;
+                s_hg[t] = -hg;
+                s_hu[t] = hu;
+            }
         }
         float pmm = 0.f, pms = 0.f, pss = 0.f;
         for (long long i = tid; i < P; i += BW_THREADS) {
@@ -867,19 +964,50 @@ __global__ void __launch_bounds__(BW_THREADS) bwd_mlp_kernel(bwd_args a, int d, 
         const float gms = block_sum(pms, red);
         const float gss = block_sum(pss, red);
         __syncthreads();
-        for (int i = tid; i < n; i += BW_THREADS) {
+        // One column i per thread; each warp sums its lanes' step-t terms by shuffles and one lane adds them
+        // (see the linear memory); the column's values for 8 steps are loaded before those steps are computed.
+        {
+            const int i = tid, lane = tid & 31, wmin = tid & ~31;
+            const bool col = i < n;
             float cG = 0.f, cU = 0.f;
-            for (int t = n - 1; t >= i; --t) {
-                const float gG = -(AA[t * b + i] * Zy[t * b + i] + QK[t * b + i] * Zh[t * b + i]) +
-                                 (t == n - 1 ? s_hg[i] : 0.0f) + cG;
-                const float gu = (t == n - 1 ? s_hu[i] : 0.0f) + s_e[t] * gG + cU;
-                const float Gprev = t > i ? Gam[(t - 1) * b + i] : 0.0f;
-                atomicAdd(&s_da[t], gG * Gprev);
-                atomicAdd(&s_de[t], gG * U[t * b + i]);
-                if (t > i) atomicAdd(&s_db[t], gu * U[(t - 1) * b + i]);
-                else atomicAdd(&s_dc[i], gu);
-                cG = s_a[t] * gG;
-                cU = s_b[t] * gu;
+            for (int th = n - 1; th >= wmin; th -= 8) {
+                float aa[8], zy[8], qk[8], zh[8], gp[8], u0[8], u1[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int t = th - j;
+                    const bool in = col && t >= i;
+                    aa[j] = in ? AA[t * b + i] : 0.0f;
+                    zy[j] = in ? Zy[t * b + i] : 0.0f;
+                    qk[j] = in ? QK[t * b + i] : 0.0f;
+                    zh[j] = in ? Zh[t * b + i] : 0.0f;
+                    gp[j] = in && t > i ? Gam[(t - 1) * b + i] : 0.0f;
+                    u0[j] = in ? U[t * b + i] : 0.0f;
+                    u1[j] = in && t > i ? U[(t - 1) * b + i] : 0.0f;
+                }
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int t = th - j;
+                    if (t < wmin) break;  // the same for the whole warp
+                    float ta = 0.f, te = 0.f, tb = 0.f;
+                    if (col && t >= i) {
+                        const float gG = -(aa[j] * zy[j] + qk[j] * zh[j]) + (t == n - 1 ? s_hg[i] : 0.0f) + cG;
+                        const float gu = (t == n - 1 ? s_hu[i] : 0.0f) + s_e[t] * gG + cU;
+                        ta = gG * gp[j];
+                        te = gG * u0[j];
+                        if (t > i) tb = gu * u1[j];
+                        else s_dc[i] += gu;
+                        cG = s_a[t] * gG;
+                        cU = s_b[t] * gu;
+                    }
+                    ta = warp_sum(ta);
+                    te = warp_sum(te);
+                    tb = warp_sum(tb);
+                    if (lane == 0) {
+                        atomicAdd(&s_da[t], ta);
+                        atomicAdd(&s_de[t], te);
+                        atomicAdd(&s_db[t], tb);
+                    }
+                }
             }
         }
         for (int idx = tid; idx < n * hd; idx += BW_THREADS) SGh[idx] = sA[idx / hd] * DH[idx];
