@@ -313,10 +313,9 @@ int nm_inject_missing_load(nm_handle_t h);
  *   Workspace: one file-scope device array of NM_NOALLOC_SCRATCH_BYTES,
  *   present on every GPU that loads this library until the process exits.
  *   A call needing more than that (B*H units of
- *   4*(2b^2 + 2b + 4bd + 4bh) bytes each for two layers; for L > 2 layers
- *   4*(2 r4(b^2) + 2 r4(b) + 4bd + (3L - 1)bh + 2P) with r4 rounding up to a
- *   multiple of 4 and P the parameter count) returns NM_ERR_TOO_LARGE with
- *   nothing launched.  Every call looks up the array's device address on the
+ *   4*(2 r4(b^2) + 2 r4(b) + 4bd + (3L - 1)bh + 2P) bytes each for an L-layer
+ *   memory (L = 2 by default), with r4 rounding up to a multiple of 4 and P
+ *   the parameter count) returns NM_ERR_TOO_LARGE with nothing launched.  Every call looks up the array's device address on the
  *   current device (cudaGetSymbolAddress); the first call on a device may load
  *   the library's module there, so make that first call before any stream
  *   capture.  The address is not cached, so calls stay correct after

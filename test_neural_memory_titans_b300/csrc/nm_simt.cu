@@ -195,227 +195,14 @@ cudaError_t launch_linear_d(const nm_config& c, const nm_args& a, cudaStream_t s
     }
 }
 
-// ----------------------------------------------------------------- MLP2
+// ----------------------------------------------------------------- MLP memories
 
 constexpr int MLP_THREADS = 512;
 constexpr int MLP_MAX_CHUNK = 256;
 
-__host__ __device__ inline size_t mlp_unit_floats(int d, int h, int b) {
-    return 2 * (size_t)b * b + 2 * (size_t)b + 4 * (size_t)b * d + 4 * (size_t)b * h;
-}
-
-template <typename Tin, typename Tout>
-__global__ void __launch_bounds__(MLP_THREADS) simt_mlp_kernel(nm_args a, int d, int hd, int chunk, int c_mode) {
-    __shared__ float sA[MLP_MAX_CHUNK], sB[MLP_MAX_CHUNK], sSg[MLP_MAX_CHUNK];
-    __shared__ float sa[MLP_MAX_CHUNK], se[MLP_MAX_CHUNK], sbt[MLP_MAX_CHUNK], sc[MLP_MAX_CHUNK];
-    const long long unit = blockIdx.x;
-    const int tid = threadIdx.x;
-    const int NT = blockDim.x;
-    const long long T = a.T;
-    const long long P = 2LL * hd * d;
-    const int b = chunk;
-
-    float* ws = (float*)a.scratch + unit * mlp_unit_floats(d, hd, b);
-    float* Gam = ws;                   // [b][b]   Gamma_{t,i}
-    float* ub = Gam + (size_t)b * b;   // [b]      u_{n-1,i}
-    float* gl = ub + b;                // [b]      Gamma_{n-1,i}
-    float* Kf = gl + b;                // [b][d]
-    float* Qf = Kf + (size_t)b * d;    // [b][d]
-    float* Vf = Qf + (size_t)b * d;    // [b][d]
-    float* E = Vf + (size_t)b * d;     // [b][d]   e_t = 2 (yhat_t - v_t)
-    float* Z = E + (size_t)b * d;      // [b][h]   W1 k_t
-    float* Ak = Z + (size_t)b * hd;    // [b][h]   silu(W1 k_t)
-    float* Dl = Ak + (size_t)b * hd;   // [b][h]   delta_t = (W2^T e_t) * silu'(z_t)
-    float* Aq = Dl + (size_t)b * hd;   // [b][h]   silu(W1_t q_t)
-    float* Pm = Aq + (size_t)b * hd;   // [b][b]   Gamma (.) (inner products)
-
-    const Tin* q = (const Tin*)a.q + unit * T * d;
-    const Tin* k = (const Tin*)a.k + unit * T * d;
-    const Tin* v = (const Tin*)a.v + unit * T * d;
-    const float* al = a.alpha + unit * T;
-    const float* et = a.eta + unit * T;
-    const float* be = a.beta + unit * T;
-    const float* cc = a.c ? a.c + unit * T : nullptr;
-    Tout* y = (Tout*)a.y + unit * T * d;
-    float* W1 = a.M_T + unit * P;        // [h][d]
-    float* W2 = W1 + (long long)hd * d;  // [d][h]
-    float* S1 = a.S_T + unit * P;
-    float* S2 = S1 + (long long)hd * d;
-    if (a.M_T != a.M0)
-        for (long long i = tid; i < P; i += NT) W1[i] = a.M0[unit * P + i];
-    if (a.S_T != a.S0)
-        for (long long i = tid; i < P; i += NT) S1[i] = a.S0[unit * P + i];
-    __syncthreads();
-
-    for (long long t0 = 0; t0 < T; t0 += b) {
-        const int n = (int)min((long long)b, T - t0);
-        if (a.ckpt) {  // the chunk-start state (W1 | W2, S1 | S2), for the backward pass
-            float* ck = a.ckpt + (unit * ((T + b - 1) / b) + t0 / b) * 2 * P;
-            for (long long i = tid; i < P; i += NT) {
-                ck[i] = W1[i];
-                ck[P + i] = S1[i];
-            }
-        }
-        for (int i = tid; i < n * d; i += NT) {
-            Kf[i] = ld_in(k + t0 * d + i);
-            Qf[i] = ld_in(q + t0 * d + i);
-            Vf[i] = ld_in(v + t0 * d + i);
-        }
-        for (int i = tid; i < n; i += NT) {
-            sa[i] = 1.0f - al[t0 + i];
-            se[i] = et[t0 + i];
-            sbt[i] = be[t0 + i];
-            sc[i] = momentum_coef(c_mode, be[t0 + i], cc, t0 + i);
-        }
-        __syncthreads();
-        // decay / momentum scan, one column i of Gamma per thread
-        for (int i = tid; i < n; i += NT) {
-            float u = sc[i];
-            float G = se[i] * u;
-            Gam[(size_t)i * b + i] = G;
-            for (int t = i + 1; t < n; ++t) {
-                u *= sbt[t];
-                G = fmaf(sa[t], G, se[t] * u);
-                Gam[(size_t)t * b + i] = G;
-            }
-            ub[i] = u;
-            gl[i] = G;
-        }
-        if (tid == 0) {
-            float A = 1.f, Bc = 1.f, sg = 0.f;
-            for (int t = 0; t < n; ++t) {
-                A *= sa[t];
-                Bc *= sbt[t];
-                sg = fmaf(sa[t], sg, se[t] * Bc);
-                sA[t] = A;
-                sB[t] = Bc;
-                sSg[t] = sg;
-            }
-        }
-        __syncthreads();
-        // key forward at W0: z = W1 k, a = silu(z)
-        for (int idx = tid; idx < n * hd; idx += NT) {
-            const int t = idx / hd, j = idx % hd;
-            float acc = 0.f;
-            for (int x = 0; x < d; ++x) acc = fmaf(Kf[t * d + x], W1[(long long)j * d + x], acc);
-            Z[idx] = acc;
-            Ak[idx] = silu_f(acc);
-        }
-        __syncthreads();
-        // e = 2 (W2 a - v), clipped for the Huber loss
-        for (int idx = tid; idx < n * d; idx += NT) {
-            const int t = idx / d, o = idx % d;
-            float acc = 0.f;
-            for (int j = 0; j < hd; ++j) acc = fmaf(Ak[t * hd + j], W2[(long long)o * hd + j], acc);
-            E[idx] = nm_clip_err(2.0f * (acc - Vf[idx]), a.e_clip);
-        }
-        __syncthreads();
-        // delta = (W2^T e) * silu'(z);  Pm = Gamma (.) (Q K^T), lower triangle
-        for (int idx = tid; idx < n * hd; idx += NT) {
-            const int t = idx / hd, j = idx % hd;
-            float acc = 0.f;
-            for (int o = 0; o < d; ++o) acc = fmaf(E[t * d + o], W2[(long long)o * hd + j], acc);
-            Dl[idx] = acc * dsilu_f(Z[idx]);
-        }
-        for (int idx = tid; idx < n * n; idx += NT) {
-            const int t = idx / n, i = idx % n;
-            float acc = 0.f;
-            if (i <= t) {
-                for (int x = 0; x < d; ++x) acc = fmaf(Qf[t * d + x], Kf[i * d + x], acc);
-                acc *= Gam[(size_t)t * b + i];
-            }
-            Pm[(size_t)t * b + i] = acc;
-        }
-        __syncthreads();
-        if (a.surprise) {
-            // surprise_t = ||(delta_t k_t^T, e_t a(k_t)^T)||_F
-            //            = sqrt(||delta_t||^2 ||k_t||^2 + ||e_t||^2 ||a(k_t)||^2), one thread per token
-            for (int t = tid; t < n; t += NT) {
-                float d2 = 0.f, a2 = 0.f, e2 = 0.f, k2 = 0.f;
-                for (int j0 = 0; j0 < hd; ++j0) {
-                    const int j = (j0 + t) % hd;  // rotated: conflict-free across the warp
-                    d2 = fmaf(Dl[t * hd + j], Dl[t * hd + j], d2);
-                    a2 = fmaf(Ak[t * hd + j], Ak[t * hd + j], a2);
-                }
-                for (int x0 = 0; x0 < d; ++x0) {
-                    const int x = (x0 + t) % d;
-                    e2 = fmaf(E[t * d + x], E[t * d + x], e2);
-                    k2 = fmaf(Kf[t * d + x], Kf[t * d + x], k2);
-                }
-                a.surprise[unit * T + t0 + t] = sqrtf(fmaf(d2, k2, e2 * a2));
-            }
-        }
-        // layer 1 at token t: A_t W1 q - sigma_t S1 q - sum_i Gamma_{t,i} (k_i.q) delta_i
-        for (int idx = tid; idx < n * hd; idx += NT) {
-            const int t = idx / hd, j = idx % hd;
-            float m1 = 0.f, s1 = 0.f, g = 0.f;
-            for (int x = 0; x < d; ++x) {
-                const float qx = Qf[t * d + x];
-                m1 = fmaf(qx, W1[(long long)j * d + x], m1);
-                s1 = fmaf(qx, S1[(long long)j * d + x], s1);
-            }
-            for (int i = 0; i <= t; ++i) g = fmaf(Pm[(size_t)t * b + i], Dl[i * hd + j], g);
-            Aq[idx] = silu_f(sA[t] * m1 - sSg[t] * s1 - g);
-        }
-        __syncthreads();
-        // Pm = Gamma (.) (Aq Ak^T)
-        for (int idx = tid; idx < n * n; idx += NT) {
-            const int t = idx / n, i = idx % n;
-            float acc = 0.f;
-            if (i <= t) {
-                for (int j = 0; j < hd; ++j) acc = fmaf(Aq[t * hd + j], Ak[i * hd + j], acc);
-                acc *= Gam[(size_t)t * b + i];
-            }
-            Pm[(size_t)t * b + i] = acc;
-        }
-        __syncthreads();
-        // layer 2 at token t: A_t W2 a - sigma_t S2 a - sum_i Gamma_{t,i} (a(k_i).a) e_i
-        for (int idx = tid; idx < n * d; idx += NT) {
-            const int t = idx / d, o = idx % d;
-            float m2 = 0.f, s2 = 0.f, g = 0.f;
-            for (int j = 0; j < hd; ++j) {
-                const float aj = Aq[t * hd + j];
-                m2 = fmaf(aj, W2[(long long)o * hd + j], m2);
-                s2 = fmaf(aj, S2[(long long)o * hd + j], s2);
-            }
-            for (int i = 0; i <= t; ++i) g = fmaf(Pm[(size_t)t * b + i], E[i * d + o], g);
-            if (a.y) st_out(y + (t0 + t) * d + o, nm_gated(a, y + (t0 + t) * d + o, sA[t] * m2 - sSg[t] * s2 - g));
-        }
-        __syncthreads();
-        // chunk-end state: W = A W0 - sigma S0 - sum_i Gamma_{n-1,i} g_i, S = B S0 + sum_i u_{n-1,i} g_i
-        const float An = sA[n - 1], Bn = sB[n - 1], sn = sSg[n - 1];
-        for (int idx = tid; idx < hd * d; idx += NT) {
-            const int j = idx / d, x = idx % d;
-            float gw = 0.f, gs = 0.f;
-            for (int i = 0; i < n; ++i) {
-                const float dk = Dl[i * hd + j] * Kf[i * d + x];
-                gw = fmaf(gl[i], dk, gw);
-                gs = fmaf(ub[i], dk, gs);
-            }
-            const float w = W1[idx], s1 = S1[idx];
-            W1[idx] = An * w - sn * s1 - gw;
-            S1[idx] = Bn * s1 + gs;
-        }
-        for (int idx = tid; idx < d * hd; idx += NT) {
-            const int o = idx / hd, j = idx % hd;
-            float gw = 0.f, gs = 0.f;
-            for (int i = 0; i < n; ++i) {
-                const float ea = E[i * d + o] * Ak[i * hd + j];
-                gw = fmaf(gl[i], ea, gw);
-                gs = fmaf(ub[i], ea, gs);
-            }
-            const float w = W2[idx], s2 = S2[idx];
-            W2[idx] = An * w - sn * s2 - gw;
-            S2[idx] = Bn * s2 + gs;
-        }
-        __syncthreads();
-    }
-}
-
-// ----------------------------------------------------------------- deeper MLP memories
-// M(x) = W_L silu(W_{L-1} ... silu(W1 x)), L >= 3 (the explainer's
-// "ニューラル長期メモリモジュール": an MLP of L_M >= 1 layers).  The chunked form of the
-// 2-layer kernel above, layer by layer: every token's gradient is taken at
+// M(x) = W_L silu(W_{L-1} ... silu(W1 x)), L >= 2 (the explainer's
+// "ニューラル長期メモリモジュール": an MLP of L_M >= 1 layers; the 2-layer memory is
+// L = 2).  The chunked form, layer by layer: every token's gradient is taken at
 // the chunk-start weights, g_{l,i} = delta_{l,i} x_{l-1,i}^T with x_0 = k_i
 // and delta_L = e_i, so each layer's weights after token t are
 // W_l(t) = A_t W_l - sigma_t S_l - sum_{i<=t} Gamma_{t,i} delta_{l,i} x_{l-1,i}^T,
@@ -482,6 +269,13 @@ __global__ void __launch_bounds__(MLP_THREADS) simt_deep_kernel(nm_args a, int d
 
     for (long long t0 = 0; t0 < T; t0 += b) {
         const int n = (int)min((long long)b, T - t0);
+        if (a.ckpt) {  // the chunk-start state (W1 .. W_L, then S), for the backward pass
+            float* ck = a.ckpt + (unit * ((T + b - 1) / b) + t0 / b) * 2 * P;
+            for (long long i = tid; i < P; i += NT) {
+                ck[i] = Mw[i];
+                ck[P + i] = Sw[i];
+            }
+        }
         for (int i = tid; i < n * d; i += NT) {
             Kf[i] = ld_in(k + t0 * d + i);
             Qf[i] = ld_in(q + t0 * d + i);
@@ -660,7 +454,7 @@ __global__ void __launch_bounds__(MLP_THREADS) simt_deep_kernel(nm_args a, int d
                 for (int c4 = 0; c4 < 4; ++c4) {
                     const float pre = sA[t] * mv[c4] - sSg[t] * sv[c4] - gv[c4];
                     if (l < L) rn[(size_t)t * out + j + c4] = silu_f(pre);
-                    else st_out(y + (t0 + t) * d + j + c4, nm_gated(a, y + (t0 + t) * d + j + c4, pre));
+                    else if (a.y) st_out(y + (t0 + t) * d + j + c4, nm_gated(a, y + (t0 + t) * d + j + c4, pre));
                 }
             }
             __syncthreads();
@@ -704,25 +498,18 @@ __global__ void __launch_bounds__(MLP_THREADS) simt_deep_kernel(nm_args a, int d
 
 template <typename Tin, typename Tout>
 cudaError_t launch_deep(const nm_config& c, const nm_args& a, cudaStream_t s) {
-    simt_deep_kernel<Tin, Tout><<<(unsigned)(a.B * a.H), MLP_THREADS, 0, s>>>(a, c.d, c.hidden, c.layers, c.chunk,
+    simt_deep_kernel<Tin, Tout><<<(unsigned)(a.B * a.H), MLP_THREADS, 0, s>>>(a, c.d, c.hidden, nm_layers(c), c.chunk,
                                                                             c.c_mode);
     return cudaGetLastError();
 }
 
-template <typename Tin, typename Tout>
-cudaError_t launch_mlp(const nm_config& c, const nm_args& a, cudaStream_t s) {
-    simt_mlp_kernel<Tin, Tout><<<(unsigned)(a.B * a.H), MLP_THREADS, 0, s>>>(a, c.d, c.hidden, c.chunk, c.c_mode);
-    return cudaGetLastError();
-}
 
 template <typename Tin>
 cudaError_t dispatch_out(const nm_config& c, const nm_args& a, cudaStream_t s) {
     if (c.kind == NM_LINEAR)
         return c.out_dtype == NM_BF16 ? launch_linear_d<Tin, __nv_bfloat16>(c, a, s)
                                       : launch_linear_d<Tin, float>(c, a, s);
-    if (nm_layers(c) > 2)
-        return c.out_dtype == NM_BF16 ? launch_deep<Tin, __nv_bfloat16>(c, a, s) : launch_deep<Tin, float>(c, a, s);
-    return c.out_dtype == NM_BF16 ? launch_mlp<Tin, __nv_bfloat16>(c, a, s) : launch_mlp<Tin, float>(c, a, s);
+    return c.out_dtype == NM_BF16 ? launch_deep<Tin, __nv_bfloat16>(c, a, s) : launch_deep<Tin, float>(c, a, s);
 }
 
 }  // namespace
@@ -737,9 +524,7 @@ bool nm_simt_supports(const nm_config& c) {
 
 size_t nm_simt_scratch_bytes(const nm_config& c, int B, int H) {
     if (c.kind == NM_LINEAR) return 0;
-    if (nm_layers(c) > 2)
-        return sizeof(float) * deep_unit_floats(c.d, c.hidden, c.chunk, nm_layers(c)) * (size_t)B * (size_t)H;
-    return sizeof(float) * mlp_unit_floats(c.d, c.hidden, c.chunk) * (size_t)B * (size_t)H;
+    return sizeof(float) * deep_unit_floats(c.d, c.hidden, c.chunk, nm_layers(c)) * (size_t)B * (size_t)H;
 }
 
 cudaError_t nm_simt_launch(const nm_config& c, const nm_args& a, cudaStream_t s, long long* launches) {

@@ -9,9 +9,8 @@ through the C ABI and require the result to equal nm_forward's bit for bit
 (a workspace-offset mistake that perturbs the result slightly would not pass
 a tolerance-free comparison): two calls in a row on different inputs (the
 second over the array left behind by the first), then a deeper (3-layer)
-memory, whose workspace per unit is laid out differently.  They also check
-that calls needing more than the array return NM_ERR_TOO_LARGE, for the two-
-and the three-layer sizes.
+memory.  They also check that calls needing more than the array return
+NM_ERR_TOO_LARGE, for the two- and the three-layer sizes.
 
 This file is named so that pytest collects it last.
 """
@@ -114,11 +113,8 @@ def _round4(n):
 @pytest.mark.parametrize("layers", [2, 3])
 def test_noalloc_rejects_calls_beyond_its_workspace(layers):
     d, hidden, b = 64, 256 if layers == 2 else 128, 64
-    if layers == 2:
-        per_unit = 4 * (2 * b ** 2 + 2 * b + 4 * b * d + 4 * b * hidden)
-    else:
-        P = nm.param_count(nm.MLP2, d, hidden, layers)
-        per_unit = 4 * (2 * _round4(b * b) + 2 * _round4(b) + 4 * b * d + (3 * layers - 1) * b * hidden + 2 * P)
+    P = nm.param_count(nm.MLP2, d, hidden, layers)
+    per_unit = 4 * (2 * _round4(b * b) + 2 * _round4(b) + 4 * b * d + (3 * layers - 1) * b * hidden + 2 * P)
     H = SCRATCH_BYTES // per_unit + 1
     w = W.WORKLOADS[1].with_sizes(B=1, H=H, T=1)
     x = W.make_inputs(w, "cuda", seed=3)
