@@ -37,9 +37,10 @@
 // epilogue r_l three times (plain, times A_t, times -sigma_t), the inner-product
 // epilogue -G, and the update epilogue, next to the fp32 state, W_l and S_l as
 // [o][i] and W_l as [i][o] for the backward.  A block of a product is then one
-// or two bulk copies (cp.async.bulk) into shared memory, issued by one thread,
-// which also issues the MMAs: the copies run up to 3 blocks ahead over a ring
-// of stages (full / empty mbarriers), and no thread stages operands.  The
+// or two bulk copies (cp.async.bulk) into shared memory, issued by a copy
+// thread (warp 0) while an MMA thread (warp 1) issues the products: the two
+// meet only at the full / empty mbarriers of a ring of 2 to 8 stages, the
+// copies run up to ns - 1 blocks ahead, and no thread stages operands.  The
 // scalings of the formula (A_t, -sigma_t, gamma_i, u_i) live in those copies,
 // so each of retrieval's three chains and each update adds into its
 // accumulator directly.  Transposes cost nothing extra: a thread that holds a
