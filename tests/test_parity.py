@@ -324,6 +324,35 @@ def test_forward_host_matches_device(wid, B, H, T, grouped):
         torch.testing.assert_close(a_, b_.cpu(), rtol=0, atol=0)
 
 
+def test_forward_host_deep_memory_matches_device():
+    """nm_forward_host with a deeper memory on the tensor cores: that kernel
+    keeps a per-unit workspace in the handle, so the host path runs it as one
+    launch (the grouped copy / compute overlap would share the workspace) and
+    must equal nm_forward bit for bit.  10.5 MB of q, k, v and y: a size at
+    which the host path would otherwise take the grouped overlap."""
+    d, hidden, layers, T = 64, 128, 3, 640
+    wl = dataclasses.replace(W.WORKLOADS[1], hidden=hidden, layers=layers).with_sizes(B=2, H=16, T=T)
+    x = W.make_inputs(wl, "cpu", seed=21)
+    x["eta"] *= 0.5
+    g = torch.Generator().manual_seed(22)
+    M0 = (0.5 / hidden) ** 0.5 * torch.randn((2, 16, wl.P), generator=g)
+    S0 = 0.1 * M0.flip(-1).contiguous()
+    mem = nm.NeuralMemory(nm.MLP2, d, hidden, 64, in_dtype=torch.bfloat16, layers=layers, path=nm.PATH_TC)
+    pin = lambda t: t.contiguous().pin_memory()
+    l0 = mem.launches
+    yh, Mh, Sh = mem.forward_host(pin(x["q"]), pin(x["k"]), pin(x["v"]), pin(x["alpha"]), pin(x["eta"]),
+                                  pin(x["beta"]), pin(M0), pin(S0))
+    assert mem.launches - l0 == 1
+    dev = lambda t: t.cuda()
+    yd, Md, Sd = mem.forward(dev(x["q"]), dev(x["k"]), dev(x["v"]), dev(x["alpha"]), dev(x["eta"]), dev(x["beta"]),
+                             dev(M0), dev(S0))
+    assert mem.synchronize() == nm.NM_OK
+    mem.close()
+    for a_, b_ in ((yh, yd), (Mh, Md), (Sh, Sd)):
+        assert torch.isfinite(a_.float()).all()
+        torch.testing.assert_close(a_, b_.cpu(), rtol=0, atol=0)
+
+
 @pytest.mark.parametrize("hidden", [128, 256])
 @pytest.mark.parametrize("T,eta_scale,state_scale", [(64, 1.0, 1.0), (100, 1.0, 1.0), (257, 0.5, 0.5),
                                                      (385, 0.5, 0.5)])
