@@ -67,8 +67,8 @@ NCU_TRAFFIC = {
                                            "d70d351ebd9b6b93", 4.178e9),
     "linear_d64_bf16_b1h8_t2097152_c256_seg65536": (("nm_tc_linear64.cu", "tc_common.cuh", "nm_internal.h"),
                                                     "cd0494a3b25f3211", 254.6e6),
-    "mlp_64x256_bf16_b4h8_t4096_c64_L3": (("nm_tc_deep.cu", "tc_common.cuh", "nm_internal.h"), "8340c6d6e7fd91c1",
-                                          8.446e9),
+    "mlp_64x256_bf16_b4h8_t4096_c64_L3": (("nm_tc_deep.cu", "tc_common.cuh", "nm_internal.h"), "f471c769b7e276b8",
+                                          8.442e9),
 }
 
 
