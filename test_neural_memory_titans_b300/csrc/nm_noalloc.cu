@@ -8,7 +8,7 @@
 // still own and pass every input and output buffer; what they cannot provide
 // is the per-unit workspace the fp32 FFMA MLP kernel needs for a chunk's
 // intermediates (keys' hidden activations, errors, backpropagated errors, the
-// b x b decay matrix).  This entry point runs that same kernel with its
+// b x b decay matrix, the chunk-start weights transposed).  This entry point runs that same kernel with its
 // workspace taken from one file-scope device array instead of a handle.
 //
 // The array is NM_NOALLOC_SCRATCH_BYTES (16 MiB) and lives on every GPU that
