@@ -83,3 +83,30 @@ def test_workload_overrides():
     assert short.segment == 0
     with pytest.raises(SystemExit):
         b.workload(_args(workload=2, layers=3))
+
+
+def test_roofline_takes_the_peak_of_the_products_operand_type():
+    """The 2-layer tensor-core kernels' products are bf16 (the measured bf16
+    peak); the deeper memory's are tf32 (that peak times 1.1 / 2.25, the
+    nominal dense tf32 / bf16 ratio of a B300); the fp32 FFMA path of an MLP
+    memory is still measured against the tensor roofline of the workload."""
+    b = _bench()
+    peaks = {"hbm_gbs": 6500.0, "bf16_tflops": 1750.0, "bf16_tflops_sustained": 1350.0}
+    wl1 = W.WORKLOADS[1]
+    r = b.roofline(wl1, 0.6, True, peaks, "measured", None)
+    assert r["bound"] == "tensor" and r["peak"] == 1750.0
+    assert r["frac"] == pytest.approx(b.algorithmic(wl1)["flops"] / 0.6e-3 / 1e12 / 1750.0, rel=1e-12)
+    wl3 = dataclasses.replace(W.WORKLOADS[1], layers=3)
+    r3 = b.roofline(wl3, 14.0, True, peaks, "measured", None)
+    assert r3["peak"] == pytest.approx(1750.0 * 1.1 / 2.25, rel=1e-12) and "tf32" in r3["peak_source"]
+    assert r3["frac"] == pytest.approx(r3["achieved"] / r3["peak"], rel=1e-12)
+    r3f = b.roofline(wl3, 147.0, False, peaks, "measured", None)
+    assert r3f["peak"] == 1750.0
+    r2 = b.roofline(W.WORKLOADS[2], 1.14, True, peaks, "measured", 2.17e9)
+    assert r2["bound"] == "hbm" and r2["peak"] == 6500.0 and r2["traffic"] == 2.17e9
+
+
+def test_deep_traffic_entry_names_the_deep_kernel_sources():
+    b = _bench()
+    files, digest, nbytes = b.NCU_TRAFFIC["mlp_64x256_bf16_b4h8_t4096_c64_L3"]
+    assert files[0] == "nm_tc_deep.cu" and len(digest) == 16 and nbytes > 0
