@@ -80,6 +80,37 @@ __device__ __forceinline__ float momentum_c(int mode, float beta, const float* c
     return 1.0f;
 }
 
+// Runs store(i, load(i)) for every i in [0, N) over the block, U indices per
+// thread at a time, the loads of all U issued before any store: the passes of
+// the sweep read and write the same per-unit workspace, so in a plain loop
+// each iteration's loads wait for the previous iteration's stores (a round
+// trip to L2 per iteration).  The kernels with the register-tiled FFMA
+// products take U = 1 (a plain loop): there a larger U costs spills (MLP
+// memory) or gains nothing (linear memory, measured at U = 2).
+template <int U, typename L, typename S>
+__device__ __forceinline__ void each(int N, L&& load, S&& store) {
+    using V = decltype(load(0));
+    for (int i0 = threadIdx.x; i0 < N; i0 += U * BW_THREADS) {
+        V v[U];
+#pragma unroll
+        for (int j = 0; j < U; ++j) {
+            const int i = i0 + j * BW_THREADS;
+            if (i < N) v[j] = load(i);
+        }
+#pragma unroll
+        for (int j = 0; j < U; ++j) {
+            const int i = i0 + j * BW_THREADS;
+            if (i < N) store(i, v[j]);
+        }
+    }
+}
+struct F6 {
+    float a, b, c, d, e, f;
+};
+struct F9 {
+    float a, b, c, d, e, f, g, h, k;
+};
+
 // Sum over the warp, returned to every lane (all 32 lanes must call it).
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
@@ -357,6 +388,7 @@ __global__ void __launch_bounds__(BW_THREADS) bwd_linear_kernel(bwd_args a, int 
     __shared__ __align__(16) float gsh[GEMM_SMEM_FLOATS];
     TcCtx tcx;
     if constexpr (TC) tg_setup(tcx);
+    constexpr int EU = TC ? 4 : 1;  // elementwise passes: indices batched per thread
     // every chunk-sized contraction: tcgen05 tf32 products or fp32 FFMA block GEMMs
     auto gemm_ = [&](int M_, int N_, int K_, const float* A_, long long am_, long long ak_, const float* B_, long long bk_,
                      long long bn_, float* C_, long long cm_, float alpha_, bool acc_, float* sh_) {
@@ -470,15 +502,17 @@ __global__ void __launch_bounds__(BW_THREADS) bwd_linear_kernel(bwd_args a, int 
         gemm_(n, d, d, Qf, d, 1, Sc, 1, d, Sq, d, 1.0f, false, gsh);
         gemm_(n, n, d, Qf, d, 1, Kf, 1, d, QK, b, 1.0f, false, gsh);
         // ---- e_i = clip(2 (Mc k_i - v_i)); P_Q = Gamma (.) QK (lower triangle)
-        for (int idx = tid; idx < n * d; idx += BW_THREADS) {
-            const float r2 = 2.0f * (LR[idx] - Vf[idx]);
-            LR[idx] = r2;
-            E[idx] = nm_clip_err(r2, a.e_clip);
-        }
-        for (int idx = tid; idx < n * n; idx += BW_THREADS) {
-            const int t = idx / n, i = idx % n;
-            PQ[t * b + i] = i <= t ? Gam[t * b + i] * QK[t * b + i] : 0.0f;
-        }
+        each<EU>(n * d, [&](int idx) { return make_float2(LR[idx], Vf[idx]); },
+              [&](int idx, float2 x) {
+                  const float r2 = 2.0f * (x.x - x.y);
+                  LR[idx] = r2;
+                  E[idx] = nm_clip_err(r2, a.e_clip);
+              });
+        each<EU>(n * n, [&](int idx) { const int t = idx / n, i = idx % n; return make_float2(Gam[t * b + i], QK[t * b + i]); },
+              [&](int idx, float2 x) {
+                  const int t = idx / n, i = idx % n;
+                  PQ[t * b + i] = i <= t ? x.x * x.y : 0.0f;
+              });
         __syncthreads();
         // ---- Z = Gy E^T; GM k_i, GS k_i (B(x, o) = G[o][x]); GM^T e_i, GS^T e_i (B(o, x) = G[o][x])
         gemm_(n, n, d, Gyf, d, 1, E, 1, d, Z, b, 1.0f, false, gsh);
@@ -488,21 +522,23 @@ __global__ void __launch_bounds__(BW_THREADS) bwd_linear_kernel(bwd_args a, int 
         gemm_(n, d, d, E, d, 1, GS, d, 1, GStE, d, 1.0f, false, gsh);
         // ---- lambda_e (first part): -(Gamma (.) QK)^T Gy   (A(i, t) = P_Q[t][i])
         gemm_(n, d, n, PQ, 1, b, Gyf, d, 1, LE, d, -1.0f, false, gsh);
-        for (int idx = tid; idx < n * n; idx += BW_THREADS) {
-            const int t = idx / n, i = idx % n;
-            const float z = i <= t ? Z[t * b + i] : 0.0f;
-            Z[t * b + i] = z;
-            PZ[t * b + i] = Gam[t * b + i] * z;
-        }
+        each<EU>(n * n, [&](int idx) { const int t = idx / n, i = idx % n; return make_float2(Z[t * b + i], Gam[t * b + i]); },
+              [&](int idx, float2 x) {
+                  const int t = idx / n, i = idx % n;
+                  const float z = i <= t ? x.x : 0.0f;
+                  Z[t * b + i] = z;
+                  PZ[t * b + i] = x.y * z;
+              });
         // ---- lambda_e = ... - gamma_i GM k_i + u_i GS k_i; lambda_r = 2 [inside the clip] lambda_e; dv = -lambda_r
-        for (int idx = tid; idx < n * d; idx += BW_THREADS) {
-            const int i = idx / d;
-            const float le = LE[idx] - s_gam[i] * GMk[idx] + s_u[i] * GSk[idx];
-            const float r2 = LR[idx];
-            const float lr = (r2 <= a.e_clip && r2 >= -a.e_clip) ? 2.0f * le : 0.0f;
-            LR[idx] = lr;
-            a.dv[(unit * T + t0) * d + idx] = -lr;
-        }
+        each<EU>(n * d, [&](int idx) { return make_float4(LE[idx], GMk[idx], GSk[idx], LR[idx]); },
+              [&](int idx, float4 x) {
+                  const int i = idx / d;
+                  const float le = x.x - s_gam[i] * x.y + s_u[i] * x.z;
+                  const float r2 = x.w;
+                  const float lr = (r2 <= a.e_clip && r2 >= -a.e_clip) ? 2.0f * le : 0.0f;
+                  LR[idx] = lr;
+                  a.dv[(unit * T + t0) * d + idx] = -lr;
+              });
         __syncthreads();
         // ---- dk = -(Gamma (.) Z)^T Q + lambda_r Mc (...) ; dq parts Gy Mc, Gy Sc, (Gamma (.) Z) K
         gemm_(n, d, n, PZ, 1, b, Qf, d, 1, DK, d, -1.0f, false, gsh);
@@ -510,11 +546,12 @@ __global__ void __launch_bounds__(BW_THREADS) bwd_linear_kernel(bwd_args a, int 
         gemm_(n, d, d, Gyf, d, 1, Mc, d, 1, DQ1, d, 1.0f, false, gsh);
         gemm_(n, d, d, Gyf, d, 1, Sc, d, 1, DQ2, d, 1.0f, false, gsh);
         gemm_(n, d, n, PZ, b, 1, Kf, d, 1, LE, d, 1.0f, false, gsh);
-        for (int idx = tid; idx < n * d; idx += BW_THREADS) {
-            const int i = idx / d;  // also the token t of dq
-            a.dk[(unit * T + t0) * d + idx] = DK[idx] - s_gam[i] * GMtE[idx] + s_u[i] * GStE[idx];
-            a.dq[(unit * T + t0) * d + idx] = sA[i] * DQ1[idx] - sS[i] * DQ2[idx] - LE[idx];
-        }
+        each<EU>(n * d, [&](int idx) { return F6{DK[idx], GMtE[idx], GStE[idx], DQ1[idx], DQ2[idx], LE[idx]}; },
+              [&](int idx, F6 x) {
+                  const int i = idx / d;  // also the token t of dq
+                  a.dk[(unit * T + t0) * d + idx] = x.a - s_gam[i] * x.b + s_u[i] * x.c;
+                  a.dq[(unit * T + t0) * d + idx] = sA[i] * x.d - sS[i] * x.e - x.f;
+              });
         // ---- scalar adjoints of A, sigma (per token) and of the chunk-end gamma, u (per column)
         // (four threads per token, each over every fourth feature, summed by shuffles)
         for (int base = 0; base < n; base += BW_THREADS / 4) {
@@ -601,7 +638,7 @@ __global__ void __launch_bounds__(BW_THREADS) bwd_linear_kernel(bwd_args a, int 
             }
         }
         // ---- A_t Gy_t as rows, for dMc
-        for (int idx = tid; idx < n * d; idx += BW_THREADS) SG[idx] = sA[idx / d] * Gyf[idx];
+        each<EU>(n * d, [&](int idx) { return Gyf[idx]; }, [&](int idx, float g) { SG[idx] = sA[idx / d] * g; });
         __syncthreads();
         // ---- reverse of A_t = a_t A_{t-1}, B_t = beta_t B_{t-1}, sigma_t = a_t sigma_{t-1} + eta_t B_t
         if (tid == 0) {
@@ -630,17 +667,17 @@ __global__ void __launch_bounds__(BW_THREADS) bwd_linear_kernel(bwd_args a, int 
             a.dbeta[g] = s_db[t] + (c_mode == NM_C_ONE_MINUS_BETA ? -s_dc[t] : 0.0f);
             if (a.dc) a.dc[g] = s_dc[t];
         }
-        for (int idx = tid; idx < n * d; idx += BW_THREADS) SG[idx] = sS[idx / d] * Gyf[idx];
+        each<EU>(n * d, [&](int idx) { return Gyf[idx]; }, [&](int idx, float g) { SG[idx] = sS[idx / d] * g; });
         __syncthreads();
         // ---- dSc = - sum_t sigma_t Gy_t q_t^T (- sigma GM + B GS below)
         gemm_(d, d, n, SG, 1, d, Qf, d, 1, TS, d, -1.0f, false, gsh);
         // ---- the chunk-start state's adjoint becomes the previous chunk's (GM, GS), in place
         const float An = sA[n - 1], Bn = sB[n - 1], Sn = sS[n - 1];
-        for (int idx = tid; idx < P; idx += BW_THREADS) {
-            const float gm = GM[idx], gs = GS[idx];
-            GS[idx] = TS[idx] - Sn * gm + Bn * gs;
-            GM[idx] = TM[idx] + An * gm;
-        }
+        each<EU>(P, [&](int idx) { return make_float4(GM[idx], GS[idx], TS[idx], TM[idx]); },
+              [&](int idx, float4 x) {
+                  GS[idx] = x.z - Sn * x.x + Bn * x.y;
+                  GM[idx] = x.w + An * x.x;
+              });
     }
     __syncthreads();
     for (int i = tid; i < P; i += BW_THREADS) {
@@ -698,6 +735,7 @@ __global__ void __launch_bounds__(BW_THREADS) bwd_mlp_kernel(bwd_args a, int d, 
     __shared__ __align__(16) float gsh[GEMM_SMEM_FLOATS];
     TcCtx tcx;
     if constexpr (TC) tg_setup(tcx);
+    constexpr int EU = TC ? 4 : 1;  // elementwise passes: indices batched per thread
     // every chunk-sized contraction: tcgen05 tf32 products or fp32 FFMA block GEMMs
     auto gemm_ = [&](int M_, int N_, int K_, const float* A_, long long am_, long long ak_, const float* B_, long long bk_,
                      long long bn_, float* C_, long long cm_, float alpha_, bool acc_, float* sh_) {
@@ -808,59 +846,67 @@ __global__ void __launch_bounds__(BW_THREADS) bwd_mlp_kernel(bwd_args a, int d, 
         gemm_(n, hd, d, Qf, d, 1, W1c, 1, d, W1q, hd, 1.0f, false, gsh);
         gemm_(n, hd, d, Qf, d, 1, S1c, 1, d, S1q, hd, 1.0f, false, gsh);
         gemm_(n, n, d, Qf, d, 1, Kf, 1, d, QK, b, 1.0f, false, gsh);
-        for (int idx = tid; idx < n * hd; idx += BW_THREADS) {
-            const float z = Zs[idx], s = sig_f(z);
-            Ak[idx] = z * s;
-            PH[idx] = s * (1.0f + z * (1.0f - s));
-        }
-        for (int idx = tid; idx < n * n; idx += BW_THREADS) {
-            const int t = idx / n, i = idx % n;
-            PQ[t * b + i] = i <= t ? Gam[t * b + i] * QK[t * b + i] : 0.0f;
-        }
+        each<EU>(n * hd, [&](int idx) { return Zs[idx]; },
+              [&](int idx, float z) {
+                  const float s = sig_f(z);
+                  Ak[idx] = z * s;
+                  PH[idx] = s * (1.0f + z * (1.0f - s));
+              });
+        each<EU>(n * n, [&](int idx) { const int t = idx / n, i = idx % n; return make_float2(Gam[t * b + i], QK[t * b + i]); },
+              [&](int idx, float2 x) {
+                  const int t = idx / n, i = idx % n;
+                  PQ[t * b + i] = i <= t ? x.x * x.y : 0.0f;
+              });
         __syncthreads();
         // ---- F2: e = clip(2 (W2 a - v))   (B(j, o) = W2[o][j])
         gemm_(n, d, hd, Ak, hd, 1, W2c, 1, hd, R2, d, 1.0f, false, gsh);
-        for (int idx = tid; idx < n * d; idx += BW_THREADS) {
-            const float r2 = 2.0f * (R2[idx] - Vf[idx]);
-            R2[idx] = r2;
-            E[idx] = nm_clip_err(r2, a.e_clip);
-        }
+        each<EU>(n * d, [&](int idx) { return make_float2(R2[idx], Vf[idx]); },
+              [&](int idx, float2 x) {
+                  const float r2 = 2.0f * (x.x - x.y);
+                  R2[idx] = r2;
+                  E[idx] = nm_clip_err(r2, a.e_clip);
+              });
         __syncthreads();
         // ---- F3: p = W2^T e (B(o, j) = W2[o][j]), delta = p (.) silu'(z)
         gemm_(n, hd, d, E, d, 1, W2c, hd, 1, PP, hd, 1.0f, false, gsh);
-        for (int idx = tid; idx < n * hd; idx += BW_THREADS) DL[idx] = PP[idx] * PH[idx];
+        each<EU>(n * hd, [&](int idx) { return make_float2(PP[idx], PH[idx]); },
+              [&](int idx, float2 x) { DL[idx] = x.x * x.y; });
         __syncthreads();
         // ---- F4: h_t = A_t W1 q_t - sigma_t S1 q_t - sum_{i<=t} Gamma QK delta_i; b_t = silu(h_t)
         gemm_(n, hd, n, PQ, b, 1, DL, hd, 1, C1, hd, 1.0f, false, gsh);
-        for (int idx = tid; idx < n * hd; idx += BW_THREADS) {
-            const int t = idx / hd;
-            const float hh = sA[t] * W1q[idx] - sS[t] * S1q[idx] - C1[idx];
-            const float s = sig_f(hh);
-            Bt[idx] = hh * s;
-            PSI[idx] = s * (1.0f + hh * (1.0f - s));
-        }
+        each<EU>(n * hd, [&](int idx) { return make_float3(W1q[idx], S1q[idx], C1[idx]); },
+              [&](int idx, float3 x) {
+                  const int t = idx / hd;
+                  const float hh = sA[t] * x.x - sS[t] * x.y - x.z;
+                  const float s = sig_f(hh);
+                  Bt[idx] = hh * s;
+                  PSI[idx] = s * (1.0f + hh * (1.0f - s));
+              });
         __syncthreads();
         // ---- F5: AA = b a^T, Zy = Gy e^T; W2 b_t, S2 b_t
         gemm_(n, n, hd, Bt, hd, 1, Ak, 1, hd, AA, b, 1.0f, false, gsh);
         gemm_(n, n, d, Gyf, d, 1, E, 1, d, Zy, b, 1.0f, false, gsh);
         gemm_(n, d, hd, Bt, hd, 1, W2c, 1, hd, W2b, d, 1.0f, false, gsh);
         gemm_(n, d, hd, Bt, hd, 1, S2c, 1, hd, S2b, d, 1.0f, false, gsh);
-        for (int idx = tid; idx < n * n; idx += BW_THREADS) {
-            const int t = idx / n, i = idx % n;
-            const float zy = i <= t ? Zy[t * b + i] : 0.0f;
-            Zy[t * b + i] = zy;
-            PZy[t * b + i] = Gam[t * b + i] * zy;
-            PA[t * b + i] = i <= t ? Gam[t * b + i] * AA[t * b + i] : 0.0f;
-        }
+        each<EU>(n * n,
+              [&](int idx) { const int t = idx / n, i = idx % n; return make_float3(Zy[t * b + i], Gam[t * b + i], AA[t * b + i]); },
+              [&](int idx, float3 x) {
+                  const int t = idx / n, i = idx % n;
+                  const float zy = i <= t ? x.x : 0.0f;
+                  Zy[t * b + i] = zy;
+                  PZy[t * b + i] = x.y * zy;
+                  PA[t * b + i] = i <= t ? x.y * x.z : 0.0f;
+              });
         __syncthreads();
         // ---- B2: db_t = A_t W2^T Gy_t - sigma_t S2^T Gy_t - sum_i Gamma Zy a_i;  dh_t = db_t (.) silu'(h_t)
         gemm_(n, hd, d, Gyf, d, 1, W2c, hd, 1, GyW2, hd, 1.0f, false, gsh);
         gemm_(n, hd, d, Gyf, d, 1, S2c, hd, 1, GyS2, hd, 1.0f, false, gsh);
         gemm_(n, hd, n, PZy, b, 1, Ak, hd, 1, C1, hd, 1.0f, false, gsh);
-        for (int idx = tid; idx < n * hd; idx += BW_THREADS) {
-            const int t = idx / hd;
-            DH[idx] = (sA[t] * GyW2[idx] - sS[t] * GyS2[idx] - C1[idx]) * PSI[idx];
-        }
+        each<EU>(n * hd, [&](int idx) { return make_float4(GyW2[idx], GyS2[idx], C1[idx], PSI[idx]); },
+              [&](int idx, float4 x) {
+                  const int t = idx / hd;
+                  DH[idx] = (sA[t] * x.x - sS[t] * x.y - x.z) * x.w;
+              });
         // ---- B5: the end state's adjoints against the chunk's vectors
         gemm_(n, hd, d, Kf, d, 1, GW1, 1, d, G1k, hd, 1.0f, false, gsh);   // G1 k_i
         gemm_(n, hd, d, Kf, d, 1, GS1, 1, d, H1k, hd, 1.0f, false, gsh);   // H1 k_i
@@ -872,55 +918,61 @@ __global__ void __launch_bounds__(BW_THREADS) bwd_mlp_kernel(bwd_args a, int d, 
         gemm_(n, d, hd, DL, hd, 1, GS1, d, 1, H1td, d, 1.0f, false, gsh); // H1^T delta_i
         // ---- B3: Zh = dh delta^T; B4: dq
         gemm_(n, n, hd, DH, hd, 1, DL, 1, hd, Zh, b, 1.0f, false, gsh);
-        for (int idx = tid; idx < n * n; idx += BW_THREADS) {
-            const int t = idx / n, i = idx % n;
-            const float zh = i <= t ? Zh[t * b + i] : 0.0f;
-            Zh[t * b + i] = zh;
-            PZh[t * b + i] = Gam[t * b + i] * zh;
-        }
+        each<EU>(n * n, [&](int idx) { const int t = idx / n, i = idx % n; return make_float2(Zh[t * b + i], Gam[t * b + i]); },
+              [&](int idx, float2 x) {
+                  const int t = idx / n, i = idx % n;
+                  const float zh = i <= t ? x.x : 0.0f;
+                  Zh[t * b + i] = zh;
+                  PZh[t * b + i] = x.y * zh;
+              });
         __syncthreads();
         gemm_(n, d, hd, DH, hd, 1, W1c, d, 1, DHW1, d, 1.0f, false, gsh);
         gemm_(n, d, hd, DH, hd, 1, S1c, d, 1, DHS1, d, 1.0f, false, gsh);
         gemm_(n, d, n, PZh, b, 1, Kf, d, 1, PZhK, d, 1.0f, false, gsh);
-        for (int idx = tid; idx < n * d; idx += BW_THREADS) {
-            const int t = idx / d;
-            a.dq[(unit * T + t0) * d + idx] = sA[t] * DHW1[idx] - sS[t] * DHS1[idx] - PZhK[idx];
-        }
+        each<EU>(n * d, [&](int idx) { return make_float3(DHW1[idx], DHS1[idx], PZhK[idx]); },
+              [&](int idx, float3 x) {
+                  const int t = idx / d;
+                  a.dq[(unit * T + t0) * d + idx] = sA[t] * x.x - sS[t] * x.y - x.z;
+              });
         // ---- B6: ddelta -> dp and the silu'' part of dz; the direct parts of da, de, dk
         gemm_(n, hd, n, PQ, 1, b, DH, hd, 1, C1, hd, -1.0f, false, gsh);    // -sum_t Gamma QK dh_t
         gemm_(n, hd, n, PZy, 1, b, Bt, hd, 1, DAk, hd, -1.0f, false, gsh);  // -sum_t Gamma Zy b_t
         gemm_(n, d, n, PA, 1, b, Gyf, d, 1, DE, d, -1.0f, false, gsh);      // -sum_t Gamma AA Gy_t
         gemm_(n, d, n, PZh, 1, b, Qf, d, 1, DK, d, -1.0f, false, gsh);     // -sum_t Gamma Zh q_t
-        for (int idx = tid; idx < n * hd; idx += BW_THREADS) {
-            const int i = idx / hd;
-            const float dd = C1[idx] - s_gam[i] * G1k[idx] + s_u[i] * H1k[idx];
-            const float z = Zs[idx], s = sig_f(z);
-            DP[idx] = dd * PH[idx];
-            DZ[idx] = dd * PP[idx] * (s * (1.0f - s) * (2.0f + z * (1.0f - 2.0f * s)));
-            DAk[idx] += -s_gam[i] * G2te[idx] + s_u[i] * H2te[idx];
-        }
-        for (int idx = tid; idx < n * d; idx += BW_THREADS) {
-            const int i = idx / d;
-            DE[idx] += -s_gam[i] * G2a[idx] + s_u[i] * H2a[idx];
-            DK[idx] += -s_gam[i] * G1td[idx] + s_u[i] * H1td[idx];
-        }
+        each<EU>(n * hd, [&](int idx) { return F9{C1[idx], G1k[idx], H1k[idx], Zs[idx], PH[idx], PP[idx], DAk[idx], G2te[idx], H2te[idx]}; },
+              [&](int idx, F9 x) {
+                  const int i = idx / hd;
+                  const float dd = x.a - s_gam[i] * x.b + s_u[i] * x.c;
+                  const float z = x.d, s = sig_f(z);
+                  DP[idx] = dd * x.e;
+                  DZ[idx] = dd * x.f * (s * (1.0f - s) * (2.0f + z * (1.0f - 2.0f * s)));
+                  DAk[idx] = x.g + (-s_gam[i] * x.h + s_u[i] * x.k);
+              });
+        each<EU>(n * d, [&](int idx) { return F6{DE[idx], G2a[idx], H2a[idx], DK[idx], G1td[idx], H1td[idx]}; },
+              [&](int idx, F6 x) {
+                  const int i = idx / d;
+                  DE[idx] = x.a + (-s_gam[i] * x.b + s_u[i] * x.c);
+                  DK[idx] = x.d + (-s_gam[i] * x.e + s_u[i] * x.f);
+              });
         __syncthreads();
         // ---- B7: de += W2 dp (B(j, o) = W2[o][j]); dr = 2 [inside the clip] de; dv = -dr
         gemm_(n, d, hd, DP, hd, 1, W2c, 1, hd, DE, d, 1.0f, true, gsh);
-        for (int idx = tid; idx < n * d; idx += BW_THREADS) {
-            const float r2 = R2[idx];
-            const float dr = (r2 <= a.e_clip && r2 >= -a.e_clip) ? 2.0f * DE[idx] : 0.0f;
-            R2[idx] = dr;
-            a.dv[(unit * T + t0) * d + idx] = -dr;
-        }
+        each<EU>(n * d, [&](int idx) { return make_float2(R2[idx], DE[idx]); },
+              [&](int idx, float2 x) {
+                  const float r2 = x.x;
+                  const float dr = (r2 <= a.e_clip && r2 >= -a.e_clip) ? 2.0f * x.y : 0.0f;
+                  R2[idx] = dr;
+                  a.dv[(unit * T + t0) * d + idx] = -dr;
+              });
         __syncthreads();
         // ---- B8: da += W2^T dr (B(o, j) = W2[o][j]); dz += da (.) silu'(z)
         gemm_(n, hd, d, R2, d, 1, W2c, hd, 1, DAk, hd, 1.0f, true, gsh);
-        for (int idx = tid; idx < n * hd; idx += BW_THREADS) DZ[idx] = fmaf(DAk[idx], PH[idx], DZ[idx]);
+        each<EU>(n * hd, [&](int idx) { return make_float3(DAk[idx], PH[idx], DZ[idx]); },
+              [&](int idx, float3 x) { DZ[idx] = fmaf(x.x, x.y, x.z); });
         __syncthreads();
         // ---- B9: dk += W1^T dz (B(j, x) = W1[j][x])
         gemm_(n, d, hd, DZ, hd, 1, W1c, d, 1, DK, d, 1.0f, true, gsh);
-        for (int idx = tid; idx < n * d; idx += BW_THREADS) a.dk[(unit * T + t0) * d + idx] = DK[idx];
+        each<EU>(n * d, [&](int idx) { return DK[idx]; }, [&](int idx, float x) { a.dk[(unit * T + t0) * d + idx] = x; });
         // ---- B10: scalar adjoints of A, sigma and of the chunk-end gamma, u
         // (four threads per token, each over every fourth feature, summed by shuffles)
         for (int base = 0; base < n; base += BW_THREADS / 4) {
@@ -1010,8 +1062,8 @@ __global__ void __launch_bounds__(BW_THREADS) bwd_mlp_kernel(bwd_args a, int d, 
                 }
             }
         }
-        for (int idx = tid; idx < n * hd; idx += BW_THREADS) SGh[idx] = sA[idx / hd] * DH[idx];
-        for (int idx = tid; idx < n * d; idx += BW_THREADS) SGy[idx] = sA[idx / d] * Gyf[idx];
+        each<EU>(n * hd, [&](int idx) { return DH[idx]; }, [&](int idx, float g) { SGh[idx] = sA[idx / hd] * g; });
+        each<EU>(n * d, [&](int idx) { return Gyf[idx]; }, [&](int idx, float g) { SGy[idx] = sA[idx / d] * g; });
         __syncthreads();
         if (tid == 0) {
             float cA = 0.f, cS = 0.f, cB = 0.f;
@@ -1043,8 +1095,8 @@ __global__ void __launch_bounds__(BW_THREADS) bwd_mlp_kernel(bwd_args a, int d, 
             a.dbeta[g] = s_db[t] + (c_mode == NM_C_ONE_MINUS_BETA ? -s_dc[t] : 0.0f);
             if (a.dc) a.dc[g] = s_dc[t];
         }
-        for (int idx = tid; idx < n * hd; idx += BW_THREADS) SGh[idx] = sS[idx / hd] * DH[idx];
-        for (int idx = tid; idx < n * d; idx += BW_THREADS) SGy[idx] = sS[idx / d] * Gyf[idx];
+        each<EU>(n * hd, [&](int idx) { return DH[idx]; }, [&](int idx, float g) { SGh[idx] = sS[idx / hd] * g; });
+        each<EU>(n * d, [&](int idx) { return Gyf[idx]; }, [&](int idx, float g) { SGy[idx] = sS[idx / d] * g; });
         __syncthreads();
         //      dS1 = - sum_t sigma_t dh_t q_t^T, dS2 = - sum_t sigma_t Gy_t b_t^T  (the state terms below)
         gemm_(hd, d, n, SGh, 1, hd, Qf, d, 1, TS1, d, -1.0f, false, gsh);
