@@ -85,8 +85,8 @@ __device__ __forceinline__ float momentum_c(int mode, float beta, const float* c
 // the sweep read and write the same per-unit workspace, so in a plain loop
 // each iteration's loads wait for the previous iteration's stores (a round
 // trip to L2 per iteration).  The kernels with the register-tiled FFMA
-// products take U = 1 (a plain loop): there a larger U costs spills (MLP
-// memory) or gains nothing (linear memory, measured at U = 2).
+// products take a smaller U, as far as it costs no spills: 2 for the linear
+// memory, 1 (a plain loop) for the MLP memory.
 template <int U, typename L, typename S>
 __device__ __forceinline__ void each(int N, L&& load, S&& store) {
     using V = decltype(load(0));
@@ -388,7 +388,7 @@ __global__ void __launch_bounds__(BW_THREADS) bwd_linear_kernel(bwd_args a, int 
     __shared__ __align__(16) float gsh[GEMM_SMEM_FLOATS];
     TcCtx tcx;
     if constexpr (TC) tg_setup(tcx);
-    constexpr int EU = TC ? 4 : 1;  // elementwise passes: indices batched per thread
+    constexpr int EU = TC ? 4 : 2;  // elementwise passes: indices batched per thread
     // every chunk-sized contraction: tcgen05 tf32 products or fp32 FFMA block GEMMs
     auto gemm_ = [&](int M_, int N_, int K_, const float* A_, long long am_, long long ak_, const float* B_, long long bk_,
                      long long bn_, float* C_, long long cm_, float alpha_, bool acc_, float* sh_) {
