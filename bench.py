@@ -61,8 +61,8 @@ METRIC = "memory-layer fwd tokens/sec (B*H*T/s) and % of roofline (TC FLOPs vs H
 NCU_TRAFFIC = {
     "mlp_64x256_bf16_b4h8_t4096_c64": (("nm_tc_mlp.cu", "tc_common.cuh", "nm_internal.h"), "810ad16e5ee50003",
                                        62.45e6),
-    "linear_d128_bf16_b8h16_t16384_c64": (("nm_tc_linear.cu", "tc_common.cuh", "nm_internal.h"), "f6f951c6577d621c",
-                                          2.173e9),
+    "linear_d128_bf16_b8h16_t16384_c64": (("nm_tc_linear.cu", "tc_common.cuh", "nm_internal.h"), "54eb102664576f30",
+                                          2.172e9),
     "mlp_128x512_bf16_b2h16_t131072_c64": (("nm_tc_mlp_wide.cu", "tc_common.cuh", "nm_internal.h"),
                                            "d70d351ebd9b6b93", 4.178e9),
     "linear_d64_bf16_b1h8_t2097152_c256_seg65536": (("nm_tc_linear64.cu", "tc_common.cuh", "nm_internal.h"),
@@ -535,7 +535,8 @@ def run_backward(args, rank, world, local_rank):
         peak = float(peaks["bf16_tflops"]) * TF32_PER_BF16
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
                 "traffic": None, "peak_source": peak_src + " (burst bf16 x 1.1/2.25, the nominal tf32 ratio)",
-                "kernel": "nm_backward (fp32 FFMA checkpointing forward + reverse sweep with tcgen05 tf32 contractions)"}
+                "kernel": "nm_backward (checkpointing forward, tcgen05 for the linear d=128 memory, else fp32 FFMA; "
+                          "reverse sweep with tcgen05 tf32 contractions)"}
     else:
         roof = {"bound": "alu", "achieved": achieved, "peak": FP32_PEAK_TFLOPS, "unit": "TFLOP/s",
                 "frac": achieved / FP32_PEAK_TFLOPS, "traffic": None,

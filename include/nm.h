@@ -210,7 +210,9 @@ int nm_forward_gated(nm_handle_t h, int B, int H, int T,
  *   a multiple of 32, chunk <= 256, fp32 or bf16 inputs, either loss); deeper
  *   MLP memories return NM_ERR_UNSUPPORTED.  The gradient is that of
  *   the chunked forward in fp32 arithmetic: the call first runs the forward
- *   once more on the fp32 FFMA kernel, recording every chunk's start state in
+ *   once more on the fp32 FFMA kernel (on an NM_PATH_TC handle of the linear
+ *   memory with d = 128, chunk 64, the tcgen05 forward kernel, whose states
+ *   carry its bf16 operand rounding), recording every chunk's start state in
  *   a handle-owned workspace (B*H*ceil(T/chunk)*2*P floats plus per-unit
  *   scratch; it grows on demand, so a first call at a larger size
  *   allocates), then sweeps the chunks from last to first.  The sweep's

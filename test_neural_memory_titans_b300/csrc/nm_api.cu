@@ -9,6 +9,7 @@
 
 // The backward pass's reverse sweep with tensor-core contractions (nm_backward.cu).
 cudaError_t nm_bwd_launch_tc(const nm_config& c, const nm_bwd_call& call, int* status, cudaStream_t s);
+bool nm_tc_supports_ckpt(const nm_config& c);  // (nm_tc.cu)
 
 namespace {
 
@@ -335,7 +336,10 @@ int nm_backward(nm_handle_t h, int B, int H, int T, const void* q, const void* k
     const size_t sc_b = up((size_t)units * nm_bwd_ws_floats(cfg) * sizeof(float));
     nm_config fc = cfg;
     fc.path = NM_PATH_SIMT;
-    const size_t fw_b = up(nm_simt_scratch_bytes(fc, B, H));  // the forward kernel's own workspace
+    // the checkpointing forward: on a tensor-core handle the tcgen05 kernel where one records checkpoints
+    // (its states carry the bf16-operand rounding of that path's forward), else the fp32 FFMA kernel
+    const bool tc_ckpt = cfg.path == NM_PATH_TC && nm_tc_supports_ckpt(cfg);
+    const size_t fw_b = tc_ckpt ? 0 : up(nm_simt_scratch_bytes(fc, B, H));  // the forward kernel's own workspace
     const size_t need = ck_b + fin_b + sc_b + fw_b;
     if (need > h->bwd_ws_bytes) {
         if (h->bwd_ws) cudaFree(h->bwd_ws);
@@ -353,7 +357,7 @@ int nm_backward(nm_handle_t h, int B, int H, int T, const void* q, const void* k
     float* scratch = (float*)(w + ck_b + fin_b);
     void* fw_scratch = fw_b ? (void*)(w + ck_b + fin_b + sc_b) : nullptr;
 
-    // the forward once more, on the fp32 FFMA kernel, recording each chunk's start state (y is not written)
+    // the forward once more, recording each chunk's start state (y is not written)
     nm_args a;
     a.B = B; a.H = H; a.T = T;
     a.q = q; a.k = k; a.v = v;
@@ -367,7 +371,8 @@ int nm_backward(nm_handle_t h, int B, int H, int T, const void* q, const void* k
     a.surprise = nullptr;
     a.y_attn = nullptr;
     a.ckpt = ckpt;
-    if (nm_simt_launch(fc, a, s, &h->launches) != cudaSuccess) {
+    if ((tc_ckpt ? nm_tc_launch(cfg, a, s, h->num_sms, &h->launches) : nm_simt_launch(fc, a, s, &h->launches)) !=
+        cudaSuccess) {
         cudaGetLastError();
         return NM_ERR_CUDA;
     }

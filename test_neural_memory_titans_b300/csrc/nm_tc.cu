@@ -26,6 +26,10 @@ bool nm_tc_supports_surprise(const nm_config& c) {
            nm_tc_mlp_wide_supports(c);
 }
 
+// Kernels that can record every chunk's start state (nm_args.ckpt) for the
+// backward pass, without writing y.
+bool nm_tc_supports_ckpt(const nm_config& c) { return nm_layers(c) <= 2 && nm_tc_linear_supports(c); }
+
 // Only the deep-memory kernel keeps a per-unit workspace (the chunk's activations).
 size_t nm_tc_scratch_bytes(const nm_config& c, int B, int H) {
     return nm_layers(c) > 2 && nm_tc_deep_supports(c) ? nm_tc_deep_scratch_bytes(c, B, H) : 0;

@@ -122,8 +122,9 @@ template <>
 __device__ __forceinline__ void store_y<float>(float* p, float x) { *p = x; }
 
 // OPT: bit 0 = write the surprise (a.surprise), bit 1 = Huber loss (clip e), bit 2 = the
-// gated output o = sigmoid(y) (.) y_attn (a.y_attn); compiled
-// variants, so that the plain forward carries neither.
+// gated output o = sigmoid(y) (.) y_attn (a.y_attn), bit 3 = the checkpointing forward of
+// the backward pass (every chunk's start state into a.ckpt, y not written); compiled
+// variants, so that the plain forward carries none of them.
 template <typename Tout, int OPT>
 __global__ void __launch_bounds__(NTHREADS, 1)
     tc_linear_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
@@ -241,6 +242,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 }
                 tmem_st32(tl + (which ? COL_S : COL_M) + c0, r);
                 put_row32(sm + (which ? OFF_SH : OFF_MH), 128, orow, c0, r);
+                if (OPT & 8) {  // chunk 0's start state, for the backward pass
+                    float* ck = a.ckpt + unit * nchunks * 2 * P + (which ? P : 0) + (long long)orow * D + c0;
+#pragma unroll
+                    for (int q = 0; q < 32; q += 4)
+                        *reinterpret_cast<float4*>(ck + q) = make_float4(r[q], r[q + 1], r[q + 2], r[q + 3]);
+                }
             }
         }
     }
@@ -538,6 +545,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 if (!last) {
                     put_row32(sm + OFF_MH, 128, orow, c0, m);
                     put_row32(sm + OFF_SH, 128, orow, c0, s);
+                    if (OPT & 8) {  // chunk c + 1's start state, for the backward pass
+                        float* mk = a.ckpt + (unit * nchunks + c + 1) * 2 * P + (long long)orow * D + c0;
+#pragma unroll
+                        for (int q = 0; q < 32; q += 4) {
+                            *reinterpret_cast<float4*>(mk + q) = make_float4(m[q], m[q + 1], m[q + 2], m[q + 3]);
+                            *reinterpret_cast<float4*>(mk + P + q) = make_float4(s[q], s[q + 1], s[q + 2], s[q + 3]);
+                        }
+                    }
                 } else {
                     float* mt = a.M_T + unit * P + (long long)orow * D + c0;
                     float* st = a.S_T + unit * P + (long long)orow * D + c0;
@@ -550,7 +565,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             }
         }
         handoff();
-        if (tid == 0 && !failed) {
+        if (!(OPT & 8) && tid == 0 && !failed) {  // (no y for a checkpointing forward)
             tma_store_3d(&ty, sm + OFF_EG, 0, (int)t0, (int)unit);
             bulk_commit();
         }
@@ -573,7 +588,8 @@ cudaError_t launch(const nm_config& c, const nm_args& a, cudaStream_t s) {
     const long long units = (long long)a.B * a.H;
     if (!make_token_map(&tq, a.q, D, a.T, units) || !make_token_map(&tk, a.k, D, a.T, units) ||
         !make_token_map(&tv, a.v, D, a.T, units) ||
-        !make_token_store_map(&ty, a.y, D, a.T, units, sizeof(Tout) == 2))
+        // without y (a checkpointing forward) the map is made over q, of y's bf16 shape, and never used
+        !make_token_store_map(&ty, a.y ? a.y : const_cast<void*>(a.q), D, a.T, units, sizeof(Tout) == 2))
         return cudaErrorInvalidValue;
     auto kern = tc_linear_kernel<Tout, OPT>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
@@ -604,5 +620,9 @@ bool nm_tc_linear_supports(const nm_config& c) {
 
 cudaError_t nm_tc_linear_launch(const nm_config& c, const nm_args& a, cudaStream_t s) {
     const int opt = (a.surprise ? 1 : 0) | (a.e_clip < HUGE_VALF ? 2 : 0) | (a.y_attn ? 4 : 0);
+    if (a.ckpt) {  // the checkpointing forward: no y, no surprise, no gate; its y map is made over q (bf16)
+        if (a.y || a.surprise || a.y_attn) return cudaErrorInvalidValue;
+        return opt & 2 ? launch<__nv_bfloat16, 10>(c, a, s) : launch<__nv_bfloat16, 8>(c, a, s);
+    }
     return c.out_dtype == NM_BF16 ? launch_opt<__nv_bfloat16>(opt, c, a, s) : launch_opt<float>(opt, c, a, s);
 }
