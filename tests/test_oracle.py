@@ -437,7 +437,8 @@ def test_huber_grad_finite_differences_and_library(kind, d, hidden):
         lt = _huber_torch(_torch_memory(kind, d, hidden, Wt, torch.tensor(k)) - torch.tensor(v), delta)
         (gt,) = torch.autograd.grad(lt, Wt)
         np.testing.assert_allclose(g, gt.numpy(), rtol=1e-12, atol=1e-13)
-        assert abs(oracle.loss(kind, d, hidden, W, k, v, oracle.LOSS_HUBER, delta) - float(lt)) <= 1e-12 * abs(float(lt))
+        lv = float(lt.detach())
+        assert abs(oracle.loss(kind, d, hidden, W, k, v, oracle.LOSS_HUBER, delta) - lv) <= 1e-12 * abs(lv)
     assert checked_clip
 
 
