@@ -57,7 +57,8 @@ METRIC = "memory-layer fwd tokens/sec (B*H*T/s) and % of roofline (TC FLOPs vs H
 # The 128->512->128 figure is scaled from a capture of a 16384-token slice of the workload (token
 # traffic x 8, plus the state read and written once per call); the streamed workload's is one
 # 65536-token segment call, which is what one launch of its bench step processes; the 3-layer memory's
-# from a 512-token capture (8 of the 64 chunks: its per-chunk traffic x 64, plus the state once).
+# from a 512-token capture (8 of the 64 chunks: its per-chunk traffic x 64, plus the state once); the
+# backward sweep's from a 512-token capture (8 of the 256 chunks: x 32, its traffic being per chunk).
 NCU_TRAFFIC = {
     "mlp_64x256_bf16_b4h8_t4096_c64": (("nm_tc_mlp.cu", "tc_common.cuh", "nm_internal.h"), "810ad16e5ee50003",
                                        62.45e6),
@@ -69,6 +70,9 @@ NCU_TRAFFIC = {
                                                     "cd0494a3b25f3211", 254.6e6),
     "mlp_64x256_bf16_b4h8_t4096_c64_L3": (("nm_tc_deep.cu", "tc_common.cuh", "nm_internal.h"), "f471c769b7e276b8",
                                           8.442e9),
+    # the backward pass's reverse sweep on tensor-core contractions (bwd_linear_kernel), one launch
+    "linear_d128_bf16_b8h16_t16384_c64@backward_tc": (("nm_backward.cu", "tc_common.cuh", "nm_internal.h"),
+                                                      "eaf54753b26663c9", 71.8e9),
 }
 
 
@@ -533,10 +537,13 @@ def run_backward(args, rank, world, local_rank):
     if tc:
         peaks, peak_src = load_peaks()
         peak = float(peaks["bf16_tflops"]) * TF32_PER_BF16
+        sweep_bytes = ncu_traffic(wl.name + "@backward_tc")
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                "traffic": None, "peak_source": peak_src + " (burst bf16 x 1.1/2.25, the nominal tf32 ratio)",
+                "traffic": sweep_bytes, "peak_source": peak_src + " (burst bf16 x 1.1/2.25, the nominal tf32 ratio)",
                 "kernel": "nm_backward (checkpointing forward, tcgen05 for the linear d=128 memory, else fp32 FFMA; "
                           "reverse sweep with tcgen05 tf32 contractions)"}
+        if sweep_bytes is not None:
+            roof["traffic_kernel"] = "bwd_linear_kernel (the reverse sweep), DRAM bytes of one launch"
     else:
         roof = {"bound": "alu", "achieved": achieved, "peak": FP32_PEAK_TFLOPS, "unit": "TFLOP/s",
                 "frac": achieved / FP32_PEAK_TFLOPS, "traffic": None,

@@ -110,3 +110,12 @@ def test_deep_traffic_entry_names_the_deep_kernel_sources():
     b = _bench()
     files, digest, nbytes = b.NCU_TRAFFIC["mlp_64x256_bf16_b4h8_t4096_c64_L3"]
     assert files[0] == "nm_tc_deep.cu" and len(digest) == 16 and nbytes > 0
+
+
+def test_backward_traffic_entry_names_the_sweep_sources():
+    """The backward line's traffic is the reverse sweep's (nm_backward.cu), keyed
+    apart from the forward kernel's entry of the same workload."""
+    b = _bench()
+    files, digest, nbytes = b.NCU_TRAFFIC["linear_d128_bf16_b8h16_t16384_c64@backward_tc"]
+    assert files[0] == "nm_backward.cu" and len(digest) == 16
+    assert nbytes > b.NCU_TRAFFIC["linear_d128_bf16_b8h16_t16384_c64"][2]
