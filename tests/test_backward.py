@@ -14,7 +14,9 @@ the bound is 1e-5, ten times tighter than the fp32 forward's 1e-4.
 
 On a tensor-core handle (NM_PATH_TC) the reverse sweep's contractions run as
 tf32 tensor-core products (operands rounded to 11 significant bits, fp32
-accumulation): those cases are held to the bf16-input tolerances of the
+accumulation), and for the linear memory with d = 128, chunk 64 the
+chunk-start states come from the tensor-core forward (bf16 copies of the
+state as operands): those cases are held to the bf16-input tolerances of the
 forward (relative L2 1e-2 on the state's gradients dM0, dS0, 2e-2 on the
 others).
 """
