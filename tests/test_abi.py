@@ -39,6 +39,16 @@ def test_library_loads_and_exports_header_symbols():
     assert set(nm.EXPORTED) <= exported
 
 
+@pytest.mark.parametrize("lang,std", [("c", "-std=c99"), ("c++", "-std=c++11")])
+def test_headers_compile_as_plain_c_and_cpp(lang, std):
+    """The boundary is a C ABI: its headers take no CUDA, torch or C++-only
+    type and compile on their own, warning-free, from C and from C++."""
+    for h in HEADERS:
+        r = subprocess.run(["gcc", "-fsyntax-only", std, "-Wall", "-Wextra", "-Werror", "-x", lang, h],
+                           capture_output=True, text=True)
+        assert r.returncode == 0, (h, r.stderr)
+
+
 def test_status_strings_without_gpu():
     for code in range(0, 9):
         s = nm.status_string(code)
