@@ -1,9 +1,11 @@
 """Planted mistakes: each one is a plausible error in the oracle (a dropped
 factor, a wrong sign, the wrong weights, a transposed operand, an ignored
-coefficient, a wrong derivative, a wrong layer offset).  The test compiles a
-copy of nm_oracle.c with the mistake, points the oracle at it, and checks that
-the pins of tests/test_oracle.py catch it.  Mistakes are planted only in this
-temporary copy of the oracle, on the CPU."""
+coefficient, a wrong derivative, a wrong layer offset, a wrong surprise norm,
+a wrong gate).  For the C oracle the test compiles a copy of nm_oracle.c with
+the mistake and points the oracle at it; for the Memory-as-Gate combination
+(numpy) it builds a copy of the function with the mistake.  Either way it
+checks that the pins of tests/test_oracle.py catch it.  Mistakes are planted
+only in those temporary copies, on the CPU."""
 import os
 import subprocess
 import tempfile
@@ -30,6 +32,8 @@ MUTATIONS = {
     "Huber gradient not clipped": ("if (r > delta) return 2.0 * delta;", "if (r > delta) return 2.0 * r;"),
     "wrong offset of the hidden layers": ("off[l] = off[l - 1] + (long)h * h;", "off[l] = off[l - 1] + (long)h * d;"),
     "momentum decay dropped": ("S[p] = beta[t] * S[p] + ct * g[p];", "S[p] = S[p] + ct * g[p];"),
+    "surprise as the squared norm": ("surprise[t] = sqrt(n2);", "surprise[t] = n2;"),
+    "surprise from absolute values": ("n2 += g[p] * g[p];", "n2 += fabs(g[p]);"),
 }
 
 PIN_CALLS = [
@@ -46,6 +50,8 @@ PIN_CALLS = [
     (pins.test_huber_grad_finite_differences_and_library, (oracle.LINEAR, 3, 0)),
     (pins.test_deep_grad_finite_differences_and_library, (2, 3, 3)),
     (pins.test_deep_chunk1_equals_sequential_and_chunk_sums_gradients, (3,)),
+    (pins.test_surprise_is_the_gradient_norm_at_chunk_start, (oracle.LINEAR, 4, 0, oracle.LOSS_L2)),
+    (pins.test_surprise_is_the_gradient_norm_at_chunk_start, (oracle.MLP2, 3, 6, oracle.LOSS_HUBER)),
 ]
 
 
@@ -81,3 +87,46 @@ def test_planted_mistake_is_caught(name, tmp_path):
                            "-lm"])
     failed = _caught(str(so))
     assert failed, "no pin caught: %s" % name
+
+
+# The Memory-as-Gate combination is plain numpy in oracle/__init__.py: its mistakes are planted in an
+# in-memory copy of that function, which the pins then call in place of the original.
+GATE_MUTATIONS = {
+    "sigmoid of -y": ("y_attn / (1.0 + np.exp(-y_mem))", "y_attn / (1.0 + np.exp(y_mem))"),
+    "operands swapped": ("y_attn / (1.0 + np.exp(-y_mem))", "y_mem / (1.0 + np.exp(-y_attn))"),
+    "tanh for the sigmoid": ("y_attn / (1.0 + np.exp(-y_mem))", "y_attn * np.tanh(y_mem)"),
+}
+GATE_PINS = [pins.test_mag_gate_hand_worked, pins.test_mag_gate_symmetry_limits_and_library]
+
+
+def _gate_caught(fn, monkeypatch):
+    failed = []
+    with monkeypatch.context() as m:
+        m.setattr(oracle, "mag_gate", fn)
+        for pin in GATE_PINS:
+            try:
+                pin()
+            except AssertionError:
+                failed.append(pin.__name__)
+    return failed
+
+
+def _gate_from(source):
+    import inspect
+    ns = dict(oracle.__dict__)
+    exec(compile(source, inspect.getsourcefile(oracle) + " [mag_gate]", "exec"), ns)
+    return ns["mag_gate"]
+
+
+def test_unmodified_gate_passes_its_pins(monkeypatch):
+    import inspect
+    assert _gate_caught(_gate_from(inspect.getsource(oracle.mag_gate)), monkeypatch) == []
+
+
+@pytest.mark.parametrize("name", sorted(GATE_MUTATIONS))
+def test_planted_gate_mistake_is_caught(name, monkeypatch):
+    import inspect
+    old, new = GATE_MUTATIONS[name]
+    src = inspect.getsource(oracle.mag_gate)
+    assert src.count(old) == 1, "the mutation site moved: %s" % name
+    assert _gate_caught(_gate_from(src.replace(old, new)), monkeypatch), "no pin caught: %s" % name
