@@ -32,6 +32,10 @@ MUTATIONS = {
     "Huber gradient not clipped": ("if (r > delta) return 2.0 * delta;", "if (r > delta) return 2.0 * r;"),
     "wrong offset of the hidden layers": ("off[l] = off[l - 1] + (long)h * h;", "off[l] = off[l - 1] + (long)h * d;"),
     "momentum decay dropped": ("S[p] = beta[t] * S[p] + ct * g[p];", "S[p] = S[p] + ct * g[p];"),
+    "coefficient 1 - beta taken as beta": ("if (c_mode == OR_C_ONE_MINUS_BETA) ct = 1.0 - beta[t];",
+                                           "if (c_mode == OR_C_ONE_MINUS_BETA) ct = beta[t];"),
+    "forgetting factor taken as alpha": ("M[p] = (1.0 - alpha[t]) * M[p] - eta[t] * S[p];",
+                                         "M[p] = alpha[t] * M[p] - eta[t] * S[p];"),
     "surprise as the squared norm": ("surprise[t] = sqrt(n2);", "surprise[t] = n2;"),
     "surprise from absolute values": ("n2 += g[p] * g[p];", "n2 += fabs(g[p]);"),
 }
