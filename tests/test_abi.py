@@ -98,6 +98,47 @@ def test_null_handle_and_bad_config_without_gpu():
             nm.NM_ERR_ARG, nm.NM_ERR_UNSUPPORTED)
 
 
+def _shape_taken(lib, kind, d, hidden, chunk, dtype, path, layers=0):
+    """Whether nm_create's path selection takes the shape: it decides before any
+    CUDA call, so without a GPU a taken shape fails later, at the device query
+    (NM_ERR_CUDA, or NM_ERR_ARG when no device is listed), and a shape no
+    kernel of the path takes returns NM_ERR_UNSUPPORTED."""
+    h = ctypes.c_void_p()
+    cfg = nm._Config(kind, d, hidden, chunk, dtype, nm.BF16, nm.C_ONE, path, nm.LOSS_L2, 0.0, layers)
+    rc = lib.nm_create(ctypes.byref(cfg), 0, ctypes.byref(h))
+    if rc == nm.NM_OK:  # (a run with a GPU)
+        lib.nm_destroy(h)
+    assert rc in (nm.NM_OK, nm.NM_ERR_CUDA, nm.NM_ERR_ARG, nm.NM_ERR_UNSUPPORTED), rc
+    return rc != nm.NM_ERR_UNSUPPORTED
+
+
+def test_shapes_each_path_takes_without_gpu():
+    """The shape table of nm_config's documentation, path by path."""
+    lib = nm.load_library()
+    L, M, B16, F32, TC, SIMT = nm.LINEAR, nm.MLP2, nm.BF16, nm.F32, nm.PATH_TC, nm.PATH_SIMT
+    tc_taken = [(L, 128, 0, 64), (L, 64, 0, 64), (L, 64, 0, 128), (L, 64, 0, 256),  # linear d = 128; d = 64
+                (M, 64, 128, 64), (M, 64, 256, 64),                                  # MLP d = 64
+                (M, 128, 128, 64), (M, 128, 256, 64), (M, 128, 512, 64)]             # MLP d = 128
+    tc_not = [(L, 128, 0, 32), (L, 64, 0, 32), (L, 32, 0, 64), (L, 16, 0, 64),
+              (M, 64, 512, 64), (M, 64, 256, 32), (M, 128, 1024, 64), (M, 32, 128, 64)]
+    for kind, d, hid, ch in tc_taken:
+        assert _shape_taken(lib, kind, d, hid, ch, B16, TC), (kind, d, hid, ch)
+        assert not _shape_taken(lib, kind, d, hid, ch, F32, TC), (kind, d, hid, ch)  # bf16 inputs only
+    for kind, d, hid, ch in tc_not:
+        assert not _shape_taken(lib, kind, d, hid, ch, B16, TC), (kind, d, hid, ch)
+    # deeper memories on the tensor cores: d 64 or 128, hidden a multiple of 64 up to 512, chunk <= 64
+    for d, hid, ch, ok in ((64, 256, 64, True), (128, 512, 64, True), (64, 64, 1, True), (64, 256, 32, True),
+                           (64, 96, 64, False), (64, 576, 64, False), (64, 256, 128, False), (32, 256, 64, False)):
+        assert _shape_taken(lib, M, d, hid, ch, B16, TC, layers=3) == ok, (d, hid, ch)
+    # the fp32 FFMA path: d in {16, 32, 64, 128}, chunk 1..256, hidden a multiple of 32 up to 1024
+    for kind, d, hid, ch, ok in ((L, 16, 0, 1, True), (L, 128, 0, 256, True), (L, 48, 0, 64, False),
+                                 (L, 64, 0, 257, False), (M, 32, 1024, 16, True), (M, 64, 1056, 64, False),
+                                 (M, 64, 48, 64, False)):
+        for dt in (F32, B16):
+            assert _shape_taken(lib, kind, d, hid, ch, dt, SIMT) == ok, (kind, d, hid, ch, dt)
+    assert _shape_taken(lib, M, 64, 96, 8, F32, SIMT, layers=5)
+
+
 # ------------------------------------------------------------------ on a GPU
 
 def _args(wl, dev="cuda"):
