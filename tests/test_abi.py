@@ -139,6 +139,44 @@ def test_shapes_each_path_takes_without_gpu():
     assert _shape_taken(lib, M, 64, 96, 8, F32, SIMT, layers=5)
 
 
+@pytest.mark.skipif(torch.cuda.is_available(), reason="fake addresses are for a machine without a GPU")
+def test_noalloc_host_checks_without_gpu():
+    """nm_forward_mlp2_noalloc checks alignment, overlaps, the c argument and
+    the workspace bound on the host, before any CUDA call.  Every call below
+    breaks one of those rules, so the addresses (fake, never dereferenced) are
+    only compared; the test does not run where a GPU is visible."""
+    fn = nm.load_library().nm_forward_mlp2_noalloc
+    vp = ctypes.c_void_p
+    fn.argtypes = [ctypes.POINTER(nm._Config), ctypes.c_int, ctypes.c_int, ctypes.c_int] + [vp] * 13
+    fn.restype = ctypes.c_int
+    d, hidden, chunk, B, H, T = 64, 128, 64, 1, 2, 100
+    cfg = nm._Config(nm.MLP2, d, hidden, chunk, nm.BF16, nm.BF16, nm.C_ONE, nm.PATH_AUTO)
+    P = nm.param_count(nm.MLP2, d, hidden)
+    MB = 1 << 20
+    # disjoint, 16-byte-aligned ranges: inputs (bf16 [B,H,T,d]), gates, states, y, M_T, S_T
+    base = dict(q=1 * MB, k=2 * MB, v=3 * MB, alpha=4 * MB, eta=5 * MB, beta=6 * MB, c=None, M0=8 * MB,
+                S0=9 * MB, y=10 * MB, M_T=11 * MB, S_T=12 * MB)
+    order = ("q", "k", "v", "alpha", "eta", "beta", "c", "M0", "S0", "y", "M_T", "S_T")
+
+    def call(cf=cfg, units=(B, H, T), **over):
+        p = dict(base)
+        p.update(over)
+        return fn(ctypes.byref(cf), *units, *(None if p[n] is None else vp(p[n]) for n in order), None)
+
+    assert call(q=1 * MB + 2) == nm.NM_ERR_ALIGN
+    assert call(S_T=12 * MB + 8) == nm.NM_ERR_ALIGN
+    assert call(y=1 * MB + 64) == nm.NM_ERR_ALIAS                 # y inside q
+    assert call(M_T=8 * MB + 16) == nm.NM_ERR_ALIAS               # M_T partly over M0
+    assert call(S_T=11 * MB + 4 * P - 16) == nm.NM_ERR_ALIAS      # S_T's start inside M_T
+    assert call(c=7 * MB) == nm.NM_ERR_ARG                        # c given without NM_C_PER_TOKEN
+    per_token = nm._Config(nm.MLP2, d, hidden, chunk, nm.BF16, nm.BF16, nm.C_PER_TOKEN, nm.PATH_AUTO)
+    assert call(cf=per_token) == nm.NM_ERR_ARG                    # c missing with it
+    assert call(y=None) == nm.NM_ERR_ARG
+    assert call(units=(1, 1 << 16, T)) == 9                       # NM_ERR_TOO_LARGE: beyond the fixed workspace
+    tc = nm._Config(nm.MLP2, d, hidden, chunk, nm.BF16, nm.BF16, nm.C_ONE, nm.PATH_TC)
+    assert call(cf=tc) == nm.NM_ERR_UNSUPPORTED                   # the fp32 FFMA kernel only
+
+
 # ------------------------------------------------------------------ on a GPU
 
 def _args(wl, dev="cuda"):
